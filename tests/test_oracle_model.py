@@ -1,0 +1,177 @@
+"""Model-level pins of the oracle on tiny shapes: grouped-query repeat (not
+tile), the causal mask, the KV-cache invariant under five chunkings, the
+planted position bug, and fp32 against fp64 agreement."""
+import numpy as np
+import pytest
+import torch
+
+from transformer_decode_gb300 import synth
+
+
+def _rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+@pytest.fixture(scope="module")
+def tiny(orc):
+    w = synth.model_weights(synth.TINY, seed=0)
+    return orc.OracleModel(synth.TINY, w), w
+
+
+@pytest.fixture(scope="module")
+def tiny_qk(orc):
+    w = synth.model_weights(synth.TINY_QKNORM, seed=0)
+    return orc.OracleModel(synth.TINY_QKNORM, w), w
+
+
+def _bf16(t):
+    return torch.tensor(t, dtype=torch.float32).to(torch.bfloat16)
+
+
+def test_gqa_repeats_kv_heads(orc):
+    """nanoinfer "Model architecture": query head h reads kv head h // G, so
+    kv head 0 serves query heads 0..G-1 (repeat, not tile).
+
+    Construction: W_v = 0 and the v bias of kv head g is the constant c_g, and
+    every cached V of head g is c_g too, so attention returns c_g for every
+    query head that reads kv head g whatever the scores. W_o = I and W_d = 0
+    make the block output x + a."""
+    s = synth.TINY
+    D, G = s.head_dim, s.group
+    w = synth.model_weights(s, seed=0)
+    lw = w["layers"][0]
+    consts = [0.5, -1.25]
+    lw["wv"] = torch.zeros_like(lw["wv"])
+    lw["bv"] = _bf16(np.repeat(consts, D))
+    lw["wo"] = _bf16(np.eye(s.hidden, s.q_dim))
+    lw["wd"] = torch.zeros_like(lw["wd"])
+    m = orc.OracleModel(s, w)
+    kv = m.new_kv(1, 8)
+    pos = 5
+    for g, c in enumerate(consts):
+        kv.v[0, 0, g, :pos] = _bf16(np.full((pos, D), c)).view(torch.int16).numpy().view(np.uint16)
+    kv.k[0, 0, :, :pos] = synth.normal_bf16(0, 99, (s.n_kv_heads, pos, D), 0.5).view(
+        torch.int16).numpy().view(np.uint16)
+    x = np.random.default_rng(0).standard_normal(s.hidden)
+    out = m.block_decode(0, kv, 0, pos, x, "f64")
+    a = (out - x).reshape(s.n_q_heads, D)
+    for h in range(s.n_q_heads):
+        assert np.allclose(a[h], consts[h // G], rtol=1e-12), h
+    # the tiled pairing (h % Hkv) would differ
+    assert any(consts[h // G] != consts[h % s.n_kv_heads] for h in range(s.n_q_heads))
+
+
+def test_causal_mask(tiny):
+    """Row i of the uncached forward does not depend on tokens after i, and a
+    token attends to itself (row 0 depends on token 0)."""
+    m, _ = tiny
+    toks = synth.token_ids(9, synth.TINY.vocab, stream=3)
+    a = m.forward_full(toks, "f64")
+    t2 = toks.clone()
+    t2[6:] = (t2[6:] + 17) % synth.TINY.vocab
+    b = m.forward_full(t2, "f64")
+    assert np.array_equal(a[:6], b[:6])
+    assert not np.allclose(a[6:], b[6:])
+    t3 = toks.clone()
+    t3[0] = (t3[0] + 1) % synth.TINY.vocab
+    assert not np.allclose(m.forward_full(t3, "f64")[0], a[0])
+
+
+@pytest.mark.parametrize("which", ["tiny", "tiny_qk"])
+@pytest.mark.parametrize("prec", ["f32", "f64"])
+def test_cache_invariant_five_chunkings(which, prec, request):
+    """nanoinfer "KV cache": the same 8 tokens under five chunkings (one shot,
+    one at a time, prompt then decode, halves, ragged) give what one uncached
+    pass gives."""
+    m, _ = request.getfixturevalue(which)
+    toks = synth.token_ids(8, m.shape.vocab, stream=4)
+    ref = m.forward_full(toks, prec)
+    for chunks in ([8], [1] * 8, [5, 1, 1, 1], [4, 4], [3, 2, 3]):
+        kv = m.new_kv(1, 8)
+        rows, start = [], 0
+        for n in chunks:
+            rows.append(m.forward_chunk(kv, 0, toks[start:start + n], start, prec))
+            start += n
+        got = np.concatenate(rows)
+        assert _rel_l2(got, ref) < (1e-6 if prec == "f32" else 1e-14), chunks
+    # token-major decode steps (the decode path proper)
+    kv = m.new_kv(1, 8)
+    for i in range(8):
+        logits, nxt = m.decode_step(kv, toks[i:i + 1], np.array([i], np.int32), prec)
+    assert _rel_l2(logits[0], ref[-1]) < (1e-6 if prec == "f32" else 1e-14)
+    assert nxt[0] == int(np.argmax(ref[-1]))
+
+
+def test_decode_batch_rows_are_independent(tiny):
+    """Two sequences in one batch give what each gives alone."""
+    m, _ = tiny
+    toks = synth.token_ids(6, m.shape.vocab, stream=5).numpy()
+    kv = m.new_kv(2, 8)
+    kva, kvb = m.new_kv(1, 8), m.new_kv(1, 8)
+    for i in range(3):
+        both, _ = m.decode_step(kv, toks[[i, 3 + i]], np.array([i, i], np.int32))
+        la, _ = m.decode_step(kva, toks[[i]], np.array([i], np.int32))
+        lb, _ = m.decode_step(kvb, toks[[3 + i]], np.array([i], np.int32))
+        assert np.array_equal(both[0], la[0]) and np.array_equal(both[1], lb[0])
+
+
+def test_planted_position_bug_changes_output(tiny):
+    """nanoinfer "KV cache": a decode step at position 0 instead of the cache
+    length gives finite but different numbers (the bug that must be caught by
+    comparison, since it raises nothing)."""
+    m, _ = tiny
+    toks = synth.token_ids(6, m.shape.vocab, stream=6)
+    kv = m.new_kv(1, 8)
+    m.forward_chunk(kv, 0, toks[:5], 0)
+    kv_bug = kv.copy()
+    good, _ = m.decode_step(kv, toks[5:6], np.array([5], np.int32))
+    bad, _ = m.decode_step(kv_bug, toks[5:6], np.array([0], np.int32))
+    assert np.all(np.isfinite(bad)) and _rel_l2(bad, good) > 1e-3
+
+
+def test_invalid_position_rejected(tiny):
+    m, _ = tiny
+    kv = m.new_kv(1, 4)
+    with pytest.raises(ValueError):
+        m.decode_step(kv, np.array([1], np.int32), np.array([4], np.int32))
+
+
+@pytest.mark.parametrize("which", ["tiny", "tiny_qk"])
+def test_f32_oracle_close_to_f64(which, request):
+    """The oracle's own rounding is far below the 5e-4 parity gate."""
+    m, _ = request.getfixturevalue(which)
+    toks = synth.token_ids(12, m.shape.vocab, stream=7)
+    a = m.forward_full(toks, "f32")
+    b = m.forward_full(toks, "f64")
+    assert _rel_l2(a, b) < 1e-5
+
+
+def test_hidden_states_drift_per_layer(tiny):
+    """The per-layer residual stream is reported and the last entry feeds the
+    head: logits equal the head applied to hidden[-1]."""
+    m, w = tiny
+    kv = m.new_kv(1, 4)
+    logits, nxt, hid = m.decode_step(kv, np.array([3], np.int32), np.array([0], np.int32),
+                                     "f64", hidden=True)
+    import oracle
+    n = oracle.rmsnorm(hid[0, -1], w["g_final"], m.shape.rms_eps, "f64")
+    assert np.allclose(oracle.matvec_bf16(w["embed"], n, "f64"), logits[0], rtol=1e-14)
+    e = oracle.bf16_to_f32(w["embed"][3].view(torch.int16).numpy())
+    assert np.array_equal(hid[0, 0], e.astype(np.float64))
+
+
+def test_w8a8_model_close_to_bf16(orc, tiny):
+    """The W8A8 model is the bf16 model up to quantisation error."""
+    _, w = tiny
+    m8 = orc.OracleModel(synth.TINY, w, w8a8=True)
+    m16 = orc.OracleModel(synth.TINY, w)
+    toks = synth.token_ids(6, synth.TINY.vocab, stream=8)
+    a = m8.forward_full(toks, "f64")
+    b = m16.forward_full(toks, "f64")
+    assert 0 < _rel_l2(a, b) < 0.1
+    kv = m8.new_kv(1, 8)
+    for i in range(6):
+        lg, _ = m8.decode_step(kv, toks[i:i + 1], np.array([i], np.int32), "f64")
+    assert _rel_l2(lg[0], a[-1]) < 1e-14
