@@ -62,8 +62,8 @@ class Model(C.Structure):
 
 
 class KV(C.Structure):
-    _fields_ = [("batch", C.c_int), ("max_ctx", C.c_int),
-                ("k", C.POINTER(C.c_uint16)), ("v", C.POINTER(C.c_uint16))]
+    _fields_ = [("batch", C.c_int), ("max_ctx", C.c_int), ("bf16", C.c_int),
+                ("k", C.c_void_p), ("v", C.c_void_p)]
 
 
 def _p(a, ct):
@@ -103,7 +103,7 @@ def _declare(L):
         g("silu").argtypes = [rt]
         g("silu").restype = rt
         g("softmax").argtypes = [rp, C.c_int, rp]
-        g("attention_head").argtypes = [rp, u16p, u16p, C.c_int, C.c_int, rp]
+        g("attention_head").argtypes = [rp, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, rp]
         g("linear_w8a8").argtypes = [i8p, f32p, u16p, C.c_int, C.c_int, rp, rp]
         g("block_decode").argtypes = [C.POINTER(Model), C.c_int, C.POINTER(KV), C.c_int,
                                       C.c_int, rp]
@@ -113,7 +113,7 @@ def _declare(L):
         g("forward_chunk").argtypes = [C.POINTER(Model), C.POINTER(KV), C.c_int, C.c_int,
                                        i32p, C.c_int, rp]
         g("forward_chunk").restype = C.c_int
-        g("forward_full").argtypes = [C.POINTER(Model), C.c_int, i32p, rp]
+        g("forward_full").argtypes = [C.POINTER(Model), C.c_int, i32p, C.c_int, rp]
         g("forward_full").restype = C.c_int
 
 
@@ -202,15 +202,27 @@ def softmax(s, prec="f32"):
 
 
 def attention_head(q, k, v, prec="f32"):
-    """q [D]; k, v bf16 bits [n_pos, D]."""
+    """q [D]; k, v [n_pos, D] as bf16 bits (uint16 arrays, bf16 tensors) or
+    fp32 values (float32 arrays or tensors)."""
     dt, ct = _real(prec)
     q = _np(q, dt)
-    k = _np(k, np.uint16)
-    v = _np(v, np.uint16)
+    bf16 = _is_bf16(k)
+    k = _np(k, np.uint16 if bf16 else np.float32)
+    v = _np(v, np.uint16 if bf16 else np.float32)
     out = np.empty(q.size, dt)
-    getattr(lib(), f"orc_attention_head_{prec}")(_p(q, ct), _p(k, C.c_uint16), _p(v, C.c_uint16),
+    getattr(lib(), f"orc_attention_head_{prec}")(_p(q, ct), k.ctypes.data, v.ctypes.data, int(bf16),
                                                 k.shape[0], q.size, _p(out, ct))
     return out
+
+
+def _is_bf16(a):
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            return a.dtype == torch.bfloat16
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(a).dtype == np.uint16
 
 
 def quantize_row(v):
@@ -316,8 +328,8 @@ class OracleModel:
         self.struct = Model(cfg, _p(emb, C.c_uint16), _p(head, C.c_uint16),
                             _p(gf, C.c_uint16), layers, int(w8a8))
 
-    def new_kv(self, batch, max_ctx):
-        return OracleKV(self.shape, batch, max_ctx)
+    def new_kv(self, batch, max_ctx, bf16=False):
+        return OracleKV(self.shape, batch, max_ctx, bf16)
 
     def decode_step(self, kv, tokens, positions, prec="f32", hidden=False):
         dt, ct = _real(prec)
@@ -352,28 +364,33 @@ class OracleModel:
             raise ValueError("chunk does not fit the cache")
         return logits
 
-    def forward_full(self, tokens, prec="f32"):
+    def forward_full(self, tokens, prec="f32", kv_bf16=False):
         dt, ct = _real(prec)
         tokens = _np(tokens, np.int32)
         logits = np.empty((tokens.size, self.shape.vocab), dt)
         getattr(lib(), f"orc_forward_full_{prec}")(C.byref(self.struct), tokens.size,
-                                                  _p(tokens, C.c_int32), _p(logits, ct))
+                                                  _p(tokens, C.c_int32), int(kv_bf16),
+                                                  _p(logits, ct))
         return logits
 
 
 class OracleKV:
-    """Logical KV cache, bf16 bits [L][B][Hkv][max_ctx][D]."""
+    """Logical KV cache [L][B][Hkv][max_ctx][D]: fp32 values, or bf16 bits
+    (uint16) when bf16=True."""
 
-    def __init__(self, shape, batch, max_ctx):
+    def __init__(self, shape, batch, max_ctx, bf16=False):
         dims = (shape.n_layers, batch, shape.n_kv_heads, max_ctx, shape.head_dim)
-        self.k = np.zeros(dims, np.uint16)
-        self.v = np.zeros(dims, np.uint16)
-        self.struct = KV(batch, max_ctx, _p(self.k, C.c_uint16), _p(self.v, C.c_uint16))
+        dt = np.uint16 if bf16 else np.float32
+        self.bf16 = bool(bf16)
+        self.k = np.zeros(dims, dt)
+        self.v = np.zeros(dims, dt)
+        self.struct = KV(batch, max_ctx, int(bf16), self.k.ctypes.data, self.v.ctypes.data)
 
     def copy(self):
         o = OracleKV.__new__(OracleKV)
+        o.bf16 = self.bf16
         o.k = self.k.copy()
         o.v = self.v.copy()
-        o.struct = KV(self.struct.batch, self.struct.max_ctx, _p(o.k, C.c_uint16),
-                      _p(o.v, C.c_uint16))
+        o.struct = KV(self.struct.batch, self.struct.max_ctx, int(o.bf16), o.k.ctypes.data,
+                      o.v.ctypes.data)
         return o

@@ -27,9 +27,11 @@
  * Readings where the pages are silent (each listed in the design notes):
  *   attention scale 1/sqrt(D); RMSNorm (x * r) * g with r = 1/sqrt(ss/n + eps);
  *   inv_freq[i] = float(1 / theta^(2i/D)) computed in double; angle is the
- *   fp32 product float(pos) * inv_freq[i]; K and V are rounded to bf16 when
- *   stored; per-head q/k RMSNorm (8B shape) is applied before RoPE with gains
- *   [D] shared by all heads; argmax takes the lowest index on ties.
+ *   fp32 product float(pos) * inv_freq[i]; the cache stores K and V in fp32
+ *   (nanoinfer's cache), or in bf16 when asked (rounded to nearest even on
+ *   store, in the cached and the uncached forward alike); per-head q/k
+ *   RMSNorm (8B shape) is applied before RoPE with gains [D] shared by all
+ *   heads; argmax takes the lowest index on ties.
  *
  * Precision: every function exists as _f32 (the oracle) and _f64 (the same
  * definition in double, used to show the oracle's own rounding is far below
@@ -78,12 +80,15 @@ typedef struct {
   int w8a8;                 /* projections use the int8 fields */
 } orc_model;
 
-/* Logical KV cache: k, v are bf16 [L][B][Hkv][max_ctx][D]. */
+/* Logical KV cache: k, v are [L][B][Hkv][max_ctx][D] of fp32 (bf16 = 0, the
+ * nanoinfer cache: "24 KiB per token at fp32") or of bf16 bit patterns
+ * (bf16 = 1, rounded to nearest even when stored). */
 typedef struct {
   int batch;
   int max_ctx;
-  uint16_t *k;
-  uint16_t *v;
+  int bf16;
+  void *k;
+  void *v;
 } orc_kv;
 
 /* ---- bf16 ---- */
@@ -116,7 +121,7 @@ void orc_rope_inv_freq(double theta, int d, float* inv_freq);
   void orc_rope_interleaved_##SFX(REAL* v, int d, int pos, double theta);               \
   REAL orc_silu_##SFX(REAL x);                                                          \
   void orc_softmax_##SFX(const REAL* s, int n, REAL* p);                                \
-  void orc_attention_head_##SFX(const REAL* q, const uint16_t* k, const uint16_t* v,    \
+  void orc_attention_head_##SFX(const REAL* q, const void* k, const void* v, int kv_bf16, \
                                 int n_pos, int d, REAL* out);                            \
   void orc_linear_w8a8_##SFX(const int8_t* w, const float* sw, const uint16_t* bias,     \
                              int n, int k, const REAL* x, REAL* y);                       \
@@ -128,7 +133,7 @@ void orc_rope_inv_freq(double theta, int d, float* inv_freq);
   int orc_forward_chunk_##SFX(const orc_model* m, orc_kv* kv, int b, int n,               \
                               const int32_t* tokens, int start_pos, REAL* logits);        \
   int orc_forward_full_##SFX(const orc_model* m, int t, const int32_t* tokens,           \
-                             REAL* logits);
+                             int kv_bf16, REAL* logits);
 
 ORC_DECLARE(float, f32)
 ORC_DECLARE(double, f64)

@@ -19,6 +19,17 @@ static REAL F(sqrtr)(REAL x) {
 
 static uint16_t F(narrow)(REAL v) { return orc_f32_to_bf16((float)v); }
 
+/* Element i of a K/V array stored as bf16 (kv_bf16 = 1) or fp32. */
+static REAL F(kv_get)(const void* p, int kv_bf16, long i) {
+  return kv_bf16 ? F(widen)(((const uint16_t*)p)[i]) : (REAL)((const float*)p)[i];
+}
+static void F(kv_put)(void* p, int kv_bf16, long i, REAL v) {
+  if (kv_bf16)
+    ((uint16_t*)p)[i] = F(narrow)(v);
+  else
+    ((float*)p)[i] = (float)v;
+}
+
 /* nanocompile "Phase 1": the mean square is a sum then a divide; the norm is
  * a sqrt then a reciprocal; the gain multiplies the normalised value. */
 void F(orc_rmsnorm)(const REAL* x, int n, const uint16_t* g, double eps, REAL* out) {
@@ -102,22 +113,22 @@ void F(orc_softmax)(const REAL* s, int n, REAL* p) {
   for (int i = 0; i < n; ++i) p[i] = p[i] / l;
 }
 
-/* One query head against n_pos cached keys/values (bf16 [n_pos, d]):
+/* One query head against n_pos cached keys/values ([n_pos, d], bf16 or fp32):
  * s_t = (q . k_t) / sqrt(d), p = softmax(s), out = sum_t p_t v_t. */
-void F(orc_attention_head)(const REAL* q, const uint16_t* k, const uint16_t* v,
+void F(orc_attention_head)(const REAL* q, const void* k, const void* v, int kv_bf16,
                            int n_pos, int d, REAL* out) {
   REAL* s = (REAL*)malloc(sizeof(REAL) * (size_t)n_pos);
   REAL* p = (REAL*)malloc(sizeof(REAL) * (size_t)n_pos);
   REAL scale = (REAL)1 / F(sqrtr)((REAL)d);
   for (int t = 0; t < n_pos; ++t) {
     REAL dot = 0;
-    for (int i = 0; i < d; ++i) dot += q[i] * F(widen)(k[(long)t * d + i]);
+    for (int i = 0; i < d; ++i) dot += q[i] * F(kv_get)(k, kv_bf16, (long)t * d + i);
     s[t] = dot * scale;
   }
   F(orc_softmax)(s, n_pos, p);
   for (int i = 0; i < d; ++i) {
     REAL acc = 0;
-    for (int t = 0; t < n_pos; ++t) acc += p[t] * F(widen)(v[(long)t * d + i]);
+    for (int t = 0; t < n_pos; ++t) acc += p[t] * F(kv_get)(v, kv_bf16, (long)t * d + i);
     out[i] = acc;
   }
   free(s);
@@ -205,9 +216,14 @@ static void F(post_attention)(const orc_model* m, int layer, const REAL* a, REAL
   free(up);
 }
 
+/* Address of element `off` of a cache array (fp32 or bf16 elements). */
+static const void* F(kv_at)(const orc_kv* kv, const void* p, long off) {
+  return (const char*)p + off * (kv->bf16 ? 2 : 4);
+}
+
 /* One block for one token of sequence b at position pos (pos = number of
- * tokens already cached). K and V are rounded to bf16 and stored in slot pos;
- * query head h attends with kv head h / (Hq/Hkv) over slots 0..pos. */
+ * tokens already cached). K and V are stored in slot pos (fp32, or rounded
+ * to bf16); query head h attends with kv head h / (Hq/Hkv) over slots 0..pos. */
 void F(orc_block_decode)(const orc_model* m, int layer, orc_kv* kv, int b, int pos, REAL* x) {
   const orc_config* c = &m->cfg;
   int D = c->head_dim, G = c->n_q_heads / c->n_kv_heads;
@@ -220,14 +236,15 @@ void F(orc_block_decode)(const orc_model* m, int layer, orc_kv* kv, int b, int p
   for (int g = 0; g < c->n_kv_heads; ++g) {
     long base = F(kv_off)(c, kv, layer, b, g) + (long)pos * D;
     for (int i = 0; i < D; ++i) {
-      kv->k[base + i] = F(narrow)(k[g * D + i]);
-      kv->v[base + i] = F(narrow)(v[g * D + i]);
+      F(kv_put)(kv->k, kv->bf16, base + i, k[g * D + i]);
+      F(kv_put)(kv->v, kv->bf16, base + i, v[g * D + i]);
     }
   }
 #pragma omp parallel for schedule(static)
   for (int h = 0; h < c->n_q_heads; ++h) {
     long base = F(kv_off)(c, kv, layer, b, h / G);
-    F(orc_attention_head)(q + h * D, kv->k + base, kv->v + base, pos + 1, D, a + h * D);
+    F(orc_attention_head)(q + h * D, F(kv_at)(kv, kv->k, base), F(kv_at)(kv, kv->v, base),
+                          kv->bf16, pos + 1, D, a + h * D);
   }
   F(post_attention)(m, layer, a, x);
   free(q);
@@ -303,16 +320,17 @@ int F(orc_forward_chunk)(const orc_model* m, orc_kv* kv, int b, int n, const int
       for (int g = 0; g < c->n_kv_heads; ++g) {
         long base = F(kv_off)(c, kv, l, b, g) + (long)(start_pos + i) * D;
         for (int e = 0; e < D; ++e) {
-          kv->k[base + e] = F(narrow)(k[g * D + e]);
-          kv->v[base + e] = F(narrow)(v[g * D + e]);
+          F(kv_put)(kv->k, kv->bf16, base + e, k[g * D + e]);
+          F(kv_put)(kv->v, kv->bf16, base + e, v[g * D + e]);
         }
       }
     }
     for (int i = 0; i < n; ++i) {
       for (int h = 0; h < c->n_q_heads; ++h) {
         long base = F(kv_off)(c, kv, l, b, h / G);
-        F(orc_attention_head)(q + (long)i * qd + h * D, kv->k + base, kv->v + base,
-                              start_pos + i + 1, D, a + h * D);
+        F(orc_attention_head)(q + (long)i * qd + h * D, F(kv_at)(kv, kv->k, base),
+                              F(kv_at)(kv, kv->v, base), kv->bf16, start_pos + i + 1, D,
+                              a + h * D);
       }
       F(post_attention)(m, l, a, x + (long)i * H);
     }
@@ -329,9 +347,10 @@ int F(orc_forward_chunk)(const orc_model* m, orc_kv* kv, int b, int n, const int
 /* The uncached forward over a whole sequence of t tokens at positions
  * 0 .. t-1: per layer, all keys and values are computed from that layer's
  * input, the t x t score matrix is masked causally (key j visible to query i
- * iff j <= i) and softmaxed row by row. K and V are rounded to bf16 exactly as
- * the cache stores them. logits: [t, V]. */
-int F(orc_forward_full)(const orc_model* m, int t, const int32_t* tokens, REAL* logits) {
+ * iff j <= i) and softmaxed row by row. K and V are rounded exactly as a cache
+ * of that type stores them (fp32, or bf16 when kv_bf16). logits: [t, V]. */
+int F(orc_forward_full)(const orc_model* m, int t, const int32_t* tokens, int kv_bf16,
+                        REAL* logits) {
   const orc_config* c = &m->cfg;
   int H = c->hidden, D = c->head_dim, G = c->n_q_heads / c->n_kv_heads;
   int qd = c->n_q_heads * D, kd = c->n_kv_heads * D;
@@ -349,8 +368,9 @@ int F(orc_forward_full)(const orc_model* m, int t, const int32_t* tokens, REAL* 
     for (int i = 0; i < t; ++i) {
       F(qkv_token)(m, l, x + (long)i * H, i, q + (long)i * qd, k + (long)i * kd, v + (long)i * kd);
       for (int e = 0; e < kd; ++e) {
-        k[(long)i * kd + e] = F(widen)(F(narrow)(k[(long)i * kd + e]));
-        v[(long)i * kd + e] = F(widen)(F(narrow)(v[(long)i * kd + e]));
+        const long j = (long)i * kd + e;
+        k[j] = kv_bf16 ? F(widen)(F(narrow)(k[j])) : (REAL)(float)k[j];
+        v[j] = kv_bf16 ? F(widen)(F(narrow)(v[j])) : (REAL)(float)v[j];
       }
     }
     for (int i = 0; i < t; ++i) {

@@ -51,9 +51,8 @@ def test_gqa_repeats_kv_heads(orc):
     kv = m.new_kv(1, 8)
     pos = 5
     for g, c in enumerate(consts):
-        kv.v[0, 0, g, :pos] = _bf16(np.full((pos, D), c)).view(torch.int16).numpy().view(np.uint16)
-    kv.k[0, 0, :, :pos] = synth.normal_bf16(0, 99, (s.n_kv_heads, pos, D), 0.5).view(
-        torch.int16).numpy().view(np.uint16)
+        kv.v[0, 0, g, :pos] = c
+    kv.k[0, 0, :, :pos] = synth.normal_bf16(0, 99, (s.n_kv_heads, pos, D), 0.5).float().numpy()
     x = np.random.default_rng(0).standard_normal(s.hidden)
     out = m.block_decode(0, kv, 0, pos, x, "f64")
     a = (out - x).reshape(s.n_q_heads, D)
@@ -81,15 +80,16 @@ def test_causal_mask(tiny):
 
 @pytest.mark.parametrize("which", ["tiny", "tiny_qk"])
 @pytest.mark.parametrize("prec", ["f32", "f64"])
-def test_cache_invariant_five_chunkings(which, prec, request):
+@pytest.mark.parametrize("kv_bf16", [False, True])
+def test_cache_invariant_five_chunkings(which, prec, kv_bf16, request):
     """nanoinfer "KV cache": the same 8 tokens under five chunkings (one shot,
     one at a time, prompt then decode, halves, ragged) give what one uncached
-    pass gives."""
+    pass gives, for a cache that stores fp32 or bf16."""
     m, _ = request.getfixturevalue(which)
     toks = synth.token_ids(8, m.shape.vocab, stream=4)
-    ref = m.forward_full(toks, prec)
+    ref = m.forward_full(toks, prec, kv_bf16=kv_bf16)
     for chunks in ([8], [1] * 8, [5, 1, 1, 1], [4, 4], [3, 2, 3]):
-        kv = m.new_kv(1, 8)
+        kv = m.new_kv(1, 8, bf16=kv_bf16)
         rows, start = [], 0
         for n in chunks:
             rows.append(m.forward_chunk(kv, 0, toks[start:start + n], start, prec))
@@ -97,7 +97,7 @@ def test_cache_invariant_five_chunkings(which, prec, request):
         got = np.concatenate(rows)
         assert _rel_l2(got, ref) < (1e-6 if prec == "f32" else 1e-14), chunks
     # token-major decode steps (the decode path proper)
-    kv = m.new_kv(1, 8)
+    kv = m.new_kv(1, 8, bf16=kv_bf16)
     for i in range(8):
         logits, nxt = m.decode_step(kv, toks[i:i + 1], np.array([i], np.int32), prec)
     assert _rel_l2(logits[0], ref[-1]) < (1e-6 if prec == "f32" else 1e-14)

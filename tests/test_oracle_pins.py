@@ -218,6 +218,9 @@ def test_attention_matches_torch_sdpa(orc):
             q.view(1, 1, 1, d), k.double().view(1, 1, n, d), v.double().view(1, 1, n, d)).view(d)
         out = orc.attention_head(q.numpy(), k, v, "f64")
         assert _rel_l2(out, ref.numpy()) < 1e-13
+        # the same keys and values held as fp32 (the default cache type)
+        out32 = orc.attention_head(q.numpy(), k.float().numpy(), v.float().numpy(), "f64")
+        assert _rel_l2(out32, ref.numpy()) < 1e-13
 
 
 # ---------------------------------------------------------------- int8

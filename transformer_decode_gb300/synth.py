@@ -73,10 +73,11 @@ QWEN3_8B = ModelShape(hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
                       qk_norm=True, tie_embeddings=False)
 # A tiny model that keeps brute force cheap: every size still spans ragged
 # tails of the kernels' tiles.
-TINY = ModelShape(hidden=64, n_q_heads=4, n_kv_heads=2, head_dim=16, ffn=128,
-                  n_layers=2, vocab=256)
-TINY_QKNORM = dataclasses.replace(TINY, qkv_bias=False, qk_norm=True,
-                                  tie_embeddings=False)
+TINY = ModelShape(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, ffn=512,
+                  n_layers=2, vocab=512)
+TINY_QKNORM = ModelShape(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=128, ffn=384,
+                         n_layers=2, vocab=328, qkv_bias=False, qk_norm=True,
+                         tie_embeddings=False)
 
 
 @dataclasses.dataclass(frozen=True)
