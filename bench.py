@@ -1,0 +1,417 @@
+"""Decode-step benchmark: tokens/s and achieved HBM bandwidth on one GB300.
+
+Default workload (N = 1): the full 24-layer Qwen2-0.5B-shaped model with
+seeded random bf16 weights, batch 1, a 32-token prompt run through the decode
+step, then greedy decoding of 64 tokens (positions 32..95) on a contiguous KV
+cache. One timed step is one decode step (all layers plus the LM head and the
+arg-max) through nc_decode_step's CUDA graph. The 64-token sequence is decoded
+repeatedly: timed step i runs at position 32 + (i mod 64), and every 64 steps
+the sequence restarts (an 8-byte host-to-device reset of token and position).
+
+Printed (rank 0, one JSON line): the contract keys plus `roofline` (dominant
+kernel vs the measured HBM copy peak), `cpu_baseline` (the CPU oracle on the
+host cores, bounded sample), `e2e` (host buffers, copies inside the timed
+region), `hbm` (algorithmic bytes per step over step time) and `clocks`.
+
+--impl reference times the CPU oracle itself on the same workload (the
+reference arm of this build).
+Multi-GPU (torchrun, N > 1): replicas only, one independent model per GPU, no
+collective on the data path; value = tokens of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from transformer_decode_gb300 import nc, synth  # noqa: E402
+
+METRIC = "decode tokens/s at 1 GB300 and achieved HBM GB/s as fraction of ~8 TB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = "qwen2_0p5b_b1_greedy64"
+
+
+# ---------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(shape, batch, positions, kv_elem=4):
+    """Algorithmic HBM bytes of one decode step: every weight byte once, the
+    embedding rows, K/V of slots 0..p read once per layer and kv head, the new
+    K/V written, the logits written and tokens/positions read. kv_elem is the
+    cache element size (4: fp32 cache, 2: bf16)."""
+    H, D, F, L, V = shape.hidden, shape.head_dim, shape.ffn, shape.n_layers, shape.vocab
+    nqkv = shape.q_dim + 2 * shape.kv_dim
+    per_layer = 2 * (nqkv * H + shape.q_dim * H + 2 * F * H + H * F) + 2 * 2 * H
+    if shape.qkv_bias:
+        per_layer += 2 * nqkv
+    if shape.qk_norm:
+        per_layer += 2 * 2 * D
+    head = 2 * V * H + 2 * H
+    emb = 2 * H * batch
+    kv_row = 2 * shape.kv_dim * kv_elem  # K and V of one position, one layer
+    kv_read = sum((p + 1) for p in positions) * L * kv_row
+    kv_write = batch * L * kv_row
+    return L * per_layer + head + emb + kv_read + kv_write + 4 * V * batch + 8 * batch
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.15]
+        use = inside if inside else [min(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))] if rows else []
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm = [float(p[1]) for _, p in use if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in use for i in range(4)
+                          if p[5 + i].lower().startswith("active")})
+        pw = [float(p[3]) for _, p in use if p[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(use),
+                "samples_in_timed_region": len(inside)}
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, v):
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(shape, weights_cpu, prompt, seconds, max_steps):
+    """Time the CPU oracle decoding the workload's sequence (prompt steps, then
+    greedy) until `seconds` of work or `max_steps` steps. Returns
+    (steps, elapsed_s, threads)."""
+    import oracle
+    oracle.build()
+    om = oracle.OracleModel(shape, weights_cpu)
+    kv = om.new_kv(1, len(prompt) + max_steps + 1)
+    tok = np.array([prompt[0]], np.int32)
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_steps:
+        _, nxt = om.decode_step(kv, tok, np.array([n], np.int32))
+        n += 1
+        tok = np.array([prompt[n]], np.int32) if n < len(prompt) else nxt.astype(np.int32)
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return n, time.perf_counter() - t0, oracle.get_threads()
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    shape = synth.QWEN2_0P5B
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wd = synth.model_weights(shape, device=dev)
+    wc = {k: (None if v is None else v.cpu()) for k, v in wd.items() if k != "layers"}
+    wc["layers"] = [{k: (None if v is None else v.cpu()) for k, v in lw.items()}
+                    for lw in wd["layers"]]
+    del wd
+    prompt = synth.token_ids(32, shape.vocab).tolist()
+    steps = args.warmup + args.steps
+    n, el, thr = oracle_sample(shape, wc, prompt, seconds=1e9, max_steps=steps)
+    per = el / n
+    value = 1.0 / per
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 1, "prompt": 32,
+                   "note": "CPU oracle (plain C, fp32, OpenMP over output rows); every step "
+                           "of the sample timed, warm-up steps included"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                         "sample": f"{n} decode steps of the workload from position 0"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def time_kernel_gu(shape, wd, reps=48):
+    """Average duration of the gate|up + SiLU GEMV (nc_swiglu_gemv) at the
+    model's shape, cycling over the 24 layers' distinct weights so every launch
+    streams its 17.4 MB from HBM. Returns (avg_seconds, bytes_per_launch)."""
+    H, F = shape.hidden, shape.ffn
+    mats = [torch.cat([lw["wg"], lw["wu"]]).contiguous() for lw in wd["layers"]]
+    gam = [lw["g_mlp"] for lw in wd["layers"]]
+    x = torch.randn(1, H, device="cuda")
+    h = torch.empty(1, F, device="cuda")
+    st = torch.cuda.current_stream()
+    for i in range(len(mats)):
+        nc.swiglu_gemv(x, gam[i], shape.rms_eps, mats[i], h)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    torch.cuda.synchronize()
+    for r in range(reps):
+        i = r % len(mats)
+        evs[r][0].record(st)
+        nc.swiglu_gemv(x, gam[i], shape.rms_eps, mats[i], h)
+        evs[r][1].record(st)
+    torch.cuda.synchronize()
+    avg = sum(a.elapsed_time(b) for a, b in evs) / reps / 1e3
+    nbytes = 2 * F * H * 2 + H * 4 + H * 2 + F * 4
+    del mats
+    return avg, nbytes
+
+
+def run_nc(args, ws, rank, local):
+    torch.cuda.set_device(local)
+    shape = synth.QWEN2_0P5B
+    B, n_prompt, n_gen = 1, 32, 64
+    wd = synth.model_weights(shape, device="cuda")
+    max_ctx = n_prompt + n_gen + 16
+    model = nc.Model(shape, wd, max_batch=B, max_ctx=max_ctx)
+    kv = nc.KVCache(shape, B, max_ctx=max_ctx)
+    logits = torch.empty(B, shape.vocab, device="cuda")
+    prompt = synth.token_ids(n_prompt, shape.vocab).tolist()
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    pos = torch.empty(B, dtype=torch.int32, device="cuda")
+    reset_host = torch.tensor([prompt[-1], n_prompt - 1], dtype=torch.int32).pin_memory()
+
+    # prompt: each prompt token runs as one decode step (positions 0..30); the
+    # last prompt token (position 31) opens every decode cycle below
+    pos.fill_(0)
+    for i in range(n_prompt - 1):
+        tok.fill_(prompt[i])
+        model.decode_step(tok, pos, [i], kv, logits, use_graph=True, advance=True)
+    # A cycle is 65 decode steps at positions 31..95: the last prompt token
+    # (set from the host, 8 bytes) then 64 greedy tokens fed back on the device.
+    cycle = n_gen + 1
+
+    def run_steps(k):
+        """k decode steps of repeated cycles; returns the positions used."""
+        used = []
+        for i in range(k):
+            p = n_prompt - 1 + (i % cycle)
+            if i % cycle == 0:
+                tok.copy_(reset_host[:1], non_blocking=True)
+                pos.copy_(reset_host[1:], non_blocking=True)
+            model.decode_step(tok, pos, [p], kv, logits, use_graph=True, advance=True)
+            used.append(p)
+        return used
+
+    run_steps(args.warmup)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    e0.record(st)
+    used = run_steps(args.steps)
+    e1.record(st)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier(ws)
+    if rank == 0:
+        time.sleep(0.2)
+        sampler.stop()
+    el = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3)
+    restarts = sum(1 for i in range(args.steps) if i % cycle == 0)
+    value = ws * B * args.steps / el
+    ms = el / args.steps * 1e3
+    bytes_avg = sum(step_bytes(shape, B, [p]) for p in used) / len(used)
+    hbm_gbs = bytes_avg / (el / args.steps) / 1e9
+    peak, peak_kind = peaks()
+
+    # ---- e2e: public API with host buffers, copies inside the timed region
+    tok_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    pos_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    nxt_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    nxt_d = torch.empty(B, dtype=torch.int32, device="cuda")
+    # warm the (tokens, positions, logits, next) graph of this buffer set
+    tok_h[0] = prompt[-1]
+    pos_h[0] = n_prompt - 1
+    tok.copy_(tok_h)
+    pos.copy_(pos_h)
+    model.decode_step(tok, pos, [n_prompt - 1], kv, logits, nxt_d, use_graph=True)
+    torch.cuda.synchronize()
+    k_e2e = min(args.steps, 520)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    cur_tok = prompt[-1]
+    for i in range(k_e2e):
+        p = n_prompt - 1 + (i % cycle)
+        if i % cycle == 0:
+            cur_tok = prompt[-1]
+        tok_h[0] = cur_tok
+        pos_h[0] = p
+        tok.copy_(tok_h, non_blocking=True)
+        pos.copy_(pos_h, non_blocking=True)
+        model.decode_step(tok, pos, [p], kv, logits, nxt_d, use_graph=True)
+        nxt_h.copy_(nxt_d, non_blocking=True)
+        st.synchronize()
+        cur_tok = int(nxt_h[0])
+    t_e2e = max_over_ranks(ws, time.perf_counter() - t0)
+    e2e_value = ws * B * k_e2e / t_e2e
+
+    # ---- dominant kernel, timed alone with CUDA events on its stream
+    dur, kbytes = time_kernel_gu(shape, wd)
+    achieved = kbytes / dur / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        wc = {k: (None if v is None else v.cpu()) for k, v in wd.items() if k != "layers"}
+        wc["layers"] = [{k: (None if v is None else v.cpu()) for k, v in lw.items()}
+                        for lw in wd["layers"]]
+        n, sec, thr = oracle_sample(shape, wc, prompt, seconds=args.cpu_seconds, max_steps=96)
+        cpu = {"value": n / sec, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+               "sample": f"{n} decode steps of the workload from position 0 (prompt steps "
+                         f"first), {sec:.1f} s on {cpu_threads()} host cores"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": B, "prompt": n_prompt,
+                       "positions": f"cycles of {cycle} steps at positions {n_prompt - 1}.."
+                                    f"{n_prompt + n_gen - 1} ({restarts} cycles timed)",
+                       "weights": "bf16 seeded N(0,0.02) stand-in, fp32 accumulate",
+                       "kv": "contiguous fp32", "path": "nc_decode_step CUDA graph",
+                       "l2": "inputs larger than L2: 988 MB of weights stream every step",
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "hbm": {"bytes_per_step": bytes_avg, "gbs": hbm_gbs,
+                    "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
+                    "frac_of_measured_copy": hbm_gbs / peak, "peak_kind": peak_kind},
+            "roofline": {"bound": "hbm", "kernel": "k_gemv<1,SwiGLU> (gate|up + SiLU, 4864x2 rows x 896)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_kind": peak_kind, "avg_launch_us": dur * 1e6,
+                         "algorithmic_bytes_per_launch": kbytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": k_e2e,
+                    "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
+            "gpu_launches": args.steps * (2 + 7 * shape.n_layers),
+            "clocks": sampler.summary(w0, w1),
+        }
+        print(json.dumps(line), flush=True)
+    model.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", default="nc", choices=["nc", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_nc(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

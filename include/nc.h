@@ -1,0 +1,236 @@
+/*
+ * nc.h -- C ABI of libnc: the single-token decode step of a Qwen2-style
+ * decoder on one GB300 (sm_103a), as hand-written CUDA kernels.
+ *
+ * The model: pre-norm blocks x += attn(rmsnorm(x)); x += mlp(rmsnorm(x))
+ * (nanoinfer, "Model architecture"); grouped-query attention where query head
+ * h reads kv head h / (Hq/Hkv) (same section: repeat, not tile); half-split
+ * RoPE pairing i with i + D/2, applied once when K enters the cache (nanoinfer,
+ * "KV cache"); QKV bias and no o-proj bias; SwiGLU down(silu(gate) * up);
+ * tied embedding head after a final norm; greedy = argmax, lowest index on
+ * ties (nanoinfer, "Sampling": temperature 0).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev, and every tensor pointer unless stated, are DEVICE
+ *     pointers owned by the caller; libnc never frees them. *_host pointers
+ *     are host memory read synchronously during the call.
+ *   - bf16 tensors are raw bf16 bit patterns (2 bytes, round-to-nearest-even
+ *     when libnc narrows); activations are fp32; matrices are [out, in]
+ *     row-major (y = W x), rows 16-byte aligned (in * 2 % 16 == 0).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
+ *     enqueued asynchronously; nothing is read back from the device during a
+ *     call (validation uses host-side sizes and *_host copies only).
+ *   - Invalid input returns an error code before anything is enqueued and
+ *     leaves all state untouched. A CUDA error latches the model UNHEALTHY:
+ *     every later call on it returns NC_ERR_UNHEALTHY.
+ *   - nc_last_error_message() gives a thread-local description of the last
+ *     failure.
+ */
+#ifndef NC_H
+#define NC_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NC_ABI_VERSION 1
+
+typedef enum {
+  NC_OK = 0,
+  NC_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad flag */
+  NC_ERR_SHAPE = 2,            /* sizes inconsistent or unsupported */
+  NC_ERR_DTYPE = 3,            /* weight type not supported by this call */
+  NC_ERR_CAPACITY = 4,         /* batch or positions beyond what was reserved */
+  NC_ERR_POSITION = 5,         /* a position outside [0, capacity) or a block-table hole */
+  NC_ERR_CUDA = 6,             /* a CUDA runtime call failed (model now unhealthy) */
+  NC_ERR_TIMEOUT = 7,          /* a bounded device-side wait expired */
+  NC_ERR_UNHEALTHY = 8,        /* the model saw an earlier CUDA failure */
+  NC_ERR_UNSUPPORTED = 9
+} nc_status;
+
+typedef enum { NC_BF16 = 0, NC_INT8 = 1 } nc_wtype;
+
+/* Hyperparameters. head_dim must be 64 or 128; n_q_heads a multiple of
+ * n_kv_heads with group <= 8; hidden, ffn, n_q_heads*head_dim multiples of 8. */
+typedef struct {
+  int hidden;          /* H */
+  int n_q_heads;       /* Hq */
+  int n_kv_heads;      /* Hkv */
+  int head_dim;        /* D */
+  int ffn;             /* F */
+  int n_layers;        /* L */
+  int vocab;           /* V */
+  float rms_eps;       /* RMSNorm epsilon */
+  float rope_theta;    /* RoPE base */
+  int qkv_bias;        /* 1: q, k, v projections carry a bias (Qwen2) */
+  int qk_norm;         /* 1: per-head RMSNorm of q and k before RoPE (gains [D]) */
+  int tie_embeddings;  /* 1: logits use the embedding matrix */
+  nc_wtype wtype;      /* NC_INT8: the seven projections run W8A8 */
+} nc_config;
+
+/* One block's weights in checkpoint layout (device, bf16, caller-owned; read
+ * only during nc_model_create, which keeps its own packed copy). */
+typedef struct {
+  const void *wq, *wk, *wv;     /* [Hq*D, H], [Hkv*D, H], [Hkv*D, H] */
+  const void *bq, *bk, *bv;     /* [Hq*D], [Hkv*D], [Hkv*D]; NULL unless qkv_bias */
+  const void *wo;               /* [H, Hq*D] */
+  const void *wg, *wu;          /* [F, H] */
+  const void *wd;               /* [H, F] */
+  const void *g_attn, *g_mlp;   /* [H] */
+  const void *g_q, *g_k;        /* [D]; NULL unless qk_norm */
+} nc_layer_weights;
+
+typedef struct {
+  const void* embed;               /* [V, H] */
+  const void* lm_head;             /* [V, H]; NULL when tie_embeddings */
+  const void* g_final;             /* [H] */
+  const nc_layer_weights* layers;  /* HOST array of n_layers entries */
+} nc_weights;
+
+/* Element type of the KV cache. fp32 is nanoinfer's cache ("24 KiB per token
+ * at fp32" for the 0.5B shape) and the default; bf16 halves the cache traffic
+ * and rounds K and V to nearest even when they are stored. */
+typedef enum { NC_KV_F32 = 0, NC_KV_BF16 = 1 } nc_kv_dtype;
+
+/* KV cache (caller-owned device memory of `dtype`). K and V of the new token
+ * are written at slot `position` of its sequence; attention reads slots
+ * 0..position.
+ *   contiguous (paged = 0): k, v are [L][batch_capacity][Hkv][max_ctx][D].
+ *   paged (paged = 1):      k, v are [L][num_blocks][Hkv][block_size][D];
+ *     position p of sequence b lives in block block_table[b][p / block_size]
+ *     at offset p % block_size (vLLM-style gather; Tang section 2.1 "paged KV
+ *     caches" as a gather view). block_table is int32 [batch][max_blocks_per_seq]
+ *     on the device, with an identical host copy used for validation. */
+typedef struct {
+  int paged;
+  nc_kv_dtype dtype;
+  int batch_capacity;      /* contiguous: sequences reserved */
+  int max_ctx;             /* contiguous: slots per sequence; paged: max_blocks_per_seq*block_size */
+  int block_size;          /* paged */
+  int num_blocks;          /* paged: physical blocks per layer */
+  int max_blocks_per_seq;  /* paged */
+  void* k;
+  void* v;
+  const int32_t* block_table;       /* device, paged only */
+  const int32_t* block_table_host;  /* host, paged only */
+} nc_kv_cache;
+
+typedef struct nc_model nc_model; /* opaque: packed weights, workspace, graphs */
+
+const char* nc_status_string(nc_status s);
+const char* nc_last_error_message(void);
+int nc_abi_version(void);
+
+/* Build a model: validates cfg, packs the weights into model-owned device
+ * memory (QKV rows concatenated, gate and up concatenated; NC_INT8 quantises
+ * the seven projections per output row, nanoinfer "Quantization"), and
+ * reserves the workspace for up to max_batch sequences of up to max_ctx
+ * positions. Synchronises `stream` before returning. */
+nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, int max_batch, int max_ctx,
+                          void* stream, nc_model** out);
+nc_status nc_model_destroy(nc_model* m);
+/* Bytes of packed weights and of workspace held by the model. */
+nc_status nc_model_memory(const nc_model* m, size_t* weight_bytes, size_t* workspace_bytes);
+
+/* Flags of nc_decode_step. */
+#define NC_STEP_GRAPH 1   /* replay a CUDA graph captured on first use for this
+                             (batch, kv layout, buffer pointers); else launch
+                             the kernels directly */
+#define NC_STEP_ADVANCE 2 /* after the step, on the device: positions_dev[b] += 1
+                             and tokens_dev[b] = the greedy token, so the next
+                             call continues greedy decoding with no host work
+                             (the caller then passes positions_host + 1) */
+
+/* One decode step for `batch` sequences (nanoinfer "Model architecture" and
+ * "KV cache"; the one-call-per-token step of nanocompile's phase 7): token
+ * tokens_dev[b] enters sequence b at position positions[b] (= tokens already
+ * cached). Every layer writes K/V at that slot; logits_dev [batch, V] fp32
+ * receives the head output and next_dev [batch] int32 (nullable) the argmax
+ * (lowest index on ties; -1 if a logit is NaN). positions_host must equal
+ * positions_dev. tokens_dev and positions_dev are written only under
+ * NC_STEP_ADVANCE. */
+nc_status nc_decode_step(nc_model* m, int batch, int32_t* tokens_dev, int32_t* positions_dev,
+                         const int32_t* positions_host, const nc_kv_cache* kv, float* logits_dev,
+                         int32_t* next_dev, int flags, void* stream);
+
+/* One block (layer `layer`) for `batch` sequences: x_dev [batch, H] fp32 is
+ * the residual stream, updated in place; K/V are appended at positions. */
+nc_status nc_block_forward(nc_model* m, int layer, int batch, float* x_dev,
+                           const int32_t* positions_dev, const int32_t* positions_host,
+                           const nc_kv_cache* kv, void* stream);
+
+/* Device watchdog word (0 = fine, else an nc_status set by a kernel, e.g. a
+ * NaN in the logits or an expired bounded wait). Synchronises `stream`,
+ * reads the word and clears it. */
+nc_status nc_get_device_status(nc_model* m, void* stream, int* code);
+
+/* ---------------- per-stage entry points (no model needed unless named) ---- */
+
+/* y[b, n] = sum_k W[n, k] * xn[b, k] (+ bias[n]), xn = rmsnorm(x[b]) * gamma
+ * when gamma != NULL (nanocompile: the five passes of rms_norm fused into one,
+ * and the norm fused into the GEMV that follows), else xn = x.
+ * x [B, K] fp32, gamma [K] bf16, W [N, K] bf16, bias [N] bf16 or NULL,
+ * y [B, N] fp32. B <= 16. */
+nc_status nc_rmsnorm_gemv(const float* x, const void* gamma, float eps, const void* W,
+                          const void* bias, int B, int K, int N, float* y, void* stream);
+
+/* x[b, n] += sum_k W[n, k] * a[b, k]: the o-proj and down projections with
+ * the residual add fused in (nanocompile, "Phase 3": "output projection with
+ * its residual add"). a [B, K], x [B, N] fp32 in place, W [N, K] bf16. */
+nc_status nc_gemv_residual(const float* a, const void* W, int B, int K, int N, float* x,
+                           void* stream);
+
+/* h[b, f] = silu(g_f) * u_f with g = W_gate xn, u = W_up xn and xn the
+ * normed x (Tang section 2.3: sibling reductions gate|up merged; nanoinfer
+ * "Phase 8" sigmoid form). W_gu is [2F, K] bf16: rows 0..F-1 gate, F..2F-1 up.
+ * x [B, K], h [B, F] fp32. */
+nc_status nc_swiglu_gemv(const float* x, const void* gamma, float eps, const void* W_gu, int B,
+                         int K, int F, float* h, void* stream);
+
+/* RoPE (half-split) on q and k of layer `layer` at positions, optional
+ * per-head q/k RMSNorm before it, then K and V rounded to bf16 and stored at
+ * slot positions[b] (nanoinfer "KV cache": rotate once on insert).
+ * qkv [B, (Hq + 2 Hkv) D] fp32 (bias already added), q_out [B, Hq D] fp32. */
+nc_status nc_rope_qkv(const nc_model* m, int layer, int B, const float* qkv,
+                      const int32_t* positions_dev, const int32_t* positions_host,
+                      float* q_out, const nc_kv_cache* kv, void* stream);
+
+/* Split-K GQA decode attention (Tang section 2.2: online softmax is a monoid
+ * on (max, rescaled sum, weighted values); section 2.5: split is valid for
+ * any associative monoid): for query head h of sequence b, softmax over
+ * slots 0..positions[b] of q.k_t / sqrt(D), weighted sum of v_t. Partials of
+ * each split go to the model's workspace and are merged into out
+ * [B, Hq D] fp32. q [B, Hq D] fp32 (already rotated). */
+nc_status nc_attn_decode(const nc_model* m, int layer, int B, const float* q,
+                         const int32_t* positions_dev, const int32_t* positions_host,
+                         const nc_kv_cache* kv, float* out, void* stream);
+
+/* logits[b, v] = sum_k W[v, k] * xn[b, k] with xn = rmsnorm(x[b]) * gamma,
+ * and next[b] = argmax_v logits[b, v], lowest index on ties, -1 on NaN
+ * (Tang section 2.2: arg-max is a monoid on (value, index)). next nullable.
+ * Needs scratch for per-block partials: uses the model's workspace. */
+nc_status nc_lm_head_argmax(nc_model* m, const float* x, const void* gamma, float eps,
+                            const void* W, int B, int K, int V, float* logits, int32_t* next,
+                            void* stream);
+
+/* ---------------- W8A8 (nanoinfer "Quantization", per-token activations) ---- */
+
+/* Per-output-row symmetric weight quantisation: scale[n] = amax_n / 127,
+ * q[n, k] = clamp(round_half_away(W[n, k] / scale[n]), -127, 127); a zero row
+ * gets scale 0 and q = 0. W [N, K] bf16, q [N, K] int8, scale [N] fp32. */
+nc_status nc_quantize_weight(const void* W, int N, int K, int8_t* q, float* scale, void* stream);
+
+/* y[b, n] = float(acc[b, n]) * (w_scale[n] * sx[b]) (+ bias[n]) with
+ * acc = sum_k Wq[n, k] * xq[b, k] in int32, xq/sx the per-token quantisation
+ * of xn (normed when gamma != NULL). The optional outputs expose xq [B, K]
+ * int8, sx [B] fp32 and acc [B, N] int32 for bit-exact checks. */
+nc_status nc_w8a8_gemv(const float* x, const void* gamma, float eps, const int8_t* Wq,
+                       const float* w_scale, const void* bias, int B, int K, int N, float* y,
+                       int8_t* xq_out, float* sx_out, int32_t* acc_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NC_H */

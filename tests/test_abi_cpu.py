@@ -1,0 +1,93 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/nc.h declares, and rejects invalid input before
+any CUDA call (nothing here reaches a kernel)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from transformer_decode_gb300 import nc, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "nc.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nc_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return nc.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(nc.EXPORTS)
+    assert lib.nc_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(nc.STATUS):
+        assert lib.nc_status_string(code).decode() == name
+
+
+def _cfg(**kw):
+    s = synth.QWEN2_0P5B
+    c = nc.Config(s.hidden, s.n_q_heads, s.n_kv_heads, s.head_dim, s.ffn, s.n_layers, s.vocab,
+                  1e-6, 1e6, 1, 0, 1, 0)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value", [("head_dim", 96), ("n_kv_heads", 3), ("hidden", 900),
+                                          ("rms_eps", 0.0), ("wtype", 7), ("vocab", 0)])
+def test_model_create_rejects_bad_config(lib, field, value):
+    cfg = _cfg(**{field: value})
+    layers = (nc.LayerWeights * cfg.n_layers)()
+    w = nc.Weights(16, 0, 16, layers)
+    h = C.c_void_p()
+    rc = lib.nc_model_create(C.byref(cfg), C.byref(w), 1, 128, None, C.byref(h))
+    assert rc == nc.STATUS.index("NC_ERR_SHAPE"), lib.nc_last_error_message()
+    assert h.value is None
+
+
+def test_model_create_rejects_null_and_misaligned_weights(lib):
+    cfg = _cfg()
+    layers = (nc.LayerWeights * cfg.n_layers)()
+    h = C.c_void_p()
+    rc = lib.nc_model_create(C.byref(cfg), C.byref(nc.Weights(0, 0, 16, layers)), 1, 128, None,
+                             C.byref(h))
+    assert rc == nc.STATUS.index("NC_ERR_INVALID_ARGUMENT")
+    rc = lib.nc_model_create(C.byref(cfg), C.byref(nc.Weights(24, 0, 16, layers)), 1, 128, None,
+                             C.byref(h))
+    assert rc == nc.STATUS.index("NC_ERR_INVALID_ARGUMENT")
+    assert b"aligned" in lib.nc_last_error_message()
+    # a layer pointer missing
+    rc = lib.nc_model_create(C.byref(cfg), C.byref(nc.Weights(16, 0, 16, layers)), 1, 128, None,
+                             C.byref(h))
+    assert rc == nc.STATUS.index("NC_ERR_INVALID_ARGUMENT")
+    # capacity
+    rc = lib.nc_model_create(C.byref(cfg), C.byref(nc.Weights(16, 0, 16, layers)), 17, 128, None,
+                             C.byref(h))
+    assert rc == nc.STATUS.index("NC_ERR_CAPACITY")
+
+
+def test_stage_entry_points_reject_bad_shapes(lib):
+    P = C.c_void_p(4096)
+    assert lib.nc_rmsnorm_gemv(None, None, 1e-6, P, None, 1, 64, 8, P, None) == 1
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, None, 1, 60, 8, P, None) == 2   # K % 8
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, None, 17, 64, 8, P, None) == 2  # B > 16
+    assert lib.nc_rmsnorm_gemv(C.c_void_p(4100), None, 1e-6, P, None, 1, 64, 8, P, None) == 1
+    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, 0, 64, 8, P, None) == 2
+    assert lib.nc_gemv_residual(P, P, 1, 64, 0, P, None) == 2
+    assert lib.nc_w8a8_gemv(P, None, 1e-6, P, P, None, 1, 40, 8, P, None, None, None, None) == 2
+    assert lib.nc_quantize_weight(P, 0, 8, P, P, None) == 2
+    assert lib.nc_decode_step(None, 1, P, P, P, None, P, None, 1, None) == 1
+    assert lib.nc_model_destroy(None) == 1

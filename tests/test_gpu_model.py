@@ -1,0 +1,236 @@
+"""GPU parity of whole blocks and whole decode steps against the CPU oracle,
+through the C ABI (nc_block_forward, nc_decode_step)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import REL_L2_GATE, bf16_bits, f32, rel_l2, to_device, token_agrees, weights_both
+from transformer_decode_gb300 import nc, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    nc.load()
+    oracle.build()
+
+
+def test_generator_same_bits_on_gpu_and_cpu():
+    a = synth.normal_bf16(0, 42, (3, 1_000_003), 0.02, device="cuda")
+    b = synth.normal_bf16(0, 42, (3, 1_000_003), 0.02, device="cpu")
+    assert torch.equal(a.cpu().view(torch.int16), b.view(torch.int16))
+    assert torch.equal(synth.token_ids(999, 151936, device="cuda").cpu(), synth.token_ids(999, 151936))
+
+
+def _fill_past(kv, okv, shape, positions, layers):
+    """Synthetic past K/V (seed 4) for slots 0..p-1 of every sequence, written
+    into both caches."""
+    for l in range(layers):
+        for b, p in enumerate(positions):
+            if p == 0:
+                continue
+            for g in range(shape.n_kv_heads):
+                kr = synth.synthetic_kv_rows(shape, l, b, g, 0, p, device="cuda")
+                vr = synth.synthetic_kv_rows(shape, l, b, g, 1, p, device="cuda")
+                kv.write_sequence(l, b, g, kr, vr)
+                if okv.bf16:
+                    okv.k[l, b, g, :p] = bf16_bits(kr).reshape(p, -1)
+                    okv.v[l, b, g, :p] = bf16_bits(vr).reshape(p, -1)
+                else:
+                    okv.k[l, b, g, :p] = f32(kr).reshape(p, -1)
+                    okv.v[l, b, g, :p] = f32(vr).reshape(p, -1)
+
+
+# ------------------------------------------------------------------ one block (C0 shape)
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("kv_bf16", [False, True])
+def test_block_forward_0p5b_past16(paged, kv_bf16):
+    shape = dataclasses.replace(synth.QWEN2_0P5B.with_layers(1), vocab=1024)
+    wd, wc = weights_both(shape)
+    model = nc.Model(shape, wd, max_batch=1, max_ctx=64)
+    om = oracle.OracleModel(shape, wc)
+    pos = 16
+    kdt = torch.bfloat16 if kv_bf16 else torch.float32
+    if paged:
+        table, nblk = synth.block_tables([pos], 1, 16)
+        kv = nc.KVCache(shape, 1, paged=True, block_table=table, num_blocks=nblk, dtype=kdt)
+    else:
+        kv = nc.KVCache(shape, 1, max_ctx=64, dtype=kdt)
+    okv = om.new_kv(1, 64, bf16=kv_bf16)
+    _fill_past(kv, okv, shape, [pos], 1)
+    x0 = synth.normal_bf16(0, 9999, (1, shape.hidden), 1.0).float()
+    x = x0.cuda()
+    p = torch.tensor([pos], dtype=torch.int32)
+    model.block_forward(0, x, p.cuda(), p, kv)
+    torch.cuda.synchronize()
+    ref = om.block_decode(0, okv, 0, pos, x0[0].numpy())
+    assert rel_l2(f32(x[0]), ref) < REL_L2_GATE / 10
+    widen = oracle.bf16_to_f32 if kv_bf16 else (lambda a: a)
+    for g in range(shape.n_kv_heads):
+        ks, vs = kv.slot_view(0, 0, g, pos)
+        tol = 1e-3 if kv_bf16 else 1e-5
+        assert rel_l2(f32(ks), widen(okv.k[0, 0, g, pos])) < tol
+        assert rel_l2(f32(vs), widen(okv.v[0, 0, g, pos])) < tol
+    model.close()
+
+
+# ------------------------------------------------------------------ greedy decode
+def _greedy_compare(shape, wd, wc, prompt, steps, batch=1, past=None, paged=False, w8a8=False,
+                    use_graph=True, gate=REL_L2_GATE, kv_bf16=False, derived_gate=False):
+    """Teacher-forced greedy decode: both sides consume the oracle's token.
+    Returns the worst logit rel-L2 seen.
+
+    derived_gate: for paths with a rounding discontinuity inside the model
+    (int8 activation codes, bf16 K/V), the gate at each step is
+    max(gate, 4 x the rel-L2 between the fp32 oracle and its fp64 twin on the
+    same inputs): two fp32 evaluations of the same definition land on
+    different sides of a rounding boundary about that often."""
+    om = oracle.OracleModel(shape, wc, w8a8=w8a8)
+    past = past or [0] * batch
+    n_total = len(prompt[0]) + steps if prompt is not None else steps
+    max_ctx = max(past) + n_total + 1
+    model = nc.Model(shape, wd, max_batch=batch, max_ctx=max_ctx + 16, w8a8=w8a8)
+    kdt = torch.bfloat16 if kv_bf16 else torch.float32
+    if paged:
+        table, nblk = synth.block_tables(past, n_total, 16)
+        kv = nc.KVCache(shape, batch, paged=True, block_table=table, num_blocks=nblk, dtype=kdt)
+    else:
+        kv = nc.KVCache(shape, batch, max_ctx=max_ctx, dtype=kdt)
+    okv = om.new_kv(batch, max_ctx, bf16=kv_bf16)
+    _fill_past(kv, okv, shape, past, shape.n_layers)
+    okv64 = okv.copy() if derived_gate else None
+    logits = torch.empty(batch, shape.vocab, device="cuda")
+    nxt = torch.empty(batch, dtype=torch.int32, device="cuda")
+    pos = np.array(past, np.int32)
+    tok = np.array([prompt[b][0] for b in range(batch)] if prompt is not None else
+                   synth.token_ids(batch, shape.vocab, stream=77).tolist(), np.int32)
+    worst = 0.0
+    n_prompt = len(prompt[0]) if prompt is not None else 0
+    tok_d = torch.empty(batch, dtype=torch.int32, device="cuda")
+    pos_d = torch.empty(batch, dtype=torch.int32, device="cuda")
+    for i in range(n_total):
+        tok_d.copy_(torch.from_numpy(tok))
+        pos_d.copy_(torch.from_numpy(pos))
+        model.decode_step(tok_d, pos_d, pos, kv, logits, nxt, use_graph=use_graph)
+        ol, on = om.decode_step(okv, tok, pos)
+        if derived_gate:
+            ol64, _ = om.decode_step(okv64, tok, pos, "f64")
+        torch.cuda.synchronize()
+        gl, gn = logits.cpu().numpy(), nxt.cpu().numpy()
+        for b in range(batch):
+            e = rel_l2(gl[b], ol[b])
+            worst = max(worst, e)
+            g_b = max(gate, 4 * rel_l2(ol[b], ol64[b])) if derived_gate else gate
+            assert e < g_b, (i, b, e, g_b)
+            assert gn[b] == int(np.argmax(gl[b]))
+            assert token_agrees(int(gn[b]), ol[b], e), (i, b, gn[b], on[b])
+        pos = pos + 1
+        if i + 1 < n_prompt:
+            tok = np.array([prompt[b][i + 1] for b in range(batch)], np.int32)
+        else:
+            tok = on.astype(np.int32)
+    assert model.device_status() == 0
+    model.close()
+    return worst
+
+
+@pytest.mark.parametrize("shape", [synth.TINY, synth.TINY_QKNORM])
+@pytest.mark.parametrize("use_graph", [True, False])
+def test_decode_tiny(shape, use_graph):
+    wd, wc = weights_both(shape)
+    prompt = [synth.token_ids(5, shape.vocab, stream=11).tolist()]
+    _greedy_compare(shape, wd, wc, prompt, steps=20, use_graph=use_graph)
+
+
+def test_decode_tiny_batch_paged():
+    shape = synth.TINY
+    wd, wc = weights_both(shape)
+    _greedy_compare(shape, wd, wc, None, steps=12, batch=5, past=[0, 3, 16, 31, 70], paged=True)
+
+
+def test_decode_0p5b_prompt32_greedy64():
+    """The full 24-layer 0.5B-shaped model: a 32-token prompt then 64 greedy
+    tokens, contiguous cache, CUDA graph replay."""
+    shape = synth.QWEN2_0P5B
+    wd, wc = weights_both(shape)
+    prompt = [synth.token_ids(32, shape.vocab).tolist()]
+    worst = _greedy_compare(shape, wd, wc, prompt, steps=64)
+    print(f"0.5B greedy: worst logit rel-L2 {worst:.3e}")
+
+
+def test_decode_0p5b_w8a8_past512():
+    """W8A8 whole model: per-token int8 activation codes are a rounding
+    discontinuity, so the gate is derived per step from the oracle's own
+    fp32/fp64 spread; the integer arithmetic itself is checked bit-exact in
+    test_gpu_stages."""
+    shape = synth.QWEN2_0P5B
+    wd, wc = weights_both(shape)
+    worst = _greedy_compare(shape, wd, wc, None, steps=8, past=[512], w8a8=True,
+                            derived_gate=True)
+    print(f"0.5B W8A8: worst logit rel-L2 {worst:.3e}")
+
+
+@pytest.mark.parametrize("kv_bf16", [False, True])
+def test_decode_0p5b_batch16_paged(kv_bf16):
+    shape = synth.QWEN2_0P5B
+    wd, wc = weights_both(shape)
+    past = synth.past_lengths(16, 256, 4096).tolist()
+    worst = _greedy_compare(shape, wd, wc, None, steps=2, batch=16, past=past, paged=True,
+                            kv_bf16=kv_bf16, derived_gate=kv_bf16)
+    print(f"0.5B B16 paged (bf16 KV {kv_bf16}): worst logit rel-L2 {worst:.3e}")
+
+
+def test_decode_0p5b_bf16_kv_prompt():
+    """bf16 K/V from position 0: the stored rounding is a discontinuity (the
+    oracle's fp32 and fp64 runs differ by about 1e-3 here), so the gate is the
+    derived one."""
+    shape = synth.QWEN2_0P5B
+    wd, wc = weights_both(shape)
+    prompt = [synth.token_ids(8, shape.vocab).tolist()]
+    worst = _greedy_compare(shape, wd, wc, prompt, steps=8, kv_bf16=True, derived_gate=True)
+    print(f"0.5B bf16 KV: worst logit rel-L2 {worst:.3e}")
+
+
+def test_decode_8b_shape_two_layers_past4096():
+    shape = synth.QWEN3_8B.with_layers(2)
+    wd, wc = weights_both(shape)
+    worst = _greedy_compare(shape, wd, wc, None, steps=3, past=[4096])
+    print(f"8B-shaped (2 layers): worst logit rel-L2 {worst:.3e}")
+
+
+def test_invalid_inputs_leave_state_untouched():
+    shape = synth.TINY
+    wd, _ = weights_both(shape)
+    model = nc.Model(shape, wd, max_batch=2, max_ctx=32)
+    kv = nc.KVCache(shape, 2, max_ctx=32)
+    logits = torch.empty(2, shape.vocab, device="cuda")
+    tok = torch.zeros(2, dtype=torch.int32, device="cuda")
+    with pytest.raises(nc.NCError) as e:
+        model.decode_step(tok, tok, np.array([0, 32], np.int32), kv, logits)
+    assert e.value.code == nc.STATUS.index("NC_ERR_POSITION")
+    with pytest.raises(nc.NCError) as e:
+        model.decode_step(torch.zeros(3, dtype=torch.int32, device="cuda"),
+                          torch.zeros(3, dtype=torch.int32, device="cuda"), [0, 0, 0], kv,
+                          torch.empty(3, shape.vocab, device="cuda"))
+    assert e.value.code == nc.STATUS.index("NC_ERR_CAPACITY")
+    big = nc.KVCache(shape, 2, max_ctx=64)
+    with pytest.raises(nc.NCError) as e:
+        model.decode_step(tok, tok, [0, 0], big, logits)
+    assert e.value.code == nc.STATUS.index("NC_ERR_CAPACITY")
+    # paged: a hole in the block table is refused on the host
+    table = torch.tensor([[0, 1], [2, -1]], dtype=torch.int32)
+    pk = nc.KVCache(shape, 2, paged=True, block_table=table, num_blocks=3)
+    with pytest.raises(nc.NCError) as e:
+        model.decode_step(tok, tok, [3, 17], pk, logits)
+    assert e.value.code == nc.STATUS.index("NC_ERR_POSITION")
+    assert not kv.k.any() and not pk.k.any()
+    # an out-of-range token id is caught on the device without a fault
+    bad = torch.tensor([shape.vocab + 5, 1], dtype=torch.int32, device="cuda")
+    model.decode_step(bad, tok, [0, 0], kv, logits, use_graph=False)
+    torch.cuda.synchronize()
+    assert model.device_status() != 0
+    model.close()

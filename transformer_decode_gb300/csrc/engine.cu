@@ -1,0 +1,444 @@
+// engine.cu -- the model object, weight packing, and the decode step.
+//
+// nc_model_create packs the caller's checkpoint-layout weights once into
+// model-owned device memory (nanocompile "Phase 4": the runtime packs each
+// weight once): QKV rows concatenated into one [(Hq + 2 Hkv) D, H] matrix
+// (one wide GEMV, ForgeML "shared-projection fusion"), gate and up stacked
+// into [2F, H] (Tang section 2.3, merge_siblings), or, for W8A8, the int8
+// rows and per-row scales. The workspace (residual stream, q/k/v, attention
+// partials, gate|up output, arg-max partials, status word) is reserved here
+// too, so a decode step allocates nothing (nanocompile phase 7: one call per
+// token, a static memory plan).
+//
+// A step launches: embed -> L x [QKV GEMV, RoPE+append, attention, o-proj +
+// residual, gate|up + SiLU, down + residual] -> LM head + arg-max. With
+// use_graph the sequence is captured once per (batch, buffers) and replayed
+// as one CUDA graph: control crosses from host to device once per token and
+// never back inside the step (nanoserve day 49: host readbacks were the
+// graph breaks).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "engine.h"
+#include "kernels.h"
+
+namespace nc {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Bump allocator over one cudaMalloc; with a null base it only measures.
+struct Arena {
+  char* base = nullptr;
+  size_t used = 0;
+  template <class T>
+  T* take(size_t n) {
+    used = align_up(used, 256);
+    T* p = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(base) + used);
+    used += n * sizeof(T);
+    return p;
+  }
+};
+
+Model::~Model() {
+  for (auto& kv : graphs) cudaGraphExecDestroy(kv.second);
+  if (cap_stream) cudaStreamDestroy(cap_stream);
+  if (status_host) cudaFreeHost(status_host);
+  if (weights) cudaFree(weights);
+  if (workspace) cudaFree(workspace);
+}
+
+bool valid_config(const nc_config& c, std::string* why) {
+  char buf[256];
+  auto bad = [&](const char* m) {
+    snprintf(buf, sizeof buf, "%s", m);
+    *why = buf;
+    return false;
+  };
+  if (c.hidden <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.ffn <= 0 || c.n_layers <= 0 ||
+      c.vocab <= 0)
+    return bad("all sizes must be positive");
+  if (c.head_dim != 64 && c.head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (c.n_q_heads % c.n_kv_heads != 0) return bad("n_q_heads must be a multiple of n_kv_heads");
+  if (c.n_q_heads / c.n_kv_heads > 8) return bad("GQA group above 8 is unsupported");
+  if (c.hidden % 16 || c.ffn % 16) return bad("hidden and ffn must be multiples of 16");
+  if (c.hidden > 16384 || c.ffn > 65536) return bad("hidden or ffn too large");
+  if (!(c.rms_eps > 0) || !(c.rope_theta > 1)) return bad("rms_eps must be > 0 and rope_theta > 1");
+  if (c.wtype != NC_BF16 && c.wtype != NC_INT8) return bad("unknown weight type");
+  return true;
+}
+
+static nc_status check_ptr(const void* p, const char* name) {
+  if (!p) return fail(NC_ERR_INVALID_ARGUMENT, "weight pointer %s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(p) % 16)
+    return fail(NC_ERR_INVALID_ARGUMENT, "weight pointer %s is not 16-byte aligned", name);
+  return NC_OK;
+}
+
+nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch, int max_ctx,
+                       cudaStream_t s, Model** out) {
+  NC_CHECK(cfg && w && out && w->layers, NC_ERR_INVALID_ARGUMENT, "null argument");
+  std::string why;
+  NC_CHECK(valid_config(*cfg, &why), NC_ERR_SHAPE, "invalid config: %s", why.c_str());
+  NC_CHECK(max_batch >= 1 && max_batch <= 16, NC_ERR_CAPACITY, "max_batch must be in [1, 16]");
+  NC_CHECK(max_ctx >= 1 && max_ctx <= (1 << 20), NC_ERR_CAPACITY, "max_ctx out of range");
+  const nc_config& c = *cfg;
+  const int bt = max_batch <= 1 ? 1 : max_batch <= 2 ? 2 : max_batch <= 4 ? 4 : max_batch <= 8 ? 8 : 16;
+  NC_CHECK(bt * c.hidden <= 51200, NC_ERR_SHAPE,
+           "max_batch (rounded up to a power of 2) * hidden must be <= 51200 for the LM head");
+  nc_status st;
+  if ((st = check_ptr(w->embed, "embed")) || (st = check_ptr(w->g_final, "g_final"))) return st;
+  if (!c.tie_embeddings && (st = check_ptr(w->lm_head, "lm_head"))) return st;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const nc_layer_weights& L = w->layers[l];
+    const void* req[] = {L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd, L.g_attn, L.g_mlp};
+    for (const void* p : req)
+      if ((st = check_ptr(p, "layer projection or norm"))) return st;
+    if (c.qkv_bias)
+      for (const void* p : {L.bq, L.bk, L.bv})
+        if ((st = check_ptr(p, "qkv bias"))) return st;
+    if (c.qk_norm)
+      for (const void* p : {L.g_q, L.g_k})
+        if ((st = check_ptr(p, "q/k norm gain"))) return st;
+  }
+
+  auto m = new Model();
+  m->cfg = c;
+  m->max_batch = max_batch;
+  m->max_ctx = max_ctx;
+  const int H = c.hidden, D = c.head_dim, F = c.ffn, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
+  const size_t qd = (size_t)Hq * D, kd = (size_t)Hkv * D, nqkv = qd + 2 * kd;
+  const bool i8 = c.wtype == NC_INT8;
+
+  // Two passes over one layout function: first with null bases to size the
+  // arenas, then with the real allocations to assign every pointer.
+  size_t part_max = 0;
+  for (int b = 1; b <= max_batch; ++b) {
+    const size_t pf = attn_part_floats(b, Hq, D, attn_splits(b, Hkv, max_ctx));
+    if (pf > part_max) part_max = pf;
+  }
+  auto layout = [&](Arena& A, Arena& W) {
+    m->layers.assign(c.n_layers, LayerPacked{});
+    for (int l = 0; l < c.n_layers; ++l) {
+      LayerPacked& P = m->layers[l];
+      if (!i8) {
+        P.w_qkv = A.take<uint16_t>(nqkv * H);
+        P.w_o = A.take<uint16_t>(qd * H);
+        P.w_gu = A.take<uint16_t>(2 * (size_t)F * H);
+        P.w_d = A.take<uint16_t>((size_t)H * F);
+      } else {
+        P.q_qkv = A.take<int8_t>(nqkv * H);
+        P.q_o = A.take<int8_t>(qd * H);
+        P.q_gu = A.take<int8_t>(2 * (size_t)F * H);
+        P.q_d = A.take<int8_t>((size_t)H * F);
+        P.s_qkv = A.take<float>(nqkv);
+        P.s_o = A.take<float>(H);
+        P.s_gu = A.take<float>(2 * (size_t)F);
+        P.s_d = A.take<float>(H);
+      }
+      P.b_qkv = c.qkv_bias ? A.take<uint16_t>(nqkv) : nullptr;
+      P.g_attn = A.take<uint16_t>(H);
+      P.g_mlp = A.take<uint16_t>(H);
+      P.g_q = c.qk_norm ? A.take<uint16_t>(D) : nullptr;
+      P.g_k = c.qk_norm ? A.take<uint16_t>(D) : nullptr;
+    }
+    m->embed = A.take<uint16_t>((size_t)c.vocab * H);
+    m->head = c.tie_embeddings ? m->embed : A.take<uint16_t>((size_t)c.vocab * H);
+    m->g_final = A.take<uint16_t>(H);
+    m->inv_freq = A.take<float>(D / 2);
+
+    m->x = W.take<float>((size_t)max_batch * H);
+    m->qkv = W.take<float>((size_t)max_batch * nqkv);
+    m->q = W.take<float>((size_t)max_batch * qd);
+    m->attn = W.take<float>((size_t)max_batch * qd);
+    m->part = W.take<float>(part_max);
+    m->h = W.take<float>((size_t)max_batch * F);
+    m->am_part = W.take<unsigned long long>((size_t)max_batch * lm_head_grid());
+    m->ticket = W.take<unsigned int>(1);
+    m->status = W.take<int>(1);
+  };
+  Arena A0, W0;
+  layout(A0, W0);
+  const size_t wb = A0.used, ws = W0.used;
+
+  cudaError_t e = cudaMalloc(&m->weights, wb);
+  if (e == cudaSuccess) e = cudaMalloc(&m->workspace, ws);
+  if (e == cudaSuccess) e = cudaMallocHost(&m->status_host, sizeof(int));
+  if (e != cudaSuccess) {
+    delete m;
+    return fail(NC_ERR_CUDA, "cudaMalloc of %zu + %zu bytes failed: %s", wb, ws,
+                cudaGetErrorString(e));
+  }
+  m->weight_bytes = wb;
+  m->workspace_bytes = ws;
+  Arena A{static_cast<char*>(m->weights)}, W{static_cast<char*>(m->workspace)};
+  layout(A, W);
+
+  auto copy = [&](void* dst, const void* src, size_t bytes) -> cudaError_t {
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+  };
+  e = cudaSuccess;
+  for (int l = 0; l < c.n_layers && e == cudaSuccess; ++l) {
+    const nc_layer_weights& L = w->layers[l];
+    const LayerPacked& P = m->layers[l];
+    const uint16_t* wq = static_cast<const uint16_t*>(L.wq);
+    const uint16_t* wk = static_cast<const uint16_t*>(L.wk);
+    const uint16_t* wv = static_cast<const uint16_t*>(L.wv);
+    const uint16_t* wo = static_cast<const uint16_t*>(L.wo);
+    const uint16_t* wg = static_cast<const uint16_t*>(L.wg);
+    const uint16_t* wu = static_cast<const uint16_t*>(L.wu);
+    const uint16_t* wd = static_cast<const uint16_t*>(L.wd);
+    if (!i8) {
+      if (!e) e = copy(P.w_qkv, wq, qd * H * 2);
+      if (!e) e = copy(P.w_qkv + qd * H, wk, kd * H * 2);
+      if (!e) e = copy(P.w_qkv + (qd + kd) * H, wv, kd * H * 2);
+      if (!e) e = copy(P.w_o, wo, qd * H * 2);
+      if (!e) e = copy(P.w_gu, wg, (size_t)F * H * 2);
+      if (!e) e = copy(P.w_gu + (size_t)F * H, wu, (size_t)F * H * 2);
+      if (!e) e = copy(P.w_d, wd, (size_t)H * F * 2);
+    } else {
+      if (!e) e = launch_quantize_weight(wq, (int)qd, H, P.q_qkv, P.s_qkv, s);
+      if (!e) e = launch_quantize_weight(wk, (int)kd, H, P.q_qkv + qd * H, P.s_qkv + qd, s);
+      if (!e) e = launch_quantize_weight(wv, (int)kd, H, P.q_qkv + (qd + kd) * H, P.s_qkv + qd + kd, s);
+      if (!e) e = launch_quantize_weight(wo, H, (int)qd, P.q_o, P.s_o, s);
+      if (!e) e = launch_quantize_weight(wg, F, H, P.q_gu, P.s_gu, s);
+      if (!e) e = launch_quantize_weight(wu, F, H, P.q_gu + (size_t)F * H, P.s_gu + F, s);
+      if (!e) e = launch_quantize_weight(wd, H, F, P.q_d, P.s_d, s);
+    }
+    if (c.qkv_bias) {
+      if (!e) e = copy(P.b_qkv, L.bq, qd * 2);
+      if (!e) e = copy(P.b_qkv + qd, L.bk, kd * 2);
+      if (!e) e = copy(P.b_qkv + qd + kd, L.bv, kd * 2);
+    }
+    if (!e) e = copy(P.g_attn, L.g_attn, (size_t)H * 2);
+    if (!e) e = copy(P.g_mlp, L.g_mlp, (size_t)H * 2);
+    if (c.qk_norm) {
+      if (!e) e = copy(P.g_q, L.g_q, (size_t)D * 2);
+      if (!e) e = copy(P.g_k, L.g_k, (size_t)D * 2);
+    }
+  }
+  if (!e) e = copy(m->embed, w->embed, (size_t)c.vocab * H * 2);
+  if (!c.tie_embeddings && !e) e = copy(m->head, w->lm_head, (size_t)c.vocab * H * 2);
+  if (!e) e = copy(m->g_final, w->g_final, (size_t)H * 2);
+  // RoPE frequencies: float(1 / theta^(2i/D)), evaluated in double on the host.
+  std::vector<float> inv(D / 2);
+  for (int i = 0; i < D / 2; ++i) inv[i] = (float)(1.0 / pow((double)c.rope_theta, (2.0 * i) / D));
+  if (!e) e = cudaMemcpyAsync(m->inv_freq, inv.data(), inv.size() * 4, cudaMemcpyHostToDevice, s);
+  if (!e) e = cudaMemsetAsync(m->workspace, 0, ws, s);
+  if (!e) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    delete m;
+    return fail(NC_ERR_CUDA, "packing the weights failed: %s", cudaGetErrorString(e));
+  }
+  *out = m;
+  return NC_OK;
+}
+
+// ------------------------------------------------------------------ step
+KVView kv_view(const Model* m, const nc_kv_cache& kv) {
+  KVView v;
+  v.k = kv.k;
+  v.v = kv.v;
+  v.block_table = kv.block_table;
+  v.paged = kv.paged;
+  v.bf16 = kv.dtype == NC_KV_BF16;
+  v.batch_capacity = kv.batch_capacity;
+  v.max_ctx = kv.max_ctx;
+  v.block_size = kv.block_size;
+  v.num_blocks = kv.num_blocks;
+  v.max_blocks_per_seq = kv.max_blocks_per_seq;
+  v.n_kv_heads = m->cfg.n_kv_heads;
+  v.head_dim = m->cfg.head_dim;
+  return v;
+}
+
+int kv_capacity(const nc_kv_cache& kv) {
+  return kv.paged ? kv.max_blocks_per_seq * kv.block_size : kv.max_ctx;
+}
+
+nc_status validate_kv(const Model* m, int batch, const int32_t* positions_host,
+                      const nc_kv_cache* kv) {
+  NC_CHECK(kv && kv->k && kv->v, NC_ERR_INVALID_ARGUMENT, "kv cache pointers are NULL");
+  NC_CHECK(kv->dtype == NC_KV_F32 || kv->dtype == NC_KV_BF16, NC_ERR_DTYPE,
+           "unknown kv dtype %d", (int)kv->dtype);
+  NC_CHECK(reinterpret_cast<uintptr_t>(kv->k) % 16 == 0 && reinterpret_cast<uintptr_t>(kv->v) % 16 == 0,
+           NC_ERR_INVALID_ARGUMENT, "kv cache pointers must be 16-byte aligned");
+  NC_CHECK(positions_host, NC_ERR_INVALID_ARGUMENT, "positions_host is NULL");
+  const int cap = kv_capacity(*kv);
+  NC_CHECK(cap >= 1 && cap <= m->max_ctx, NC_ERR_CAPACITY,
+           "kv capacity %d outside [1, %d] reserved at model creation", cap, m->max_ctx);
+  if (!kv->paged) {
+    NC_CHECK(kv->batch_capacity >= batch, NC_ERR_CAPACITY, "kv batch_capacity %d < batch %d",
+             kv->batch_capacity, batch);
+  } else {
+    NC_CHECK(kv->block_table && kv->block_table_host, NC_ERR_INVALID_ARGUMENT,
+             "paged cache needs block_table and block_table_host");
+    NC_CHECK(kv->block_size >= 1 && kv->num_blocks >= 1 && kv->max_blocks_per_seq >= 1,
+             NC_ERR_SHAPE, "paged cache sizes must be positive");
+  }
+  for (int b = 0; b < batch; ++b) {
+    const int p = positions_host[b];
+    NC_CHECK(p >= 0 && p < cap, NC_ERR_POSITION, "position %d of sequence %d outside [0, %d)", p,
+             b, cap);
+    if (kv->paged) {
+      for (int i = 0; i <= p / kv->block_size; ++i) {
+        const int blk = kv->block_table_host[(size_t)b * kv->max_blocks_per_seq + i];
+        NC_CHECK(blk >= 0 && blk < kv->num_blocks, NC_ERR_POSITION,
+                 "block table entry %d of sequence %d is %d (pool has %d blocks)", i, b, blk,
+                 kv->num_blocks);
+      }
+    }
+  }
+  return NC_OK;
+}
+
+static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* positions,
+                                 const KVView& kvv, int splits, cudaStream_t s) {
+  const nc_config& c = m->cfg;
+  const LayerPacked& P = m->layers[layer];
+  const int H = c.hidden, D = c.head_dim, F = c.ffn, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
+  const int nqkv = (Hq + 2 * Hkv) * D;
+  const bool i8 = c.wtype == NC_INT8;
+  cudaError_t e;
+  if (!i8) {
+    e = launch_gemv(Epi::Store, {m->x, P.g_attn, c.rms_eps, P.w_qkv, P.b_qkv, batch, H, nqkv, m->qkv}, s);
+  } else {
+    W8Args a{m->x, P.g_attn, c.rms_eps, P.q_qkv, P.s_qkv, P.b_qkv, batch, H, nqkv, m->qkv,
+             nullptr, nullptr, nullptr};
+    e = launch_w8a8(Epi::Store, a, s);
+  }
+  if (e) return e;
+  RopeArgs r{m->qkv, positions, m->inv_freq, P.g_q, P.g_k, c.rms_eps, batch, Hq, Hkv, D, layer,
+             m->q, kvv, m->status};
+  if ((e = launch_rope_qkv(r, s))) return e;
+  AttnArgs at{m->q, positions, batch, Hq, Hkv, D, layer, splits, m->part, m->attn, kvv, m->status};
+  if ((e = launch_attn(at, s))) return e;
+  if (!i8) {
+    if ((e = launch_gemv(Epi::Residual, {m->attn, nullptr, 0.f, P.w_o, nullptr, batch, Hq * D, H, m->x}, s)))
+      return e;
+    if ((e = launch_gemv(Epi::SwiGLU, {m->x, P.g_mlp, c.rms_eps, P.w_gu, nullptr, batch, H, F, m->h}, s)))
+      return e;
+    return launch_gemv(Epi::Residual, {m->h, nullptr, 0.f, P.w_d, nullptr, batch, F, H, m->x}, s);
+  }
+  W8Args o{m->attn, nullptr, 0.f, P.q_o, P.s_o, nullptr, batch, Hq * D, H, m->x, nullptr, nullptr, nullptr};
+  if ((e = launch_w8a8(Epi::Residual, o, s))) return e;
+  W8Args gu{m->x, P.g_mlp, c.rms_eps, P.q_gu, P.s_gu, nullptr, batch, H, F, m->h, nullptr, nullptr, nullptr};
+  if ((e = launch_w8a8(Epi::SwiGLU, gu, s))) return e;
+  W8Args dn{m->h, nullptr, 0.f, P.q_d, P.s_d, nullptr, batch, F, H, m->x, nullptr, nullptr, nullptr};
+  return launch_w8a8(Epi::Residual, dn, s);
+}
+
+struct StepIO {
+  int32_t* tokens;
+  int32_t* positions;
+  float* logits;
+  int32_t* next;
+  bool advance;
+};
+
+static cudaError_t enqueue_step(Model* m, int batch, const StepIO& io, const KVView& kvv,
+                                int splits, cudaStream_t s) {
+  const nc_config& c = m->cfg;
+  cudaError_t e = launch_embed(m->embed, io.tokens, batch, c.hidden, c.vocab, m->x, m->status, s);
+  if (e) return e;
+  for (int l = 0; l < c.n_layers; ++l)
+    if ((e = enqueue_block(m, l, batch, io.positions, kvv, splits, s))) return e;
+  LmHeadArgs a{m->x, m->g_final, c.rms_eps, m->head, batch, c.hidden, c.vocab, io.logits, io.next,
+               m->am_part, m->ticket, m->status, io.advance ? io.tokens : nullptr,
+               io.advance ? io.positions : nullptr};
+  return launch_lm_head(a, s);
+}
+
+nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
+                      const int32_t* positions_host, const nc_kv_cache* kv, float* logits,
+                      int32_t* next, int flags, cudaStream_t s) {
+  NC_CHECK(m, NC_ERR_INVALID_ARGUMENT, "model is NULL");
+  NC_CHECK(!m->unhealthy, NC_ERR_UNHEALTHY, "model saw an earlier CUDA failure");
+  NC_CHECK(batch >= 1 && batch <= m->max_batch, NC_ERR_CAPACITY, "batch %d outside [1, %d]",
+           batch, m->max_batch);
+  NC_CHECK(tokens && positions && logits, NC_ERR_INVALID_ARGUMENT, "null device pointer");
+  NC_CHECK((flags & ~(NC_STEP_GRAPH | NC_STEP_ADVANCE)) == 0, NC_ERR_INVALID_ARGUMENT,
+           "unknown flags 0x%x", flags);
+  nc_status st = validate_kv(m, batch, positions_host, kv);
+  if (st) return st;
+  const KVView kvv = kv_view(m, *kv);
+  const int splits = attn_splits(batch, m->cfg.n_kv_heads, kv_capacity(*kv));
+  const StepIO io{tokens, positions, logits, next, (flags & NC_STEP_ADVANCE) != 0};
+  cudaError_t e;
+  if (!(flags & NC_STEP_GRAPH)) {
+    e = enqueue_step(m, batch, io, kvv, splits, s);
+  } else {
+    GraphKey key{batch, tokens, positions, logits, next, kv->k, kv->v, kv->block_table,
+                 kv->paged, kv->batch_capacity, kv->max_ctx, kv->block_size, kv->num_blocks,
+                 kv->max_blocks_per_seq, (int)io.advance, (int)kv->dtype};
+    auto it = m->graphs.find(key);
+    if (it == m->graphs.end()) {
+      // First use: launch once eagerly (sets per-kernel attributes), then capture.
+      e = enqueue_step(m, batch, io, kvv, splits, s);
+      if (!e) e = cudaStreamSynchronize(s);
+      if (e) {
+        m->unhealthy = true;
+        return fail(NC_ERR_CUDA, "decode step launch failed: %s", cudaGetErrorString(e));
+      }
+      cudaGraph_t g = nullptr;
+      cudaGraphExec_t ge = nullptr;
+      // Capture on the model's own stream: the legacy default stream cannot be
+      // captured, and capturing executes nothing.
+      if (!e && !m->cap_stream) e = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking);
+      if (!e) e = cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal);
+      if (!e) {
+        cudaError_t e2 = enqueue_step(m, batch, io, kvv, splits, m->cap_stream);
+        e = cudaStreamEndCapture(m->cap_stream, &g);
+        if (!e) e = e2;
+      }
+      if (!e) e = cudaGraphInstantiate(&ge, g, 0);
+      if (g) cudaGraphDestroy(g);
+      if (e) {
+        m->unhealthy = true;
+        return fail(NC_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+      }
+      it = m->graphs.emplace(key, ge).first;
+      // The eager launch above already performed this step; its KV writes and
+      // logits are identical to a replay, so the replay is skipped.
+      return NC_OK;
+    }
+    e = cudaGraphLaunch(it->second, s);
+  }
+  if (e) {
+    m->unhealthy = true;
+    return fail(NC_ERR_CUDA, "decode step launch failed: %s", cudaGetErrorString(e));
+  }
+  return NC_OK;
+}
+
+nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t* positions,
+                        const int32_t* positions_host, const nc_kv_cache* kv, cudaStream_t s) {
+  NC_CHECK(m, NC_ERR_INVALID_ARGUMENT, "model is NULL");
+  NC_CHECK(!m->unhealthy, NC_ERR_UNHEALTHY, "model saw an earlier CUDA failure");
+  NC_CHECK(layer >= 0 && layer < m->cfg.n_layers, NC_ERR_SHAPE, "layer %d outside [0, %d)", layer,
+           m->cfg.n_layers);
+  NC_CHECK(batch >= 1 && batch <= m->max_batch, NC_ERR_CAPACITY, "batch %d outside [1, %d]",
+           batch, m->max_batch);
+  NC_CHECK(x && positions, NC_ERR_INVALID_ARGUMENT, "null device pointer");
+  nc_status st = validate_kv(m, batch, positions_host, kv);
+  if (st) return st;
+  const KVView kvv = kv_view(m, *kv);
+  const int splits = attn_splits(batch, m->cfg.n_kv_heads, kv_capacity(*kv));
+  cudaError_t e = cudaMemcpyAsync(m->x, x, (size_t)batch * m->cfg.hidden * 4,
+                                  cudaMemcpyDeviceToDevice, s);
+  if (!e) e = enqueue_block(m, layer, batch, positions, kvv, splits, s);
+  if (!e)
+    e = cudaMemcpyAsync(x, m->x, (size_t)batch * m->cfg.hidden * 4, cudaMemcpyDeviceToDevice, s);
+  if (e) {
+    m->unhealthy = true;
+    return fail(NC_ERR_CUDA, "block launch failed: %s", cudaGetErrorString(e));
+  }
+  return NC_OK;
+}
+
+}  // namespace nc

@@ -1,0 +1,62 @@
+// engine.h -- the model object behind nc_model (internal).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "kernels.h"
+
+namespace nc {
+
+struct LayerPacked {
+  uint16_t* w_qkv = nullptr;  // [(Hq + 2 Hkv) D, H] bf16 (NC_BF16)
+  uint16_t* b_qkv = nullptr;  // [(Hq + 2 Hkv) D] or null
+  uint16_t* w_o = nullptr;    // [H, Hq D]
+  uint16_t* w_gu = nullptr;   // [2F, H]: gate rows then up rows
+  uint16_t* w_d = nullptr;    // [H, F]
+  int8_t *q_qkv = nullptr, *q_o = nullptr, *q_gu = nullptr, *q_d = nullptr;  // NC_INT8 rows
+  float *s_qkv = nullptr, *s_o = nullptr, *s_gu = nullptr, *s_d = nullptr;   // per-row scales
+  uint16_t *g_attn = nullptr, *g_mlp = nullptr, *g_q = nullptr, *g_k = nullptr;
+};
+
+using GraphKey = std::tuple<int, const void*, const void*, const void*, const void*, const void*,
+                            const void*, const void*, int, int, int, int, int, int, int, int>;
+
+struct Model {
+  nc_config cfg{};
+  int max_batch = 0, max_ctx = 0;
+  void* weights = nullptr;    // packed weight arena
+  void* workspace = nullptr;  // workspace arena
+  size_t weight_bytes = 0, workspace_bytes = 0;
+  std::vector<LayerPacked> layers;
+  uint16_t *embed = nullptr, *head = nullptr, *g_final = nullptr;
+  float* inv_freq = nullptr;
+  // workspace
+  float *x = nullptr, *qkv = nullptr, *q = nullptr, *attn = nullptr, *part = nullptr, *h = nullptr;
+  unsigned long long* am_part = nullptr;
+  unsigned int* ticket = nullptr;
+  int* status = nullptr;
+  bool unhealthy = false;
+  cudaStream_t cap_stream = nullptr;  // private stream used only for graph capture
+  int* status_host = nullptr;         // pinned host copy of the status word
+  std::map<GraphKey, cudaGraphExec_t> graphs;
+  ~Model();
+};
+
+bool valid_config(const nc_config& c, std::string* why);
+nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch, int max_ctx,
+                       cudaStream_t s, Model** out);
+KVView kv_view(const Model* m, const nc_kv_cache& kv);
+int kv_capacity(const nc_kv_cache& kv);
+nc_status validate_kv(const Model* m, int batch, const int32_t* positions_host,
+                      const nc_kv_cache* kv);
+nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
+                      const int32_t* positions_host, const nc_kv_cache* kv, float* logits,
+                      int32_t* next, int flags, cudaStream_t s);
+nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t* positions,
+                        const int32_t* positions_host, const nc_kv_cache* kv, cudaStream_t s);
+
+}  // namespace nc

@@ -1,0 +1,111 @@
+// kernels.h -- launch interfaces of libnc's kernels (host side, internal).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nc_internal.cuh"
+
+namespace nc {
+
+int num_sms();  // SM count of the current device (cached)
+
+// ------------------------------------------------------------ streaming GEMV
+enum class Epi : int { Store = 0, Residual = 1, SwiGLU = 2 };
+
+struct GemvArgs {
+  const float* x;         // [B, K] activations
+  const uint16_t* gamma;  // [K] RMSNorm gain, or null (no norm)
+  float eps;
+  const uint16_t* W;      // [N, K] bf16; SwiGLU: [2N, K] (gate rows, then up rows)
+  const uint16_t* bias;   // [N] bf16 or null (Store only)
+  int B, K, N;
+  float* y;               // [B, N]; Residual: updated in place
+};
+cudaError_t launch_gemv(Epi epi, const GemvArgs& a, cudaStream_t s);
+
+// LM head: logits = W rmsnorm(x) and the greedy token per sequence.
+struct LmHeadArgs {
+  const float* x;
+  const uint16_t* gamma;
+  float eps;
+  const uint16_t* W;            // [V, K]
+  int B, K, V;
+  float* logits;                // [B, V]
+  int32_t* next;                // [B] or null
+  unsigned long long* part;     // [B, grid] arg-max partial keys (workspace)
+  unsigned int* ticket;         // zero on entry; the last block resets it
+  int* status;                  // device status word
+  int32_t* advance_tokens;      // non-null: tokens[b] = greedy token after the step
+  int32_t* advance_positions;   // non-null: positions[b] += 1 after the step
+};
+int lm_head_grid();
+cudaError_t launch_lm_head(const LmHeadArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------ attention
+struct RopeArgs {
+  const float* qkv;         // [B, (Hq + 2 Hkv) D]
+  const int32_t* positions; // [B]
+  const float* inv_freq;    // [D/2]
+  const uint16_t* g_q;      // [D] or null
+  const uint16_t* g_k;      // [D] or null
+  float eps;
+  int B, Hq, Hkv, D, layer;
+  float* q_out;             // [B, Hq D]
+  KVView kv;
+  int* status;              // device status word (NC_ERR_POSITION on a bad slot)
+};
+cudaError_t launch_rope_qkv(const RopeArgs& a, cudaStream_t s);
+
+struct AttnArgs {
+  const float* q;           // [B, Hq D] rotated
+  const int32_t* positions; // [B]
+  int B, Hq, Hkv, D, layer, splits;
+  float* part;              // [B, Hq, splits, D + 2] (m, l, acc[D])
+  float* out;               // [B, Hq D]
+  KVView kv;
+  int* status;              // device status word (NC_ERR_POSITION on a bad slot)
+};
+int attn_splits(int B, int Hkv, int max_ctx);
+size_t attn_part_floats(int B, int Hq, int D, int splits);
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------ W8A8
+struct W8Args {
+  const float* x;
+  const uint16_t* gamma;
+  float eps;
+  const int8_t* Wq;       // [N, K]
+  const float* w_scale;   // [N]
+  const uint16_t* bias;   // [N] or null
+  int B, K, N;
+  float* y;               // [B, N] (Residual: in place)
+  int8_t* xq_out;         // [B, K] or null
+  float* sx_out;          // [B] or null
+  int32_t* acc_out;       // [B, N] or null
+};
+cudaError_t launch_w8a8(Epi epi, const W8Args& a, cudaStream_t s);
+cudaError_t launch_quantize_weight(const uint16_t* W, int N, int K, int8_t* q, float* scale,
+                                   cudaStream_t s);
+
+// ------------------------------------------------------------ misc
+// x[b] = widen(E[tokens[b]]); a token outside [0, V) reads row 0 and sets *status.
+cudaError_t launch_embed(const uint16_t* E, const int32_t* tokens, int B, int H, int V, float* x,
+                         int* status, cudaStream_t s);
+
+// Raise a kernel's dynamic shared memory limit to the device's opt-in maximum,
+// once per kernel (outside any stream capture on the first call).
+int max_smem_optin();
+// The limit is the opt-in maximum less the kernel's static shared memory.
+template <auto Kern>
+cudaError_t ensure_smem() {
+  static const cudaError_t e = [] {
+    cudaFuncAttributes fa;
+    cudaError_t r = cudaFuncGetAttributes(&fa, Kern);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                max_smem_optin() - (int)fa.sharedSizeBytes);
+  }();
+  return e;
+}
+
+}  // namespace nc

@@ -1,0 +1,173 @@
+// nc_internal.cuh -- helpers shared by libnc's kernels and host code.
+//
+// Nothing here is numerics beyond bf16 widening (exact: a bf16 value is the
+// top half of an fp32 word) and fp32 reductions.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdio>
+#include <string>
+
+#include "../../include/nc.h"
+
+namespace nc {
+
+constexpr int kWarp = 32;
+constexpr int kNumSMs = 152;  // GB300; the host code queries the real count
+
+// ---------------------------------------------------------------- errors
+void set_error(const char* fmt, ...);
+nc_status fail(nc_status s, const char* fmt, ...);
+
+#define NC_CUDA_TRY(expr)                                                              \
+  do {                                                                                 \
+    cudaError_t _e = (expr);                                                           \
+    if (_e != cudaSuccess)                                                             \
+      return ::nc::fail(NC_ERR_CUDA, "%s failed: %s (%s:%d)", #expr, cudaGetErrorString(_e), \
+                        __FILE__, __LINE__);                                            \
+  } while (0)
+
+#define NC_CHECK(cond, status, ...)                      \
+  do {                                                   \
+    if (!(cond)) return ::nc::fail((status), __VA_ARGS__); \
+  } while (0)
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+// Round to nearest even (the hardware conversion).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  unsigned short r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// 16-byte streaming load of data read once (weights): no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// 8 bf16 (one 16-byte chunk) times 8 fp32 from shared memory.
+__device__ __forceinline__ float dot8(const uint4& w, const float* x) {
+  const float4 a = *reinterpret_cast<const float4*>(x);
+  const float4 b = *reinterpret_cast<const float4*>(x + 4);
+  float s = bf16_lo(w.x) * a.x;
+  s = fmaf(bf16_hi(w.x), a.y, s);
+  s = fmaf(bf16_lo(w.y), a.z, s);
+  s = fmaf(bf16_hi(w.y), a.w, s);
+  s = fmaf(bf16_lo(w.z), b.x, s);
+  s = fmaf(bf16_hi(w.z), b.y, s);
+  s = fmaf(bf16_lo(w.w), b.z, s);
+  s = fmaf(bf16_hi(w.w), b.w, s);
+  return s;
+}
+
+// Order-preserving map of a float to uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// Arg-max key: value in the high word, (0xFFFFFFFF - index) in the low word so
+// that equal values resolve to the lowest index under max. NaN -> all ones.
+__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
+  if (v != v) return ~0ull;
+  return (static_cast<unsigned long long>(float_order_key(v)) << 32) |
+         static_cast<unsigned long long>(0xFFFFFFFFu - idx);
+}
+
+// ---------------------------------------------------------------- KV addressing
+struct KVView {
+  void* k;  // fp32 or bf16 elements (bf16 != 0)
+  void* v;
+  const int32_t* block_table;  // paged only
+  int paged;
+  int bf16;
+  int batch_capacity;
+  int max_ctx;
+  int block_size;
+  int num_blocks;
+  int max_blocks_per_seq;
+  int n_kv_heads;
+  int head_dim;
+  __device__ __forceinline__ int capacity() const {
+    return paged ? max_blocks_per_seq * block_size : max_ctx;
+  }
+  // True when slot t of sequence b exists: t inside the capacity and, when
+  // paged, its block-table entry inside the pool. The host validates the same
+  // facts from its copies; this guards against device copies that disagree.
+  __device__ __forceinline__ bool slot_ok(int b, int t) const {
+    if (t < 0 || t >= capacity()) return false;
+    if (!paged) return true;
+    const int blk = block_table[(size_t)b * max_blocks_per_seq + t / block_size];
+    return blk >= 0 && blk < num_blocks;
+  }
+  // element offset of (layer, seq b, kv head g, position t)
+  __device__ __forceinline__ size_t offset(int layer, int b, int g, int t) const {
+    if (!paged) {
+      return ((((size_t)layer * batch_capacity + b) * n_kv_heads + g) * max_ctx + t) *
+             (size_t)head_dim;
+    }
+    const int blk = block_table[(size_t)b * max_blocks_per_seq + t / block_size];
+    return ((((size_t)layer * num_blocks + blk) * n_kv_heads + g) * block_size +
+            t % block_size) *
+           (size_t)head_dim;
+  }
+};
+
+// Eight consecutive cache elements (16-byte aligned start) widened to fp32.
+template <bool KV16>
+__device__ __forceinline__ void kv_load8(const void* base, size_t off, float (&f)[8]) {
+  if constexpr (KV16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off);
+    f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+    f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z); f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+    const float4 a = p[0], b = p[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+}
+// Two consecutive cache elements (8-byte aligned for fp32, 4 for bf16).
+template <bool KV16>
+__device__ __forceinline__ float2 kv_load2(const void* base, size_t off) {
+  if constexpr (KV16) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(base) + off);
+    return make_float2(bf16_lo(w), bf16_hi(w));
+  } else {
+    return *reinterpret_cast<const float2*>(static_cast<const float*>(base) + off);
+  }
+}
+// Store one cache element (bf16: round to nearest even).
+template <bool KV16>
+__device__ __forceinline__ void kv_store(void* base, size_t off, float v) {
+  if constexpr (KV16)
+    static_cast<uint16_t*>(base)[off] = f32_to_bf16(v);
+  else
+    static_cast<float*>(base)[off] = v;
+}
+
+}  // namespace nc
