@@ -207,6 +207,29 @@ nc_status nc_attn_decode(const nc_model* m, int layer, int B, const float* q,
                          const int32_t* positions_dev, const int32_t* positions_host,
                          const nc_kv_cache* kv, float* out, void* stream);
 
+/* The same attention as nc_attn_decode, for callers that cannot allocate
+ * device memory (the pages have no counterpart of this entry point). Such
+ * callers include code running while a stream of the process is in
+ * global-mode graph capture, where cudaMalloc is not permitted; code whose
+ * device memory is owned by a framework allocator that forbids raw
+ * cudaMalloc; and latency-critical loops that cannot afford cudaMalloc's
+ * implicit synchronisation. It needs no model and allocates nothing: the
+ * split partials live in a static device array of 1,048,576 floats (4 MiB)
+ * that every GPU loading libnc holds until the process exits. A request whose
+ * partials, batch * n_q_heads * splits * (head_dim + 2) floats, exceed it
+ * returns NC_ERR_CAPACITY before anything is enqueued. The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture. All calls
+ * share the array: calls that overlap on the GPU (on different streams, or
+ * from different threads) race and must be serialised by the caller. Every
+ * scratch element a call reads is written earlier in the same call, so what
+ * the previous call left there does not matter. n_layers is the cache's
+ * layer count (bounds `layer`); other arguments as for nc_attn_decode. */
+nc_status nc_attn_decode_static(int n_q_heads, int n_kv_heads, int head_dim, int n_layers,
+                                int layer, int B, const float* q, const int32_t* positions_dev,
+                                const int32_t* positions_host, const nc_kv_cache* kv, float* out,
+                                void* stream);
+
 /* logits[b, v] = sum_k W[v, k] * xn[b, k] with xn = rmsnorm(x[b]) * gamma,
  * and next[b] = argmax_v logits[b, v], lowest index on ties, -1 on NaN
  * (Tang section 2.2: arg-max is a monoid on (value, index)). next nullable.

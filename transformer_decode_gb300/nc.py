@@ -31,6 +31,7 @@ EXPORTS = [
     "nc_model_destroy", "nc_model_memory", "nc_decode_step", "nc_block_forward",
     "nc_get_device_status", "nc_rmsnorm_gemv", "nc_gemv_residual", "nc_swiglu_gemv",
     "nc_rope_qkv", "nc_attn_decode", "nc_lm_head_argmax", "nc_quantize_weight", "nc_w8a8_gemv",
+    "nc_attn_decode_static",
 ]
 
 
@@ -112,6 +113,7 @@ def _declare(L):
     L.nc_lm_head_argmax.argtypes = [vp, vp, vp, f, vp, i, i, i, vp, vp, vp]
     L.nc_quantize_weight.argtypes = [vp, i, i, vp, vp, vp]
     L.nc_w8a8_gemv.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
+    L.nc_attn_decode_static.argtypes = [i, i, i, i, i, i, vp, vp, vp, C.POINTER(KVStruct), vp, vp]
     for n in EXPORTS:
         if n not in ("nc_status_string", "nc_last_error_message"):
             getattr(L, n).restype = C.c_int
@@ -192,6 +194,20 @@ def w8a8_gemv(x, gamma, eps, Wq, w_scale, bias, y, xq_out=None, sx_out=None, acc
                                _ptr(y, torch.float32, "y", B * N),
                                _ptr(xq_out, torch.int8, "xq_out"), _ptr(sx_out, torch.float32, "sx_out"),
                                _ptr(acc_out, torch.int32, "acc_out"), _stream(stream)))
+
+
+def attn_decode_static(shape, layer, q, positions, positions_host, kv, out, stream=None):
+    """nc_attn_decode_static: split-K decode attention that allocates nothing
+    (its scratch is a static device array). For callers that cannot allocate
+    device memory; see include/nc.h for the size limit and the set-up rule."""
+    B = q.shape[0]
+    ph = _host_i32(positions_host)
+    s = kv.struct()
+    _check(load().nc_attn_decode_static(
+        shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.n_layers, layer, B,
+        _ptr(q, torch.float32, "q", B * shape.q_dim), _ptr(positions, torch.int32, "positions", B),
+        ph.ctypes.data_as(C.c_void_p), C.byref(s),
+        _ptr(out, torch.float32, "out", B * shape.q_dim), _stream(stream)))
 
 
 # ------------------------------------------------------------------ KV cache
