@@ -142,6 +142,12 @@ nc_status nc_model_memory(const nc_model* m, size_t* weight_bytes, size_t* works
                              and tokens_dev[b] = the greedy token, so the next
                              call continues greedy decoding with no host work
                              (the caller then passes positions_host + 1) */
+#define NC_STEP_STAGED 4  /* use the per-stage kernels even where the persistent
+                             decode kernel applies. By default a step with bf16
+                             weights, batch <= 4 and a cache of at most 2048
+                             positions per sequence runs as one persistent,
+                             cooperative kernel (one launch, no graph); other
+                             steps run the per-stage kernels. */
 
 /* One decode step for `batch` sequences (nanoinfer "Model architecture" and
  * "KV cache"; the one-call-per-token step of nanocompile's phase 7): token
@@ -165,6 +171,19 @@ nc_status nc_block_forward(nc_model* m, int layer, int batch, float* x_dev,
  * NaN in the logits or an expired bounded wait). Synchronises `stream`,
  * reads the word and clears it. */
 nc_status nc_get_device_status(nc_model* m, void* stream, int* code);
+
+/* Phase profile of the persistent decode kernel (a per-phase step profile in
+ * the spirit of nanocompile's per-primitive profile of one step). While
+ * enabled, every persistent step records %globaltimer (ns) in CTA 0 at the
+ * start of each phase and when the phase's input had arrived; phases are, per
+ * layer, QKV, attention, o-proj, gate|up, down, then the LM head.
+ * nc_read_phase_profile synchronises `stream` and copies the last step's
+ * record, 2 * (5 * n_layers + 1) + 2 values: [2p] start of phase p,
+ * [2p + 1] its input in, then the kernel start and the end of the last CTA.
+ * *n receives the count. */
+nc_status nc_profile_phases(nc_model* m, int enable);
+nc_status nc_read_phase_profile(nc_model* m, void* stream, unsigned long long* out_host,
+                                int capacity, int* n);
 
 /* ---------------- per-stage entry points (no model needed unless named) ---- */
 

@@ -80,7 +80,8 @@ def test_block_forward_0p5b_past16(paged, kv_bf16):
 
 # ------------------------------------------------------------------ greedy decode
 def _greedy_compare(shape, wd, wc, prompt, steps, batch=1, past=None, paged=False, w8a8=False,
-                    use_graph=True, gate=REL_L2_GATE, kv_bf16=False, derived_gate=False):
+                    use_graph=True, gate=REL_L2_GATE, kv_bf16=False, derived_gate=False,
+                    staged=False):
     """Teacher-forced greedy decode: both sides consume the oracle's token.
     Returns the worst logit rel-L2 seen.
 
@@ -115,7 +116,7 @@ def _greedy_compare(shape, wd, wc, prompt, steps, batch=1, past=None, paged=Fals
     for i in range(n_total):
         tok_d.copy_(torch.from_numpy(tok))
         pos_d.copy_(torch.from_numpy(pos))
-        model.decode_step(tok_d, pos_d, pos, kv, logits, nxt, use_graph=use_graph)
+        model.decode_step(tok_d, pos_d, pos, kv, logits, nxt, use_graph=use_graph, staged=staged)
         ol, on = om.decode_step(okv, tok, pos)
         if derived_gate:
             ol64, _ = om.decode_step(okv64, tok, pos, "f64")
@@ -139,11 +140,22 @@ def _greedy_compare(shape, wd, wc, prompt, steps, batch=1, past=None, paged=Fals
 
 
 @pytest.mark.parametrize("shape", [synth.TINY, synth.TINY_QKNORM])
-@pytest.mark.parametrize("use_graph", [True, False])
-def test_decode_tiny(shape, use_graph):
+@pytest.mark.parametrize("path", ["persistent", "staged-graph", "staged-eager"])
+def test_decode_tiny(shape, path):
+    """Both step paths: the persistent kernel (default at these sizes) and the
+    per-stage kernels, replayed from a graph or launched directly."""
     wd, wc = weights_both(shape)
     prompt = [synth.token_ids(5, shape.vocab, stream=11).tolist()]
-    _greedy_compare(shape, wd, wc, prompt, steps=20, use_graph=use_graph)
+    _greedy_compare(shape, wd, wc, prompt, steps=20, use_graph=path != "staged-eager",
+                    staged=path != "persistent")
+
+
+@pytest.mark.parametrize("batch", [2, 4])
+def test_decode_tiny_persistent_batch(batch):
+    """The persistent kernel at batch 2 and 4, mixed positions."""
+    shape = synth.TINY
+    wd, wc = weights_both(shape)
+    _greedy_compare(shape, wd, wc, None, steps=10, batch=batch, past=[0, 7, 19, 3][:batch])
 
 
 def test_decode_tiny_batch_paged():
@@ -152,14 +164,15 @@ def test_decode_tiny_batch_paged():
     _greedy_compare(shape, wd, wc, None, steps=12, batch=5, past=[0, 3, 16, 31, 70], paged=True)
 
 
-def test_decode_0p5b_prompt32_greedy64():
+@pytest.mark.parametrize("staged", [False, True])
+def test_decode_0p5b_prompt32_greedy64(staged):
     """The full 24-layer 0.5B-shaped model: a 32-token prompt then 64 greedy
-    tokens, contiguous cache, CUDA graph replay."""
+    tokens, contiguous cache; the persistent kernel and the per-stage path."""
     shape = synth.QWEN2_0P5B
     wd, wc = weights_both(shape)
     prompt = [synth.token_ids(32, shape.vocab).tolist()]
-    worst = _greedy_compare(shape, wd, wc, prompt, steps=64)
-    print(f"0.5B greedy: worst logit rel-L2 {worst:.3e}")
+    worst = _greedy_compare(shape, wd, wc, prompt, steps=64, staged=staged)
+    print(f"0.5B greedy (staged {staged}): worst logit rel-L2 {worst:.3e}")
 
 
 def test_decode_0p5b_w8a8_past512():

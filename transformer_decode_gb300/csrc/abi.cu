@@ -122,6 +122,29 @@ nc_status nc_get_device_status(nc_model* m, void* stream, int* code) {
   return NC_OK;
 }
 
+nc_status nc_profile_phases(nc_model* m, int enable) {
+  NC_CHECK(m, NC_ERR_INVALID_ARGUMENT, "model is NULL");
+  M(m)->prof_on = enable != 0;
+  return NC_OK;
+}
+
+nc_status nc_read_phase_profile(nc_model* m, void* stream, unsigned long long* out_host,
+                                int capacity, int* n) {
+  NC_CHECK(m && out_host && n, NC_ERR_INVALID_ARGUMENT, "null argument");
+  Model* mm = M(m);
+  const int count = 2 * (5 * mm->cfg.n_layers + 1) + 2;
+  NC_CHECK(capacity >= count, NC_ERR_CAPACITY, "the profile holds %d values", count);
+  cudaError_t e = cudaStreamSynchronize(S(stream));
+  if (!e) e = cudaMemcpy(out_host, mm->prof, sizeof(unsigned long long) * count,
+                         cudaMemcpyDeviceToHost);
+  if (e) {
+    mm->unhealthy = true;
+    return fail(NC_ERR_CUDA, "reading the phase profile failed: %s", cudaGetErrorString(e));
+  }
+  *n = count;
+  return NC_OK;
+}
+
 nc_status nc_rmsnorm_gemv(const float* x, const void* gamma, float eps, const void* W,
                           const void* bias, int B, int K, int N, float* y, void* stream) {
   NC_CHECK(x && W && y, NC_ERR_INVALID_ARGUMENT, "null pointer");

@@ -161,6 +161,15 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     m->am_part = W.take<unsigned long long>((size_t)max_batch * lm_head_grid());
     m->ticket = W.take<unsigned int>(1);
     m->status = W.take<int>(1);
+    const size_t pb = max_batch < kPMaxBatch ? max_batch : kPMaxBatch;
+    m->xw = W.take<uint64_t>(pb * H);
+    m->qkvw = W.take<uint64_t>(pb * nqkv);
+    m->aw = W.take<uint64_t>(pb * qd);
+    m->hw = W.take<uint64_t>(pb * F);
+    m->pticket = W.take<unsigned int>(1);
+    m->seq = W.take<unsigned int>(1);
+    m->prof = W.take<unsigned long long>(2 * (5 * (size_t)c.n_layers + 1) + 2);
+    m->players = A.take<PLayer>(c.n_layers);
   };
   Arena A0, W0;
   layout(A0, W0);
@@ -229,7 +238,18 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
   std::vector<float> inv(D / 2);
   for (int i = 0; i < D / 2; ++i) inv[i] = (float)(1.0 / pow((double)c.rope_theta, (2.0 * i) / D));
   if (!e) e = cudaMemcpyAsync(m->inv_freq, inv.data(), inv.size() * 4, cudaMemcpyHostToDevice, s);
+  // per-layer pointers for the persistent kernel
+  std::vector<PLayer> pl(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerPacked& P = m->layers[l];
+    pl[l] = PLayer{P.w_qkv, P.b_qkv, P.w_o, P.w_gu, P.w_d, P.g_attn, P.g_mlp, P.g_q, P.g_k};
+  }
+  if (!e) e = cudaMemcpyAsync(m->players, pl.data(), pl.size() * sizeof(PLayer),
+                              cudaMemcpyHostToDevice, s);
   if (!e) e = cudaMemsetAsync(m->workspace, 0, ws, s);
+  // The step sequence starts at 1: epoch 0 would match the zeroed hand-over words.
+  const unsigned one = 1u;
+  if (!e) e = cudaMemcpyAsync(m->seq, &one, sizeof one, cudaMemcpyHostToDevice, s);
   if (!e) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     delete m;
@@ -237,6 +257,57 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
   }
   *out = m;
   return NC_OK;
+}
+
+// The persistent kernel serves bf16 weights, small batches and caches short
+// enough for one CTA per (sequence, kv head) to scan.
+static bool use_persistent(const Model* m, int batch, const nc_kv_cache& kv, int flags) {
+  const nc_config& c = m->cfg;
+  return !(flags & NC_STEP_STAGED) && c.wtype == NC_BF16 && batch <= kPMaxBatch &&
+         kv_capacity(kv) <= kPMaxCtx &&
+         persistent_supported(c.hidden, c.n_q_heads * c.head_dim, c.ffn, c.head_dim,
+                              c.n_q_heads / c.n_kv_heads, batch);
+}
+
+static cudaError_t enqueue_persistent(Model* m, int batch, int32_t* tokens, int32_t* positions,
+                                      float* logits, int32_t* next, bool advance,
+                                      const KVView& kvv, cudaStream_t s) {
+  const nc_config& c = m->cfg;
+  PersistArgs a{};
+  a.layers = m->players;
+  a.L = c.n_layers;
+  a.embed = m->embed;
+  a.head = m->head;
+  a.g_final = m->g_final;
+  a.inv_freq = m->inv_freq;
+  a.H = c.hidden;
+  a.Hq = c.n_q_heads;
+  a.Hkv = c.n_kv_heads;
+  a.D = c.head_dim;
+  a.F = c.ffn;
+  a.V = c.vocab;
+  a.nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  a.eps = c.rms_eps;
+  a.B = batch;
+  a.tokens = tokens;
+  a.positions = positions;
+  a.logits = logits;
+  a.next = next;
+  a.advance = advance ? 1 : 0;
+  a.kv = kvv;
+  a.xw = m->xw;
+  a.qkvw = m->qkvw;
+  a.aw = m->aw;
+  a.hw = m->hw;
+  a.am_part = m->am_part;
+  a.ticket = m->pticket;
+  a.seq = m->seq;
+  a.status = m->status;
+  a.timeout_ns = 200ull * 1000 * 1000;  // 200 ms; a step takes well under 10 ms
+  a.grid = num_sms();
+  a.prof = m->prof_on ? m->prof : nullptr;
+  a.slot_bytes = kPSlotBytes;
+  return launch_persistent(a, s);
 }
 
 // ------------------------------------------------------------------ step
@@ -362,7 +433,8 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
   NC_CHECK(batch >= 1 && batch <= m->max_batch, NC_ERR_CAPACITY, "batch %d outside [1, %d]",
            batch, m->max_batch);
   NC_CHECK(tokens && positions && logits, NC_ERR_INVALID_ARGUMENT, "null device pointer");
-  NC_CHECK((flags & ~(NC_STEP_GRAPH | NC_STEP_ADVANCE)) == 0, NC_ERR_INVALID_ARGUMENT,
+  NC_CHECK((flags & ~(NC_STEP_GRAPH | NC_STEP_ADVANCE | NC_STEP_STAGED)) == 0,
+           NC_ERR_INVALID_ARGUMENT,
            "unknown flags 0x%x", flags);
   nc_status st = validate_kv(m, batch, positions_host, kv);
   if (st) return st;
@@ -370,7 +442,9 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
   const int splits = attn_splits(batch, m->cfg.n_kv_heads, kv_capacity(*kv));
   const StepIO io{tokens, positions, logits, next, (flags & NC_STEP_ADVANCE) != 0};
   cudaError_t e;
-  if (!(flags & NC_STEP_GRAPH)) {
+  if (use_persistent(m, batch, *kv, flags)) {
+    e = enqueue_persistent(m, batch, tokens, positions, logits, next, io.advance, kvv, s);
+  } else if (!(flags & NC_STEP_GRAPH)) {
     e = enqueue_step(m, batch, io, kvv, splits, s);
   } else {
     GraphKey key{batch, tokens, positions, logits, next, kv->k, kv->v, kv->block_table,

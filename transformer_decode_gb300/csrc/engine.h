@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "kernels.h"
+#include "persistent.h"
 
 namespace nc {
 
@@ -39,6 +40,13 @@ struct Model {
   unsigned long long* am_part = nullptr;
   unsigned int* ticket = nullptr;
   int* status = nullptr;
+  // persistent decode kernel: epoch-tagged hand-over words, its ticket, the
+  // step sequence number and the device copy of the per-layer pointers
+  uint64_t *xw = nullptr, *qkvw = nullptr, *aw = nullptr, *hw = nullptr;
+  unsigned int *pticket = nullptr, *seq = nullptr;
+  PLayer* players = nullptr;
+  unsigned long long* prof = nullptr;  // phase profile [2 * (5L + 1) + 2]
+  bool prof_on = false;
   bool unhealthy = false;
   cudaStream_t cap_stream = nullptr;  // private stream used only for graph capture
   int* status_host = nullptr;         // pinned host copy of the status word

@@ -1,0 +1,61 @@
+// persistent.h -- launch interface of the persistent decode kernel (internal).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nc_internal.cuh"
+
+namespace nc {
+
+constexpr int kMaxSlots = 8;           // weight ring slots (shared memory)
+constexpr int kPMaxBatch = 4;          // sequences per persistent step
+constexpr int kPSlotBytes = 32 * 1024; // bytes per ring slot
+constexpr int kPMaxCtx = 2048;         // cache capacity up to which it is chosen
+constexpr int kPMaxRows = 128;         // rows of H one CTA may own (H <= 128 * grid)
+
+// Per-layer packed weights as the persistent kernel reads them.
+struct PLayer {
+  const uint16_t *w_qkv, *b_qkv, *w_o, *w_gu, *w_d, *g_attn, *g_mlp, *g_q, *g_k;
+};
+
+struct PersistArgs {
+  const PLayer* layers;  // device array [L]
+  int L;
+  const uint16_t* embed;
+  const uint16_t* head;
+  const uint16_t* g_final;
+  const float* inv_freq;
+  int H, Hq, Hkv, D, F, V, nqkv;
+  float eps;
+  int B;
+  int32_t* tokens;
+  int32_t* positions;
+  float* logits;
+  int32_t* next;
+  int advance;
+  KVView kv;
+  // epoch-tagged hand-over words (value in the low half, epoch in the high)
+  uint64_t* xw;    // [kPMaxBatch][H] residual stream
+  uint64_t* qkvw;  // [kPMaxBatch][nqkv]
+  uint64_t* aw;    // [kPMaxBatch][Hq D] attention output
+  uint64_t* hw;    // [kPMaxBatch][F] SiLU(gate) * up
+  unsigned long long* am_part;  // [B][grid] arg-max partial keys
+  unsigned int* ticket;         // zero between steps
+  unsigned int* seq;            // step sequence number (starts at 1)
+  int* status;
+  unsigned long long timeout_ns;  // bound of every wait
+  int grid;                       // CTAs (one per SM)
+  // Optional phase profile (null: off): CTA 0 records %globaltimer at the
+  // start of every phase (2*ph) and when its input is in (2*ph + 1); then the
+  // kernel start (2*nph) and the end of the last CTA (2*nph + 1).
+  unsigned long long* prof;
+  // shared-memory plan (filled by launch_persistent)
+  int slot_bytes, nslots, ring_offset, xs_offset, attn_offset;
+};
+
+// True when the persistent kernel fits this shape (shared memory, batch,
+// head_dim, GQA group).
+bool persistent_supported(int H, int qd, int F, int D, int G, int B);
+cudaError_t launch_persistent(PersistArgs a, cudaStream_t s);
+
+}  // namespace nc

@@ -23,7 +23,7 @@ STATUS = ["NC_OK", "NC_ERR_INVALID_ARGUMENT", "NC_ERR_SHAPE", "NC_ERR_DTYPE", "N
           "NC_ERR_POSITION", "NC_ERR_CUDA", "NC_ERR_TIMEOUT", "NC_ERR_UNHEALTHY",
           "NC_ERR_UNSUPPORTED"]
 NC_BF16, NC_INT8 = 0, 1
-NC_STEP_GRAPH, NC_STEP_ADVANCE = 1, 2
+NC_STEP_GRAPH, NC_STEP_ADVANCE, NC_STEP_STAGED = 1, 2, 4
 NC_KV_F32, NC_KV_BF16 = 0, 1
 
 EXPORTS = [
@@ -31,7 +31,7 @@ EXPORTS = [
     "nc_model_destroy", "nc_model_memory", "nc_decode_step", "nc_block_forward",
     "nc_get_device_status", "nc_rmsnorm_gemv", "nc_gemv_residual", "nc_swiglu_gemv",
     "nc_rope_qkv", "nc_attn_decode", "nc_lm_head_argmax", "nc_quantize_weight", "nc_w8a8_gemv",
-    "nc_attn_decode_static",
+    "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile",
 ]
 
 
@@ -114,6 +114,8 @@ def _declare(L):
     L.nc_quantize_weight.argtypes = [vp, i, i, vp, vp, vp]
     L.nc_w8a8_gemv.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
     L.nc_attn_decode_static.argtypes = [i, i, i, i, i, i, vp, vp, vp, C.POINTER(KVStruct), vp, vp]
+    L.nc_profile_phases.argtypes = [vp, i]
+    L.nc_read_phase_profile.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), i, C.POINTER(i)]
     for n in EXPORTS:
         if n not in ("nc_status_string", "nc_last_error_message"):
             getattr(L, n).restype = C.c_int
@@ -345,13 +347,15 @@ class Model:
         return wb.value, ws.value
 
     def decode_step(self, tokens, positions, positions_host, kv, logits, next_tokens=None,
-                    use_graph=True, advance=False, stream=None):
+                    use_graph=True, advance=False, staged=False, stream=None):
         """One decode step (nc_decode_step). advance=True: the device then sets
-        tokens = greedy token and positions += 1 for the next call."""
+        tokens = greedy token and positions += 1 for the next call.
+        staged=True forces the per-stage kernels instead of the persistent one."""
         B = tokens.numel()
         ph = _host_i32(positions_host)
         s = kv.struct()
-        flags = (NC_STEP_GRAPH if use_graph else 0) | (NC_STEP_ADVANCE if advance else 0)
+        flags = ((NC_STEP_GRAPH if use_graph else 0) | (NC_STEP_ADVANCE if advance else 0)
+                 | (NC_STEP_STAGED if staged else 0))
         _check(load().nc_decode_step(self.handle, B, _ptr(tokens, torch.int32, "tokens"),
                                      _ptr(positions, torch.int32, "positions", B),
                                      ph.ctypes.data_as(C.c_void_p), C.byref(s),
@@ -394,6 +398,22 @@ class Model:
                                         _ptr(logits, torch.float32, "logits", B * V),
                                         _ptr(next_tokens, torch.int32, "next_tokens"),
                                         _stream(stream)))
+
+    def profile_phases(self, enable=True):
+        _check(load().nc_profile_phases(self.handle, int(enable)))
+
+    def read_phase_profile(self, stream=None):
+        """Last persistent step's phase timestamps (ns): a dict with 'start'
+        [5L+1], 'input' [5L+1] (input arrived), 'kernel_start', 'kernel_end'."""
+        L = self.shape.n_layers
+        cap = 2 * (5 * L + 1) + 2
+        buf = (C.c_ulonglong * cap)()
+        n = C.c_int()
+        _check(load().nc_read_phase_profile(self.handle, _stream(stream), buf, cap, C.byref(n)))
+        v = list(buf)
+        nph = 5 * L + 1
+        return {"start": v[0:2 * nph:2], "input": v[1:2 * nph:2], "kernel_start": v[2 * nph],
+                "kernel_end": v[2 * nph + 1]}
 
     def device_status(self, stream=None):
         code = C.c_int()
