@@ -174,13 +174,15 @@ nc_status nc_get_device_status(nc_model* m, void* stream, int* code);
 
 /* Phase profile of the persistent decode kernel (a per-phase step profile in
  * the spirit of nanocompile's per-primitive profile of one step). While
- * enabled, every persistent step records %globaltimer (ns) in CTA 0 at the
+ * enabled, every persistent step records %globaltimer (ns) in each CTA at the
  * start of each phase and when the phase's input had arrived; phases are, per
  * layer, QKV, attention, o-proj, gate|up, down, then the LM head.
  * nc_read_phase_profile synchronises `stream` and copies the last step's
- * record, 2 * (5 * n_layers + 1) + 2 values: [2p] start of phase p,
- * [2p + 1] its input in, then the kernel start and the end of the last CTA.
- * *n receives the count. */
+ * record: for each of the n_sm CTAs (one per SM) 2 * P + 2 values, P =
+ * 5 * n_layers + 1: [2p] start of phase p, [2p + 1] its input in, then the
+ * CTA's start and end (the CTA that finishes the step: the step's end).
+ * *n receives the count n_sm * (2 * P + 2); a smaller capacity returns
+ * NC_ERR_CAPACITY. */
 nc_status nc_profile_phases(nc_model* m, int enable);
 nc_status nc_read_phase_profile(nc_model* m, void* stream, unsigned long long* out_host,
                                 int capacity, int* n);

@@ -168,7 +168,7 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     m->hw = W.take<uint64_t>(pb * F);
     m->pticket = W.take<unsigned int>(1);
     m->seq = W.take<unsigned int>(1);
-    m->prof = W.take<unsigned long long>(2 * (5 * (size_t)c.n_layers + 1) + 2);
+    m->prof = W.take<unsigned long long>((size_t)num_sms() * (2 * (5 * (size_t)c.n_layers + 1) + 2));
     m->players = A.take<PLayer>(c.n_layers);
   };
   Arena A0, W0;
@@ -306,7 +306,6 @@ static cudaError_t enqueue_persistent(Model* m, int batch, int32_t* tokens, int3
   a.timeout_ns = 200ull * 1000 * 1000;  // 200 ms; a step takes well under 10 ms
   a.grid = num_sms();
   a.prof = m->prof_on ? m->prof : nullptr;
-  a.slot_bytes = kPSlotBytes;
   return launch_persistent(a, s);
 }
 

@@ -40,6 +40,7 @@ constexpr int kPThreads = 384;
 constexpr int kPConsumerWarps = kPThreads / kWarp - 1;
 constexpr int kPConsumerThreads = kPConsumerWarps * kWarp;
 constexpr int kPhasesPerLayer = 5;
+constexpr int kUnitsPerWarp = 4;  // output units (rows, gate|up pairs) a warp takes per tile
 enum PhaseKind : int { kQKV = 0, kATTN = 1, kOPROJ = 2, kGU = 3, kDOWN = 4, kHEAD = 5 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -102,7 +103,8 @@ struct PShared {
   float red[kPConsumerWarps][kPMaxBatch];
   unsigned long long best[kPConsumerWarps][kPMaxBatch];
   float xold[kPMaxBatch][kPMaxRows];  // residual rows the o-proj/down epilogue adds to
-  float kred[kPConsumerWarps][2][kPMaxBatch];  // k-segment partial sums of a tile
+  float bias[kPMaxRows];              // QKV bias of this CTA's rows
+  float kred[2][kUnitsPerWarp * kPConsumerWarps][2 * kPMaxBatch];  // k-segment partials, 2 buffers
   bool last;
 };
 
@@ -135,7 +137,7 @@ __device__ __forceinline__ float ll_get(const uint64_t* p, uint32_t epoch, Spin&
 
 // Read `count` words p[0], p[stride], ... (count <= kLLBatch) with all loads
 // in flight at once, then re-poll only the words whose epoch is stale.
-constexpr int kLLBatch = 8;
+constexpr int kLLBatch = 16;
 __device__ __forceinline__ void ll_get_batch(const uint64_t* p, int stride, int count,
                                              uint32_t epoch, float* out, Spin& sp) {
   uint64_t w[kLLBatch];
@@ -159,6 +161,36 @@ __device__ __forceinline__ void ll_get_batch(const uint64_t* p, int stride, int 
 
 __device__ __forceinline__ uint32_t epoch_of(uint32_t seq, int phase) {
   return ((seq & 0xFFFFFFu) << 8) | static_cast<uint32_t>(phase);
+}
+
+// Position in the slot ring: tiles passed, the slot, and the parity of the
+// slot's current fill. Producer and consumers walk the same sequence.
+struct RingPos {
+  uint32_t n = 0;
+  int s = 0;
+  uint32_t par = 0;
+  __device__ __forceinline__ void next(int nslots) {
+    ++n;
+    if (++s == nslots) {
+      s = 0;
+      par ^= 1u;
+    }
+  }
+};
+
+// Bounded wait for phase `par` of an mbarrier; false once the CTA gave up.
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t par, Spin& sp) {
+  int k = 0;
+  while (!mbar_try_wait(bar, par))
+    if ((++k & 15) == 0 && sp.expired()) return false;
+  return true;
+}
+
+
+// CTAs that run attention items (item i on CTA i) and hold no o-proj rows.
+__host__ __device__ __forceinline__ int attn_ctas(const PersistArgs& a, int grid) {
+  const int items = a.B * a.Hkv;
+  return items < grid / 2 ? items : 0;
 }
 
 // Rows of phase `ph` given to CTA `cta` and the tile shape used to stream them.
@@ -188,33 +220,48 @@ __device__ __forceinline__ Rows phase_rows(const PersistArgs& a, int ph, int cta
       default: return r;  // attention streams no weights
     }
   }
+  if (ph < kPhasesPerLayer * a.L && ph % kPhasesPerLayer == kOPROJ) {
+    // the CTAs that ran the attention items come out of it last: the o-proj
+    // rows go to the others, which are idle meanwhile
+    const int na = attn_ctas(a, grid);
+    if (cta < na) {
+      r.r0 = r.r1 = 0;
+      return r;
+    }
+    cta -= na;
+    grid -= na;
+  }
   r.r0 = (int)(((long long)cta * N) / grid);
   r.r1 = (int)(((long long)(cta + 1) * N) / grid);
   const int row_bytes = r.K * 2 * (r.m1 ? 2 : 1);
-  r.R = slot_bytes / row_bytes;
-  if (r.R > kPConsumerWarps) r.R = kPConsumerWarps;  // one unit per consumer warp
-  if (r.R < 1) r.R = 1;
+  int rmax = slot_bytes / row_bytes;
+  if (rmax > kUnitsPerWarp * kPConsumerWarps) rmax = kUnitsPerWarp * kPConsumerWarps;
+  if (rmax < 1) rmax = 1;
+  // tiles of (nearly) equal size: the fewest tiles that fit, rows spread evenly
+  const int nr = r.r1 - r.r0;
+  const int nt = nr > 0 ? (nr + rmax - 1) / rmax : 1;
+  r.R = nr > 0 ? (nr + nt - 1) / nt : 1;
   return r;
 }
 
 // ------------------------------------------------------------------ producer
 template <bool KV16>
 __device__ bool produce_kv(const PersistArgs& a, PShared& S, char* ring, int slot_bytes,
-                           int nslots, int layer, int b, int g, int npos, uint32_t& iter,
+                           int nslots, int layer, int b, int g, int npos, RingPos& rp,
                            Spin& sp);
 
 template <bool KV16>
 __device__ void producer(const PersistArgs& a, PShared& S, char* ring, int slot_bytes, int nslots,
                          Spin& sp) {
   const int nph = kPhasesPerLayer * a.L + 1;
-  uint32_t iter = 0;
+  RingPos rp;
   for (int ph = 0; ph < nph; ++ph) {
     if (ph < kPhasesPerLayer * a.L && ph % kPhasesPerLayer == kATTN) {
       for (int it = blockIdx.x; it < a.B * a.Hkv; it += gridDim.x) {
         const int b = it / a.Hkv, g = it % a.Hkv;
         const int npos = a.kv.slot_ok(b, S.pos[b]) ? S.pos[b] : 0;
         if (!produce_kv<KV16>(a, S, ring, slot_bytes, nslots, ph / kPhasesPerLayer, b, g, npos,
-                              iter, sp))
+                              rp, sp))
           return;
       }
       continue;
@@ -222,20 +269,16 @@ __device__ void producer(const PersistArgs& a, PShared& S, char* ring, int slot_
     const Rows r = phase_rows(a, ph, blockIdx.x, gridDim.x, slot_bytes);
     for (int row = r.r0; row < r.r1; row += r.R) {
       const int n = min(r.R, r.r1 - row);
-      const int s = iter % nslots;
-      if (iter >= (uint32_t)nslots) {
-        const uint32_t par = ((iter / nslots) - 1) & 1;
-        int k = 0;
-        while (!mbar_try_wait(&S.empty[s], par))
-          if ((++k & 15) == 0 && sp.expired()) return;
-      }
+      const int s = rp.s;
+      if (rp.n >= (uint32_t)nslots && !ring_wait(&S.empty[s], rp.par ^ 1u, sp)) return;
       if (*reinterpret_cast<volatile int*>(&S.abort)) return;
       const uint32_t bytes = (uint32_t)n * r.K * 2;
       char* dst = ring + (size_t)s * slot_bytes;
       mbar_expect_tx(&S.full[s], bytes * (r.m1 ? 2u : 1u));
       bulk_g2s(dst, r.m0 + (size_t)row * r.K, bytes, &S.full[s]);
       if (r.m1) bulk_g2s(dst + bytes, r.m1 + (size_t)row * r.K, bytes, &S.full[s]);
-      S.issued = ++iter;
+      rp.next(nslots);
+      S.issued = rp.n;
     }
   }
 }
@@ -258,20 +301,48 @@ __device__ __forceinline__ bool consumer_any(bool v) {
   return r != 0;
 }
 
+// Where element i of an input row of n (a multiple of 8) sits in shared
+// memory: the first four elements of every 8-element chunk in the lower half,
+// the last four in the upper half. A lane reading chunk c then reads two
+// float4 at a 16-byte stride across the warp, which no two lanes of a load
+// phase share a bank group in.
+__device__ __forceinline__ int xs_at(int i, int n) {
+  return ((i & 4) ? (n >> 1) : 0) + ((i >> 3) << 2) + (i & 3);
+}
+
 // Gather the phase input [B][n] from epoch-tagged words into xs (fp32);
 // with gamma, also compute the RMSNorm factor per sequence and scale xs.
+// The gains of this thread's elements are fetched before the words are
+// polled, so their round trip overlaps the wait for the previous phase.
+constexpr int kGainRegs = 16;  // per thread: RMSNorm inputs up to 16 * 352 = 5632 wide
 template <int BT>
-__device__ void gather_input(const PersistArgs& a, PShared& S, const uint64_t* src, int n,
-                             uint32_t epoch, const uint16_t* embed_rows, const uint16_t* gamma,
-                             float* xs, Spin& sp) {
+__device__ __noinline__ void gather_input(const PersistArgs& a, const uint64_t* src, int n,
+                                          uint32_t epoch, const uint16_t* embed_rows,
+                                          const uint16_t* gamma, Spin& sp) {
+  // shared-memory pointers are derived from the dynamic shared array here, so
+  // the compiler addresses them as shared, not generic
+  extern __shared__ __align__(128) char smem[];
+  PShared& S = *reinterpret_cast<PShared*>(smem);
+  float* xs = reinterpret_cast<float*>(smem + a.xs_offset);
+  const int nb = a.B;
+  const float eps = a.eps;
   const int ct = threadIdx.x - kWarp, warp = ct / kWarp, lane = ct % kWarp;
+  float gr[kGainRegs];
+  const bool gain_regs = gamma && n <= kGainRegs * kPConsumerThreads;
+  if (gain_regs) {
+#pragma unroll
+    for (int u = 0; u < kGainRegs; ++u) {
+      const int i = ct + u * kPConsumerThreads;
+      gr[u] = i < n ? bf16_to_f32(gamma[i]) : 0.f;
+    }
+  }
 #pragma unroll 1
   for (int b = 0; b < BT; ++b) {
     float ss = 0.f;
     for (int i0 = ct; i0 < n; i0 += kLLBatch * kPConsumerThreads) {
       const int count = min(kLLBatch, (n - i0 + kPConsumerThreads - 1) / kPConsumerThreads);
       float v[kLLBatch];
-      if (b >= a.B) {
+      if (b >= nb) {
 #pragma unroll
         for (int u = 0; u < kLLBatch; ++u) v[u] = 0.f;
       } else if (embed_rows) {
@@ -285,7 +356,7 @@ __device__ void gather_input(const PersistArgs& a, PShared& S, const uint64_t* s
 #pragma unroll
       for (int u = 0; u < kLLBatch; ++u) {
         if (u >= count) break;
-        xs[b * n + i0 + u * kPConsumerThreads] = v[u];
+        xs[b * n + xs_at(i0 + u * kPConsumerThreads, n)] = v[u];
         ss = fmaf(v[u], v[u], ss);
       }
     }
@@ -302,13 +373,29 @@ __device__ void gather_input(const PersistArgs& a, PShared& S, const uint64_t* s
   if (ct < BT) {
     float t = 0.f;
     for (int w = 0; w < kPConsumerWarps; ++w) t += S.red[w][ct];
-    S.rn[ct] = 1.f / sqrtf(t / (float)n + a.eps);
+    S.rn[ct] = 1.f / sqrtf(t / (float)n + eps);
   }
   consumer_sync();
-  for (int i = ct; i < n; i += kPConsumerThreads) {
-    const float g = bf16_to_f32(gamma[i]);
+  if (gain_regs) {
 #pragma unroll
-    for (int b = 0; b < BT; ++b) xs[b * n + i] = (xs[b * n + i] * S.rn[b]) * g;
+    for (int u = 0; u < kGainRegs; ++u) {
+      const int i = ct + u * kPConsumerThreads;
+      if (i < n)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          float* x = xs + b * n + xs_at(i, n);
+          *x = (*x * S.rn[b]) * gr[u];
+        }
+    }
+  } else {
+    for (int i = ct; i < n; i += kPConsumerThreads) {
+      const float g = bf16_to_f32(gamma[i]);
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        float* x = xs + b * n + xs_at(i, n);
+        *x = (*x * S.rn[b]) * g;
+      }
+    }
   }
   consumer_sync();
 }
@@ -335,22 +422,91 @@ __device__ __forceinline__ float dot8r(const uint4& w, const float (&x)[8]) {
   return s;
 }
 
+// One row of a tile times the input held in registers (the lane's chunks
+// lane, lane + 32, ...): the per-lane partial of the row's dot product.
+__device__ __forceinline__ float row_dot_xreg(const uint16_t* w, const float (&xr)[kXReg][8],
+                                              int C, int lane) {
+  float p[kXReg];
+#pragma unroll
+  for (int jj = 0; jj < kXReg; ++jj) {
+    const int c = lane + jj * kWarp;
+    p[jj] = c < C ? dot8r(*reinterpret_cast<const uint4*>(w + c * 8), xr[jj]) : 0.f;
+  }
+  float s = p[0];
+#pragma unroll
+  for (int jj = 1; jj < kXReg; ++jj) s += p[jj];
+  return s;
+}
+
+// Chunks [c0, c1) of one row (and of its up row when w1 is set) times the
+// input [BT][K] in shared memory: per-lane partials into o[m * BT + b].
+template <int BT>
+__device__ __forceinline__ void row_dot_smem(const uint16_t* w0, const uint16_t* w1,
+                                             const float* xs, int K, int c0, int c1, int lane,
+                                             float* o) {
+#pragma unroll 2
+  for (int c = c0 + lane; c < c1; c += kWarp) {
+    const uint4 wa = *reinterpret_cast<const uint4*>(w0 + c * 8);
+    const uint4 wb = w1 ? *reinterpret_cast<const uint4*>(w1 + c * 8) : uint4{};
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      float xb[8];
+      const float4 p0 = *reinterpret_cast<const float4*>(xs + b * K + c * 4);
+      const float4 p1 = *reinterpret_cast<const float4*>(xs + b * K + K / 2 + c * 4);
+      xb[0] = p0.x; xb[1] = p0.y; xb[2] = p0.z; xb[3] = p0.w;
+      xb[4] = p1.x; xb[5] = p1.y; xb[6] = p1.z; xb[7] = p1.w;
+      o[b] += dot8r(wa, xb);
+      if (w1) o[BT + b] += dot8r(wb, xb);
+    }
+  }
+}
+
+// Sums each of the N values of a lane over the warp in N - 1 + (5 - log2 N)
+// shuffles instead of 5 N: every butterfly step swaps half of the values
+// with the partner lane, so the number a lane carries halves. Afterwards
+// v[0] of lane i * (32 / N) holds the warp total of value i.
+template <int N>
+__device__ __forceinline__ void warp_sum_many(float (&v)[N]) {
+  static_assert(N >= 1 && N <= kWarp && (N & (N - 1)) == 0, "N must be a power of two");
+  const int lane = threadIdx.x % kWarp;
+  int o = kWarp / 2;
+#pragma unroll
+  for (int half = N / 2; half >= 1; half /= 2, o /= 2) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = upper ? v[k] : v[k + half];
+      const float keep = upper ? v[k + half] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+    }
+  }
+#pragma unroll
+  for (; o > 0; o /= 2) v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
+}
+
+// Where a phase's outputs go, read from the arguments once per phase: the
+// tile loop then touches no argument field (after every asm statement with a
+// memory clobber the compiler would have to load those again).
+struct PhaseOut {
+  uint64_t* words;  // epoch-tagged outputs [B][stride] (QKV, residual, SiLU * up)
+  float* logits;    // [B][stride] (LM head)
+  int stride;
+};
+
 // Epilogue of output row j of sequence b on the reducing thread: bias, the
 // residual add, silu(gate) * up, or the logit and its arg-max key.
 template <int BT>
-__device__ __forceinline__ void tile_epilogue(const PersistArgs& a, const PShared& S, int kind,
-                                              const PLayer* P, int r0, int j, int b, float v0,
-                                              float v1, uint32_t ep,
-                                              unsigned long long (&best)[BT]) {
+__device__ __forceinline__ void tile_epilogue(const PShared& S, int kind, const PhaseOut& po,
+                                              int r0, int j, int b, float v0, float v1,
+                                              uint32_t ep, unsigned long long (&best)[BT]) {
   if (kind == kQKV) {
-    if (P->b_qkv) v0 += bf16_to_f32(P->b_qkv[j]);
-    st_word(a.qkvw + (size_t)b * a.nqkv + j, v0, ep);
+    st_word(po.words + (size_t)b * po.stride + j, v0 + S.bias[j - r0], ep);
   } else if (kind == kOPROJ || kind == kDOWN) {
-    st_word(a.xw + (size_t)b * a.H + j, S.xold[b][j - r0] + v0, ep);
+    st_word(po.words + (size_t)b * po.stride + j, S.xold[b][j - r0] + v0, ep);
   } else if (kind == kGU) {
-    st_word(a.hw + (size_t)b * a.F + j, silu_mul_p(v0, v1), ep);
+    st_word(po.words + (size_t)b * po.stride + j, silu_mul_p(v0, v1), ep);
   } else {
-    a.logits[(size_t)b * a.V + j] = v0;
+    po.logits[(size_t)b * po.stride + j] = v0;
     const unsigned long long key = argmax_key(v0, (uint32_t)j);
 #pragma unroll
     for (int bb = 0; bb < BT; ++bb)
@@ -365,26 +521,22 @@ __device__ __forceinline__ void tile_epilogue(const PersistArgs& a, const PShare
 // never leaves shared memory.
 constexpr int kAttnMaxChunk = 128;
 __host__ __device__ __forceinline__ int attn_chunk(int slot_bytes, int D, int es) {
-  return slot_bytes / (2 * D * es);
+  const int cp = slot_bytes / (2 * D * es);
+  return cp < kAttnMaxChunk ? cp : kAttnMaxChunk;
 }
 
 // Producer: issue the chunk tiles of (layer, b, g) for slots [0, npos).
 template <bool KV16>
 __device__ bool produce_kv(const PersistArgs& a, PShared& S, char* ring, int slot_bytes,
-                           int nslots, int layer, int b, int g, int npos, uint32_t& iter,
+                           int nslots, int layer, int b, int g, int npos, RingPos& rp,
                            Spin& sp) {
   constexpr int ES = KV16 ? 2 : 4;
   const int D = a.D, CP = attn_chunk(slot_bytes, D, ES);
   const int bs = a.kv.paged ? a.kv.block_size : npos;
   for (int t0 = 0; t0 < npos; t0 += CP) {
     const int n = min(CP, npos - t0);
-    const int s = iter % nslots;
-    if (iter >= (uint32_t)nslots) {
-      const uint32_t par = ((iter / nslots) - 1) & 1;
-      int k = 0;
-      while (!mbar_try_wait(&S.empty[s], par))
-        if ((++k & 15) == 0 && sp.expired()) return false;
-    }
+    const int s = rp.s;
+    if (rp.n >= (uint32_t)nslots && !ring_wait(&S.empty[s], rp.par ^ 1u, sp)) return false;
     if (*reinterpret_cast<volatile int*>(&S.abort)) return false;
     // runs of positions contiguous in the cache: the whole chunk when the
     // cache is contiguous, a block's worth when it is paged
@@ -408,7 +560,8 @@ __device__ bool produce_kv(const PersistArgs& a, PShared& S, char* ring, int slo
       }
       t += len;
     }
-    S.issued = ++iter;
+    rp.next(nslots);
+    S.issued = rp.n;
   }
   return true;
 }
@@ -419,96 +572,165 @@ __device__ __forceinline__ float kv_smem(const char* base, int idx) {
   else return reinterpret_cast<const float*>(base)[idx];
 }
 
+// Elements idx .. idx + 3 (idx a multiple of 4) in one 16- or 8-byte load.
+template <bool KV16>
+__device__ __forceinline__ void kv_smem4(const char* base, int idx, float (&o)[4]) {
+  if constexpr (KV16) {
+    const uint2 w = *reinterpret_cast<const uint2*>(base + (size_t)idx * 2);
+    o[0] = bf16_lo(w.x); o[1] = bf16_hi(w.x); o[2] = bf16_lo(w.y); o[3] = bf16_hi(w.y);
+  } else {
+    const float4 v = *reinterpret_cast<const float4*>(base + (size_t)idx * 4);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+}
+// Elements idx, idx + 1 (idx even) in one load.
+template <bool KV16>
+__device__ __forceinline__ float2 kv_smem2(const char* base, int idx) {
+  if constexpr (KV16) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(base + (size_t)idx * 2);
+    return make_float2(bf16_lo(w), bf16_hi(w));
+  } else {
+    return *reinterpret_cast<const float2*>(base + (size_t)idx * 4);
+  }
+}
+
 // Consumer: one (sequence b, kv head g). RoPE (+ q/k norm) of the G query
 // heads and the key, K/V append at slot pos, then the online-softmax scan:
 // the new position first, then the cached chunks from the ring.
+constexpr int kAttnWords = 4;  // q/k/v words gathered per thread: (G + 2) D <= 4 * 352
 template <int D, bool KV16>
-__device__ void attention_item(const PersistArgs& a, PShared& S, int b, int g, int layer,
-                               uint32_t ep_qkv, uint32_t ep_out, float* scratch, char* ring,
-                               int slot_bytes, int nslots, uint32_t& iter, Spin& sp) {
-  constexpr int GM = 8, ES = KV16 ? 2 : 4;
+__device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int layer,
+                                            uint32_t ep_qkv, uint32_t ep_out, int nslots,
+                                            RingPos& rp, Spin& sp) {
+  // shared-memory pointers are derived from the dynamic shared array here, so
+  // the compiler addresses them as shared, not generic
+  extern __shared__ __align__(128) char smem[];
+  PShared& S = *reinterpret_cast<PShared*>(smem);
+  float* scratch = reinterpret_cast<float*>(smem + a.attn_offset);
+  char* ring = smem + a.ring_offset;
+  const int slot_bytes = a.slot_bytes;
+  constexpr int GM = 8, ES = KV16 ? 2 : 4, E = D / 32;
   const int ct = threadIdx.x - kWarp, warp = ct / kWarp, lane = ct % kWarp;
-  const int G = a.Hq / a.Hkv;
+  // the arguments this item uses, as locals: `a` sits behind a generic
+  // reference, and every store through the shared-memory pointers below
+  // would otherwise make the compiler read its fields again
+  const KVView kv = a.kv;
+  const int Hq = a.Hq, Hkv = a.Hkv;
+  const float eps = a.eps;
+  int* const status = a.status;
+  const int G = Hq / Hkv;
   const int CP = attn_chunk(slot_bytes, D, ES);
   const int pos = S.pos[b];
-  float* qs = scratch;                    // [GM][D]
-  float* kn = qs + GM * D;                // [D]
-  float* vn = kn + D;                     // [D]
-  float* sc = vn + D;                     // [GM][kAttnMaxChunk]
-  float* mrun = sc + GM * kAttnMaxChunk;  // [GM] running max
-  float* lrun = mrun + GM;                // [GM] running sum
-  float* resc = lrun + GM;                // [GM] rescale of the chunk
+  float* qs = scratch;                        // [GM][D]
+  float* kn = qs + GM * D;                    // [D]
+  float* vn = kn + D;                         // [D]
+  float* sc = vn + D;                         // [2][GM][kAttnMaxChunk], by chunk parity
+  float* mrun = sc + 2 * GM * kAttnMaxChunk;  // [GM] running max
+  float* lrun = mrun + GM;                    // [GM] running sum
+  float* resc = lrun + GM;                    // [GM] rescale of the chunk
   const PLayer& P = a.layers[layer];
-  const uint64_t* qkv = a.qkvw + (size_t)b * a.nqkv;
 
-  // gather q heads, k, v of this group
-  for (int i = ct; i < (G + 2) * D; i += kPConsumerThreads) {
+  // gather the G query heads, k and v of this group: all loads in flight
+  // first; while they are out, fetch what does not depend on them (the
+  // rotation angles of this lane's dimension pairs -- every RoPE warp below
+  // uses the same lane -> dimension map -- and the q/k norm gains); then
+  // re-poll the words that were stale
+  const uint64_t* qkv = a.qkvw + (size_t)b * a.nqkv;
+  const int total = (G + 2) * D;
+  uint64_t w[kAttnWords];
+  int src[kAttnWords];
+#pragma unroll
+  for (int u = 0; u < kAttnWords; ++u) {
+    const int i = ct + u * kPConsumerThreads;
     const int h = i / D, d = i % D;
-    int src;
-    if (h < G) src = (g * G + h) * D + d;
-    else if (h == G) src = (a.Hq + g) * D + d;
-    else src = (a.Hq + a.Hkv + g) * D + d;
-    const float v = ll_get(qkv + src, ep_qkv, sp);
-    if (h < G) qs[h * D + d] = v;
-    else if (h == G) kn[d] = v;
-    else vn[d] = v;
+    src[u] = h < G ? (g * G + h) * D + d
+                   : (h == G ? (Hq + g) * D + d : (Hq + Hkv + g) * D + d);
+    if (i < total) w[u] = ld_word(qkv + src[u]);
+  }
+  const float* inv_freq = a.inv_freq;
+  float cs[E / 2], sn[E / 2];
+#pragma unroll
+  for (int j = 0; j < E / 2; ++j) {
+    const float angle = __fmul_rn((float)pos, inv_freq[lane + 32 * j]);
+    sincosf(angle, &sn[j], &cs[j]);
+  }
+  const uint16_t* gq = P.g_q;
+  const uint16_t* gk = P.g_k;
+  float gain_q[E], gain_k[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    gain_q[j] = gq ? bf16_to_f32(gq[lane + 32 * j]) : 1.f;
+    gain_k[j] = gk ? bf16_to_f32(gk[lane + 32 * j]) : 1.f;
+  }
+  {
+#pragma unroll
+    for (int u = 0; u < kAttnWords; ++u) {
+      const int i = ct + u * kPConsumerThreads;
+      if (i >= total) break;
+      int k = 0;
+      while (static_cast<uint32_t>(w[u] >> 32) != ep_qkv) {
+        if ((++k & 63) == 0 && sp.expired()) {
+          w[u] = 0;
+          break;
+        }
+        w[u] = ld_word(qkv + src[u]);
+      }
+      float v = __uint_as_float(static_cast<uint32_t>(w[u]));
+      const int h = i / D, d = i % D;
+      if (h < G) {
+        qs[h * D + d] = v;
+      } else if (h == G) {
+        kn[d] = v;
+      } else {
+        if (KV16) v = bf16_to_f32(f32_to_bf16(v));  // the scan uses v as the cache stores it
+        vn[d] = v;
+      }
+    }
   }
   consumer_sync();
   // per-head RMSNorm (q/k norm) and RoPE, one warp per head (G is the key)
   for (int hh = warp; hh <= G; hh += kPConsumerWarps) {
     float* v = hh < G ? qs + hh * D : kn;
-    constexpr int E = D / 32;
     float e[E];
 #pragma unroll
     for (int j = 0; j < E; ++j) e[j] = v[lane + 32 * j];
-    const uint16_t* gain = hh < G ? P.g_q : P.g_k;
-    if (gain) {
+    if (hh < G ? gq != nullptr : gk != nullptr) {
       float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < E; ++j) ss = fmaf(e[j], e[j], ss);
       ss = warp_sum(ss);
-      const float r = 1.f / sqrtf(ss / (float)D + a.eps);
+      const float r = 1.f / sqrtf(ss / (float)D + eps);
 #pragma unroll
-      for (int j = 0; j < E; ++j) e[j] = (e[j] * r) * bf16_to_f32(gain[lane + 32 * j]);
+      for (int j = 0; j < E; ++j) e[j] = (e[j] * r) * (hh < G ? gain_q[j] : gain_k[j]);
     }
 #pragma unroll
     for (int j = 0; j < E / 2; ++j) {
-      const int i = lane + 32 * j;
-      const float angle = __fmul_rn((float)pos, a.inv_freq[i]);
-      float sn, cs;
-      sincosf(angle, &sn, &cs);
       const float x0 = e[j], x1 = e[j + E / 2];
-      e[j] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
-      e[j + E / 2] = __fadd_rn(__fmul_rn(x1, cs), __fmul_rn(x0, sn));
+      e[j] = __fsub_rn(__fmul_rn(x0, cs[j]), __fmul_rn(x1, sn[j]));
+      e[j + E / 2] = __fadd_rn(__fmul_rn(x1, cs[j]), __fmul_rn(x0, sn[j]));
     }
 #pragma unroll
-    for (int j = 0; j < E; ++j) v[lane + 32 * j] = e[j];
+    for (int j = 0; j < E; ++j) {
+      float x = e[j];
+      if (KV16 && hh == G) x = bf16_to_f32(f32_to_bf16(x));  // k as the cache stores it
+      v[lane + 32 * j] = x;
+    }
   }
   consumer_sync();
-  // append K/V at slot pos; the scan reads slot pos from kn/vn as stored
-  const bool pos_ok = a.kv.slot_ok(b, pos);
-  if (!pos_ok && ct == 0 && a.status) atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
-  if (ct < D) {
-    float k_st = kn[ct], v_st = vn[ct];
-    if (pos_ok) {
-      const size_t off = a.kv.offset(layer, b, g, pos);
-      kv_store<KV16>(a.kv.k, off + ct, k_st);
-      kv_store<KV16>(a.kv.v, off + ct, v_st);
-    }
-    if (KV16) {
-      k_st = bf16_to_f32(f32_to_bf16(k_st));
-      v_st = bf16_to_f32(f32_to_bf16(v_st));
-    }
-    kn[ct] = k_st;
-    vn[ct] = v_st;
+  // append K/V at slot pos; the new position opens the running state:
+  // m = its score, l = 1, acc = v
+  const bool pos_ok = kv.slot_ok(b, pos);
+  if (!pos_ok && ct == 0 && status) atomicCAS(status, 0, (int)NC_ERR_POSITION);
+  if (ct < D && pos_ok) {
+    const size_t off = kv.offset(layer, b, g, pos);
+    kv_store<KV16>(kv.k, off + ct, kn[ct]);
+    kv_store<KV16>(kv.v, off + ct, vn[ct]);
   }
-  consumer_sync();
   const float scale = 1.f / sqrtf((float)D);
-  // the new position opens the running state: m = its score, l = 1, acc = v
   for (int h = warp; h < G; h += kPConsumerWarps) {
     float s = 0.f;
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) s = fmaf(qs[h * D + lane + 32 * j], kn[lane + 32 * j], s);
+    for (int j = 0; j < E; ++j) s = fmaf(qs[h * D + lane + 32 * j], kn[lane + 32 * j], s);
     s = warp_sum(s) * scale;
     if (lane == 0) {
       mrun[h] = pos_ok ? s : -INFINITY;
@@ -524,17 +746,14 @@ __device__ void attention_item(const PersistArgs& a, PShared& S, int b, int g, i
   }
   consumer_sync();
   const int npos = pos_ok ? pos : 0;
-  for (int t0 = 0; t0 < npos; t0 += CP) {
+  int cpar = 0;
+  for (int t0 = 0; t0 < npos; t0 += CP, cpar ^= 1) {
     const int n = min(CP, npos - t0);
-    const int s = iter % nslots;
-    {
-      const uint32_t par = (iter / nslots) & 1;
-      int k = 0;
-      while (!mbar_try_wait(&S.full[s], par))
-        if ((++k & 15) == 0 && sp.expired()) break;
-    }
+    const int s = rp.s;
+    ring_wait(&S.full[s], rp.par, sp);
     const char* Ks = ring + (size_t)s * slot_bytes;
     const char* Vs = Ks + (size_t)CP * D * ES;
+    float* scc = sc + cpar * GM * kAttnMaxChunk;  // the other buffer may still be read
     // scores: warp -> (head, 32 positions); lane l reads its row from column
     // (d + l) mod D so the 32 rows of a warp fall in different banks
     const int blocks = (n + 31) / 32;
@@ -542,29 +761,38 @@ __device__ void attention_item(const PersistArgs& a, PShared& S, int b, int g, i
       const int h = wb % G, p = (wb / G) * 32 + lane;
       if (p < n) {
         float sv = -INFINITY;
-        if (a.kv.slot_ok(b, t0 + p)) {
-          float acc = 0.f;
-#pragma unroll 8
-          for (int d = 0; d < D; ++d) {
-            const int dd = (d + lane) & (D - 1);
-            acc = fmaf(qs[h * D + dd], kv_smem<KV16>(Ks, p * D + dd), acc);
+        if (kv.slot_ok(b, t0 + p)) {
+          // 4-element columns, skewed by lane: the 8 lanes of each 16-byte
+          // load phase read 8 different bank groups
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+          const float* qh = qs + h * D;
+#pragma unroll
+          for (int j = 0; j < D / 4; ++j) {
+            const int c = ((j + lane) & (D / 4 - 1)) * 4;
+            const float4 q4 = *reinterpret_cast<const float4*>(qh + c);
+            float k4[4];
+            kv_smem4<KV16>(Ks, p * D + c, k4);
+            s4[0] = fmaf(q4.x, k4[0], s4[0]);
+            s4[1] = fmaf(q4.y, k4[1], s4[1]);
+            s4[2] = fmaf(q4.z, k4[2], s4[2]);
+            s4[3] = fmaf(q4.w, k4[3], s4[3]);
           }
-          sv = acc * scale;
+          sv = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * scale;
         }
-        sc[h * kAttnMaxChunk + p] = sv;
+        scc[h * kAttnMaxChunk + p] = sv;
       }
     }
     consumer_sync();
     for (int h = warp; h < G; h += kPConsumerWarps) {
       float m = -INFINITY;
-      for (int t = lane; t < n; t += kWarp) m = fmaxf(m, sc[h * kAttnMaxChunk + t]);
+      for (int t = lane; t < n; t += kWarp) m = fmaxf(m, scc[h * kAttnMaxChunk + t]);
       m = warp_max(m);
       const float m_new = fmaxf(mrun[h], m);
       float l = 0.f;
       for (int t = lane; t < n; t += kWarp) {
-        const float x = sc[h * kAttnMaxChunk + t];
+        const float x = scc[h * kAttnMaxChunk + t];
         const float p = x == -INFINITY ? 0.f : expf(x - m_new);
-        sc[h * kAttnMaxChunk + t] = p;
+        scc[h * kAttnMaxChunk + t] = p;
         l += p;
       }
       l = warp_sum(l);
@@ -578,23 +806,39 @@ __device__ void attention_item(const PersistArgs& a, PShared& S, int b, int g, i
     consumer_sync();
     if (ct < npair) {
       const float r = resc[my_h];
-      acc0 *= r;
-      acc1 *= r;
-      for (int t = 0; t < n; ++t) {
-        const float p = sc[my_h * kAttnMaxChunk + t];
-        if (p == 0.f) continue;
-        acc0 = fmaf(p, kv_smem<KV16>(Vs, t * D + 2 * my_d2), acc0);
-        acc1 = fmaf(p, kv_smem<KV16>(Vs, t * D + 2 * my_d2 + 1), acc1);
+      // two interleaved chains per output; a masked position (p = 0) may sit
+      // over stale shared memory, so its value is replaced, not multiplied
+      float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;
+      const float* ph = scc + my_h * kAttnMaxChunk;
+      int t = 0;
+#pragma unroll 4
+      for (; t + 1 < n; t += 2) {
+        const float pa = ph[t], pb = ph[t + 1];
+        const float2 va = kv_smem2<KV16>(Vs, t * D + 2 * my_d2);
+        const float2 vb = kv_smem2<KV16>(Vs, (t + 1) * D + 2 * my_d2);
+        e0 = fmaf(pa, pa == 0.f ? 0.f : va.x, e0);
+        e1 = fmaf(pa, pa == 0.f ? 0.f : va.y, e1);
+        o0 = fmaf(pb, pb == 0.f ? 0.f : vb.x, o0);
+        o1 = fmaf(pb, pb == 0.f ? 0.f : vb.y, o1);
       }
+      if (t < n) {
+        const float pa = ph[t];
+        const float2 va = kv_smem2<KV16>(Vs, t * D + 2 * my_d2);
+        e0 = fmaf(pa, pa == 0.f ? 0.f : va.x, e0);
+        e1 = fmaf(pa, pa == 0.f ? 0.f : va.y, e1);
+      }
+      acc0 = fmaf(acc0, r, e0 + o0);
+      acc1 = fmaf(acc1, r, e1 + o1);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[s]);
-    ++iter;
-    consumer_sync();  // sc is rewritten by the next chunk
+    rp.next(nslots);
+    // no barrier here: the next chunk writes the other score buffer, and the
+    // one after it is behind that chunk's two barriers
   }
   if (ct < npair) {
     const float inv = lrun[my_h] > 0.f ? 1.f / lrun[my_h] : 0.f;
-    uint64_t* out = a.aw + (size_t)b * a.Hq * D + (size_t)(g * G + my_h) * D + 2 * my_d2;
+    uint64_t* out = a.aw + (size_t)b * Hq * D + (size_t)(g * G + my_h) * D + 2 * my_d2;
     st_word(out, acc0 * inv, ep_out);
     st_word(out + 1, acc1 * inv, ep_out);
   }
@@ -609,7 +853,6 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs 
   const int slot_bytes = a.slot_bytes, nslots = a.nslots;
   char* ring = smem + a.ring_offset;
   float* xs = reinterpret_cast<float*>(smem + a.xs_offset);
-  float* scratch = reinterpret_cast<float*>(smem + a.attn_offset);
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
 
   if (threadIdx.x == 0) {
@@ -634,35 +877,36 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs 
   __syncthreads();
   const uint32_t seq = *reinterpret_cast<volatile const unsigned*>(a.seq);
   Spin sp{global_timer() + a.timeout_ns, &S.abort, a.status};
-  if (a.prof && blockIdx.x == 0 && threadIdx.x == 0)
-    a.prof[2 * (kPhasesPerLayer * a.L + 1)] = global_timer();
+  const int nph_all = kPhasesPerLayer * a.L + 1;
+  unsigned long long* const prof_cta =
+      a.prof ? a.prof + (size_t)blockIdx.x * (2 * nph_all + 2) : nullptr;
+  if (prof_cta && threadIdx.x == 0) prof_cta[2 * nph_all] = global_timer();
 
   if (warp == 0) {
     if (lane == 0) producer<KV16>(a, S, ring, slot_bytes, nslots, sp);
   } else {
     const int ct = threadIdx.x - kWarp, cw = ct / kWarp;
     const int L = a.L, nph = kPhasesPerLayer * L + 1;
-    uint32_t iter = 0;
+    RingPos rp;
+    int kb = 0;  // k-split partial-sum buffer of the next split tile
     unsigned long long best[BT];
 #pragma unroll
     for (int b = 0; b < BT; ++b) best[b] = 0ull;
-    float xr[kXReg][8];      // batch 1: this lane's input chunks (see the tile loop)
-    int xr_ks = -1, xr_seg = -1;
     for (int ph = 0; ph < nph; ++ph) {
       // Uniform across the consumer warps, and a barrier: no warp overwrites
       // the shared input vector while another still reduces against it.
       if (consumer_any(*reinterpret_cast<volatile int*>(&S.abort) != 0)) break;
-      const bool prof = a.prof && blockIdx.x == 0 && ct == 0;
-      if (prof) a.prof[2 * ph] = global_timer();
+      unsigned long long* const prof = ct == 0 ? prof_cta : nullptr;
+      if (prof) prof[2 * ph] = global_timer();
       const int layer = ph / kPhasesPerLayer;
       const int kind = ph == kPhasesPerLayer * L ? kHEAD : ph % kPhasesPerLayer;
       const uint32_t ep = epoch_of(seq, ph);
       if (kind == kATTN) {
         const int items = a.B * a.Hkv;
         for (int it = blockIdx.x; it < items; it += gridDim.x)
-          attention_item<D, KV16>(a, S, it / a.Hkv, it % a.Hkv, layer, epoch_of(seq, ph - 1),
-                                  ep, scratch, ring, slot_bytes, nslots, iter, sp);
-        if (prof) a.prof[2 * ph + 1] = global_timer();
+          attention_item<D, KV16>(a, it / a.Hkv, it % a.Hkv, layer, epoch_of(seq, ph - 1), ep,
+                                  nslots, rp, sp);
+        if (prof) prof[2 * ph + 1] = global_timer();
         continue;
       }
       const Rows r = phase_rows(a, ph, blockIdx.x, gridDim.x, slot_bytes);
@@ -686,134 +930,112 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs 
         }
       }
       if (kind == kQKV) {
-        gather_input<BT>(a, S, a.xw, K, epoch_of(seq, ph - 1), layer == 0 ? a.embed : nullptr,
-                         P->g_attn, xs, sp);
+        const int nr = r.r1 - r.r0;  // the bias is read before the input is in
+        for (int i = ct; i < nr; i += kPConsumerThreads)
+          S.bias[i] = P->b_qkv ? bf16_to_f32(P->b_qkv[r.r0 + i]) : 0.f;
+        gather_input<BT>(a, a.xw, K, epoch_of(seq, ph - 1), layer == 0 ? a.embed : nullptr,
+                         P->g_attn, sp);
       } else if (kind == kOPROJ) {
-        gather_input<BT>(a, S, a.aw, K, epoch_of(seq, ph - 1), nullptr, nullptr, xs, sp);
+        gather_input<BT>(a, a.aw, K, epoch_of(seq, ph - 1), nullptr, nullptr, sp);
       } else if (kind == kGU) {
-        gather_input<BT>(a, S, a.xw, K, epoch_of(seq, ph - 1), nullptr, P->g_mlp, xs, sp);
+        gather_input<BT>(a, a.xw, K, epoch_of(seq, ph - 1), nullptr, P->g_mlp, sp);
       } else if (kind == kDOWN) {
-        gather_input<BT>(a, S, a.hw, K, epoch_of(seq, ph - 1), nullptr, nullptr, xs, sp);
+        gather_input<BT>(a, a.hw, K, epoch_of(seq, ph - 1), nullptr, nullptr, sp);
       } else {
-        gather_input<BT>(a, S, a.xw, K, epoch_of(seq, ph - 1), nullptr, a.g_final, xs, sp);
+        gather_input<BT>(a, a.xw, K, epoch_of(seq, ph - 1), nullptr, a.g_final, sp);
       }
-      if (prof) a.prof[2 * ph + 1] = global_timer();
-      xr_ks = -1;  // a new input vector: reload the register copy
+      if (prof) prof[2 * ph + 1] = global_timer();
       const int two = r.m1 ? 2 : 1;
+      PhaseOut po;
+      po.words = kind == kQKV ? a.qkvw : (kind == kGU ? a.hw : a.xw);
+      po.logits = a.logits;
+      po.stride = kind == kQKV ? a.nqkv : (kind == kGU ? a.F : (kind == kHEAD ? a.V : a.H));
+      const int nb = a.B;
+      const int C = K / 8;  // 16-byte chunks per row
+      // batch 1 and rows of at most 1024: every lane keeps its chunks of the
+      // input in registers for the whole phase, and each unit is one row (or
+      // one gate|up pair) reduced by one warp
+      const bool xreg = BT == 1 && C <= kXReg * kWarp;
+      float xr[kXReg][8];
+      if (xreg) {
+#pragma unroll
+        for (int jj = 0; jj < kXReg; ++jj) {
+          const int c = lane + jj * kWarp;
+          float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
+          if (c < C) {  // two 16-byte loads, not eight scalar ones
+            p0 = *reinterpret_cast<const float4*>(xs + c * 4);
+            p1 = *reinterpret_cast<const float4*>(xs + K / 2 + c * 4);
+          }
+          xr[jj][0] = p0.x; xr[jj][1] = p0.y; xr[jj][2] = p0.z; xr[jj][3] = p0.w;
+          xr[jj][4] = p1.x; xr[jj][5] = p1.y; xr[jj][6] = p1.z; xr[jj][7] = p1.w;
+        }
+      }
       for (int row = r.r0; row < r.r1; row += r.R) {
         const int n = min(r.R, r.r1 - row);
-        const int s = iter % nslots;
-        {
-          const uint32_t par = (iter / nslots) & 1;
-          int k = 0;
-          while (!mbar_try_wait(&S.full[s], par))
-            if ((++k & 15) == 0 && sp.expired()) break;
+        // Long rows (or batch > 1, x read from shared memory) are cut into KS
+        // k-segments when the tile has few units, so the work spreads over all
+        // warps (up to kUnitsPerWarp items each); a segment keeps at least 64
+        // chunks, two per lane.
+        int KS = 1;
+        if (!xreg && n < kPConsumerWarps) {
+          KS = kUnitsPerWarp * kPConsumerWarps / n;
+          const int kmax = C / 64;
+          if (KS > kmax) KS = kmax;
+          if (KS < 1) KS = 1;
         }
-        if (*reinterpret_cast<volatile int*>(&S.abort)) break;
-        const uint16_t* tile = reinterpret_cast<const uint16_t*>(ring + (size_t)s * slot_bytes);
-        // Work split: an output unit (a row; a gate|up pair) is cut into KS
-        // k-segments and each warp takes one (unit, segment), so a tile of few
-        // long rows still keeps every warp busy on a short chain. Tiles hold
-        // at most kPConsumerWarps units.
-        const int KS = n >= kPConsumerWarps ? 1 : kPConsumerWarps / n;
-        const int C = K / 8;  // 16-byte chunks per row
-        const bool active = cw < n * KS;
-        const int ui = cw / KS, seg = cw % KS;
-        float acc[2][BT];
+        const int items = n * KS;  // warp cw takes items cw, cw + W, ... (at most kUnitsPerWarp)
+        ring_wait(&S.full[rp.s], rp.par, sp);  // on expiry the tile is garbage; the step is failed
+        const uint16_t* tile =
+            reinterpret_cast<const uint16_t*>(ring + (size_t)rp.s * slot_bytes);
+        const size_t ms = (size_t)n * K;  // the up rows follow the n gate rows
+        constexpr int NV = kUnitsPerWarp * 2 * BT;  // [item u][matrix m][sequence b]
+        float v[NV];
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+        for (int i = 0; i < NV; ++i) v[i] = 0.f;
 #pragma unroll
-          for (int b = 0; b < BT; ++b) acc[u][b] = 0.f;
-        if (active && BT == 1) {
-          // batch 1: this lane's input chunks stay in registers across the
-          // phase's tiles; only the weights are read from shared memory
-          const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
-          if (KS != xr_ks || seg != xr_seg) {
-#pragma unroll
-            for (int jj = 0; jj < kXReg; ++jj) {
-              const int c = c0 + lane + jj * kWarp;
-              if (c < c1) {
-                const float4 p0 = *reinterpret_cast<const float4*>(xs + c * 8);
-                const float4 p1 = *reinterpret_cast<const float4*>(xs + c * 8 + 4);
-                xr[jj][0] = p0.x; xr[jj][1] = p0.y; xr[jj][2] = p0.z; xr[jj][3] = p0.w;
-                xr[jj][4] = p1.x; xr[jj][5] = p1.y; xr[jj][6] = p1.z; xr[jj][7] = p1.w;
-              }
-            }
-            xr_ks = KS;
-            xr_seg = seg;
-          }
-          for (int u = 0; u < two; ++u) {
-            const uint16_t* w = tile + ((size_t)u * n + ui) * K;
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int jj = 0; jj < kXReg; jj += 2) {
-              const int c = c0 + lane + jj * kWarp;
-              if (c < c1) a0 += dot8r(*reinterpret_cast<const uint4*>(w + c * 8), xr[jj]);
-              if (jj + 1 < kXReg && c + kWarp < c1)
-                a1 += dot8r(*reinterpret_cast<const uint4*>(w + (c + kWarp) * 8), xr[jj + 1]);
-            }
-            for (int c = c0 + lane + kXReg * kWarp; c < c1; c += kWarp)  // beyond the registers
-              a0 += dot8(*reinterpret_cast<const uint4*>(w + c * 8), xs + c * 8);
-            acc[u][0] = warp_sum(a0 + a1);
-          }
-        } else if (active) {
-          const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
-          for (int u = 0; u < two; ++u) {
-            const uint16_t* w = tile + ((size_t)u * n + ui) * K;
-            float acc2[BT];
-#pragma unroll
-            for (int b = 0; b < BT; ++b) acc2[b] = 0.f;
-            int c = c0 + lane;
-            for (; c + kWarp < c1; c += 2 * kWarp) {  // two independent chains
-              const uint4 w0 = *reinterpret_cast<const uint4*>(w + c * 8);
-              const uint4 w1 = *reinterpret_cast<const uint4*>(w + (c + kWarp) * 8);
-#pragma unroll
-              for (int b = 0; b < BT; ++b) {
-                acc[u][b] += dot8(w0, xs + b * K + c * 8);
-                acc2[b] += dot8(w1, xs + b * K + (c + kWarp) * 8);
-              }
-            }
-            if (c < c1) {
-              const uint4 w0 = *reinterpret_cast<const uint4*>(w + c * 8);
-#pragma unroll
-              for (int b = 0; b < BT; ++b) acc[u][b] += dot8(w0, xs + b * K + c * 8);
-            }
-#pragma unroll
-            for (int b = 0; b < BT; ++b) acc[u][b] = warp_sum(acc[u][b] + acc2[b]);
+        for (int u = 0; u < kUnitsPerWarp; ++u) {
+          const int it = cw + u * kPConsumerWarps;
+          if (it >= items) break;  // uniform across the warp
+          if (xreg) {
+            const uint16_t* w0 = tile + (size_t)it * K;
+            v[2 * u] = row_dot_xreg(w0, xr, C, lane);
+            if (two == 2) v[2 * u + 1] = row_dot_xreg(w0 + ms, xr, C, lane);
+          } else {
+            const int ui = it / KS, seg = it % KS;
+            const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
+            const uint16_t* w0 = tile + (size_t)ui * K;
+            row_dot_smem<BT>(w0, two == 2 ? w0 + ms : nullptr, xs, K, c0, c1, lane,
+                             v + 2 * u * BT);
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[s]);  // this warp is done with the slot
-        ++iter;
+        if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
+        rp.next(nslots);
+        // value i of the warp ends up in lane i * hl
+        constexpr int hl = kWarp / NV;
+        warp_sum_many<NV>(v);
+        const int i = lane / hl, b = i % BT, m = (i / BT) & 1, u = i / (2 * BT);
+        const int it = cw + u * kPConsumerWarps;
         if (KS == 1) {
-          if (active && lane < BT && lane < a.B) {
-            float v0 = acc[0][0], v1 = acc[1][0];
-#pragma unroll
-            for (int bb = 1; bb < BT; ++bb)
-              if (lane == bb) {
-                v0 = acc[0][bb];
-                v1 = acc[1][bb];
-              }
-            tile_epilogue<BT>(a, S, kind, P, r.r0, row + ui, lane, v0, v1, ep, best);
-          }
+          const float vup = __shfl_down_sync(0xFFFFFFFFu, v[0], BT * hl);  // the up partner
+          if (lane % hl == 0 && m == 0 && b < nb && it < items)
+            tile_epilogue<BT>(S, kind, po, r.r0, row + it, b, v[0], vup, ep, best);
         } else {
-          if (active && lane == 0)
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-#pragma unroll
-              for (int b = 0; b < BT; ++b) S.kred[cw][u][b] = acc[u][b];
+          if (lane % hl == 0 && it < items) S.kred[kb][it][m * BT + b] = v[0];
           consumer_sync();
           for (int t = ct; t < n * BT; t += kPConsumerThreads) {
-            const int i = t / BT, b = t % BT;
-            if (b >= a.B) continue;
+            const int ui = t / BT, bb = t % BT;
+            if (bb >= nb) continue;
             float v0 = 0.f, v1 = 0.f;
-            for (int sg = 0; sg < KS; ++sg) {
-              v0 += S.kred[i * KS + sg][0][b];
-              v1 += S.kred[i * KS + sg][1][b];
-            }
-            tile_epilogue<BT>(a, S, kind, P, r.r0, row + i, b, v0, v1, ep, best);
+#pragma unroll
+            for (int sg = 0; sg < kPConsumerWarps; ++sg)  // independent loads, one chain of adds
+              if (sg < KS) {
+                v0 += S.kred[kb][ui * KS + sg][bb];
+                v1 += S.kred[kb][ui * KS + sg][BT + bb];
+              }
+            tile_epilogue<BT>(S, kind, po, r.r0, row + ui, bb, v0, v1, ep, best);
           }
-          consumer_sync();  // kred is rewritten by the next tile
+          kb ^= 1;  // the next split tile writes the other buffer: no second barrier
         }
       }
     }
@@ -848,6 +1070,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs 
   }
   __threadfence();
   __syncthreads();
+  if (prof_cta && threadIdx.x == 0) prof_cta[2 * nph_all + 1] = global_timer();
   if (threadIdx.x == 0) S.last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
   __syncthreads();
   if (!S.last) return;
@@ -878,7 +1101,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs 
   __syncthreads();
   if (threadIdx.x == 0) {
     *a.seq = seq + 1;  // next step's epochs
-    if (a.prof) a.prof[2 * (kPhasesPerLayer * a.L + 1) + 1] = global_timer();
+    if (prof_cta) prof_cta[2 * nph_all + 1] = global_timer();
     *a.ticket = 0u;
     __threadfence();
   }
@@ -894,7 +1117,7 @@ static size_t round128(size_t x) { return (x + 127) / 128 * 128; }
 static size_t persistent_fixed_smem(int H, int qd, int F, int D, int BT) {
   size_t off = round128(sizeof(PShared));
   off = round128(off + (size_t)BT * kmax_of(H, qd, F) * 4);
-  off += sizeof(float) * (8 * D + 2 * D + 8 * kAttnMaxChunk + 3 * 8);
+  off += sizeof(float) * (8 * D + 2 * D + 2 * 8 * kAttnMaxChunk + 3 * 8);
   return round128(off);
 }
 
@@ -931,11 +1154,11 @@ cudaError_t launch_persistent(PersistArgs a, cudaStream_t s) {
   a.attn_offset = (int)round128(pshared + (size_t)BT * kmax_of(a.H, qd, a.F) * 4);
   a.ring_offset = (int)fixed;
   const size_t avail = (size_t)max_smem_optin();
-  if (fixed + (size_t)a.slot_bytes * 2 > avail) return cudaErrorInvalidConfiguration;
-  int nslots = (int)((avail - fixed) / a.slot_bytes);
-  if (nslots > kMaxSlots) nslots = kMaxSlots;
-  a.nslots = nslots;
-  const size_t smem = fixed + (size_t)nslots * a.slot_bytes;
+  if (fixed + (size_t)kPMinSlotBytes * kPSlots > avail) return cudaErrorInvalidConfiguration;
+  // the rest of shared memory as kPSlots equal slots (multiples of 128 bytes)
+  a.nslots = kPSlots;
+  a.slot_bytes = (int)(((avail - fixed) / kPSlots) / 128 * 128);
+  const size_t smem = fixed + (size_t)a.nslots * a.slot_bytes;
   if (BT == 1) return launch_b<1>(a, smem, s);
   if (BT == 2) return launch_b<2>(a, smem, s);
   return launch_b<4>(a, smem, s);
@@ -945,9 +1168,13 @@ bool persistent_supported(int H, int qd, int F, int D, int G, int B) {
   if (B < 1 || B > kPMaxBatch || (D != 64 && D != 128)) return false;
   if (G < 1 || G > 8 || G * (D / 2) > kPConsumerThreads) return false;
   if (H % 8 || qd % 8 || F % 8) return false;
-  if ((H + num_sms() - 1) / num_sms() > kPMaxRows) return false;
+  if ((G + 2) * D > kAttnWords * kPConsumerThreads) return false;
+  // rows one CTA may own: the o-proj rows go to at least half of the CTAs
+  const int grid = num_sms(), half = grid - grid / 2;
+  const long long nqkv = (long long)qd + 2LL * (qd / G);
+  if ((H + half - 1) / half > kPMaxRows || (nqkv + grid - 1) / grid > kPMaxRows) return false;
   const size_t fixed = persistent_fixed_smem(H, qd, F, D, bt_of(B));
-  return fixed + 2 * (size_t)kPSlotBytes <= (size_t)max_smem_optin();
+  return fixed + (size_t)kPMinSlotBytes * kPSlots <= (size_t)max_smem_optin();
 }
 
 }  // namespace nc

@@ -9,7 +9,8 @@ namespace nc {
 
 constexpr int kMaxSlots = 8;           // weight ring slots (shared memory)
 constexpr int kPMaxBatch = 4;          // sequences per persistent step
-constexpr int kPSlotBytes = 32 * 1024; // bytes per ring slot
+constexpr int kPSlots = 3;                // weight ring slots; they share what shared memory is left
+constexpr int kPMinSlotBytes = 32 * 1024; // smallest slot the kernel is run with
 constexpr int kPMaxCtx = 2048;         // cache capacity up to which it is chosen
 constexpr int kPMaxRows = 128;         // rows of H one CTA may own (H <= 128 * grid)
 
@@ -45,9 +46,10 @@ struct PersistArgs {
   int* status;
   unsigned long long timeout_ns;  // bound of every wait
   int grid;                       // CTAs (one per SM)
-  // Optional phase profile (null: off): CTA 0 records %globaltimer at the
-  // start of every phase (2*ph) and when its input is in (2*ph + 1); then the
-  // kernel start (2*nph) and the end of the last CTA (2*nph + 1).
+  // Optional phase profile (null: off), [grid][2 * nph + 2]: each CTA records
+  // %globaltimer at the start of every phase (2*ph) and when its input is in
+  // (2*ph + 1); then its own start (2*nph) and end (2*nph + 1; for the CTA
+  // that finishes the step, the end of the step).
   unsigned long long* prof;
   // shared-memory plan (filled by launch_persistent)
   int slot_bytes, nslots, ring_offset, xs_offset, attn_offset;

@@ -403,17 +403,19 @@ class Model:
         _check(load().nc_profile_phases(self.handle, int(enable)))
 
     def read_phase_profile(self, stream=None):
-        """Last persistent step's phase timestamps (ns): a dict with 'start'
-        [5L+1], 'input' [5L+1] (input arrived), 'kernel_start', 'kernel_end'."""
+        """Last persistent step's phase timestamps (ns), one row per CTA: a
+        dict of int64 tensors 'start' [ncta, 5L+1], 'input' [ncta, 5L+1]
+        (input arrived), 'cta_start' [ncta], 'cta_end' [ncta]."""
         L = self.shape.n_layers
-        cap = 2 * (5 * L + 1) + 2
+        nph = 5 * L + 1
+        ncta = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        cap = ncta * (2 * nph + 2)
         buf = (C.c_ulonglong * cap)()
         n = C.c_int()
         _check(load().nc_read_phase_profile(self.handle, _stream(stream), buf, cap, C.byref(n)))
-        v = list(buf)
-        nph = 5 * L + 1
-        return {"start": v[0:2 * nph:2], "input": v[1:2 * nph:2], "kernel_start": v[2 * nph],
-                "kernel_end": v[2 * nph + 1]}
+        v = torch.tensor(list(buf)[:n.value], dtype=torch.int64).view(-1, 2 * nph + 2)
+        return {"start": v[:, 0:2 * nph:2], "input": v[:, 1:2 * nph:2], "cta_start": v[:, 2 * nph],
+                "cta_end": v[:, 2 * nph + 1]}
 
     def device_status(self, stream=None):
         code = C.c_int()
