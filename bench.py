@@ -4,11 +4,12 @@ Default workload (N = 1): the full 24-layer Qwen2-0.5B-shaped model with
 seeded random bf16 weights, batch 1, a 32-token prompt run through the decode
 step, then greedy decoding of 64 tokens (positions 32..95) on a contiguous KV
 cache. One timed step is one decode step (all layers plus the LM head and the
-arg-max) through nc_decode_step's CUDA graph. The 64-token sequence is decoded
+arg-max) through nc_decode_step, which at this batch runs the whole step as
+one persistent cooperative kernel launch. The 64-token sequence is decoded
 repeatedly: timed step i runs at position 32 + (i mod 64), and every 64 steps
 the sequence restarts (an 8-byte host-to-device reset of token and position).
 
-Printed (rank 0, one JSON line): the contract keys plus `roofline` (dominant
+Printed (rank 0, one JSON line): the contract keys plus `roofline` (the step
 kernel vs the measured HBM copy peak), `cpu_baseline` (the CPU oracle on the
 host cores, bounded sample), `e2e` (host buffers, copies inside the timed
 region), `hbm` (algorithmic bytes per step over step time) and `clocks`.
@@ -21,6 +22,7 @@ collective on the data path; value = tokens of all ranks / max time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -224,31 +226,26 @@ def run_reference(args, ws, rank):
 
 
 # ---------------------------------------------------------------- our arm
-def time_kernel_gu(shape, wd, reps=48):
-    """Average duration of the gate|up + SiLU GEMV (nc_swiglu_gemv) at the
-    model's shape, cycling over the 24 layers' distinct weights so every launch
-    streams its 17.4 MB from HBM. Returns (avg_seconds, bytes_per_launch)."""
-    H, F = shape.hidden, shape.ffn
-    mats = [torch.cat([lw["wg"], lw["wu"]]).contiguous() for lw in wd["layers"]]
-    gam = [lw["g_mlp"] for lw in wd["layers"]]
-    x = torch.randn(1, H, device="cuda")
-    h = torch.empty(1, F, device="cuda")
-    st = torch.cuda.current_stream()
-    for i in range(len(mats)):
-        nc.swiglu_gemv(x, gam[i], shape.rms_eps, mats[i], h)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(reps)]
-    torch.cuda.synchronize()
-    for r in range(reps):
-        i = r % len(mats)
-        evs[r][0].record(st)
-        nc.swiglu_gemv(x, gam[i], shape.rms_eps, mats[i], h)
-        evs[r][1].record(st)
-    torch.cuda.synchronize()
-    avg = sum(a.elapsed_time(b) for a, b in evs) / reps / 1e3
-    nbytes = 2 * F * H * 2 + H * 4 + H * 2 + F * 4
-    del mats
-    return avg, nbytes
+PERSISTENT_SRC = os.path.join(ROOT, "transformer_decode_gb300", "csrc", "persistent.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_decode_persistent_qwen2_0p5b_b1_dram.md")
+
+
+def counted_traffic():
+    """DRAM bytes per launch of the step kernel from the committed ncu summary
+    (dram__bytes_read.sum + dram__bytes_write.sum of one capture of this
+    workload), or None when there is none or the kernel source changed since
+    (the summary records the source's sha256)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    fields = {}
+    for line in open(TRAFFIC_FILE):
+        if ":" in line and line.strip().startswith(("source_sha256", "dram_bytes_per_launch")):
+            k, v = line.strip().split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    src = hashlib.sha256(open(PERSISTENT_SRC, "rb").read()).hexdigest()
+    if fields.get("source_sha256") != src or "dram_bytes_per_launch" not in fields:
+        return None
+    return float(fields["dram_bytes_per_launch"])
 
 
 def run_nc(args, ws, rank, local):
@@ -348,9 +345,13 @@ def run_nc(args, ws, rank, local):
     t_e2e = max_over_ranks(ws, time.perf_counter() - t0)
     e2e_value = ws * B * k_e2e / t_e2e
 
-    # ---- dominant kernel, timed alone with CUDA events on its stream
-    dur, kbytes = time_kernel_gu(shape, wd)
-    achieved = kbytes / dur / 1e9
+    # ---- the step kernel: one launch per timed step, so its average launch
+    # duration is the timed region over the steps (CUDA events on its stream;
+    # the region holds only these launches and the 8-byte cycle resets)
+    path = model.decode_path(B, kv)
+    launches_per_step = 1 if path == "persistent" else 2 + 7 * shape.n_layers
+    dur = el / args.steps
+    achieved = bytes_avg / dur / 1e9
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -372,21 +373,26 @@ def run_nc(args, ws, rank, local):
                        "positions": f"cycles of {cycle} steps at positions {n_prompt - 1}.."
                                     f"{n_prompt + n_gen - 1} ({restarts} cycles timed)",
                        "weights": "bf16 seeded N(0,0.02) stand-in, fp32 accumulate",
-                       "kv": "contiguous fp32", "path": "nc_decode_step CUDA graph",
+                       "kv": "contiguous fp32",
+                       "path": ("nc_decode_step: one persistent cooperative launch per step"
+                                if path == "persistent" else "nc_decode_step: stage kernels, CUDA graph"),
                        "l2": "inputs larger than L2: 988 MB of weights stream every step",
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
             "hbm": {"bytes_per_step": bytes_avg, "gbs": hbm_gbs,
                     "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
                     "frac_of_measured_copy": hbm_gbs / peak, "peak_kind": peak_kind},
-            "roofline": {"bound": "hbm", "kernel": "k_gemv<1,SwiGLU> (gate|up + SiLU, 4864x2 rows x 896)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("k_decode_persistent<1,64,fp32 KV> (the whole step)"
+                                    if path == "persistent" else "stage kernels (whole step)"),
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak,
+                         "traffic": counted_traffic() if path == "persistent" else None,
                          "peak_kind": peak_kind, "avg_launch_us": dur * 1e6,
-                         "algorithmic_bytes_per_launch": kbytes},
+                         "algorithmic_bytes_per_launch": bytes_avg},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": k_e2e,
                     "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
-            "gpu_launches": args.steps * (2 + 7 * shape.n_layers),
+            "gpu_launches": args.steps * launches_per_step,
             "clocks": sampler.summary(w0, w1),
         }
         print(json.dumps(line), flush=True)

@@ -172,6 +172,15 @@ nc_status nc_block_forward(nc_model* m, int layer, int batch, float* x_dev,
  * reads the word and clears it. */
 nc_status nc_get_device_status(nc_model* m, void* stream, int* code);
 
+/* Which implementation nc_decode_step runs for these arguments (nothing is
+ * launched): NC_PATH_PERSISTENT, the whole step as one cooperative
+ * persistent kernel (bf16 weights, batch <= 4, cache capacity <= 2048, shape
+ * within its shared-memory plan, NC_STEP_STAGED not set), else
+ * NC_PATH_STAGED, the per-stage kernels (2 + 7 per layer launches, in a CUDA
+ * graph with NC_STEP_GRAPH). */
+typedef enum { NC_PATH_STAGED = 0, NC_PATH_PERSISTENT = 1 } nc_path;
+nc_status nc_decode_path(nc_model* m, int batch, const nc_kv_cache* kv, int flags, int* path);
+
 /* Phase profile of the persistent decode kernel (a per-phase step profile in
  * the spirit of nanocompile's per-primitive profile of one step). While
  * enabled, every persistent step records %globaltimer (ns) in each CTA at the

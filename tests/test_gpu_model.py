@@ -150,6 +150,23 @@ def test_decode_tiny(shape, path):
                     staged=path != "persistent")
 
 
+def test_decode_path_dispatch():
+    """nc_decode_path reports the implementation a step would run: the
+    persistent kernel up to batch 4 and cache capacity 2048, else the stage
+    kernels; NC_STEP_STAGED forces the latter."""
+    shape = synth.TINY
+    wd, _ = weights_both(shape)
+    model = nc.Model(shape, wd, max_batch=8, max_ctx=4096)
+    small = nc.KVCache(shape, 8, max_ctx=64)
+    big = nc.KVCache(shape, 1, max_ctx=4096)
+    assert model.decode_path(1, small) == "persistent"
+    assert model.decode_path(4, small) == "persistent"
+    assert model.decode_path(5, small) == "staged"
+    assert model.decode_path(1, small, staged=True) == "staged"
+    assert model.decode_path(1, big) == "staged"
+    model.close()
+
+
 @pytest.mark.parametrize("batch", [2, 4])
 def test_decode_tiny_persistent_batch(batch):
     """The persistent kernel at batch 2 and 4, mixed positions."""

@@ -122,6 +122,14 @@ nc_status nc_get_device_status(nc_model* m, void* stream, int* code) {
   return NC_OK;
 }
 
+nc_status nc_decode_path(nc_model* m, int batch, const nc_kv_cache* kv, int flags, int* path) {
+  NC_CHECK(m && kv && path, NC_ERR_INVALID_ARGUMENT, "null argument");
+  NC_CHECK(batch >= 1 && batch <= M(m)->max_batch, NC_ERR_INVALID_ARGUMENT,
+           "batch %d outside [1, %d]", batch, M(m)->max_batch);
+  *path = use_persistent(M(m), batch, *kv, flags) ? NC_PATH_PERSISTENT : NC_PATH_STAGED;
+  return NC_OK;
+}
+
 nc_status nc_profile_phases(nc_model* m, int enable) {
   NC_CHECK(m, NC_ERR_INVALID_ARGUMENT, "model is NULL");
   M(m)->prof_on = enable != 0;

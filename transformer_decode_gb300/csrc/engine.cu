@@ -261,11 +261,11 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
 
 // The persistent kernel serves bf16 weights, small batches and caches short
 // enough for one CTA per (sequence, kv head) to scan.
-static bool use_persistent(const Model* m, int batch, const nc_kv_cache& kv, int flags) {
+bool use_persistent(const Model* m, int batch, const nc_kv_cache& kv, int flags) {
   const nc_config& c = m->cfg;
   return !(flags & NC_STEP_STAGED) && c.wtype == NC_BF16 && batch <= kPMaxBatch &&
          kv_capacity(kv) <= kPMaxCtx &&
-         persistent_supported(c.hidden, c.n_q_heads * c.head_dim, c.ffn, c.head_dim,
+         persistent_supported(c.n_layers, c.hidden, c.n_q_heads * c.head_dim, c.ffn, c.head_dim,
                               c.n_q_heads / c.n_kv_heads, batch);
 }
 

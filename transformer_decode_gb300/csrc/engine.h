@@ -64,6 +64,8 @@ nc_status validate_kv(const Model* m, int batch, const int32_t* positions_host,
 nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
                       const int32_t* positions_host, const nc_kv_cache* kv, float* logits,
                       int32_t* next, int flags, cudaStream_t s);
+// True when a decode step with these arguments runs as the persistent kernel.
+bool use_persistent(const Model* m, int batch, const nc_kv_cache& kv, int flags);
 nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t* positions,
                         const int32_t* positions_host, const nc_kv_cache* kv, cudaStream_t s);
 

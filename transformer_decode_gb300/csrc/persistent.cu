@@ -76,6 +76,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// 16-byte asynchronous copy global -> shared (L2, not L1: the words may have
+// been written by other SMs); completion by cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ uint64_t global_timer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -91,8 +101,24 @@ __device__ __forceinline__ void st_word(uint64_t* p, float v, uint32_t epoch) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
 
+// Rows of one phase given to a CTA and the tile shape used to stream them.
+struct Rows {
+  int r0, r1, R;          // rows [r0, r1), R rows per tile
+  int K;                  // elements per row
+  const uint16_t* m0;     // matrix (gate block for gate|up)
+  const uint16_t* m1;     // up block, or null
+};
+
 // ------------------------------------------------------------------ shared state
 struct PShared {
+  // residual words (value, epoch) of the rows the o-proj/down epilogue adds
+  // to, from row r0 rounded down to even; raw bf16 QKV bias of this CTA's
+  // rows, from r0 rounded down to a multiple of 8 (both copied 16 bytes at a
+  // time while the phase input is polled)
+  alignas(16) uint64_t xoldw[kPMaxBatch][kPMaxRows + 2];
+  alignas(16) uint16_t biasr[kPMaxRows + 16];
+  PLayer layers[kPMaxLayers];  // per-layer pointers, read once per step
+  Rows rows[kHEAD + 1];        // this CTA's rows and tile shape per phase kind
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
   int abort;        // set once a bounded wait expired in this CTA
@@ -102,8 +128,6 @@ struct PShared {
   float rn[kPMaxBatch];
   float red[kPConsumerWarps][kPMaxBatch];
   unsigned long long best[kPConsumerWarps][kPMaxBatch];
-  float xold[kPMaxBatch][kPMaxRows];  // residual rows the o-proj/down epilogue adds to
-  float bias[kPMaxRows];              // QKV bias of this CTA's rows
   float kred[2][kUnitsPerWarp * kPConsumerWarps][2 * kPMaxBatch];  // k-segment partials, 2 buffers
   bool last;
 };
@@ -135,28 +159,48 @@ __device__ __forceinline__ float ll_get(const uint64_t* p, uint32_t epoch, Spin&
   return __uint_as_float(static_cast<uint32_t>(w));
 }
 
-// Read `count` words p[0], p[stride], ... (count <= kLLBatch) with all loads
-// in flight at once, then re-poll only the words whose epoch is stale.
+// Words w[u] = *addr[u] (u < count) were loaded once; re-load, in rounds
+// with every stale word's load in flight together, until all carry `epoch`.
+// One round costs one memory round trip however many words are stale (a
+// word-by-word re-poll would pay one per word). On expiry the stale words
+// read as 0.
+template <int N>
+__device__ __forceinline__ void ll_settle(const uint64_t* const (&addr)[N], int count,
+                                          uint32_t epoch, uint64_t (&w)[N], Spin& sp) {
+  for (int round = 1;; ++round) {
+    bool stale = false;
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+      if (u < count && static_cast<uint32_t>(w[u] >> 32) != epoch) stale = true;
+    if (!stale) return;
+    if ((round & 15) == 0 && sp.expired()) {
+#pragma unroll
+      for (int u = 0; u < N; ++u)
+        if (u < count && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = 0;
+      return;
+    }
+#pragma unroll
+    for (int u = 0; u < N; ++u)
+      if (u < count && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = ld_word(addr[u]);
+  }
+}
+
+// Read `count` words p[0], p[stride], ... (count <= kLLBatch): all loads in
+// flight at once, then settle the stale ones.
 constexpr int kLLBatch = 16;
 __device__ __forceinline__ void ll_get_batch(const uint64_t* p, int stride, int count,
                                              uint32_t epoch, float* out, Spin& sp) {
   uint64_t w[kLLBatch];
-#pragma unroll
-  for (int u = 0; u < kLLBatch; ++u)
-    if (u < count) w[u] = ld_word(p + (size_t)u * stride);
+  const uint64_t* addr[kLLBatch];
 #pragma unroll
   for (int u = 0; u < kLLBatch; ++u) {
-    if (u >= count) break;
-    int n = 0;
-    while (static_cast<uint32_t>(w[u] >> 32) != epoch) {
-      if ((++n & 63) == 0 && sp.expired()) {
-        w[u] = 0;
-        break;
-      }
-      w[u] = ld_word(p + (size_t)u * stride);
-    }
-    out[u] = __uint_as_float(static_cast<uint32_t>(w[u]));
+    addr[u] = p + (size_t)u * stride;
+    if (u < count) w[u] = ld_word(addr[u]);
   }
+  ll_settle<kLLBatch>(addr, count, epoch, w, sp);
+#pragma unroll
+  for (int u = 0; u < kLLBatch; ++u)
+    if (u < count) out[u] = __uint_as_float(static_cast<uint32_t>(w[u]));
 }
 
 __device__ __forceinline__ uint32_t epoch_of(uint32_t seq, int phase) {
@@ -193,47 +237,31 @@ __host__ __device__ __forceinline__ int attn_ctas(const PersistArgs& a, int grid
   return items < grid / 2 ? items : 0;
 }
 
-// Rows of phase `ph` given to CTA `cta` and the tile shape used to stream them.
-struct Rows {
-  int r0, r1, R;          // rows [r0, r1), R rows per tile
-  int K;                  // elements per row
-  const uint16_t* m0;     // matrix (gate block for gate|up)
-  const uint16_t* m1;     // up block, or null
-};
-
-__device__ __forceinline__ Rows phase_rows(const PersistArgs& a, int ph, int cta, int grid,
-                                           int slot_bytes) {
+// The row range and tile shape of one phase kind for CTA `cta` (the same in
+// every layer); the matrix pointers are left null.
+__device__ Rows kind_rows(const PersistArgs& a, int kind, int cta, int grid, int slot_bytes) {
   Rows r{0, 0, 1, 0, nullptr, nullptr};
   int N = 0;
-  if (ph == kPhasesPerLayer * a.L) {
-    N = a.V;
-    r.K = a.H;
-    r.m0 = a.head;
-  } else {
-    const PLayer& P = a.layers[ph / kPhasesPerLayer];
-    switch (ph % kPhasesPerLayer) {
-      case kQKV: N = a.nqkv; r.K = a.H; r.m0 = P.w_qkv; break;
-      case kOPROJ: N = a.H; r.K = a.Hq * a.D; r.m0 = P.w_o; break;
-      case kGU:
-        N = a.F; r.K = a.H; r.m0 = P.w_gu; r.m1 = P.w_gu + (size_t)a.F * a.H; break;
-      case kDOWN: N = a.H; r.K = a.F; r.m0 = P.w_d; break;
-      default: return r;  // attention streams no weights
-    }
+  bool pair = false;
+  switch (kind) {
+    case kQKV: N = a.nqkv; r.K = a.H; break;
+    case kOPROJ: N = a.H; r.K = a.Hq * a.D; break;
+    case kGU: N = a.F; r.K = a.H; pair = true; break;
+    case kDOWN: N = a.H; r.K = a.F; break;
+    case kHEAD: N = a.V; r.K = a.H; break;
+    default: return r;  // attention streams no weights
   }
-  if (ph < kPhasesPerLayer * a.L && ph % kPhasesPerLayer == kOPROJ) {
+  if (kind == kOPROJ) {
     // the CTAs that ran the attention items come out of it last: the o-proj
     // rows go to the others, which are idle meanwhile
     const int na = attn_ctas(a, grid);
-    if (cta < na) {
-      r.r0 = r.r1 = 0;
-      return r;
-    }
+    if (cta < na) return r;
     cta -= na;
     grid -= na;
   }
   r.r0 = (int)(((long long)cta * N) / grid);
   r.r1 = (int)(((long long)(cta + 1) * N) / grid);
-  const int row_bytes = r.K * 2 * (r.m1 ? 2 : 1);
+  const int row_bytes = r.K * 2 * (pair ? 2 : 1);
   int rmax = slot_bytes / row_bytes;
   if (rmax > kUnitsPerWarp * kPConsumerWarps) rmax = kUnitsPerWarp * kPConsumerWarps;
   if (rmax < 1) rmax = 1;
@@ -241,6 +269,27 @@ __device__ __forceinline__ Rows phase_rows(const PersistArgs& a, int ph, int cta
   const int nr = r.r1 - r.r0;
   const int nt = nr > 0 ? (nr + rmax - 1) / rmax : 1;
   r.R = nr > 0 ? (nr + nt - 1) / nt : 1;
+  return r;
+}
+
+// Rows of phase `ph` for this CTA: the per-kind shape computed once per step
+// (kept in shared memory) plus this layer's matrices.
+__device__ __forceinline__ Rows phase_rows(const PersistArgs& a, const PShared& S, int ph) {
+  const int L = a.L;
+  const int kind = ph == kPhasesPerLayer * L ? kHEAD : ph % kPhasesPerLayer;
+  Rows r = S.rows[kind];
+  if (kind == kHEAD) {
+    r.m0 = a.head;
+  } else {
+    const PLayer& P = S.layers[ph / kPhasesPerLayer];
+    switch (kind) {
+      case kQKV: r.m0 = P.w_qkv; break;
+      case kOPROJ: r.m0 = P.w_o; break;
+      case kGU: r.m0 = P.w_gu; r.m1 = P.w_gu + (size_t)a.F * a.H; break;
+      case kDOWN: r.m0 = P.w_d; break;
+      default: break;
+    }
+  }
   return r;
 }
 
@@ -266,7 +315,7 @@ __device__ void producer(const PersistArgs& a, PShared& S, char* ring, int slot_
       }
       continue;
     }
-    const Rows r = phase_rows(a, ph, blockIdx.x, gridDim.x, slot_bytes);
+    const Rows r = phase_rows(a, S, ph);
     for (int row = r.r0; row < r.r1; row += r.R) {
       const int n = min(r.R, r.r1 - row);
       const int s = rp.s;
@@ -312,9 +361,8 @@ __device__ __forceinline__ int xs_at(int i, int n) {
 
 // Gather the phase input [B][n] from epoch-tagged words into xs (fp32);
 // with gamma, also compute the RMSNorm factor per sequence and scale xs.
-// The gains of this thread's elements are fetched before the words are
-// polled, so their round trip overlaps the wait for the previous phase.
-constexpr int kGainRegs = 16;  // per thread: RMSNorm inputs up to 16 * 352 = 5632 wide
+// The gains are copied asynchronously before the words are polled, so their
+// round trip overlaps the wait for the previous phase.
 template <int BT>
 __device__ __noinline__ void gather_input(const PersistArgs& a, const uint64_t* src, int n,
                                           uint32_t epoch, const uint16_t* embed_rows,
@@ -324,17 +372,16 @@ __device__ __noinline__ void gather_input(const PersistArgs& a, const uint64_t* 
   extern __shared__ __align__(128) char smem[];
   PShared& S = *reinterpret_cast<PShared*>(smem);
   float* xs = reinterpret_cast<float*>(smem + a.xs_offset);
+  // the gains go to the attention scratch (idle during a projection phase),
+  // copied asynchronously while the input words are polled
+  uint16_t* gs = reinterpret_cast<uint16_t*>(smem + a.attn_offset);
   const int nb = a.B;
   const float eps = a.eps;
   const int ct = threadIdx.x - kWarp, warp = ct / kWarp, lane = ct % kWarp;
-  float gr[kGainRegs];
-  const bool gain_regs = gamma && n <= kGainRegs * kPConsumerThreads;
-  if (gain_regs) {
-#pragma unroll
-    for (int u = 0; u < kGainRegs; ++u) {
-      const int i = ct + u * kPConsumerThreads;
-      gr[u] = i < n ? bf16_to_f32(gamma[i]) : 0.f;
-    }
+  const bool gain_smem = gamma && n * 2 <= a.attn_bytes;
+  if (gain_smem) {
+    for (int c = ct; c < n / 8; c += kPConsumerThreads) cp_async16(gs + 8 * c, gamma + 8 * c);
+    cp_async_commit();
   }
 #pragma unroll 1
   for (int b = 0; b < BT; ++b) {
@@ -365,36 +412,26 @@ __device__ __noinline__ void gather_input(const PersistArgs& a, const uint64_t* 
       if (lane == 0) S.red[warp][b] = ss;
     }
   }
-  if (!gamma) {
-    consumer_sync();
-    return;
-  }
+  // this thread's asynchronous copies (the caller's too) have landed; the
+  // barrier makes everyone's visible
+  cp_async_wait_all();
   consumer_sync();
-  if (ct < BT) {
+  if (!gamma) return;
+  // every thread forms the norm factors itself: no single-thread step and no
+  // second barrier before the scaling
+  float rn[BT];
+#pragma unroll
+  for (int b = 0; b < BT; ++b) {
     float t = 0.f;
-    for (int w = 0; w < kPConsumerWarps; ++w) t += S.red[w][ct];
-    S.rn[ct] = 1.f / sqrtf(t / (float)n + eps);
+    for (int w = 0; w < kPConsumerWarps; ++w) t += S.red[w][b];
+    rn[b] = 1.f / sqrtf(t / (float)n + eps);
   }
-  consumer_sync();
-  if (gain_regs) {
+  for (int i = ct; i < n; i += kPConsumerThreads) {
+    const float g = bf16_to_f32(gain_smem ? gs[i] : gamma[i]);
 #pragma unroll
-    for (int u = 0; u < kGainRegs; ++u) {
-      const int i = ct + u * kPConsumerThreads;
-      if (i < n)
-#pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          float* x = xs + b * n + xs_at(i, n);
-          *x = (*x * S.rn[b]) * gr[u];
-        }
-    }
-  } else {
-    for (int i = ct; i < n; i += kPConsumerThreads) {
-      const float g = bf16_to_f32(gamma[i]);
-#pragma unroll
-      for (int b = 0; b < BT; ++b) {
-        float* x = xs + b * n + xs_at(i, n);
-        *x = (*x * S.rn[b]) * g;
-      }
+    for (int b = 0; b < BT; ++b) {
+      float* x = xs + b * n + xs_at(i, n);
+      *x = (*x * rn[b]) * g;
     }
   }
   consumer_sync();
@@ -422,20 +459,51 @@ __device__ __forceinline__ float dot8r(const uint4& w, const float (&x)[8]) {
   return s;
 }
 
-// One row of a tile times the input held in registers (the lane's chunks
-// lane, lane + 32, ...): the per-lane partial of the row's dot product.
-__device__ __forceinline__ float row_dot_xreg(const uint16_t* w, const float (&xr)[kXReg][8],
-                                              int C, int lane) {
-  float p[kXReg];
+// U <= 4 units of a tile (rows cw, cw + W, ... from w0; with PAIR also their up
+// rows, ms elements further) times the input held in registers (the lane's
+// chunks lane, lane + 32, ...): per-lane partials into v[2 u + m]. All loads of
+// one chunk position are independent, so the U (x 2) chains run side by side.
+template <bool PAIR>
+__device__ __forceinline__ void units_xreg(const uint16_t* w0, int U, int K, size_t ms,
+                                           const float (&xr)[kXReg][8], int C, int lane,
+                                           float (&v)[2 * kUnitsPerWarp]) {
 #pragma unroll
   for (int jj = 0; jj < kXReg; ++jj) {
     const int c = lane + jj * kWarp;
-    p[jj] = c < C ? dot8r(*reinterpret_cast<const uint4*>(w + c * 8), xr[jj]) : 0.f;
-  }
-  float s = p[0];
+    if (c < C) {
 #pragma unroll
-  for (int jj = 1; jj < kXReg; ++jj) s += p[jj];
-  return s;
+      for (int u = 0; u < kUnitsPerWarp; ++u) {
+        if (u < U) {
+          const uint16_t* w = w0 + (size_t)u * kPConsumerWarps * K + c * 8;
+          v[2 * u] += dot8r(*reinterpret_cast<const uint4*>(w), xr[jj]);
+          if (PAIR) v[2 * u + 1] += dot8r(*reinterpret_cast<const uint4*>(w + ms), xr[jj]);
+        }
+      }
+    }
+  }
+}
+
+// Chunks [c0, c1) of NR <= 8 rows of a tile (row r = unit r / two, matrix r % two;
+// units from w0, up rows ms elements further) times the input in shared
+// memory: per-lane partials into o[r]. The input chunk is loaded once for all
+// NR rows.
+__device__ __forceinline__ void seg_rows(const uint16_t* w0, int NR, int K, size_t ms, int two,
+                                         const float* xs, int c0, int c1, int lane,
+                                         float (&o)[8]) {
+  const uint16_t* wr[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) wr[r] = w0 + (size_t)(r / two) * K + (r % two) * ms;
+#pragma unroll 2
+  for (int c = c0 + lane; c < c1; c += kWarp) {
+    float xb[8];
+    const float4 p0 = *reinterpret_cast<const float4*>(xs + c * 4);
+    const float4 p1 = *reinterpret_cast<const float4*>(xs + K / 2 + c * 4);
+    xb[0] = p0.x; xb[1] = p0.y; xb[2] = p0.z; xb[3] = p0.w;
+    xb[4] = p1.x; xb[5] = p1.y; xb[6] = p1.z; xb[7] = p1.w;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < NR) o[r] += dot8r(*reinterpret_cast<const uint4*>(wr[r] + c * 8), xb);
+  }
 }
 
 // Chunks [c0, c1) of one row (and of its up row when w1 is set) times the
@@ -491,6 +559,9 @@ struct PhaseOut {
   uint64_t* words;  // epoch-tagged outputs [B][stride] (QKV, residual, SiLU * up)
   float* logits;    // [B][stride] (LM head)
   int stride;
+  int base;         // first row held in xoldw / biasr
+  uint32_t ep_old;  // epoch of the residual words the o-proj/down epilogue adds to
+  bool bias;        // QKV bias present
 };
 
 // Epilogue of output row j of sequence b on the reducing thread: bias, the
@@ -498,11 +569,20 @@ struct PhaseOut {
 template <int BT>
 __device__ __forceinline__ void tile_epilogue(const PShared& S, int kind, const PhaseOut& po,
                                               int r0, int j, int b, float v0, float v1,
-                                              uint32_t ep, unsigned long long (&best)[BT]) {
+                                              uint32_t ep, unsigned long long (&best)[BT],
+                                              Spin& sp) {
   if (kind == kQKV) {
-    st_word(po.words + (size_t)b * po.stride + j, v0 + S.bias[j - r0], ep);
+    const float bias = po.bias ? bf16_to_f32(S.biasr[j - po.base]) : 0.f;
+    st_word(po.words + (size_t)b * po.stride + j, v0 + bias, ep);
   } else if (kind == kOPROJ || kind == kDOWN) {
-    st_word(po.words + (size_t)b * po.stride + j, S.xold[b][j - r0] + v0, ep);
+    uint64_t* dst = po.words + (size_t)b * po.stride + j;
+    const uint64_t w = S.xoldw[b][j - po.base];
+    // complete before this phase began (its readers checked), so the epoch
+    // matches; a mismatch falls back to polling the word
+    const float old = static_cast<uint32_t>(w >> 32) == po.ep_old
+                          ? __uint_as_float(static_cast<uint32_t>(w))
+                          : ll_get(dst, po.ep_old, sp);
+    st_word(dst, old + v0, ep);
   } else if (kind == kGU) {
     st_word(po.words + (size_t)b * po.stride + j, silu_mul_p(v0, v1), ep);
   } else {
@@ -628,7 +708,7 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   float* mrun = sc + 2 * GM * kAttnMaxChunk;  // [GM] running max
   float* lrun = mrun + GM;                    // [GM] running sum
   float* resc = lrun + GM;                    // [GM] rescale of the chunk
-  const PLayer& P = a.layers[layer];
+  const PLayer& P = S.layers[layer];
 
   // gather the G query heads, k and v of this group: all loads in flight
   // first; while they are out, fetch what does not depend on them (the
@@ -638,14 +718,15 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   const uint64_t* qkv = a.qkvw + (size_t)b * a.nqkv;
   const int total = (G + 2) * D;
   uint64_t w[kAttnWords];
-  int src[kAttnWords];
+  const uint64_t* addr[kAttnWords];
+  const int nw = total > ct ? (total - ct + kPConsumerThreads - 1) / kPConsumerThreads : 0;
 #pragma unroll
   for (int u = 0; u < kAttnWords; ++u) {
     const int i = ct + u * kPConsumerThreads;
     const int h = i / D, d = i % D;
-    src[u] = h < G ? (g * G + h) * D + d
-                   : (h == G ? (Hq + g) * D + d : (Hq + Hkv + g) * D + d);
-    if (i < total) w[u] = ld_word(qkv + src[u]);
+    addr[u] = qkv + (h < G ? (g * G + h) * D + d
+                           : (h == G ? (Hq + g) * D + d : (Hq + Hkv + g) * D + d));
+    if (u < nw) w[u] = ld_word(addr[u]);
   }
   const float* inv_freq = a.inv_freq;
   float cs[E / 2], sn[E / 2];
@@ -662,19 +743,12 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     gain_q[j] = gq ? bf16_to_f32(gq[lane + 32 * j]) : 1.f;
     gain_k[j] = gk ? bf16_to_f32(gk[lane + 32 * j]) : 1.f;
   }
+  ll_settle<kAttnWords>(addr, nw, ep_qkv, w, sp);
   {
 #pragma unroll
     for (int u = 0; u < kAttnWords; ++u) {
       const int i = ct + u * kPConsumerThreads;
-      if (i >= total) break;
-      int k = 0;
-      while (static_cast<uint32_t>(w[u] >> 32) != ep_qkv) {
-        if ((++k & 63) == 0 && sp.expired()) {
-          w[u] = 0;
-          break;
-        }
-        w[u] = ld_word(qkv + src[u]);
-      }
+      if (u >= nw) break;
       float v = __uint_as_float(static_cast<uint32_t>(w[u]));
       const int h = i / D, d = i % D;
       if (h < G) {
@@ -847,7 +921,7 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
 
 // ------------------------------------------------------------------ the kernel
 template <int BT, int D, bool KV16>
-__global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs a) {
+__global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid_constant__ PersistArgs a) {
   extern __shared__ __align__(128) char smem[];
   PShared& S = *reinterpret_cast<PShared*>(smem);
   const int slot_bytes = a.slot_bytes, nslots = a.nslots;
@@ -873,6 +947,14 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs 
       t = 0;
     }
     S.tok[b] = t;
+  }
+  if (threadIdx.x < kHEAD + 1)
+    S.rows[threadIdx.x] = kind_rows(a, threadIdx.x, blockIdx.x, gridDim.x, a.slot_bytes);
+  {  // the per-layer pointer table, copied once
+    const int words = a.L * (int)(sizeof(PLayer) / sizeof(uint64_t));
+    const uint64_t* src = reinterpret_cast<const uint64_t*>(a.layers);
+    uint64_t* dst = reinterpret_cast<uint64_t*>(S.layers);
+    for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
   }
   __syncthreads();
   const uint32_t seq = *reinterpret_cast<volatile const unsigned*>(a.seq);
@@ -909,30 +991,46 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs 
         if (prof) prof[2 * ph + 1] = global_timer();
         continue;
       }
-      const Rows r = phase_rows(a, ph, blockIdx.x, gridDim.x, slot_bytes);
+      const Rows r = phase_rows(a, S, ph);
       if (r.r0 >= r.r1) continue;
       // phase input
-      const PLayer* P = kind == kHEAD ? nullptr : &a.layers[layer];
+      const PLayer* P = kind == kHEAD ? nullptr : &S.layers[layer];
       const int K = r.K;
+      PhaseOut po;
+      po.base = 0;
+      po.ep_old = 0;
+      po.bias = false;
+      // Rows this phase's epilogue needs that do not wait on the phase input
+      // are copied asynchronously now; the gather waits for them before its
+      // first barrier.
       if (kind == kOPROJ || kind == kDOWN) {
-        // The residual rows this CTA updates are older than the phase input,
-        // so reading them first overlaps their round trip with the wait.
-        const int nr = r.r1 - r.r0;
-        const uint32_t ep_old = epoch_of(seq, kind == kOPROJ ? ph - 3 : ph - 2);
-        for (int i = ct; i < nr * BT; i += kPConsumerThreads) {
-          const int b = i / nr, jr = i % nr, j = r.r0 + jr;
-          float old = 0.f;
-          if (b < a.B)
-            old = (kind == kOPROJ && layer == 0)
-                      ? bf16_to_f32(a.embed[(size_t)S.tok[b] * a.H + j])
-                      : ll_get(a.xw + (size_t)b * a.H + j, ep_old, sp);
-          S.xold[b][jr] = old;
+        // the residual rows this CTA updates: complete since an earlier phase
+        po.ep_old = epoch_of(seq, kind == kOPROJ ? ph - 3 : ph - 2);
+        po.base = r.r0 & ~1;
+        if (kind == kOPROJ && layer == 0) {
+          const int nr = r.r1 - po.base;
+          for (int i = ct; i < nr * BT; i += kPConsumerThreads) {
+            const int b = i / nr, jr = i % nr;
+            const float old = b < a.B ? bf16_to_f32(a.embed[(size_t)S.tok[b] * a.H + po.base + jr]) : 0.f;
+            S.xoldw[b][jr] = (static_cast<uint64_t>(po.ep_old) << 32) | __float_as_uint(old);
+          }
+        } else {
+          const int npair = (r.r1 - po.base + 1) / 2;
+          for (int i = ct; i < npair * BT; i += kPConsumerThreads) {
+            const int b = i / npair, q = i % npair;
+            if (b < a.B) cp_async16(&S.xoldw[b][2 * q], a.xw + (size_t)b * a.H + po.base + 2 * q);
+          }
         }
       }
+      if (kind == kQKV && P->b_qkv) {
+        po.base = r.r0 & ~7;
+        po.bias = true;
+        const int nchunk = (r.r1 - po.base + 7) / 8;
+        for (int i = ct; i < nchunk; i += kPConsumerThreads)
+          cp_async16(&S.biasr[8 * i], P->b_qkv + po.base + 8 * i);
+      }
+      cp_async_commit();
       if (kind == kQKV) {
-        const int nr = r.r1 - r.r0;  // the bias is read before the input is in
-        for (int i = ct; i < nr; i += kPConsumerThreads)
-          S.bias[i] = P->b_qkv ? bf16_to_f32(P->b_qkv[r.r0 + i]) : 0.f;
         gather_input<BT>(a, a.xw, K, epoch_of(seq, ph - 1), layer == 0 ? a.embed : nullptr,
                          P->g_attn, sp);
       } else if (kind == kOPROJ) {
@@ -946,7 +1044,6 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs 
       }
       if (prof) prof[2 * ph + 1] = global_timer();
       const int two = r.m1 ? 2 : 1;
-      PhaseOut po;
       po.words = kind == kQKV ? a.qkvw : (kind == kGU ? a.hw : a.xw);
       po.logits = a.logits;
       po.stride = kind == kQKV ? a.nqkv : (kind == kGU ? a.F : (kind == kHEAD ? a.V : a.H));
@@ -972,70 +1069,129 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(PersistArgs 
       }
       for (int row = r.r0; row < r.r1; row += r.R) {
         const int n = min(r.R, r.r1 - row);
-        // Long rows (or batch > 1, x read from shared memory) are cut into KS
-        // k-segments when the tile has few units, so the work spreads over all
-        // warps (up to kUnitsPerWarp items each); a segment keeps at least 64
-        // chunks, two per lane.
-        int KS = 1;
-        if (!xreg && n < kPConsumerWarps) {
-          KS = kUnitsPerWarp * kPConsumerWarps / n;
-          const int kmax = C / 64;
-          if (KS > kmax) KS = kmax;
-          if (KS < 1) KS = 1;
-        }
-        const int items = n * KS;  // warp cw takes items cw, cw + W, ... (at most kUnitsPerWarp)
         ring_wait(&S.full[rp.s], rp.par, sp);  // on expiry the tile is garbage; the step is failed
         const uint16_t* tile =
             reinterpret_cast<const uint16_t*>(ring + (size_t)rp.s * slot_bytes);
         const size_t ms = (size_t)n * K;  // the up rows follow the n gate rows
-        constexpr int NV = kUnitsPerWarp * 2 * BT;  // [item u][matrix m][sequence b]
-        float v[NV];
-#pragma unroll
-        for (int i = 0; i < NV; ++i) v[i] = 0.f;
-#pragma unroll
-        for (int u = 0; u < kUnitsPerWarp; ++u) {
-          const int it = cw + u * kPConsumerWarps;
-          if (it >= items) break;  // uniform across the warp
+        // How the warps share the tile:
+        //  batch 1, rows of at most 1024: warp w reduces whole units w, w + W, ...
+        //    against the input held in registers;
+        //  batch 1, longer rows: the k range is cut into W segments, warp w
+        //    reduces segment w of every unit (each input chunk loaded once for
+        //    all of them) and the partials are summed across warps;
+        //  batch > 1: units are cut into KS segments as needed, the input is
+        //    read from shared memory.
+        if constexpr (BT == 1) {
           if (xreg) {
-            const uint16_t* w0 = tile + (size_t)it * K;
-            v[2 * u] = row_dot_xreg(w0, xr, C, lane);
-            if (two == 2) v[2 * u + 1] = row_dot_xreg(w0 + ms, xr, C, lane);
+            const int U = cw < n ? (n - cw + kPConsumerWarps - 1) / kPConsumerWarps : 0;
+            float v[2 * kUnitsPerWarp];
+#pragma unroll
+            for (int i = 0; i < 2 * kUnitsPerWarp; ++i) v[i] = 0.f;
+            const uint16_t* wt = tile + (size_t)cw * K;
+            if (two == 2) units_xreg<true>(wt, U, K, ms, xr, C, lane, v);
+            else units_xreg<false>(wt, U, K, ms, xr, C, lane, v);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
+            rp.next(nslots);
+            if (U > 0) {
+              warp_sum_many<2 * kUnitsPerWarp>(v);  // value i = (unit i / 2, matrix i % 2) in lane 4 i
+              const float vup = __shfl_down_sync(0xFFFFFFFFu, v[0], 4);
+              const int i = lane / 4, u = i / 2, it = cw + u * kPConsumerWarps;
+              if (lane % 4 == 0 && (i & 1) == 0 && u < U && nb > 0)
+                tile_epilogue<BT>(S, kind, po, r.r0, row + it, 0, v[0], vup, ep, best, sp);
+            }
           } else {
+            // segment w of the k range, all units in passes of up to 8 rows
+            const int KS = C >= kPConsumerWarps * kWarp ? kPConsumerWarps : max(1, C / kWarp);
+            const int seg = cw;
+            const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
+            const int upp = 8 / two;  // units per pass
+            for (int g0 = 0; g0 < n; g0 += upp) {
+              const int nu = min(upp, n - g0), nr = nu * two;
+              float o[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o[i] = 0.f;
+              if (seg < KS) {
+                const uint16_t* wt = tile + (size_t)g0 * K;
+                seg_rows(wt, nr, K, ms, two, xs, c0, c1, lane, o);
+              }
+              if (g0 + upp >= n) {  // the slot is no longer read by this warp
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[rp.s]);
+              }
+              warp_sum_many<8>(o);  // row i of the pass in lane 4 i
+              if (lane % 4 == 0) S.kred[kb][seg][lane / 4] = seg < KS ? o[0] : 0.f;
+              consumer_sync();
+              for (int u = ct; u < nu; u += kPConsumerThreads) {
+                float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+                for (int sg = 0; sg < kPConsumerWarps; ++sg)  // independent loads, one chain of adds
+                  if (sg < KS) {
+                    v0 += S.kred[kb][sg][u * two];
+                    if (two == 2) v1 += S.kred[kb][sg][u * two + 1];
+                  }
+                if (nb > 0)
+                  tile_epilogue<BT>(S, kind, po, r.r0, row + g0 + u, 0, v0, v1, ep, best, sp);
+              }
+              kb ^= 1;  // the next pass writes the other buffer: no second barrier
+            }
+            rp.next(nslots);
+          }
+        } else {
+          // batch > 1: long rows are cut into KS k-segments when the tile has few
+          // units, so the work spreads over all warps (up to kUnitsPerWarp items
+          // each); a segment keeps at least 64 chunks, two per lane
+          int KS = 1;
+          if (n < kPConsumerWarps) {
+            KS = kUnitsPerWarp * kPConsumerWarps / n;
+            const int kmax = C / 64;
+            if (KS > kmax) KS = kmax;
+            if (KS < 1) KS = 1;
+          }
+          const int items = n * KS;  // warp cw takes items cw, cw + W, ...
+          constexpr int NV = kUnitsPerWarp * 2 * BT;  // [item u][matrix m][sequence b]
+          float v[NV];
+#pragma unroll
+          for (int i = 0; i < NV; ++i) v[i] = 0.f;
+#pragma unroll
+          for (int u = 0; u < kUnitsPerWarp; ++u) {
+            const int it = cw + u * kPConsumerWarps;
+            if (it >= items) break;  // uniform across the warp
             const int ui = it / KS, seg = it % KS;
             const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
             const uint16_t* w0 = tile + (size_t)ui * K;
             row_dot_smem<BT>(w0, two == 2 ? w0 + ms : nullptr, xs, K, c0, c1, lane,
                              v + 2 * u * BT);
           }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
-        rp.next(nslots);
-        // value i of the warp ends up in lane i * hl
-        constexpr int hl = kWarp / NV;
-        warp_sum_many<NV>(v);
-        const int i = lane / hl, b = i % BT, m = (i / BT) & 1, u = i / (2 * BT);
-        const int it = cw + u * kPConsumerWarps;
-        if (KS == 1) {
-          const float vup = __shfl_down_sync(0xFFFFFFFFu, v[0], BT * hl);  // the up partner
-          if (lane % hl == 0 && m == 0 && b < nb && it < items)
-            tile_epilogue<BT>(S, kind, po, r.r0, row + it, b, v[0], vup, ep, best);
-        } else {
-          if (lane % hl == 0 && it < items) S.kred[kb][it][m * BT + b] = v[0];
-          consumer_sync();
-          for (int t = ct; t < n * BT; t += kPConsumerThreads) {
-            const int ui = t / BT, bb = t % BT;
-            if (bb >= nb) continue;
-            float v0 = 0.f, v1 = 0.f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
+          rp.next(nslots);
+          // value i of the warp ends up in lane i * hl
+          constexpr int hl = kWarp / NV;
+          warp_sum_many<NV>(v);
+          const int i = lane / hl, b = i % BT, m = (i / BT) & 1, u = i / (2 * BT);
+          const int it = cw + u * kPConsumerWarps;
+          if (KS == 1) {
+            const float vup = __shfl_down_sync(0xFFFFFFFFu, v[0], BT * hl);  // the up partner
+            if (lane % hl == 0 && m == 0 && b < nb && it < items)
+              tile_epilogue<BT>(S, kind, po, r.r0, row + it, b, v[0], vup, ep, best, sp);
+          } else {
+            if (lane % hl == 0 && it < items) S.kred[kb][it][m * BT + b] = v[0];
+            consumer_sync();
+            for (int t = ct; t < n * BT; t += kPConsumerThreads) {
+              const int ui = t / BT, bb = t % BT;
+              if (bb >= nb) continue;
+              float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-            for (int sg = 0; sg < kPConsumerWarps; ++sg)  // independent loads, one chain of adds
-              if (sg < KS) {
-                v0 += S.kred[kb][ui * KS + sg][bb];
-                v1 += S.kred[kb][ui * KS + sg][BT + bb];
-              }
-            tile_epilogue<BT>(S, kind, po, r.r0, row + ui, bb, v0, v1, ep, best);
+              for (int sg = 0; sg < kPConsumerWarps; ++sg)  // independent loads, one chain of adds
+                if (sg < KS) {
+                  v0 += S.kred[kb][ui * KS + sg][bb];
+                  v1 += S.kred[kb][ui * KS + sg][BT + bb];
+                }
+              tile_epilogue<BT>(S, kind, po, r.r0, row + ui, bb, v0, v1, ep, best, sp);
+            }
+            kb ^= 1;  // the next split tile writes the other buffer: no second barrier
           }
-          kb ^= 1;  // the next split tile writes the other buffer: no second barrier
         }
       }
     }
@@ -1114,10 +1270,13 @@ static int bt_of(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : 4; }
 static int kmax_of(int H, int qd, int F) { return H > qd ? (H > F ? H : F) : (qd > F ? qd : F); }
 static size_t round128(size_t x) { return (x + 127) / 128 * 128; }
 
+static size_t attn_scratch_bytes(int D) {
+  return sizeof(float) * (8 * D + 2 * D + 2 * 8 * kAttnMaxChunk + 3 * 8);
+}
 static size_t persistent_fixed_smem(int H, int qd, int F, int D, int BT) {
   size_t off = round128(sizeof(PShared));
   off = round128(off + (size_t)BT * kmax_of(H, qd, F) * 4);
-  off += sizeof(float) * (8 * D + 2 * D + 2 * 8 * kAttnMaxChunk + 3 * 8);
+  off += attn_scratch_bytes(D);
   return round128(off);
 }
 
@@ -1153,6 +1312,7 @@ cudaError_t launch_persistent(PersistArgs a, cudaStream_t s) {
   a.xs_offset = (int)pshared;
   a.attn_offset = (int)round128(pshared + (size_t)BT * kmax_of(a.H, qd, a.F) * 4);
   a.ring_offset = (int)fixed;
+  a.attn_bytes = (int)attn_scratch_bytes(a.D);
   const size_t avail = (size_t)max_smem_optin();
   if (fixed + (size_t)kPMinSlotBytes * kPSlots > avail) return cudaErrorInvalidConfiguration;
   // the rest of shared memory as kPSlots equal slots (multiples of 128 bytes)
@@ -1164,8 +1324,9 @@ cudaError_t launch_persistent(PersistArgs a, cudaStream_t s) {
   return launch_b<4>(a, smem, s);
 }
 
-bool persistent_supported(int H, int qd, int F, int D, int G, int B) {
+bool persistent_supported(int L, int H, int qd, int F, int D, int G, int B) {
   if (B < 1 || B > kPMaxBatch || (D != 64 && D != 128)) return false;
+  if (L < 1 || L > kPMaxLayers) return false;
   if (G < 1 || G > 8 || G * (D / 2) > kPConsumerThreads) return false;
   if (H % 8 || qd % 8 || F % 8) return false;
   if ((G + 2) * D > kAttnWords * kPConsumerThreads) return false;

@@ -13,6 +13,7 @@ constexpr int kPSlots = 3;                // weight ring slots; they share what 
 constexpr int kPMinSlotBytes = 32 * 1024; // smallest slot the kernel is run with
 constexpr int kPMaxCtx = 2048;         // cache capacity up to which it is chosen
 constexpr int kPMaxRows = 128;         // rows of H one CTA may own (H <= 128 * grid)
+constexpr int kPMaxLayers = 64;        // layers the persistent kernel handles
 
 // Per-layer packed weights as the persistent kernel reads them.
 struct PLayer {
@@ -52,12 +53,12 @@ struct PersistArgs {
   // that finishes the step, the end of the step).
   unsigned long long* prof;
   // shared-memory plan (filled by launch_persistent)
-  int slot_bytes, nslots, ring_offset, xs_offset, attn_offset;
+  int slot_bytes, nslots, ring_offset, xs_offset, attn_offset, attn_bytes;
 };
 
 // True when the persistent kernel fits this shape (shared memory, batch,
 // head_dim, GQA group).
-bool persistent_supported(int H, int qd, int F, int D, int G, int B);
+bool persistent_supported(int L, int H, int qd, int F, int D, int G, int B);
 cudaError_t launch_persistent(PersistArgs a, cudaStream_t s);
 
 }  // namespace nc

@@ -31,7 +31,7 @@ EXPORTS = [
     "nc_model_destroy", "nc_model_memory", "nc_decode_step", "nc_block_forward",
     "nc_get_device_status", "nc_rmsnorm_gemv", "nc_gemv_residual", "nc_swiglu_gemv",
     "nc_rope_qkv", "nc_attn_decode", "nc_lm_head_argmax", "nc_quantize_weight", "nc_w8a8_gemv",
-    "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile",
+    "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile", "nc_decode_path",
 ]
 
 
@@ -115,6 +115,7 @@ def _declare(L):
     L.nc_w8a8_gemv.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
     L.nc_attn_decode_static.argtypes = [i, i, i, i, i, i, vp, vp, vp, C.POINTER(KVStruct), vp, vp]
     L.nc_profile_phases.argtypes = [vp, i]
+    L.nc_decode_path.argtypes = [vp, i, vp, i, C.POINTER(i)]
     L.nc_read_phase_profile.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), i, C.POINTER(i)]
     for n in EXPORTS:
         if n not in ("nc_status_string", "nc_last_error_message"):
@@ -362,6 +363,15 @@ class Model:
                                      _ptr(logits, torch.float32, "logits", B * self.shape.vocab),
                                      _ptr(next_tokens, torch.int32, "next_tokens"),
                                      flags, _stream(stream)))
+
+    def decode_path(self, batch, kv, staged=False):
+        """'persistent' or 'staged': the implementation nc_decode_step runs for
+        this batch and cache (nc_decode_path; nothing is launched)."""
+        s = kv.struct()
+        out = C.c_int()
+        _check(load().nc_decode_path(self.handle, batch, C.byref(s),
+                                     NC_STEP_STAGED if staged else 0, C.byref(out)))
+        return "persistent" if out.value == 1 else "staged"
 
     def block_forward(self, layer, x, positions, positions_host, kv, stream=None):
         B = x.shape[0]
