@@ -175,6 +175,16 @@ def test_decode_tiny_persistent_batch(batch):
     _greedy_compare(shape, wd, wc, None, steps=10, batch=batch, past=[0, 7, 19, 3][:batch])
 
 
+@pytest.mark.parametrize("paged", [False, True])
+def test_decode_tiny_persistent_splits(paged):
+    """Attention split over positions (scans longer than 128 positions, up to
+    four splits per sequence and kv head, merged in the o-proj gather): past
+    lengths 300, 200, 129 and 5 give 3, 2, 2 and 1 splits."""
+    shape = synth.TINY
+    wd, wc = weights_both(shape)
+    _greedy_compare(shape, wd, wc, None, steps=6, batch=4, past=[300, 200, 129, 5], paged=paged)
+
+
 def test_decode_tiny_batch_paged():
     shape = synth.TINY
     wd, wc = weights_both(shape)

@@ -164,7 +164,8 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     const size_t pb = max_batch < kPMaxBatch ? max_batch : kPMaxBatch;
     m->xw = W.take<uint64_t>(pb * H);
     m->qkvw = W.take<uint64_t>(pb * nqkv);
-    m->aw = W.take<uint64_t>(pb * qd);
+    m->aw = W.take<uint64_t>(pb * kPMaxSplits * qd);
+    m->mlw = W.take<uint64_t>(pb * kPMaxSplits * c.n_q_heads * 2);
     m->hw = W.take<uint64_t>(pb * F);
     m->pticket = W.take<unsigned int>(1);
     m->seq = W.take<unsigned int>(1);
@@ -298,6 +299,7 @@ static cudaError_t enqueue_persistent(Model* m, int batch, int32_t* tokens, int3
   a.xw = m->xw;
   a.qkvw = m->qkvw;
   a.aw = m->aw;
+  a.mlw = m->mlw;
   a.hw = m->hw;
   a.am_part = m->am_part;
   a.ticket = m->pticket;

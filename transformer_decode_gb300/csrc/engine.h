@@ -42,7 +42,7 @@ struct Model {
   int* status = nullptr;
   // persistent decode kernel: epoch-tagged hand-over words, its ticket, the
   // step sequence number and the device copy of the per-layer pointers
-  uint64_t *xw = nullptr, *qkvw = nullptr, *aw = nullptr, *hw = nullptr;
+  uint64_t *xw = nullptr, *qkvw = nullptr, *aw = nullptr, *hw = nullptr, *mlw = nullptr;
   unsigned int *pticket = nullptr, *seq = nullptr;
   PLayer* players = nullptr;
   unsigned long long* prof = nullptr;  // phase profile [2 * (5L + 1) + 2]

@@ -119,6 +119,8 @@ struct PShared {
   alignas(16) uint16_t biasr[kPMaxRows + 16];
   PLayer layers[kPMaxLayers];  // per-layer pointers, read once per step
   Rows rows[kHEAD + 1];        // this CTA's rows and tile shape per phase kind
+  int nsplit[kPMaxBatch];      // attention: position splits per sequence
+  int item0[kPMaxBatch + 1];   // attention: first item of each sequence (items = sum Hkv * splits)
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
   int abort;        // set once a bounded wait expired in this CTA
@@ -159,29 +161,29 @@ __device__ __forceinline__ float ll_get(const uint64_t* p, uint32_t epoch, Spin&
   return __uint_as_float(static_cast<uint32_t>(w));
 }
 
-// Words w[u] = *addr[u] (u < count) were loaded once; re-load, in rounds
+// Words w[u] = *addr(u) (bit u of `valid` set) were loaded once; re-load, in rounds
 // with every stale word's load in flight together, until all carry `epoch`.
 // One round costs one memory round trip however many words are stale (a
 // word-by-word re-poll would pay one per word). On expiry the stale words
 // read as 0.
-template <int N>
-__device__ __forceinline__ void ll_settle(const uint64_t* const (&addr)[N], int count,
-                                          uint32_t epoch, uint64_t (&w)[N], Spin& sp) {
+template <int N, class Addr>
+__device__ __forceinline__ void ll_settle(const Addr& addr, uint32_t valid, uint32_t epoch,
+                                          uint64_t (&w)[N], Spin& sp) {
   for (int round = 1;; ++round) {
     bool stale = false;
 #pragma unroll
     for (int u = 0; u < N; ++u)
-      if (u < count && static_cast<uint32_t>(w[u] >> 32) != epoch) stale = true;
+      if (((valid >> u) & 1u) && static_cast<uint32_t>(w[u] >> 32) != epoch) stale = true;
     if (!stale) return;
     if ((round & 15) == 0 && sp.expired()) {
 #pragma unroll
       for (int u = 0; u < N; ++u)
-        if (u < count && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = 0;
+        if (((valid >> u) & 1u) && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = 0;
       return;
     }
 #pragma unroll
     for (int u = 0; u < N; ++u)
-      if (u < count && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = ld_word(addr[u]);
+      if (((valid >> u) & 1u) && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = ld_word(addr(u));
   }
 }
 
@@ -191,13 +193,11 @@ constexpr int kLLBatch = 16;
 __device__ __forceinline__ void ll_get_batch(const uint64_t* p, int stride, int count,
                                              uint32_t epoch, float* out, Spin& sp) {
   uint64_t w[kLLBatch];
-  const uint64_t* addr[kLLBatch];
+  const auto addr = [p, stride](int u) { return p + (size_t)u * stride; };
 #pragma unroll
-  for (int u = 0; u < kLLBatch; ++u) {
-    addr[u] = p + (size_t)u * stride;
-    if (u < count) w[u] = ld_word(addr[u]);
-  }
-  ll_settle<kLLBatch>(addr, count, epoch, w, sp);
+  for (int u = 0; u < kLLBatch; ++u)
+    if (u < count) w[u] = ld_word(addr(u));
+  ll_settle<kLLBatch>(addr, (1u << count) - 1u, epoch, w, sp);
 #pragma unroll
   for (int u = 0; u < kLLBatch; ++u)
     if (u < count) out[u] = __uint_as_float(static_cast<uint32_t>(w[u]));
@@ -231,9 +231,59 @@ __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t par, Spin& sp)
 }
 
 
+// Cached positions sequence b attends to in this step (slot pos itself comes
+// from the step's own k/v): pos, or 0 when pos is outside the cache.
+__device__ __forceinline__ int cached_positions(const PersistArgs& a, int b, int pos) {
+  return a.kv.slot_ok(b, pos) ? pos : 0;
+}
+
+// Attention work plan: the cached positions of each (sequence, kv head) are
+// split into up to kPMaxSplits ranges of at least kAttnSplitMin positions,
+// each range one item on its own CTA (split-K over positions; the o-proj
+// gather merges the partial softmax states). Items of all sequences together
+// stay within half of the grid. Returns the item count.
+constexpr int kAttnSplitMin = 128;  // one chunk: shorter scans are not split
+__device__ int attn_plan(const PersistArgs& a, int grid, int (&nsplit)[kPMaxBatch],
+                         int (&item0)[kPMaxBatch + 1]) {
+  int cap = (grid / 2) / (a.B * a.Hkv);
+  if (cap > kPMaxSplits) cap = kPMaxSplits;
+  if (cap < 1) cap = 1;
+  item0[0] = 0;
+  for (int b = 0; b < kPMaxBatch; ++b) {
+    int ns = 0;
+    if (b < a.B) {
+      const int np = cached_positions(a, b, a.positions[b]);
+      ns = (np + kAttnSplitMin - 1) / kAttnSplitMin;
+      if (ns > cap) ns = cap;
+      if (ns < 1) ns = 1;
+    }
+    nsplit[b] = ns;
+    item0[b + 1] = item0[b] + a.Hkv * ns;
+  }
+  return item0[kPMaxBatch];
+}
+
+// Item `it` of the plan: sequence b, kv head g, split sp of ns, and its range
+// of cached positions [p0, p1).
+struct AttnItem {
+  int b, g, sp, ns, p0, p1;
+};
+__device__ __forceinline__ AttnItem attn_item_of(const PShared& S, int Hkv, int it) {
+  AttnItem t{0, 0, 0, 1, 0, 0};
+  int b = 0;
+  while (b + 1 < kPMaxBatch && it >= S.item0[b + 1]) ++b;
+  const int r = it - S.item0[b];
+  t.b = b;
+  t.ns = S.nsplit[b];
+  t.g = r / t.ns;
+  t.sp = r % t.ns;
+  return t;
+}
+
 // CTAs that run attention items (item i on CTA i) and hold no o-proj rows.
-__host__ __device__ __forceinline__ int attn_ctas(const PersistArgs& a, int grid) {
-  const int items = a.B * a.Hkv;
+__device__ __forceinline__ int attn_ctas(const PersistArgs& a, int grid) {
+  int ns[kPMaxBatch], i0[kPMaxBatch + 1];
+  const int items = attn_plan(a, grid, ns, i0);
   return items < grid / 2 ? items : 0;
 }
 
@@ -296,7 +346,7 @@ __device__ __forceinline__ Rows phase_rows(const PersistArgs& a, const PShared& 
 // ------------------------------------------------------------------ producer
 template <bool KV16>
 __device__ bool produce_kv(const PersistArgs& a, PShared& S, char* ring, int slot_bytes,
-                           int nslots, int layer, int b, int g, int npos, RingPos& rp,
+                           int nslots, int layer, int b, int g, int p0, int p1, RingPos& rp,
                            Spin& sp);
 
 template <bool KV16>
@@ -306,11 +356,13 @@ __device__ void producer(const PersistArgs& a, PShared& S, char* ring, int slot_
   RingPos rp;
   for (int ph = 0; ph < nph; ++ph) {
     if (ph < kPhasesPerLayer * a.L && ph % kPhasesPerLayer == kATTN) {
-      for (int it = blockIdx.x; it < a.B * a.Hkv; it += gridDim.x) {
-        const int b = it / a.Hkv, g = it % a.Hkv;
-        const int npos = a.kv.slot_ok(b, S.pos[b]) ? S.pos[b] : 0;
-        if (!produce_kv<KV16>(a, S, ring, slot_bytes, nslots, ph / kPhasesPerLayer, b, g, npos,
-                              rp, sp))
+      for (int it = blockIdx.x; it < S.item0[kPMaxBatch]; it += gridDim.x) {
+        AttnItem t = attn_item_of(S, a.Hkv, it);
+        const int np = cached_positions(a, t.b, S.pos[t.b]);
+        t.p0 = (int)(((long long)t.sp * np) / t.ns);
+        t.p1 = (int)(((long long)(t.sp + 1) * np) / t.ns);
+        if (!produce_kv<KV16>(a, S, ring, slot_bytes, nslots, ph / kPhasesPerLayer, t.b, t.g,
+                              t.p0, t.p1, rp, sp))
           return;
       }
       continue;
@@ -359,14 +411,16 @@ __device__ __forceinline__ int xs_at(int i, int n) {
   return ((i & 4) ? (n >> 1) : 0) + ((i >> 3) << 2) + (i & 3);
 }
 
-// Gather the phase input [B][n] from epoch-tagged words into xs (fp32);
+// Gather the phase input [B][n] (sequences src_stride words apart) from
+// epoch-tagged words into xs (fp32);
 // with gamma, also compute the RMSNorm factor per sequence and scale xs.
 // The gains are copied asynchronously before the words are polled, so their
 // round trip overlaps the wait for the previous phase.
 template <int BT>
 __device__ __noinline__ void gather_input(const PersistArgs& a, const uint64_t* src, int n,
-                                          uint32_t epoch, const uint16_t* embed_rows,
-                                          const uint16_t* gamma, Spin& sp) {
+                                          size_t src_stride, uint32_t epoch,
+                                          const uint16_t* embed_rows, const uint16_t* gamma,
+                                          Spin& sp) {
   // shared-memory pointers are derived from the dynamic shared array here, so
   // the compiler addresses them as shared, not generic
   extern __shared__ __align__(128) char smem[];
@@ -398,7 +452,7 @@ __device__ __noinline__ void gather_input(const PersistArgs& a, const uint64_t* 
           if (u < count)
             v[u] = bf16_to_f32(embed_rows[(size_t)S.tok[b] * n + i0 + u * kPConsumerThreads]);
       } else {
-        ll_get_batch(src + (size_t)b * n + i0, kPConsumerThreads, count, epoch, v, sp);
+        ll_get_batch(src + (size_t)b * src_stride + i0, kPConsumerThreads, count, epoch, v, sp);
       }
 #pragma unroll
       for (int u = 0; u < kLLBatch; ++u) {
@@ -437,11 +491,111 @@ __device__ __noinline__ void gather_input(const PersistArgs& a, const uint64_t* 
   consumer_sync();
 }
 
+// The o-proj input: each sequence's attention output merged over its
+// position splits with the online-softmax combine (Tang section 2.2): per
+// head M = max_s m_s, c_s = exp(m_s - M) l_s / sum_t exp(m_t - M) l_t and
+// out = sum_s c_s o_s (o_s = acc_s / l_s). One split gives c = 1 and out = o
+// exactly. A thread's output words (its elements x the splits) and one (m, l)
+// word are loaded in one round.
+constexpr int kMergeElems = 4;  // elements per thread per round (x kPMaxSplits words)
+template <int BT>
+__device__ __noinline__ void gather_attn(const PersistArgs& a, uint32_t epoch, Spin& sp) {
+  extern __shared__ __align__(128) char smem[];
+  PShared& S = *reinterpret_cast<PShared*>(smem);
+  float* xs = reinterpret_cast<float*>(smem + a.xs_offset);
+  float* mlv = reinterpret_cast<float*>(smem + a.attn_offset);  // [split][head][m, l]
+  float* coef = mlv + 2 * kPMaxSplits * kPMaxHeads;             // [head][split]
+  const int Hq = a.Hq, D = a.D, qd = Hq * D, nb = a.B;
+  const int ct = threadIdx.x - kWarp;
+  const int per = (qd + kPConsumerThreads - 1) / kPConsumerThreads;  // elements per thread
+  const int nround = (per + kMergeElems - 1) / kMergeElems;
+  constexpr int NW = kMergeElems * kPMaxSplits;
+#pragma unroll 1
+  for (int b = 0; b < BT; ++b) {
+    if (b >= nb) {
+      for (int i = ct; i < qd; i += kPConsumerThreads) xs[b * qd + xs_at(i, qd)] = 0.f;
+      continue;
+    }
+    const int ns = S.nsplit[b];
+    const uint64_t* ow = a.aw + (size_t)b * kPMaxSplits * qd;
+    const uint64_t* mw = a.mlw + (size_t)b * kPMaxSplits * Hq * 2;
+#pragma unroll 1
+    for (int rd = 0; rd < nround; ++rd) {
+      uint64_t w[NW];
+      // word u: element u / kPMaxSplits, split u % kPMaxSplits
+      const int ibase = ct + rd * kMergeElems * kPConsumerThreads;
+      const auto adr = [ow, qd, ibase](int u) {
+        return ow + (size_t)(u % kPMaxSplits) * qd + ibase + (u / kPMaxSplits) * kPConsumerThreads;
+      };
+      uint32_t valid = 0;
+#pragma unroll
+      for (int u = 0; u < NW; ++u) {
+        const int e = u / kPMaxSplits, t = u % kPMaxSplits;
+        if (t < ns && ibase + e * kPConsumerThreads < qd) {
+          valid |= 1u << u;
+          w[u] = ld_word(adr(u));
+        }
+      }
+      const bool ml_here = rd == 0 && ct < ns * Hq * 2;
+      const uint64_t* mp = mw + (ml_here ? ct : 0);
+      const auto madr = [mp](int) { return mp; };
+      uint64_t mwd[1] = {0};
+      if (ml_here) mwd[0] = ld_word(mp);
+      ll_settle<NW>(adr, valid, epoch, w, sp);
+      if (ml_here) {
+        ll_settle<1>(madr, 1u, epoch, mwd, sp);
+        mlv[ct] = __uint_as_float(static_cast<uint32_t>(mwd[0]));
+      }
+      if (rd == 0) {
+        consumer_sync();
+        if (ct < Hq) {
+          float M = -INFINITY;
+          for (int t = 0; t < ns; ++t) M = fmaxf(M, mlv[(t * Hq + ct) * 2]);
+          float wl[kPMaxSplits], L = 0.f;
+#pragma unroll
+          for (int t = 0; t < kPMaxSplits; ++t) {
+            wl[t] = 0.f;
+            if (t < ns) {
+              const float m = mlv[(t * Hq + ct) * 2], l = mlv[(t * Hq + ct) * 2 + 1];
+              wl[t] = m == -INFINITY ? 0.f : expf(m - M) * l;
+              L += wl[t];
+            }
+          }
+          // a division (not a reciprocal) so that one split gives c = l / l = 1
+#pragma unroll
+          for (int t = 0; t < kPMaxSplits; ++t) coef[ct * kPMaxSplits + t] = L > 0.f ? wl[t] / L : 0.f;
+        }
+        consumer_sync();
+      }
+#pragma unroll
+      for (int e = 0; e < kMergeElems; ++e) {
+        const int i = ct + (rd * kMergeElems + e) * kPConsumerThreads;
+        if (i < qd) {
+          const int h = i / D;
+          float out = 0.f;
+#pragma unroll
+          for (int t = 0; t < kPMaxSplits; ++t)
+            if (t < ns)
+              out = fmaf(coef[h * kPMaxSplits + t],
+                         __uint_as_float(static_cast<uint32_t>(w[e * kPMaxSplits + t])), out);
+          xs[b * qd + xs_at(i, qd)] = out;
+        }
+      }
+    }
+    consumer_sync();  // coef and mlv are rewritten for the next sequence
+  }
+  consumer_sync();  // xs complete (also the rows of absent sequences)
+}
+
 __device__ __forceinline__ float silu_mul_p(float g, float u) {
   const float e = expf(-fabsf(g));
   const float sig = g >= 0.f ? 1.f / (1.f + e) : e / (1.f + e);
   return (g * sig) * u;
 }
+
+// An empty asm with a memory clobber: the compiler moves no memory access
+// across it (scheduling only; it emits no instruction).
+__device__ __forceinline__ void compiler_fence() { asm volatile("" ::: "memory"); }
 
 // Input chunks kept in registers per lane at batch 1 (8 floats each).
 constexpr int kXReg = 4;
@@ -480,6 +634,9 @@ __device__ __forceinline__ void units_xreg(const uint16_t* w0, int U, int K, siz
         }
       }
     }
+    // one chunk position's loads at a time: keeps the compiler from hoisting
+    // all 32 of them (and their registers) to the top
+    compiler_fence();
   }
 }
 
@@ -490,9 +647,9 @@ __device__ __forceinline__ void units_xreg(const uint16_t* w0, int U, int K, siz
 __device__ __forceinline__ void seg_rows(const uint16_t* w0, int NR, int K, size_t ms, int two,
                                          const float* xs, int c0, int c1, int lane,
                                          float (&o)[8]) {
-  const uint16_t* wr[8];
+  int wr[8];  // element offsets of the rows (a tile holds well under 2^31 elements)
 #pragma unroll
-  for (int r = 0; r < 8; ++r) wr[r] = w0 + (size_t)(r / two) * K + (r % two) * ms;
+  for (int r = 0; r < 8; ++r) wr[r] = (r / two) * K + (r % two) * (int)ms;
 #pragma unroll 2
   for (int c = c0 + lane; c < c1; c += kWarp) {
     float xb[8];
@@ -502,7 +659,8 @@ __device__ __forceinline__ void seg_rows(const uint16_t* w0, int NR, int K, size
     xb[4] = p1.x; xb[5] = p1.y; xb[6] = p1.z; xb[7] = p1.w;
 #pragma unroll
     for (int r = 0; r < 8; ++r)
-      if (r < NR) o[r] += dot8r(*reinterpret_cast<const uint4*>(wr[r] + c * 8), xb);
+      if (r < NR) o[r] += dot8r(*reinterpret_cast<const uint4*>(w0 + wr[r] + c * 8), xb);
+    compiler_fence();
   }
 }
 
@@ -605,16 +763,16 @@ __host__ __device__ __forceinline__ int attn_chunk(int slot_bytes, int D, int es
   return cp < kAttnMaxChunk ? cp : kAttnMaxChunk;
 }
 
-// Producer: issue the chunk tiles of (layer, b, g) for slots [0, npos).
+// Producer: issue the chunk tiles of (layer, b, g) for cached slots [p0, p1).
 template <bool KV16>
 __device__ bool produce_kv(const PersistArgs& a, PShared& S, char* ring, int slot_bytes,
-                           int nslots, int layer, int b, int g, int npos, RingPos& rp,
+                           int nslots, int layer, int b, int g, int p0, int p1, RingPos& rp,
                            Spin& sp) {
   constexpr int ES = KV16 ? 2 : 4;
   const int D = a.D, CP = attn_chunk(slot_bytes, D, ES);
-  const int bs = a.kv.paged ? a.kv.block_size : npos;
-  for (int t0 = 0; t0 < npos; t0 += CP) {
-    const int n = min(CP, npos - t0);
+  const int bs = a.kv.paged ? a.kv.block_size : (1 << 30);
+  for (int t0 = p0; t0 < p1; t0 += CP) {
+    const int n = min(CP, p1 - t0);
     const int s = rp.s;
     if (rp.n >= (uint32_t)nslots && !ring_wait(&S.empty[s], rp.par ^ 1u, sp)) return false;
     if (*reinterpret_cast<volatile int*>(&S.abort)) return false;
@@ -674,14 +832,18 @@ __device__ __forceinline__ float2 kv_smem2(const char* base, int idx) {
   }
 }
 
-// Consumer: one (sequence b, kv head g). RoPE (+ q/k norm) of the G query
-// heads and the key, K/V append at slot pos, then the online-softmax scan:
-// the new position first, then the cached chunks from the ring.
+// Consumer: one item, i.e. split `split` of (sequence b, kv head g). RoPE
+// (+ q/k norm) of the G query heads and the key; split 0 appends K/V at slot
+// pos and opens the online-softmax state with the new position; then the scan
+// over the split's cached positions [p0, p1), in chunks from the ring. The
+// split's state leaves as its normalised output o = acc / l per (head, dim)
+// and (m, l) per head (Tang section 2.2: the partials of a split-K scan that
+// the o-proj gather merges).
 constexpr int kAttnWords = 4;  // q/k/v words gathered per thread: (G + 2) D <= 4 * 352
 template <int D, bool KV16>
-__device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int layer,
-                                            uint32_t ep_qkv, uint32_t ep_out, int nslots,
-                                            RingPos& rp, Spin& sp) {
+__device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int split,
+                                            int p0, int p1, int layer, uint32_t ep_qkv,
+                                            uint32_t ep_out, int nslots, RingPos& rp, Spin& sp) {
   // shared-memory pointers are derived from the dynamic shared array here, so
   // the compiler addresses them as shared, not generic
   extern __shared__ __align__(128) char smem[];
@@ -718,16 +880,16 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   const uint64_t* qkv = a.qkvw + (size_t)b * a.nqkv;
   const int total = (G + 2) * D;
   uint64_t w[kAttnWords];
-  const uint64_t* addr[kAttnWords];
   const int nw = total > ct ? (total - ct + kPConsumerThreads - 1) / kPConsumerThreads : 0;
-#pragma unroll
-  for (int u = 0; u < kAttnWords; ++u) {
+  const auto addr = [qkv, ct, G, g, Hq, Hkv](int u) {
     const int i = ct + u * kPConsumerThreads;
     const int h = i / D, d = i % D;
-    addr[u] = qkv + (h < G ? (g * G + h) * D + d
-                           : (h == G ? (Hq + g) * D + d : (Hq + Hkv + g) * D + d));
-    if (u < nw) w[u] = ld_word(addr[u]);
-  }
+    return qkv + (h < G ? (g * G + h) * D + d
+                        : (h == G ? (Hq + g) * D + d : (Hq + Hkv + g) * D + d));
+  };
+#pragma unroll
+  for (int u = 0; u < kAttnWords; ++u)
+    if (u < nw) w[u] = ld_word(addr(u));
   const float* inv_freq = a.inv_freq;
   float cs[E / 2], sn[E / 2];
 #pragma unroll
@@ -743,7 +905,7 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     gain_q[j] = gq ? bf16_to_f32(gq[lane + 32 * j]) : 1.f;
     gain_k[j] = gk ? bf16_to_f32(gk[lane + 32 * j]) : 1.f;
   }
-  ll_settle<kAttnWords>(addr, nw, ep_qkv, w, sp);
+  ll_settle<kAttnWords>(addr, (1u << nw) - 1u, ep_qkv, w, sp);
   {
 #pragma unroll
     for (int u = 0; u < kAttnWords; ++u) {
@@ -794,8 +956,9 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   // append K/V at slot pos; the new position opens the running state:
   // m = its score, l = 1, acc = v
   const bool pos_ok = kv.slot_ok(b, pos);
-  if (!pos_ok && ct == 0 && status) atomicCAS(status, 0, (int)NC_ERR_POSITION);
-  if (ct < D && pos_ok) {
+  const bool own_new = pos_ok && split == 0;  // the new position belongs to split 0
+  if (!pos_ok && split == 0 && ct == 0 && status) atomicCAS(status, 0, (int)NC_ERR_POSITION);
+  if (ct < D && own_new) {
     const size_t off = kv.offset(layer, b, g, pos);
     kv_store<KV16>(kv.k, off + ct, kn[ct]);
     kv_store<KV16>(kv.v, off + ct, vn[ct]);
@@ -807,22 +970,21 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     for (int j = 0; j < E; ++j) s = fmaf(qs[h * D + lane + 32 * j], kn[lane + 32 * j], s);
     s = warp_sum(s) * scale;
     if (lane == 0) {
-      mrun[h] = pos_ok ? s : -INFINITY;
-      lrun[h] = pos_ok ? 1.f : 0.f;
+      mrun[h] = own_new ? s : -INFINITY;
+      lrun[h] = own_new ? 1.f : 0.f;
     }
   }
   const int npair = G * (D / 2);
   const int my_h = ct / (D / 2), my_d2 = ct % (D / 2);
   float acc0 = 0.f, acc1 = 0.f;
-  if (ct < npair && pos_ok) {
+  if (ct < npair && own_new) {
     acc0 = vn[2 * my_d2];
     acc1 = vn[2 * my_d2 + 1];
   }
   consumer_sync();
-  const int npos = pos_ok ? pos : 0;
   int cpar = 0;
-  for (int t0 = 0; t0 < npos; t0 += CP, cpar ^= 1) {
-    const int n = min(CP, npos - t0);
+  for (int t0 = p0; t0 < p1; t0 += CP, cpar ^= 1) {
+    const int n = min(CP, p1 - t0);
     const int s = rp.s;
     ring_wait(&S.full[s], rp.par, sp);
     const char* Ks = ring + (size_t)s * slot_bytes;
@@ -910,13 +1072,282 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     // no barrier here: the next chunk writes the other score buffer, and the
     // one after it is behind that chunk's two barriers
   }
+  const size_t part = (size_t)b * kPMaxSplits + split;
   if (ct < npair) {
     const float inv = lrun[my_h] > 0.f ? 1.f / lrun[my_h] : 0.f;
-    uint64_t* out = a.aw + (size_t)b * Hq * D + (size_t)(g * G + my_h) * D + 2 * my_d2;
+    uint64_t* out = a.aw + part * Hq * D + (size_t)(g * G + my_h) * D + 2 * my_d2;
     st_word(out, acc0 * inv, ep_out);
     st_word(out + 1, acc1 * inv, ep_out);
   }
+  if (ct < G) {
+    uint64_t* ml = a.mlw + (part * Hq + g * G + ct) * 2;
+    st_word(ml, mrun[ct], ep_out);
+    st_word(ml + 1, lrun[ct], ep_out);
+  }
   consumer_sync();  // the scratch is reused by the next item
+}
+
+// The tiles of one projection phase (see gemv_phase). MODE 0: batch 1, rows of
+// at most 1024 (input in registers); 1: batch 1, longer rows (k segments
+// across warps); 2: batch > 1. Inlined: a call here would save and restore
+// the live registers of all 352 consumer threads through local memory, which
+// with ~28 KB of L1 next to the ring spills to L2 and costs a round trip.
+template <int BT, int MODE>
+__device__ __forceinline__ void gemv_tiles(const PersistArgs& a, const Rows& rin,
+                                        const PhaseOut& poin, int kind, uint32_t ep,
+                                        RingPos& rp_io, int& kb_io,
+                                        unsigned long long (&best_io)[BT], Spin& sp) {
+  extern __shared__ __align__(128) char smem[];
+  PShared& S = *reinterpret_cast<PShared*>(smem);
+  char* ring = smem + a.ring_offset;
+  float* xs = reinterpret_cast<float*>(smem + a.xs_offset);
+  const int slot_bytes = a.slot_bytes, nslots = a.nslots;
+  const int ct = threadIdx.x - kWarp, cw = ct / kWarp, lane = threadIdx.x % kWarp;
+  const Rows r = rin;
+  PhaseOut po = poin;
+  const int K = r.K;
+  RingPos rp = rp_io;
+  int kb = kb_io;
+  unsigned long long best[BT];
+#pragma unroll
+  for (int b = 0; b < BT; ++b) best[b] = best_io[b];
+  const int two = r.m1 ? 2 : 1;
+  const int nb = a.B;
+  const int C = K / 8;  // 16-byte chunks per row
+  // batch 1 and rows of at most 1024: every lane keeps its chunks of the
+  // input in registers for the whole phase, and each unit is one row (or
+  // one gate|up pair) reduced by one warp
+  const bool xreg = MODE == 0;
+  float xr[kXReg][8];
+  if (xreg) {
+#pragma unroll
+    for (int jj = 0; jj < kXReg; ++jj) {
+      const int c = lane + jj * kWarp;
+      float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
+      if (c < C) {  // two 16-byte loads, not eight scalar ones
+        p0 = *reinterpret_cast<const float4*>(xs + c * 4);
+        p1 = *reinterpret_cast<const float4*>(xs + K / 2 + c * 4);
+      }
+      xr[jj][0] = p0.x; xr[jj][1] = p0.y; xr[jj][2] = p0.z; xr[jj][3] = p0.w;
+      xr[jj][4] = p1.x; xr[jj][5] = p1.y; xr[jj][6] = p1.z; xr[jj][7] = p1.w;
+    }
+  }
+  for (int row = r.r0; row < r.r1; row += r.R) {
+    const int n = min(r.R, r.r1 - row);
+    ring_wait(&S.full[rp.s], rp.par, sp);  // on expiry the tile is garbage; the step is failed
+    const uint16_t* tile =
+        reinterpret_cast<const uint16_t*>(ring + (size_t)rp.s * slot_bytes);
+    const size_t ms = (size_t)n * K;  // the up rows follow the n gate rows
+    // How the warps share the tile:
+    //  batch 1, rows of at most 1024: warp w reduces whole units w, w + W, ...
+    //    against the input held in registers;
+    //  batch 1, longer rows: the k range is cut into W segments, warp w
+    //    reduces segment w of every unit (each input chunk loaded once for
+    //    all of them) and the partials are summed across warps;
+    //  batch > 1: units are cut into KS segments as needed, the input is
+    //    read from shared memory.
+    if constexpr (BT == 1) {
+      if (xreg) {
+        const int U = cw < n ? (n - cw + kPConsumerWarps - 1) / kPConsumerWarps : 0;
+        float v[2 * kUnitsPerWarp];
+#pragma unroll
+        for (int i = 0; i < 2 * kUnitsPerWarp; ++i) v[i] = 0.f;
+        const uint16_t* wt = tile + (size_t)cw * K;
+        if (two == 2) units_xreg<true>(wt, U, K, ms, xr, C, lane, v);
+        else units_xreg<false>(wt, U, K, ms, xr, C, lane, v);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
+        rp.next(nslots);
+        if (U > 0) {
+          warp_sum_many<2 * kUnitsPerWarp>(v);  // value i = (unit i / 2, matrix i % 2) in lane 4 i
+          const float vup = __shfl_down_sync(0xFFFFFFFFu, v[0], 4);
+          const int i = lane / 4, u = i / 2, it = cw + u * kPConsumerWarps;
+          if (lane % 4 == 0 && (i & 1) == 0 && u < U && nb > 0)
+            tile_epilogue<BT>(S, kind, po, r.r0, row + it, 0, v[0], vup, ep, best, sp);
+        }
+      } else {
+        // segment w of the k range, all units in passes of up to 8 rows
+        const int KS = C >= kPConsumerWarps * kWarp ? kPConsumerWarps : max(1, C / kWarp);
+        const int seg = cw;
+        const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
+        const int upp = 8 / two;  // units per pass
+        for (int g0 = 0; g0 < n; g0 += upp) {
+          const int nu = min(upp, n - g0), nr = nu * two;
+          float o[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] = 0.f;
+          if (seg < KS) {
+            const uint16_t* wt = tile + (size_t)g0 * K;
+            seg_rows(wt, nr, K, ms, two, xs, c0, c1, lane, o);
+          }
+          if (g0 + upp >= n) {  // the slot is no longer read by this warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[rp.s]);
+          }
+          warp_sum_many<8>(o);  // row i of the pass in lane 4 i
+          if (lane % 4 == 0) S.kred[kb][seg][lane / 4] = seg < KS ? o[0] : 0.f;
+          consumer_sync();
+          for (int u = ct; u < nu; u += kPConsumerThreads) {
+            float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+            for (int sg = 0; sg < kPConsumerWarps; ++sg)  // independent loads, one chain of adds
+              if (sg < KS) {
+                v0 += S.kred[kb][sg][u * two];
+                if (two == 2) v1 += S.kred[kb][sg][u * two + 1];
+              }
+            if (nb > 0)
+              tile_epilogue<BT>(S, kind, po, r.r0, row + g0 + u, 0, v0, v1, ep, best, sp);
+          }
+          kb ^= 1;  // the next pass writes the other buffer: no second barrier
+        }
+        rp.next(nslots);
+      }
+    } else {
+      // batch > 1: long rows are cut into KS k-segments when the tile has few
+      // units, so the work spreads over all warps (up to kUnitsPerWarp items
+      // each); a segment keeps at least 64 chunks, two per lane
+      int KS = 1;
+      if (n < kPConsumerWarps) {
+        KS = kUnitsPerWarp * kPConsumerWarps / n;
+        const int kmax = C / 64;
+        if (KS > kmax) KS = kmax;
+        if (KS < 1) KS = 1;
+      }
+      const int items = n * KS;  // warp cw takes items cw, cw + W, ...
+      constexpr int NV = kUnitsPerWarp * 2 * BT;  // [item u][matrix m][sequence b]
+      float v[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] = 0.f;
+#pragma unroll
+      for (int u = 0; u < kUnitsPerWarp; ++u) {
+        const int it = cw + u * kPConsumerWarps;
+        if (it >= items) break;  // uniform across the warp
+        const int ui = it / KS, seg = it % KS;
+        const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
+        const uint16_t* w0 = tile + (size_t)ui * K;
+        row_dot_smem<BT>(w0, two == 2 ? w0 + ms : nullptr, xs, K, c0, c1, lane,
+                         v + 2 * u * BT);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
+      rp.next(nslots);
+      // value i of the warp ends up in lane i * hl
+      constexpr int hl = kWarp / NV;
+      warp_sum_many<NV>(v);
+      const int i = lane / hl, b = i % BT, m = (i / BT) & 1, u = i / (2 * BT);
+      const int it = cw + u * kPConsumerWarps;
+      if (KS == 1) {
+        const float vup = __shfl_down_sync(0xFFFFFFFFu, v[0], BT * hl);  // the up partner
+        if (lane % hl == 0 && m == 0 && b < nb && it < items)
+          tile_epilogue<BT>(S, kind, po, r.r0, row + it, b, v[0], vup, ep, best, sp);
+      } else {
+        if (lane % hl == 0 && it < items) S.kred[kb][it][m * BT + b] = v[0];
+        consumer_sync();
+        for (int t = ct; t < n * BT; t += kPConsumerThreads) {
+          const int ui = t / BT, bb = t % BT;
+          if (bb >= nb) continue;
+          float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+          for (int sg = 0; sg < kPConsumerWarps; ++sg)  // independent loads, one chain of adds
+            if (sg < KS) {
+              v0 += S.kred[kb][ui * KS + sg][bb];
+              v1 += S.kred[kb][ui * KS + sg][BT + bb];
+            }
+          tile_epilogue<BT>(S, kind, po, r.r0, row + ui, bb, v0, v1, ep, best, sp);
+        }
+        kb ^= 1;  // the next split tile writes the other buffer: no second barrier
+      }
+    }
+  }
+  rp_io = rp;
+  kb_io = kb;
+#pragma unroll
+  for (int b = 0; b < BT; ++b) best_io[b] = best[b];
+}
+
+// One projection phase (QKV, o-proj, gate|up, down or the LM head) on the
+// consumer warps: the epilogue's asynchronous prefetches, the input gather
+// (out of line) and the tiles (per mode). The ring position, the
+// split-buffer parity and the arg-max keys are carried in and out.
+template <int BT>
+__device__ __forceinline__ void gemv_phase(const PersistArgs& a, int ph, uint32_t seq,
+                                           RingPos& rp_io, int& kb_io,
+                                           unsigned long long (&best_io)[BT],
+                                           unsigned long long* prof, Spin& sp) {
+  extern __shared__ __align__(128) char smem[];
+  PShared& S = *reinterpret_cast<PShared*>(smem);
+  const int ct = threadIdx.x - kWarp;
+  const int L = a.L;
+  const int layer = ph / kPhasesPerLayer;
+  const int kind = ph == kPhasesPerLayer * L ? kHEAD : ph % kPhasesPerLayer;
+  const uint32_t ep = epoch_of(seq, ph);
+  const Rows r = phase_rows(a, S, ph);
+  if (r.r0 >= r.r1) return;
+  // phase input
+  const PLayer* P = kind == kHEAD ? nullptr : &S.layers[layer];
+  const int K = r.K;
+  PhaseOut po;
+  po.base = 0;
+  po.ep_old = 0;
+  po.bias = false;
+  // Rows this phase's epilogue needs that do not wait on the phase input
+  // are copied asynchronously now; the gather waits for them before its
+  // first barrier.
+  if (kind == kOPROJ || kind == kDOWN) {
+    // the residual rows this CTA updates: complete since an earlier phase
+    po.ep_old = epoch_of(seq, kind == kOPROJ ? ph - 3 : ph - 2);
+    po.base = r.r0 & ~1;
+    if (kind == kOPROJ && layer == 0) {
+      const int nr = r.r1 - po.base;
+      for (int i = ct; i < nr * BT; i += kPConsumerThreads) {
+        const int b = i / nr, jr = i % nr;
+        const float old = b < a.B ? bf16_to_f32(a.embed[(size_t)S.tok[b] * a.H + po.base + jr]) : 0.f;
+        S.xoldw[b][jr] = (static_cast<uint64_t>(po.ep_old) << 32) | __float_as_uint(old);
+      }
+    } else {
+      const int npair = (r.r1 - po.base + 1) / 2;
+      for (int i = ct; i < npair * BT; i += kPConsumerThreads) {
+        const int b = i / npair, q = i % npair;
+        if (b < a.B) cp_async16(&S.xoldw[b][2 * q], a.xw + (size_t)b * a.H + po.base + 2 * q);
+      }
+    }
+  }
+  if (kind == kQKV && P->b_qkv) {
+    po.base = r.r0 & ~7;
+    po.bias = true;
+    const int nchunk = (r.r1 - po.base + 7) / 8;
+    for (int i = ct; i < nchunk; i += kPConsumerThreads)
+      cp_async16(&S.biasr[8 * i], P->b_qkv + po.base + 8 * i);
+  }
+  cp_async_commit();
+  if (kind == kQKV) {
+    gather_input<BT>(a, a.xw, K, K, epoch_of(seq, ph - 1), layer == 0 ? a.embed : nullptr,
+                     P->g_attn, sp);
+  } else if (kind == kOPROJ) {
+    // unsplit scans (every sequence's attention in one item per kv head) need
+    // no merge: split 0's output words are the attention output
+    bool split = false;
+    for (int b = 0; b < BT; ++b) split |= S.nsplit[b] > 1;
+    if (split) gather_attn<BT>(a, epoch_of(seq, ph - 1), sp);
+    else gather_input<BT>(a, a.aw, K, (size_t)kPMaxSplits * K, epoch_of(seq, ph - 1), nullptr,
+                          nullptr, sp);
+  } else if (kind == kGU) {
+    gather_input<BT>(a, a.xw, K, K, epoch_of(seq, ph - 1), nullptr, P->g_mlp, sp);
+  } else if (kind == kDOWN) {
+    gather_input<BT>(a, a.hw, K, K, epoch_of(seq, ph - 1), nullptr, nullptr, sp);
+  } else {
+    gather_input<BT>(a, a.xw, K, K, epoch_of(seq, ph - 1), nullptr, a.g_final, sp);
+  }
+  if (prof) prof[2 * ph + 1] = global_timer();
+  po.words = kind == kQKV ? a.qkvw : (kind == kGU ? a.hw : a.xw);
+  po.logits = a.logits;
+  po.stride = kind == kQKV ? a.nqkv : (kind == kGU ? a.F : (kind == kHEAD ? a.V : a.H));
+  if constexpr (BT == 1) {
+    if (K / 8 <= kXReg * kWarp) gemv_tiles<1, 0>(a, r, po, kind, ep, rp_io, kb_io, best_io, sp);
+    else gemv_tiles<1, 1>(a, r, po, kind, ep, rp_io, kb_io, best_io, sp);
+  } else {
+    gemv_tiles<BT, 2>(a, r, po, kind, ep, rp_io, kb_io, best_io, sp);
+  }
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -926,7 +1357,6 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   PShared& S = *reinterpret_cast<PShared*>(smem);
   const int slot_bytes = a.slot_bytes, nslots = a.nslots;
   char* ring = smem + a.ring_offset;
-  float* xs = reinterpret_cast<float*>(smem + a.xs_offset);
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
 
   if (threadIdx.x == 0) {
@@ -950,6 +1380,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   }
   if (threadIdx.x < kHEAD + 1)
     S.rows[threadIdx.x] = kind_rows(a, threadIdx.x, blockIdx.x, gridDim.x, a.slot_bytes);
+  if (threadIdx.x == kWarp) attn_plan(a, gridDim.x, S.nsplit, S.item0);
   {  // the per-layer pointer table, copied once
     const int words = a.L * (int)(sizeof(PLayer) / sizeof(uint64_t));
     const uint64_t* src = reinterpret_cast<const uint64_t*>(a.layers);
@@ -984,216 +1415,18 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       const int kind = ph == kPhasesPerLayer * L ? kHEAD : ph % kPhasesPerLayer;
       const uint32_t ep = epoch_of(seq, ph);
       if (kind == kATTN) {
-        const int items = a.B * a.Hkv;
-        for (int it = blockIdx.x; it < items; it += gridDim.x)
-          attention_item<D, KV16>(a, it / a.Hkv, it % a.Hkv, layer, epoch_of(seq, ph - 1), ep,
+        for (int it = blockIdx.x; it < S.item0[kPMaxBatch]; it += gridDim.x) {
+          const AttnItem t = attn_item_of(S, a.Hkv, it);
+          const int np = cached_positions(a, t.b, S.pos[t.b]);
+          const int p0 = (int)(((long long)t.sp * np) / t.ns);
+          const int p1 = (int)(((long long)(t.sp + 1) * np) / t.ns);
+          attention_item<D, KV16>(a, t.b, t.g, t.sp, p0, p1, layer, epoch_of(seq, ph - 1), ep,
                                   nslots, rp, sp);
+        }
         if (prof) prof[2 * ph + 1] = global_timer();
         continue;
       }
-      const Rows r = phase_rows(a, S, ph);
-      if (r.r0 >= r.r1) continue;
-      // phase input
-      const PLayer* P = kind == kHEAD ? nullptr : &S.layers[layer];
-      const int K = r.K;
-      PhaseOut po;
-      po.base = 0;
-      po.ep_old = 0;
-      po.bias = false;
-      // Rows this phase's epilogue needs that do not wait on the phase input
-      // are copied asynchronously now; the gather waits for them before its
-      // first barrier.
-      if (kind == kOPROJ || kind == kDOWN) {
-        // the residual rows this CTA updates: complete since an earlier phase
-        po.ep_old = epoch_of(seq, kind == kOPROJ ? ph - 3 : ph - 2);
-        po.base = r.r0 & ~1;
-        if (kind == kOPROJ && layer == 0) {
-          const int nr = r.r1 - po.base;
-          for (int i = ct; i < nr * BT; i += kPConsumerThreads) {
-            const int b = i / nr, jr = i % nr;
-            const float old = b < a.B ? bf16_to_f32(a.embed[(size_t)S.tok[b] * a.H + po.base + jr]) : 0.f;
-            S.xoldw[b][jr] = (static_cast<uint64_t>(po.ep_old) << 32) | __float_as_uint(old);
-          }
-        } else {
-          const int npair = (r.r1 - po.base + 1) / 2;
-          for (int i = ct; i < npair * BT; i += kPConsumerThreads) {
-            const int b = i / npair, q = i % npair;
-            if (b < a.B) cp_async16(&S.xoldw[b][2 * q], a.xw + (size_t)b * a.H + po.base + 2 * q);
-          }
-        }
-      }
-      if (kind == kQKV && P->b_qkv) {
-        po.base = r.r0 & ~7;
-        po.bias = true;
-        const int nchunk = (r.r1 - po.base + 7) / 8;
-        for (int i = ct; i < nchunk; i += kPConsumerThreads)
-          cp_async16(&S.biasr[8 * i], P->b_qkv + po.base + 8 * i);
-      }
-      cp_async_commit();
-      if (kind == kQKV) {
-        gather_input<BT>(a, a.xw, K, epoch_of(seq, ph - 1), layer == 0 ? a.embed : nullptr,
-                         P->g_attn, sp);
-      } else if (kind == kOPROJ) {
-        gather_input<BT>(a, a.aw, K, epoch_of(seq, ph - 1), nullptr, nullptr, sp);
-      } else if (kind == kGU) {
-        gather_input<BT>(a, a.xw, K, epoch_of(seq, ph - 1), nullptr, P->g_mlp, sp);
-      } else if (kind == kDOWN) {
-        gather_input<BT>(a, a.hw, K, epoch_of(seq, ph - 1), nullptr, nullptr, sp);
-      } else {
-        gather_input<BT>(a, a.xw, K, epoch_of(seq, ph - 1), nullptr, a.g_final, sp);
-      }
-      if (prof) prof[2 * ph + 1] = global_timer();
-      const int two = r.m1 ? 2 : 1;
-      po.words = kind == kQKV ? a.qkvw : (kind == kGU ? a.hw : a.xw);
-      po.logits = a.logits;
-      po.stride = kind == kQKV ? a.nqkv : (kind == kGU ? a.F : (kind == kHEAD ? a.V : a.H));
-      const int nb = a.B;
-      const int C = K / 8;  // 16-byte chunks per row
-      // batch 1 and rows of at most 1024: every lane keeps its chunks of the
-      // input in registers for the whole phase, and each unit is one row (or
-      // one gate|up pair) reduced by one warp
-      const bool xreg = BT == 1 && C <= kXReg * kWarp;
-      float xr[kXReg][8];
-      if (xreg) {
-#pragma unroll
-        for (int jj = 0; jj < kXReg; ++jj) {
-          const int c = lane + jj * kWarp;
-          float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
-          if (c < C) {  // two 16-byte loads, not eight scalar ones
-            p0 = *reinterpret_cast<const float4*>(xs + c * 4);
-            p1 = *reinterpret_cast<const float4*>(xs + K / 2 + c * 4);
-          }
-          xr[jj][0] = p0.x; xr[jj][1] = p0.y; xr[jj][2] = p0.z; xr[jj][3] = p0.w;
-          xr[jj][4] = p1.x; xr[jj][5] = p1.y; xr[jj][6] = p1.z; xr[jj][7] = p1.w;
-        }
-      }
-      for (int row = r.r0; row < r.r1; row += r.R) {
-        const int n = min(r.R, r.r1 - row);
-        ring_wait(&S.full[rp.s], rp.par, sp);  // on expiry the tile is garbage; the step is failed
-        const uint16_t* tile =
-            reinterpret_cast<const uint16_t*>(ring + (size_t)rp.s * slot_bytes);
-        const size_t ms = (size_t)n * K;  // the up rows follow the n gate rows
-        // How the warps share the tile:
-        //  batch 1, rows of at most 1024: warp w reduces whole units w, w + W, ...
-        //    against the input held in registers;
-        //  batch 1, longer rows: the k range is cut into W segments, warp w
-        //    reduces segment w of every unit (each input chunk loaded once for
-        //    all of them) and the partials are summed across warps;
-        //  batch > 1: units are cut into KS segments as needed, the input is
-        //    read from shared memory.
-        if constexpr (BT == 1) {
-          if (xreg) {
-            const int U = cw < n ? (n - cw + kPConsumerWarps - 1) / kPConsumerWarps : 0;
-            float v[2 * kUnitsPerWarp];
-#pragma unroll
-            for (int i = 0; i < 2 * kUnitsPerWarp; ++i) v[i] = 0.f;
-            const uint16_t* wt = tile + (size_t)cw * K;
-            if (two == 2) units_xreg<true>(wt, U, K, ms, xr, C, lane, v);
-            else units_xreg<false>(wt, U, K, ms, xr, C, lane, v);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
-            rp.next(nslots);
-            if (U > 0) {
-              warp_sum_many<2 * kUnitsPerWarp>(v);  // value i = (unit i / 2, matrix i % 2) in lane 4 i
-              const float vup = __shfl_down_sync(0xFFFFFFFFu, v[0], 4);
-              const int i = lane / 4, u = i / 2, it = cw + u * kPConsumerWarps;
-              if (lane % 4 == 0 && (i & 1) == 0 && u < U && nb > 0)
-                tile_epilogue<BT>(S, kind, po, r.r0, row + it, 0, v[0], vup, ep, best, sp);
-            }
-          } else {
-            // segment w of the k range, all units in passes of up to 8 rows
-            const int KS = C >= kPConsumerWarps * kWarp ? kPConsumerWarps : max(1, C / kWarp);
-            const int seg = cw;
-            const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
-            const int upp = 8 / two;  // units per pass
-            for (int g0 = 0; g0 < n; g0 += upp) {
-              const int nu = min(upp, n - g0), nr = nu * two;
-              float o[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o[i] = 0.f;
-              if (seg < KS) {
-                const uint16_t* wt = tile + (size_t)g0 * K;
-                seg_rows(wt, nr, K, ms, two, xs, c0, c1, lane, o);
-              }
-              if (g0 + upp >= n) {  // the slot is no longer read by this warp
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.empty[rp.s]);
-              }
-              warp_sum_many<8>(o);  // row i of the pass in lane 4 i
-              if (lane % 4 == 0) S.kred[kb][seg][lane / 4] = seg < KS ? o[0] : 0.f;
-              consumer_sync();
-              for (int u = ct; u < nu; u += kPConsumerThreads) {
-                float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-                for (int sg = 0; sg < kPConsumerWarps; ++sg)  // independent loads, one chain of adds
-                  if (sg < KS) {
-                    v0 += S.kred[kb][sg][u * two];
-                    if (two == 2) v1 += S.kred[kb][sg][u * two + 1];
-                  }
-                if (nb > 0)
-                  tile_epilogue<BT>(S, kind, po, r.r0, row + g0 + u, 0, v0, v1, ep, best, sp);
-              }
-              kb ^= 1;  // the next pass writes the other buffer: no second barrier
-            }
-            rp.next(nslots);
-          }
-        } else {
-          // batch > 1: long rows are cut into KS k-segments when the tile has few
-          // units, so the work spreads over all warps (up to kUnitsPerWarp items
-          // each); a segment keeps at least 64 chunks, two per lane
-          int KS = 1;
-          if (n < kPConsumerWarps) {
-            KS = kUnitsPerWarp * kPConsumerWarps / n;
-            const int kmax = C / 64;
-            if (KS > kmax) KS = kmax;
-            if (KS < 1) KS = 1;
-          }
-          const int items = n * KS;  // warp cw takes items cw, cw + W, ...
-          constexpr int NV = kUnitsPerWarp * 2 * BT;  // [item u][matrix m][sequence b]
-          float v[NV];
-#pragma unroll
-          for (int i = 0; i < NV; ++i) v[i] = 0.f;
-#pragma unroll
-          for (int u = 0; u < kUnitsPerWarp; ++u) {
-            const int it = cw + u * kPConsumerWarps;
-            if (it >= items) break;  // uniform across the warp
-            const int ui = it / KS, seg = it % KS;
-            const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
-            const uint16_t* w0 = tile + (size_t)ui * K;
-            row_dot_smem<BT>(w0, two == 2 ? w0 + ms : nullptr, xs, K, c0, c1, lane,
-                             v + 2 * u * BT);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
-          rp.next(nslots);
-          // value i of the warp ends up in lane i * hl
-          constexpr int hl = kWarp / NV;
-          warp_sum_many<NV>(v);
-          const int i = lane / hl, b = i % BT, m = (i / BT) & 1, u = i / (2 * BT);
-          const int it = cw + u * kPConsumerWarps;
-          if (KS == 1) {
-            const float vup = __shfl_down_sync(0xFFFFFFFFu, v[0], BT * hl);  // the up partner
-            if (lane % hl == 0 && m == 0 && b < nb && it < items)
-              tile_epilogue<BT>(S, kind, po, r.r0, row + it, b, v[0], vup, ep, best, sp);
-          } else {
-            if (lane % hl == 0 && it < items) S.kred[kb][it][m * BT + b] = v[0];
-            consumer_sync();
-            for (int t = ct; t < n * BT; t += kPConsumerThreads) {
-              const int ui = t / BT, bb = t % BT;
-              if (bb >= nb) continue;
-              float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-              for (int sg = 0; sg < kPConsumerWarps; ++sg)  // independent loads, one chain of adds
-                if (sg < KS) {
-                  v0 += S.kred[kb][ui * KS + sg][bb];
-                  v1 += S.kred[kb][ui * KS + sg][BT + bb];
-                }
-              tile_epilogue<BT>(S, kind, po, r.r0, row + ui, bb, v0, v1, ep, best, sp);
-            }
-            kb ^= 1;  // the next split tile writes the other buffer: no second barrier
-          }
-        }
-      }
+      gemv_phase<BT>(a, ph, seq, rp, kb, best, prof, sp);
     }
     // per-CTA arg-max partials (any lane of a warp may hold a row's key)
 #pragma unroll
@@ -1330,6 +1563,7 @@ bool persistent_supported(int L, int H, int qd, int F, int D, int G, int B) {
   if (G < 1 || G > 8 || G * (D / 2) > kPConsumerThreads) return false;
   if (H % 8 || qd % 8 || F % 8) return false;
   if ((G + 2) * D > kAttnWords * kPConsumerThreads) return false;
+  if (qd / D > kPMaxHeads) return false;
   // rows one CTA may own: the o-proj rows go to at least half of the CTAs
   const int grid = num_sms(), half = grid - grid / 2;
   const long long nqkv = (long long)qd + 2LL * (qd / G);

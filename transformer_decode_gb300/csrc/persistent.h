@@ -14,6 +14,8 @@ constexpr int kPMinSlotBytes = 32 * 1024; // smallest slot the kernel is run wit
 constexpr int kPMaxCtx = 2048;         // cache capacity up to which it is chosen
 constexpr int kPMaxRows = 128;         // rows of H one CTA may own (H <= 128 * grid)
 constexpr int kPMaxLayers = 64;        // layers the persistent kernel handles
+constexpr int kPMaxSplits = 4;         // attention position splits per (sequence, kv head)
+constexpr int kPMaxHeads = 64;         // query heads
 
 // Per-layer packed weights as the persistent kernel reads them.
 struct PLayer {
@@ -39,7 +41,8 @@ struct PersistArgs {
   // epoch-tagged hand-over words (value in the low half, epoch in the high)
   uint64_t* xw;    // [kPMaxBatch][H] residual stream
   uint64_t* qkvw;  // [kPMaxBatch][nqkv]
-  uint64_t* aw;    // [kPMaxBatch][Hq D] attention output
+  uint64_t* aw;    // [kPMaxBatch][kPMaxSplits][Hq D] attention output per split (o = acc / l)
+  uint64_t* mlw;   // [kPMaxBatch][kPMaxSplits][Hq][2] softmax state (m, l) per split and head
   uint64_t* hw;    // [kPMaxBatch][F] SiLU(gate) * up
   unsigned long long* am_part;  // [B][grid] arg-max partial keys
   unsigned int* ticket;         // zero between steps
