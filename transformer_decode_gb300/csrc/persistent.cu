@@ -41,6 +41,9 @@ constexpr int kPConsumerWarps = kPThreads / kWarp - 1;
 constexpr int kPConsumerThreads = kPConsumerWarps * kWarp;
 constexpr int kPhasesPerLayer = 5;
 constexpr int kUnitsPerWarp = 4;  // output units (rows, gate|up pairs) a warp takes per tile
+// ... at batch BT: fewer at larger batches, where every unit holds BT sums
+__host__ __device__ constexpr int units_per_warp(int BT) { return BT == 1 ? 4 : (BT == 2 ? 2 : 1); }
+__host__ __device__ constexpr int bt_of_batch(int B) { return B <= 1 ? 1 : (B <= 2 ? 2 : 4); }
 enum PhaseKind : int { kQKV = 0, kATTN = 1, kOPROJ = 2, kGU = 3, kDOWN = 4, kHEAD = 5 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -313,7 +316,8 @@ __device__ Rows kind_rows(const PersistArgs& a, int kind, int cta, int grid, int
   r.r1 = (int)(((long long)(cta + 1) * N) / grid);
   const int row_bytes = r.K * 2 * (pair ? 2 : 1);
   int rmax = slot_bytes / row_bytes;
-  if (rmax > kUnitsPerWarp * kPConsumerWarps) rmax = kUnitsPerWarp * kPConsumerWarps;
+  const int umax = units_per_warp(bt_of_batch(a.B)) * kPConsumerWarps;
+  if (rmax > umax) rmax = umax;
   if (rmax < 1) rmax = 1;
   // tiles of (nearly) equal size: the fewest tiles that fit, rows spread evenly
   const int nr = r.r1 - r.r0;
@@ -660,6 +664,41 @@ __device__ __forceinline__ void seg_rows(const uint16_t* w0, int NR, int K, size
 #pragma unroll
     for (int r = 0; r < 8; ++r)
       if (r < NR) o[r] += dot8r(*reinterpret_cast<const uint4*>(w0 + wr[r] + c * 8), xb);
+    compiler_fence();
+  }
+}
+
+// Batch > 1, whole rows: U <= UPW units (rows cw, cw + W, ... from w0, with
+// their up rows ms elements further when pair) times the input [BT][K] in
+// shared memory. Each chunk of the input is loaded once for all units:
+// partials into v[(2 u + m) BT + b].
+template <int BT, int UPW>
+__device__ __forceinline__ void units_smem(const uint16_t* w0, int U, int K, size_t ms, bool pair,
+                                           const float* xs, int C, int lane,
+                                           float (&v)[UPW * 2 * BT]) {
+  for (int c = lane; c < C; c += kWarp) {
+    float xb[BT][8];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      const float4 p0 = *reinterpret_cast<const float4*>(xs + b * K + c * 4);
+      const float4 p1 = *reinterpret_cast<const float4*>(xs + b * K + K / 2 + c * 4);
+      xb[b][0] = p0.x; xb[b][1] = p0.y; xb[b][2] = p0.z; xb[b][3] = p0.w;
+      xb[b][4] = p1.x; xb[b][5] = p1.y; xb[b][6] = p1.z; xb[b][7] = p1.w;
+    }
+#pragma unroll
+    for (int u = 0; u < UPW; ++u) {
+      if (u < U) {
+        const uint16_t* w = w0 + (size_t)u * kPConsumerWarps * K + c * 8;
+        const uint4 wa = *reinterpret_cast<const uint4*>(w);
+#pragma unroll
+        for (int b = 0; b < BT; ++b) v[(2 * u) * BT + b] += dot8r(wa, xb[b]);
+        if (pair) {
+          const uint4 wb = *reinterpret_cast<const uint4*>(w + ms);
+#pragma unroll
+          for (int b = 0; b < BT; ++b) v[(2 * u + 1) * BT + b] += dot8r(wb, xb[b]);
+        }
+      }
+    }
     compiler_fence();
   }
 }
@@ -1207,26 +1246,33 @@ __device__ __forceinline__ void gemv_tiles(const PersistArgs& a, const Rows& rin
       // units, so the work spreads over all warps (up to kUnitsPerWarp items
       // each); a segment keeps at least 64 chunks, two per lane
       int KS = 1;
+      constexpr int UPW = units_per_warp(BT);
       if (n < kPConsumerWarps) {
-        KS = kUnitsPerWarp * kPConsumerWarps / n;
+        KS = UPW * kPConsumerWarps / n;
         const int kmax = C / 64;
         if (KS > kmax) KS = kmax;
         if (KS < 1) KS = 1;
       }
       const int items = n * KS;  // warp cw takes items cw, cw + W, ...
-      constexpr int NV = kUnitsPerWarp * 2 * BT;  // [item u][matrix m][sequence b]
+      constexpr int NV = UPW * 2 * BT;  // [item u][matrix m][sequence b]
       float v[NV];
 #pragma unroll
       for (int i = 0; i < NV; ++i) v[i] = 0.f;
+      if (KS == 1) {
+        // whole rows: the warp's units share each input chunk (loaded once)
+        const int U = cw < n ? min(UPW, (n - cw + kPConsumerWarps - 1) / kPConsumerWarps) : 0;
+        units_smem<BT, UPW>(tile + (size_t)cw * K, U, K, ms, two == 2, xs, C, lane, v);
+      } else {
 #pragma unroll
-      for (int u = 0; u < kUnitsPerWarp; ++u) {
-        const int it = cw + u * kPConsumerWarps;
-        if (it >= items) break;  // uniform across the warp
-        const int ui = it / KS, seg = it % KS;
-        const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
-        const uint16_t* w0 = tile + (size_t)ui * K;
-        row_dot_smem<BT>(w0, two == 2 ? w0 + ms : nullptr, xs, K, c0, c1, lane,
-                         v + 2 * u * BT);
+        for (int u = 0; u < UPW; ++u) {
+          const int it = cw + u * kPConsumerWarps;
+          if (it >= items) break;  // uniform across the warp
+          const int ui = it / KS, seg = it % KS;
+          const int c0 = (seg * C) / KS, c1 = ((seg + 1) * C) / KS;
+          const uint16_t* w0 = tile + (size_t)ui * K;
+          row_dot_smem<BT>(w0, two == 2 ? w0 + ms : nullptr, xs, K, c0, c1, lane,
+                           v + 2 * u * BT);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
