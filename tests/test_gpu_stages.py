@@ -33,7 +33,9 @@ def _norm_ref(x, gamma, eps):
     (1, 896, 151936, True, False),   # 0.5B head-sized
     (1, 4864, 896, False, False),    # 0.5B down
     (3, 896, 37, True, True),        # ragged rows, small batch
-    (16, 896, 300, True, False),     # batch 16
+    (16, 896, 300, True, False),     # batch 16 (tensor cores)
+    (9, 896, 1152, True, True),      # batch 9, QKV-shaped (tensor cores, ragged batch)
+    (16, 2048, 77, True, True),      # tensor cores at the largest single k range
     (16, 4864, 40, False, False),    # batch 16, K split into tiles
     (1, 8, 5, True, True),           # minimum K
     (1, 20000, 9, True, False),      # K beyond one shared-memory tile
@@ -59,7 +61,8 @@ def test_rmsnorm_gemv(B, K, N, norm, bias):
         assert rel_l2(got, ref) < REL_L2_GATE / 10, (r, rel_l2(got, ref))
 
 
-@pytest.mark.parametrize("B,K,N", [(1, 896, 896), (1, 4864, 896), (5, 896, 130), (16, 4864, 64)])
+@pytest.mark.parametrize("B,K,N", [(1, 896, 896), (1, 4864, 896), (5, 896, 130), (16, 4864, 64),
+                                   (16, 896, 896), (12, 4864, 896)])
 def test_gemv_residual(B, K, N):
     a = _x(B, K, 7 + K)
     x0 = _x(B, N, 8 + N)
@@ -72,7 +75,8 @@ def test_gemv_residual(B, K, N):
         assert rel_l2(f32(x[r]), ref) < REL_L2_GATE / 10
 
 
-@pytest.mark.parametrize("B,K,F", [(1, 896, 4864), (2, 256, 512), (16, 896, 100), (1, 4096, 333)])
+@pytest.mark.parametrize("B,K,F", [(1, 896, 4864), (2, 256, 512), (16, 896, 100), (1, 4096, 333),
+                                   (16, 896, 4864), (10, 896, 37)])
 def test_swiglu_gemv(B, K, F):
     x = _x(B, K, 20 + F)
     W = synth.normal_bf16(0, 520 + F, (2 * F, K), 0.02)
@@ -239,25 +243,27 @@ def test_rope_append_and_attention(shape, positions, paged, kv_bf16):
 
 
 # ------------------------------------------------------------------ LM head + argmax
-def test_lm_head_argmax_and_ties():
+@pytest.mark.parametrize("B", [4, 16])
+def test_lm_head_argmax_and_ties(B):
+    """LM head logits and greedy tokens; B = 16 runs on the tensor cores."""
     s = synth.TINY
-    _, w, model = _one_layer_model(s, 4, 32)
+    _, w, model = _one_layer_model(s, B, 32)
     V, K = 151936, 896
     W = synth.normal_bf16(0, 560, (V, K), 0.02)
     # planted exact tie: rows 1000 and 90000 identical and dominant for b = 0
-    x = _x(4, K, 61)
+    x = _x(B, K, 61)
     xn0 = oracle.rmsnorm(x[0].numpy(), synth.normal_bf16(0, 562, (K,), 0.02, 1.0), 1e-6)
     hot = torch.tensor(np.sign(xn0) * 0.1, dtype=torch.float32).to(torch.bfloat16)
     W[1000] = hot
     W[90000] = hot
     gamma = synth.normal_bf16(0, 562, (K,), 0.02, 1.0)
-    logits = torch.empty(4, V, device="cuda")
-    nxt = torch.full((4,), -7, dtype=torch.int32, device="cuda")
+    logits = torch.empty(B, V, device="cuda")
+    nxt = torch.full((B,), -7, dtype=torch.int32, device="cuda")
     model.lm_head_argmax(x.cuda(), gamma.cuda(), 1e-6, W.cuda(), logits, nxt)
     torch.cuda.synchronize()
     assert nxt[0].item() == 1000
     assert logits[0, 1000].item() == logits[0, 90000].item()
-    for b in range(4):
+    for b in range(B):
         ref = oracle.matvec_bf16(W, oracle.rmsnorm(x[b].numpy(), gamma, 1e-6))
         got = f32(logits[b])
         assert rel_l2(got, ref) < REL_L2_GATE / 10

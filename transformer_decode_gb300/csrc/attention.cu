@@ -103,7 +103,8 @@ size_t attn_part_floats(int B, int Hq, int D, int splits) {
 
 template <int D, int GM, bool KV16>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a, int cap) {
-  extern __shared__ float p_s[];  // [GM][cap] scores, then probabilities
+  extern __shared__ float p_s[];  // [GM][cap] scores, then probabilities; then [cap] row offsets
+  size_t* off_s = reinterpret_cast<size_t*>(p_s + ((GM * cap + 1) & ~1));  // 8-byte aligned
   __shared__ float q_s[GM][D];
   __shared__ float m_s[GM], l_s[GM];
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z, S = gridDim.x;
@@ -131,9 +132,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a, int cap
       if (a.status) atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
 #pragma unroll
       for (int h = 0; h < GM; ++h) p_s[h * cap + t] = -INFINITY;
+      off_s[t] = 0;  // never dereferenced with a nonzero weight
       continue;
     }
     const size_t kr = a.kv.offset(a.layer, b, g, t0 + t);
+    off_s[t] = kr;  // the row's offset, for the value pass
     float s[GM];
 #pragma unroll
     for (int h = 0; h < GM; ++h) s[h] = 0.f;
@@ -170,16 +173,20 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a, int cap
   }
   __syncthreads();
 
-  // weighted values: one thread per (head, pair of dims)
+  // weighted values: one thread per (head, pair of dims). The row offsets
+  // come from shared memory, so the loads of several positions are in flight
+  // together (a per-position block-table lookup before each load would
+  // serialise them).
   for (int idx = threadIdx.x; idx < G * (D / 2); idx += kAttnThreads) {
     const int h = idx / (D / 2), d2 = idx % (D / 2);
     float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 8
     for (int t = 0; t < len; ++t) {
       const float p = p_s[h * cap + t];
-      if (p == 0.f) continue;  // excluded slot (or a weight that underflowed to 0)
-      const float2 w = kv_load2<KV16>(a.kv.v, a.kv.offset(a.layer, b, g, t0 + t) + 2 * d2);
-      acc0 = fmaf(p, w.x, acc0);
-      acc1 = fmaf(p, w.y, acc1);
+      const float2 w = kv_load2<KV16>(a.kv.v, off_s[t] + 2 * d2);
+      // an excluded slot (p = 0) is not multiplied: its row may be anything
+      acc0 = fmaf(p, p == 0.f ? 0.f : w.x, acc0);
+      acc1 = fmaf(p, p == 0.f ? 0.f : w.y, acc1);
     }
     float* ph = part + ((size_t)h * S + c) * (D + 2);
     ph[2 + 2 * d2] = acc0;
@@ -210,7 +217,7 @@ __global__ void k_attn_merge(AttnArgs a) {
 
 template <int D, int GM, bool KV16>
 static cudaError_t attn_split(const AttnArgs& a, int cap, cudaStream_t s) {
-  const size_t smem = sizeof(float) * (size_t)GM * cap;
+  const size_t smem = sizeof(float) * (size_t)((GM * cap + 1) & ~1) + sizeof(size_t) * (size_t)cap;
   cudaError_t e = ensure_smem<k_attn_split<D, GM, KV16>>();
   if (e != cudaSuccess) return e;
   k_attn_split<D, GM, KV16><<<dim3(a.splits, a.Hkv, a.B), kAttnThreads, smem, s>>>(a, cap);

@@ -211,6 +211,7 @@ static cudaError_t gemv_epi(const GemvArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_gemv(Epi epi, const GemvArgs& a, cudaStream_t s) {
+  if (gemm16_supported(epi, a.B, a.K)) return launch_gemm16(epi, a, s);
   switch (epi) {
     case Epi::Store: return gemv_epi<Epi::Store>(a, s);
     case Epi::Residual: return gemv_epi<Epi::Residual>(a, s);
@@ -309,6 +310,7 @@ static cudaError_t lm_bt(const LmHeadArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_lm_head(const LmHeadArgs& a, cudaStream_t s) {
+  if (lm_head16_supported(a.B, a.K)) return launch_lm_head16(a, s);
   if (a.B <= 1) return lm_bt<1>(a, s);
   if (a.B <= 2) return lm_bt<2>(a, s);
   if (a.B <= 4) return lm_bt<4>(a, s);

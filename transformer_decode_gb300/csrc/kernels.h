@@ -22,6 +22,10 @@ struct GemvArgs {
   float* y;               // [B, N]; Residual: updated in place
 };
 cudaError_t launch_gemv(Epi epi, const GemvArgs& a, cudaStream_t s);
+// Batch 9..16 on the tensor cores (gemm16.cu); launch_gemv and launch_lm_head
+// dispatch there when these report support.
+bool gemm16_supported(Epi epi, int B, int K);
+cudaError_t launch_gemm16(Epi epi, const GemvArgs& a, cudaStream_t s);
 
 // LM head: logits = W rmsnorm(x) and the greedy token per sequence.
 struct LmHeadArgs {
@@ -40,6 +44,8 @@ struct LmHeadArgs {
 };
 int lm_head_grid();
 cudaError_t launch_lm_head(const LmHeadArgs& a, cudaStream_t s);
+bool lm_head16_supported(int B, int K);
+cudaError_t launch_lm_head16(const LmHeadArgs& a, cudaStream_t s);
 
 // ------------------------------------------------------------ attention
 struct RopeArgs {
