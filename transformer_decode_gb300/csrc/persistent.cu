@@ -540,16 +540,22 @@ __device__ __noinline__ void gather_attn(const PersistArgs& a, uint32_t epoch, S
           w[u] = ld_word(adr(u));
         }
       }
-      const bool ml_here = rd == 0 && ct < ns * Hq * 2;
-      const uint64_t* mp = mw + (ml_here ? ct : 0);
-      const auto madr = [mp](int) { return mp; };
-      uint64_t mwd[1] = {0};
-      if (ml_here) mwd[0] = ld_word(mp);
+      // the (m, l) words of every (split, head): up to three per thread
+      const int nml = rd == 0 ? ns * Hq * 2 : 0;
+      const auto madr = [mw, ct](int u) { return mw + ct + u * kPConsumerThreads; };
+      uint64_t mwd[3] = {0, 0, 0};
+      uint32_t mvalid = 0;
+#pragma unroll
+      for (int u = 0; u < 3; ++u)
+        if (ct + u * kPConsumerThreads < nml) {
+          mvalid |= 1u << u;
+          mwd[u] = ld_word(madr(u));
+        }
       ll_settle<NW>(adr, valid, epoch, w, sp);
-      if (ml_here) {
-        ll_settle<1>(madr, 1u, epoch, mwd, sp);
-        mlv[ct] = __uint_as_float(static_cast<uint32_t>(mwd[0]));
-      }
+      ll_settle<3>(madr, mvalid, epoch, mwd, sp);
+#pragma unroll
+      for (int u = 0; u < 3; ++u)
+        if ((mvalid >> u) & 1u) mlv[ct + u * kPConsumerThreads] = __uint_as_float(static_cast<uint32_t>(mwd[u]));
       if (rd == 0) {
         consumer_sync();
         if (ct < Hq) {
