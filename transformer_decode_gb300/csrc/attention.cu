@@ -6,8 +6,8 @@
 //
 // Attention (Tang section 2.2: online softmax is the monoid on (m, l, acc);
 // section 2.5: split is valid for any associative monoid): the positions
-// 0..pos of one (sequence, kv head) are cut into `splits` chunks. Each CTA
-// reads its chunk of K and V once for all G query heads of the group (the
+// 0..pos of one (sequence, kv head) are cut into `splits` ranges. Each CTA
+// reads its range of K and V once for all G query heads of the group (the
 // repeat_kv expansion folded into indexing, nanocompile "Phase 3"), produces
 // the partial (m, l, acc[D]) per head, and a merge combines the partials:
 //   M = max_c m_c,  out = sum_c acc_c e^(m_c - M) / sum_c l_c e^(m_c - M).
@@ -101,12 +101,40 @@ size_t attn_part_floats(int B, int Hq, int D, int splits) {
   return (size_t)B * Hq * splits * (D + 2);
 }
 
+// Positions per chunk staged in shared memory.
+constexpr int kAttnChunk = 64;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// One CTA per (split c, kv head g, sequence b). The split's positions are
+// scanned in chunks of kAttnChunk: the chunk's K and V rows are copied into
+// shared memory with asynchronous 16-byte copies (the next chunk's copies in
+// flight while this one is used), so the cache is read with coalesced
+// transfers instead of per-thread row walks. Scores: one position per thread
+// for all G heads (K rows padded by 16 bytes so the threads' equal-column
+// reads fall in different banks; q reads are broadcasts). Softmax statistics
+// run online over the chunks, one warp per head; values: one thread per
+// (head, pair of dims), the running sums rescaled at each chunk.
 template <int D, int GM, bool KV16>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a, int cap) {
-  extern __shared__ float p_s[];  // [GM][cap] scores, then probabilities; then [cap] row offsets
-  size_t* off_s = reinterpret_cast<size_t*>(p_s + ((GM * cap + 1) & ~1));  // 8-byte aligned
+  constexpr int ES = KV16 ? 2 : 4;
+  constexpr int RS = D + 16 / ES;  // padded row, elements
+  constexpr int PPR = D * ES / 16; // 16-byte pieces per row
+  extern __shared__ __align__(16) unsigned char sm[];
+  unsigned char* kbuf = sm;                                   // [2][kAttnChunk][RS]
+  unsigned char* vbuf = kbuf + 2 * kAttnChunk * RS * ES;      // [2][kAttnChunk][RS]
+  float* p_s = reinterpret_cast<float*>(vbuf + 2 * kAttnChunk * RS * ES);  // [GM][kAttnChunk]
+  size_t* off_s = reinterpret_cast<size_t*>(p_s + GM * kAttnChunk);      // [cap] row offsets
   __shared__ float q_s[GM][D];
-  __shared__ float m_s[GM], l_s[GM];
+  __shared__ float m_s[GM], l_s[GM], r_s[GM];
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z, S = gridDim.x;
   const int G = a.Hq / a.Hkv;
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -123,77 +151,140 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a, int cap
     const int h = i / D;
     q_s[h][i % D] = h < G ? a.q[((size_t)b * a.Hq + g * G + h) * D + i % D] : 0.f;
   }
-  __syncthreads();
-  const float scale = 1.f / sqrtf((float)D);
-
-  // scores: one position per thread, its K row read once for all heads
+  // row offsets of the split (the block table read once); ~0 marks a slot
+  // outside the cache: its row is not copied and its score is -inf
   for (int t = threadIdx.x; t < len; t += kAttnThreads) {
-    if (!a.kv.slot_ok(b, t0 + t)) {  // excluded from the softmax
+    if (a.kv.slot_ok(b, t0 + t)) {
+      off_s[t] = a.kv.offset(a.layer, b, g, t0 + t);
+    } else {
+      off_s[t] = ~(size_t)0;
       if (a.status) atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
-#pragma unroll
-      for (int h = 0; h < GM; ++h) p_s[h * cap + t] = -INFINITY;
-      off_s[t] = 0;  // never dereferenced with a nonzero weight
-      continue;
     }
-    const size_t kr = a.kv.offset(a.layer, b, g, t0 + t);
-    off_s[t] = kr;  // the row's offset, for the value pass
-    float s[GM];
-#pragma unroll
-    for (int h = 0; h < GM; ++h) s[h] = 0.f;
-#pragma unroll
-    for (int ch = 0; ch < D / 8; ++ch) {
-      float kf[8];
-      kv_load8<KV16>(a.kv.k, kr + ch * 8, kf);
-#pragma unroll
-      for (int h = 0; h < GM; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) s[h] = fmaf(q_s[h][ch * 8 + e], kf[e], s[h]);
-    }
-#pragma unroll
-    for (int h = 0; h < GM; ++h) p_s[h * cap + t] = s[h] * scale;
+  }
+  if (threadIdx.x < GM) {
+    m_s[threadIdx.x] = -INFINITY;
+    l_s[threadIdx.x] = 0.f;
   }
   __syncthreads();
 
-  // softmax statistics of the chunk, one warp per head
-  for (int h = warp; h < G; h += kAttnThreads / kWarp) {
-    float m = -INFINITY;
-    for (int t = lane; t < len; t += kWarp) m = fmaxf(m, p_s[h * cap + t]);
-    m = warp_max(m);
-    float l = 0.f;
-    for (int t = lane; t < len; t += kWarp) {
-      const float p = expf(p_s[h * cap + t] - m);
-      p_s[h * cap + t] = p;
-      l += p;
+  const int nchunks = (len + kAttnChunk - 1) / kAttnChunk;
+  const auto issue = [&](int ci) {
+    const int q0 = ci * kAttnChunk, m = min(kAttnChunk, len - q0);
+    unsigned char* kd = kbuf + (size_t)(ci & 1) * kAttnChunk * RS * ES;
+    unsigned char* vd = vbuf + (size_t)(ci & 1) * kAttnChunk * RS * ES;
+    for (int i = threadIdx.x; i < m * PPR; i += kAttnThreads) {
+      const int row = i / PPR, piece = i % PPR;
+      const size_t off = off_s[q0 + row];
+      if (off == ~(size_t)0) continue;
+      const size_t src = off * ES + (size_t)piece * 16;
+      cp_async16(kd + (size_t)row * RS * ES + piece * 16,
+                 static_cast<const unsigned char*>(a.kv.k) + src);
+      cp_async16(vd + (size_t)row * RS * ES + piece * 16,
+                 static_cast<const unsigned char*>(a.kv.v) + src);
     }
-    l = warp_sum(l);
-    if (lane == 0) {
-      m_s[h] = m;
-      l_s[h] = l;
+    cp_async_commit();
+  };
+  const float scale = 1.f / sqrtf((float)D);
+  const int h_pv = threadIdx.x / (D / 2), d2 = threadIdx.x % (D / 2);
+  const bool pv = threadIdx.x < G * (D / 2);
+  float acc0 = 0.f, acc1 = 0.f;
+  if (nchunks > 0) issue(0);
+  for (int ci = 0; ci < nchunks; ++ci) {
+    if (ci + 1 < nchunks) {
+      issue(ci + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
+    __syncthreads();
+    const int q0 = ci * kAttnChunk, m = min(kAttnChunk, len - q0);
+    const unsigned char* kc = kbuf + (size_t)(ci & 1) * kAttnChunk * RS * ES;
+    const unsigned char* vc = vbuf + (size_t)(ci & 1) * kAttnChunk * RS * ES;
+    // scores of every head for one position per thread
+    for (int t = threadIdx.x; t < m; t += kAttnThreads) {
+      if (off_s[q0 + t] == ~(size_t)0) {
+#pragma unroll
+        for (int h = 0; h < GM; ++h) p_s[h * kAttnChunk + t] = -INFINITY;
+        continue;
+      }
+      float sc[GM];
+#pragma unroll
+      for (int h = 0; h < GM; ++h) sc[h] = 0.f;
+#pragma unroll 4
+      for (int k4 = 0; k4 < D / 4; ++k4) {
+        float kf[4];
+        if constexpr (KV16) {
+          const uint2 w = *reinterpret_cast<const uint2*>(kc + ((size_t)t * RS + 4 * k4) * ES);
+          kf[0] = bf16_lo(w.x); kf[1] = bf16_hi(w.x); kf[2] = bf16_lo(w.y); kf[3] = bf16_hi(w.y);
+        } else {
+          const float4 w = *reinterpret_cast<const float4*>(kc + ((size_t)t * RS + 4 * k4) * ES);
+          kf[0] = w.x; kf[1] = w.y; kf[2] = w.z; kf[3] = w.w;
+        }
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+          const float4 qv = *reinterpret_cast<const float4*>(&q_s[h][4 * k4]);
+          sc[h] = fmaf(qv.x, kf[0], sc[h]);
+          sc[h] = fmaf(qv.y, kf[1], sc[h]);
+          sc[h] = fmaf(qv.z, kf[2], sc[h]);
+          sc[h] = fmaf(qv.w, kf[3], sc[h]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < GM; ++h) p_s[h * kAttnChunk + t] = sc[h] * scale;
+    }
+    __syncthreads();
+    // running softmax statistics, one warp per head
+    for (int h = warp; h < G; h += kAttnThreads / kWarp) {
+      float mx = -INFINITY;
+      for (int t = lane; t < m; t += kWarp) mx = fmaxf(mx, p_s[h * kAttnChunk + t]);
+      mx = warp_max(mx);
+      const float m_new = fmaxf(m_s[h], mx);
+      float l = 0.f;
+      for (int t = lane; t < m; t += kWarp) {
+        const float x = p_s[h * kAttnChunk + t];
+        const float p = x == -INFINITY ? 0.f : expf(x - m_new);
+        p_s[h * kAttnChunk + t] = p;
+        l += p;
+      }
+      l = warp_sum(l);
+      if (lane == 0) {
+        const float r = m_s[h] == -INFINITY ? 0.f : expf(m_s[h] - m_new);
+        r_s[h] = r;
+        l_s[h] = l_s[h] * r + l;
+        m_s[h] = m_new;
+      }
+    }
+    __syncthreads();
+    // values, running sums rescaled by the chunk's factor
+    if (pv) {
+      float e0 = 0.f, e1 = 0.f;
+#pragma unroll 4
+      for (int t = 0; t < m; ++t) {
+        const float p = p_s[h_pv * kAttnChunk + t];
+        float2 v;
+        if constexpr (KV16) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(vc + ((size_t)t * RS + 2 * d2) * ES);
+          v = make_float2(bf16_lo(w), bf16_hi(w));
+        } else {
+          v = *reinterpret_cast<const float2*>(vc + ((size_t)t * RS + 2 * d2) * ES);
+        }
+        // a slot outside the cache (p = 0) left its row stale: not multiplied
+        e0 = fmaf(p, p == 0.f ? 0.f : v.x, e0);
+        e1 = fmaf(p, p == 0.f ? 0.f : v.y, e1);
+      }
+      const float r = r_s[h_pv];
+      acc0 = fmaf(acc0, r, e0);
+      acc1 = fmaf(acc1, r, e1);
+    }
+    __syncthreads();  // the buffers of this chunk are refilled two chunks on
   }
-  __syncthreads();
-
-  // weighted values: one thread per (head, pair of dims). The row offsets
-  // come from shared memory, so the loads of several positions are in flight
-  // together (a per-position block-table lookup before each load would
-  // serialise them).
-  for (int idx = threadIdx.x; idx < G * (D / 2); idx += kAttnThreads) {
-    const int h = idx / (D / 2), d2 = idx % (D / 2);
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 8
-    for (int t = 0; t < len; ++t) {
-      const float p = p_s[h * cap + t];
-      const float2 w = kv_load2<KV16>(a.kv.v, off_s[t] + 2 * d2);
-      // an excluded slot (p = 0) is not multiplied: its row may be anything
-      acc0 = fmaf(p, p == 0.f ? 0.f : w.x, acc0);
-      acc1 = fmaf(p, p == 0.f ? 0.f : w.y, acc1);
-    }
-    float* ph = part + ((size_t)h * S + c) * (D + 2);
+  if (pv) {
+    float* ph = part + ((size_t)h_pv * S + c) * (D + 2);
     ph[2 + 2 * d2] = acc0;
     ph[3 + 2 * d2] = acc1;
     if (d2 == 0) {
-      ph[0] = len > 0 ? m_s[h] : -INFINITY;
-      ph[1] = len > 0 ? l_s[h] : 0.f;
+      ph[0] = len > 0 ? m_s[h_pv] : -INFINITY;
+      ph[1] = len > 0 ? l_s[h_pv] : 0.f;
     }
   }
 }
@@ -217,7 +308,9 @@ __global__ void k_attn_merge(AttnArgs a) {
 
 template <int D, int GM, bool KV16>
 static cudaError_t attn_split(const AttnArgs& a, int cap, cudaStream_t s) {
-  const size_t smem = sizeof(float) * (size_t)((GM * cap + 1) & ~1) + sizeof(size_t) * (size_t)cap;
+  constexpr int ES = KV16 ? 2 : 4, RS = D + 16 / ES;
+  const size_t smem = (size_t)4 * kAttnChunk * RS * ES + sizeof(float) * GM * kAttnChunk +
+                      sizeof(size_t) * (size_t)cap;
   cudaError_t e = ensure_smem<k_attn_split<D, GM, KV16>>();
   if (e != cudaSuccess) return e;
   k_attn_split<D, GM, KV16><<<dim3(a.splits, a.Hkv, a.B), kAttnThreads, smem, s>>>(a, cap);
