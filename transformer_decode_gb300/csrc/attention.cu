@@ -26,12 +26,14 @@ __global__ void __launch_bounds__(256) k_rope_qkv(RopeArgs a) {
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   const int pos = a.positions[b];
   if (!a.kv.slot_ok(b, pos)) {
-    if (threadIdx.x == 0 && a.status) atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
+    if (threadIdx.x == 0 && blockIdx.y == 0 && a.status) atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
     return;
   }
   const int qkv_dim = (a.Hq + 2 * a.Hkv) * D;
   const float* src = a.qkv + (size_t)b * qkv_dim;
-  for (int hh = warp; hh < a.Hq + a.Hkv; hh += blockDim.x / kWarp) {
+  // blockIdx.y picks this CTA's heads: one per warp, so the heads run side by side
+  for (int hh = blockIdx.y * (blockDim.x / kWarp) + warp; hh < a.Hq + a.Hkv;
+       hh += gridDim.y * (blockDim.x / kWarp)) {
     const bool is_q = hh < a.Hq;
     const float* v = src + (size_t)hh * D;
     float e[E];
@@ -75,16 +77,18 @@ __global__ void __launch_bounds__(256) k_rope_qkv(RopeArgs a) {
 }
 
 cudaError_t launch_rope_qkv(const RopeArgs& a, cudaStream_t s) {
+  const dim3 grid(a.B, (a.Hq + a.Hkv + 7) / 8);  // 8 warps per CTA, one head each
   if (a.D == 64)
-    (a.kv.bf16 ? k_rope_qkv<64, true> : k_rope_qkv<64, false>)<<<a.B, 256, 0, s>>>(a);
+    (a.kv.bf16 ? k_rope_qkv<64, true> : k_rope_qkv<64, false>)<<<grid, 256, 0, s>>>(a);
   else
-    (a.kv.bf16 ? k_rope_qkv<128, true> : k_rope_qkv<128, false>)<<<a.B, 256, 0, s>>>(a);
+    (a.kv.bf16 ? k_rope_qkv<128, true> : k_rope_qkv<128, false>)<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ attention
 constexpr int kAttnThreads = 256;
 constexpr int kMaxChunk = 512;
+constexpr int kMaxSplits = 128;  // splits of one (sequence, kv head); the merge keeps one weight each
 
 int attn_splits(int B, int Hkv, int max_ctx) {
   const int target = 2 * num_sms();
@@ -93,7 +97,7 @@ int attn_splits(int B, int Hkv, int max_ctx) {
   const int hi = (max_ctx + 15) / 16;
   if (s > hi) s = hi;
   if (s < lo) s = lo;
-  if (s > 256) s = 256;
+  if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : s;
 }
 
@@ -291,18 +295,36 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a, int cap
 
 template <int D>
 __global__ void k_attn_merge(AttnArgs a) {
+  // M = max_c m_c and the split weights w_c = e^(m_c - M) are formed once and
+  // shared; each thread then sums its dimension over the splits with the
+  // loads independent of one another
+  __shared__ float w_s[kMaxSplits];
+  __shared__ float red[2][D / kWarp];
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, S = a.splits;
+  const int warp = d / kWarp, lane = d % kWarp;
   const float* ph = a.part + ((size_t)b * a.Hq + h) * S * (D + 2);
   float M = -INFINITY;
-  for (int c = 0; c < S; ++c) M = fmaxf(M, ph[(size_t)c * (D + 2)]);
-  float num = 0.f, den = 0.f;
-  for (int c = 0; c < S; ++c) {
-    const float mc = ph[(size_t)c * (D + 2)];
-    if (mc == -INFINITY) continue;
-    const float w = expf(mc - M);
+  for (int c = d; c < S; c += D) M = fmaxf(M, ph[(size_t)c * (D + 2)]);
+  M = warp_max(M);
+  if (lane == 0) red[0][warp] = M;
+  __syncthreads();
+  M = red[0][0];
+  for (int i = 1; i < D / kWarp; ++i) M = fmaxf(M, red[0][i]);
+  float den = 0.f;
+  for (int c = d; c < S; c += D) {
+    const float m = ph[(size_t)c * (D + 2)];
+    const float w = m == -INFINITY ? 0.f : expf(m - M);
+    w_s[c] = w;
     den = fmaf(ph[(size_t)c * (D + 2) + 1], w, den);
-    num = fmaf(ph[(size_t)c * (D + 2) + 2 + d], w, num);
   }
+  den = warp_sum(den);
+  if (lane == 0) red[1][warp] = den;
+  __syncthreads();
+  den = 0.f;
+  for (int i = 0; i < D / kWarp; ++i) den += red[1][i];
+  float num = 0.f;
+#pragma unroll 8
+  for (int c = 0; c < S; ++c) num = fmaf(ph[(size_t)c * (D + 2) + 2 + d], w_s[c], num);
   a.out[((size_t)b * a.Hq + h) * D + d] = num / den;
 }
 

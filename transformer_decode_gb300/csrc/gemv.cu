@@ -68,20 +68,22 @@ __device__ __forceinline__ void fill_xs(const float* x, const uint16_t* gamma, c
 }
 
 // acc[r][b] += W_r[tile] . xs[b][tile] for the R rows of one warp; lanes take
-// 16-byte chunks lane, lane+32, ...; four chunks per row are loaded before use.
+// 16-byte chunks lane, lane+32, ...; U chunks per row (eight at batch 1) are loaded
+// before use.
 template <int BT, int R>
 __device__ __forceinline__ void warp_dot(const uint16_t* const (&row)[R], int nchunk,
                                          const float* xs, int kt, float (&acc)[R][BT]) {
   const int lane = threadIdx.x % kWarp;
+  constexpr int U = BT == 1 ? 8 : 4;  // chunks per row in flight
   int c = lane;
-  for (; c + 3 * kWarp < nchunk; c += 4 * kWarp) {
-    uint4 w[R][4];
+  for (; c + (U - 1) * kWarp < nchunk; c += U * kWarp) {
+    uint4 w[R][U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int r = 0; r < R; ++r) w[r][u] = ld_stream(row[r] + (size_t)(c + u * kWarp) * 8);
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
