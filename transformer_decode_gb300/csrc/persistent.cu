@@ -129,6 +129,7 @@ struct PShared {
   int abort;        // set once a bounded wait expired in this CTA
   unsigned issued;  // tiles the producer issued
   int pos[kPMaxBatch];
+  float rope_cs[kPMaxBatch][64], rope_sn[kPMaxBatch][64];  // RoPE cos / sin at each position (D/2 <= 64)
   int tok[kPMaxBatch];
   float rn[kPMaxBatch];
   float red[kPConsumerWarps][kPMaxBatch];
@@ -884,7 +885,6 @@ __device__ __forceinline__ float2 kv_smem2(const char* base, int idx) {
 // split's state leaves as its normalised output o = acc / l per (head, dim)
 // and (m, l) per head (Tang section 2.2: the partials of a split-K scan that
 // the o-proj gather merges).
-constexpr int kAttnWords = 4;  // q/k/v words gathered per thread: (G + 2) D <= 4 * 352
 template <int D, bool KV16>
 __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int split,
                                             int p0, int p1, int layer, uint32_t ep_qkv,
@@ -917,97 +917,64 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   float* resc = lrun + GM;                    // [GM] rescale of the chunk
   const PLayer& P = S.layers[layer];
 
-  // gather the G query heads, k and v of this group: all loads in flight
-  // first; while they are out, fetch what does not depend on them (the
-  // rotation angles of this lane's dimension pairs -- every RoPE warp below
-  // uses the same lane -> dimension map -- and the q/k norm gains); then
-  // re-poll the words that were stale
-  const uint64_t* qkv = a.qkvw + (size_t)b * a.nqkv;
-  const int total = (G + 2) * D;
-  uint64_t w[kAttnWords];
-  const int nw = total > ct ? (total - ct + kPConsumerThreads - 1) / kPConsumerThreads : 0;
-  const auto addr = [qkv, ct, G, g, Hq, Hkv](int u) {
-    const int i = ct + u * kPConsumerThreads;
-    const int h = i / D, d = i % D;
-    return qkv + (h < G ? (g * G + h) * D + d
-                        : (h == G ? (Hq + g) * D + d : (Hq + Hkv + g) * D + d));
-  };
-#pragma unroll
-  for (int u = 0; u < kAttnWords; ++u)
-    if (u < nw) w[u] = ld_word(addr(u));
-  const float* inv_freq = a.inv_freq;
-  float cs[E / 2], sn[E / 2];
-#pragma unroll
-  for (int j = 0; j < E / 2; ++j) {
-    const float angle = __fmul_rn((float)pos, inv_freq[lane + 32 * j]);
-    sincosf(angle, &sn[j], &cs[j]);
-  }
+  // Warp w < G gathers query head w, warp G the key, warp G + 1 the value;
+  // lane l holds dims l + 32 j, so a RoPE pair (i, i + D/2) sits in one lane:
+  // the q/k norm and the rotation run in registers (angles from the per-step
+  // table), then K and V go to the cache straight from the owning warps.
+  const bool pos_ok = kv.slot_ok(b, pos);
+  const bool own_new = pos_ok && split == 0;  // the new position belongs to split 0
+  if (!pos_ok && split == 0 && ct == 0 && status) atomicCAS(status, 0, (int)NC_ERR_POSITION);
   const uint16_t* gq = P.g_q;
   const uint16_t* gk = P.g_k;
-  float gain_q[E], gain_k[E];
+  if (warp < G + 2) {
+    const uint64_t* qkv = a.qkvw + (size_t)b * a.nqkv;
+    const uint64_t* src =
+        qkv + (warp < G ? (g * G + warp) * D : (warp == G ? (Hq + g) * D : (Hq + Hkv + g) * D));
+    const auto addr = [src, lane](int j) { return src + lane + 32 * j; };
+    uint64_t w[E];
 #pragma unroll
-  for (int j = 0; j < E; ++j) {
-    gain_q[j] = gq ? bf16_to_f32(gq[lane + 32 * j]) : 1.f;
-    gain_k[j] = gk ? bf16_to_f32(gk[lane + 32 * j]) : 1.f;
-  }
-  ll_settle<kAttnWords>(addr, (1u << nw) - 1u, ep_qkv, w, sp);
-  {
+    for (int j = 0; j < E; ++j) w[j] = ld_word(addr(j));
+    const uint16_t* gain = warp < G ? gq : (warp == G ? gk : nullptr);
+    float gn[E];
 #pragma unroll
-    for (int u = 0; u < kAttnWords; ++u) {
-      const int i = ct + u * kPConsumerThreads;
-      if (u >= nw) break;
-      float v = __uint_as_float(static_cast<uint32_t>(w[u]));
-      const int h = i / D, d = i % D;
-      if (h < G) {
-        qs[h * D + d] = v;
-      } else if (h == G) {
-        kn[d] = v;
-      } else {
-        if (KV16) v = bf16_to_f32(f32_to_bf16(v));  // the scan uses v as the cache stores it
-        vn[d] = v;
-      }
-    }
-  }
-  consumer_sync();
-  // per-head RMSNorm (q/k norm) and RoPE, one warp per head (G is the key)
-  for (int hh = warp; hh <= G; hh += kPConsumerWarps) {
-    float* v = hh < G ? qs + hh * D : kn;
+    for (int j = 0; j < E; ++j) gn[j] = gain ? bf16_to_f32(gain[lane + 32 * j]) : 1.f;
+    ll_settle<E>(addr, (1u << E) - 1u, ep_qkv, w, sp);
     float e[E];
 #pragma unroll
-    for (int j = 0; j < E; ++j) e[j] = v[lane + 32 * j];
-    if (hh < G ? gq != nullptr : gk != nullptr) {
+    for (int j = 0; j < E; ++j) e[j] = __uint_as_float(static_cast<uint32_t>(w[j]));
+    if (gain) {  // per-head RMSNorm over D
       float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < E; ++j) ss = fmaf(e[j], e[j], ss);
       ss = warp_sum(ss);
       const float r = 1.f / sqrtf(ss / (float)D + eps);
 #pragma unroll
-      for (int j = 0; j < E; ++j) e[j] = (e[j] * r) * (hh < G ? gain_q[j] : gain_k[j]);
+      for (int j = 0; j < E; ++j) e[j] = (e[j] * r) * gn[j];
     }
+    if (warp <= G) {  // RoPE on q and k
 #pragma unroll
-    for (int j = 0; j < E / 2; ++j) {
-      const float x0 = e[j], x1 = e[j + E / 2];
-      e[j] = __fsub_rn(__fmul_rn(x0, cs[j]), __fmul_rn(x1, sn[j]));
-      e[j + E / 2] = __fadd_rn(__fmul_rn(x1, cs[j]), __fmul_rn(x0, sn[j]));
+      for (int j = 0; j < E / 2; ++j) {
+        const float cs = S.rope_cs[b][lane + 32 * j], sn = S.rope_sn[b][lane + 32 * j];
+        const float x0 = e[j], x1 = e[j + E / 2];
+        e[j] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+        e[j + E / 2] = __fadd_rn(__fmul_rn(x1, cs), __fmul_rn(x0, sn));
+      }
     }
+    if (KV16 && warp >= G)  // k and v as the cache stores them
 #pragma unroll
-    for (int j = 0; j < E; ++j) {
-      float x = e[j];
-      if (KV16 && hh == G) x = bf16_to_f32(f32_to_bf16(x));  // k as the cache stores it
-      v[lane + 32 * j] = x;
+      for (int j = 0; j < E; ++j) e[j] = bf16_to_f32(f32_to_bf16(e[j]));
+    float* dst = warp < G ? qs + warp * D : (warp == G ? kn : vn);
+#pragma unroll
+    for (int j = 0; j < E; ++j) dst[lane + 32 * j] = e[j];
+    if (warp >= G && own_new) {  // append at slot pos
+      const size_t off = kv.offset(layer, b, g, pos);
+      void* cache = warp == G ? kv.k : kv.v;
+#pragma unroll
+      for (int j = 0; j < E; ++j) kv_store<KV16>(cache, off + lane + 32 * j, e[j]);
     }
   }
   consumer_sync();
-  // append K/V at slot pos; the new position opens the running state:
-  // m = its score, l = 1, acc = v
-  const bool pos_ok = kv.slot_ok(b, pos);
-  const bool own_new = pos_ok && split == 0;  // the new position belongs to split 0
-  if (!pos_ok && split == 0 && ct == 0 && status) atomicCAS(status, 0, (int)NC_ERR_POSITION);
-  if (ct < D && own_new) {
-    const size_t off = kv.offset(layer, b, g, pos);
-    kv_store<KV16>(kv.k, off + ct, kn[ct]);
-    kv_store<KV16>(kv.v, off + ct, vn[ct]);
-  }
+  // the new position opens the running state: m = its score, l = 1, acc = v
   const float scale = 1.f / sqrtf((float)D);
   for (int h = warp; h < G; h += kPConsumerWarps) {
     float s = 0.f;
@@ -1452,6 +1419,15 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   } else {
     const int ct = threadIdx.x - kWarp, cw = ct / kWarp;
     const int L = a.L, nph = kPhasesPerLayer * L + 1;
+    // RoPE angles of this step's positions, read by the attention items
+    for (int i = ct; i < BT * (D / 2); i += kPConsumerThreads) {
+      const int b = i / (D / 2), j = i % (D / 2);
+      float sn, cs;
+      sincosf(__fmul_rn((float)S.pos[b], a.inv_freq[j]), &sn, &cs);
+      S.rope_cs[b][j] = cs;
+      S.rope_sn[b][j] = sn;
+    }
+    consumer_sync();
     RingPos rp;
     int kb = 0;  // k-split partial-sum buffer of the next split tile
     unsigned long long best[BT];
@@ -1614,7 +1590,7 @@ bool persistent_supported(int L, int H, int qd, int F, int D, int G, int B) {
   if (L < 1 || L > kPMaxLayers) return false;
   if (G < 1 || G > 8 || G * (D / 2) > kPConsumerThreads) return false;
   if (H % 8 || qd % 8 || F % 8) return false;
-  if ((G + 2) * D > kAttnWords * kPConsumerThreads) return false;
+  if (G + 2 > kPConsumerWarps) return false;  // one gathering warp per q head, k and v
   if (qd / D > kPMaxHeads) return false;
   // rows one CTA may own: the o-proj rows go to at least half of the CTAs
   const int grid = num_sms(), half = grid - grid / 2;
