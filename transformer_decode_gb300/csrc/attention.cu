@@ -22,6 +22,7 @@ namespace nc {
 template <int D, bool KV16>
 __global__ void __launch_bounds__(256) k_rope_qkv(RopeArgs a) {
   constexpr int E = D / 32;  // elements per lane
+  pdl_wait();
   const int b = blockIdx.x;
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   const int pos = a.positions[b];
@@ -78,11 +79,9 @@ __global__ void __launch_bounds__(256) k_rope_qkv(RopeArgs a) {
 
 cudaError_t launch_rope_qkv(const RopeArgs& a, cudaStream_t s) {
   const dim3 grid(a.B, (a.Hq + a.Hkv + 7) / 8);  // 8 warps per CTA, one head each
-  if (a.D == 64)
-    (a.kv.bf16 ? k_rope_qkv<64, true> : k_rope_qkv<64, false>)<<<grid, 256, 0, s>>>(a);
-  else
-    (a.kv.bf16 ? k_rope_qkv<128, true> : k_rope_qkv<128, false>)<<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  const auto kern = a.D == 64 ? (a.kv.bf16 ? k_rope_qkv<64, true> : k_rope_qkv<64, false>)
+                              : (a.kv.bf16 ? k_rope_qkv<128, true> : k_rope_qkv<128, false>);
+  return launch_pdl(kern, grid, dim3(256), 0, s, a);
 }
 
 // ------------------------------------------------------------------ attention
@@ -142,6 +141,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a, int cap
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z, S = gridDim.x;
   const int G = a.Hq / a.Hkv;
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  pdl_wait();
   const int pos = a.positions[b];
   if ((pos < 0 || pos >= a.kv.capacity()) && threadIdx.x == 0 && c == 0 && g == 0 && a.status)
     atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
@@ -302,6 +302,7 @@ __global__ void k_attn_merge(AttnArgs a) {
   __shared__ float red[2][D / kWarp];
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, S = a.splits;
   const int warp = d / kWarp, lane = d % kWarp;
+  pdl_wait();
   const float* ph = a.part + ((size_t)b * a.Hq + h) * S * (D + 2);
   float M = -INFINITY;
   for (int c = d; c < S; c += D) M = fmaxf(M, ph[(size_t)c * (D + 2)]);
@@ -335,16 +336,15 @@ static cudaError_t attn_split(const AttnArgs& a, int cap, cudaStream_t s) {
                       sizeof(size_t) * (size_t)cap;
   cudaError_t e = ensure_smem<k_attn_split<D, GM, KV16>>();
   if (e != cudaSuccess) return e;
-  k_attn_split<D, GM, KV16><<<dim3(a.splits, a.Hkv, a.B), kAttnThreads, smem, s>>>(a, cap);
-  return cudaGetLastError();
+  return launch_pdl(k_attn_split<D, GM, KV16>, dim3(a.splits, a.Hkv, a.B), dim3(kAttnThreads), smem,
+                    s, a, cap);
 }
 
 template <int D, int GM>
 static cudaError_t attn_dg(const AttnArgs& a, int cap, cudaStream_t s) {
   cudaError_t e = a.kv.bf16 ? attn_split<D, GM, true>(a, cap, s) : attn_split<D, GM, false>(a, cap, s);
   if (e != cudaSuccess) return e;
-  k_attn_merge<D><<<dim3(a.Hq, a.B), D, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_attn_merge<D>, dim3(a.Hq, a.B), dim3(D), 0, s, a);
 }
 
 template <int D>

@@ -203,6 +203,13 @@ __global__ void __launch_bounds__(kGThreads) k_gemm16(GemvArgs a, int KR) {
   uint16_t* hi = gsm;
   uint16_t* lo = gsm + 16 * stride;
 
+  // warm L2 with this tile's weights (no earlier kernel writes them), then
+  // wait for the activations
+  if (threadIdx.x < 16 && r0 + (int)threadIdx.x < N) {
+    prefetch_l2(a.W + (size_t)(r0 + threadIdx.x) * K + k0, (uint32_t)kr * 2);
+    if (PAIR) prefetch_l2(a.W + ((size_t)N + r0 + threadIdx.x) * K + k0, (uint32_t)kr * 2);
+  }
+  pdl_wait();
   if (a.gamma) norms16(a.x, a.B, K, a.eps, rn);
   __syncthreads();
   build_planes(a.x, a.gamma, rn, a.B, K, k0, kr, stride, hi, lo);
@@ -245,6 +252,9 @@ __global__ void __launch_bounds__(kGThreads) k_lm_head16(LmHeadArgs a) {
   const int stride = K + kGPad;
   uint16_t* hi = gsm;
   uint16_t* lo = gsm + 16 * stride;
+  if (threadIdx.x < 16 && blockIdx.x * 16 + (int)threadIdx.x < V)
+    prefetch_l2(a.W + (size_t)(blockIdx.x * 16 + threadIdx.x) * K, (uint32_t)K * 2);
+  pdl_wait();
   norms16(a.x, a.B, K, a.eps, rn);
   __syncthreads();
   build_planes(a.x, a.gamma, rn, a.B, K, 0, K, stride, hi, lo);
@@ -339,8 +349,7 @@ static cudaError_t gemm16_epi(const GemvArgs& a, cudaStream_t s) {
   auto kern = k_gemm16<EPI>;
   cudaError_t e = ensure_smem<k_gemm16<EPI>>();
   if (e != cudaSuccess) return e;
-  kern<<<dim3(tiles, ks), kGThreads, planes_bytes(KR), s>>>(a, KR);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(tiles, ks), dim3(kGThreads), planes_bytes(KR), s, a, KR);
 }
 
 cudaError_t launch_gemm16(Epi epi, const GemvArgs& a, cudaStream_t s) {
@@ -354,8 +363,7 @@ cudaError_t launch_gemm16(Epi epi, const GemvArgs& a, cudaStream_t s) {
 cudaError_t launch_lm_head16(const LmHeadArgs& a, cudaStream_t s) {
   cudaError_t e = ensure_smem<k_lm_head16>();
   if (e != cudaSuccess) return e;
-  k_lm_head16<<<lm_head_grid(), kGThreads, planes_bytes(a.K), s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_lm_head16, dim3(lm_head_grid()), dim3(kGThreads), planes_bytes(a.K), s, a);
 }
 
 }  // namespace nc

@@ -16,6 +16,8 @@
 //     block, combined by the last block to finish (Tang section 2.2).
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include "kernels.h"
 
 namespace nc {
@@ -23,6 +25,7 @@ namespace nc {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / kWarp;
 constexpr int kXsFloats = 16384;  // activations kept in shared memory per K tile (64 KB)
+constexpr int kRowPrefetchBytes = 32768;  // L2 warm-up per weight row before the wait
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
   // nanoinfer "Phase 8": both sigmoid halves share e = exp(-|g|).
@@ -31,16 +34,21 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return (g * sig) * u;
 }
 
-// Per-row RMSNorm factors r[b] = 1 / sqrt(sum(x^2) / K + eps) into rn[] (shared).
+// Per-row RMSNorm factors r[b] = 1 / sqrt(sum(x^2) / K + eps) into rn[] (shared):
+// every warp sums a slice of each row, the partials are added in a fixed order.
 template <int BT>
-__device__ __forceinline__ void row_norms(const float* x, int B, int K, float eps, float* rn) {
+__device__ __forceinline__ void row_norms(const float* x, int B, int K, float eps,
+                                          float (*part)[BT], float* rn) {
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-  for (int b = warp; b < BT; b += kWarps) {
+  const int nv = K / 4;
+#pragma unroll 1
+  for (int b = 0; b < BT; ++b) {
     float ss = 0.f;
     if (b < B) {
-      const float* xb = x + (size_t)b * K;
-      for (int k = lane * 4; k < K; k += kWarp * 4) {
-        const float4 v = *reinterpret_cast<const float4*>(xb + k);
+      const float4* xb = reinterpret_cast<const float4*>(x + (size_t)b * K);
+#pragma unroll 4
+      for (int i = threadIdx.x; i < nv; i += kThreads) {
+        const float4 v = xb[i];
         ss = fmaf(v.x, v.x, ss);
         ss = fmaf(v.y, v.y, ss);
         ss = fmaf(v.z, v.z, ss);
@@ -48,55 +56,74 @@ __device__ __forceinline__ void row_norms(const float* x, int B, int K, float ep
       }
     }
     ss = warp_sum(ss);
-    if (lane == 0) rn[b] = 1.f / sqrtf(ss / (float)K + eps);
+    if (lane == 0) part[warp][b] = ss;
+  }
+  __syncthreads();
+  if (threadIdx.x < BT) {
+    float ss = 0.f;
+    for (int w = 0; w < kWarps; ++w) ss += part[w][threadIdx.x];
+    rn[threadIdx.x] = 1.f / sqrtf(ss / (float)K + eps);
   }
 }
 
-// xs[b][kk] = x[b][k0 + kk] * r[b] * gamma[k0 + kk] for kk < kt (zero for b >= B).
+// xs[b][kk] = x[b][k0 + kk] * r[b] * gamma[k0 + kk] for kk < kt (zero for b >= B),
+// four elements per thread and step (kt a multiple of 4).
 template <int BT>
 __device__ __forceinline__ void fill_xs(const float* x, const uint16_t* gamma, const float* rn,
                                         int B, int K, int k0, int kt, float* xs) {
-  for (int i = threadIdx.x; i < BT * kt; i += kThreads) {
-    const int b = i / kt, kk = i - b * kt;
-    float v = 0.f;
+  const int kt4 = kt / 4;
+  const bool g8 = (reinterpret_cast<uintptr_t>(gamma) & 7) == 0;
+#pragma unroll 4
+  for (int i = threadIdx.x; i < BT * kt4; i += kThreads) {
+    const int b = i / kt4, kk = (i - b * kt4) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (b < B) {
-      v = x[(size_t)b * K + k0 + kk];
-      if (gamma) v = (v * rn[b]) * bf16_to_f32(gamma[k0 + kk]);
+      v = *reinterpret_cast<const float4*>(x + (size_t)b * K + k0 + kk);
+      if (gamma) {
+        const uint16_t* gp = gamma + k0 + kk;
+        float g0, g1, g2, g3;
+        if (g8) {
+          const uint2 gw = *reinterpret_cast<const uint2*>(gp);
+          g0 = bf16_lo(gw.x); g1 = bf16_hi(gw.x); g2 = bf16_lo(gw.y); g3 = bf16_hi(gw.y);
+        } else {
+          g0 = bf16_to_f32(gp[0]); g1 = bf16_to_f32(gp[1]);
+          g2 = bf16_to_f32(gp[2]); g3 = bf16_to_f32(gp[3]);
+        }
+        const float r = rn[b];
+        v.x = (v.x * r) * g0;
+        v.y = (v.y * r) * g1;
+        v.z = (v.z * r) * g2;
+        v.w = (v.w * r) * g3;
+      }
     }
-    xs[i] = v;
+    *reinterpret_cast<float4*>(xs + (size_t)b * kt + kk) = v;
   }
 }
 
 // acc[r][b] += W_r[tile] . xs[b][tile] for the R rows of one warp; lanes take
-// 16-byte chunks lane, lane+32, ...; U chunks per row (eight at batch 1) are loaded
-// before use.
+// 16-byte chunks lane, lane+32, ...; U chunks per row (eight at batch 1) are
+// loaded before use, the ones past the row's end predicated off.
 template <int BT, int R>
 __device__ __forceinline__ void warp_dot(const uint16_t* const (&row)[R], int nchunk,
                                          const float* xs, int kt, float (&acc)[R][BT]) {
   const int lane = threadIdx.x % kWarp;
   constexpr int U = BT == 1 ? 8 : 4;  // chunks per row in flight
-  int c = lane;
-  for (; c + (U - 1) * kWarp < nchunk; c += U * kWarp) {
+  for (int c = lane; c < nchunk; c += U * kWarp) {
     uint4 w[R][U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int r = 0; r < R; ++r) w[r][u] = ld_stream(row[r] + (size_t)(c + u * kWarp) * 8);
+      for (int r = 0; r < R; ++r)
+        w[r][u] = c + u * kWarp < nchunk ? ld_stream(row[r] + (size_t)(c + u * kWarp) * 8)
+                                         : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int u = 0; u < U; ++u)
+      if (c + u * kWarp < nchunk)
 #pragma unroll
-      for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int b = 0; b < BT; ++b) acc[r][b] += dot8(w[r][u], xs + b * kt + (c + u * kWarp) * 8);
-  }
-  for (; c < nchunk; c += kWarp) {
-    uint4 w[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) w[r] = ld_stream(row[r] + (size_t)c * 8);
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int b = 0; b < BT; ++b) acc[r][b] += dot8(w[r], xs + b * kt + c * 8);
+          for (int b = 0; b < BT; ++b)
+            acc[r][b] += dot8(w[r][u], xs + b * kt + (c + u * kWarp) * 8);
   }
 }
 
@@ -104,27 +131,40 @@ __host__ __device__ constexpr int tile_k(int K, int BT) {
   return K <= kXsFloats / BT ? K : (kXsFloats / BT) / 256 * 256;
 }
 
+// Block i owns the rows [N i / grid, N (i + 1) / grid): an even split, so every
+// SM streams the same bytes; the grid is one wave of resident blocks.
 template <int BT, Epi EPI>
 __global__ void __launch_bounds__(kThreads) k_gemv(GemvArgs a) {
   extern __shared__ float4 smem4[];
   float* xs = reinterpret_cast<float*>(smem4);
+  __shared__ float part[kWarps][BT];
   __shared__ float rn[BT];
   constexpr int R = EPI == Epi::SwiGLU ? 2 : 1;
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   const int K = a.K, kt = tile_k(K, BT);
   const bool one_tile = kt >= K;
+  const int r0 = (int)((long long)a.N * blockIdx.x / gridDim.x);
+  const int r1 = (int)((long long)a.N * (blockIdx.x + 1) / gridDim.x);
 
-  if (a.gamma) row_norms<BT>(a.x, a.B, K, a.eps, rn);
+  // the weights depend on no earlier kernel: pull this warp's first row(s)
+  // into L2 while the previous kernel drains
+  if (lane == 0 && r0 + warp < r1) {
+    const uint32_t nb = (uint32_t)min((size_t)K * 2, (size_t)kRowPrefetchBytes);
+    prefetch_l2(a.W + (size_t)(r0 + warp) * K, nb);
+    if constexpr (R == 2) prefetch_l2(a.W + ((size_t)a.N + r0 + warp) * K, nb);
+  }
+  pdl_wait();
+
+  if (a.gamma) row_norms<BT>(a.x, a.B, K, a.eps, part, rn);
   __syncthreads();
   if (one_tile) {
     fill_xs<BT>(a.x, a.gamma, rn, a.B, K, 0, K, xs);
     __syncthreads();
   }
-  const int groups = (a.N + kWarps - 1) / kWarps;
-  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
-    const int n = grp * kWarps + warp;
-    const bool live = n < a.N;
-    const int nr = live ? n : a.N - 1;  // idle warps re-read a valid row, result unused
+  const int iters = (r1 - r0 + kWarps - 1) / kWarps;  // the same for every warp (barriers below)
+  for (int it = 0; it < iters; ++it) {
+    const int n = r0 + it * kWarps + warp;
+    const bool live = n < r1;
     float acc[R][BT];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -137,16 +177,19 @@ __global__ void __launch_bounds__(kThreads) k_gemv(GemvArgs a) {
         fill_xs<BT>(a.x, a.gamma, rn, a.B, K, k0, cur, xs);
         __syncthreads();
       }
-      const uint16_t* rows[R];
-      rows[0] = a.W + (size_t)nr * K + k0;
-      if constexpr (R == 2) rows[1] = a.W + ((size_t)a.N + nr) * K + k0;
-      warp_dot<BT, R>(rows, cur / 8, xs, cur, acc);
+      if (live) {
+        const uint16_t* rows[R];
+        rows[0] = a.W + (size_t)n * K + k0;
+        if constexpr (R == 2) rows[1] = a.W + ((size_t)a.N + n) * K + k0;
+        warp_dot<BT, R>(rows, cur / 8, xs, cur, acc);
+      }
     }
+    if (!live) continue;  // warp-uniform
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int b = 0; b < BT; ++b) acc[r][b] = warp_sum(acc[r][b]);
-    if (live && lane < BT && lane < a.B) {
+    if (lane < BT && lane < a.B) {
       float v[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -165,6 +208,14 @@ __global__ void __launch_bounds__(kThreads) k_gemv(GemvArgs a) {
       }
     }
   }
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("NC_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 int max_smem_optin() {
@@ -197,10 +248,19 @@ static cudaError_t gemv_bt(const GemvArgs& a, cudaStream_t s) {
   auto kern = k_gemv<BT, EPI>;
   cudaError_t e = ensure_smem<k_gemv<BT, EPI>>();
   if (e != cudaSuccess) return e;
+  // one wave: the resident blocks per SM at this shared-memory size, times the SMs
+  static size_t occ_smem = ~(size_t)0;
+  static int occ = 1;
+  if (occ_smem != smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess || n < 1)
+      n = 1;
+    occ = n;
+    occ_smem = smem;
+  }
   const int groups = (a.N + kWarps - 1) / kWarps;
-  const int grid = groups < num_sms() * 8 ? groups : num_sms() * 8;
-  kern<<<grid, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  const int grid = groups < num_sms() * occ ? groups : num_sms() * occ;
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
 }
 
 template <Epi EPI>
@@ -229,9 +289,16 @@ __global__ void __launch_bounds__(kThreads) k_lm_head(LmHeadArgs a) {
   __shared__ float rn[BT];
   __shared__ unsigned long long best_s[kWarps][BT];
   __shared__ bool last_s;
+  __shared__ float part[kWarps][BT];
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   const int K = a.K;
-  row_norms<BT>(a.x, a.B, K, a.eps, rn);
+  {
+    const int n = blockIdx.x * kWarps + warp;
+    if (lane == 0 && n < a.V)
+      prefetch_l2(a.W + (size_t)n * K, (uint32_t)min((size_t)K * 2, (size_t)kRowPrefetchBytes));
+  }
+  pdl_wait();
+  row_norms<BT>(a.x, a.B, K, a.eps, part, rn);
   __syncthreads();
   fill_xs<BT>(a.x, a.gamma, rn, a.B, K, 0, K, xs);
   __syncthreads();
@@ -307,8 +374,7 @@ static cudaError_t lm_bt(const LmHeadArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(float) * (size_t)BT * a.K;
   cudaError_t e = ensure_smem<k_lm_head<BT>>();
   if (e != cudaSuccess) return e;
-  k_lm_head<BT><<<lm_head_grid(), kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_lm_head<BT>, dim3(lm_head_grid()), dim3(kThreads), smem, s, a);
 }
 
 cudaError_t launch_lm_head(const LmHeadArgs& a, cudaStream_t s) {
@@ -323,6 +389,7 @@ cudaError_t launch_lm_head(const LmHeadArgs& a, cudaStream_t s) {
 // ------------------------------------------------------------------ embedding
 __global__ void k_embed(const uint16_t* E, const int32_t* tokens, int B, int H, int V, float* x,
                         int* status) {
+  pdl_wait();
   const int b = blockIdx.y;
   int tok = tokens[b];
   if (tok < 0 || tok >= V) {
@@ -336,8 +403,8 @@ __global__ void k_embed(const uint16_t* E, const int32_t* tokens, int B, int H, 
 
 cudaError_t launch_embed(const uint16_t* E, const int32_t* tokens, int B, int H, int V, float* x,
                          int* status, cudaStream_t s) {
-  k_embed<<<dim3((H + 255) / 256, B), 256, 0, s>>>(E, tokens, B, H, V, x, status);
-  return cudaGetLastError();
+  return launch_pdl(k_embed, dim3((H + 255) / 256, B), dim3(256), 0, s, E, tokens, B, H, V, x,
+                    status);
 }
 
 }  // namespace nc

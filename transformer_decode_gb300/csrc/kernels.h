@@ -3,11 +3,34 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "nc_internal.cuh"
 
 namespace nc {
 
 int num_sms();  // SM count of the current device (cached)
+
+// Launch a stage kernel with programmatic stream serialisation: it may begin
+// while the previous kernel in the stream drains, so it must call pdl_wait()
+// before it touches memory that earlier kernels write. NC_PDL=0 in the
+// environment launches every kernel the ordinary way.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------------ streaming GEMV
 enum class Epi : int { Store = 0, Residual = 1, SwiGLU = 2 };

@@ -55,6 +55,20 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+// Programmatic dependent launch. Stage kernels are launched so that the next
+// kernel in the stream may start once every CTA of this one has exited,
+// before the grid's completion is flushed: its prologue does only work that
+// reads no output of an earlier kernel and writes no global memory (warming
+// L2 with its weights), then waits for the earlier kernels to complete and
+// their writes to be visible (pdl_wait). Launched the ordinary way, the wait
+// is a no-op. (Letting the successor launch early, from the top of a kernel,
+// measured slower: its L2 warm-up then runs too far ahead of use.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Fetch [p, p + bytes) into L2 without waiting (p 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

@@ -31,37 +31,75 @@ __device__ __forceinline__ float silu_mul8(float g, float u) {
   return (g * sig) * u;
 }
 
+// Block i owns the rows [N i / grid, N (i + 1) / grid) (an even split; one wave).
 template <int BT, Epi EPI>
 __global__ void __launch_bounds__(kW8Threads) k_w8a8(W8Args a) {
   extern __shared__ int4 smem_i4[];
   int8_t* xq = reinterpret_cast<int8_t*>(smem_i4);  // [BT][K]
   __shared__ float rn[BT], sx[BT];
+  __shared__ float part[kW8Warps][BT];
   constexpr int R = EPI == Epi::SwiGLU ? 2 : 1;
+  constexpr int U = 4;  // 16-byte chunks per row in flight
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   const int K = a.K;
+  const int r0 = (int)((long long)a.N * blockIdx.x / gridDim.x);
+  const int r1 = (int)((long long)a.N * (blockIdx.x + 1) / gridDim.x);
 
-  // RMSNorm factor and amax of the normed row, one warp per sequence
-  for (int b = warp; b < BT; b += kW8Warps) {
+  // the int8 weights depend on no earlier kernel: warm L2 with this warp's
+  // first row(s) while the previous kernel drains
+  if (lane == 0 && r0 + warp < r1) {
+    const uint32_t nb = (uint32_t)min(K, 32768);
+    prefetch_l2(a.Wq + (size_t)(r0 + warp) * K, nb);
+    if constexpr (R == 2) prefetch_l2(a.Wq + ((size_t)a.N + r0 + warp) * K, nb);
+  }
+  pdl_wait();
+
+  // RMSNorm factor per sequence: every warp sums a slice, the partials are
+  // added in a fixed order
+  if (a.gamma) {
+#pragma unroll 1
+    for (int b = 0; b < BT; ++b) {
+      float ss = 0.f;
+      if (b < a.B) {
+        const float* xb = a.x + (size_t)b * K;
+        for (int k = threadIdx.x; k < K; k += kW8Threads) ss = fmaf(xb[k], xb[k], ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) part[warp][b] = ss;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x < BT) {
     float r = 1.f;
+    if (a.gamma) {
+      float ss = 0.f;
+      for (int w = 0; w < kW8Warps; ++w) ss += part[w][threadIdx.x];
+      r = 1.f / sqrtf(ss / (float)K + a.eps);
+    }
+    rn[threadIdx.x] = r;
+  }
+  __syncthreads();
+  // amax of each normed row (a max: the order of the partials does not matter)
+#pragma unroll 1
+  for (int b = 0; b < BT; ++b) {
     float amax = 0.f;
     if (b < a.B) {
       const float* xb = a.x + (size_t)b * K;
-      if (a.gamma) {
-        float ss = 0.f;
-        for (int k = lane; k < K; k += kWarp) ss = fmaf(xb[k], xb[k], ss);
-        ss = warp_sum(ss);
-        r = 1.f / sqrtf(ss / (float)K + a.eps);
-      }
-      for (int k = lane; k < K; k += kWarp) {
+      const float r = rn[b];
+      for (int k = threadIdx.x; k < K; k += kW8Threads) {
         const float v = a.gamma ? (xb[k] * r) * bf16_to_f32(a.gamma[k]) : xb[k];
         amax = fmaxf(amax, fabsf(v));
       }
-      amax = warp_max(amax);
     }
-    if (lane == 0) {
-      rn[b] = r;
-      sx[b] = __fdiv_rn(amax, 127.f);
-    }
+    amax = warp_max(amax);
+    __syncwarp();
+    if (lane == 0) part[warp][b] = amax;
+  }
+  __syncthreads();
+  if (threadIdx.x < BT) {
+    float amax = 0.f;
+    for (int w = 0; w < kW8Warps; ++w) amax = fmaxf(amax, part[w][threadIdx.x]);
+    sx[threadIdx.x] = __fdiv_rn(amax, 127.f);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < BT * K; i += kW8Threads) {
@@ -79,10 +117,7 @@ __global__ void __launch_bounds__(kW8Threads) k_w8a8(W8Args a) {
   __syncthreads();
 
   const int nchunk = K / 16;
-  const int groups = (a.N + kW8Warps - 1) / kW8Warps;
-  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
-    const int n = grp * kW8Warps + warp;
-    if (n >= a.N) continue;  // warp-uniform; no block barrier below
+  for (int n = r0 + warp; n < r1; n += kW8Warps) {  // no block barrier below
     int acc[R][BT];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -91,19 +126,27 @@ __global__ void __launch_bounds__(kW8Threads) k_w8a8(W8Args a) {
     const int8_t* rows[R];
     rows[0] = a.Wq + (size_t)n * K;
     if constexpr (R == 2) rows[1] = a.Wq + ((size_t)a.N + n) * K;
-    for (int c = lane; c < nchunk; c += kWarp) {
-      uint4 w[R];
+    for (int c = lane; c < nchunk; c += U * kWarp) {
+      uint4 w[R][U];
 #pragma unroll
-      for (int r = 0; r < R; ++r) w[r] = ld_stream(rows[r] + (size_t)c * 16);
+      for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int b = 0; b < BT; ++b) {
-        const int4 xv = *reinterpret_cast<const int4*>(xq + (size_t)b * K + c * 16);
+        for (int r = 0; r < R; ++r)
+          w[r][u] = c + u * kWarp < nchunk ? ld_stream(rows[r] + (size_t)(c + u * kWarp) * 16)
+                                           : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          acc[r][b] = __dp4a((int)w[r].x, xv.x, acc[r][b]);
-          acc[r][b] = __dp4a((int)w[r].y, xv.y, acc[r][b]);
-          acc[r][b] = __dp4a((int)w[r].z, xv.z, acc[r][b]);
-          acc[r][b] = __dp4a((int)w[r].w, xv.w, acc[r][b]);
+      for (int u = 0; u < U; ++u) {
+        if (c + u * kWarp >= nchunk) break;
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          const int4 xv = *reinterpret_cast<const int4*>(xq + (size_t)b * K + (c + u * kWarp) * 16);
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            acc[r][b] = __dp4a((int)w[r][u].x, xv.x, acc[r][b]);
+            acc[r][b] = __dp4a((int)w[r][u].y, xv.y, acc[r][b]);
+            acc[r][b] = __dp4a((int)w[r][u].z, xv.z, acc[r][b]);
+            acc[r][b] = __dp4a((int)w[r][u].w, xv.w, acc[r][b]);
+          }
         }
       }
     }
@@ -144,10 +187,21 @@ static cudaError_t w8_bt(const W8Args& a, cudaStream_t s) {
   const size_t smem = (size_t)BT * a.K;
   cudaError_t e = ensure_smem<k_w8a8<BT, EPI>>();
   if (e != cudaSuccess) return e;
+  // one wave: the resident blocks per SM at this shared-memory size, times the SMs
+  static size_t occ_smem = ~(size_t)0;
+  static int occ = 1;
+  if (occ_smem != smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_w8a8<BT, EPI>, kW8Threads, smem) !=
+            cudaSuccess ||
+        n < 1)
+      n = 1;
+    occ = n;
+    occ_smem = smem;
+  }
   const int groups = (a.N + kW8Warps - 1) / kW8Warps;
-  const int grid = groups < num_sms() * 8 ? groups : num_sms() * 8;
-  k_w8a8<BT, EPI><<<grid, kW8Threads, smem, s>>>(a);
-  return cudaGetLastError();
+  const int grid = groups < num_sms() * occ ? groups : num_sms() * occ;
+  return launch_pdl(k_w8a8<BT, EPI>, dim3(grid), dim3(kW8Threads), smem, s, a);
 }
 
 template <Epi EPI>
