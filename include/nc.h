@@ -245,8 +245,10 @@ nc_status nc_attn_decode(const nc_model* m, int layer, int B, const float* q,
  * cudaMalloc; and latency-critical loops that cannot afford cudaMalloc's
  * implicit synchronisation. It needs no model and allocates nothing: the
  * split partials live in a static device array of 1,048,576 floats (4 MiB)
- * that every GPU loading libnc holds until the process exits. A request whose
- * partials, batch * n_q_heads * splits * (head_dim + 2) floats, exceed it
+ * that every GPU loading libnc holds until the process exits, beside 1,024
+ * static merge counters (zero at load; each call returns the ones it used to
+ * zero). A request whose partials, batch * n_q_heads * splits * (head_dim + 2)
+ * floats, exceed the array, or whose batch * n_kv_heads exceeds the counters,
  * returns NC_ERR_CAPACITY before anything is enqueued. The first call on each
  * device looks up the array's device address (cudaGetSymbolAddress, with that
  * device current); make that first call before any stream capture. All calls

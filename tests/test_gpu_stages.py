@@ -1,5 +1,7 @@
 """GPU parity of each stage entry point against the CPU oracle, through the
 C ABI, on seeded inputs that span several tiles and ragged tails."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -179,10 +181,15 @@ CASES = [
     (synth.QWEN2_0P5B, [0], False),                 # single key: attention returns v
     (synth.QWEN2_0P5B, [16], False),                # 16 past positions
     (synth.QWEN2_0P5B, [17, 1, 100], False),        # ragged batch
+    (synth.QWEN2_0P5B, [512], False),               # nine splits of one chunk each
     (synth.QWEN2_0P5B, [15, 16, 31, 4095], True),   # paged, block boundaries, long
     (synth.QWEN3_8B, [4096], False),                # 8B shape, q/k norm, D = 128
     (synth.QWEN3_8B, [33, 700], True),
     (synth.TINY, [5, 0], True),
+    # a group of 8 query heads per kv head at D = 128 (two value pairs per thread)
+    (dataclasses.replace(synth.TINY_QKNORM, hidden=1024, n_q_heads=8, n_kv_heads=1), [300, 64], True),
+    # one query head per kv head
+    (dataclasses.replace(synth.TINY, n_kv_heads=4), [130, 2], False),
 ]
 
 

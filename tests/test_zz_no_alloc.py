@@ -65,12 +65,12 @@ def test_static_scratch_matches_model_workspace_two_calls():
 def test_static_scratch_rejects_oversized_requests():
     """A request whose partials exceed the static array is refused before any
     launch, with NC_ERR_CAPACITY."""
-    shape = dataclasses.replace(synth.QWEN2_0P5B.with_layers(1), n_q_heads=128, n_kv_heads=16,
+    # 16 x 512 query heads of 130 partial floats already exceed 2^20 floats
+    # with a single split
+    shape = dataclasses.replace(synth.QWEN2_0P5B.with_layers(1), n_q_heads=512, n_kv_heads=64,
                                 head_dim=128, vocab=512)
     B = 16
-    # a paged cache whose tables allow 20,480 positions (40 splits) over a
-    # one-block pool: the request is large, the memory is not
-    table = torch.zeros(B, 1280, dtype=torch.int32)
+    table = torch.zeros(B, 4, dtype=torch.int32)
     kv = nc.KVCache(shape, B, paged=True, block_table=table, num_blocks=1)
     q = torch.zeros(B, shape.q_dim, device="cuda")
     out = torch.zeros(B, shape.q_dim, device="cuda")
@@ -79,3 +79,20 @@ def test_static_scratch_rejects_oversized_requests():
         nc.attn_decode_static(shape, 0, q, pos.cuda(), pos, kv, out)
     assert e.value.code == nc.STATUS.index("NC_ERR_CAPACITY")
     assert b"scratch" in nc.load().nc_last_error_message()
+
+
+def test_static_tickets_reject_oversized_requests():
+    """More (sequence, kv head) pairs than static merge counters: refused
+    before any launch, with NC_ERR_CAPACITY."""
+    shape = dataclasses.replace(synth.QWEN2_0P5B.with_layers(1), n_q_heads=128, n_kv_heads=128,
+                                head_dim=64, vocab=512)
+    B = 16
+    table = torch.zeros(B, 4, dtype=torch.int32)
+    kv = nc.KVCache(shape, B, paged=True, block_table=table, num_blocks=1)
+    q = torch.zeros(B, shape.q_dim, device="cuda")
+    out = torch.zeros(B, shape.q_dim, device="cuda")
+    pos = torch.zeros(B, dtype=torch.int32)
+    with pytest.raises(nc.NCError) as e:
+        nc.attn_decode_static(shape, 0, q, pos.cuda(), pos, kv, out)
+    assert e.value.code == nc.STATUS.index("NC_ERR_CAPACITY")
+    assert b"tickets" in nc.load().nc_last_error_message()

@@ -211,9 +211,10 @@ nc_status nc_attn_decode(const nc_model* m, int layer, int B, const float* q,
   nc_status st = validate_kv(mm, B, positions_host, kv);
   if (st) return st;
   const nc_config& c = mm->cfg;
-  const int splits = attn_splits(B, c.n_kv_heads, kv_capacity(*kv));
+  const int splits =
+      attn_splits(B, c.n_kv_heads, c.head_dim, kv->dtype == NC_KV_BF16, kv_capacity(*kv));
   AttnArgs a{q, positions_dev, B, c.n_q_heads, c.n_kv_heads, c.head_dim, layer, splits,
-             mm->part, out, kv_view(mm, *kv), mm->status};
+             mm->part, out, kv_view(mm, *kv), mm->status, mm->atickets};
   return launch_result(launch_attn(a, S(stream)), "nc_attn_decode");
 }
 

@@ -9,7 +9,8 @@
 // 0..pos of one (sequence, kv head) are cut into `splits` ranges. Each CTA
 // reads its range of K and V once for all G query heads of the group (the
 // repeat_kv expansion folded into indexing, nanocompile "Phase 3"), produces
-// the partial (m, l, acc[D]) per head, and a merge combines the partials:
+// the partial (m, l, acc[D]) per head, and the last CTA of the group to
+// finish combines the partials:
 //   M = max_c m_c,  out = sum_c acc_c e^(m_c - M) / sum_c l_c e^(m_c - M).
 #include <cuda_runtime.h>
 #include <math.h>
@@ -86,16 +87,32 @@ cudaError_t launch_rope_qkv(const RopeArgs& a, cudaStream_t s) {
 
 // ------------------------------------------------------------------ attention
 constexpr int kAttnThreads = 256;
-constexpr int kMaxChunk = 512;
+constexpr int kAttnWarps = kAttnThreads / kWarp;
+constexpr int kAttnCh = 64;      // positions per staged chunk
+constexpr int kAttnStages = 3;   // chunks in shared memory: two in flight while one is used
 constexpr int kMaxSplits = 128;  // splits of one (sequence, kv head); the merge keeps one weight each
+constexpr uint64_t kAttnWaitNs = 1000000000ull;  // bound on any wait for a staged chunk
 
-int attn_splits(int B, int Hkv, int max_ctx) {
-  const int target = 2 * num_sms();
-  int s = (target + B * Hkv - 1) / (B * Hkv);
-  const int lo = (max_ctx + kMaxChunk - 1) / kMaxChunk;
-  const int hi = (max_ctx + 15) / 16;
+template <int D, bool KV16>
+struct AttnGeo {
+  static constexpr int ES = KV16 ? 2 : 4;
+  static constexpr size_t kRow = (size_t)D * ES;          // bytes of one cached row
+  static constexpr size_t kStage = 2 * kAttnCh * kRow;    // a chunk's K rows, then its V rows
+  static constexpr size_t kSmem = kAttnStages * kStage + sizeof(float) * 8 * kAttnCh +
+                                  sizeof(uint64_t) * kAttnStages;
+};
+
+// CTAs of the split kernel one SM holds (shared memory bound), cached per shape.
+template <int D, bool KV16>
+static int attn_occupancy();
+
+// One wave of split CTAs: splits = resident CTAs / (B Hkv), at least one chunk each.
+int attn_splits(int B, int Hkv, int D, bool kv16, int max_ctx) {
+  const int occ = D == 64 ? (kv16 ? attn_occupancy<64, true>() : attn_occupancy<64, false>())
+                          : (kv16 ? attn_occupancy<128, true>() : attn_occupancy<128, false>());
+  int s = num_sms() * occ / (B * Hkv);
+  const int hi = (max_ctx + kAttnCh - 1) / kAttnCh;
   if (s > hi) s = hi;
-  if (s < lo) s = lo;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : s;
 }
@@ -104,151 +121,182 @@ size_t attn_part_floats(int B, int Hq, int D, int splits) {
   return (size_t)B * Hq * splits * (D + 2);
 }
 
-// Positions per chunk staged in shared memory.
-constexpr int kAttnChunk = 64;
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-               "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// One CTA per (split c, kv head g, sequence b). The split's positions are
-// scanned in chunks of kAttnChunk: the chunk's K and V rows are copied into
-// shared memory with asynchronous 16-byte copies (the next chunk's copies in
-// flight while this one is used), so the cache is read with coalesced
-// transfers instead of per-thread row walks. Scores: one position per thread
-// for all G heads (K rows padded by 16 bytes so the threads' equal-column
-// reads fall in different banks; q reads are broadcasts). Softmax statistics
-// run online over the chunks, one warp per head; values: one thread per
-// (head, pair of dims), the running sums rescaled at each chunk.
+// One CTA per (split c, kv head g, sequence b). Thread 0 streams the split's
+// positions through a ring of kAttnStages shared-memory stages with bulk
+// copies (one per run of positions contiguous in the cache: the whole chunk
+// when the cache is contiguous, one block's worth when it is paged), so the
+// next chunks are in flight while one is used. Scores: each warp takes
+// 32 / GM positions at a time, a lane holding D / 32 dimensions of every
+// query head in registers and of the position's K row, the G x (32 / GM)
+// partial dots summed over the warp in one reduce-scatter. Online softmax
+// statistics run over the chunks, one warp per head; values: one thread per
+// (head, pair of dims), the running sums rescaled at each chunk. The last
+// CTA of (b, g) to finish merges the splits' partials (Tang section 2.2):
+//   M = max_c m_c,  out = sum_c acc_c e^(m_c - M) / sum_c l_c e^(m_c - M).
 template <int D, int GM, bool KV16>
-__global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a, int cap) {
-  constexpr int ES = KV16 ? 2 : 4;
-  constexpr int RS = D + 16 / ES;  // padded row, elements
-  constexpr int PPR = D * ES / 16; // 16-byte pieces per row
-  extern __shared__ __align__(16) unsigned char sm[];
-  unsigned char* kbuf = sm;                                   // [2][kAttnChunk][RS]
-  unsigned char* vbuf = kbuf + 2 * kAttnChunk * RS * ES;      // [2][kAttnChunk][RS]
-  float* p_s = reinterpret_cast<float*>(vbuf + 2 * kAttnChunk * RS * ES);  // [GM][kAttnChunk]
-  size_t* off_s = reinterpret_cast<size_t*>(p_s + GM * kAttnChunk);      // [cap] row offsets
-  __shared__ float q_s[GM][D];
-  __shared__ float m_s[GM], l_s[GM], r_s[GM];
+__global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
+  using Geo = AttnGeo<D, KV16>;
+  constexpr int ES = Geo::ES, E = D / kWarp;      // elements of a row per lane
+  constexpr int NP = kWarp / GM;                  // positions per warp step of the scores
+  constexpr int NPV = (GM * (D / 2) + kAttnThreads - 1) / kAttnThreads;  // value pairs per thread
+  extern __shared__ __align__(128) unsigned char sm[];
+  float* p_s = reinterpret_cast<float*>(sm + kAttnStages * Geo::kStage);  // [GM][kAttnCh]
+  uint64_t* full = reinterpret_cast<uint64_t*>(p_s + 8 * kAttnCh);        // [kAttnStages]
+  __shared__ float m_s[GM], l_s[GM], r_s[GM], den_s[GM];
+  __shared__ unsigned long long valid_s[kAttnStages];  // positions of each stage that were copied
+  __shared__ bool last_s;
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z, S = gridDim.x;
   const int G = a.Hq / a.Hkv;
-  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+  if (tid == 0) {
+    for (int s = 0; s < kAttnStages; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < GM) {
+    m_s[tid] = -INFINITY;
+    l_s[tid] = 0.f;
+  }
   pdl_wait();
   const int pos = a.positions[b];
-  if ((pos < 0 || pos >= a.kv.capacity()) && threadIdx.x == 0 && c == 0 && g == 0 && a.status)
+  const int cap = a.kv.capacity();
+  if ((pos < 0 || pos >= cap) && tid == 0 && c == 0 && g == 0 && a.status)
     atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
-  const int n = max(0, min(pos + 1, a.kv.capacity()));
-  const int chunk = (n + S - 1) / S;
-  const int t0 = c * chunk;
-  const int len = max(0, min(n, t0 + chunk) - t0);
+  const int n = max(0, min(pos + 1, cap));
+  const int per = (n + S - 1) / S;
+  const int t0 = min(n, c * per);
+  const int len = max(0, min(n, t0 + per) - t0);
+  const int nch = (len + kAttnCh - 1) / kAttnCh;
   float* part = a.part + ((size_t)b * a.Hq + (size_t)g * G) * S * (D + 2);
 
-  for (int i = threadIdx.x; i < GM * D; i += kAttnThreads) {
-    const int h = i / D;
-    q_s[h][i % D] = h < G ? a.q[((size_t)b * a.Hq + g * G + h) * D + i % D] : 0.f;
-  }
-  // row offsets of the split (the block table read once); ~0 marks a slot
-  // outside the cache: its row is not copied and its score is -inf
-  for (int t = threadIdx.x; t < len; t += kAttnThreads) {
-    if (a.kv.slot_ok(b, t0 + t)) {
-      off_s[t] = a.kv.offset(a.layer, b, g, t0 + t);
-    } else {
-      off_s[t] = ~(size_t)0;
-      if (a.status) atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
-    }
-  }
-  if (threadIdx.x < GM) {
-    m_s[threadIdx.x] = -INFINITY;
-    l_s[threadIdx.x] = 0.f;
-  }
-  __syncthreads();
+  // this lane's dimensions [lane E, lane E + E) of every query head
+  float qr[GM][E];
+#pragma unroll
+  for (int h = 0; h < GM; ++h)
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      qr[h][e] = h < G ? a.q[((size_t)b * a.Hq + g * G + h) * D + lane * E + e] : 0.f;
+  __syncthreads();  // barriers initialised
 
-  const int nchunks = (len + kAttnChunk - 1) / kAttnChunk;
+  // Warp 0 fills stage ci % kAttnStages with chunk ci: lane i takes the
+  // chunk's i-th run of positions inside one cache block (the whole chunk
+  // when the cache is contiguous), so the block-table reads run side by side.
+  // Positions whose block-table entry is a hole are not copied; the stage's
+  // mask of copied positions goes to valid_s before the barrier's arrive.
+  const int bs = a.kv.paged ? a.kv.block_size : (1 << 30);
   const auto issue = [&](int ci) {
-    const int q0 = ci * kAttnChunk, m = min(kAttnChunk, len - q0);
-    unsigned char* kd = kbuf + (size_t)(ci & 1) * kAttnChunk * RS * ES;
-    unsigned char* vd = vbuf + (size_t)(ci & 1) * kAttnChunk * RS * ES;
-    for (int i = threadIdx.x; i < m * PPR; i += kAttnThreads) {
-      const int row = i / PPR, piece = i % PPR;
-      const size_t off = off_s[q0 + row];
-      if (off == ~(size_t)0) continue;
-      const size_t src = off * ES + (size_t)piece * 16;
-      cp_async16(kd + (size_t)row * RS * ES + piece * 16,
-                 static_cast<const unsigned char*>(a.kv.k) + src);
-      cp_async16(vd + (size_t)row * RS * ES + piece * 16,
-                 static_cast<const unsigned char*>(a.kv.v) + src);
-    }
-    cp_async_commit();
-  };
-  const float scale = 1.f / sqrtf((float)D);
-  const int h_pv = threadIdx.x / (D / 2), d2 = threadIdx.x % (D / 2);
-  const bool pv = threadIdx.x < G * (D / 2);
-  float acc0 = 0.f, acc1 = 0.f;
-  if (nchunks > 0) issue(0);
-  for (int ci = 0; ci < nchunks; ++ci) {
-    if (ci + 1 < nchunks) {
-      issue(ci + 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const int q0 = ci * kAttnChunk, m = min(kAttnChunk, len - q0);
-    const unsigned char* kc = kbuf + (size_t)(ci & 1) * kAttnChunk * RS * ES;
-    const unsigned char* vc = vbuf + (size_t)(ci & 1) * kAttnChunk * RS * ES;
-    // scores of every head for one position per thread
-    for (int t = threadIdx.x; t < m; t += kAttnThreads) {
-      if (off_s[q0 + t] == ~(size_t)0) {
-#pragma unroll
-        for (int h = 0; h < GM; ++h) p_s[h * kAttnChunk + t] = -INFINITY;
-        continue;
+    const int st = ci % kAttnStages;
+    unsigned char* kd = sm + (size_t)st * Geo::kStage;
+    unsigned char* vd = kd + kAttnCh * Geo::kRow;
+    const int q0 = t0 + ci * kAttnCh, m = min(kAttnCh, len - ci * kAttnCh);
+    const int pg0 = q0 / bs, npg = (q0 + m - 1) / bs - pg0 + 1;
+    uint32_t bytes = 0;
+    unsigned long long vmask = 0ull;
+    for (int i = lane; i < npg; i += kWarp) {
+      const int s0 = max(q0, (pg0 + i) * bs);
+      const int s1 = (int)min((long long)(q0 + m), (long long)(pg0 + i + 1) * bs);
+      if (a.kv.slot_ok(b, s0)) {
+        bytes += 2u * (uint32_t)(s1 - s0) * (uint32_t)Geo::kRow;
+        const int nrun = s1 - s0;
+        vmask |= (nrun >= 64 ? ~0ull : ((1ull << nrun) - 1ull)) << (s0 - q0);
+      } else if (a.status) {
+        atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
       }
-      float sc[GM];
+    }
+    bytes = __reduce_add_sync(0xFFFFFFFFu, bytes);
+    const uint32_t vlo = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)vmask);
+    const uint32_t vhi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(vmask >> 32));
+    if (lane == 0) {
+      valid_s[st] = ((unsigned long long)vhi << 32) | vlo;
+      mbar_expect_tx(&full[st], bytes);
+    }
+    __syncwarp();
+    for (int i = lane; i < npg; i += kWarp) {
+      const int s0 = max(q0, (pg0 + i) * bs);
+      const int s1 = (int)min((long long)(q0 + m), (long long)(pg0 + i + 1) * bs);
+      if (a.kv.slot_ok(b, s0)) {
+        const size_t off = a.kv.offset(a.layer, b, g, s0) * ES;
+        const uint32_t nb = (uint32_t)(s1 - s0) * (uint32_t)Geo::kRow;
+        bulk_g2s(kd + (size_t)(s0 - q0) * Geo::kRow, static_cast<const char*>(a.kv.k) + off, nb,
+                 &full[st]);
+        bulk_g2s(vd + (size_t)(s0 - q0) * Geo::kRow, static_cast<const char*>(a.kv.v) + off, nb,
+                 &full[st]);
+      }
+    }
+  };
+  if (warp == 0)
+    for (int ci = 0; ci < nch && ci < kAttnStages; ++ci) issue(ci);
+
+  const float scale = 1.f / sqrtf((float)D);
+  float acc[NPV][2];
 #pragma unroll
-      for (int h = 0; h < GM; ++h) sc[h] = 0.f;
-#pragma unroll 4
-      for (int k4 = 0; k4 < D / 4; ++k4) {
-        float kf[4];
+  for (int j = 0; j < NPV; ++j) acc[j][0] = acc[j][1] = 0.f;
+  const uint64_t deadline = global_timer() + kAttnWaitNs;
+  int done = 0;  // chunks consumed
+  for (int ci = 0; ci < nch; ++ci) {
+    const int st = ci % kAttnStages;
+    int late = 0;
+    while (!mbar_try_wait(&full[st], (uint32_t)(ci / kAttnStages) & 1u))
+      if (global_timer() > deadline) {
+        late = 1;
+        break;
+      }
+    if (__syncthreads_or(late)) {  // a copy that never lands: report it, keep no partial
+      if (tid == 0 && a.status) atomicCAS(a.status, 0, (int)NC_ERR_TIMEOUT);
+      break;
+    }
+    const unsigned char* kc = sm + (size_t)st * Geo::kStage;
+    const unsigned char* vc = kc + kAttnCh * Geo::kRow;
+    const int m = min(kAttnCh, len - ci * kAttnCh);
+    // scores of NP positions x GM heads per warp step
+    for (int p0 = warp * NP; p0 < m; p0 += kAttnWarps * NP) {
+      float v[GM * NP];
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        float kf[E];
+        const unsigned char* row = kc + (size_t)(p0 + p) * Geo::kRow + (size_t)lane * E * ES;
         if constexpr (KV16) {
-          const uint2 w = *reinterpret_cast<const uint2*>(kc + ((size_t)t * RS + 4 * k4) * ES);
-          kf[0] = bf16_lo(w.x); kf[1] = bf16_hi(w.x); kf[2] = bf16_lo(w.y); kf[3] = bf16_hi(w.y);
+          if constexpr (E == 4) {
+            const uint2 w = *reinterpret_cast<const uint2*>(row);
+            kf[0] = bf16_lo(w.x); kf[1] = bf16_hi(w.x); kf[2] = bf16_lo(w.y); kf[3] = bf16_hi(w.y);
+          } else {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(row);
+            kf[0] = bf16_lo(w); kf[1] = bf16_hi(w);
+          }
         } else {
-          const float4 w = *reinterpret_cast<const float4*>(kc + ((size_t)t * RS + 4 * k4) * ES);
-          kf[0] = w.x; kf[1] = w.y; kf[2] = w.z; kf[3] = w.w;
+          if constexpr (E == 4) {
+            const float4 w = *reinterpret_cast<const float4*>(row);
+            kf[0] = w.x; kf[1] = w.y; kf[2] = w.z; kf[3] = w.w;
+          } else {
+            const float2 w = *reinterpret_cast<const float2*>(row);
+            kf[0] = w.x; kf[1] = w.y;
+          }
         }
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
-          const float4 qv = *reinterpret_cast<const float4*>(&q_s[h][4 * k4]);
-          sc[h] = fmaf(qv.x, kf[0], sc[h]);
-          sc[h] = fmaf(qv.y, kf[1], sc[h]);
-          sc[h] = fmaf(qv.z, kf[2], sc[h]);
-          sc[h] = fmaf(qv.w, kf[3], sc[h]);
+          float d = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) d = fmaf(qr[h][e], kf[e], d);
+          v[p * GM + h] = d;
         }
       }
-#pragma unroll
-      for (int h = 0; h < GM; ++h) p_s[h * kAttnChunk + t] = sc[h] * scale;
+      warp_sum_many<GM * NP>(v);  // lane i: value i = (position i / GM, head i % GM)
+      const int p = lane / GM, h = lane % GM, t = p0 + p;
+      if (h < G && t < m)  // a block-table hole (no row copied) scores -inf
+        p_s[h * kAttnCh + t] = (valid_s[st] >> t) & 1ull ? v[0] * scale : -INFINITY;
     }
     __syncthreads();
     // running softmax statistics, one warp per head
-    for (int h = warp; h < G; h += kAttnThreads / kWarp) {
+    for (int h = warp; h < G; h += kAttnWarps) {
       float mx = -INFINITY;
-      for (int t = lane; t < m; t += kWarp) mx = fmaxf(mx, p_s[h * kAttnChunk + t]);
+      for (int t = lane; t < m; t += kWarp) mx = fmaxf(mx, p_s[h * kAttnCh + t]);
       mx = warp_max(mx);
       const float m_new = fmaxf(m_s[h], mx);
       float l = 0.f;
       for (int t = lane; t < m; t += kWarp) {
-        const float x = p_s[h * kAttnChunk + t];
-        const float p = x == -INFINITY ? 0.f : expf(x - m_new);
-        p_s[h * kAttnChunk + t] = p;
-        l += p;
+        const float x = p_s[h * kAttnCh + t];
+        const float pr = x == -INFINITY ? 0.f : expf(x - m_new);
+        p_s[h * kAttnCh + t] = pr;
+        l += pr;
       }
       l = warp_sum(l);
       if (lane == 0) {
@@ -260,106 +308,137 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a, int cap
     }
     __syncthreads();
     // values, running sums rescaled by the chunk's factor
-    if (pv) {
-      float e0 = 0.f, e1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NPV; ++j) {
+      const int pr = tid + j * kAttnThreads, h = pr / (D / 2), d2 = pr % (D / 2);
+      if (h < G) {
+        float e0 = 0.f, e1 = 0.f;
 #pragma unroll 4
-      for (int t = 0; t < m; ++t) {
-        const float p = p_s[h_pv * kAttnChunk + t];
-        float2 v;
-        if constexpr (KV16) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(vc + ((size_t)t * RS + 2 * d2) * ES);
-          v = make_float2(bf16_lo(w), bf16_hi(w));
-        } else {
-          v = *reinterpret_cast<const float2*>(vc + ((size_t)t * RS + 2 * d2) * ES);
+        for (int t = 0; t < m; ++t) {
+          const float w = p_s[h * kAttnCh + t];
+          float2 vv;
+          if constexpr (KV16) {
+            const uint32_t x = *reinterpret_cast<const uint32_t*>(vc + (size_t)t * Geo::kRow + 4 * d2);
+            vv = make_float2(bf16_lo(x), bf16_hi(x));
+          } else {
+            vv = *reinterpret_cast<const float2*>(vc + (size_t)t * Geo::kRow + 8 * d2);
+          }
+          // a hole (w = 0) left its row unwritten: not multiplied
+          e0 = fmaf(w, w == 0.f ? 0.f : vv.x, e0);
+          e1 = fmaf(w, w == 0.f ? 0.f : vv.y, e1);
         }
-        // a slot outside the cache (p = 0) left its row stale: not multiplied
-        e0 = fmaf(p, p == 0.f ? 0.f : v.x, e0);
-        e1 = fmaf(p, p == 0.f ? 0.f : v.y, e1);
+        const float r = r_s[h];
+        acc[j][0] = fmaf(acc[j][0], r, e0);
+        acc[j][1] = fmaf(acc[j][1], r, e1);
       }
-      const float r = r_s[h_pv];
-      acc0 = fmaf(acc0, r, e0);
-      acc1 = fmaf(acc1, r, e1);
     }
-    __syncthreads();  // the buffers of this chunk are refilled two chunks on
+    __syncthreads();  // stage st is free again
+    ++done;
+    if (warp == 0 && ci + kAttnStages < nch) issue(ci + kAttnStages);
   }
-  if (pv) {
-    float* ph = part + ((size_t)h_pv * S + c) * (D + 2);
-    ph[2 + 2 * d2] = acc0;
-    ph[3 + 2 * d2] = acc1;
-    if (d2 == 0) {
-      ph[0] = len > 0 ? m_s[h_pv] : -INFINITY;
-      ph[1] = len > 0 ? l_s[h_pv] : 0.f;
+  if (done < nch) {
+    // abandoned: let the copies already issued land (bounded) before the
+    // shared memory is reused or released; this split contributes nothing
+    if (tid == 0) {
+      const uint64_t dl = global_timer() + kAttnWaitNs;
+      for (int ci = done; ci < nch && ci < done + kAttnStages; ++ci)
+        while (!mbar_try_wait(&full[ci % kAttnStages], (uint32_t)(ci / kAttnStages) & 1u))
+          if (global_timer() > dl) break;
+    }
+    if (tid < GM) {
+      m_s[tid] = -INFINITY;
+      l_s[tid] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < NPV; ++j) acc[j][0] = acc[j][1] = 0.f;
+    __syncthreads();
+  }
+#pragma unroll
+  for (int j = 0; j < NPV; ++j) {
+    const int pr = tid + j * kAttnThreads, h = pr / (D / 2), d2 = pr % (D / 2);
+    if (h < G) {
+      float* ph = part + ((size_t)h * S + c) * (D + 2);
+      ph[2 + 2 * d2] = acc[j][0];
+      ph[3 + 2 * d2] = acc[j][1];
+      if (d2 == 0) {
+        ph[0] = len > 0 ? m_s[h] : -INFINITY;
+        ph[1] = len > 0 ? l_s[h] : 0.f;
+      }
     }
   }
+
+  // the last CTA of (b, g) merges the S partials of its G heads
+  __threadfence();
+  __syncthreads();
+  unsigned int* ticket = a.tickets + (size_t)b * a.Hkv + g;
+  if (tid == 0) last_s = atomicAdd(ticket, 1u) == (unsigned int)(S - 1);
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  float* w_s = reinterpret_cast<float*>(sm);  // [GM][kMaxSplits]; the stages are spent
+  for (int h = warp; h < G; h += kAttnWarps) {
+    const float* ph = part + (size_t)h * S * (D + 2);
+    float M = -INFINITY;
+    for (int cc = lane; cc < S; cc += kWarp) M = fmaxf(M, __ldcg(ph + (size_t)cc * (D + 2)));
+    M = warp_max(M);
+    float den = 0.f;
+    for (int cc = lane; cc < S; cc += kWarp) {
+      const float mc = __ldcg(ph + (size_t)cc * (D + 2));
+      const float w = mc == -INFINITY ? 0.f : expf(mc - M);
+      w_s[h * kMaxSplits + cc] = w;
+      den = fmaf(__ldcg(ph + (size_t)cc * (D + 2) + 1), w, den);
+    }
+    den = warp_sum(den);
+    if (lane == 0) den_s[h] = den;
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += kAttnThreads) {
+    const int h = i / D, d = i % D;
+    const float* ph = part + (size_t)h * S * (D + 2) + 2 + d;
+    float num = 0.f;
+#pragma unroll 8
+    for (int cc = 0; cc < S; ++cc) num = fmaf(__ldcg(ph + (size_t)cc * (D + 2)), w_s[h * kMaxSplits + cc], num);
+    a.out[((size_t)b * a.Hq + g * G + h) * D + d] = num / den_s[h];
+  }
+  if (tid == 0) *ticket = 0u;  // ready for the next launch
 }
 
-template <int D>
-__global__ void k_attn_merge(AttnArgs a) {
-  // M = max_c m_c and the split weights w_c = e^(m_c - M) are formed once and
-  // shared; each thread then sums its dimension over the splits with the
-  // loads independent of one another
-  __shared__ float w_s[kMaxSplits];
-  __shared__ float red[2][D / kWarp];
-  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, S = a.splits;
-  const int warp = d / kWarp, lane = d % kWarp;
-  pdl_wait();
-  const float* ph = a.part + ((size_t)b * a.Hq + h) * S * (D + 2);
-  float M = -INFINITY;
-  for (int c = d; c < S; c += D) M = fmaxf(M, ph[(size_t)c * (D + 2)]);
-  M = warp_max(M);
-  if (lane == 0) red[0][warp] = M;
-  __syncthreads();
-  M = red[0][0];
-  for (int i = 1; i < D / kWarp; ++i) M = fmaxf(M, red[0][i]);
-  float den = 0.f;
-  for (int c = d; c < S; c += D) {
-    const float m = ph[(size_t)c * (D + 2)];
-    const float w = m == -INFINITY ? 0.f : expf(m - M);
-    w_s[c] = w;
-    den = fmaf(ph[(size_t)c * (D + 2) + 1], w, den);
-  }
-  den = warp_sum(den);
-  if (lane == 0) red[1][warp] = den;
-  __syncthreads();
-  den = 0.f;
-  for (int i = 0; i < D / kWarp; ++i) den += red[1][i];
-  float num = 0.f;
-#pragma unroll 8
-  for (int c = 0; c < S; ++c) num = fmaf(ph[(size_t)c * (D + 2) + 2 + d], w_s[c], num);
-  a.out[((size_t)b * a.Hq + h) * D + d] = num / den;
+template <int D, bool KV16>
+static int attn_occupancy() {
+  static const int occ = [] {
+    int n = 0;
+    const auto kern = k_attn_split<D, 8, KV16>;
+    if (ensure_smem<k_attn_split<D, 8, KV16>>() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kAttnThreads, AttnGeo<D, KV16>::kSmem) !=
+            cudaSuccess ||
+        n < 1)
+      n = 1;
+    return n;
+  }();
+  return occ;
 }
 
 template <int D, int GM, bool KV16>
-static cudaError_t attn_split(const AttnArgs& a, int cap, cudaStream_t s) {
-  constexpr int ES = KV16 ? 2 : 4, RS = D + 16 / ES;
-  const size_t smem = (size_t)4 * kAttnChunk * RS * ES + sizeof(float) * GM * kAttnChunk +
-                      sizeof(size_t) * (size_t)cap;
+static cudaError_t attn_split(const AttnArgs& a, cudaStream_t s) {
   cudaError_t e = ensure_smem<k_attn_split<D, GM, KV16>>();
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_attn_split<D, GM, KV16>, dim3(a.splits, a.Hkv, a.B), dim3(kAttnThreads), smem,
-                    s, a, cap);
-}
-
-template <int D, int GM>
-static cudaError_t attn_dg(const AttnArgs& a, int cap, cudaStream_t s) {
-  cudaError_t e = a.kv.bf16 ? attn_split<D, GM, true>(a, cap, s) : attn_split<D, GM, false>(a, cap, s);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(k_attn_merge<D>, dim3(a.Hq, a.B), dim3(D), 0, s, a);
+  return launch_pdl(k_attn_split<D, GM, KV16>, dim3(a.splits, a.Hkv, a.B), dim3(kAttnThreads),
+                    AttnGeo<D, KV16>::kSmem, s, a);
 }
 
 template <int D>
-static cudaError_t attn_d(const AttnArgs& a, int cap, cudaStream_t s) {
+static cudaError_t attn_d(const AttnArgs& a, cudaStream_t s) {
   const int G = a.Hq / a.Hkv;
-  if (G <= 1) return attn_dg<D, 1>(a, cap, s);
-  if (G <= 2) return attn_dg<D, 2>(a, cap, s);
-  if (G <= 4) return attn_dg<D, 4>(a, cap, s);
-  return attn_dg<D, 8>(a, cap, s);
+  const bool h = a.kv.bf16;
+  if (G <= 1) return h ? attn_split<D, 1, true>(a, s) : attn_split<D, 1, false>(a, s);
+  if (G <= 2) return h ? attn_split<D, 2, true>(a, s) : attn_split<D, 2, false>(a, s);
+  if (G <= 4) return h ? attn_split<D, 4, true>(a, s) : attn_split<D, 4, false>(a, s);
+  return h ? attn_split<D, 8, true>(a, s) : attn_split<D, 8, false>(a, s);
 }
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
-  const int max_ctx = a.kv.paged ? a.kv.max_blocks_per_seq * a.kv.block_size : a.kv.max_ctx;
-  const int cap = (max_ctx + a.splits - 1) / a.splits;
-  return a.D == 64 ? attn_d<64>(a, cap, s) : attn_d<128>(a, cap, s);
+  if (a.splits < 1 || a.splits > kMaxSplits) return cudaErrorInvalidValue;
+  return a.D == 64 ? attn_d<64>(a, s) : attn_d<128>(a, s);
 }
 
 }  // namespace nc

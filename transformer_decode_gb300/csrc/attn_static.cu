@@ -28,13 +28,19 @@ namespace nc {
 // Partials of one call: [B][Hq][splits][D + 2] floats, at most 4 MiB.
 constexpr size_t kStaticAttnScratchFloats = size_t(1) << 20;
 static __device__ __align__(256) float g_attn_scratch[kStaticAttnScratchFloats];
+// Merge tickets of one call, [B][Hkv]: zero at load, and the kernel leaves
+// every ticket it used at zero again.
+constexpr int kStaticAttnTickets = 1024;
+static __device__ unsigned int g_attn_tickets[kStaticAttnTickets];
 
 constexpr int kMaxDevices = 64;
 static float* g_scratch_ptr[kMaxDevices];
+static unsigned int* g_ticket_ptr[kMaxDevices];
 static std::mutex g_scratch_mutex;
 
-// Device address of g_attn_scratch on the current device (looked up once).
-static cudaError_t static_scratch(float** out) {
+// Device addresses of g_attn_scratch and g_attn_tickets on the current
+// device (looked up once).
+static cudaError_t static_scratch(float** out, unsigned int** tickets) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -42,11 +48,15 @@ static cudaError_t static_scratch(float** out) {
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
+    void* t = nullptr;
     e = cudaGetSymbolAddress(&p, g_attn_scratch);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&t, g_attn_tickets);
     if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = static_cast<float*>(p);
+    g_ticket_ptr[dev] = static_cast<unsigned int*>(t);
   }
   *out = g_scratch_ptr[dev];
+  *tickets = g_ticket_ptr[dev];
   return cudaSuccess;
 }
 
@@ -93,14 +103,18 @@ extern "C" nc_status nc_attn_decode_static(int n_q_heads, int n_kv_heads, int he
                  "block table entry %d of sequence %d is %d", i, b, blk);
       }
   }
-  const int splits = attn_splits(B, n_kv_heads, cap);
+  NC_CHECK(B * n_kv_heads <= kStaticAttnTickets, NC_ERR_CAPACITY,
+           "batch x kv heads = %d exceeds the %d static merge tickets", B * n_kv_heads,
+           kStaticAttnTickets);
+  const int splits = attn_splits(B, n_kv_heads, head_dim, kv->dtype == NC_KV_BF16, cap);
   const size_t need = attn_part_floats(B, n_q_heads, head_dim, splits);
   NC_CHECK(need <= kStaticAttnScratchFloats, NC_ERR_CAPACITY,
            "attention needs %zu scratch floats (%d splits); the static array holds %zu", need,
            splits, kStaticAttnScratchFloats);
 
   float* scratch = nullptr;
-  cudaError_t e = static_scratch(&scratch);
+  unsigned int* tickets = nullptr;
+  cudaError_t e = static_scratch(&scratch, &tickets);
   if (e != cudaSuccess)
     return fail(NC_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed: %s",
                 cudaGetErrorString(e));
@@ -118,7 +132,7 @@ extern "C" nc_status nc_attn_decode_static(int n_q_heads, int n_kv_heads, int he
   v.n_kv_heads = n_kv_heads;
   v.head_dim = head_dim;
   AttnArgs a{q, positions_dev, B, n_q_heads, n_kv_heads, head_dim, layer, splits, scratch, out, v,
-             nullptr};
+             nullptr, tickets};
   e = launch_attn(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(NC_ERR_CUDA, "nc_attn_decode_static: %s", cudaGetErrorString(e));

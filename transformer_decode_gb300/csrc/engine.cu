@@ -25,6 +25,8 @@
 #include <tuple>
 #include <vector>
 
+#include <algorithm>
+
 #include "engine.h"
 #include "kernels.h"
 
@@ -119,7 +121,8 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
   // arenas, then with the real allocations to assign every pointer.
   size_t part_max = 0;
   for (int b = 1; b <= max_batch; ++b) {
-    const size_t pf = attn_part_floats(b, Hq, D, attn_splits(b, Hkv, max_ctx));
+    const int sp = std::max(attn_splits(b, Hkv, D, false, max_ctx), attn_splits(b, Hkv, D, true, max_ctx));
+    const size_t pf = attn_part_floats(b, Hq, D, sp);
     if (pf > part_max) part_max = pf;
   }
   auto layout = [&](Arena& A, Arena& W) {
@@ -160,6 +163,7 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     m->h = W.take<float>((size_t)max_batch * F);
     m->am_part = W.take<unsigned long long>((size_t)max_batch * lm_head_grid());
     m->ticket = W.take<unsigned int>(1);
+    m->atickets = W.take<unsigned int>((size_t)max_batch * Hkv);
     m->status = W.take<int>(1);
     const size_t pb = max_batch < kPMaxBatch ? max_batch : kPMaxBatch;
     m->xw = W.take<uint64_t>(pb * H);
@@ -388,7 +392,8 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
   RopeArgs r{m->qkv, positions, m->inv_freq, P.g_q, P.g_k, c.rms_eps, batch, Hq, Hkv, D, layer,
              m->q, kvv, m->status};
   if ((e = launch_rope_qkv(r, s))) return e;
-  AttnArgs at{m->q, positions, batch, Hq, Hkv, D, layer, splits, m->part, m->attn, kvv, m->status};
+  AttnArgs at{m->q, positions, batch, Hq, Hkv, D, layer, splits, m->part, m->attn, kvv, m->status,
+              m->atickets};
   if ((e = launch_attn(at, s))) return e;
   if (!i8) {
     if ((e = launch_gemv(Epi::Residual, {m->attn, nullptr, 0.f, P.w_o, nullptr, batch, Hq * D, H, m->x}, s)))
@@ -440,7 +445,8 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
   nc_status st = validate_kv(m, batch, positions_host, kv);
   if (st) return st;
   const KVView kvv = kv_view(m, *kv);
-  const int splits = attn_splits(batch, m->cfg.n_kv_heads, kv_capacity(*kv));
+  const int splits = attn_splits(batch, m->cfg.n_kv_heads, m->cfg.head_dim, kv->dtype == NC_KV_BF16,
+                                 kv_capacity(*kv));
   const StepIO io{tokens, positions, logits, next, (flags & NC_STEP_ADVANCE) != 0};
   cudaError_t e;
   if (use_persistent(m, batch, *kv, flags)) {
@@ -503,7 +509,8 @@ nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t*
   nc_status st = validate_kv(m, batch, positions_host, kv);
   if (st) return st;
   const KVView kvv = kv_view(m, *kv);
-  const int splits = attn_splits(batch, m->cfg.n_kv_heads, kv_capacity(*kv));
+  const int splits = attn_splits(batch, m->cfg.n_kv_heads, m->cfg.head_dim, kv->dtype == NC_KV_BF16,
+                                 kv_capacity(*kv));
   cudaError_t e = cudaMemcpyAsync(m->x, x, (size_t)batch * m->cfg.hidden * 4,
                                   cudaMemcpyDeviceToDevice, s);
   if (!e) e = enqueue_block(m, layer, batch, positions, kvv, splits, s);

@@ -39,6 +39,7 @@ struct Model {
   float *x = nullptr, *qkv = nullptr, *q = nullptr, *attn = nullptr, *part = nullptr, *h = nullptr;
   unsigned long long* am_part = nullptr;
   unsigned int* ticket = nullptr;
+  unsigned int* atickets = nullptr;  // [max_batch, Hkv] split-attention merge tickets
   int* status = nullptr;
   // persistent decode kernel: epoch-tagged hand-over words, its ticket, the
   // step sequence number and the device copy of the per-layer pointers

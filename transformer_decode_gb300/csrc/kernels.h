@@ -93,8 +93,9 @@ struct AttnArgs {
   float* out;               // [B, Hq D]
   KVView kv;
   int* status;              // device status word (NC_ERR_POSITION on a bad slot)
+  unsigned int* tickets;    // [B, Hkv], zero between launches (the merging CTA resets its own)
 };
-int attn_splits(int B, int Hkv, int max_ctx);
+int attn_splits(int B, int Hkv, int D, bool kv16, int max_ctx);
 size_t attn_part_floats(int B, int Hq, int D, int splits);
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
 

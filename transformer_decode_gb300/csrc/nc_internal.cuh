@@ -113,6 +113,68 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) 
          static_cast<unsigned long long>(0xFFFFFFFFu - idx);
 }
 
+// ---------------------------------------------------------------- async copies
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Sums each of the N values of a lane over the warp in N - 1 + (5 - log2 N)
+// shuffles instead of 5 N: every butterfly step swaps half of the values
+// with the partner lane, so the number a lane carries halves. Afterwards
+// v[0] of lane i * (32 / N) holds the warp total of value i.
+template <int N>
+__device__ __forceinline__ void warp_sum_many(float (&v)[N]) {
+  static_assert(N >= 1 && N <= kWarp && (N & (N - 1)) == 0, "N must be a power of two");
+  const int lane = threadIdx.x % kWarp;
+  int o = kWarp / 2;
+#pragma unroll
+  for (int half = N / 2; half >= 1; half /= 2, o /= 2) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = upper ? v[k] : v[k + half];
+      const float keep = upper ? v[k + half] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+    }
+  }
+#pragma unroll
+  for (; o > 0; o /= 2) v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
+}
+
 // ---------------------------------------------------------------- KV addressing
 struct KVView {
   void* k;  // fp32 or bf16 elements (bf16 != 0)
