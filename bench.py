@@ -14,7 +14,11 @@ kernel vs the measured HBM copy peak), `cpu_baseline` (the CPU oracle on the
 host cores, bounded sample), `e2e` (host buffers, copies inside the timed
 region), `hbm` (algorithmic bytes per step over step time) and `clocks`.
 
---impl reference times the CPU oracle itself on the same workload (the
+--workload picks one of the other measured configurations instead (batch 16
+on a paged cache, W8A8, the 8B shape; see WORKLOADS): the same JSON line,
+without the CPU baseline.
+
+--impl reference times the CPU oracle itself on the default workload (the
 reference arm of this build).
 Multi-GPU (torchrun, N > 1): replicas only, one independent model per GPU, no
 collective on the data path; value = tokens of all ranks / max time.
@@ -55,14 +59,19 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def step_bytes(shape, batch, positions, kv_elem=4):
+def step_bytes(shape, batch, positions, kv_elem=4, w8a8=False):
     """Algorithmic HBM bytes of one decode step: every weight byte once, the
     embedding rows, K/V of slots 0..p read once per layer and kv head, the new
     K/V written, the logits written and tokens/positions read. kv_elem is the
-    cache element size (4: fp32 cache, 2: bf16)."""
+    cache element size (4: fp32 cache, 2: bf16); w8a8: the seven projections
+    are int8 with one fp32 scale per output row (the LM head stays bf16)."""
     H, D, F, L, V = shape.hidden, shape.head_dim, shape.ffn, shape.n_layers, shape.vocab
     nqkv = shape.q_dim + 2 * shape.kv_dim
-    per_layer = 2 * (nqkv * H + shape.q_dim * H + 2 * F * H + H * F) + 2 * 2 * H
+    if w8a8:
+        per_layer = (nqkv * H + shape.q_dim * H + 2 * F * H + H * F) + 4 * (nqkv + H + 2 * F + H)
+    else:
+        per_layer = 2 * (nqkv * H + shape.q_dim * H + 2 * F * H + H * F)
+    per_layer += 2 * 2 * H
     if shape.qkv_bias:
         per_layer += 2 * nqkv
     if shape.qk_norm:
@@ -349,7 +358,7 @@ def run_nc(args, ws, rank, local):
     # duration is the timed region over the steps (CUDA events on its stream;
     # the region holds only these launches and the 8-byte cycle resets)
     path = model.decode_path(B, kv)
-    launches_per_step = 1 if path == "persistent" else 2 + 7 * shape.n_layers
+    launches_per_step = 1 if path == "persistent" else 2 + 6 * shape.n_layers
     dur = el / args.steps
     achieved = bytes_avg / dur / 1e9
 
@@ -399,6 +408,164 @@ def run_nc(args, ws, rank, local):
     model.close()
 
 
+# Other measured configurations (not the metric's workload): name -> setup.
+# Past K/V are the seeded synthetic rows the tests use; each timed cycle runs
+# `gen` greedy steps from the past lengths, then the host resets tokens and
+# positions (B x 8 bytes).
+WORKLOADS = {
+    "qwen2_0p5b_b16_paged_past256-4096": dict(shape="QWEN2_0P5B", batch=16, paged=True,
+                                              past="uniform 256..4096", gen=32, w8a8=False),
+    "qwen2_0p5b_w8a8_b1_past512": dict(shape="QWEN2_0P5B", batch=1, paged=False, past=512,
+                                       gen=64, w8a8=True),
+    "qwen3_8b_shape_b1_past4096": dict(shape="QWEN3_8B", batch=1, paged=False, past=4096,
+                                       gen=64, w8a8=False),
+}
+
+
+def fill_past(kv, shape, past):
+    """Seeded synthetic K/V rows into slots 0..p-1 of every (layer, sequence, kv head)."""
+    D = shape.head_dim
+    for l in range(shape.n_layers):
+        for b, p in enumerate(past):
+            if p == 0:
+                continue
+            for g in range(shape.n_kv_heads):
+                kr = synth.synthetic_kv_rows(shape, l, b, g, 0, p, device="cuda")
+                vr = synth.synthetic_kv_rows(shape, l, b, g, 1, p, device="cuda")
+                if not kv.paged:
+                    kv.k[l, b, g, :p] = kr.to(kv.k.dtype).view(p, D)
+                    kv.v[l, b, g, :p] = vr.to(kv.v.dtype).view(p, D)
+                else:
+                    t = torch.arange(p, device="cuda")
+                    blk = kv.table[b, t // kv.block_size].long()
+                    kv.k[l, blk, g, t % kv.block_size] = kr.to(kv.k.dtype).view(p, D)
+                    kv.v[l, blk, g, t % kv.block_size] = vr.to(kv.v.dtype).view(p, D)
+
+
+def run_workload(args, ws, rank, local, name):
+    cfg = WORKLOADS[name]
+    torch.cuda.set_device(local)
+    shape = getattr(synth, cfg["shape"])
+    B, gen = cfg["batch"], cfg["gen"]
+    past = (synth.past_lengths(B, 256, 4096).tolist() if isinstance(cfg["past"], str)
+            else [cfg["past"]] * B)
+    wd = synth.model_weights(shape, device="cuda")
+    max_ctx = max(past) + gen + 16
+    model = nc.Model(shape, wd, max_batch=B, max_ctx=max_ctx, w8a8=cfg["w8a8"])
+    del wd
+    if cfg["paged"]:
+        table, nblk = synth.block_tables(past, gen + 1, 16)
+        kv = nc.KVCache(shape, B, paged=True, block_table=table, num_blocks=nblk)
+    else:
+        kv = nc.KVCache(shape, B, max_ctx=max_ctx)
+    fill_past(kv, shape, past)
+    logits = torch.empty(B, shape.vocab, device="cuda")
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    pos = torch.empty(B, dtype=torch.int32, device="cuda")
+    start = synth.token_ids(B, shape.vocab, stream=77).to(torch.int32)
+    reset_host = torch.stack([start, torch.tensor(past, dtype=torch.int32)]).pin_memory()
+    past_np = np.array(past, np.int32)
+
+    def run_steps(k):
+        used = []
+        for i in range(k):
+            j = i % gen
+            if j == 0:
+                tok.copy_(reset_host[0], non_blocking=True)
+                pos.copy_(reset_host[1], non_blocking=True)
+            model.decode_step(tok, pos, past_np + j, kv, logits, use_graph=True, advance=True)
+            used.append(past_np + j)
+        return used
+
+    run_steps(args.warmup)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    e0.record(st)
+    used = run_steps(args.steps)
+    e1.record(st)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier(ws)
+    if rank == 0:
+        time.sleep(0.2)
+        sampler.stop()
+    el = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3)
+    value = ws * B * args.steps / el
+    dur = el / args.steps
+    bytes_avg = sum(step_bytes(shape, B, u.tolist(), w8a8=cfg["w8a8"]) for u in used) / len(used)
+    peak, peak_kind = peaks()
+
+    # e2e: tokens and positions from pinned host memory, next tokens read back
+    tok_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    pos_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    nxt_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    nxt_d = torch.empty(B, dtype=torch.int32, device="cuda")
+    tok_h.copy_(start)
+    pos_h.copy_(torch.tensor(past, dtype=torch.int32))
+    tok.copy_(tok_h)
+    pos.copy_(pos_h)
+    model.decode_step(tok, pos, past_np, kv, logits, nxt_d, use_graph=True)
+    torch.cuda.synchronize()
+    k_e2e = min(args.steps, 4 * gen)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    cur = start.clone()
+    for i in range(k_e2e):
+        j = i % gen
+        if j == 0:
+            cur = start.clone()
+        tok_h.copy_(cur)
+        pos_h.copy_(torch.from_numpy(past_np + j))
+        tok.copy_(tok_h, non_blocking=True)
+        pos.copy_(pos_h, non_blocking=True)
+        model.decode_step(tok, pos, past_np + j, kv, logits, nxt_d, use_graph=True)
+        nxt_h.copy_(nxt_d, non_blocking=True)
+        st.synchronize()
+        cur = nxt_h.clone()
+    t_e2e = max_over_ranks(ws, time.perf_counter() - t0)
+    path = model.decode_path(B, kv)
+    launches_per_step = 1 if path == "persistent" else 2 + 6 * shape.n_layers
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dur * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "i8/i32" if cfg["w8a8"] else "f32", "data": "synthetic",
+            "config": {"workload": name, "batch": B, "past": cfg["past"], "greedy_steps": gen,
+                       "weights": ("int8 per-row scales (W8A8)" if cfg["w8a8"] else "bf16") +
+                                  " from seeded N(0,0.02)",
+                       "kv": ("paged (block 16, shuffled tables)" if cfg["paged"] else "contiguous")
+                             + " fp32",
+                       "path": ("nc_decode_step: one persistent cooperative launch per step"
+                                if path == "persistent" else "nc_decode_step: stage kernels, CUDA graph"),
+                       "l2": "inputs larger than L2: the weights stream every step",
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "hbm": {"bytes_per_step": bytes_avg, "gbs": bytes_avg / dur / 1e9,
+                    "frac_of_8tbs": bytes_avg / dur / 1e9 / NOMINAL_HBM_GBS,
+                    "frac_of_measured_copy": bytes_avg / dur / 1e9 / peak, "peak_kind": peak_kind},
+            "roofline": {"bound": "hbm", "kernel": "the whole step (" + path + " path)",
+                         "achieved": bytes_avg / dur / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": bytes_avg / dur / 1e9 / peak, "traffic": None,
+                         "peak_kind": peak_kind, "avg_step_us": dur * 1e6,
+                         "algorithmic_bytes_per_step": bytes_avg},
+            "cpu_baseline": None,
+            "e2e": {"value": ws * B * k_e2e / t_e2e, "unit": "tokens/s", "steps": k_e2e,
+                    "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
+            "gpu_launches": args.steps * launches_per_step,
+            "clocks": sampler.summary(w0, w1),
+        }), flush=True)
+    model.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,11 +574,14 @@ def main():
     ap.add_argument("--impl", default="nc", choices=["nc", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD] + list(WORKLOADS))
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     ws, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.workload != WORKLOAD:
+        run_workload(args, ws, rank, local, args.workload)
     else:
         run_nc(args, ws, rank, local)
     if ws > 1:
