@@ -358,7 +358,7 @@ def run_nc(args, ws, rank, local):
     # duration is the timed region over the steps (CUDA events on its stream;
     # the region holds only these launches and the 8-byte cycle resets)
     path = model.decode_path(B, kv)
-    launches_per_step = 1 if path == "persistent" else 2 + 6 * shape.n_layers
+    launches_per_step = 1 if path == "persistent" else 2 + 5 * shape.n_layers
     dur = el / args.steps
     achieved = bytes_avg / dur / 1e9
 
@@ -533,7 +533,7 @@ def run_workload(args, ws, rank, local, name):
         cur = nxt_h.clone()
     t_e2e = max_over_ranks(ws, time.perf_counter() - t0)
     path = model.decode_path(B, kv)
-    launches_per_step = 1 if path == "persistent" else 2 + 6 * shape.n_layers
+    launches_per_step = 1 if path == "persistent" else 2 + 5 * shape.n_layers
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,

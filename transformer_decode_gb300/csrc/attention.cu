@@ -133,7 +133,13 @@ size_t attn_part_floats(int B, int Hq, int D, int splits) {
 // (head, pair of dims), the running sums rescaled at each chunk. The last
 // CTA of (b, g) to finish merges the splits' partials (Tang section 2.2):
 //   M = max_c m_c,  out = sum_c acc_c e^(m_c - M) / sum_c l_c e^(m_c - M).
-template <int D, int GM, bool KV16>
+// ROPE: the CTA starts from the projections instead (a.qkv, as the QKV GEMV
+// left them) and does what k_rope_qkv would: q/k norm and RoPE of its G query
+// heads (every split of the group recomputes them); split 0 also rotates the
+// new key, appends K and V at slot pos and opens its running state with the
+// new position, so the scan covers the cached positions 0..pos-1 only and
+// nothing reads the appended row in this launch.
+template <int D, int GM, bool KV16, bool ROPE>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   using Geo = AttnGeo<D, KV16>;
   constexpr int ES = Geo::ES, E = D / kWarp;      // elements of a row per lane
@@ -145,6 +151,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   __shared__ float m_s[GM], l_s[GM], r_s[GM], den_s[GM];
   __shared__ unsigned long long valid_s[kAttnStages];  // positions of each stage that were copied
   __shared__ bool last_s;
+  __shared__ float q_s[ROPE ? GM : 1][D], kn_s[ROPE ? D : 1], vn_s[ROPE ? D : 1];
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z, S = gridDim.x;
   const int G = a.Hq / a.Hkv;
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
@@ -159,14 +166,64 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   pdl_wait();
   const int pos = a.positions[b];
   const int cap = a.kv.capacity();
-  if ((pos < 0 || pos >= cap) && tid == 0 && c == 0 && g == 0 && a.status)
+  const bool pos_ok = ROPE ? a.kv.slot_ok(b, pos) : (pos >= 0 && pos < cap);
+  if (!pos_ok && tid == 0 && c == 0 && g == 0 && a.status)
     atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
-  const int n = max(0, min(pos + 1, cap));
+  const int n = ROPE ? max(0, min(pos, cap)) : max(0, min(pos + 1, cap));
   const int per = (n + S - 1) / S;
   const int t0 = min(n, c * per);
   const int len = max(0, min(n, t0 + per) - t0);
   const int nch = (len + kAttnCh - 1) / kAttnCh;
   float* part = a.part + ((size_t)b * a.Hq + (size_t)g * G) * S * (D + 2);
+
+  if constexpr (ROPE) {
+    // warp w < G: query head w; then (split 0 only) warp G % 8 the key and
+    // the next warp the value. Lane l holds dims l + 32 j: a RoPE pair
+    // (i, i + D/2) sits in one lane. Same arithmetic as k_rope_qkv.
+    constexpr int EJ = D / kWarp;
+    const float* src = a.qkv + (size_t)b * (a.Hq + 2 * a.Hkv) * D;
+    for (int hh = warp; hh < G + 2; hh += kAttnWarps) {
+      if (hh >= G && c != 0) continue;  // warp-uniform
+      const float* v = src + (size_t)(hh < G ? g * G + hh : (hh == G ? a.Hq + g : a.Hq + a.Hkv + g)) * D;
+      float e[EJ];
+#pragma unroll
+      for (int j = 0; j < EJ; ++j) e[j] = v[lane + 32 * j];
+      const uint16_t* gain = hh < G ? a.g_q : (hh == G ? a.g_k : nullptr);
+      if (gain) {  // per-head RMSNorm over D
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) ss = fmaf(e[j], e[j], ss);
+        ss = warp_sum(ss);
+        const float r = 1.f / sqrtf(ss / (float)D + a.eps);
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) e[j] = (e[j] * r) * bf16_to_f32(gain[lane + 32 * j]);
+      }
+      if (hh <= G) {
+#pragma unroll
+        for (int j = 0; j < EJ / 2; ++j) {
+          const float angle = __fmul_rn((float)pos, a.inv_freq[lane + 32 * j]);
+          float sn, cs;
+          sincosf(angle, &sn, &cs);
+          const float x0 = e[j], x1 = e[j + EJ / 2];
+          e[j] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+          e[j + EJ / 2] = __fadd_rn(__fmul_rn(x1, cs), __fmul_rn(x0, sn));
+        }
+      }
+      if (hh >= G && KV16)  // k and v as the cache stores them
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) e[j] = bf16_to_f32(f32_to_bf16(e[j]));
+      float* dst = hh < G ? q_s[hh] : (hh == G ? kn_s : vn_s);
+#pragma unroll
+      for (int j = 0; j < EJ; ++j) dst[lane + 32 * j] = e[j];
+      if (hh >= G && pos_ok) {
+        const size_t off = a.kv.offset(a.layer, b, g, pos);
+        void* cache = hh == G ? a.kv.k : a.kv.v;
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) kv_store<KV16>(cache, off + lane + 32 * j, e[j]);
+      }
+    }
+  }
+  __syncthreads();  // barriers initialised (and the rotated heads in shared memory)
 
   // this lane's dimensions [lane E, lane E + E) of every query head
   float qr[GM][E];
@@ -174,8 +231,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   for (int h = 0; h < GM; ++h)
 #pragma unroll
     for (int e = 0; e < E; ++e)
-      qr[h][e] = h < G ? a.q[((size_t)b * a.Hq + g * G + h) * D + lane * E + e] : 0.f;
-  __syncthreads();  // barriers initialised
+      qr[h][e] = h >= G ? 0.f
+                 : ROPE ? q_s[ROPE ? h : 0][lane * E + e]
+                        : a.q[((size_t)b * a.Hq + g * G + h) * D + lane * E + e];
 
   // Warp 0 fills stage ci % kAttnStages with chunk ci: lane i takes the
   // chunk's i-th run of positions inside one cache block (the whole chunk
@@ -230,6 +288,28 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   float acc[NPV][2];
 #pragma unroll
   for (int j = 0; j < NPV; ++j) acc[j][0] = acc[j][1] = 0.f;
+  if constexpr (ROPE) {
+    if (c == 0 && pos_ok) {  // the new position opens split 0: m = its score, l = 1, acc = v
+      for (int h = warp; h < G; h += kAttnWarps) {
+        float sc = 0.f;
+#pragma unroll
+        for (int j = 0; j < D / kWarp; ++j) sc = fmaf(q_s[h][lane + 32 * j], kn_s[lane + 32 * j], sc);
+        sc = warp_sum(sc);
+        if (lane == 0) {
+          m_s[h] = sc * scale;
+          l_s[h] = 1.f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NPV; ++j) {
+        const int pr = tid + j * kAttnThreads, h = pr / (D / 2), d2 = pr % (D / 2);
+        if (h < G) {
+          acc[j][0] = vn_s[2 * d2];
+          acc[j][1] = vn_s[2 * d2 + 1];
+        }
+      }
+    }
+  }
   const uint64_t deadline = global_timer() + kAttnWaitNs;
   int done = 0;  // chunks consumed
   for (int ci = 0; ci < nch; ++ci) {
@@ -353,6 +433,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
     for (int j = 0; j < NPV; ++j) acc[j][0] = acc[j][1] = 0.f;
     __syncthreads();
   }
+  __syncthreads();  // m_s, l_s final (also when no chunk ran)
 #pragma unroll
   for (int j = 0; j < NPV; ++j) {
     const int pr = tid + j * kAttnThreads, h = pr / (D / 2), d2 = pr % (D / 2);
@@ -360,9 +441,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
       float* ph = part + ((size_t)h * S + c) * (D + 2);
       ph[2 + 2 * d2] = acc[j][0];
       ph[3 + 2 * d2] = acc[j][1];
-      if (d2 == 0) {
-        ph[0] = len > 0 ? m_s[h] : -INFINITY;
-        ph[1] = len > 0 ? l_s[h] : 0.f;
+      if (d2 == 0) {  // (-inf, 0) when the split saw no position
+        ph[0] = m_s[h];
+        ph[1] = l_s[h];
       }
     }
   }
@@ -407,8 +488,8 @@ template <int D, bool KV16>
 static int attn_occupancy() {
   static const int occ = [] {
     int n = 0;
-    const auto kern = k_attn_split<D, 8, KV16>;
-    if (ensure_smem<k_attn_split<D, 8, KV16>>() != cudaSuccess ||
+    const auto kern = k_attn_split<D, 8, KV16, true>;  // the larger static shared memory
+    if (ensure_smem<k_attn_split<D, 8, KV16, true>>() != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kAttnThreads, AttnGeo<D, KV16>::kSmem) !=
             cudaSuccess ||
         n < 1)
@@ -418,12 +499,17 @@ static int attn_occupancy() {
   return occ;
 }
 
+template <int D, int GM, bool KV16, bool ROPE>
+static cudaError_t attn_launch(const AttnArgs& a, cudaStream_t s) {
+  cudaError_t e = ensure_smem<k_attn_split<D, GM, KV16, ROPE>>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_attn_split<D, GM, KV16, ROPE>, dim3(a.splits, a.Hkv, a.B),
+                    dim3(kAttnThreads), AttnGeo<D, KV16>::kSmem, s, a);
+}
+
 template <int D, int GM, bool KV16>
 static cudaError_t attn_split(const AttnArgs& a, cudaStream_t s) {
-  cudaError_t e = ensure_smem<k_attn_split<D, GM, KV16>>();
-  if (e != cudaSuccess) return e;
-  return launch_pdl(k_attn_split<D, GM, KV16>, dim3(a.splits, a.Hkv, a.B), dim3(kAttnThreads),
-                    AttnGeo<D, KV16>::kSmem, s, a);
+  return a.qkv ? attn_launch<D, GM, KV16, true>(a, s) : attn_launch<D, GM, KV16, false>(a, s);
 }
 
 template <int D>

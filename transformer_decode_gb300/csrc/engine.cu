@@ -389,11 +389,14 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
     e = launch_w8a8(Epi::Store, a, s);
   }
   if (e) return e;
-  RopeArgs r{m->qkv, positions, m->inv_freq, P.g_q, P.g_k, c.rms_eps, batch, Hq, Hkv, D, layer,
-             m->q, kvv, m->status};
-  if ((e = launch_rope_qkv(r, s))) return e;
+  // RoPE (+ q/k norm) and the K/V append run inside the attention launch
   AttnArgs at{m->q, positions, batch, Hq, Hkv, D, layer, splits, m->part, m->attn, kvv, m->status,
               m->atickets};
+  at.qkv = m->qkv;
+  at.inv_freq = m->inv_freq;
+  at.g_q = P.g_q;
+  at.g_k = P.g_k;
+  at.eps = c.rms_eps;
   if ((e = launch_attn(at, s))) return e;
   if (!i8) {
     if ((e = launch_gemv(Epi::Residual, {m->attn, nullptr, 0.f, P.w_o, nullptr, batch, Hq * D, H, m->x}, s)))

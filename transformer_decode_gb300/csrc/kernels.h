@@ -94,6 +94,13 @@ struct AttnArgs {
   KVView kv;
   int* status;              // device status word (NC_ERR_POSITION on a bad slot)
   unsigned int* tickets;    // [B, Hkv], zero between launches (the merging CTA resets its own)
+  // Non-null: RoPE (+ q/k norm) and the K/V append run inside the attention
+  // launch, from the projections [B, (Hq + 2 Hkv) D]; q is then unused.
+  const float* qkv = nullptr;
+  const float* inv_freq = nullptr;  // [D/2]
+  const uint16_t* g_q = nullptr;    // [D] or null
+  const uint16_t* g_k = nullptr;    // [D] or null
+  float eps = 0.f;
 };
 int attn_splits(int B, int Hkv, int D, bool kv16, int max_ctx);
 size_t attn_part_floats(int B, int Hq, int D, int splits);
