@@ -98,8 +98,9 @@ struct AttnGeo {
   static constexpr int ES = KV16 ? 2 : 4;
   static constexpr size_t kRow = (size_t)D * ES;          // bytes of one cached row
   static constexpr size_t kStage = 2 * kAttnCh * kRow;    // a chunk's K rows, then its V rows
-  static constexpr size_t kSmem = kAttnStages * kStage + sizeof(float) * 8 * kAttnCh +
-                                  sizeof(uint64_t) * kAttnStages;
+  static constexpr size_t kSmem = kAttnStages * kStage + sizeof(uint64_t) * kAttnStages;
+  static_assert(kAttnStages * kStage >= sizeof(float) * (8 * 8 * D + 2 * 8 * 8),
+                "the warps' states are combined in the spent stages");
 };
 
 // CTAs of the split kernel one SM holds (shared memory bound), cached per shape.
@@ -121,6 +122,28 @@ size_t attn_part_floats(int B, int Hq, int D, int splits) {
   return (size_t)B * Hq * splits * (D + 2);
 }
 
+// E consecutive cached elements (E = 2 or 4) of one staged row, widened to fp32.
+template <int E, bool KV16>
+__device__ __forceinline__ void load_row(const unsigned char* p, float (&f)[E]) {
+  if constexpr (KV16) {
+    if constexpr (E == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(p);
+      f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+      f[0] = bf16_lo(w); f[1] = bf16_hi(w);
+    }
+  } else {
+    if constexpr (E == 4) {
+      const float4 w = *reinterpret_cast<const float4*>(p);
+      f[0] = w.x; f[1] = w.y; f[2] = w.z; f[3] = w.w;
+    } else {
+      const float2 w = *reinterpret_cast<const float2*>(p);
+      f[0] = w.x; f[1] = w.y;
+    }
+  }
+}
+
 // One CTA per (split c, kv head g, sequence b). Thread 0 streams the split's
 // positions through a ring of kAttnStages shared-memory stages with bulk
 // copies (one per run of positions contiguous in the cache: the whole chunk
@@ -128,10 +151,13 @@ size_t attn_part_floats(int B, int Hq, int D, int splits) {
 // next chunks are in flight while one is used. Scores: each warp takes
 // 32 / GM positions at a time, a lane holding D / 32 dimensions of every
 // query head in registers and of the position's K row, the G x (32 / GM)
-// partial dots summed over the warp in one reduce-scatter. Online softmax
-// statistics run over the chunks, one warp per head; values: one thread per
-// (head, pair of dims), the running sums rescaled at each chunk. The last
-// CTA of (b, g) to finish merges the splits' partials (Tang section 2.2):
+// partial dots summed over the warp in one reduce-scatter. Each warp keeps
+// its own online-softmax state (m, l, acc) over the positions it scored and
+// accumulates their values at once, a lane holding D / 32 dims of every head,
+// so a chunk needs no block barrier but the one that frees its stage; the
+// warps' states are combined at the end (Tang section 2.2: the online softmax
+// is a monoid on (m, l, acc), so any grouping merges exactly). The last CTA
+// of (b, g) to finish merges the splits' partials the same way:
 //   M = max_c m_c,  out = sum_c acc_c e^(m_c - M) / sum_c l_c e^(m_c - M).
 // ROPE: the CTA starts from the projections instead (a.qkv, as the QKV GEMV
 // left them) and does what k_rope_qkv would: q/k norm and RoPE of its G query
@@ -144,11 +170,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   using Geo = AttnGeo<D, KV16>;
   constexpr int ES = Geo::ES, E = D / kWarp;      // elements of a row per lane
   constexpr int NP = kWarp / GM;                  // positions per warp step of the scores
-  constexpr int NPV = (GM * (D / 2) + kAttnThreads - 1) / kAttnThreads;  // value pairs per thread
   extern __shared__ __align__(128) unsigned char sm[];
-  float* p_s = reinterpret_cast<float*>(sm + kAttnStages * Geo::kStage);  // [GM][kAttnCh]
-  uint64_t* full = reinterpret_cast<uint64_t*>(p_s + 8 * kAttnCh);        // [kAttnStages]
-  __shared__ float m_s[GM], l_s[GM], r_s[GM], den_s[GM];
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kAttnStages * Geo::kStage);  // [kAttnStages]
+  __shared__ float den_s[GM];
   __shared__ unsigned long long valid_s[kAttnStages];  // positions of each stage that were copied
   __shared__ bool last_s;
   __shared__ float q_s[ROPE ? GM : 1][D], kn_s[ROPE ? D : 1], vn_s[ROPE ? D : 1];
@@ -159,10 +183,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
     for (int s = 0; s < kAttnStages; ++s) mbar_init(&full[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (tid < GM) {
-    m_s[tid] = -INFINITY;
-    l_s[tid] = 0.f;
-  }
+  __syncthreads();  // barriers initialised
   pdl_wait();
   const int pos = a.positions[b];
   const int cap = a.kv.capacity();
@@ -175,6 +196,56 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   const int len = max(0, min(n, t0 + per) - t0);
   const int nch = (len + kAttnCh - 1) / kAttnCh;
   float* part = a.part + ((size_t)b * a.Hq + (size_t)g * G) * S * (D + 2);
+
+  // Warp 0 fills stage ci % kAttnStages with chunk ci: lane i takes the
+  // chunk's i-th run of positions inside one cache block (the whole chunk
+  // when the cache is contiguous), so the block-table reads run side by side.
+  // Positions whose block-table entry is a hole are not copied; the stage's
+  // mask of copied positions goes to valid_s before the barrier's arrive.
+  const int bs = a.kv.paged ? a.kv.block_size : (1 << 30);
+  const auto issue = [&](int ci) {
+    const int st = ci % kAttnStages;
+    unsigned char* kd = sm + (size_t)st * Geo::kStage;
+    unsigned char* vd = kd + kAttnCh * Geo::kRow;
+    const int q0 = t0 + ci * kAttnCh, m = min(kAttnCh, len - ci * kAttnCh);
+    const int pg0 = q0 / bs, npg = (q0 + m - 1) / bs - pg0 + 1;
+    uint32_t bytes = 0;
+    unsigned long long vmask = 0ull;
+    for (int i = lane; i < npg; i += kWarp) {
+      const int s0 = max(q0, (pg0 + i) * bs);
+      const int s1 = (int)min((long long)(q0 + m), (long long)(pg0 + i + 1) * bs);
+      if (a.kv.slot_ok(b, s0)) {
+        bytes += 2u * (uint32_t)(s1 - s0) * (uint32_t)Geo::kRow;
+        const int nrun = s1 - s0;
+        vmask |= (nrun >= 64 ? ~0ull : ((1ull << nrun) - 1ull)) << (s0 - q0);
+      } else if (a.status) {
+        atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
+      }
+    }
+    bytes = __reduce_add_sync(0xFFFFFFFFu, bytes);
+    const uint32_t vlo = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)vmask);
+    const uint32_t vhi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(vmask >> 32));
+    if (lane == 0) {
+      valid_s[st] = ((unsigned long long)vhi << 32) | vlo;
+      mbar_expect_tx(&full[st], bytes);
+    }
+    __syncwarp();
+    for (int i = lane; i < npg; i += kWarp) {
+      const int s0 = max(q0, (pg0 + i) * bs);
+      const int s1 = (int)min((long long)(q0 + m), (long long)(pg0 + i + 1) * bs);
+      if (a.kv.slot_ok(b, s0)) {
+        const size_t off = a.kv.offset(a.layer, b, g, s0) * ES;
+        const uint32_t nb = (uint32_t)(s1 - s0) * (uint32_t)Geo::kRow;
+        bulk_g2s(kd + (size_t)(s0 - q0) * Geo::kRow, static_cast<const char*>(a.kv.k) + off, nb,
+                 &full[st]);
+        bulk_g2s(vd + (size_t)(s0 - q0) * Geo::kRow, static_cast<const char*>(a.kv.v) + off, nb,
+                 &full[st]);
+      }
+    }
+  };
+  // the copies depend on the positions only: issue them before the q work
+  if (warp == 0)
+    for (int ci = 0; ci < nch && ci < kAttnStages; ++ci) issue(ci);
 
   if constexpr (ROPE) {
     // warp w < G: query head w; then (split 0 only) warp G % 8 the key and
@@ -223,7 +294,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
       }
     }
   }
-  __syncthreads();  // barriers initialised (and the rotated heads in shared memory)
+  __syncthreads();  // the rotated heads in shared memory
 
   // this lane's dimensions [lane E, lane E + E) of every query head
   float qr[GM][E];
@@ -235,78 +306,35 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
                  : ROPE ? q_s[ROPE ? h : 0][lane * E + e]
                         : a.q[((size_t)b * a.Hq + g * G + h) * D + lane * E + e];
 
-  // Warp 0 fills stage ci % kAttnStages with chunk ci: lane i takes the
-  // chunk's i-th run of positions inside one cache block (the whole chunk
-  // when the cache is contiguous), so the block-table reads run side by side.
-  // Positions whose block-table entry is a hole are not copied; the stage's
-  // mask of copied positions goes to valid_s before the barrier's arrive.
-  const int bs = a.kv.paged ? a.kv.block_size : (1 << 30);
-  const auto issue = [&](int ci) {
-    const int st = ci % kAttnStages;
-    unsigned char* kd = sm + (size_t)st * Geo::kStage;
-    unsigned char* vd = kd + kAttnCh * Geo::kRow;
-    const int q0 = t0 + ci * kAttnCh, m = min(kAttnCh, len - ci * kAttnCh);
-    const int pg0 = q0 / bs, npg = (q0 + m - 1) / bs - pg0 + 1;
-    uint32_t bytes = 0;
-    unsigned long long vmask = 0ull;
-    for (int i = lane; i < npg; i += kWarp) {
-      const int s0 = max(q0, (pg0 + i) * bs);
-      const int s1 = (int)min((long long)(q0 + m), (long long)(pg0 + i + 1) * bs);
-      if (a.kv.slot_ok(b, s0)) {
-        bytes += 2u * (uint32_t)(s1 - s0) * (uint32_t)Geo::kRow;
-        const int nrun = s1 - s0;
-        vmask |= (nrun >= 64 ? ~0ull : ((1ull << nrun) - 1ull)) << (s0 - q0);
-      } else if (a.status) {
-        atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
-      }
-    }
-    bytes = __reduce_add_sync(0xFFFFFFFFu, bytes);
-    const uint32_t vlo = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)vmask);
-    const uint32_t vhi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(vmask >> 32));
-    if (lane == 0) {
-      valid_s[st] = ((unsigned long long)vhi << 32) | vlo;
-      mbar_expect_tx(&full[st], bytes);
-    }
-    __syncwarp();
-    for (int i = lane; i < npg; i += kWarp) {
-      const int s0 = max(q0, (pg0 + i) * bs);
-      const int s1 = (int)min((long long)(q0 + m), (long long)(pg0 + i + 1) * bs);
-      if (a.kv.slot_ok(b, s0)) {
-        const size_t off = a.kv.offset(a.layer, b, g, s0) * ES;
-        const uint32_t nb = (uint32_t)(s1 - s0) * (uint32_t)Geo::kRow;
-        bulk_g2s(kd + (size_t)(s0 - q0) * Geo::kRow, static_cast<const char*>(a.kv.k) + off, nb,
-                 &full[st]);
-        bulk_g2s(vd + (size_t)(s0 - q0) * Geo::kRow, static_cast<const char*>(a.kv.v) + off, nb,
-                 &full[st]);
-      }
-    }
-  };
-  if (warp == 0)
-    for (int ci = 0; ci < nch && ci < kAttnStages; ++ci) issue(ci);
 
+  // Each warp keeps its own online-softmax state over the positions it
+  // scores: (m, l) of head lane % GM in every lane of that head's lane group,
+  // acc[h][e] of dims lane E + e of every head. No block barrier inside a
+  // chunk; the warps' states are combined once at the end.
   const float scale = 1.f / sqrtf((float)D);
-  float acc[NPV][2];
+  const int hl = lane % GM;  // the head whose (m, l) this lane carries
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[GM][E];
 #pragma unroll
-  for (int j = 0; j < NPV; ++j) acc[j][0] = acc[j][1] = 0.f;
+  for (int h = 0; h < GM; ++h)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
   if constexpr (ROPE) {
-    if (c == 0 && pos_ok) {  // the new position opens split 0: m = its score, l = 1, acc = v
-      for (int h = warp; h < G; h += kAttnWarps) {
+    if (c == 0 && pos_ok && warp == 0) {  // the new position opens warp 0 of split 0
+      for (int h = 0; h < G; ++h) {
         float sc = 0.f;
 #pragma unroll
         for (int j = 0; j < D / kWarp; ++j) sc = fmaf(q_s[h][lane + 32 * j], kn_s[lane + 32 * j], sc);
         sc = warp_sum(sc);
-        if (lane == 0) {
-          m_s[h] = sc * scale;
-          l_s[h] = 1.f;
+        if (hl == h) {
+          m_run = sc * scale;
+          l_run = 1.f;
         }
-      }
 #pragma unroll
-      for (int j = 0; j < NPV; ++j) {
-        const int pr = tid + j * kAttnThreads, h = pr / (D / 2), d2 = pr % (D / 2);
-        if (h < G) {
-          acc[j][0] = vn_s[2 * d2];
-          acc[j][1] = vn_s[2 * d2 + 1];
-        }
+        for (int hh = 0; hh < GM; ++hh)
+          if (hh == h)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[hh][e] = vn_s[lane * E + e];
       }
     }
   }
@@ -327,30 +355,14 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
     const unsigned char* kc = sm + (size_t)st * Geo::kStage;
     const unsigned char* vc = kc + kAttnCh * Geo::kRow;
     const int m = min(kAttnCh, len - ci * kAttnCh);
-    // scores of NP positions x GM heads per warp step
+    const unsigned long long valid = valid_s[st];
     for (int p0 = warp * NP; p0 < m; p0 += kAttnWarps * NP) {
+      // scores of NP positions x GM heads
       float v[GM * NP];
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
         float kf[E];
-        const unsigned char* row = kc + (size_t)(p0 + p) * Geo::kRow + (size_t)lane * E * ES;
-        if constexpr (KV16) {
-          if constexpr (E == 4) {
-            const uint2 w = *reinterpret_cast<const uint2*>(row);
-            kf[0] = bf16_lo(w.x); kf[1] = bf16_hi(w.x); kf[2] = bf16_lo(w.y); kf[3] = bf16_hi(w.y);
-          } else {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(row);
-            kf[0] = bf16_lo(w); kf[1] = bf16_hi(w);
-          }
-        } else {
-          if constexpr (E == 4) {
-            const float4 w = *reinterpret_cast<const float4*>(row);
-            kf[0] = w.x; kf[1] = w.y; kf[2] = w.z; kf[3] = w.w;
-          } else {
-            const float2 w = *reinterpret_cast<const float2*>(row);
-            kf[0] = w.x; kf[1] = w.y;
-          }
-        }
+        load_row<E, KV16>(kc + (size_t)(p0 + p) * Geo::kRow + (size_t)lane * E * ES, kf);
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
           float d = 0.f;
@@ -360,56 +372,40 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
         }
       }
       warp_sum_many<GM * NP>(v);  // lane i: value i = (position i / GM, head i % GM)
-      const int p = lane / GM, h = lane % GM, t = p0 + p;
-      if (h < G && t < m)  // a block-table hole (no row copied) scores -inf
-        p_s[h * kAttnCh + t] = (valid_s[st] >> t) & 1ull ? v[0] * scale : -INFINITY;
-    }
-    __syncthreads();
-    // running softmax statistics, one warp per head
-    for (int h = warp; h < G; h += kAttnWarps) {
-      float mx = -INFINITY;
-      for (int t = lane; t < m; t += kWarp) mx = fmaxf(mx, p_s[h * kAttnCh + t]);
-      mx = warp_max(mx);
-      const float m_new = fmaxf(m_s[h], mx);
-      float l = 0.f;
-      for (int t = lane; t < m; t += kWarp) {
-        const float x = p_s[h * kAttnCh + t];
-        const float pr = x == -INFINITY ? 0.f : expf(x - m_new);
-        p_s[h * kAttnCh + t] = pr;
-        l += pr;
-      }
-      l = warp_sum(l);
-      if (lane == 0) {
-        const float r = m_s[h] == -INFINITY ? 0.f : expf(m_s[h] - m_new);
-        r_s[h] = r;
-        l_s[h] = l_s[h] * r + l;
-        m_s[h] = m_new;
-      }
-    }
-    __syncthreads();
-    // values, running sums rescaled by the chunk's factor
+      const int t = p0 + lane / GM;
+      // a block-table hole (no row copied) scores -inf
+      const float sc = hl < G && t < m && ((valid >> t) & 1ull) ? v[0] * scale : -INFINITY;
+      // this warp's running max and sum of head hl: lanes hl, hl + GM, ...
+      float mx = sc;
 #pragma unroll
-    for (int j = 0; j < NPV; ++j) {
-      const int pr = tid + j * kAttnThreads, h = pr / (D / 2), d2 = pr % (D / 2);
-      if (h < G) {
-        float e0 = 0.f, e1 = 0.f;
-#pragma unroll 4
-        for (int t = 0; t < m; ++t) {
-          const float w = p_s[h * kAttnCh + t];
-          float2 vv;
-          if constexpr (KV16) {
-            const uint32_t x = *reinterpret_cast<const uint32_t*>(vc + (size_t)t * Geo::kRow + 4 * d2);
-            vv = make_float2(bf16_lo(x), bf16_hi(x));
-          } else {
-            vv = *reinterpret_cast<const float2*>(vc + (size_t)t * Geo::kRow + 8 * d2);
-          }
-          // a hole (w = 0) left its row unwritten: not multiplied
-          e0 = fmaf(w, w == 0.f ? 0.f : vv.x, e0);
-          e1 = fmaf(w, w == 0.f ? 0.f : vv.y, e1);
+      for (int o = GM; o < kWarp; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      const float m_new = fmaxf(m_run, mx);
+      const float pr = sc == -INFINITY ? 0.f : expf(sc - m_new);
+      float ls = pr;
+#pragma unroll
+      for (int o = GM; o < kWarp; o <<= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, o);
+      const float r = m_run == -INFINITY ? 0.f : expf(m_run - m_new);
+      l_run = fmaf(l_run, r, ls);
+      m_run = m_new;
+#pragma unroll
+      for (int h = 0; h < GM; ++h) {
+        const float rh = __shfl_sync(0xFFFFFFFFu, r, h);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[h][e] *= rh;
+      }
+      // values: position p's weights come from lanes p GM .. p GM + GM - 1
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        if (p0 + p >= m) break;  // warp-uniform
+        float vf[E];
+        load_row<E, KV16>(vc + (size_t)(p0 + p) * Geo::kRow + (size_t)lane * E * ES, vf);
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+          const float w = __shfl_sync(0xFFFFFFFFu, pr, p * GM + h);
+#pragma unroll
+          for (int e = 0; e < E; ++e)  // a hole (w = 0) left its row unwritten: not multiplied
+            acc[h][e] = fmaf(w, w == 0.f ? 0.f : vf[e], acc[h][e]);
         }
-        const float r = r_s[h];
-        acc[j][0] = fmaf(acc[j][0], r, e0);
-        acc[j][1] = fmaf(acc[j][1], r, e1);
       }
     }
     __syncthreads();  // stage st is free again
@@ -425,26 +421,45 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
         while (!mbar_try_wait(&full[ci % kAttnStages], (uint32_t)(ci / kAttnStages) & 1u))
           if (global_timer() > dl) break;
     }
-    if (tid < GM) {
-      m_s[tid] = -INFINITY;
-      l_s[tid] = 0.f;
-    }
+    m_run = -INFINITY;
+    l_run = 0.f;
 #pragma unroll
-    for (int j = 0; j < NPV; ++j) acc[j][0] = acc[j][1] = 0.f;
-    __syncthreads();
+    for (int h = 0; h < GM; ++h)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
   }
-  __syncthreads();  // m_s, l_s final (also when no chunk ran)
+  // combine the warps' states into the CTA's partial (the stages are spent)
+  __syncthreads();
+  float* wacc = reinterpret_cast<float*>(sm);        // [warps][GM][D]
+  float* wm = wacc + kAttnWarps * GM * D;            // [warps][GM]
+  float* wl = wm + kAttnWarps * GM;                  // [warps][GM]
+  if (lane < GM) {
+    wm[warp * GM + lane] = m_run;
+    wl[warp * GM + lane] = l_run;
+  }
 #pragma unroll
-  for (int j = 0; j < NPV; ++j) {
-    const int pr = tid + j * kAttnThreads, h = pr / (D / 2), d2 = pr % (D / 2);
-    if (h < G) {
-      float* ph = part + ((size_t)h * S + c) * (D + 2);
-      ph[2 + 2 * d2] = acc[j][0];
-      ph[3 + 2 * d2] = acc[j][1];
-      if (d2 == 0) {  // (-inf, 0) when the split saw no position
-        ph[0] = m_s[h];
-        ph[1] = l_s[h];
-      }
+  for (int h = 0; h < GM; ++h)
+#pragma unroll
+    for (int e = 0; e < E; ++e) wacc[(warp * GM + h) * D + lane * E + e] = acc[h][e];
+  __syncthreads();
+  for (int i = tid; i < G * D; i += kAttnThreads) {
+    const int h = i / D, d = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w * GM + h]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float mw = wm[w * GM + h];
+      const float f = mw == -INFINITY ? 0.f : expf(mw - M);
+      num = fmaf(wacc[(w * GM + h) * D + d], f, num);
+      den = fmaf(wl[w * GM + h], f, den);
+    }
+    float* ph = part + ((size_t)h * S + c) * (D + 2);
+    ph[2 + d] = num;
+    if (d == 0) {  // (-inf, 0) when the split saw no position
+      ph[0] = M;
+      ph[1] = den;
     }
   }
 
@@ -456,6 +471,19 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   __syncthreads();
   if (!last_s) return;
   __threadfence();
+  // The values of the first kMB splits are loaded up front, so their round
+  // trip overlaps the (m, l) pass.
+  constexpr int kMB = 16;
+  constexpr int NIT = (GM * D + kAttnThreads - 1) / kAttnThreads;  // (head, dim) items per thread
+  float av[NIT][kMB];
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int i = tid + it * kAttnThreads, h = i / D, d = i % D;
+    const float* ph = part + (size_t)h * S * (D + 2) + 2 + d;
+#pragma unroll
+    for (int cc = 0; cc < kMB; ++cc)
+      av[it][cc] = h < G && cc < S ? __ldcg(ph + (size_t)cc * (D + 2)) : 0.f;
+  }
   float* w_s = reinterpret_cast<float*>(sm);  // [GM][kMaxSplits]; the stages are spent
   for (int h = warp; h < G; h += kAttnWarps) {
     const float* ph = part + (size_t)h * S * (D + 2);
@@ -473,12 +501,17 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
     if (lane == 0) den_s[h] = den;
   }
   __syncthreads();
-  for (int i = tid; i < G * D; i += kAttnThreads) {
-    const int h = i / D, d = i % D;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int i = tid + it * kAttnThreads, h = i / D, d = i % D;
+    if (h >= G) continue;
     const float* ph = part + (size_t)h * S * (D + 2) + 2 + d;
     float num = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < kMB; ++cc)
+      if (cc < S) num = fmaf(av[it][cc], w_s[h * kMaxSplits + cc], num);
 #pragma unroll 8
-    for (int cc = 0; cc < S; ++cc) num = fmaf(__ldcg(ph + (size_t)cc * (D + 2)), w_s[h * kMaxSplits + cc], num);
+    for (int cc = kMB; cc < S; ++cc) num = fmaf(__ldcg(ph + (size_t)cc * (D + 2)), w_s[h * kMaxSplits + cc], num);
     a.out[((size_t)b * a.Hq + g * G + h) * D + d] = num / den_s[h];
   }
   if (tid == 0) *ticket = 0u;  // ready for the next launch
