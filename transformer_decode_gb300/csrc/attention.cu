@@ -92,6 +92,7 @@ constexpr int kAttnCh = 64;      // positions per staged chunk
 constexpr int kAttnStages = 3;   // chunks in shared memory: two in flight while one is used
 constexpr int kMaxSplits = 128;  // splits of one (sequence, kv head); the merge keeps one weight each
 constexpr uint64_t kAttnWaitNs = 1000000000ull;  // bound on any wait for a staged chunk
+constexpr int kAttnMinPer = 32;  // positions per split at least (shorter scans are not split)
 
 template <int D, bool KV16>
 struct AttnGeo {
@@ -107,19 +108,24 @@ struct AttnGeo {
 template <int D, bool KV16>
 static int attn_occupancy();
 
-// One wave of split CTAs: splits = resident CTAs / (B Hkv), at least one chunk each.
+// CTAs per kv head (the grid's x): one wave of resident CTAs over the kv
+// heads, at most one per kAttnMinPer positions a full batch could scan, at
+// least one per sequence; the kernel deals them to the sequences by length.
 int attn_splits(int B, int Hkv, int D, bool kv16, int max_ctx) {
   const int occ = D == 64 ? (kv16 ? attn_occupancy<64, true>() : attn_occupancy<64, false>())
                           : (kv16 ? attn_occupancy<128, true>() : attn_occupancy<128, false>());
-  int s = num_sms() * occ / (B * Hkv);
-  const int hi = (max_ctx + kAttnCh - 1) / kAttnCh;
+  long long s = (long long)num_sms() * occ / Hkv;
+  const long long hi = (long long)B * ((max_ctx + kAttnMinPer - 1) / kAttnMinPer);
   if (s > hi) s = hi;
   if (s > kMaxSplits) s = kMaxSplits;
-  return s < 1 ? 1 : s;
+  if (s < B) s = B;
+  return (int)s;
 }
 
+// Partials of one launch: [Hkv][splits][G][D + 2] = Hq x splits x (D + 2) floats.
 size_t attn_part_floats(int B, int Hq, int D, int splits) {
-  return (size_t)B * Hq * splits * (D + 2);
+  (void)B;
+  return (size_t)Hq * splits * (D + 2);
 }
 
 // E consecutive cached elements (E = 2 or 4) of one staged row, widened to fp32.
@@ -176,17 +182,54 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   __shared__ unsigned long long valid_s[kAttnStages];  // positions of each stage that were copied
   __shared__ bool last_s;
   __shared__ float q_s[ROPE ? GM : 1][D], kn_s[ROPE ? D : 1], vn_s[ROPE ? D : 1];
-  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z, S = gridDim.x;
+  __shared__ int plan_s[5];  // sequence (-1: idle), split, the sequence's splits, its first, position
+  const int g = blockIdx.y, NB = gridDim.x;
   const int G = a.Hq / a.Hkv;
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
   if (tid == 0) {
     for (int s = 0; s < kAttnStages; ++s) mbar_init(&full[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();  // barriers initialised
-  pdl_wait();
-  const int pos = a.positions[b];
   const int cap = a.kv.capacity();
+  pdl_wait();
+  if (warp == 0) {
+    // The plan (every CTA derives the same one): the NB CTAs of kv head g are
+    // dealt to the sequences in proportion to the positions each scans, at
+    // least one each and at most one per kAttnMinPer positions; a sequence's
+    // splits are consecutive CTAs. CTAs past the last split stay idle.
+    int nb = 0, pb = 0;
+    if (lane < a.B) {
+      pb = a.positions[lane];
+      nb = ROPE ? max(0, min(pb, cap)) : max(0, min(pb + 1, cap));
+    }
+    const int total = warp_sum_i(nb);
+    int sb = 0;
+    if (lane < a.B) {
+      sb = total > 0 ? 1 + (int)((long long)(NB - a.B) * nb / total) : 1;
+      sb = min(sb, max(1, (nb + kAttnMinPer - 1) / kAttnMinPer));
+    }
+    int incl = sb;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int j0 = incl - sb, j = blockIdx.x;
+    const bool mine = lane < a.B && j >= j0 && j < j0 + sb;
+    if (mine) {
+      plan_s[0] = lane;
+      plan_s[1] = j - j0;
+      plan_s[2] = sb;
+      plan_s[3] = j0;
+      plan_s[4] = pb;
+    }
+    if (__ballot_sync(0xFFFFFFFFu, mine) == 0u && lane == 0) plan_s[0] = -1;
+  }
+  __syncthreads();  // barriers initialised, plan in shared memory
+  const int b = plan_s[0];
+  if (b < 0) return;  // idle: no copy issued, no ticket taken
+  const int c = plan_s[1], S = plan_s[2];
+  const int pos = plan_s[4];
   const bool pos_ok = ROPE ? a.kv.slot_ok(b, pos) : (pos >= 0 && pos < cap);
   if (!pos_ok && tid == 0 && c == 0 && g == 0 && a.status)
     atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
@@ -195,7 +238,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   const int t0 = min(n, c * per);
   const int len = max(0, min(n, t0 + per) - t0);
   const int nch = (len + kAttnCh - 1) / kAttnCh;
-  float* part = a.part + ((size_t)b * a.Hq + (size_t)g * G) * S * (D + 2);
+  // partials of (b, g): splits plan_s[3] .. + S of kv head g, [S][G][D + 2]
+  float* part = a.part + ((size_t)g * NB + plan_s[3]) * G * (D + 2);
+  const size_t cs = (size_t)G * (D + 2);  // split stride
 
   // Warp 0 fills stage ci % kAttnStages with chunk ci: lane i takes the
   // chunk's i-th run of positions inside one cache block (the whole chunk
@@ -455,7 +500,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
       num = fmaf(wacc[(w * GM + h) * D + d], f, num);
       den = fmaf(wl[w * GM + h], f, den);
     }
-    float* ph = part + ((size_t)h * S + c) * (D + 2);
+    float* ph = part + ((size_t)c * G + h) * (D + 2);
     ph[2 + d] = num;
     if (d == 0) {  // (-inf, 0) when the split saw no position
       ph[0] = M;
@@ -479,23 +524,23 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
 #pragma unroll
   for (int it = 0; it < NIT; ++it) {
     const int i = tid + it * kAttnThreads, h = i / D, d = i % D;
-    const float* ph = part + (size_t)h * S * (D + 2) + 2 + d;
+    const float* ph = part + (size_t)h * (D + 2) + 2 + d;
 #pragma unroll
     for (int cc = 0; cc < kMB; ++cc)
-      av[it][cc] = h < G && cc < S ? __ldcg(ph + (size_t)cc * (D + 2)) : 0.f;
+      av[it][cc] = h < G && cc < S ? __ldcg(ph + (size_t)cc * cs) : 0.f;
   }
   float* w_s = reinterpret_cast<float*>(sm);  // [GM][kMaxSplits]; the stages are spent
   for (int h = warp; h < G; h += kAttnWarps) {
-    const float* ph = part + (size_t)h * S * (D + 2);
+    const float* ph = part + (size_t)h * (D + 2);
     float M = -INFINITY;
-    for (int cc = lane; cc < S; cc += kWarp) M = fmaxf(M, __ldcg(ph + (size_t)cc * (D + 2)));
+    for (int cc = lane; cc < S; cc += kWarp) M = fmaxf(M, __ldcg(ph + (size_t)cc * cs));
     M = warp_max(M);
     float den = 0.f;
     for (int cc = lane; cc < S; cc += kWarp) {
-      const float mc = __ldcg(ph + (size_t)cc * (D + 2));
+      const float mc = __ldcg(ph + (size_t)cc * cs);
       const float w = mc == -INFINITY ? 0.f : expf(mc - M);
       w_s[h * kMaxSplits + cc] = w;
-      den = fmaf(__ldcg(ph + (size_t)cc * (D + 2) + 1), w, den);
+      den = fmaf(__ldcg(ph + (size_t)cc * cs + 1), w, den);
     }
     den = warp_sum(den);
     if (lane == 0) den_s[h] = den;
@@ -505,13 +550,13 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   for (int it = 0; it < NIT; ++it) {
     const int i = tid + it * kAttnThreads, h = i / D, d = i % D;
     if (h >= G) continue;
-    const float* ph = part + (size_t)h * S * (D + 2) + 2 + d;
+    const float* ph = part + (size_t)h * (D + 2) + 2 + d;
     float num = 0.f;
 #pragma unroll
     for (int cc = 0; cc < kMB; ++cc)
       if (cc < S) num = fmaf(av[it][cc], w_s[h * kMaxSplits + cc], num);
 #pragma unroll 8
-    for (int cc = kMB; cc < S; ++cc) num = fmaf(__ldcg(ph + (size_t)cc * (D + 2)), w_s[h * kMaxSplits + cc], num);
+    for (int cc = kMB; cc < S; ++cc) num = fmaf(__ldcg(ph + (size_t)cc * cs), w_s[h * kMaxSplits + cc], num);
     a.out[((size_t)b * a.Hq + g * G + h) * D + d] = num / den_s[h];
   }
   if (tid == 0) *ticket = 0u;  // ready for the next launch
@@ -536,7 +581,7 @@ template <int D, int GM, bool KV16, bool ROPE>
 static cudaError_t attn_launch(const AttnArgs& a, cudaStream_t s) {
   cudaError_t e = ensure_smem<k_attn_split<D, GM, KV16, ROPE>>();
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_attn_split<D, GM, KV16, ROPE>, dim3(a.splits, a.Hkv, a.B),
+  return launch_pdl(k_attn_split<D, GM, KV16, ROPE>, dim3(a.splits, a.Hkv),
                     dim3(kAttnThreads), AttnGeo<D, KV16>::kSmem, s, a);
 }
 
@@ -556,7 +601,7 @@ static cudaError_t attn_d(const AttnArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
-  if (a.splits < 1 || a.splits > kMaxSplits) return cudaErrorInvalidValue;
+  if (a.splits < a.B || a.splits > kMaxSplits || a.B > kWarp) return cudaErrorInvalidValue;
   return a.D == 64 ? attn_d<64>(a, s) : attn_d<128>(a, s);
 }
 
