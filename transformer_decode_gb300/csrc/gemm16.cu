@@ -122,14 +122,31 @@ __device__ __forceinline__ void warp_tiles(const uint16_t* W0, const uint16_t* W
   const uint16_t* A1 = W0 + (size_t)rb * K;
   const uint16_t* U0 = PAIR ? W1 + (size_t)ra * K : nullptr;
   const uint16_t* U1 = PAIR ? W1 + (size_t)rb * K : nullptr;
+  // the next group's weights are loaded while this one multiplies
+  uint4 cur[2][4], nxt[2][4];
+  const auto load = [&](int c, uint4 (&w)[2][4]) {
+    const int kb = c * 64 + 16 * t4;  // the lane's 16 k of group c
+    w[0][0] = ld_stream(A0 + kb);
+    w[0][1] = ld_stream(A0 + kb + 8);
+    w[0][2] = ld_stream(A1 + kb);
+    w[0][3] = ld_stream(A1 + kb + 8);
+    if (PAIR) {
+      w[1][0] = ld_stream(U0 + kb);
+      w[1][1] = ld_stream(U0 + kb + 8);
+      w[1][2] = ld_stream(U1 + kb);
+      w[1][3] = ld_stream(U1 + kb + 8);
+    }
+  };
+  if (g0 < g1) load(g0, cur);
   for (int c = g0; c < g1; ++c) {
     const int kb = c * 64 + 16 * t4;  // the lane's 16 k of this group
+    if (c + 1 < g1) load(c + 1, nxt);
     uint32_t wa[8], wb[8], ua[8], ub[8];
-    words8(ld_stream(A0 + kb), ld_stream(A0 + kb + 8), wa);
-    words8(ld_stream(A1 + kb), ld_stream(A1 + kb + 8), wb);
+    words8(cur[0][0], cur[0][1], wa);
+    words8(cur[0][2], cur[0][3], wb);
     if (PAIR) {
-      words8(ld_stream(U0 + kb), ld_stream(U0 + kb + 8), ua);
-      words8(ld_stream(U1 + kb), ld_stream(U1 + kb + 8), ub);
+      words8(cur[1][0], cur[1][1], ua);
+      words8(cur[1][2], cur[1][3], ub);
     }
     uint32_t bh[2][8], bl[2][8];
 #pragma unroll
@@ -156,6 +173,10 @@ __device__ __forceinline__ void warp_tiles(const uint16_t* W0, const uint16_t* W
         }
       }
     }
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cur[m][q] = nxt[m][q];
   }
 }
 
