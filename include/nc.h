@@ -176,7 +176,7 @@ nc_status nc_get_device_status(nc_model* m, void* stream, int* code);
  * launched): NC_PATH_PERSISTENT, the whole step as one cooperative
  * persistent kernel (bf16 weights, batch <= 4, cache capacity <= 2048, shape
  * within its shared-memory plan, NC_STEP_STAGED not set), else
- * NC_PATH_STAGED, the per-stage kernels (2 + 7 per layer launches, in a CUDA
+ * NC_PATH_STAGED, the per-stage kernels (2 + 5 per layer launches, in a CUDA
  * graph with NC_STEP_GRAPH). */
 typedef enum { NC_PATH_STAGED = 0, NC_PATH_PERSISTENT = 1 } nc_path;
 nc_status nc_decode_path(nc_model* m, int batch, const nc_kv_cache* kv, int flags, int* path);
