@@ -22,10 +22,17 @@ warpers the page checks itself against:
 
 Precision: the scaled logits, the top-p softmax and its running sum are fp32
 (as in the page's implementation), each added in the stated order. The page
-leaves the precision of the draw open; here it is fp64: the kept tokens'
-weights exp(s - max), their running sum in index order, and the first token
-whose running sum exceeds u times the total (so the weights need not sum to
-exactly one, as the page notes). u is the caller's uniform number in [0, 1).
+leaves the precision of the draw open; here its weights are the same fp32
+values exp(s - max) that top-p thresholds, summed in fp64 in index order,
+and the drawn token is the first kept one with a positive weight whose
+running sum exceeds u times the total (so the weights need not sum to
+exactly one, as the page notes; if rounding leaves none, the last kept token
+of positive weight). u is the caller's uniform number in [0, 1).
+
+Rows the distribution is undefined for give -1: a NaN logit (any
+temperature), and at temperature > 0 a scaled logit of +inf or a row whose
+scaled logits are all -inf. A logit of -inf is a valid masked token: its
+weight is 0 and it is never drawn.
 """
 from __future__ import annotations
 
@@ -43,8 +50,9 @@ def _argmax_lowest(v: np.ndarray) -> int:
 
 
 def scaled(logits, temperature: float) -> np.ndarray:
-    """logits / temperature, each quotient rounded to fp32."""
-    return (np.asarray(logits, np.float32) / F32(temperature)).astype(np.float32)
+    """logits / temperature, each quotient rounded to fp32 (overflow gives inf)."""
+    with np.errstate(over="ignore"):
+        return (np.asarray(logits, np.float32) / F32(temperature)).astype(np.float32)
 
 
 def top_k_mask(s: np.ndarray, k: int) -> np.ndarray:
@@ -55,51 +63,104 @@ def top_k_mask(s: np.ndarray, k: int) -> np.ndarray:
     return s >= kth
 
 
+def weights(s: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """fp32 exp(s_i - max) of the tokens idx (the max over the kept tokens is
+    the row's max: the largest score always stays)."""
+    m = F32(np.max(s[idx]))
+    return np.array([np.exp(F32(s[i] - m), dtype=np.float32) for i in idx], np.float32)
+
+
+def top_p_trace(s: np.ndarray, keep: np.ndarray, p: float):
+    """The steps of the top-p cut: the kept tokens in stable ascending order,
+    their fp32 softmax total, the fp32 running sums c_j and the cut position
+    (the first j < n - 1 with c_j > 1 - p, else n - 1; tokens before it drop).
+    Returns (order, tot, c, cut); c has n - 1 entries, filled up to the cut."""
+    idx = np.nonzero(keep)[0]
+    order = idx[np.argsort(s[idx], kind="stable")]  # ascending; equal scores by index
+    e = weights(s, order)
+    tot = F32(0)
+    for x in e:
+        tot = F32(tot + x)
+    thr = F32(F32(1) - F32(p))
+    c = np.full(max(order.size - 1, 0), np.nan, np.float32)
+    run = F32(0)
+    cut = order.size - 1
+    for j in range(order.size - 1):  # the largest always stays
+        run = F32(run + F32(e[j] / tot))
+        c[j] = run
+        if run > thr:
+            cut = j
+            break
+    return order, tot, c, cut
+
+
 def top_p_mask(s: np.ndarray, keep: np.ndarray, p: float) -> np.ndarray:
     """Drop, from the kept tokens in stable ascending order, those whose running
     softmax sum is <= 1 - p (p >= 1: nothing dropped)."""
     keep = keep.copy()
     if p >= 1.0:
         return keep
-    idx = np.nonzero(keep)[0]
-    order = idx[np.argsort(s[idx], kind="stable")]  # ascending; equal scores by index
-    m = s[order[-1]]
-    e = [np.exp(F32(s[i] - m), dtype=np.float32) for i in order]
-    tot = F32(0)
-    for x in e:
-        tot = F32(tot + x)
-    thr = F32(F32(1) - F32(p))
-    c = F32(0)
-    for j in range(order.size - 1):  # the largest always stays
-        c = F32(c + F32(e[j] / tot))
-        if c <= thr:
-            keep[order[j]] = False
-        else:
-            break
+    order, _, _, cut = top_p_trace(s, keep, p)
+    keep[order[:cut]] = False
     return keep
 
 
-def draw(s: np.ndarray, keep: np.ndarray, u: float) -> int:
-    """Inverse-CDF draw over the kept tokens in index order, fp64."""
+def draw_trace(s: np.ndarray, keep: np.ndarray, u: float):
+    """Inverse-CDF draw over the kept tokens in index order: fp32 weights,
+    fp64 running sums. Returns (token, idx, running sums, r)."""
     idx = np.nonzero(keep)[0]
-    m = float(max(s[i] for i in idx))
-    w = [np.exp(float(s[i]) - m) for i in idx]
+    w = weights(s, idx)
     tot = 0.0
     for x in w:
-        tot += x
+        tot += float(x)
     r = float(u) * tot
+    cum = np.empty(idx.size, np.float64)
     c = 0.0
-    for i, x in zip(idx, w):
-        c += x
-        if c > r:
-            return int(i)
-    return int(idx[-1])
+    tok = -1
+    for j, (i, x) in enumerate(zip(idx, w)):
+        c += float(x)
+        cum[j] = c
+        if tok < 0 and x > 0 and c > r:
+            tok = int(i)
+    if tok < 0:
+        tok = int(idx[np.nonzero(w > 0)[0][-1]])
+    return tok, idx, cum, r
+
+
+def draw(s: np.ndarray, keep: np.ndarray, u: float) -> int:
+    return draw_trace(s, keep, u)[0]
+
+
+def valid(logits, temperature: float) -> bool:
+    """False for the rows the sampler answers with -1."""
+    v = np.asarray(logits, np.float32)
+    if np.isnan(v).any():
+        return False
+    if temperature == 0.0:
+        return True
+    s = scaled(v, temperature)
+    return not (np.isposinf(s).any() or np.isneginf(s).all())
+
+
+def sample_counts(logits, temperature: float, top_k: int, top_p: float):
+    """(tokens kept after top-k, tokens kept after top-p): (1, 1) at
+    temperature 0, (0, 0) for an invalid row."""
+    if not valid(logits, temperature):
+        return 0, 0
+    if temperature == 0.0:
+        return 1, 1
+    s = scaled(logits, temperature)
+    k = top_k_mask(s, top_k)
+    return int(k.sum()), int(top_p_mask(s, k, top_p).sum())
 
 
 def sample(logits, temperature: float, top_k: int, top_p: float, u: float,
            return_kept: bool = False):
     """The sampled token of one row (and, with return_kept, the kept set)."""
     v = np.asarray(logits, np.float32)
+    if not valid(v, temperature):
+        keep = np.zeros(v.size, bool)
+        return (-1, keep) if return_kept else -1
     if temperature == 0.0:
         t = _argmax_lowest(v)
         keep = np.zeros(v.size, bool)

@@ -112,3 +112,72 @@ def test_drawn_token_is_kept_and_extremes():
     assert t0 == int(np.nonzero(keep)[0][0])  # u = 0: the first kept index
     t1 = sampling.sample(v, 0.7, 20, 0.8, 0.9999999)
     assert t1 == int(np.nonzero(keep)[0][-1])  # u -> 1: the last kept index
+
+
+def test_rows_without_a_distribution_give_minus_one():
+    v = np.array([0.5, 1.0, -2.0], np.float32)
+    for T in (0.0, 0.7):
+        assert sampling.sample(np.array([0.5, np.nan, 1.0], np.float32), T, 0, 1.0, 0.3) == -1
+    assert sampling.sample(np.array([0.5, np.inf, 1.0], np.float32), 0.7, 0, 1.0, 0.3) == -1
+    assert sampling.sample(np.array([0.5, np.inf, 1.0], np.float32), 0.0, 0, 1.0, 0.3) == 1
+    ninf = np.full(5, -np.inf, np.float32)
+    assert sampling.sample(ninf, 0.9, 0, 0.8, 0.3) == -1
+    assert sampling.sample(ninf, 0.0, 0, 0.8, 0.3) == 0  # all equal: lowest index
+    # a large logit over a tiny temperature overflows to +inf in fp32
+    assert sampling.sample(np.array([100.0, 1.0], np.float32), 1e-37, 0, 1.0, 0.3) == -1
+    assert sampling.sample_counts(np.array([0.5, np.nan], np.float32), 0.7, 0, 1.0) == (0, 0)
+    assert sampling.sample(v, 0.7, 0, 1.0, 0.3) >= 0
+
+
+def test_minus_inf_is_a_masked_token():
+    v = np.array([-np.inf, 0.3, -np.inf, 1.1, -0.4, -np.inf], np.float32)
+    seen = set()
+    for i in range(2000):
+        t = sampling.sample(v, 0.8, 0, 1.0, (i + 0.5) / 2000)
+        seen.add(t)
+    assert seen == {1, 3, 4}
+    # u -> 1: the last kept token of positive weight, never the trailing -inf
+    assert sampling.sample(v, 0.8, 0, 1.0, 1.0) == 4
+    assert sampling.sample_counts(v, 0.8, 0, 1.0) == (6, 6)
+    assert sampling.sample_counts(v, 0.8, 4, 1.0) == (6, 6)  # ties at the 4th place: all stay
+    assert sampling.sample_counts(v, 0.8, 3, 1.0) == (3, 3)
+
+
+def test_counts_and_trace_agree_with_masks():
+    rng = np.random.default_rng(9)
+    for trial in range(40):
+        v = (rng.standard_normal(300) * 3).astype(np.float32)
+        v[rng.integers(0, 300, 40)] = v[rng.integers(0, 300, 40)]  # forced ties
+        T, k, p = float(rng.uniform(0.3, 1.5)), int(rng.integers(0, 60)), float(rng.uniform(0.2, 1.0))
+        s = sampling.scaled(v, T)
+        km = sampling.top_k_mask(s, k)
+        pm = sampling.top_p_mask(s, km, p)
+        assert sampling.sample_counts(v, T, k, p) == (int(km.sum()), int(pm.sum()))
+        order, tot, c, cut = sampling.top_p_trace(s, km, p)
+        assert set(order[cut:].tolist()) == set(np.nonzero(pm)[0].tolist()) or p >= 1.0
+        # the kept set after top-p is a suffix of the ascending (score, index) order
+        keys = [(float(s[i]), int(i)) for i in order]
+        assert keys == sorted(keys)
+
+
+def test_brute_force_three_tokens():
+    """Every kept set of a three-token row from the definitions written out by
+    hand: the k largest (with ties), then the ascending cut."""
+    vals = np.array([0.0, 1.0, 2.0], np.float32)
+    e = np.exp(vals.astype(np.float64) - 2.0)
+    for k in range(0, 4):
+        for p in (0.05, 0.3, 0.6, 0.8, 0.95, 1.0):
+            kept = [0, 1, 2] if k in (0, 3) else [2, 1, 0][:k]
+            kept = sorted(kept)
+            tot = e[kept].sum()
+            c = 0.0
+            out = list(kept)
+            if p < 1.0:
+                for j in kept[:-1]:  # ascending order == index order here
+                    c += e[j] / tot
+                    if c <= 1 - p:
+                        out.remove(j)
+                    else:
+                        break
+            _, keep = sampling.sample(vals, 1.0, k, p, 0.5, return_kept=True)
+            assert sorted(np.nonzero(keep)[0].tolist()) == out, (k, p)
