@@ -18,6 +18,12 @@ region), `hbm` (algorithmic bytes per step over step time) and `clocks`.
 on a paged cache, W8A8, the 8B shape; see WORKLOADS): the same JSON line,
 without the CPU baseline.
 
+--workload qwen2_0p5b_b1_sampled64 is the default workload with nanoinfer's
+sampler (temperature 0.7, top-k 20, top-p 0.8, the values the page reads from
+Qwen2.5's config) in place of greedy: each step is nc_decode_step then
+nc_sample on its logits, the sampled token fed back on the device; the line
+adds the sampler kernel's own average duration.
+
 --impl reference times the CPU oracle itself on the default workload (the
 reference arm of this build).
 Multi-GPU (torchrun, N > 1): replicas only, one independent model per GPU, no
@@ -408,6 +414,141 @@ def run_nc(args, ws, rank, local):
     model.close()
 
 
+SAMPLED = "qwen2_0p5b_b1_sampled64"
+SAMPLER = dict(temperature=0.7, top_k=20, top_p=0.8)
+
+
+def run_sampled(args, ws, rank, local):
+    """The default workload, each step followed by nc_sample (temperature 0.7,
+    top-k 20, top-p 0.8) whose token replaces the greedy one on the device."""
+    torch.cuda.set_device(local)
+    shape = synth.QWEN2_0P5B
+    B, n_prompt, n_gen = 1, 32, 64
+    wd = synth.model_weights(shape, device="cuda")
+    max_ctx = n_prompt + n_gen + 16
+    model = nc.Model(shape, wd, max_batch=B, max_ctx=max_ctx)
+    kv = nc.KVCache(shape, B, max_ctx=max_ctx)
+    logits = torch.empty(B, shape.vocab, device="cuda")
+    prompt = synth.token_ids(n_prompt, shape.vocab).tolist()
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    pos = torch.empty(B, dtype=torch.int32, device="cuda")
+    reset_host = torch.tensor([prompt[-1], n_prompt - 1], dtype=torch.int32).pin_memory()
+    samp = nc.Sampler(B, shape.vocab)
+    n_u = args.warmup + args.steps + 256
+    u = synth.uniform_f64(5, 0, n_u * B, device="cuda").view(n_u, B)
+    pos.fill_(0)
+    for i in range(n_prompt - 1):
+        tok.fill_(prompt[i])
+        model.decode_step(tok, pos, [i], kv, logits, use_graph=True, advance=True)
+    cycle = n_gen + 1
+    T, K, P = SAMPLER["temperature"], SAMPLER["top_k"], SAMPLER["top_p"]
+
+    def run_steps(k, off):
+        used = []
+        for i in range(k):
+            p = n_prompt - 1 + (i % cycle)
+            if i % cycle == 0:
+                tok.copy_(reset_host[:1], non_blocking=True)
+                pos.copy_(reset_host[1:], non_blocking=True)
+            model.decode_step(tok, pos, [p], kv, logits, use_graph=True, advance=True)
+            samp(logits, T, K, P, u[off + i], tok)
+            used.append(p)
+        return used
+
+    run_steps(args.warmup, 0)
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    if rank == 0:
+        clk.start()
+        time.sleep(0.3)
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    e0.record(st)
+    used = run_steps(args.steps, args.warmup)
+    e1.record(st)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier(ws)
+    if rank == 0:
+        time.sleep(0.2)
+        clk.stop()
+    el = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3)
+    bytes_avg = sum(step_bytes(shape, B, [p]) for p in used) / len(used)
+    peak, peak_kind = peaks()
+
+    # the sampler alone, on the last step's logits (already in L2: the LM head wrote them)
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    kept = torch.empty(B, 2, dtype=torch.int32, device="cuda")
+    for i in range(8):
+        samp(logits, T, K, P, u[i], nxt, kept)
+    n_s = 256
+    torch.cuda.synchronize()
+    e0.record(st)
+    for i in range(n_s):
+        samp(logits, T, K, P, u[i], nxt, kept)
+    e1.record(st)
+    torch.cuda.synchronize()
+    samp_us = e0.elapsed_time(e1) / n_s * 1e3
+
+    # e2e: host token and position in, the sampled token out, every step
+    tok_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    pos_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    nxt_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    k_e2e = min(args.steps, 520)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    cur = prompt[-1]
+    for i in range(k_e2e):
+        p = n_prompt - 1 + (i % cycle)
+        if i % cycle == 0:
+            cur = prompt[-1]
+        tok_h[0] = cur
+        pos_h[0] = p
+        tok.copy_(tok_h, non_blocking=True)
+        pos.copy_(pos_h, non_blocking=True)
+        model.decode_step(tok, pos, [p], kv, logits, use_graph=True)
+        samp(logits, T, K, P, u[i % n_u], nxt)
+        nxt_h.copy_(nxt, non_blocking=True)
+        st.synchronize()
+        cur = int(nxt_h[0])
+    t_e2e = max_over_ranks(ws, time.perf_counter() - t0)
+
+    path = model.decode_path(B, kv)
+    launches = (1 if path == "persistent" else 2 + 5 * shape.n_layers) + 1
+    if rank == 0:
+        dur = el / args.steps
+        row_bytes = B * shape.vocab * 4
+        print(json.dumps({
+            "metric": METRIC, "value": ws * B * args.steps / el, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dur * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": SAMPLED, "batch": B, "prompt": n_prompt,
+                       "sampler": dict(SAMPLER, u="seeded uniforms, one per step"),
+                       "path": f"nc_decode_step ({path}) then nc_sample",
+                       "l2": "inputs larger than L2: 988 MB of weights stream every step",
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "kernel": "decode step + sampler (whole step)",
+                         "achieved": bytes_avg / dur / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": bytes_avg / dur / 1e9 / peak, "traffic": None,
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_launch": bytes_avg},
+            "sampler": {"kernel": "k_sample (one CTA of 1024 threads per row)",
+                        "avg_us": samp_us, "share_of_step": samp_us * 1e-6 / dur,
+                        "logit_bytes": row_bytes, "gbs": row_bytes / (samp_us * 1e-6) / 1e9,
+                        "bound": "latency (one row per CTA; the logits sit in L2)"},
+            "cpu_baseline": None,
+            "e2e": {"value": ws * B * k_e2e / t_e2e, "unit": "tokens/s", "steps": k_e2e,
+                    "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
+            "gpu_launches": args.steps * launches,
+            "clocks": clk.summary(w0, w1),
+        }), flush=True)
+    model.close()
+
+
 # Other measured configurations (not the metric's workload): name -> setup.
 # Past K/V are the seeded synthetic rows the tests use; each timed cycle runs
 # `gen` greedy steps from the past lengths, then the host resets tokens and
@@ -574,12 +715,15 @@ def main():
     ap.add_argument("--impl", default="nc", choices=["nc", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD] + list(WORKLOADS))
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=[WORKLOAD, SAMPLED] + list(WORKLOADS))
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     ws, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.workload == SAMPLED:
+        run_sampled(args, ws, rank, local)
     elif args.workload != WORKLOAD:
         run_workload(args, ws, rank, local, args.workload)
     else:

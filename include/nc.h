@@ -270,6 +270,41 @@ nc_status nc_lm_head_argmax(nc_model* m, const float* x, const void* gamma, floa
                             const void* W, int B, int K, int V, float* logits, int32_t* next,
                             void* stream);
 
+/* ---------------- sampling (nanoinfer, sampling section) -------------------- */
+
+/* Bytes of device scratch nc_sample needs for B rows of V logits at
+ * temperature > 0: 20 * B * (V rounded up to 64). 0 for invalid sizes. */
+size_t nc_sample_scratch_bytes(int B, int V);
+
+/* One token per row of logits [B, V] fp32 (nanoinfer, sampling section:
+ * "temperature, top-k, top-p, seeded draw", in that order, then the softmax
+ * of what is left and an inverse-CDF draw):
+ *   temperature == 0: the arg-max, lowest index on ties (greedy);
+ *   else s = logits / temperature (fp32 IEEE division); top_k > 0 keeps the
+ *   tokens whose s is >= the k-th largest (ties at the k-th place stay;
+ *   0 or >= V keeps all); top_p < 1 orders the kept tokens by ascending s,
+ *   equal s in index order, and drops each one whose running fp32 sum of
+ *   exp(s - max) / total is <= 1 - top_p (the largest always stays); then
+ *   tokens[b] is the first kept token, in index order, whose running sum of
+ *   the weights exp(s - max) (fp32 values, fp64 sums) exceeds u[b] times
+ *   their total.
+ * u [B] fp64 on the device holds the caller's uniform numbers in [0, 1)
+ * (unused at temperature 0); kept [B, 2] int32 (nullable) receives the
+ * number of tokens kept after top-k and after top-p ((1, 1) at temperature
+ * 0). A row with a NaN logit, or at temperature > 0 a score of +inf or only
+ * scores of -inf, gets token -1 and kept (0, 0); a -inf logit is a masked
+ * token that is never drawn. scratch: device memory of at least
+ * nc_sample_scratch_bytes(B, V) bytes, 16-byte aligned, owned by the caller
+ * (NULL allowed at temperature 0); its contents on entry do not matter.
+ * One CTA per row; calls sharing a scratch buffer must not overlap on the
+ * GPU. Errors: NULL pointers or temperature < 0 / not finite, top_k < 0,
+ * top_p outside (0, 1] -> NC_ERR_INVALID_ARGUMENT; B outside [1, 65535] or
+ * V outside [1, 2^24] -> NC_ERR_SHAPE; scratch smaller than needed ->
+ * NC_ERR_CAPACITY; all before anything is enqueued. */
+nc_status nc_sample(const float* logits, int B, int V, float temperature, int top_k, float top_p,
+                    const double* u, int32_t* tokens, int32_t* kept, void* scratch,
+                    size_t scratch_bytes, void* stream);
+
 /* ---------------- W8A8 (nanoinfer "Quantization", per-token activations) ---- */
 
 /* Per-output-row symmetric weight quantisation: scale[n] = amax_n / 127,

@@ -70,11 +70,12 @@ def weights(s: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return np.array([np.exp(F32(s[i] - m), dtype=np.float32) for i in idx], np.float32)
 
 
-def top_p_trace(s: np.ndarray, keep: np.ndarray, p: float):
+def top_p_trace(s: np.ndarray, keep: np.ndarray, p: float, full: bool = False):
     """The steps of the top-p cut: the kept tokens in stable ascending order,
     their fp32 softmax total, the fp32 running sums c_j and the cut position
     (the first j < n - 1 with c_j > 1 - p, else n - 1; tokens before it drop).
-    Returns (order, tot, c, cut); c has n - 1 entries, filled up to the cut."""
+    Returns (order, tot, c, cut); c has n - 1 entries, filled up to the cut
+    (with full=True, all of them: the same chain continued past the cut)."""
     idx = np.nonzero(keep)[0]
     order = idx[np.argsort(s[idx], kind="stable")]  # ascending; equal scores by index
     e = weights(s, order)
@@ -88,9 +89,10 @@ def top_p_trace(s: np.ndarray, keep: np.ndarray, p: float):
     for j in range(order.size - 1):  # the largest always stays
         run = F32(run + F32(e[j] / tot))
         c[j] = run
-        if run > thr:
+        if run > thr and cut == order.size - 1:
             cut = j
-            break
+            if not full:
+                break
     return order, tot, c, cut
 
 

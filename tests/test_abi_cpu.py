@@ -91,3 +91,31 @@ def test_stage_entry_points_reject_bad_shapes(lib):
     assert lib.nc_quantize_weight(P, 0, 8, P, P, None) == 2
     assert lib.nc_decode_step(None, 1, P, P, P, None, P, None, 1, None) == 1
     assert lib.nc_model_destroy(None) == 1
+
+
+def test_sample_rejects_bad_arguments_before_any_launch(lib):
+    P = C.c_void_p(4096)
+    V = 151936
+    need = lib.nc_sample_scratch_bytes(16, V)
+    assert need == 16 * 5 * ((V + 63) // 64 * 64) * 4
+    assert lib.nc_sample_scratch_bytes(0, V) == 0 and lib.nc_sample_scratch_bytes(1, 0) == 0
+    E = {n: nc.STATUS.index(n) for n in nc.STATUS}
+
+    def call(logits=P, B=16, V=V, T=0.7, k=20, p=0.8, u=P, tok=P, kept=None, scratch=P,
+             nbytes=need):
+        return lib.nc_sample(logits, B, V, T, k, p, u, tok, kept, scratch, nbytes, None)
+
+    assert call(logits=None) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(tok=None) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(B=0) == E["NC_ERR_SHAPE"] and call(B=65536) == E["NC_ERR_SHAPE"]
+    assert call(V=0) == E["NC_ERR_SHAPE"] and call(V=(1 << 24) + 1) == E["NC_ERR_SHAPE"]
+    for T in (-0.5, float("nan"), float("inf")):
+        assert call(T=T) == E["NC_ERR_INVALID_ARGUMENT"], T
+    assert call(k=-1) == E["NC_ERR_INVALID_ARGUMENT"]
+    for p in (0.0, -0.1, 1.01, float("nan")):
+        assert call(p=p) == E["NC_ERR_INVALID_ARGUMENT"], p
+    assert call(u=None) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(scratch=None) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(scratch=C.c_void_p(4100)) == E["NC_ERR_INVALID_ARGUMENT"]  # misaligned
+    assert call(nbytes=need - 1) == E["NC_ERR_CAPACITY"]
+    assert b"needed" in lib.nc_last_error_message()

@@ -1,6 +1,7 @@
 // abi.cu -- the extern "C" entry points of libnc: argument validation on the
 // host, then the kernels. Nothing here reads device memory.
 #include <cuda_runtime.h>
+#include <float.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -255,6 +256,35 @@ nc_status nc_w8a8_gemv(const float* x, const void* gamma, float eps, const int8_
   W8Args a{x, static_cast<const uint16_t*>(gamma), eps, Wq, w_scale,
            static_cast<const uint16_t*>(bias), B, K, N, y, xq_out, sx_out, acc_out};
   return launch_result(launch_w8a8(Epi::Store, a, S(stream)), "nc_w8a8_gemv");
+}
+
+size_t nc_sample_scratch_bytes(int B, int V) {
+  if (B < 1 || V < 1) return 0;
+  return sample_scratch_bytes(B, V);
+}
+
+nc_status nc_sample(const float* logits, int B, int V, float temperature, int top_k, float top_p,
+                    const double* u, int32_t* tokens, int32_t* kept, void* scratch,
+                    size_t scratch_bytes, void* stream) {
+  NC_CHECK(logits && tokens, NC_ERR_INVALID_ARGUMENT, "logits and tokens must not be NULL");
+  NC_CHECK(B >= 1 && B <= 65535, NC_ERR_SHAPE, "batch %d outside [1, 65535]", B);
+  NC_CHECK(V >= 1 && V <= (1 << 24), NC_ERR_SHAPE, "V = %d outside [1, 2^24]", V);
+  NC_CHECK(temperature >= 0.f && temperature <= FLT_MAX, NC_ERR_INVALID_ARGUMENT,
+           "temperature must be finite and >= 0");
+  NC_CHECK(top_k >= 0, NC_ERR_INVALID_ARGUMENT, "top_k = %d must be >= 0 (0: off)", top_k);
+  NC_CHECK(top_p > 0.f && top_p <= 1.f, NC_ERR_INVALID_ARGUMENT,
+           "top_p must lie in (0, 1] (1: off)");
+  if (temperature > 0.f) {
+    NC_CHECK(u, NC_ERR_INVALID_ARGUMENT, "u must not be NULL when temperature > 0");
+    NC_CHECK(scratch && aligned16(scratch), NC_ERR_INVALID_ARGUMENT,
+             "scratch must be a 16-byte aligned device buffer when temperature > 0");
+    const size_t need = sample_scratch_bytes(B, V);
+    NC_CHECK(scratch_bytes >= need, NC_ERR_CAPACITY, "scratch holds %zu bytes, %zu needed",
+             scratch_bytes, need);
+  }
+  return launch_result(launch_sample(logits, B, V, temperature, top_k, top_p, u, tokens, kept,
+                                     scratch, S(stream)),
+                       "nc_sample");
 }
 
 }  // extern "C"

@@ -124,6 +124,13 @@ cudaError_t launch_w8a8(Epi epi, const W8Args& a, cudaStream_t s);
 cudaError_t launch_quantize_weight(const uint16_t* W, int N, int K, int8_t* q, float* scale,
                                    cudaStream_t s);
 
+// ------------------------------------------------------------ sampling
+// Scratch of nc_sample: per row five arrays of V rounded up to 64 words.
+size_t sample_scratch_bytes(int B, int V);
+cudaError_t launch_sample(const float* logits, int B, int V, float temperature, int top_k,
+                          float top_p, const double* u, int32_t* tokens, int32_t* kept,
+                          void* scratch, cudaStream_t s);
+
 // ------------------------------------------------------------ misc
 // x[b] = widen(E[tokens[b]]); a token outside [0, V) reads row 0 and sets *status.
 cudaError_t launch_embed(const uint16_t* E, const int32_t* tokens, int B, int H, int V, float* x,

@@ -32,6 +32,7 @@ EXPORTS = [
     "nc_get_device_status", "nc_rmsnorm_gemv", "nc_gemv_residual", "nc_swiglu_gemv",
     "nc_rope_qkv", "nc_attn_decode", "nc_lm_head_argmax", "nc_quantize_weight", "nc_w8a8_gemv",
     "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile", "nc_decode_path",
+    "nc_sample", "nc_sample_scratch_bytes",
 ]
 
 
@@ -117,9 +118,12 @@ def _declare(L):
     L.nc_profile_phases.argtypes = [vp, i]
     L.nc_decode_path.argtypes = [vp, i, vp, i, C.POINTER(i)]
     L.nc_read_phase_profile.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), i, C.POINTER(i)]
+    L.nc_sample.argtypes = [vp, i, i, f, i, f, vp, vp, vp, vp, C.c_size_t, vp]
+    L.nc_sample_scratch_bytes.argtypes = [i, i]
     for n in EXPORTS:
-        if n not in ("nc_status_string", "nc_last_error_message"):
+        if n not in ("nc_status_string", "nc_last_error_message", "nc_sample_scratch_bytes"):
             getattr(L, n).restype = C.c_int
+    L.nc_sample_scratch_bytes.restype = C.c_size_t
 
 
 def _check(rc):
@@ -211,6 +215,43 @@ def attn_decode_static(shape, layer, q, positions, positions_host, kv, out, stre
         _ptr(q, torch.float32, "q", B * shape.q_dim), _ptr(positions, torch.int32, "positions", B),
         ph.ctypes.data_as(C.c_void_p), C.byref(s),
         _ptr(out, torch.float32, "out", B * shape.q_dim), _stream(stream)))
+
+
+# ------------------------------------------------------------------ sampling
+def sample_scratch_bytes(B, V):
+    return int(load().nc_sample_scratch_bytes(int(B), int(V)))
+
+
+def sample(logits, temperature, top_k, top_p, u, tokens, kept=None, scratch=None, stream=None):
+    """nc_sample: one token per row of logits [B, V] (temperature -> top-k ->
+    top-p -> inverse-CDF draw with the uniforms u [B] fp64). kept [B, 2] int32
+    receives the kept counts; scratch is a caller-owned device buffer of
+    sample_scratch_bytes(B, V) bytes (any dtype), needed when temperature > 0."""
+    B, V = logits.shape
+    sp = None
+    nbytes = 0
+    if scratch is not None:
+        sp = _ptr(scratch, None, "scratch")
+        nbytes = scratch.numel() * scratch.element_size()
+    _check(load().nc_sample(_ptr(logits, torch.float32, "logits"), B, V, float(temperature),
+                            int(top_k), float(top_p), _ptr(u, torch.float64, "u", B),
+                            _ptr(tokens, torch.int32, "tokens", B),
+                            _ptr(kept, torch.int32, "kept", 2 * B), sp, nbytes, _stream(stream)))
+
+
+class Sampler:
+    """A scratch buffer sized for up to max_batch rows of V logits, and the
+    nc_sample call that uses it."""
+
+    def __init__(self, max_batch, vocab, device="cuda"):
+        self.max_batch, self.vocab = int(max_batch), int(vocab)
+        n = sample_scratch_bytes(self.max_batch, self.vocab)
+        self.scratch = torch.empty(n, dtype=torch.uint8, device=device)
+
+    def __call__(self, logits, temperature, top_k, top_p, u, tokens, kept=None, stream=None):
+        if logits.shape[0] > self.max_batch or logits.shape[1] != self.vocab:
+            raise ValueError("logits larger than this sampler's scratch")
+        sample(logits, temperature, top_k, top_p, u, tokens, kept, self.scratch, stream)
 
 
 # ------------------------------------------------------------------ KV cache

@@ -154,6 +154,11 @@ def uint32_stream(seed: int, stream: int, n: int, device="cpu",
     return fmix32(fmix32((idx * 0x9E3779B1 + key) & _M32) ^ key)
 
 
+def uniform_f64(seed: int, stream: int, n: int, device="cpu") -> torch.Tensor:
+    """n uniform numbers in (0, 1) as fp64: (uint32 + 0.5) / 2^32."""
+    return (uint32_stream(seed, stream, n, device).double() + 0.5) / 4294967296.0
+
+
 def normal_bf16(seed: int, stream: int, shape, std: float, mean: float = 0.0,
                 device="cpu") -> torch.Tensor:
     """A bf16 tensor of the given shape with values ~ mean + std * z, where z
