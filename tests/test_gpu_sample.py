@@ -163,6 +163,28 @@ def test_model_vocab_large_kept_sets():
     assert (kept == V_MODEL).all()
 
 
+@pytest.mark.parametrize("k,p", [(3000, 0.95), (9000, 0.9), (9000, 1.0)])
+def test_model_vocab_wide_top_k(k, p):
+    """Top-k wide enough that the candidates of the first select pass may not
+    fit shared memory (9000): the radix select then finishes over the keys."""
+    lg = _rows(3, V_MODEL, seed=90 + k, std=1.0)
+    _, kept, hows = _check(lg, 1.0, k, p, _u(3, seed=14))
+    assert (kept[:, 0] >= k).all()
+    assert hows.count("boundary") <= 1
+
+
+def test_top_ties_beyond_the_candidate_buffer():
+    """10,000 equal top logits at top-k 20: every one of them stays (ties at
+    the k-th place), more than the shared-memory buffer holds."""
+    lg = _rows(2, V_MODEL, seed=95, std=1.0)
+    lg[:, 5000:15000] = 9.0
+    tok, kept, hows = _check(lg, 1.0, 20, 0.5, _u(2, seed=15))
+    assert (kept[:, 0] == 10000).all() and hows == ["exact", "exact"]
+    assert ((tok >= 5000) & (tok < 15000)).all()
+    tok, kept, _ = _check(lg, 1.0, 20, 1.0, _u(2, seed=16))
+    assert (kept == 10000).all()
+
+
 def test_ties_beyond_the_shared_sort_are_exact():
     """20,000 equal logits, top-p 0.5: every weight is exactly 1 on both
     sides, so the fp32 chain is identical and the kept half exact."""

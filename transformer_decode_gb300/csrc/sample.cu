@@ -26,12 +26,17 @@
 // After both truncations the kept set is {i : (key_i << 32 | i) >= C} for one
 // 64-bit threshold C, which is all the draw needs.
 //
-// Work per row: pass 0 writes the scores' keys to scratch and builds the top
-// digit histogram; top-k is a radix select, 8 bits per pass, over those
-// keys; top-p sorts the kept (key, index) pairs in shared memory (bitonic) up
-// to 8192 of them, else with a stable 4-bit LSD radix sort in scratch; the
-// draw reads the keys once more. Invalid rows (NaN logits; at T > 0 a +inf
-// score or all scores -inf) give token -1.
+// Work per row: pass 0 writes the scores' keys to scratch and, with top-k,
+// a histogram of their top 12 bits (warp-aggregated shared atomics: scores
+// crowd into few bins). When the bins holding the k largest keys hold at
+// most 8192 tokens (the usual case: top-k 20 keeps tens), one more pass
+// gathers those candidates into shared memory and everything else (the
+// k-th key, top-p, the draw) runs on them there. Otherwise top-k finishes
+// as a radix select over the keys (10 more bits per pass); top-p sorts the
+// kept (key, index) pairs in shared memory (bitonic) up to 8192 of them,
+// else with a stable 4-bit LSD radix sort in scratch; the draw reads the
+// keys once more. Invalid rows (NaN logits; at T > 0 a +inf score or all
+// scores -inf) give token -1.
 #include <float.h>
 
 #include "kernels.h"
@@ -42,15 +47,19 @@ namespace {
 constexpr int kT = 1024;           // threads per CTA (one row)
 constexpr int kWarps = kT / kWarp;
 constexpr int kSmallCap = 8192;    // kept sets sorted in shared memory
-constexpr size_t kDynSmem = (size_t)kSmallCap * (sizeof(unsigned long long) + sizeof(float));
+constexpr int kBins0 = 4096;       // first select pass: the keys' top 12 bits
+// comp (pairs) + e (weights) + dr (index-ordered draw list); the candidate
+// path's bucket counters (33 x kT u16) alias comp and e
+constexpr size_t kDynSmem = (size_t)kSmallCap * (2 * sizeof(unsigned long long) + sizeof(float));
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 struct SampleShared {
-  uint32_t hist[256];
+  uint32_t hist[kBins0];
   uint32_t red32[kWarps];
   unsigned long long red64[kWarps];
   double redd[kWarps];
   uint32_t bc[8];
+  uint32_t btot[33];
   unsigned long long bc64;
 };
 
@@ -187,6 +196,41 @@ __device__ int warp_cut(const float* e, int n, float tot, float thr) {
   return n - 1;
 }
 
+// The bin, among BPT * kT counts, that holds the need-th largest key (bins
+// scanned from the top): sh.bc = {bin, count in higher bins, count in bin}.
+template <int BPT>
+__device__ void select_bin(const uint32_t* hist, uint32_t need, SampleShared& sh) {
+  constexpr int nb = BPT * kT;
+  uint32_t c[BPT], sum = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    c[j] = hist[nb - 1 - (BPT * (int)threadIdx.x + j)];
+    sum += c[j];
+  }
+  uint32_t total;
+  const uint32_t exc = block_excl_scan_u32(sum, sh.red32, &total);
+  if (exc < need && exc + sum >= need) {  // exactly one thread
+    uint32_t above = exc, bin = 0, cnt = 0;
+    bool found = false;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      if (!found) {
+        if (above + c[j] >= need) {
+          found = true;
+          bin = nb - 1 - (BPT * threadIdx.x + j);
+          cnt = c[j];
+        } else {
+          above += c[j];
+        }
+      }
+    }
+    sh.bc[0] = bin;
+    sh.bc[1] = above;
+    sh.bc[2] = cnt;
+  }
+  __syncthreads();
+}
+
 // Ascending bitonic sort of n2 (a power of two, >= 2) 64-bit words in shared memory.
 __device__ void bitonic_sort_u64(unsigned long long* a, int n2) {
   for (int size = 2; size <= n2; size <<= 1) {
@@ -287,6 +331,176 @@ __device__ void finish(const SampleArgs& a, int row, int tok, uint32_t nk, uint3
   }
 }
 
+// fp64 inverse-CDF draw over n (index << 32 | fp32 weight bits) words sorted
+// by index: per-thread contiguous segments, a block scan, and the thread
+// whose segment crosses u * total walks it. Returns the token to thread 0
+// through sh.bc[6].
+__device__ void draw_list(const unsigned long long* dr, int n, double u, SampleShared& sh) {
+  const int tid = threadIdx.x;
+  const int seg = (n + kT - 1) / kT;
+  const int lo = min(n, tid * seg), hi = min(n, lo + seg);
+  double part = 0.0;
+  int last = -1;
+  for (int t = lo; t < hi; ++t) {
+    const float w = __uint_as_float((uint32_t)dr[t]);
+    if (w > 0.f) {
+      part += (double)w;
+      last = (int)(dr[t] >> 32);
+    }
+  }
+  double incl, total;
+  const double excl = block_excl_scan_f64(part, sh.redd, &incl, &total);
+  const double r = u * total;
+  const uint32_t win = block_min_u32(part > 0.0 && incl > r ? (uint32_t)tid : kFull, sh.red32);
+  const uint32_t lastpos = block_max_u32((uint32_t)(last + 1), sh.red32);
+  if (win == kFull) {
+    if (tid == 0) sh.bc[6] = lastpos - 1;
+  } else if ((uint32_t)tid == win) {
+    double c = excl;
+    int tok = -1, lastw = -1;
+    for (int t = lo; t < hi; ++t) {
+      const float w = __uint_as_float((uint32_t)dr[t]);
+      if (w > 0.f) {
+        c += (double)w;
+        lastw = (int)(dr[t] >> 32);
+        if (c > r) {
+          tok = lastw;
+          break;
+        }
+      }
+    }
+    sh.bc[6] = (uint32_t)(tok >= 0 ? tok : lastw);
+  }
+  __syncthreads();
+}
+
+// The candidate path, for 0 < k <= kSmallCap. s = v / T rounds a monotone
+// map, so the k largest scores belong to the k largest logits; the buckets
+// of log2 distance (in order keys) from the largest logit are counted
+// (pass B: per-thread u16 counters in shared memory, no atomics), and the
+// tokens of the fewest leading buckets that hold at least k are gathered
+// (pass C, dividing only those by T) into shared memory and sorted ascending
+// by (score key, index). The k-th largest key K, the kept suffix, the top-p
+// cut and the draw then all work there. A token outside the gathered set
+// has a logit key <= lkmax - 2^B, so its score key is at most that of
+// v_out / T; the path is taken only when K is above that (else a tie across
+// the boundary is possible) and the gathered set fits: returns false, with
+// nothing written, otherwise.
+__device__ bool sample_candidates(const SampleArgs& a, int row, const float* x, uint32_t lkmax,
+                                  float m, SampleShared& sh, unsigned char* dyn) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = a.V;
+  // pass B: bucket 0 holds distance 0, bucket b >= 1 distances [2^(b-1), 2^b)
+  uint16_t* cnt = reinterpret_cast<uint16_t*>(dyn);  // [33][kT], dead after the totals
+#pragma unroll
+  for (int b = 0; b < 33; ++b) cnt[b * kT + tid] = 0;
+  for (int i = tid; i < V; i += kT) {
+    const uint32_t d = lkmax - score_key(x[i]);
+    const int b = d == 0 ? 0 : 32 - __clz(d);
+    cnt[b * kT + tid] += 1;
+  }
+  __syncthreads();
+  for (int b = warp; b < 33; b += kWarps) {
+    uint32_t t = 0;
+    for (int j = lane; j < kT; j += 32) t += cnt[b * kT + j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+    if (lane == 0) sh.btot[b] = t;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t cum = 0;
+    int B = 32;
+    for (int b = 0; b < 33; ++b) {
+      cum += sh.btot[b];
+      if (cum >= (uint32_t)a.top_k) {
+        B = b;
+        break;
+      }
+    }
+    sh.bc[0] = (uint32_t)B;
+    sh.bc[1] = cum;
+    sh.bc[3] = 0;
+  }
+  __syncthreads();
+  const int B = (int)sh.bc[0];
+  const uint32_t n_c = sh.bc[1];
+  if (n_c > (uint32_t)kSmallCap) return false;
+  const unsigned long long lim = 1ull << B;  // candidates: distance < lim
+
+  unsigned long long* comp = reinterpret_cast<unsigned long long*>(dyn);
+  float* e = reinterpret_cast<float*>(dyn + (size_t)kSmallCap * sizeof(unsigned long long));
+  unsigned long long* dr = reinterpret_cast<unsigned long long*>(
+      dyn + (size_t)kSmallCap * (sizeof(unsigned long long) + sizeof(float)));
+  // pass C: gather (a warp takes its slots with one shared atomic)
+  for (int base = 0; base < V; base += kT) {
+    const int i = base + tid;
+    const float v = i < V ? x[i] : 0.f;
+    const bool take = i < V && (unsigned long long)(lkmax - score_key(v)) < lim;
+    const unsigned bal = __ballot_sync(kFull, take);
+    uint32_t slot0 = 0;
+    if (lane == 0 && bal) slot0 = atomicAdd(&sh.bc[3], (uint32_t)__popc(bal));
+    slot0 = __shfl_sync(kFull, slot0, 0);
+    if (take) {
+      const uint32_t slot = slot0 + __popc(bal & ((1u << lane) - 1u));
+      if (slot < (uint32_t)kSmallCap)
+        comp[slot] = pair_key(score_key(__fdiv_rn(v, a.temperature)), (uint32_t)i);
+    }
+  }
+  __syncthreads();
+  const int nc = (int)n_c;
+  int n2 = 2;
+  while (n2 < nc) n2 <<= 1;
+  for (int j = nc + tid; j < n2; j += kT) comp[j] = ~0ull;
+  bitonic_sort_u64(comp, n2);
+  // the k-th largest score key, and whether a token outside can reach it
+  const uint32_t K = (uint32_t)(comp[nc - a.top_k] >> 32);
+  const uint32_t kNegInf = 0x007FFFFFu;  // order key of -inf: the smallest non-NaN key
+  if ((unsigned long long)lkmax >= lim + kNegInf) {
+    const float v_out = key_score(lkmax - (uint32_t)lim);
+    if (K <= score_key(__fdiv_rn(v_out, a.temperature))) return false;
+  }
+  // the first position holding K: the kept suffix after top-k
+  for (int j = tid; j < nc; j += kT) {
+    const uint32_t kj = (uint32_t)(comp[j] >> 32);
+    if (kj >= K && (j == 0 || (uint32_t)(comp[j - 1] >> 32) < K)) sh.bc[5] = (uint32_t)j;
+  }
+  __syncthreads();
+  const int j0 = (int)sh.bc[5];
+  const int nk = nc - j0;
+  int j1 = j0;
+  if (a.top_p < 1.f && nk > 1) {
+    for (int t = tid; t < nk; t += kT)
+      e[t] = expf(__fsub_rn(key_score((uint32_t)(comp[j0 + t] >> 32)), m));
+    __syncthreads();
+    if (warp == 0) {
+      const float tot = warp_serial_sum(e, nk);
+      const int cut = warp_cut(e, nk, tot, __fsub_rn(1.f, a.top_p));
+      if (lane == 0) sh.bc[4] = (uint32_t)cut;
+    }
+    __syncthreads();
+    j1 = j0 + (int)sh.bc[4];
+  }
+  // the draw over the kept tokens in index order
+  const int np = nc - j1;
+  int np2 = 1;
+  while (np2 < np) np2 <<= 1;
+  for (int t = tid; t < np2; t += kT) {
+    if (t < np) {
+      const unsigned long long c = comp[j1 + t];
+      const float w = expf(__fsub_rn(key_score((uint32_t)(c >> 32)), m));
+      dr[t] = (c << 32) | __float_as_uint(w);
+    } else {
+      dr[t] = ~0ull;
+    }
+  }
+  if (np2 >= 2) bitonic_sort_u64(dr, np2);
+  __syncthreads();
+  draw_list(dr, np, a.u[row], sh);
+  if (tid == 0) finish(a, row, (int)sh.bc[6], (uint32_t)nk, (uint32_t)np);
+  return true;
+}
+
 __global__ void __launch_bounds__(kT, 1) k_sample(const __grid_constant__ SampleArgs a) {
   __shared__ SampleShared sh;
   extern __shared__ __align__(16) unsigned char dyn[];
@@ -314,86 +528,61 @@ __global__ void __launch_bounds__(kT, 1) k_sample(const __grid_constant__ Sample
     return;
   }
 
-  // ---- pass 0: score keys, validity, max, top digit histogram
-  uint32_t* keys = a.scratch + (size_t)row * 5 * a.vpad;
-  const bool topk = a.top_k > 0 && a.top_k < V;
-  if (tid < 256) sh.hist[tid] = 0;
-  __syncthreads();
-  uint32_t kmax = 0, bad = 0;
+  // ---- pass A: validity and the largest logit. s = v / T rounds a monotone
+  // map, so the largest score is the largest logit's (and is +inf iff some
+  // score is; -inf iff every score is).
+  uint32_t lkmax = 0, bad = 0;
   for (int i = tid; i < V; i += kT) {
     const float v = x[i];
-    const float s = __fdiv_rn(v, a.temperature);
-    if (v != v || s == __int_as_float(0x7f800000)) bad = 1;
-    const uint32_t k = score_key(s);
-    keys[i] = k;
-    kmax = max(kmax, k);
-    if (topk) atomicAdd(&sh.hist[k >> 24], 1u);
+    if (v != v) bad = 1;
+    lkmax = max(lkmax, score_key(v));
   }
   bad = block_max_u32(bad, sh.red32);
-  kmax = block_max_u32(kmax, sh.red32);
-  const float m = key_score(kmax);
-  if (bad || m == -__int_as_float(0x7f800000)) {
+  lkmax = block_max_u32(lkmax, sh.red32);
+  const float m = key_score(score_key(__fdiv_rn(key_score(lkmax), a.temperature)));
+  if (bad || fabsf(m) == __int_as_float(0x7f800000)) {
     if (tid == 0) finish(a, row, -1, 0, 0);
     return;
   }
+  const bool topk = a.top_k > 0 && a.top_k < V;
+  if (topk && a.top_k <= kSmallCap && sample_candidates(a, row, x, lkmax, m, sh, dyn)) return;
 
-  // ---- top-k: radix select of the k-th largest key, 8 bits per pass
+  // ---- general path, pass 0: every score key to scratch; with top-k, a
+  // histogram of their top 12 bits
+  uint32_t* keys = a.scratch + (size_t)row * 5 * a.vpad;
+  if (topk) {
+    for (int j = tid; j < kBins0; j += kT) sh.hist[j] = 0;
+    __syncthreads();
+  }
+  for (int i = tid; i < V; i += kT) {
+    const uint32_t k = score_key(__fdiv_rn(x[i], a.temperature));
+    keys[i] = k;
+    if (topk) atomicAdd(&sh.hist[k >> 20], 1u);
+  }
+  __syncthreads();
+
   uint32_t K = 0, nk = (uint32_t)V;
   if (topk) {
-    uint32_t prefix = 0, pmask = 0, need = (uint32_t)a.top_k, ngt = 0, neq = 0;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      if (pass > 0) {
-        if (tid < 256) sh.hist[tid] = 0;
-        __syncthreads();
-        for (int i = tid; i < V; i += kT) {
-          const uint32_t k = keys[i];
-          if ((k & pmask) == prefix) atomicAdd(&sh.hist[(k >> shift) & 255u], 1u);
-        }
+    select_bin<kBins0 / kT>(sh.hist, (uint32_t)a.top_k, sh);
+    const uint32_t b0 = sh.bc[0], above0 = sh.bc[1], cnt0 = sh.bc[2];
+    // ---- the rest of the radix select over the keys, 10 bits per pass
+    uint32_t prefix = b0 << 20, pmask = 0xFFF00000u, need = (uint32_t)a.top_k - above0;
+    uint32_t ngt = above0, neq = cnt0;
+    for (int shift = 10; shift >= 0; shift -= 10) {
+      sh.hist[tid] = 0;
+      __syncthreads();
+      for (int i = tid; i < V; i += kT) {
+        const uint32_t k = keys[i];
+        if ((k & pmask) == prefix) atomicAdd(&sh.hist[(k >> shift) & 1023u], 1u);
       }
       __syncthreads();
-      if (warp == 0) {
-        // lane l holds bins 255 - 8 l down to 248 - 8 l (descending)
-        uint32_t c[8], sum = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          c[j] = sh.hist[255 - 8 * lane - j];
-          sum += c[j];
-        }
-        uint32_t inc = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(kFull, inc, o);
-          if (lane >= o) inc += y;
-        }
-        const unsigned ball = __ballot_sync(kFull, inc >= need);
-        if (lane == __ffs(ball) - 1) {
-          uint32_t above = inc - sum, bin = 0, cnt = 0;
-          bool found = false;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (!found) {
-              if (above + c[j] >= need) {
-                found = true;
-                bin = 255 - 8 * lane - j;
-                cnt = c[j];
-              } else {
-                above += c[j];
-              }
-            }
-          }
-          sh.bc[0] = bin;
-          sh.bc[1] = above;
-          sh.bc[2] = cnt;
-        }
-      }
-      __syncthreads();
+      select_bin<1>(sh.hist, need, sh);
       const uint32_t bin = sh.bc[0], above = sh.bc[1];
       neq = sh.bc[2];
       ngt += above;
       need -= above;
       prefix |= bin << shift;
-      pmask |= 255u << shift;
+      pmask |= 1023u << shift;
       __syncthreads();
     }
     K = prefix;
