@@ -76,6 +76,26 @@ __device__ __forceinline__ unsigned long long pair_key(uint32_t k, uint32_t i) {
   return (static_cast<unsigned long long>(k) << 32) | i;
 }
 
+// One pass over a row of V elements: U coalesced loads per thread are
+// issued before any is used (one load in flight per warp would leave a pass
+// waiting on L2 latency), then f(i, value) runs for each, in order; lanes
+// past the end get i >= V and value 0 (every lane calls f, so f may use
+// warp-wide votes).
+template <int U, typename T, typename F>
+__device__ __forceinline__ void row_pass(const T* x, int V, F&& f) {
+  for (int base = 0; base < V; base += U * kT) {
+    T v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * kT + (int)threadIdx.x;
+      v[u] = i < V ? x[i] : T(0);  // plain loads: keys are written earlier in this kernel
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) f(base + u * kT + (int)threadIdx.x, v[u]);
+  }
+}
+constexpr int kUnroll = 16;
+
 // ---------------------------------------------------------------- block reductions
 // Every thread of the CTA calls these and receives the result; the scratch
 // word array is free again when they return.
@@ -394,11 +414,13 @@ __device__ bool sample_candidates(const SampleArgs& a, int row, const float* x, 
   uint16_t* cnt = reinterpret_cast<uint16_t*>(dyn);  // [33][kT], dead after the totals
 #pragma unroll
   for (int b = 0; b < 33; ++b) cnt[b * kT + tid] = 0;
-  for (int i = tid; i < V; i += kT) {
-    const uint32_t d = lkmax - score_key(x[i]);
-    const int b = d == 0 ? 0 : 32 - __clz(d);
-    cnt[b * kT + tid] += 1;
-  }
+  row_pass<kUnroll>(x, V, [&](int i, float v) {
+    if (i < V) {
+      const uint32_t d = lkmax - score_key(v);
+      const int b = d == 0 ? 0 : 32 - __clz(d);
+      cnt[b * kT + tid] += 1;
+    }
+  });
   __syncthreads();
   for (int b = warp; b < 33; b += kWarps) {
     uint32_t t = 0;
@@ -433,20 +455,20 @@ __device__ bool sample_candidates(const SampleArgs& a, int row, const float* x, 
   unsigned long long* dr = reinterpret_cast<unsigned long long*>(
       dyn + (size_t)kSmallCap * (sizeof(unsigned long long) + sizeof(float)));
   // pass C: gather (a warp takes its slots with one shared atomic)
-  for (int base = 0; base < V; base += kT) {
-    const int i = base + tid;
-    const float v = i < V ? x[i] : 0.f;
+  row_pass<kUnroll>(x, V, [&](int i, float v) {
     const bool take = i < V && (unsigned long long)(lkmax - score_key(v)) < lim;
     const unsigned bal = __ballot_sync(kFull, take);
-    uint32_t slot0 = 0;
-    if (lane == 0 && bal) slot0 = atomicAdd(&sh.bc[3], (uint32_t)__popc(bal));
-    slot0 = __shfl_sync(kFull, slot0, 0);
-    if (take) {
-      const uint32_t slot = slot0 + __popc(bal & ((1u << lane) - 1u));
-      if (slot < (uint32_t)kSmallCap)
-        comp[slot] = pair_key(score_key(__fdiv_rn(v, a.temperature)), (uint32_t)i);
+    if (bal) {
+      uint32_t slot0 = 0;
+      if (lane == 0) slot0 = atomicAdd(&sh.bc[3], (uint32_t)__popc(bal));
+      slot0 = __shfl_sync(kFull, slot0, 0);
+      if (take) {
+        const uint32_t slot = slot0 + __popc(bal & ((1u << lane) - 1u));
+        if (slot < (uint32_t)kSmallCap)
+          comp[slot] = pair_key(score_key(__fdiv_rn(v, a.temperature)), (uint32_t)i);
+      }
     }
-  }
+  });
   __syncthreads();
   const int nc = (int)n_c;
   int n2 = 2;
@@ -512,11 +534,12 @@ __global__ void __launch_bounds__(kT, 1) k_sample(const __grid_constant__ Sample
   if (a.temperature == 0.f) {
     unsigned long long best = 0;
     uint32_t nan = 0;
-    for (int i = tid; i < V; i += kT) {
-      const float v = x[i];
-      if (v != v) nan = 1;
-      best = max(best, pair_key(score_key(v), 0xFFFFFFFFu - (uint32_t)i));
-    }
+    row_pass<kUnroll>(x, V, [&](int i, float v) {
+      if (i < V) {
+        if (v != v) nan = 1;
+        best = max(best, pair_key(score_key(v), 0xFFFFFFFFu - (uint32_t)i));
+      }
+    });
     nan = block_max_u32(nan, sh.red32);
     best = block_max_u64(best, sh.red64);
     if (tid == 0) {
@@ -532,11 +555,12 @@ __global__ void __launch_bounds__(kT, 1) k_sample(const __grid_constant__ Sample
   // map, so the largest score is the largest logit's (and is +inf iff some
   // score is; -inf iff every score is).
   uint32_t lkmax = 0, bad = 0;
-  for (int i = tid; i < V; i += kT) {
-    const float v = x[i];
-    if (v != v) bad = 1;
-    lkmax = max(lkmax, score_key(v));
-  }
+  row_pass<kUnroll>(x, V, [&](int i, float v) {
+    if (i < V) {
+      if (v != v) bad = 1;
+      lkmax = max(lkmax, score_key(v));
+    }
+  });
   bad = block_max_u32(bad, sh.red32);
   lkmax = block_max_u32(lkmax, sh.red32);
   const float m = key_score(score_key(__fdiv_rn(key_score(lkmax), a.temperature)));
@@ -554,11 +578,13 @@ __global__ void __launch_bounds__(kT, 1) k_sample(const __grid_constant__ Sample
     for (int j = tid; j < kBins0; j += kT) sh.hist[j] = 0;
     __syncthreads();
   }
-  for (int i = tid; i < V; i += kT) {
-    const uint32_t k = score_key(__fdiv_rn(x[i], a.temperature));
-    keys[i] = k;
-    if (topk) atomicAdd(&sh.hist[k >> 20], 1u);
-  }
+  row_pass<kUnroll>(x, V, [&](int i, float v) {
+    if (i < V) {
+      const uint32_t k = score_key(__fdiv_rn(v, a.temperature));
+      keys[i] = k;
+      if (topk) atomicAdd(&sh.hist[k >> 20], 1u);
+    }
+  });
   __syncthreads();
 
   uint32_t K = 0, nk = (uint32_t)V;
@@ -571,10 +597,9 @@ __global__ void __launch_bounds__(kT, 1) k_sample(const __grid_constant__ Sample
     for (int shift = 10; shift >= 0; shift -= 10) {
       sh.hist[tid] = 0;
       __syncthreads();
-      for (int i = tid; i < V; i += kT) {
-        const uint32_t k = keys[i];
-        if ((k & pmask) == prefix) atomicAdd(&sh.hist[(k >> shift) & 1023u], 1u);
-      }
+      row_pass<kUnroll>(keys, V, [&](int i, uint32_t k) {
+        if (i < V && (k & pmask) == prefix) atomicAdd(&sh.hist[(k >> shift) & 1023u], 1u);
+      });
       __syncthreads();
       select_bin<1>(sh.hist, need, sh);
       const uint32_t bin = sh.bc[0], above = sh.bc[1];
