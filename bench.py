@@ -181,6 +181,14 @@ def max_over_ranks(ws, v):
     return float(t.item())
 
 
+def replica_rate(ws, batch, steps, local_seconds):
+    """Whole-job tokens/s of `ws` independent replicas, each decoding `batch`
+    sequences for `steps` steps: every rank's tokens over the slowest rank's
+    time (the max over ranks). Returns (rate, max_seconds)."""
+    el = max_over_ranks(ws, local_seconds)
+    return ws * batch * steps / el, el
+
+
 # ---------------------------------------------------------------- CPU oracle
 def oracle_sample(shape, weights_cpu, prompt, seconds, max_steps):
     """Time the CPU oracle decoding the workload's sequence (prompt steps, then
@@ -320,9 +328,8 @@ def run_nc(args, ws, rank, local):
     if rank == 0:
         time.sleep(0.2)
         sampler.stop()
-    el = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3)
+    value, el = replica_rate(ws, B, args.steps, e0.elapsed_time(e1) / 1e3)
     restarts = sum(1 for i in range(args.steps) if i % cycle == 0)
-    value = ws * B * args.steps / el
     ms = el / args.steps * 1e3
     bytes_avg = sum(step_bytes(shape, B, [p]) for p in used) / len(used)
     hbm_gbs = bytes_avg / (el / args.steps) / 1e9
@@ -357,8 +364,7 @@ def run_nc(args, ws, rank, local):
         nxt_h.copy_(nxt_d, non_blocking=True)
         st.synchronize()
         cur_tok = int(nxt_h[0])
-    t_e2e = max_over_ranks(ws, time.perf_counter() - t0)
-    e2e_value = ws * B * k_e2e / t_e2e
+    e2e_value, t_e2e = replica_rate(ws, B, k_e2e, time.perf_counter() - t0)
 
     # ---- the step kernel: one launch per timed step, so its average launch
     # duration is the timed region over the steps (CUDA events on its stream;
@@ -475,7 +481,7 @@ def run_sampled(args, ws, rank, local):
     if rank == 0:
         time.sleep(0.2)
         clk.stop()
-    el = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3)
+    value, el = replica_rate(ws, B, args.steps, e0.elapsed_time(e1) / 1e3)
     bytes_avg = sum(step_bytes(shape, B, [p]) for p in used) / len(used)
     peak, peak_kind = peaks()
 
@@ -515,7 +521,7 @@ def run_sampled(args, ws, rank, local):
         nxt_h.copy_(nxt, non_blocking=True)
         st.synchronize()
         cur = int(nxt_h[0])
-    t_e2e = max_over_ranks(ws, time.perf_counter() - t0)
+    e2e_value, t_e2e = replica_rate(ws, B, k_e2e, time.perf_counter() - t0)
 
     path = model.decode_path(B, kv)
     launches = (1 if path == "persistent" else 2 + 5 * shape.n_layers) + 1
@@ -523,7 +529,7 @@ def run_sampled(args, ws, rank, local):
         dur = el / args.steps
         row_bytes = B * shape.vocab * 4
         print(json.dumps({
-            "metric": METRIC, "value": ws * B * args.steps / el, "unit": "tokens/s",
+            "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dur * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -541,7 +547,7 @@ def run_sampled(args, ws, rank, local):
                         "logit_bytes": row_bytes, "gbs": row_bytes / (samp_us * 1e-6) / 1e9,
                         "bound": "latency (one row per CTA; the logits sit in L2)"},
             "cpu_baseline": None,
-            "e2e": {"value": ws * B * k_e2e / t_e2e, "unit": "tokens/s", "steps": k_e2e,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": k_e2e,
                     "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
             "gpu_launches": args.steps * launches,
             "clocks": clk.summary(w0, w1),
@@ -638,8 +644,7 @@ def run_workload(args, ws, rank, local, name):
     if rank == 0:
         time.sleep(0.2)
         sampler.stop()
-    el = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3)
-    value = ws * B * args.steps / el
+    value, el = replica_rate(ws, B, args.steps, e0.elapsed_time(e1) / 1e3)
     dur = el / args.steps
     bytes_avg = sum(step_bytes(shape, B, u.tolist(), w8a8=cfg["w8a8"]) for u in used) / len(used)
     peak, peak_kind = peaks()
@@ -672,7 +677,7 @@ def run_workload(args, ws, rank, local, name):
         nxt_h.copy_(nxt_d, non_blocking=True)
         st.synchronize()
         cur = nxt_h.clone()
-    t_e2e = max_over_ranks(ws, time.perf_counter() - t0)
+    e2e_value, t_e2e = replica_rate(ws, B, k_e2e, time.perf_counter() - t0)
     path = model.decode_path(B, kv)
     launches_per_step = 1 if path == "persistent" else 2 + 5 * shape.n_layers
     if rank == 0:
@@ -699,7 +704,7 @@ def run_workload(args, ws, rank, local, name):
                          "peak_kind": peak_kind, "avg_step_us": dur * 1e6,
                          "algorithmic_bytes_per_step": bytes_avg},
             "cpu_baseline": None,
-            "e2e": {"value": ws * B * k_e2e / t_e2e, "unit": "tokens/s", "steps": k_e2e,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": k_e2e,
                     "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
             "gpu_launches": args.steps * launches_per_step,
             "clocks": sampler.summary(w0, w1),

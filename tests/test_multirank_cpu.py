@@ -1,0 +1,83 @@
+"""The N > 1 path of bench.py on CPU: world-size-2 gloo ranks (replicas
+only, so the only collectives are the timing barrier and the max over
+ranks), and the reference arm under torchrun. No GPU."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, ws, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    got_ws, got_rank, local = bench.dist_init()
+    assert (got_ws, got_rank, local) == (ws, rank, rank)
+    import torch.distributed as dist
+    assert dist.get_backend() == "gloo"
+    bench.barrier(ws)
+    # rank r took 1 + r seconds for 10 steps of batch 3: the job rate is every
+    # rank's tokens over the slowest rank's time
+    rate, el = bench.replica_rate(ws, 3, 10, 1.0 + rank)
+    out[rank] = (rate, el)
+    bench.barrier(ws)
+    dist.destroy_process_group()
+
+
+def test_replica_rate_two_gloo_ranks():
+    ws = 2
+    out = mp.Manager().dict()
+    mp.spawn(_rank, args=(ws, _free_port(), out), nprocs=ws, join=True)
+    for r in range(ws):
+        rate, el = out[r]
+        assert el == 2.0
+        assert rate == pytest.approx(ws * 3 * 10 / 2.0)
+
+
+def test_replica_rate_single_process():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.replica_rate(1, 16, 64, 2.0) == (16 * 64 / 2.0, 2.0)
+
+
+WRAPPER = """
+import sys
+sys.path.insert(0, {root!r})
+from transformer_decode_gb300 import synth
+synth.QWEN2_0P5B = synth.TINY  # the launch logic under test, on a model the CPU makes fast
+import bench
+bench.main()
+"""
+
+
+def test_reference_arm_under_torchrun_prints_one_line(tmp_path):
+    """--impl reference at N = 2 under torchrun: rank 0 times the oracle and
+    prints one JSON line; rank 1 exits 0 without work."""
+    script = tmp_path / "bench_tiny.py"
+    script.write_text(WRAPPER.format(root=ROOT))
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           str(script), "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, cwd=ROOT, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
