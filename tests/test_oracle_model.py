@@ -175,3 +175,71 @@ def test_w8a8_model_close_to_bf16(orc, tiny):
     for i in range(6):
         lg, _ = m8.decode_step(kv, toks[i:i + 1], np.array([i], np.int32), "f64")
     assert _rel_l2(lg[0], a[-1]) < 1e-14
+
+
+def _torch_forward(shape, w, tokens):
+    """The whole decoder from torch's library routines in fp64, written from
+    the architecture (nanoinfer, "Model architecture"): pre-norm blocks with
+    residual adds, QKV bias or per-head q/k RMSNorm, half-split RoPE as a
+    complex rotation of (x_i, x_{i+D/2}), causal grouped-query SDPA (query
+    head h reads kv head h // G), SwiGLU, final norm, tied or untied head."""
+    F = torch.nn.functional
+    d = lambda t: None if t is None else t.double()
+    H, D, G = shape.hidden, shape.head_dim, shape.group
+    T = len(tokens)
+    x = d(w["embed"])[torch.as_tensor(tokens, dtype=torch.long)]
+    half = D // 2
+    inv = torch.tensor([1.0 / shape.rope_theta ** (2 * i / D) for i in range(half)],
+                       dtype=torch.float64)
+    rot = torch.polar(torch.ones(T, half, dtype=torch.float64),
+                      torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :])
+
+    def rope(t):  # t [heads, T, D]
+        z = torch.complex(t[..., :half], t[..., half:]) * rot
+        return torch.cat([z.real, z.imag], -1)
+
+    for lw in w["layers"]:
+        lw = {k: d(v) for k, v in lw.items()}
+        n = F.rms_norm(x, (H,), lw["g_attn"], shape.rms_eps)
+        q = F.linear(n, lw["wq"], lw["bq"]).view(T, -1, D).transpose(0, 1)
+        k = F.linear(n, lw["wk"], lw["bk"]).view(T, -1, D).transpose(0, 1)
+        v = F.linear(n, lw["wv"], lw["bv"]).view(T, -1, D).transpose(0, 1)
+        if shape.qk_norm:
+            q = F.rms_norm(q, (D,), lw["g_q"], shape.rms_eps)
+            k = F.rms_norm(k, (D,), lw["g_k"], shape.rms_eps)
+        q, k = rope(q), rope(k)
+        k = k.repeat_interleave(G, 0)
+        v = v.repeat_interleave(G, 0)
+        a = F.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True)[0]
+        x = x + F.linear(a.transpose(0, 1).reshape(T, -1), lw["wo"])
+        n2 = F.rms_norm(x, (H,), lw["g_mlp"], shape.rms_eps)
+        x = x + F.linear(F.silu(F.linear(n2, lw["wg"])) * F.linear(n2, lw["wu"]), lw["wd"])
+    head = d(w["lm_head"]) if w.get("lm_head") is not None else d(w["embed"])
+    return F.linear(F.rms_norm(x, (H,), d(w["g_final"]), shape.rms_eps), head).numpy()
+
+
+@pytest.fixture(scope="module")
+def qwen_dims(orc):
+    """The 0.5B layer shape (14 query heads, group 7, H 896, F 4864) with two
+    layers and a 1000-token vocabulary, so fp64 torch stays small."""
+    import dataclasses
+    s = dataclasses.replace(synth.QWEN2_0P5B, n_layers=2, vocab=1000)
+    w = synth.model_weights(s, seed=0)
+    return orc.OracleModel(s, w), w
+
+
+@pytest.mark.parametrize("which", ["tiny", "tiny_qk", "qwen_dims"])
+def test_whole_model_matches_torch_library_composition(which, request):
+    """The oracle's wiring of the pieces (which gain feeds which norm, the
+    residual order, bias or q/k norm before RoPE, the head) against the same
+    model composed from torch's own routines: one shape carries the QKV bias
+    and the tied head, the other q/k norm, no bias and an untied head."""
+    m, w = request.getfixturevalue(which)
+    toks = synth.token_ids(10, m.shape.vocab, stream=11)
+    ref = _torch_forward(m.shape, w, toks.tolist())
+    got = m.forward_full(toks, "f64")
+    assert _rel_l2(got, ref) < 1e-6
+    # a planted wiring mistake (the MLP norm reading the attention gain) is seen
+    w2 = dict(w)
+    w2["layers"] = [dict(lw, g_mlp=lw["g_attn"]) for lw in w["layers"]]
+    assert _rel_l2(got, _torch_forward(m.shape, w2, toks.tolist())) > 1e-4
