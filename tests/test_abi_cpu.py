@@ -119,3 +119,53 @@ def test_sample_rejects_bad_arguments_before_any_launch(lib):
     assert call(scratch=C.c_void_p(4100)) == E["NC_ERR_INVALID_ARGUMENT"]  # misaligned
     assert call(nbytes=need - 1) == E["NC_ERR_CAPACITY"]
     assert b"needed" in lib.nc_last_error_message()
+
+
+def test_static_attention_validates_cache_and_positions_on_the_host(lib):
+    """nc_attn_decode_static needs no model: every rejection below is decided
+    from host data (sizes, positions_host, block_table_host) before anything
+    touches the device. Every call here must be rejected: the pointers are
+    fake and must never reach a kernel."""
+    import numpy as np
+    E = {n: nc.STATUS.index(n) for n in nc.STATUS}
+    P = C.c_void_p(4096)
+
+    def kv(**kw):
+        d = dict(paged=0, dtype=nc.NC_KV_F32, batch_capacity=2, max_ctx=64, block_size=16,
+                 num_blocks=8, max_blocks_per_seq=4, k=4096, v=8192, block_table=None,
+                 block_table_host=None)
+        d.update(kw)
+        return nc.KVStruct(**d)
+
+    def call(pos=(3, 5), B=2, Hq=14, Hkv=2, D=64, L=24, layer=0, cache=None, q=P, out=P):
+        ph = np.ascontiguousarray(np.asarray(pos, np.int32))
+        c = cache if cache is not None else kv()
+        return lib.nc_attn_decode_static(Hq, Hkv, D, L, layer, B, q, P,
+                                         ph.ctypes.data_as(C.c_void_p), C.byref(c), out, None)
+
+    assert call(q=None) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(out=None) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(cache=kv(k=0)) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(D=96) == E["NC_ERR_SHAPE"]
+    assert call(Hq=15) == E["NC_ERR_SHAPE"]                 # not a multiple of Hkv
+    assert call(Hq=18, Hkv=2) == E["NC_ERR_SHAPE"]          # group 9 > 8
+    assert call(layer=24) == E["NC_ERR_SHAPE"] and call(layer=-1) == E["NC_ERR_SHAPE"]
+    assert call(B=0, pos=()) == E["NC_ERR_CAPACITY"]
+    assert call(B=17, pos=[0] * 17) == E["NC_ERR_CAPACITY"]
+    assert call(cache=kv(dtype=5)) == E["NC_ERR_DTYPE"]
+    assert call(cache=kv(k=4100)) == E["NC_ERR_INVALID_ARGUMENT"]   # misaligned
+    assert call(cache=kv(batch_capacity=1)) == E["NC_ERR_CAPACITY"]
+    assert call(pos=(3, 64)) == E["NC_ERR_POSITION"]        # slot 64 of a 64-slot cache
+    assert call(pos=(-1, 0)) == E["NC_ERR_POSITION"]
+    # paged: tables required; every block up to the position must be in the pool
+    assert call(cache=kv(paged=1)) == E["NC_ERR_INVALID_ARGUMENT"]
+    table = np.array([[0, 1, 2, 3], [4, 5, -1, 7]], np.int32)
+    pk = kv(paged=1, block_table=4096, block_table_host=table.ctypes.data)
+    assert call(pos=(63, 32), cache=pk) == E["NC_ERR_POSITION"]       # block 2 of row 1 is a hole
+    table[0, 3] = 8                                                   # outside the 8-block pool
+    assert call(pos=(63, 0), cache=pk) == E["NC_ERR_POSITION"]
+    assert call(pos=(64, 0), cache=pk) == E["NC_ERR_POSITION"]        # past 4 blocks x 16
+    # the static merge tickets bound batch x kv heads
+    assert call(B=16, pos=[0] * 16, Hq=128, Hkv=128,
+                cache=kv(batch_capacity=16)) == E["NC_ERR_CAPACITY"]
+    assert b"tickets" in lib.nc_last_error_message()
