@@ -317,3 +317,34 @@ def test_generator_is_device_independent_and_seeded():
     assert not torch.equal(a.view(torch.int16), c.view(torch.int16))
     x = synth.normal_bf16(0, 9, (200000,), 0.02).float()
     assert abs(x.mean().item()) < 2e-4 and abs(x.std().item() / 0.02 - 1) < 0.01
+
+
+def test_paged_inputs_follow_the_allocation_reading():
+    """Reading R16 for the paged workloads: sequence b owns ceil((P_b + steps) / 16)
+    blocks of a pool of exactly the blocks needed, each block owned once, in a
+    seeded shuffled order; unused table entries are -1. Past lengths are
+    seeded and inside [256, 4096]."""
+    past = synth.past_lengths(16, 256, 4096).tolist()
+    assert past == synth.past_lengths(16, 256, 4096).tolist()
+    assert all(256 <= p <= 4096 for p in past) and len(set(past)) > 8
+    table, total = synth.block_tables(past, 32, 16)
+    need = [-(-(p + 32) // 16) for p in past]
+    assert total == sum(need) and table.shape == (16, max(need))
+    owned = []
+    for b, n in enumerate(need):
+        row = table[b].tolist()
+        assert all(0 <= x < total for x in row[:n]) and all(x == -1 for x in row[n:])
+        owned += row[:n]
+    assert sorted(owned) == list(range(total))                # a permutation of the pool
+    assert owned != list(range(total))                        # shuffled, not in order
+    t2, _ = synth.block_tables(past, 32, 16)
+    assert torch.equal(table, t2)                             # seeded
+    t3, _ = synth.block_tables(past, 32, 16, seed=9)
+    assert not torch.equal(table, t3)
+
+
+def test_uniform_f64_is_seeded_and_in_the_open_unit_interval():
+    u = synth.uniform_f64(5, 0, 100000)
+    assert u.dtype == torch.float64 and torch.equal(u, synth.uniform_f64(5, 0, 100000))
+    assert (u > 0).all() and (u < 1).all()
+    assert abs(u.mean().item() - 0.5) < 0.005 and abs(u.var().item() - 1 / 12) < 0.002
