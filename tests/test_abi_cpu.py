@@ -169,3 +169,28 @@ def test_static_attention_validates_cache_and_positions_on_the_host(lib):
     assert call(B=16, pos=[0] * 16, Hq=128, Hkv=128,
                 cache=kv(batch_capacity=16)) == E["NC_ERR_CAPACITY"]
     assert b"tickets" in lib.nc_last_error_message()
+
+
+def test_entry_points_reject_misaligned_pointers(lib):
+    """Each pointer must meet the widest access its kernels make through it
+    (16-byte weight and activation streams, 8-byte gain pairs, scalar fp32 /
+    int32 / fp64 elements); a misaligned one is refused on the host, before
+    any launch."""
+    E = nc.STATUS.index("NC_ERR_INVALID_ARGUMENT")
+    P, P2, P4 = C.c_void_p(4096), C.c_void_p(4098), C.c_void_p(4100)
+    # gamma read 8 bytes at a time, bias per bf16, y per fp32
+    assert lib.nc_rmsnorm_gemv(P, P4, 1e-6, P, None, 1, 64, 8, P, None) == E
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, C.c_void_p(4097), 1, 64, 8, P, None) == E
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, None, 1, 64, 8, P2, None) == E
+    assert lib.nc_swiglu_gemv(P, P4, 1e-6, P, 1, 64, 8, P, None) == E
+    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, 1, 64, 8, P2, None) == E
+    assert lib.nc_gemv_residual(P, P, 1, 64, 8, P2, None) == E
+    assert lib.nc_w8a8_gemv(P2, None, 1e-6, P, P, None, 1, 64, 8, P, None, None, None, None) == E
+    assert lib.nc_w8a8_gemv(P, None, 1e-6, P, P2, None, 1, 64, 8, P, None, None, None, None) == E
+    assert lib.nc_w8a8_gemv(P, None, 1e-6, P, P, None, 1, 64, 8, P, None, P2, None, None) == E
+    # the sampler: fp32 logits, int32 tokens and counts, fp64 uniforms
+    n = lib.nc_sample_scratch_bytes(1, 1000)
+    assert lib.nc_sample(P2, 1, 1000, 0.7, 20, 0.8, P, P, None, P, n, None) == E
+    assert lib.nc_sample(P, 1, 1000, 0.7, 20, 0.8, P4, P, None, P, n, None) == E
+    assert lib.nc_sample(P, 1, 1000, 0.7, 20, 0.8, P, P2, None, P, n, None) == E
+    assert lib.nc_sample(P, 1, 1000, 0.7, 20, 0.8, P, P, P2, P, n, None) == E

@@ -33,6 +33,8 @@ static const Model* M(const nc_model* m) { return reinterpret_cast<const Model*>
 static cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
 
 static bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+// NULL or a multiple of n bytes: the widest access the kernels make through p.
+static bool aligned(const void* p, uintptr_t n) { return reinterpret_cast<uintptr_t>(p) % n == 0; }
 
 static nc_status launch_result(cudaError_t e, const char* what) {
   if (e != cudaSuccess) return fail(NC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -158,6 +160,8 @@ nc_status nc_rmsnorm_gemv(const float* x, const void* gamma, float eps, const vo
                           const void* bias, int B, int K, int N, float* y, void* stream) {
   NC_CHECK(x && W && y, NC_ERR_INVALID_ARGUMENT, "null pointer");
   NC_CHECK(aligned16(x) && aligned16(W), NC_ERR_INVALID_ARGUMENT, "x and W must be 16-byte aligned");
+  NC_CHECK(aligned(gamma, 8) && aligned(bias, 2) && aligned(y, 4), NC_ERR_INVALID_ARGUMENT,
+           "gamma must be 8-byte aligned, bias 2-byte and y 4-byte");
   nc_status st = check_gemv_shape(B, K, N);
   if (st) return st;
   GemvArgs a{x, static_cast<const uint16_t*>(gamma), eps, static_cast<const uint16_t*>(W),
@@ -169,6 +173,7 @@ nc_status nc_gemv_residual(const float* a_in, const void* W, int B, int K, int N
                            void* stream) {
   NC_CHECK(a_in && W && x, NC_ERR_INVALID_ARGUMENT, "null pointer");
   NC_CHECK(aligned16(a_in) && aligned16(W), NC_ERR_INVALID_ARGUMENT, "inputs must be 16-byte aligned");
+  NC_CHECK(aligned(x, 4), NC_ERR_INVALID_ARGUMENT, "x must be 4-byte aligned");
   nc_status st = check_gemv_shape(B, K, N);
   if (st) return st;
   GemvArgs a{a_in, nullptr, 0.f, static_cast<const uint16_t*>(W), nullptr, B, K, N, x};
@@ -179,6 +184,8 @@ nc_status nc_swiglu_gemv(const float* x, const void* gamma, float eps, const voi
                          int K, int F, float* h, void* stream) {
   NC_CHECK(x && W_gu && h, NC_ERR_INVALID_ARGUMENT, "null pointer");
   NC_CHECK(aligned16(x) && aligned16(W_gu), NC_ERR_INVALID_ARGUMENT, "inputs must be 16-byte aligned");
+  NC_CHECK(aligned(gamma, 8) && aligned(h, 4), NC_ERR_INVALID_ARGUMENT,
+           "gamma must be 8-byte aligned and h 4-byte");
   nc_status st = check_gemv_shape(B, K, F);
   if (st) return st;
   GemvArgs a{x, static_cast<const uint16_t*>(gamma), eps, static_cast<const uint16_t*>(W_gu),
@@ -223,6 +230,10 @@ nc_status nc_lm_head_argmax(nc_model* m, const float* x, const void* gamma, floa
                             const void* W, int B, int K, int V, float* logits, int32_t* next,
                             void* stream) {
   NC_CHECK(m && x && gamma && W && logits, NC_ERR_INVALID_ARGUMENT, "null pointer");
+  NC_CHECK(aligned16(x) && aligned16(W) && aligned(gamma, 8) && aligned(logits, 4) &&
+               aligned(next, 4),
+           NC_ERR_INVALID_ARGUMENT,
+           "x and W must be 16-byte aligned, gamma 8-byte, logits and next 4-byte");
   Model* mm = M(m);
   NC_CHECK(!mm->unhealthy, NC_ERR_UNHEALTHY, "model saw an earlier CUDA failure");
   NC_CHECK(B >= 1 && B <= mm->max_batch, NC_ERR_CAPACITY, "batch outside [1, max_batch]");
@@ -248,6 +259,9 @@ nc_status nc_w8a8_gemv(const float* x, const void* gamma, float eps, const int8_
                        int8_t* xq_out, float* sx_out, int32_t* acc_out, void* stream) {
   NC_CHECK(x && Wq && w_scale && y, NC_ERR_INVALID_ARGUMENT, "null pointer");
   NC_CHECK(aligned16(Wq), NC_ERR_INVALID_ARGUMENT, "Wq must be 16-byte aligned");
+  NC_CHECK(aligned(x, 4) && aligned(gamma, 2) && aligned(w_scale, 4) && aligned(bias, 2) &&
+               aligned(y, 4) && aligned(sx_out, 4) && aligned(acc_out, 4),
+           NC_ERR_INVALID_ARGUMENT, "fp32 and int32 pointers must be 4-byte aligned, bf16 2-byte");
   NC_CHECK(B >= 1 && B <= 16, NC_ERR_SHAPE, "batch outside [1, 16]");
   const int bt = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;  // batch tile
   NC_CHECK(K >= 16 && K % 16 == 0 && (size_t)bt * K <= 200000, NC_ERR_SHAPE,
@@ -267,6 +281,8 @@ nc_status nc_sample(const float* logits, int B, int V, float temperature, int to
                     const double* u, int32_t* tokens, int32_t* kept, void* scratch,
                     size_t scratch_bytes, void* stream) {
   NC_CHECK(logits && tokens, NC_ERR_INVALID_ARGUMENT, "logits and tokens must not be NULL");
+  NC_CHECK(aligned(logits, 4) && aligned(tokens, 4) && aligned(kept, 4) && aligned(u, 8),
+           NC_ERR_INVALID_ARGUMENT, "logits, tokens and kept must be 4-byte aligned, u 8-byte");
   NC_CHECK(B >= 1 && B <= 65535, NC_ERR_SHAPE, "batch %d outside [1, 65535]", B);
   NC_CHECK(V >= 1 && V <= (1 << 24), NC_ERR_SHAPE, "V = %d outside [1, 2^24]", V);
   NC_CHECK(temperature >= 0.f && temperature <= FLT_MAX, NC_ERR_INVALID_ARGUMENT,

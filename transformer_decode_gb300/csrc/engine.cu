@@ -442,6 +442,11 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
   NC_CHECK(batch >= 1 && batch <= m->max_batch, NC_ERR_CAPACITY, "batch %d outside [1, %d]",
            batch, m->max_batch);
   NC_CHECK(tokens && positions && logits, NC_ERR_INVALID_ARGUMENT, "null device pointer");
+  NC_CHECK(reinterpret_cast<uintptr_t>(tokens) % 4 == 0 &&
+               reinterpret_cast<uintptr_t>(positions) % 4 == 0 &&
+               reinterpret_cast<uintptr_t>(logits) % 4 == 0 &&
+               reinterpret_cast<uintptr_t>(next) % 4 == 0,
+           NC_ERR_INVALID_ARGUMENT, "tokens, positions, logits and next must be 4-byte aligned");
   NC_CHECK((flags & ~(NC_STEP_GRAPH | NC_STEP_ADVANCE | NC_STEP_STAGED)) == 0,
            NC_ERR_INVALID_ARGUMENT,
            "unknown flags 0x%x", flags);
@@ -509,6 +514,8 @@ nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t*
   NC_CHECK(batch >= 1 && batch <= m->max_batch, NC_ERR_CAPACITY, "batch %d outside [1, %d]",
            batch, m->max_batch);
   NC_CHECK(x && positions, NC_ERR_INVALID_ARGUMENT, "null device pointer");
+  NC_CHECK(reinterpret_cast<uintptr_t>(positions) % 4 == 0, NC_ERR_INVALID_ARGUMENT,
+           "positions must be 4-byte aligned");
   nc_status st = validate_kv(m, batch, positions_host, kv);
   if (st) return st;
   const KVView kvv = kv_view(m, *kv);
