@@ -243,3 +243,59 @@ def test_whole_model_matches_torch_library_composition(which, request):
     w2 = dict(w)
     w2["layers"] = [dict(lw, g_mlp=lw["g_attn"]) for lw in w["layers"]]
     assert _rel_l2(got, _torch_forward(m.shape, w2, toks.tolist())) > 1e-4
+
+
+def test_w8a8_model_matches_composition_with_the_numpy_quantiser(orc):
+    """The C oracle's W8A8 model against the architecture composed from torch
+    routines with every projection replaced by the numpy quantiser's W8A8
+    product (oracle/quant.py, written separately: per-row int8 weights,
+    per-token int8 activations, int32 sums, float(acc) * (s_w * s_x) + bias).
+    The two reach the quantised activations by different summation orders,
+    so a code can flip at a rounding boundary: the gate is 1e-2, while a
+    wiring mistake (a scale of the wrong row, the bias before the scale)
+    moves the logits by far more."""
+    from oracle import quant
+    F = torch.nn.functional
+    s = synth.TINY
+    w = synth.model_weights(s, seed=0)
+    m8 = orc.OracleModel(s, w, w8a8=True)
+    toks = synth.token_ids(6, s.vocab, stream=12)
+    got = m8.forward_full(toks, "f32")
+
+    def lin8(W, b, X, wrong_row=False):
+        wq, sw = quant.quantize_rows_i8(W.float().numpy())
+        if wrong_row:
+            sw = sw[::-1].copy()  # row j dequantised with row N-1-j's scale
+        bias = None if b is None else b.float().numpy()
+        out = [quant.linear_w8a8_blocked(wq, sw, bias, x, block=x.size)[0]
+               for x in X.numpy().astype(np.float32)]
+        return torch.tensor(np.stack(out), dtype=torch.float64)
+
+    def forward(wrong_row=False):
+        H, D, G, T = s.hidden, s.head_dim, s.group, len(toks)
+        x = w["embed"].double()[torch.as_tensor(toks.tolist(), dtype=torch.long)]
+        half = D // 2
+        inv = torch.tensor([1.0 / s.rope_theta ** (2 * i / D) for i in range(half)],
+                           dtype=torch.float64)
+        rot = torch.polar(torch.ones(T, half, dtype=torch.float64),
+                          torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :])
+        rope = lambda t: torch.cat([(z := torch.complex(t[..., :half], t[..., half:]) * rot).real,
+                                    z.imag], -1)
+        for lw in w["layers"]:
+            n = F.rms_norm(x, (H,), lw["g_attn"].double(), s.rms_eps)
+            q = lin8(lw["wq"], lw["bq"], n, wrong_row).view(T, -1, D).transpose(0, 1)
+            k = lin8(lw["wk"], lw["bk"], n, wrong_row).view(T, -1, D).transpose(0, 1)
+            v = lin8(lw["wv"], lw["bv"], n, wrong_row).view(T, -1, D).transpose(0, 1)
+            q, k = rope(q), rope(k)
+            a = F.scaled_dot_product_attention(q[None], k.repeat_interleave(G, 0)[None],
+                                               v.repeat_interleave(G, 0)[None], is_causal=True)[0]
+            x = x + lin8(lw["wo"], None, a.transpose(0, 1).reshape(T, -1), wrong_row)
+            n2 = F.rms_norm(x, (H,), lw["g_mlp"].double(), s.rms_eps)
+            x = x + lin8(lw["wd"], None, F.silu(lin8(lw["wg"], None, n2, wrong_row))
+                         * lin8(lw["wu"], None, n2, wrong_row), wrong_row)
+        e = w["embed"].double()
+        return F.linear(F.rms_norm(x, (H,), w["g_final"].double(), s.rms_eps), e).numpy()
+
+    err = _rel_l2(got, forward())
+    assert err < 1e-2, err
+    assert _rel_l2(got, forward(wrong_row=True)) > 10 * max(err, 1e-3)
