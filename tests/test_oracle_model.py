@@ -299,3 +299,21 @@ def test_w8a8_model_matches_composition_with_the_numpy_quantiser(orc):
     err = _rel_l2(got, forward())
     assert err < 1e-2, err
     assert _rel_l2(got, forward(wrong_row=True)) > 10 * max(err, 1e-3)
+
+
+def test_oracle_bits_do_not_depend_on_the_thread_count(orc, tiny, tiny_qk):
+    """The oracle parallelises only over independent output rows, each sum in
+    index order, so its output is bit-identical for 1, 2, 3 and 8 threads
+    (nanocompile's thread-count sweep)."""
+    before = orc.get_threads()
+    try:
+        for m, _ in (tiny, tiny_qk):
+            toks = synth.token_ids(7, m.shape.vocab, stream=13)
+            outs = []
+            for n in (1, 2, 3, 8):
+                orc.set_threads(n)
+                outs.append(m.forward_full(toks, "f32"))
+            for o in outs[1:]:
+                assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+    finally:
+        orc.set_threads(before)
