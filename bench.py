@@ -53,7 +53,8 @@ from transformer_decode_gb300 import nc, synth  # noqa: E402
 METRIC = "decode tokens/s at 1 GB300 and achieved HBM GB/s as fraction of ~8 TB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-WORKLOAD = "qwen2_0p5b_b1_greedy64"
+WORKLOAD = "qwen3_8b_shape_b1_past4096"  # the largest single-GPU configuration
+C1 = "qwen2_0p5b_b1_greedy64"            # the 0.5B model, 32-token prompt, 64 greedy
 
 
 # ---------------------------------------------------------------- helpers
@@ -190,24 +191,58 @@ def replica_rate(ws, batch, steps, local_seconds):
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_sample(shape, weights_cpu, prompt, seconds, max_steps):
-    """Time the CPU oracle decoding the workload's sequence (prompt steps, then
-    greedy) until `seconds` of work or `max_steps` steps. Returns
-    (steps, elapsed_s, threads)."""
+def c1_oracle(shape, prompt, n_gen):
+    """The oracle on the 0.5B prompt run: the model, and a cache that has
+    taken the prompt's first 31 tokens (positions 0..30) as decode steps."""
     import oracle
     oracle.build()
-    om = oracle.OracleModel(shape, weights_cpu)
-    kv = om.new_kv(1, len(prompt) + max_steps + 1)
-    tok = np.array([prompt[0]], np.int32)
+    om = oracle.OracleModel(shape, cpu_weights(shape))
+    kv = om.new_kv(1, len(prompt) + n_gen + 1)
+    for i in range(len(prompt) - 1):
+        om.decode_step(kv, np.array([prompt[i]], np.int32), np.array([i], np.int32))
+    return om, kv
+
+
+def cpu_baseline_c1(shape, prompt, cycle, seconds):
+    """The oracle as it stands on the host cores, on the positions the GPU
+    times (cycles of 65 steps at positions 31..95 after the untimed prompt):
+    all cores of the affinity mask until `seconds` of work; and one thread,
+    block 0 and the LM head product at position 31, scaled to a step."""
+    import oracle
+    n_prompt = len(prompt)
+    om, kv = c1_oracle(shape, prompt, cycle - 1)
+    threads = oracle.get_threads()
+    cur = prompt[-1]
     t0 = time.perf_counter()
     n = 0
-    while n < max_steps:
-        _, nxt = om.decode_step(kv, tok, np.array([n], np.int32))
+    while True:
+        if n % cycle == 0:
+            cur = prompt[-1]
+        p = n_prompt - 1 + (n % cycle)
+        _, nxt = om.decode_step(kv, np.array([cur], np.int32), np.array([p], np.int32))
+        cur = int(nxt[0])
         n += 1
-        tok = np.array([prompt[n]], np.int32) if n < len(prompt) else nxt.astype(np.int32)
         if time.perf_counter() - t0 >= seconds:
             break
-    return n, time.perf_counter() - t0, oracle.get_threads()
+    el = time.perf_counter() - t0
+    oracle.set_threads(1)
+    x = synth.normal_bf16(0, 9999, (shape.hidden,), 1.0).float().numpy()
+    t1 = time.perf_counter()
+    om.block_decode(0, kv, 0, n_prompt - 1, x)
+    t_block = time.perf_counter() - t1
+    t1 = time.perf_counter()
+    oracle.matvec_bf16(om.head_w, x)
+    t_head = time.perf_counter() - t1
+    oracle.set_threads(threads)
+    return {"value": n / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "cpu": cpu_model_name(),
+            "sample": f"{n} decode steps at the timed positions ({n_prompt - 1}..), "
+                      f"{el:.1f} s on {threads} threads of {cpu_threads()} host cores",
+            "one_thread": {"value": 1.0 / (shape.n_layers * t_block + t_head),
+                           "unit": "tokens/s", "cores": 1,
+                           "sample": f"block 0 ({t_block:.3f} s) and the LM head product "
+                                     f"({t_head:.3f} s) on one thread, scaled to "
+                                     f"{shape.n_layers} blocks + head"}}
 
 
 def cpu_threads():
@@ -222,39 +257,46 @@ REFERENCE_SECONDS = 150.0  # the reference arm's timed work stops here
 
 
 def run_reference(args, ws, rank):
-    """The CPU oracle on the bench workload: the 32-token prompt run untimed as
-    decode steps (positions 0..30), then timed decode steps cycling positions
-    31..95 as our arm does (every 65 steps the sequence restarts from the last
-    prompt token), at most args.steps of them and at most REFERENCE_SECONDS of
-    work, after a few untimed warm-up steps."""
+    """The CPU oracle on the bench workload, on the positions our arm times: a
+    few untimed warm-up steps, then timed decode steps of the workload's cycle,
+    at most args.steps of them and at most REFERENCE_SECONDS of work. For the
+    0.5B prompt run the prompt's first 31 tokens run untimed first and the
+    cycle is positions 31..95."""
     if rank != 0:
         return
-    shape = synth.QWEN2_0P5B
-    n_prompt, n_gen = 32, 64
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    wd = synth.model_weights(shape, device=dev)
-    wc = {k: (None if v is None else v.cpu()) for k, v in wd.items() if k != "layers"}
-    wc["layers"] = [{k: (None if v is None else v.cpu()) for k, v in lw.items()}
-                    for lw in wd["layers"]]
-    del wd
     import oracle
-    oracle.build()
-    om = oracle.OracleModel(shape, wc)
-    kv = om.new_kv(1, n_prompt + n_gen + 1)
-    prompt = synth.token_ids(n_prompt, shape.vocab).tolist()
-    for i in range(n_prompt - 1):
-        om.decode_step(kv, np.array([prompt[i]], np.int32), np.array([i], np.int32))
-    cycle = n_gen + 1
-    cur = prompt[-1]
+    name = args.workload
+    if name == SAMPLED:
+        name = C1
+    if name == C1:
+        shape = synth.QWEN2_0P5B
+        n_prompt, n_gen = 32, 64
+        prompt = synth.token_ids(n_prompt, shape.vocab).tolist()
+        om, kv = c1_oracle(shape, prompt, n_gen)
+        cycle = n_gen + 1
+        cur = prompt[-1]
 
-    def step(i):
-        nonlocal cur
-        if i % cycle == 0:
-            cur = prompt[-1]
-        p = n_prompt - 1 + (i % cycle)
-        _, nxt = om.decode_step(kv, np.array([cur], np.int32), np.array([p], np.int32))
-        cur = int(nxt[0])
+        def step(i):
+            nonlocal cur
+            if i % cycle == 0:
+                cur = prompt[-1]
+            p = n_prompt - 1 + (i % cycle)
+            _, nxt = om.decode_step(kv, np.array([cur], np.int32), np.array([p], np.int32))
+            cur = int(nxt[0])
+        batch = 1
+        config = {"workload": C1, "batch": 1, "prompt": n_prompt,
+                  "positions": f"cycles of {cycle} steps at positions {n_prompt - 1}.."
+                               f"{n_prompt + n_gen - 1}"}
+    else:
+        cfg = WORKLOADS[name]
+        batch = cfg["batch"]
+        om, okv, past = oracle_for(cfg, max(workload_past(cfg)) + cfg["gen"] + 1)
 
+        def step(i):
+            oracle_workload_steps(om, okv, cfg, past, i, 0.0, 1)
+        config = {"workload": name, "batch": batch, "past": cfg["past"],
+                  "positions": f"cycles of {cfg['gen']} greedy steps from the past length(s)"}
+    config["note"] = "CPU oracle (plain C, fp32, OpenMP over output rows)"
     warm = min(args.warmup, 3)
     for i in range(warm):
         step(i)
@@ -267,20 +309,17 @@ def run_reference(args, ws, rank):
             break
     el = time.perf_counter() - t0
     thr = oracle.get_threads()
-    value = n / el
+    value = batch * n / el
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": ws, "steps": n, "steps_requested": args.steps, "warmup": warm,
         "ms_per_step": el / n * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": 1, "prompt": n_prompt,
-                   "positions": f"cycles of {cycle} steps at positions {n_prompt - 1}.."
-                                f"{n_prompt + n_gen - 1}",
-                   "note": "CPU oracle (plain C, fp32, OpenMP over output rows)"},
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                         "cpu": cpu_model_name(),
                          "sample": f"{n} timed decode steps of the workload (of "
                                    f"{args.steps} requested; at most {REFERENCE_SECONDS:.0f} s), "
-                                   f"{el:.1f} s on {cpu_threads()} host cores"},
+                                   f"{el:.1f} s on {thr} threads of {cpu_threads()} host cores"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -288,18 +327,18 @@ def run_reference(args, ws, rank):
 
 # ---------------------------------------------------------------- our arm
 PERSISTENT_SRC = os.path.join(ROOT, "transformer_decode_gb300", "csrc", "persistent.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_decode_persistent_qwen2_0p5b_b1_dram.md")
 
 
-def counted_traffic():
+def counted_traffic(name):
     """DRAM bytes per launch of the step kernel from the committed ncu summary
-    (dram__bytes_read.sum + dram__bytes_write.sum of one capture of this
-    workload), or None when there is none or the kernel source changed since
+    of workload `name` (dram__bytes_read.sum + dram__bytes_write.sum of one
+    capture), or None when there is none or the kernel source changed since
     (the summary records the source's sha256)."""
-    if not os.path.exists(TRAFFIC_FILE):
+    path = TRAFFIC_FILES.get(name)
+    if not path or not os.path.exists(path):
         return None
     fields = {}
-    for line in open(TRAFFIC_FILE):
+    for line in open(path):
         if ":" in line and line.strip().startswith(("source_sha256", "dram_bytes_per_launch")):
             k, v = line.strip().split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
@@ -333,10 +372,11 @@ def run_nc(args, ws, rank, local):
     # (set from the host, 8 bytes) then 64 greedy tokens fed back on the device.
     cycle = n_gen + 1
 
-    def run_steps(k):
-        """k decode steps of repeated cycles; returns the positions used."""
+    def run_steps(k, off=0):
+        """k decode steps of repeated cycles, from cycle step off; returns the
+        positions used."""
         used = []
-        for i in range(k):
+        for i in range(off, off + k):
             p = n_prompt - 1 + (i % cycle)
             if i % cycle == 0:
                 tok.copy_(reset_host[:1], non_blocking=True)
@@ -347,26 +387,24 @@ def run_nc(args, ws, rank, local):
 
     run_steps(args.warmup)
     torch.cuda.synchronize()
+    if args.phase_profile:
+        print_phase_profile(model, shape, run_steps, model.decode_path(B, kv))
 
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
         time.sleep(0.3)
     st = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
     w0 = time.time()
-    e0.record(st)
-    used = run_steps(args.steps)
-    e1.record(st)
-    torch.cuda.synchronize()
+    total_s, per_round, used = timed_rounds(st, run_steps, args.steps)
     w1 = time.time()
     barrier(ws)
     if rank == 0:
         time.sleep(0.2)
         sampler.stop()
-    value, el = replica_rate(ws, B, args.steps, e0.elapsed_time(e1) / 1e3)
+    value, el = replica_rate(ws, B, args.steps, total_s)
     restarts = sum(1 for i in range(args.steps) if i % cycle == 0)
     ms = el / args.steps * 1e3
     bytes_avg = sum(step_bytes(shape, B, [p]) for p in used) / len(used)
@@ -414,13 +452,7 @@ def run_nc(args, ws, rank, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        wc = {k: (None if v is None else v.cpu()) for k, v in wd.items() if k != "layers"}
-        wc["layers"] = [{k: (None if v is None else v.cpu()) for k, v in lw.items()}
-                        for lw in wd["layers"]]
-        n, sec, thr = oracle_sample(shape, wc, prompt, seconds=args.cpu_seconds, max_steps=96)
-        cpu = {"value": n / sec, "unit": "tokens/s", "cores": thr, "kind": "oracle",
-               "sample": f"{n} decode steps of the workload from position 0 (prompt steps "
-                         f"first), {sec:.1f} s on {cpu_threads()} host cores"}
+        cpu = cpu_baseline_c1(shape, prompt, cycle, args.cpu_seconds)
 
     if rank == 0:
         line = {
@@ -428,7 +460,7 @@ def run_nc(args, ws, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": B, "prompt": n_prompt,
+            "config": {"workload": C1, "batch": B, "prompt": n_prompt,
                        "positions": f"cycles of {cycle} steps at positions {n_prompt - 1}.."
                                     f"{n_prompt + n_gen - 1} ({restarts} cycles timed)",
                        "weights": "bf16 seeded N(0,0.02) stand-in, fp32 accumulate",
@@ -437,6 +469,7 @@ def run_nc(args, ws, rank, local):
                                 if path == "persistent" else "nc_decode_step: stage kernels, CUDA graph"),
                        "l2": "inputs larger than L2: 988 MB of weights stream every step",
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "rounds": rounds_summary(per_round),
             "hbm": {"bytes_per_step": bytes_avg, "gbs": hbm_gbs,
                     "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
                     "frac_of_measured_copy": hbm_gbs / peak, "peak_kind": peak_kind},
@@ -445,7 +478,7 @@ def run_nc(args, ws, rank, local):
                                     if path == "persistent" else "stage kernels (whole step)"),
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak,
-                         "traffic": counted_traffic() if path == "persistent" else None,
+                         "traffic": counted_traffic(C1) if path == "persistent" else None,
                          "peak_kind": peak_kind, "avg_launch_us": dur * 1e6,
                          "algorithmic_bytes_per_launch": bytes_avg},
             "cpu_baseline": cpu,
@@ -593,18 +626,32 @@ def run_sampled(args, ws, rank, local):
     model.close()
 
 
-# Other measured configurations (not the metric's workload): name -> setup.
+# Measured configurations other than the 0.5B prompt run: name -> setup.
 # Past K/V are the seeded synthetic rows the tests use; each timed cycle runs
 # `gen` greedy steps from the past lengths, then the host resets tokens and
-# positions (B x 8 bytes).
+# positions (B x 8 bytes). The first is the metric's workload: the largest
+# single-GPU configuration, the 8B shape at 4096 past positions.
 WORKLOADS = {
+    "qwen3_8b_shape_b1_past4096": dict(shape="QWEN3_8B", batch=1, paged=False, past=4096,
+                                       gen=64, w8a8=False),
     "qwen2_0p5b_b16_paged_past256-4096": dict(shape="QWEN2_0P5B", batch=16, paged=True,
                                               past="uniform 256..4096", gen=32, w8a8=False),
     "qwen2_0p5b_w8a8_b1_past512": dict(shape="QWEN2_0P5B", batch=1, paged=False, past=512,
                                        gen=64, w8a8=True),
-    "qwen3_8b_shape_b1_past4096": dict(shape="QWEN3_8B", batch=1, paged=False, past=4096,
-                                       gen=64, w8a8=False),
 }
+ROUNDS = 5  # the timed region is reported as this many equal rounds as well
+
+# ncu DRAM summaries of the step kernel (one capture each), by workload
+TRAFFIC_FILES = {
+    WORKLOAD: os.path.join(ROOT, "profiles", "k_decode_persistent_qwen3_8b_shape_b1_past4096_dram.md"),
+    C1: os.path.join(ROOT, "profiles", "k_decode_persistent_qwen2_0p5b_b1_dram.md"),
+}
+
+
+def workload_past(cfg):
+    B = cfg["batch"]
+    return (synth.past_lengths(B, 256, 4096).tolist() if isinstance(cfg["past"], str)
+            else [cfg["past"]] * B)
 
 
 def fill_past(kv, shape, past):
@@ -627,17 +674,147 @@ def fill_past(kv, shape, past):
                     kv.v[l, blk, g, t % kv.block_size] = vr.to(kv.v.dtype).view(p, D)
 
 
+def cpu_weights(shape):
+    """The seeded weights as CPU tensors, drawn on the GPU when there is one
+    (the generator gives the same bits on either device; drawing 8B-shaped
+    weights on the host takes many minutes)."""
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wd = synth.model_weights(shape, device=dev)
+    wc = {k: (None if v is None else v.cpu()) for k, v in wd.items() if k != "layers"}
+    wc["layers"] = [{k: (None if v is None else v.cpu()) for k, v in lw.items()}
+                    for lw in wd["layers"]]
+    del wd
+    return wc
+
+
+def oracle_for(cfg, max_ctx):
+    """The CPU oracle on the workload: its model and a logical cache holding
+    the same synthetic past rows as the GPU cache."""
+    import oracle
+    oracle.build()
+    shape = getattr(synth, cfg["shape"])
+    past = workload_past(cfg)
+    om = oracle.OracleModel(shape, cpu_weights(shape), w8a8=cfg["w8a8"])
+    okv = om.new_kv(cfg["batch"], max_ctx)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    for l in range(shape.n_layers):
+        for b, p in enumerate(past):
+            if p == 0:
+                continue
+            for g in range(shape.n_kv_heads):
+                kr = synth.synthetic_kv_rows(shape, l, b, g, 0, p, device=dev)
+                vr = synth.synthetic_kv_rows(shape, l, b, g, 1, p, device=dev)
+                okv.k[l, b, g, :p] = kr.float().cpu().numpy().reshape(p, -1)
+                okv.v[l, b, g, :p] = vr.float().cpu().numpy().reshape(p, -1)
+    return om, okv, past
+
+
+def cpu_model_name():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_workload_steps(om, okv, cfg, past, start, seconds, max_steps):
+    """Decode steps of the workload's cycle (greedy, `gen` steps from the past
+    lengths) on the oracle, from cycle step `start`, until `seconds` of work
+    or `max_steps` steps. Returns (steps, elapsed_s)."""
+    B, gen = cfg["batch"], cfg["gen"]
+    shape = om.shape
+    past_np = np.array(past, np.int32)
+    tok = synth.token_ids(B, shape.vocab, stream=77).numpy().astype(np.int32)
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_steps:
+        j = (start + n) % gen
+        if j == 0:
+            tok = synth.token_ids(B, shape.vocab, stream=77).numpy().astype(np.int32)
+        _, nxt = om.decode_step(okv, tok, past_np + j)
+        tok = nxt.astype(np.int32)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return n, time.perf_counter() - t0
+
+
+def cpu_baseline_for(cfg, seconds):
+    """The oracle as it stands on the GPU machine's host cores, on the workload's
+    own positions: (a) all cores of the affinity mask, whole decode steps of
+    the cycle until `seconds` of work; (b) one thread, one block and the LM
+    head at the cycle's first position, scaled to a step (L blocks + head)."""
+    import oracle
+    om, okv, past = oracle_for(cfg, max(workload_past(cfg)) + cfg["gen"] + 1)
+    shape = om.shape
+    B = cfg["batch"]
+    threads = oracle.get_threads()
+    n, el = oracle_workload_steps(om, okv, cfg, past, 0, seconds, 10 ** 6)
+    all_rate = B * n / el
+    # one thread: block 0 of every sequence plus the head product, scaled
+    oracle.set_threads(1)
+    x = synth.normal_bf16(0, 9999, (shape.hidden,), 1.0).float().numpy()
+    t0 = time.perf_counter()
+    for b in range(B):
+        om.block_decode(0, okv, b, past[b], x)
+    t_block = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    for b in range(B):
+        oracle.matvec_bf16(om.head_w, x)
+    t_head = time.perf_counter() - t0
+    oracle.set_threads(threads)
+    one_rate = B / (shape.n_layers * t_block + t_head)
+    return {
+        "value": all_rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "cpu": cpu_model_name(),
+        "sample": f"{n} decode steps of the workload's cycle (batch {B}, from past "
+                  f"{'..'.join(str(p) for p in sorted(set([min(past), max(past)])))}), "
+                  f"{el:.1f} s on {threads} threads of {cpu_threads()} host cores",
+        "one_thread": {"value": one_rate, "unit": "tokens/s", "cores": 1,
+                       "sample": f"block 0 ({t_block:.2f} s) and the LM head product "
+                                 f"({t_head:.2f} s) for {B} sequence(s) on one thread, "
+                                 f"scaled to {shape.n_layers} blocks + head"},
+    }
+
+
+def timed_rounds(st, run_steps, steps, rounds=ROUNDS):
+    """Run `steps` steps as `rounds` equal rounds inside one timed region, with
+    CUDA events on stream st at every round boundary. Returns (total_s,
+    [per-round ms per step], positions used)."""
+    cuts = [round(steps * r / rounds) for r in range(rounds + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(rounds + 1)]
+    used = []
+    ev[0].record(st)
+    for r in range(rounds):
+        used += run_steps(cuts[r + 1] - cuts[r], cuts[r])
+        ev[r + 1].record(st)
+    torch.cuda.synchronize()
+    per = [ev[r].elapsed_time(ev[r + 1]) / max(1, cuts[r + 1] - cuts[r])
+           for r in range(rounds) if cuts[r + 1] > cuts[r]]
+    return ev[0].elapsed_time(ev[rounds]) / 1e3, per, used
+
+
+def rounds_summary(per):
+    med = statistics.median(per)
+    return {"n": len(per), "ms_per_step": [round(v, 5) for v in per], "median_ms": med,
+            "min_ms": min(per), "max_ms": max(per),
+            "spread": (max(per) - min(per)) / med if med > 0 else None}
+
+
 def run_workload(args, ws, rank, local, name):
     cfg = WORKLOADS[name]
     torch.cuda.set_device(local)
     shape = getattr(synth, cfg["shape"])
     B, gen = cfg["batch"], cfg["gen"]
-    past = (synth.past_lengths(B, 256, 4096).tolist() if isinstance(cfg["past"], str)
-            else [cfg["past"]] * B)
+    past = workload_past(cfg)
     wd = synth.model_weights(shape, device="cuda")
     max_ctx = max(past) + gen + 16
     model = nc.Model(shape, wd, max_batch=B, max_ctx=max_ctx, w8a8=cfg["w8a8"])
     del wd
+    torch.cuda.empty_cache()
     if cfg["paged"]:
         table, nblk = synth.block_tables(past, gen + 1, 16)
         kv = nc.KVCache(shape, B, paged=True, block_table=table, num_blocks=nblk)
@@ -651,9 +828,9 @@ def run_workload(args, ws, rank, local, name):
     reset_host = torch.stack([start, torch.tensor(past, dtype=torch.int32)]).pin_memory()
     past_np = np.array(past, np.int32)
 
-    def run_steps(k):
+    def run_steps(k, off=0):
         used = []
-        for i in range(k):
+        for i in range(off, off + k):
             j = i % gen
             if j == 0:
                 tok.copy_(reset_host[0], non_blocking=True)
@@ -664,25 +841,24 @@ def run_workload(args, ws, rank, local, name):
 
     run_steps(args.warmup)
     torch.cuda.synchronize()
+    path = model.decode_path(B, kv)
+    if args.phase_profile:
+        print_phase_profile(model, shape, run_steps, path)
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
         time.sleep(0.3)
     st = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
     w0 = time.time()
-    e0.record(st)
-    used = run_steps(args.steps)
-    e1.record(st)
-    torch.cuda.synchronize()
+    total_s, per_round, used = timed_rounds(st, run_steps, args.steps)
     w1 = time.time()
     barrier(ws)
     if rank == 0:
         time.sleep(0.2)
         sampler.stop()
-    value, el = replica_rate(ws, B, args.steps, e0.elapsed_time(e1) / 1e3)
+    value, el = replica_rate(ws, B, args.steps, total_s)
     dur = el / args.steps
     bytes_avg = sum(step_bytes(shape, B, u.tolist(), w8a8=cfg["w8a8"]) for u in used) / len(used)
     peak, peak_kind = peaks()
@@ -716,9 +892,23 @@ def run_workload(args, ws, rank, local, name):
         st.synchronize()
         cur = nxt_h.clone()
     e2e_value, t_e2e = replica_rate(ws, B, k_e2e, time.perf_counter() - t0)
-    path = model.decode_path(B, kv)
     launches_per_step = 1 if path == "persistent" else 2 + 5 * shape.n_layers
+    model.close()
+    del kv
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_for(cfg, args.cpu_seconds)
+
     if rank == 0:
+        if path == "persistent":
+            kernel = f"k_decode_persistent<{1 if B == 1 else (2 if B == 2 else 4)}," \
+                     f"{shape.head_dim},fp32 KV> (the whole step, one launch)"
+            traffic = counted_traffic(name)
+        else:
+            kernel = "stage kernels (whole step, one CUDA graph)"
+            traffic = None
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dur * 1e3,
@@ -726,28 +916,76 @@ def run_workload(args, ws, rank, local, name):
             "dtype": "i8/i32" if cfg["w8a8"] else "f32", "data": "synthetic",
             "config": {"workload": name, "batch": B, "past": cfg["past"], "greedy_steps": gen,
                        "weights": ("int8 per-row scales (W8A8)" if cfg["w8a8"] else "bf16") +
-                                  " from seeded N(0,0.02)",
+                                  " from seeded N(0,0.02), fp32 accumulate",
                        "kv": ("paged (block 16, shuffled tables)" if cfg["paged"] else "contiguous")
                              + " fp32",
+                       "positions": f"cycles of {gen} greedy steps from the past length(s)",
                        "path": ("nc_decode_step: one persistent cooperative launch per step"
                                 if path == "persistent" else "nc_decode_step: stage kernels, CUDA graph"),
                        "l2": "inputs larger than L2: the weights stream every step",
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "rounds": rounds_summary(per_round),
             "hbm": {"bytes_per_step": bytes_avg, "gbs": bytes_avg / dur / 1e9,
                     "frac_of_8tbs": bytes_avg / dur / 1e9 / NOMINAL_HBM_GBS,
                     "frac_of_measured_copy": bytes_avg / dur / 1e9 / peak, "peak_kind": peak_kind},
-            "roofline": {"bound": "hbm", "kernel": "the whole step (" + path + " path)",
+            "roofline": {"bound": "hbm", "kernel": kernel,
                          "achieved": bytes_avg / dur / 1e9, "peak": peak, "unit": "GB/s",
-                         "frac": bytes_avg / dur / 1e9 / peak, "traffic": None,
-                         "peak_kind": peak_kind, "avg_step_us": dur * 1e6,
-                         "algorithmic_bytes_per_step": bytes_avg},
-            "cpu_baseline": None,
+                         "frac": bytes_avg / dur / 1e9 / peak, "traffic": traffic,
+                         "peak_kind": peak_kind, "avg_launch_us": dur * 1e6 / launches_per_step,
+                         "avg_step_us": dur * 1e6,
+                         "algorithmic_bytes_per_launch": bytes_avg / launches_per_step},
+            "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": k_e2e,
                     "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
             "gpu_launches": args.steps * launches_per_step,
             "clocks": sampler.summary(w0, w1),
         }), flush=True)
-    model.close()
+
+
+def print_phase_profile(model, shape, run_steps, path):
+    """Critical-path timeline of the persistent kernel (nc_profile_phases) over
+    a few steps, printed to stderr. For phase p: `handover` = the last CTA's
+    input arrival minus the moment the last CTA finished phase p - 1 (the
+    hand-over latency on the chain), `work` = the moment the last CTA finished
+    phase p minus that input arrival. Medians over layers and steps; the two
+    columns summed over all phases give the step."""
+    if path != "persistent":
+        print("phase profile: the stage path has no phase record", file=sys.stderr)
+        return
+    L = shape.n_layers
+    nph = 5 * L + 1
+    names = ["qkv", "attention", "o-proj", "gate|up", "down", "lm-head"]
+    hand = {n: [] for n in names}
+    work = {n: [] for n in names}
+    totals = []
+    model.profile_phases(True)
+    for it in range(4):
+        run_steps(1, it)
+        rec = model.read_phase_profile()
+        start = rec["start"].numpy().astype(np.int64)
+        inp = rec["input"].numpy().astype(np.int64)
+        c0 = rec["cta_start"].numpy().astype(np.int64)
+        c1 = rec["cta_end"].numpy().astype(np.int64)
+        t0 = int(c0.min())
+        totals.append((int(c1.max()) - t0) / 1e3)
+        for p in range(nph):
+            kind = names[5] if p == nph - 1 else names[p % 5]
+            ok = inp[:, p] >= start[:, p]  # CTAs that ran the phase this step
+            if not ok.any():
+                continue
+            fin_prev = start[:, p].max()
+            last_in = inp[ok, p].max()
+            fin = start[:, p + 1].max() if p + 1 < nph else c1.max()
+            hand[kind].append((last_in - fin_prev) / 1e3)
+            work[kind].append((fin - last_in) / 1e3)
+    model.profile_phases(False)
+    print(f"phase profile ({len(totals)} steps, median step {statistics.median(totals):.1f} us):",
+          file=sys.stderr)
+    print(f"{'phase':10s} {'handover us':>12s} {'work us':>9s}", file=sys.stderr)
+    for k in names:
+        if hand[k]:
+            print(f"{k:10s} {statistics.median(hand[k]):12.2f} {statistics.median(work[k]):9.2f}",
+                  file=sys.stderr)
 
 
 def main():
@@ -759,7 +997,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[WORKLOAD, SAMPLED] + list(WORKLOADS))
+                    choices=[C1, SAMPLED] + list(WORKLOADS))
+    ap.add_argument("--phase-profile", action="store_true",
+                    help="print the persistent kernel's per-phase critical path (stderr)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     ws, rank, local = dist_init()
@@ -767,10 +1007,10 @@ def main():
         run_reference(args, ws, rank)
     elif args.workload == SAMPLED:
         run_sampled(args, ws, rank, local)
-    elif args.workload != WORKLOAD:
-        run_workload(args, ws, rank, local, args.workload)
-    else:
+    elif args.workload == C1:
         run_nc(args, ws, rank, local)
+    else:
+        run_workload(args, ws, rank, local, args.workload)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

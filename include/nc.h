@@ -144,9 +144,9 @@ nc_status nc_model_memory(const nc_model* m, size_t* weight_bytes, size_t* works
                              (the caller then passes positions_host + 1) */
 #define NC_STEP_STAGED 4  /* use the per-stage kernels even where the persistent
                              decode kernel applies. By default a step with bf16
-                             weights, batch <= 4 and a cache of at most 2048
-                             positions per sequence runs as one persistent,
-                             cooperative kernel (one launch, no graph); other
+                             weights and batch <= 4 runs as one persistent,
+                             cooperative kernel (one launch, no graph; any cache
+                             length: long scans are split over the grid); other
                              steps run the per-stage kernels. */
 
 /* One decode step for `batch` sequences (nanoinfer "Model architecture" and
@@ -174,8 +174,8 @@ nc_status nc_get_device_status(nc_model* m, void* stream, int* code);
 
 /* Which implementation nc_decode_step runs for these arguments (nothing is
  * launched): NC_PATH_PERSISTENT, the whole step as one cooperative
- * persistent kernel (bf16 weights, batch <= 4, cache capacity <= 2048, shape
- * within its shared-memory plan, NC_STEP_STAGED not set), else
+ * persistent kernel (bf16 weights, batch <= 4, shape within its
+ * shared-memory plan, NC_STEP_STAGED not set), else
  * NC_PATH_STAGED, the per-stage kernels (2 + 5 per layer launches, in a CUDA
  * graph with NC_STEP_GRAPH). */
 typedef enum { NC_PATH_STAGED = 0, NC_PATH_PERSISTENT = 1 } nc_path;
@@ -247,20 +247,35 @@ nc_status nc_attn_decode(const nc_model* m, int layer, int B, const float* q,
  * split partials live in a static device array of 1,048,576 floats (4 MiB)
  * that every GPU loading libnc holds until the process exits, beside 1,024
  * static merge counters (zero at load; each call returns the ones it used to
- * zero). A request whose partials, batch * n_q_heads * splits * (head_dim + 2)
- * floats, exceed the array, or whose batch * n_kv_heads exceeds the counters,
- * returns NC_ERR_CAPACITY before anything is enqueued. The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress, with that
- * device current); make that first call before any stream capture. All calls
- * share the array: calls that overlap on the GPU (on different streams, or
- * from different threads) race and must be serialised by the caller. Every
- * scratch element a call reads is written earlier in the same call, so what
- * the previous call left there does not matter. n_layers is the cache's
- * layer count (bounds `layer`); other arguments as for nc_attn_decode. */
+ * zero) and one static status word. A request whose partials,
+ * n_q_heads * splits * (head_dim + 2) floats with splits >= B (the splits of
+ * one kv head are shared out among the sequences), exceed the array, or
+ * whose B * n_kv_heads exceeds the counters, returns NC_ERR_CAPACITY before
+ * anything is enqueued. The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current); make that
+ * first call before any stream capture. Later calls whose stream is not
+ * capturing look the address up again (a context re-created after a device
+ * reset is then picked up); a capturing call reuses the last lookup. All
+ * calls share the array: calls that overlap on the GPU (on different
+ * streams, or from different threads) race and must be serialised by the
+ * caller. Every scratch element a call reads is written earlier in the same
+ * call, so what the previous call left there does not matter. Errors the
+ * kernel detects on the device (an expired bounded wait: NC_ERR_TIMEOUT; a
+ * block-table entry or position the device copy disagrees on:
+ * NC_ERR_POSITION) leave `out` undefined for the affected heads and are
+ * recorded in the static status word; nc_attn_decode_static_status reads it.
+ * n_layers is the cache's layer count (bounds `layer`); other arguments as
+ * for nc_attn_decode. */
 nc_status nc_attn_decode_static(int n_q_heads, int n_kv_heads, int head_dim, int n_layers,
                                 int layer, int B, const float* q, const int32_t* positions_dev,
                                 const int32_t* positions_host, const nc_kv_cache* kv, float* out,
                                 void* stream);
+
+/* Synchronises `stream`, then reads the static status word of
+ * nc_attn_decode_static into *code (0 = no device-side error since the last
+ * read, else the first nc_status a kernel recorded) and clears it. Copies
+ * between the word and host memory only; allocates nothing. */
+nc_status nc_attn_decode_static_status(void* stream, int* code);
 
 /* logits[b, v] = sum_k W[v, k] * xn[b, k] with xn = rmsnorm(x[b]) * gamma,
  * and next[b] = argmax_v logits[b, v], lowest index on ties, -1 on NaN

@@ -382,6 +382,7 @@ class OracleModel:
         gf = _np(weights["g_final"], np.uint16)
         self._keep += [emb, head, gf, layers]
         self.layers = layers
+        self.head_w = emb if head is None else head  # the LM head's bf16 rows
         q8e = se = None
         if int8_embed:
             q8e, se = quantize_weight(emb)

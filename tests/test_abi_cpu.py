@@ -169,6 +169,8 @@ def test_static_attention_validates_cache_and_positions_on_the_host(lib):
     assert call(B=16, pos=[0] * 16, Hq=128, Hkv=128,
                 cache=kv(batch_capacity=16)) == E["NC_ERR_CAPACITY"]
     assert b"tickets" in lib.nc_last_error_message()
+    # the status reader refuses a null destination before touching the device
+    assert lib.nc_attn_decode_static_status(None, None) == E["NC_ERR_INVALID_ARGUMENT"]
 
 
 def test_entry_points_reject_misaligned_pointers(lib):

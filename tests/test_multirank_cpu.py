@@ -58,27 +58,34 @@ WRAPPER = """
 import sys
 sys.path.insert(0, {root!r})
 from transformer_decode_gb300 import synth
-synth.QWEN2_0P5B = synth.TINY  # the launch logic under test, on a model the CPU makes fast
+# the launch logic under test, on models the CPU makes fast
+synth.QWEN2_0P5B = synth.TINY
+synth.QWEN3_8B = synth.TINY_QKNORM
 import bench
 bench.main()
 """
 
 
-def test_reference_arm_under_torchrun_prints_one_line(tmp_path):
+@pytest.mark.parametrize("workload", [None, "qwen2_0p5b_b1_greedy64"])
+def test_reference_arm_under_torchrun_prints_one_line(tmp_path, workload):
     """--impl reference at N = 2 under torchrun: rank 0 times the oracle and
-    prints one JSON line; rank 1 exits 0 without work."""
+    prints one JSON line; rank 1 exits 0 without work. The default workload
+    (the 8B shape at 4096 past positions) and the 0.5B prompt run."""
     script = tmp_path / "bench_tiny.py"
     script.write_text(WRAPPER.format(root=ROOT))
     env = dict(os.environ, OMP_NUM_THREADS="2")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
            str(script), "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    if workload:
+        cmd += ["--workload", workload]
     r = subprocess.run(cmd, capture_output=True, text=True, cwd=ROOT, env=env, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["config"]["workload"] == (workload or "qwen3_8b_shape_b1_past4096")
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
 

@@ -15,8 +15,14 @@
 // exits. In host code its name is only a host-side stand-in, not a device
 // address: passing it to a kernel would fault, or on a GPU that can reach
 // host memory, silently use the wrong memory. The device address is taken
-// once per device with cudaGetSymbolAddress, with that device current, on
-// the first call made on it.
+// with cudaGetSymbolAddress, with that device current: on the first call made
+// on a device, and again on every call whose stream is not capturing (so a
+// context created anew after a device reset is picked up); a capturing call
+// uses the address looked up last.
+//
+// Errors the kernel finds on the device (an expired bounded wait, a block
+// table entry or position that disagrees with the host copy) go to the static
+// word g_attn_status, read and cleared by nc_attn_decode_static_status.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -32,31 +38,44 @@ static __device__ __align__(256) float g_attn_scratch[kStaticAttnScratchFloats];
 // every ticket it used at zero again.
 constexpr int kStaticAttnTickets = 1024;
 static __device__ unsigned int g_attn_tickets[kStaticAttnTickets];
+// Device-side error word of the calls (0 = none; else the first nc_status a
+// kernel recorded since it was last read).
+static __device__ int g_attn_status;
 
 constexpr int kMaxDevices = 64;
 static float* g_scratch_ptr[kMaxDevices];
 static unsigned int* g_ticket_ptr[kMaxDevices];
+static int* g_status_ptr[kMaxDevices];
 static std::mutex g_scratch_mutex;
 
-// Device addresses of g_attn_scratch and g_attn_tickets on the current
-// device (looked up once).
-static cudaError_t static_scratch(float** out, unsigned int** tickets) {
+// Device addresses of g_attn_scratch, g_attn_tickets and g_attn_status on the
+// current device: looked up on the first call on the device and on every
+// call whose stream is not capturing; while capturing, the last lookup.
+static cudaError_t static_scratch(cudaStream_t s, float** out, unsigned int** tickets,
+                                  int** status) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const bool capturing = cudaStreamIsCapturing(s, &cs) != cudaSuccess ||
+                         cs != cudaStreamCaptureStatusNone;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || !capturing) {
     void* p = nullptr;
     void* t = nullptr;
+    void* w = nullptr;
     e = cudaGetSymbolAddress(&p, g_attn_scratch);
     if (e == cudaSuccess) e = cudaGetSymbolAddress(&t, g_attn_tickets);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&w, g_attn_status);
     if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = static_cast<float*>(p);
     g_ticket_ptr[dev] = static_cast<unsigned int*>(t);
+    g_status_ptr[dev] = static_cast<int*>(w);
   }
   *out = g_scratch_ptr[dev];
   *tickets = g_ticket_ptr[dev];
+  *status = g_status_ptr[dev];
   return cudaSuccess;
 }
 
@@ -114,7 +133,8 @@ extern "C" nc_status nc_attn_decode_static(int n_q_heads, int n_kv_heads, int he
 
   float* scratch = nullptr;
   unsigned int* tickets = nullptr;
-  cudaError_t e = static_scratch(&scratch, &tickets);
+  int* status = nullptr;
+  cudaError_t e = static_scratch(static_cast<cudaStream_t>(stream), &scratch, &tickets, &status);
   if (e != cudaSuccess)
     return fail(NC_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed: %s",
                 cudaGetErrorString(e));
@@ -132,9 +152,24 @@ extern "C" nc_status nc_attn_decode_static(int n_q_heads, int n_kv_heads, int he
   v.n_kv_heads = n_kv_heads;
   v.head_dim = head_dim;
   AttnArgs a{q, positions_dev, B, n_q_heads, n_kv_heads, head_dim, layer, splits, scratch, out, v,
-             nullptr, tickets};
+             status, tickets};
   e = launch_attn(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(NC_ERR_CUDA, "nc_attn_decode_static: %s", cudaGetErrorString(e));
+  return NC_OK;
+}
+
+extern "C" nc_status nc_attn_decode_static_status(void* stream, int* code) {
+  NC_CHECK(code, NC_ERR_INVALID_ARGUMENT, "code is NULL");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  const int zero = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&word, g_attn_status, sizeof(int));
+  if (e == cudaSuccess && word != 0) e = cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int));
+  if (e != cudaSuccess)
+    return fail(NC_ERR_CUDA, "reading the static attention status failed: %s",
+                cudaGetErrorString(e));
+  *code = word;
   return NC_OK;
 }

@@ -48,7 +48,7 @@ struct Arena {
 };
 
 Model::~Model() {
-  for (auto& kv : graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : graphs) cudaGraphExecDestroy(kv.second.exec);
   if (cap_stream) cudaStreamDestroy(cap_stream);
   if (status_host) cudaFreeHost(status_host);
   if (weights) cudaFree(weights);
@@ -168,8 +168,9 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     const size_t pb = max_batch < kPMaxBatch ? max_batch : kPMaxBatch;
     m->xw = W.take<uint64_t>(pb * H);
     m->qkvw = W.take<uint64_t>(pb * nqkv);
-    m->aw = W.take<uint64_t>(pb * kPMaxSplits * qd);
-    m->mlw = W.take<uint64_t>(pb * kPMaxSplits * c.n_q_heads * 2);
+    m->aw = W.take<uint64_t>(pb * qd);
+    m->apart = W.take<float>((size_t)kPMaxBatch * kPMaxSplits * c.n_q_heads * (D + 2));
+    m->atick = W.take<unsigned int>((size_t)c.n_layers * kPMaxBatch * Hkv);
     m->hw = W.take<uint64_t>(pb * F);
     m->pticket = W.take<unsigned int>(1);
     m->seq = W.take<unsigned int>(1);
@@ -264,12 +265,12 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
   return NC_OK;
 }
 
-// The persistent kernel serves bf16 weights, small batches and caches short
-// enough for one CTA per (sequence, kv head) to scan.
+// The persistent kernel serves bf16 weights and small batches, at any cache
+// length (long scans are split over the grid).
 bool use_persistent(const Model* m, int batch, const nc_kv_cache& kv, int flags) {
   const nc_config& c = m->cfg;
+  (void)kv;
   return !(flags & NC_STEP_STAGED) && c.wtype == NC_BF16 && batch <= kPMaxBatch &&
-         kv_capacity(kv) <= kPMaxCtx &&
          persistent_supported(c.n_layers, c.hidden, c.n_q_heads * c.head_dim, c.ffn, c.head_dim,
                               c.n_q_heads / c.n_kv_heads, batch);
 }
@@ -303,7 +304,8 @@ static cudaError_t enqueue_persistent(Model* m, int batch, int32_t* tokens, int3
   a.xw = m->xw;
   a.qkvw = m->qkvw;
   a.aw = m->aw;
-  a.mlw = m->mlw;
+  a.apart = m->apart;
+  a.atick = m->atick;
   a.hw = m->hw;
   a.am_part = m->am_part;
   a.ticket = m->pticket;
@@ -467,6 +469,20 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
                  kv->max_blocks_per_seq, (int)io.advance, (int)kv->dtype};
     auto it = m->graphs.find(key);
     if (it == m->graphs.end()) {
+      if (m->graphs.size() >= kMaxGraphs) {
+        // evict the least recently used graph; a launch of it may still be
+        // in flight on another stream, so the device drains first (rare)
+        auto old = m->graphs.begin();
+        for (auto g = m->graphs.begin(); g != m->graphs.end(); ++g)
+          if (g->second.used < old->second.used) old = g;
+        e = cudaDeviceSynchronize();
+        if (!e) e = cudaGraphExecDestroy(old->second.exec);
+        if (e) {
+          m->unhealthy = true;
+          return fail(NC_ERR_CUDA, "evicting a step graph failed: %s", cudaGetErrorString(e));
+        }
+        m->graphs.erase(old);
+      }
       // First use: launch once eagerly (sets per-kernel attributes), then capture.
       e = enqueue_step(m, batch, io, kvv, splits, s);
       if (!e) e = cudaStreamSynchronize(s);
@@ -491,12 +507,13 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
         m->unhealthy = true;
         return fail(NC_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
       }
-      it = m->graphs.emplace(key, ge).first;
+      it = m->graphs.emplace(key, Model::GraphEntry{ge, ++m->graph_clock}).first;
       // The eager launch above already performed this step; its KV writes and
       // logits are identical to a replay, so the replay is skipped.
       return NC_OK;
     }
-    e = cudaGraphLaunch(it->second, s);
+    it->second.used = ++m->graph_clock;
+    e = cudaGraphLaunch(it->second.exec, s);
   }
   if (e) {
     m->unhealthy = true;

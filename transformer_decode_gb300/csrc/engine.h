@@ -12,6 +12,8 @@
 
 namespace nc {
 
+constexpr size_t kMaxGraphs = 16;  // captured step graphs a model keeps
+
 struct LayerPacked {
   uint16_t* w_qkv = nullptr;  // [(Hq + 2 Hkv) D, H] bf16 (NC_BF16)
   uint16_t* b_qkv = nullptr;  // [(Hq + 2 Hkv) D] or null
@@ -43,7 +45,9 @@ struct Model {
   int* status = nullptr;
   // persistent decode kernel: epoch-tagged hand-over words, its ticket, the
   // step sequence number and the device copy of the per-layer pointers
-  uint64_t *xw = nullptr, *qkvw = nullptr, *aw = nullptr, *hw = nullptr, *mlw = nullptr;
+  uint64_t *xw = nullptr, *qkvw = nullptr, *aw = nullptr, *hw = nullptr;
+  float* apart = nullptr;          // attention split partials
+  unsigned int* atick = nullptr;   // attention split tickets [L][kPMaxBatch][Hkv]
   unsigned int *pticket = nullptr, *seq = nullptr;
   PLayer* players = nullptr;
   unsigned long long* prof = nullptr;  // phase profile [2 * (5L + 1) + 2]
@@ -51,7 +55,15 @@ struct Model {
   bool unhealthy = false;
   cudaStream_t cap_stream = nullptr;  // private stream used only for graph capture
   int* status_host = nullptr;         // pinned host copy of the status word
-  std::map<GraphKey, cudaGraphExec_t> graphs;
+  // Captured step graphs by (batch, buffers, cache layout), each with the
+  // stamp of its last use; at most kMaxGraphs are kept (least recently used
+  // evicted), so a caller that rotates buffers does not grow the cache.
+  struct GraphEntry {
+    cudaGraphExec_t exec;
+    unsigned long long used;
+  };
+  std::map<GraphKey, GraphEntry> graphs;
+  unsigned long long graph_clock = 0;
   ~Model();
 };
 

@@ -19,9 +19,12 @@
 //    epoch): a reader spins until the epoch of the word equals the one it
 //    expects, so no separate flag or grid barrier is needed. Epochs carry the
 //    step sequence number, so values of an earlier step never match.
-//  * Attention runs one CTA per (sequence, kv head): RoPE (and q/k norm) of
-//    its heads, the K/V append, and the online-softmax scan over the cached
-//    positions in chunks (Tang section 2.2, the monoid on (m, l, acc)).
+//  * Attention runs one CTA per (sequence, kv head, position split): RoPE
+//    (and q/k norm) of its heads, the K/V append, and the online-softmax scan
+//    over the split's cached positions in chunks (Tang section 2.2, the
+//    monoid on (m, l, acc)). Long caches are split over the whole grid; the
+//    last split of each (sequence, kv head) to finish merges the partials
+//    (section 2.5: a split is valid for any associative monoid).
 //  * Every spin is bounded by %globaltimer. On expiry the CTA writes
 //    NC_ERR_TIMEOUT to the status word, stops issuing copies, waits (bounded)
 //    for the copies in flight and leaves through the final ticket, so the
@@ -90,6 +93,7 @@ struct PShared {
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
   int abort;        // set once a bounded wait expired in this CTA
+  int merge;        // attention: this CTA's split arrived last and merges
   unsigned issued;  // tiles the producer issued
   int pos[kPMaxBatch];
   float rope_cs[kPMaxBatch][64], rope_sn[kPMaxBatch][64];  // RoPE cos / sin at each position (D/2 <= 64)
@@ -206,13 +210,14 @@ __device__ __forceinline__ int cached_positions(const PersistArgs& a, int b, int
 
 // Attention work plan: the cached positions of each (sequence, kv head) are
 // split into up to kPMaxSplits ranges of at least kAttnSplitMin positions,
-// each range one item on its own CTA (split-K over positions; the o-proj
-// gather merges the partial softmax states). Items of all sequences together
-// stay within half of the grid. Returns the item count.
+// each range one item on its own CTA (split-K over positions; the last split
+// to finish merges the partial softmax states). Items of all sequences
+// together stay within the grid, so a long cache streams through every SM.
+// Returns the item count.
 constexpr int kAttnSplitMin = 128;  // one chunk: shorter scans are not split
 __device__ int attn_plan(const PersistArgs& a, int grid, int (&nsplit)[kPMaxBatch],
                          int (&item0)[kPMaxBatch + 1]) {
-  int cap = (grid / 2) / (a.B * a.Hkv);
+  int cap = grid / (a.B * a.Hkv);
   if (cap > kPMaxSplits) cap = kPMaxSplits;
   if (cap < 1) cap = 1;
   item0[0] = 0;
@@ -457,108 +462,6 @@ __device__ __noinline__ void gather_input(const PersistArgs& a, const uint64_t* 
     }
   }
   consumer_sync();
-}
-
-// The o-proj input: each sequence's attention output merged over its
-// position splits with the online-softmax combine (Tang section 2.2): per
-// head M = max_s m_s, c_s = exp(m_s - M) l_s / sum_t exp(m_t - M) l_t and
-// out = sum_s c_s o_s (o_s = acc_s / l_s). One split gives c = 1 and out = o
-// exactly. A thread's output words (its elements x the splits) and one (m, l)
-// word are loaded in one round.
-constexpr int kMergeElems = 4;  // elements per thread per round (x kPMaxSplits words)
-template <int BT>
-__device__ __noinline__ void gather_attn(const PersistArgs& a, uint32_t epoch, Spin& sp) {
-  extern __shared__ __align__(128) char smem[];
-  PShared& S = *reinterpret_cast<PShared*>(smem);
-  float* xs = reinterpret_cast<float*>(smem + a.xs_offset);
-  float* mlv = reinterpret_cast<float*>(smem + a.attn_offset);  // [split][head][m, l]
-  float* coef = mlv + 2 * kPMaxSplits * kPMaxHeads;             // [head][split]
-  const int Hq = a.Hq, D = a.D, qd = Hq * D, nb = a.B;
-  const int ct = threadIdx.x - kWarp;
-  const int per = (qd + kPConsumerThreads - 1) / kPConsumerThreads;  // elements per thread
-  const int nround = (per + kMergeElems - 1) / kMergeElems;
-  constexpr int NW = kMergeElems * kPMaxSplits;
-#pragma unroll 1
-  for (int b = 0; b < BT; ++b) {
-    if (b >= nb) {
-      for (int i = ct; i < qd; i += kPConsumerThreads) xs[b * qd + xs_at(i, qd)] = 0.f;
-      continue;
-    }
-    const int ns = S.nsplit[b];
-    const uint64_t* ow = a.aw + (size_t)b * kPMaxSplits * qd;
-    const uint64_t* mw = a.mlw + (size_t)b * kPMaxSplits * Hq * 2;
-#pragma unroll 1
-    for (int rd = 0; rd < nround; ++rd) {
-      uint64_t w[NW];
-      // word u: element u / kPMaxSplits, split u % kPMaxSplits
-      const int ibase = ct + rd * kMergeElems * kPConsumerThreads;
-      const auto adr = [ow, qd, ibase](int u) {
-        return ow + (size_t)(u % kPMaxSplits) * qd + ibase + (u / kPMaxSplits) * kPConsumerThreads;
-      };
-      uint32_t valid = 0;
-#pragma unroll
-      for (int u = 0; u < NW; ++u) {
-        const int e = u / kPMaxSplits, t = u % kPMaxSplits;
-        if (t < ns && ibase + e * kPConsumerThreads < qd) {
-          valid |= 1u << u;
-          w[u] = ld_word(adr(u));
-        }
-      }
-      // the (m, l) words of every (split, head): up to three per thread
-      const int nml = rd == 0 ? ns * Hq * 2 : 0;
-      const auto madr = [mw, ct](int u) { return mw + ct + u * kPConsumerThreads; };
-      uint64_t mwd[3] = {0, 0, 0};
-      uint32_t mvalid = 0;
-#pragma unroll
-      for (int u = 0; u < 3; ++u)
-        if (ct + u * kPConsumerThreads < nml) {
-          mvalid |= 1u << u;
-          mwd[u] = ld_word(madr(u));
-        }
-      ll_settle<NW>(adr, valid, epoch, w, sp);
-      ll_settle<3>(madr, mvalid, epoch, mwd, sp);
-#pragma unroll
-      for (int u = 0; u < 3; ++u)
-        if ((mvalid >> u) & 1u) mlv[ct + u * kPConsumerThreads] = __uint_as_float(static_cast<uint32_t>(mwd[u]));
-      if (rd == 0) {
-        consumer_sync();
-        if (ct < Hq) {
-          float M = -INFINITY;
-          for (int t = 0; t < ns; ++t) M = fmaxf(M, mlv[(t * Hq + ct) * 2]);
-          float wl[kPMaxSplits], L = 0.f;
-#pragma unroll
-          for (int t = 0; t < kPMaxSplits; ++t) {
-            wl[t] = 0.f;
-            if (t < ns) {
-              const float m = mlv[(t * Hq + ct) * 2], l = mlv[(t * Hq + ct) * 2 + 1];
-              wl[t] = m == -INFINITY ? 0.f : expf(m - M) * l;
-              L += wl[t];
-            }
-          }
-          // a division (not a reciprocal) so that one split gives c = l / l = 1
-#pragma unroll
-          for (int t = 0; t < kPMaxSplits; ++t) coef[ct * kPMaxSplits + t] = L > 0.f ? wl[t] / L : 0.f;
-        }
-        consumer_sync();
-      }
-#pragma unroll
-      for (int e = 0; e < kMergeElems; ++e) {
-        const int i = ct + (rd * kMergeElems + e) * kPConsumerThreads;
-        if (i < qd) {
-          const int h = i / D;
-          float out = 0.f;
-#pragma unroll
-          for (int t = 0; t < kPMaxSplits; ++t)
-            if (t < ns)
-              out = fmaf(coef[h * kPMaxSplits + t],
-                         __uint_as_float(static_cast<uint32_t>(w[e * kPMaxSplits + t])), out);
-          xs[b * qd + xs_at(i, qd)] = out;
-        }
-      }
-    }
-    consumer_sync();  // coef and mlv are rewritten for the next sequence
-  }
-  consumer_sync();  // xs complete (also the rows of absent sequences)
 }
 
 __device__ __forceinline__ float silu_mul_p(float g, float u) {
@@ -818,15 +721,18 @@ __device__ __forceinline__ float2 kv_smem2(const char* base, int idx) {
   }
 }
 
-// Consumer: one item, i.e. split `split` of (sequence b, kv head g). RoPE
-// (+ q/k norm) of the G query heads and the key; split 0 appends K/V at slot
-// pos and opens the online-softmax state with the new position; then the scan
-// over the split's cached positions [p0, p1), in chunks from the ring. The
-// split's state leaves as its normalised output o = acc / l per (head, dim)
-// and (m, l) per head (Tang section 2.2: the partials of a split-K scan that
-// the o-proj gather merges).
+// Consumer: one item, i.e. split `split` of the ns splits of (sequence b, kv
+// head g). RoPE (+ q/k norm) of the G query heads and the key; split 0
+// appends K/V at slot pos and opens the online-softmax state with the new
+// position; then the scan over the split's cached positions [p0, p1), in
+// chunks from the ring. An unsplit scan writes its output o = acc / l as the
+// attention output words. A split writes its state (m, l and o per head) to
+// the partials and takes a ticket; the split that arrives last merges all
+// of them (Tang section 2.2: per head M = max_s m_s, weights
+// w_s = exp(m_s - M) l_s, out = sum_s (w_s / sum_t w_t) o_s; one split gives
+// weight l / l = 1 and out = o exactly) and writes the output words.
 template <int D, bool KV16>
-__device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int split,
+__device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int split, int ns,
                                             int p0, int p1, int layer, uint32_t ep_qkv,
                                             uint32_t ep_out, int nslots, RingPos& rp, Spin& sp) {
   // shared-memory pointers are derived from the dynamic shared array here, so
@@ -1024,19 +930,62 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     // no barrier here: the next chunk writes the other score buffer, and the
     // one after it is behind that chunk's two barriers
   }
-  const size_t part = (size_t)b * kPMaxSplits + split;
+  uint64_t* const aout = a.aw + (size_t)b * Hq * D + (size_t)g * G * D;  // [G][D] words
+  if (ns == 1) {
+    if (ct < npair) {
+      const float inv = lrun[my_h] > 0.f ? 1.f / lrun[my_h] : 0.f;
+      st_word(aout + my_h * D + 2 * my_d2, acc0 * inv, ep_out);
+      st_word(aout + my_h * D + 2 * my_d2 + 1, acc1 * inv, ep_out);
+    }
+    consumer_sync();  // the scratch is reused by the next item
+    return;
+  }
+  // split partials [G][D + 2] = (m, l, o[D]) per head of this (b, g, split)
+  constexpr int DP = D + 2;
+  float* const parts = a.apart + ((size_t)b * kPMaxSplits * Hq + (size_t)g * G) * DP;
+  const size_t sstride = (size_t)Hq * DP;  // from one split's partials to the next
+  float* const mine = parts + split * sstride;
   if (ct < npair) {
     const float inv = lrun[my_h] > 0.f ? 1.f / lrun[my_h] : 0.f;
-    uint64_t* out = a.aw + part * Hq * D + (size_t)(g * G + my_h) * D + 2 * my_d2;
-    st_word(out, acc0 * inv, ep_out);
-    st_word(out + 1, acc1 * inv, ep_out);
+    mine[my_h * DP + 2 + 2 * my_d2] = acc0 * inv;
+    mine[my_h * DP + 3 + 2 * my_d2] = acc1 * inv;
   }
   if (ct < G) {
-    uint64_t* ml = a.mlw + (part * Hq + g * G + ct) * 2;
-    st_word(ml, mrun[ct], ep_out);
-    st_word(ml + 1, lrun[ct], ep_out);
+    mine[ct * DP] = mrun[ct];
+    mine[ct * DP + 1] = lrun[ct];
   }
-  consumer_sync();  // the scratch is reused by the next item
+  __threadfence();  // each writer's partials are visible GPU-wide before the ticket
+  consumer_sync();
+  unsigned int* const tick = a.atick + ((size_t)layer * kPMaxBatch + b) * Hkv + g;
+  if (ct == 0) S.merge = atomicAdd(tick, 1u) == (unsigned)(ns - 1);
+  consumer_sync();
+  if (!S.merge) return;  // uniform: read after the barrier
+  __threadfence();       // the other splits' partials, published before their tickets
+  float* coef = sc;      // [G][ns] merge weights (the score buffers are free now)
+  if (ct < G) {
+    float M = -INFINITY;
+    for (int t = 0; t < ns; ++t) M = fmaxf(M, __ldcg(parts + t * sstride + ct * DP));
+    float L = 0.f;
+    for (int t = 0; t < ns; ++t) {
+      const float m = __ldcg(parts + t * sstride + ct * DP);
+      const float l = __ldcg(parts + t * sstride + ct * DP + 1);
+      const float w = m == -INFINITY ? 0.f : expf(m - M) * l;
+      coef[ct * kPMaxSplits + t] = w;
+      L += w;
+    }
+    // a division (not a reciprocal) so that one split gives l / l = 1
+    for (int t = 0; t < ns; ++t)
+      coef[ct * kPMaxSplits + t] = L > 0.f ? coef[ct * kPMaxSplits + t] / L : 0.f;
+  }
+  consumer_sync();
+  for (int i = ct; i < G * D; i += kPConsumerThreads) {
+    const int h = i / D, d = i % D;
+    const float* src = parts + h * DP + 2 + d;
+    float o = 0.f;
+    for (int t = 0; t < ns; ++t) o = fmaf(coef[h * kPMaxSplits + t], __ldcg(src + t * sstride), o);
+    st_word(aout + i, o, ep_out);
+  }
+  consumer_sync();  // coef and the scratch are reused by the next item
 }
 
 // The tiles of one projection phase (see gemv_phase). MODE 0: batch 1, rows of
@@ -1283,13 +1232,8 @@ __device__ __forceinline__ void gemv_phase(const PersistArgs& a, int ph, uint32_
     gather_input<BT>(a, a.xw, K, K, epoch_of(seq, ph - 1), layer == 0 ? a.embed : nullptr,
                      P->g_attn, sp);
   } else if (kind == kOPROJ) {
-    // unsplit scans (every sequence's attention in one item per kv head) need
-    // no merge: split 0's output words are the attention output
-    bool split = false;
-    for (int b = 0; b < BT; ++b) split |= S.nsplit[b] > 1;
-    if (split) gather_attn<BT>(a, epoch_of(seq, ph - 1), sp);
-    else gather_input<BT>(a, a.aw, K, (size_t)kPMaxSplits * K, epoch_of(seq, ph - 1), nullptr,
-                          nullptr, sp);
+    // the attention output words, merged over the position splits
+    gather_input<BT>(a, a.aw, K, K, epoch_of(seq, ph - 1), nullptr, nullptr, sp);
   } else if (kind == kGU) {
     gather_input<BT>(a, a.xw, K, K, epoch_of(seq, ph - 1), nullptr, P->g_mlp, sp);
   } else if (kind == kDOWN) {
@@ -1388,8 +1332,8 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           const int np = cached_positions(a, t.b, S.pos[t.b]);
           const int p0 = (int)(((long long)t.sp * np) / t.ns);
           const int p1 = (int)(((long long)(t.sp + 1) * np) / t.ns);
-          attention_item<D, KV16>(a, t.b, t.g, t.sp, p0, p1, layer, epoch_of(seq, ph - 1), ep,
-                                  nslots, rp, sp);
+          attention_item<D, KV16>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, epoch_of(seq, ph - 1),
+                                  ep, nslots, rp, sp);
         }
         if (prof) prof[2 * ph + 1] = global_timer();
         continue;
@@ -1455,6 +1399,9 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       }
     }
   }
+  // the split tickets of every layer start the next step at zero (also
+  // after an abort left some of them short)
+  for (int i = threadIdx.x; i < a.L * kPMaxBatch * a.Hkv; i += blockDim.x) a.atick[i] = 0u;
   __syncthreads();
   if (threadIdx.x == 0) {
     *a.seq = seq + 1;  // next step's epochs

@@ -11,10 +11,9 @@ constexpr int kMaxSlots = 8;           // weight ring slots (shared memory)
 constexpr int kPMaxBatch = 4;          // sequences per persistent step
 constexpr int kPSlots = 3;                // weight ring slots; they share what shared memory is left
 constexpr int kPMinSlotBytes = 32 * 1024; // smallest slot the kernel is run with
-constexpr int kPMaxCtx = 2048;         // cache capacity up to which it is chosen
 constexpr int kPMaxRows = 128;         // rows of H one CTA may own (H <= 128 * grid)
 constexpr int kPMaxLayers = 64;        // layers the persistent kernel handles
-constexpr int kPMaxSplits = 4;         // attention position splits per (sequence, kv head)
+constexpr int kPMaxSplits = 32;        // attention position splits per (sequence, kv head)
 constexpr int kPMaxHeads = 64;         // query heads
 
 // Per-layer packed weights as the persistent kernel reads them.
@@ -41,8 +40,9 @@ struct PersistArgs {
   // epoch-tagged hand-over words (value in the low half, epoch in the high)
   uint64_t* xw;    // [kPMaxBatch][H] residual stream
   uint64_t* qkvw;  // [kPMaxBatch][nqkv]
-  uint64_t* aw;    // [kPMaxBatch][kPMaxSplits][Hq D] attention output per split (o = acc / l)
-  uint64_t* mlw;   // [kPMaxBatch][kPMaxSplits][Hq][2] softmax state (m, l) per split and head
+  uint64_t* aw;    // [kPMaxBatch][Hq D] attention output (merged over the position splits)
+  float* apart;    // [kPMaxBatch][kPMaxSplits][Hq][D + 2] split partials (m, l, o = acc / l)
+  unsigned int* atick;  // [L][kPMaxBatch][Hkv] split arrivals, zeroed by the step's last CTA
   uint64_t* hw;    // [kPMaxBatch][F] SiLU(gate) * up
   unsigned long long* am_part;  // [B][grid] arg-max partial keys
   unsigned int* ticket;         // zero between steps

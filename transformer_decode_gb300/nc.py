@@ -32,7 +32,7 @@ EXPORTS = [
     "nc_get_device_status", "nc_rmsnorm_gemv", "nc_gemv_residual", "nc_swiglu_gemv",
     "nc_rope_qkv", "nc_attn_decode", "nc_lm_head_argmax", "nc_quantize_weight", "nc_w8a8_gemv",
     "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile", "nc_decode_path",
-    "nc_sample", "nc_sample_scratch_bytes",
+    "nc_sample", "nc_sample_scratch_bytes", "nc_attn_decode_static_status",
 ]
 
 
@@ -115,6 +115,7 @@ def _declare(L):
     L.nc_quantize_weight.argtypes = [vp, i, i, vp, vp, vp]
     L.nc_w8a8_gemv.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
     L.nc_attn_decode_static.argtypes = [i, i, i, i, i, i, vp, vp, vp, C.POINTER(KVStruct), vp, vp]
+    L.nc_attn_decode_static_status.argtypes = [vp, C.POINTER(i)]
     L.nc_profile_phases.argtypes = [vp, i]
     L.nc_decode_path.argtypes = [vp, i, vp, i, C.POINTER(i)]
     L.nc_read_phase_profile.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), i, C.POINTER(i)]
@@ -215,6 +216,14 @@ def attn_decode_static(shape, layer, q, positions, positions_host, kv, out, stre
         _ptr(q, torch.float32, "q", B * shape.q_dim), _ptr(positions, torch.int32, "positions", B),
         ph.ctypes.data_as(C.c_void_p), C.byref(s),
         _ptr(out, torch.float32, "out", B * shape.q_dim), _stream(stream)))
+
+
+def attn_decode_static_status(stream=None):
+    """nc_attn_decode_static_status: synchronise the stream, read and clear
+    the device-side error word of attn_decode_static (0 = none)."""
+    code = C.c_int(0)
+    _check(load().nc_attn_decode_static_status(_stream(stream), C.byref(code)))
+    return code.value
 
 
 # ------------------------------------------------------------------ sampling
