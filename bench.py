@@ -693,6 +693,8 @@ def oracle_for(cfg, max_ctx):
     import oracle
     oracle.build()
     shape = getattr(synth, cfg["shape"])
+    if cfg.get("layers"):
+        shape = shape.with_layers(cfg["layers"])
     past = workload_past(cfg)
     om = oracle.OracleModel(shape, cpu_weights(shape), w8a8=cfg["w8a8"])
     okv = om.new_kv(cfg["batch"], max_ctx)
@@ -805,9 +807,12 @@ def rounds_summary(per):
 
 
 def run_workload(args, ws, rank, local, name):
-    cfg = WORKLOADS[name]
+    cfg = dict(WORKLOADS[name])
     torch.cuda.set_device(local)
     shape = getattr(synth, cfg["shape"])
+    if args.layers:  # a smaller case of the same shape, for profiler captures
+        shape = shape.with_layers(args.layers)
+        cfg["layers"] = args.layers
     B, gen = cfg["batch"], cfg["gen"]
     past = workload_past(cfg)
     wd = synth.model_weights(shape, device="cuda")
@@ -914,7 +919,9 @@ def run_workload(args, ws, rank, local, name):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dur * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "i8/i32" if cfg["w8a8"] else "f32", "data": "synthetic",
-            "config": {"workload": name, "batch": B, "past": cfg["past"], "greedy_steps": gen,
+            "config": {"workload": name + (f" (first {args.layers} layers only)"
+                                           if args.layers else ""),
+                       "batch": B, "past": cfg["past"], "greedy_steps": gen,
                        "weights": ("int8 per-row scales (W8A8)" if cfg["w8a8"] else "bf16") +
                                   " from seeded N(0,0.02), fp32 accumulate",
                        "kv": ("paged (block 16, shuffled tables)" if cfg["paged"] else "contiguous")
@@ -998,6 +1005,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=[C1, SAMPLED] + list(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers of the workload's model (a small "
+                         "case for profiler captures; not a metric line)")
     ap.add_argument("--phase-profile", action="store_true",
                     help="print the persistent kernel's per-phase critical path (stderr)")
     args = ap.parse_args()

@@ -181,6 +181,21 @@ nc_status nc_get_device_status(nc_model* m, void* stream, int* code);
 typedef enum { NC_PATH_STAGED = 0, NC_PATH_PERSISTENT = 1 } nc_path;
 nc_status nc_decode_path(nc_model* m, int batch, const nc_kv_cache* kv, int flags, int* path);
 
+/* W8A8 diagnostic (nanoinfer "Quantization": the per-token activation codes;
+ * for checking every code a whole-model W8A8 step used against the oracle's).
+ * While set, every nc_decode_step and nc_block_forward of this NC_INT8 model
+ * writes the activation codes and scales of its W8A8 products to the
+ * caller's device buffers, and a decode step runs its kernels directly (no
+ * graph). Layout for a step at batch B, per layer l of L:
+ *   codes_dev + l * B * (2 H + Hq D + F): the codes [B][H] of the QKV
+ *     product, then [B][Hq D] of the o-proj, [B][H] of gate|up, [B][F] of
+ *     the down product (nc_block_forward writes layer `layer`'s slot);
+ *   scales_dev + (l * 4 + p) * B: the B scales of product p in that order.
+ * Capacities are in elements; a step that needs more returns
+ * NC_ERR_CAPACITY. NULL, NULL turns it off. NC_ERR_DTYPE for a bf16 model. */
+nc_status nc_debug_w8a8_codes(nc_model* m, int8_t* codes_dev, size_t codes_capacity,
+                              float* scales_dev, size_t scales_capacity);
+
 /* Phase profile of the persistent decode kernel (a per-phase step profile in
  * the spirit of nanocompile's per-primitive profile of one step). While
  * enabled, every persistent step records %globaltimer (ns) in each CTA at the
@@ -198,26 +213,44 @@ nc_status nc_read_phase_profile(nc_model* m, void* stream, unsigned long long* o
 
 /* ---------------- per-stage entry points (no model needed unless named) ---- */
 
+/* The weight-type argument of the stage GEMVs (nanoinfer "Quantization"):
+ *   NC_BF16: W is bf16 [N, K] (raw bits); the scale argument and
+ *     acc_i32_debug must be NULL.
+ *   NC_INT8: W is int8 [N, K] (16-byte aligned) with fp32 per-row scales
+ *     w_scale [N] (as nc_quantize_weight makes them). The kernel quantises
+ *     each sequence's (normed) input per token: s_x = amax / 127, codes
+ *     round-half-away(v / s_x) in [-127, 127]; accumulates acc = sum_k
+ *     W[n, k] * code_k in int32 (exact: |acc| <= K * 127^2); and dequantises
+ *     y = float(acc) * (w_scale[n] * s_x), each product rounded on its own,
+ *     then + bias. K must be a multiple of 16.
+ * Any other value returns NC_ERR_DTYPE. */
+
 /* y[b, n] = sum_k W[n, k] * xn[b, k] (+ bias[n]), xn = rmsnorm(x[b]) * gamma
  * when gamma != NULL (nanocompile: the five passes of rms_norm fused into one,
- * and the norm fused into the GEMV that follows), else xn = x.
- * x [B, K] fp32, gamma [K] bf16, W [N, K] bf16, bias [N] bf16 or NULL,
- * y [B, N] fp32. B <= 16. */
+ * and the norm fused into the GEMV that follows), else xn = x: the QKV
+ * projection with its bias. x [B, K] fp32, gamma [K] bf16, W [N, K] of
+ * `wtype`, w_scale [N] fp32 (NC_INT8), bias [N] bf16 or NULL, y [B, N] fp32.
+ * acc_i32_debug (NC_INT8, nullable): [B, N] int32 receives the accumulators,
+ * for bit-exact checks. B <= 16. */
 nc_status nc_rmsnorm_gemv(const float* x, const void* gamma, float eps, const void* W,
-                          const void* bias, int B, int K, int N, float* y, void* stream);
+                          nc_wtype wtype, const float* w_scale, const void* bias, int B, int K,
+                          int N, float* y, int32_t* acc_i32_debug, void* stream);
 
 /* x[b, n] += sum_k W[n, k] * a[b, k]: the o-proj and down projections with
  * the residual add fused in (nanocompile, "Phase 3": "output projection with
- * its residual add"). a [B, K], x [B, N] fp32 in place, W [N, K] bf16. */
-nc_status nc_gemv_residual(const float* a, const void* W, int B, int K, int N, float* x,
-                           void* stream);
+ * its residual add"). a [B, K], x [B, N] fp32 in place, W [N, K] of `wtype`,
+ * w_scale [N] fp32 (NC_INT8, else NULL). */
+nc_status nc_gemv_residual(const float* a, const void* W, nc_wtype wtype, const float* w_scale,
+                           int B, int K, int N, float* x, void* stream);
 
 /* h[b, f] = silu(g_f) * u_f with g = W_gate xn, u = W_up xn and xn the
  * normed x (Tang section 2.3: sibling reductions gate|up merged; nanoinfer
- * "Phase 8" sigmoid form). W_gu is [2F, K] bf16: rows 0..F-1 gate, F..2F-1 up.
+ * "Phase 8" sigmoid form). W_gu is [2F, K] of `wtype`: rows 0..F-1 gate,
+ * F..2F-1 up; s_gu [2F] fp32 their scales (NC_INT8, else NULL).
  * x [B, K], h [B, F] fp32. */
-nc_status nc_swiglu_gemv(const float* x, const void* gamma, float eps, const void* W_gu, int B,
-                         int K, int F, float* h, void* stream);
+nc_status nc_swiglu_gemv(const float* x, const void* gamma, float eps, const void* W_gu,
+                         nc_wtype wtype, const float* s_gu, int B, int K, int F, float* h,
+                         void* stream);
 
 /* RoPE (half-split) on q and k of layer `layer` at positions, optional
  * per-head q/k RMSNorm before it, then K and V rounded to bf16 and stored at

@@ -64,7 +64,45 @@ class Model(C.Structure):
                 ("lm_head", C.POINTER(C.c_uint16)), ("g_final", C.POINTER(C.c_uint16)),
                 ("layers", C.POINTER(Layer)), ("w8a8", C.c_int), ("act_block", C.c_int),
                 ("q8_embed", C.POINTER(C.c_int8)), ("s_embed", C.POINTER(C.c_float)),
-                ("int4_group", C.c_int)]
+                ("int4_group", C.c_int), ("trace", C.c_void_p)]
+
+
+class Trace(C.Structure):
+    _fields_ = [("codes", C.POINTER(C.c_int8)), ("quot", C.POINTER(C.c_float)),
+                ("force_codes", C.POINTER(C.c_int8)), ("n_codes", C.c_long),
+                ("cap_codes", C.c_long), ("kv_own", C.POINTER(C.c_uint16)),
+                ("kv_val", C.POINTER(C.c_float)), ("force_kv", C.POINTER(C.c_uint16)),
+                ("n_kv", C.c_long), ("cap_kv", C.c_long), ("overflow", C.c_int)]
+
+
+class OracleTrace:
+    """The rounding steps of one oracle decode step (a test hook; see
+    oracle.h): per W8A8 activation quantisation its codes and the fp32
+    quotients v / s it rounded, per bf16 K/V store its bits and the fp32 value
+    it rounded, in call order (per sequence, per layer: the q, k, v, o, gate,
+    up, down products; per kv head K then V). force_codes / force_kv (same
+    layout) make the step use those values in place of its own."""
+
+    def __init__(self, n_codes, n_kv, force_codes=None, force_kv=None):
+        self.codes = np.zeros(n_codes, np.int8)
+        self.quot = np.zeros(n_codes, np.float32)
+        self.kv_own = np.zeros(n_kv, np.uint16)
+        self.kv_val = np.zeros(n_kv, np.float32)
+        self.force_codes = None if force_codes is None else np.ascontiguousarray(force_codes, np.int8)
+        self.force_kv = None if force_kv is None else np.ascontiguousarray(force_kv, np.uint16)
+        if self.force_codes is not None:
+            assert self.force_codes.size == n_codes
+        if self.force_kv is not None:
+            assert self.force_kv.size == n_kv
+        self.struct = Trace(_p(self.codes, C.c_int8), _p(self.quot, C.c_float),
+                            _p(self.force_codes, C.c_int8), 0, n_codes,
+                            _p(self.kv_own, C.c_uint16), _p(self.kv_val, C.c_float),
+                            _p(self.force_kv, C.c_uint16), 0, n_kv, 0)
+
+    @property
+    def complete(self):
+        t = self.struct
+        return not t.overflow and t.n_codes == t.cap_codes and t.n_kv == t.cap_kv
 
 
 class KV(C.Structure):
@@ -390,12 +428,14 @@ class OracleModel:
         self.q8_embed = (q8e, se)
         self.struct = Model(cfg, _p(emb, C.c_uint16), _p(head, C.c_uint16),
                             _p(gf, C.c_uint16), layers, int(w8a8), int(act_block),
-                            _p(q8e, C.c_int8), _p(se, C.c_float), int(int4_group))
+                            _p(q8e, C.c_int8), _p(se, C.c_float), int(int4_group), None)
 
     def new_kv(self, batch, max_ctx, bf16=False):
         return OracleKV(self.shape, batch, max_ctx, bf16)
 
-    def decode_step(self, kv, tokens, positions, prec="f32", hidden=False):
+    def decode_step(self, kv, tokens, positions, prec="f32", hidden=False, trace=None):
+        """One decode step; trace (an OracleTrace) records, and may force, the
+        step's W8A8 codes and bf16 K/V stores."""
         dt, ct = _real(prec)
         tokens = _np(tokens, np.int32)
         positions = _np(positions, np.int32)
@@ -403,9 +443,13 @@ class OracleModel:
         logits = np.empty((B, self.shape.vocab), dt)
         nxt = np.empty(B, np.int32)
         hid = np.empty((B, self.shape.n_layers + 1, self.shape.hidden), dt) if hidden else None
-        rc = getattr(lib(), f"orc_decode_step_{prec}")(
-            C.byref(self.struct), C.byref(kv.struct), B, _p(tokens, C.c_int32),
-            _p(positions, C.c_int32), _p(logits, ct), _p(nxt, C.c_int32), _p(hid, ct))
+        self.struct.trace = None if trace is None else C.addressof(trace.struct)
+        try:
+            rc = getattr(lib(), f"orc_decode_step_{prec}")(
+                C.byref(self.struct), C.byref(kv.struct), B, _p(tokens, C.c_int32),
+                _p(positions, C.c_int32), _p(logits, ct), _p(nxt, C.c_int32), _p(hid, ct))
+        finally:
+            self.struct.trace = None
         if rc != 0:
             raise ValueError("oracle decode step rejected its input (position or NaN)")
         return (logits, nxt, hid) if hidden else (logits, nxt)

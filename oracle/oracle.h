@@ -91,7 +91,34 @@ typedef struct {
   const float* s_embed;     /* [V] */
   int int4_group;           /* > 0: the projections use the INT4 fields, one scale per
                                group of this many weights (nanoinfer "Quantization") */
+  struct orc_trace* trace;  /* test hook of whole-model checks, or NULL (see below) */
 } orc_model;
+
+/* Trace of the rounding steps inside a decode step (NULL in orc_model: off,
+ * and nothing below happens). Two kinds of entries, each appended in call
+ * order (per sequence, per layer):
+ *   - every per-token W8A8 activation quantisation (the q, k, v, o, gate, up
+ *     and down products, in that order): its own codes [K] and the fp32
+ *     quotients v / s it rounded [K]; with force_codes set, the product then
+ *     uses force_codes (same offsets) in place of its own codes (its own
+ *     scale is kept);
+ *   - every bf16 store of the new position's K/V (per kv head: D values of K,
+ *     then D of V): its own bits and the fp32 value it rounded; with force_kv
+ *     set, force_kv's bits are stored instead.
+ * The caller sizes the arrays (cap_*); an entry that would pass the end sets
+ * overflow and is neither recorded nor forced. The rounding itself is the
+ * same with or without the trace: forcing replaces a rounded result only. */
+typedef struct orc_trace {
+  int8_t* codes;
+  float* quot;
+  const int8_t* force_codes;
+  long n_codes, cap_codes;
+  uint16_t* kv_own;
+  float* kv_val;
+  const uint16_t* force_kv;
+  long n_kv, cap_kv;
+  int overflow;
+} orc_trace;
 
 /* Logical KV cache: k, v are [L][B][Hkv][max_ctx][D] of fp32 (bf16 = 0, the
  * nanoinfer cache: "24 KiB per token at fp32") or of bf16 bit patterns

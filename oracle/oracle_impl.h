@@ -214,13 +214,44 @@ void F(orc_linear_int4)(const uint8_t* w4, const float* s4, int group, const uin
   }
 }
 
-/* The W8A8 product in the model's activation mode. */
+/* The W8A8 product in the model's activation mode. With a trace (a test
+ * hook, see oracle.h) the per-token form records its codes and quotients and
+ * may take forced codes; the arithmetic after the codes is orc_linear_w8a8's. */
 static void F(linear_i8)(const orc_model* m, const int8_t* w8, const float* sw,
                          const uint16_t* bias, int n, int k, const REAL* x, REAL* y) {
-  if (m->act_block > 0)
+  orc_trace* tr = m->trace;
+  if (m->act_block > 0) {
     F(orc_linear_w8a8_blocked)(w8, sw, bias, n, k, m->act_block, x, y);
-  else
+    return;
+  }
+  if (!tr) {
     F(orc_linear_w8a8)(w8, sw, bias, n, k, x, y);
+    return;
+  }
+  float* xf = (float*)malloc(sizeof(float) * (size_t)k);
+  int8_t* xq = (int8_t*)malloc((size_t)k);
+  int32_t* acc = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
+  for (int i = 0; i < k; ++i) xf[i] = (float)x[i];
+  float sx = orc_quantize_row_f32(xf, k, xq);
+  if (tr->n_codes + k <= tr->cap_codes) {
+    for (int i = 0; i < k; ++i) {
+      tr->codes[tr->n_codes + i] = xq[i];
+      tr->quot[tr->n_codes + i] = sx == 0.0f ? 0.0f : xf[i] / sx;
+    }
+    if (tr->force_codes) memcpy(xq, tr->force_codes + tr->n_codes, (size_t)k);
+    tr->n_codes += k;
+  } else {
+    tr->overflow = 1;
+  }
+  if (orc_matvec_i8(w8, n, k, xq, acc) != 0) abort();
+  for (int j = 0; j < n; ++j) {
+    REAL yj = (REAL)acc[j] * ((REAL)sw[j] * (REAL)sx);
+    if (bias) yj += F(widen)(bias[j]);
+    y[j] = yj;
+  }
+  free(xf);
+  free(xq);
+  free(acc);
 }
 
 /* The residual row of a token: the bf16 embedding widened, or an int8 row
@@ -317,11 +348,28 @@ void F(orc_block_decode)(const orc_model* m, int layer, orc_kv* kv, int b, int p
   REAL* v = (REAL*)malloc(sizeof(REAL) * (size_t)kd);
   REAL* a = (REAL*)malloc(sizeof(REAL) * (size_t)qd);
   F(qkv_token)(m, layer, x, pos, q, k, v);
+  orc_trace* tr = m->trace;
   for (int g = 0; g < c->n_kv_heads; ++g) {
     long base = F(kv_off)(c, kv, layer, b, g) + (long)pos * D;
     for (int i = 0; i < D; ++i) {
       F(kv_put)(kv->k, kv->bf16, base + i, k[g * D + i]);
       F(kv_put)(kv->v, kv->bf16, base + i, v[g * D + i]);
+    }
+    if (tr && kv->bf16) {  /* test hook (oracle.h): record, and maybe force, the stores */
+      if (tr->n_kv + 2 * D > tr->cap_kv) {
+        tr->overflow = 1;
+        continue;
+      }
+      for (int w = 0; w < 2; ++w) {
+        uint16_t* dst = (uint16_t*)(w ? kv->v : kv->k) + base;
+        const REAL* src = w ? v + g * D : k + g * D;
+        for (int i = 0; i < D; ++i) {
+          tr->kv_own[tr->n_kv + i] = dst[i];
+          tr->kv_val[tr->n_kv + i] = (float)src[i];
+          if (tr->force_kv) dst[i] = tr->force_kv[tr->n_kv + i];
+        }
+        tr->n_kv += D;
+      }
     }
   }
 #pragma omp parallel for schedule(static)

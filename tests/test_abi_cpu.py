@@ -81,12 +81,30 @@ def test_model_create_rejects_null_and_misaligned_weights(lib):
 
 def test_stage_entry_points_reject_bad_shapes(lib):
     P = C.c_void_p(4096)
-    assert lib.nc_rmsnorm_gemv(None, None, 1e-6, P, None, 1, 64, 8, P, None) == 1
-    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, None, 1, 60, 8, P, None) == 2   # K % 8
-    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, None, 17, 64, 8, P, None) == 2  # B > 16
-    assert lib.nc_rmsnorm_gemv(C.c_void_p(4100), None, 1e-6, P, None, 1, 64, 8, P, None) == 1
-    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, 0, 64, 8, P, None) == 2
-    assert lib.nc_gemv_residual(P, P, 1, 64, 0, P, None) == 2
+    BF, I8 = nc.NC_BF16, nc.NC_INT8
+    assert lib.nc_rmsnorm_gemv(None, None, 1e-6, P, BF, None, None, 1, 64, 8, P, None, None) == 1
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, BF, None, None, 1, 60, 8, P, None, None) == 2   # K % 8
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, BF, None, None, 17, 64, 8, P, None, None) == 2  # B > 16
+    assert lib.nc_rmsnorm_gemv(C.c_void_p(4100), None, 1e-6, P, BF, None, None, 1, 64, 8, P, None,
+                               None) == 1
+    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, BF, None, 0, 64, 8, P, None) == 2
+    assert lib.nc_gemv_residual(P, P, BF, None, 1, 64, 0, P, None) == 2
+    # the weight type: unknown -> NC_ERR_DTYPE; scales and accumulators belong to NC_INT8;
+    # NC_INT8 needs its scales and K a multiple of 16
+    E = {n: nc.STATUS.index(n) for n in nc.STATUS}
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, 7, None, None, 1, 64, 8, P, None, None) == E["NC_ERR_DTYPE"]
+    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, 7, None, 1, 64, 8, P, None) == E["NC_ERR_DTYPE"]
+    assert lib.nc_gemv_residual(P, P, 7, None, 1, 64, 8, P, None) == E["NC_ERR_DTYPE"]
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, BF, P, None, 1, 64, 8, P, None, None) == 1
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, BF, None, None, 1, 64, 8, P, P, None) == 1
+    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, BF, P, 1, 64, 8, P, None) == 1
+    assert lib.nc_gemv_residual(P, P, BF, P, 1, 64, 8, P, None) == 1
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, I8, None, None, 1, 64, 8, P, None, None) == 1
+    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, I8, None, 1, 64, 8, P, None) == 1
+    assert lib.nc_gemv_residual(P, P, I8, None, 1, 64, 8, P, None) == 1
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, I8, P, None, 1, 40, 8, P, None, None) == 2  # K % 16
+    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, I8, P, 17, 64, 8, P, None) == 2
+    assert lib.nc_gemv_residual(P, P, I8, P, 1, 64, 0, P, None) == 2
     assert lib.nc_w8a8_gemv(P, None, 1e-6, P, P, None, 1, 40, 8, P, None, None, None, None) == 2
     assert lib.nc_quantize_weight(P, 0, 8, P, P, None) == 2
     assert lib.nc_decode_step(None, 1, P, P, P, None, P, None, 1, None) == 1
@@ -181,12 +199,20 @@ def test_entry_points_reject_misaligned_pointers(lib):
     E = nc.STATUS.index("NC_ERR_INVALID_ARGUMENT")
     P, P2, P4 = C.c_void_p(4096), C.c_void_p(4098), C.c_void_p(4100)
     # gamma read 8 bytes at a time, bias per bf16, y per fp32
-    assert lib.nc_rmsnorm_gemv(P, P4, 1e-6, P, None, 1, 64, 8, P, None) == E
-    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, C.c_void_p(4097), 1, 64, 8, P, None) == E
-    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, None, 1, 64, 8, P2, None) == E
-    assert lib.nc_swiglu_gemv(P, P4, 1e-6, P, 1, 64, 8, P, None) == E
-    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, 1, 64, 8, P2, None) == E
-    assert lib.nc_gemv_residual(P, P, 1, 64, 8, P2, None) == E
+    BF, I8 = nc.NC_BF16, nc.NC_INT8
+    assert lib.nc_rmsnorm_gemv(P, P4, 1e-6, P, BF, None, None, 1, 64, 8, P, None, None) == E
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, BF, None, C.c_void_p(4097), 1, 64, 8, P, None,
+                               None) == E
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, BF, None, None, 1, 64, 8, P2, None, None) == E
+    assert lib.nc_swiglu_gemv(P, P4, 1e-6, P, BF, None, 1, 64, 8, P, None) == E
+    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, BF, None, 1, 64, 8, P2, None) == E
+    assert lib.nc_gemv_residual(P, P, BF, None, 1, 64, 8, P2, None) == E
+    # NC_INT8: 16-byte int8 rows, 4-byte scales, accumulators and outputs
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P2, I8, P, None, 1, 64, 8, P, None, None) == E
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, I8, P2, None, 1, 64, 8, P, None, None) == E
+    assert lib.nc_rmsnorm_gemv(P, None, 1e-6, P, I8, P, None, 1, 64, 8, P, P2, None) == E
+    assert lib.nc_swiglu_gemv(P, None, 1e-6, P, I8, P2, 1, 64, 8, P, None) == E
+    assert lib.nc_gemv_residual(P, P, I8, P, 1, 64, 8, P2, None) == E
     assert lib.nc_w8a8_gemv(P2, None, 1e-6, P, P, None, 1, 64, 8, P, None, None, None, None) == E
     assert lib.nc_w8a8_gemv(P, None, 1e-6, P, P2, None, 1, 64, 8, P, None, None, None, None) == E
     assert lib.nc_w8a8_gemv(P, None, 1e-6, P, P, None, 1, 64, 8, P, None, P2, None, None) == E

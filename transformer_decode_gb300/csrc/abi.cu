@@ -133,6 +133,21 @@ nc_status nc_decode_path(nc_model* m, int batch, const nc_kv_cache* kv, int flag
   return NC_OK;
 }
 
+nc_status nc_debug_w8a8_codes(nc_model* m, int8_t* codes_dev, size_t codes_capacity,
+                              float* scales_dev, size_t scales_capacity) {
+  NC_CHECK(m, NC_ERR_INVALID_ARGUMENT, "model is NULL");
+  Model* mm = M(m);
+  NC_CHECK(mm->cfg.wtype == NC_INT8, NC_ERR_DTYPE, "the model's projections are not W8A8");
+  NC_CHECK((codes_dev == nullptr) == (scales_dev == nullptr), NC_ERR_INVALID_ARGUMENT,
+           "give both buffers, or neither");
+  NC_CHECK(aligned(scales_dev, 4), NC_ERR_INVALID_ARGUMENT, "scales must be 4-byte aligned");
+  mm->dbg_codes = codes_dev;
+  mm->dbg_scales = scales_dev;
+  mm->dbg_codes_cap = codes_dev ? codes_capacity : 0;
+  mm->dbg_scales_cap = scales_dev ? scales_capacity : 0;
+  return NC_OK;
+}
+
 nc_status nc_profile_phases(nc_model* m, int enable) {
   NC_CHECK(m, NC_ERR_INVALID_ARGUMENT, "model is NULL");
   M(m)->prof_on = enable != 0;
@@ -156,9 +171,39 @@ nc_status nc_read_phase_profile(nc_model* m, void* stream, unsigned long long* o
   return NC_OK;
 }
 
+// The W8A8 form of a stage GEMV (NC_INT8): int8 rows with fp32 per-row
+// scales, the per-token activation codes formed in the kernel.
+static nc_status launch_stage_w8(Epi epi, const float* x, const void* gamma, float eps,
+                                 const void* W, const float* w_scale, const void* bias, int B,
+                                 int K, int N, float* y, int32_t* acc, cudaStream_t s,
+                                 const char* what) {
+  NC_CHECK(w_scale, NC_ERR_INVALID_ARGUMENT, "%s: NC_INT8 needs the per-row scales", what);
+  NC_CHECK(aligned16(W) && aligned(x, 4) && aligned(gamma, 2) && aligned(w_scale, 4) &&
+               aligned(bias, 2) && aligned(y, 4) && aligned(acc, 4),
+           NC_ERR_INVALID_ARGUMENT,
+           "%s: int8 W must be 16-byte aligned, fp32 and int32 pointers 4-byte, bf16 2-byte", what);
+  NC_CHECK(B >= 1 && B <= 16, NC_ERR_SHAPE, "batch %d outside [1, 16]", B);
+  const int bt = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;  // batch tile
+  NC_CHECK(K >= 16 && K % 16 == 0 && (size_t)bt * K <= 200000, NC_ERR_SHAPE,
+           "%s: NC_INT8 needs K a positive multiple of 16 with (B rounded up to a power of 2) "
+           "* K <= 200000", what);
+  NC_CHECK(N >= 1, NC_ERR_SHAPE, "N must be positive");
+  W8Args a{x, static_cast<const uint16_t*>(gamma), eps, static_cast<const int8_t*>(W), w_scale,
+           static_cast<const uint16_t*>(bias), B, K, N, y, nullptr, nullptr, acc};
+  return launch_result(launch_w8a8(epi, a, s), what);
+}
+
 nc_status nc_rmsnorm_gemv(const float* x, const void* gamma, float eps, const void* W,
-                          const void* bias, int B, int K, int N, float* y, void* stream) {
+                          nc_wtype wtype, const float* w_scale, const void* bias, int B, int K,
+                          int N, float* y, int32_t* acc_i32_debug, void* stream) {
   NC_CHECK(x && W && y, NC_ERR_INVALID_ARGUMENT, "null pointer");
+  NC_CHECK(wtype == NC_BF16 || wtype == NC_INT8, NC_ERR_DTYPE, "unknown weight type %d",
+           (int)wtype);
+  if (wtype == NC_INT8)
+    return launch_stage_w8(Epi::Store, x, gamma, eps, W, w_scale, bias, B, K, N, y,
+                           acc_i32_debug, S(stream), "nc_rmsnorm_gemv");
+  NC_CHECK(!w_scale && !acc_i32_debug, NC_ERR_INVALID_ARGUMENT,
+           "w_scale and acc_i32_debug apply to NC_INT8 weights only");
   NC_CHECK(aligned16(x) && aligned16(W), NC_ERR_INVALID_ARGUMENT, "x and W must be 16-byte aligned");
   NC_CHECK(aligned(gamma, 8) && aligned(bias, 2) && aligned(y, 4), NC_ERR_INVALID_ARGUMENT,
            "gamma must be 8-byte aligned, bias 2-byte and y 4-byte");
@@ -169,9 +214,15 @@ nc_status nc_rmsnorm_gemv(const float* x, const void* gamma, float eps, const vo
   return launch_result(launch_gemv(Epi::Store, a, S(stream)), "nc_rmsnorm_gemv");
 }
 
-nc_status nc_gemv_residual(const float* a_in, const void* W, int B, int K, int N, float* x,
-                           void* stream) {
+nc_status nc_gemv_residual(const float* a_in, const void* W, nc_wtype wtype, const float* w_scale,
+                           int B, int K, int N, float* x, void* stream) {
   NC_CHECK(a_in && W && x, NC_ERR_INVALID_ARGUMENT, "null pointer");
+  NC_CHECK(wtype == NC_BF16 || wtype == NC_INT8, NC_ERR_DTYPE, "unknown weight type %d",
+           (int)wtype);
+  if (wtype == NC_INT8)
+    return launch_stage_w8(Epi::Residual, a_in, nullptr, 0.f, W, w_scale, nullptr, B, K, N, x,
+                           nullptr, S(stream), "nc_gemv_residual");
+  NC_CHECK(!w_scale, NC_ERR_INVALID_ARGUMENT, "w_scale applies to NC_INT8 weights only");
   NC_CHECK(aligned16(a_in) && aligned16(W), NC_ERR_INVALID_ARGUMENT, "inputs must be 16-byte aligned");
   NC_CHECK(aligned(x, 4), NC_ERR_INVALID_ARGUMENT, "x must be 4-byte aligned");
   nc_status st = check_gemv_shape(B, K, N);
@@ -180,9 +231,16 @@ nc_status nc_gemv_residual(const float* a_in, const void* W, int B, int K, int N
   return launch_result(launch_gemv(Epi::Residual, a, S(stream)), "nc_gemv_residual");
 }
 
-nc_status nc_swiglu_gemv(const float* x, const void* gamma, float eps, const void* W_gu, int B,
-                         int K, int F, float* h, void* stream) {
+nc_status nc_swiglu_gemv(const float* x, const void* gamma, float eps, const void* W_gu,
+                         nc_wtype wtype, const float* s_gu, int B, int K, int F, float* h,
+                         void* stream) {
   NC_CHECK(x && W_gu && h, NC_ERR_INVALID_ARGUMENT, "null pointer");
+  NC_CHECK(wtype == NC_BF16 || wtype == NC_INT8, NC_ERR_DTYPE, "unknown weight type %d",
+           (int)wtype);
+  if (wtype == NC_INT8)
+    return launch_stage_w8(Epi::SwiGLU, x, gamma, eps, W_gu, s_gu, nullptr, B, K, F, h, nullptr,
+                           S(stream), "nc_swiglu_gemv");
+  NC_CHECK(!s_gu, NC_ERR_INVALID_ARGUMENT, "s_gu applies to NC_INT8 weights only");
   NC_CHECK(aligned16(x) && aligned16(W_gu), NC_ERR_INVALID_ARGUMENT, "inputs must be 16-byte aligned");
   NC_CHECK(aligned(gamma, 8) && aligned(h, 4), NC_ERR_INVALID_ARGUMENT,
            "gamma must be 8-byte aligned and h 4-byte");

@@ -169,7 +169,7 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     m->xw = W.take<uint64_t>(pb * H);
     m->qkvw = W.take<uint64_t>(pb * nqkv);
     m->aw = W.take<uint64_t>(pb * qd);
-    m->apart = W.take<float>((size_t)kPMaxBatch * kPMaxSplits * c.n_q_heads * (D + 2));
+    m->apart = W.take<float>((size_t)kPMaxBatch * kPMaxSplits * c.n_q_heads * (D + 4));
     m->atick = W.take<unsigned int>((size_t)c.n_layers * kPMaxBatch * Hkv);
     m->hw = W.take<uint64_t>(pb * F);
     m->pticket = W.take<unsigned int>(1);
@@ -375,6 +375,18 @@ nc_status validate_kv(const Model* m, int batch, const int32_t* positions_host,
   return NC_OK;
 }
 
+// The W8A8 diagnostic's layout for one step at `batch`: per layer the codes
+// of the four products [qkv: B x H][o: B x Hq D][gate|up: B x H][down: B x F]
+// and their scales [4][B].
+size_t dbg_codes_per_step(const Model* m, int batch) {
+  const nc_config& c = m->cfg;
+  return (size_t)c.n_layers * batch *
+         (2 * (size_t)c.hidden + (size_t)c.n_q_heads * c.head_dim + c.ffn);
+}
+size_t dbg_scales_per_step(const Model* m, int batch) {
+  return (size_t)m->cfg.n_layers * 4 * batch;
+}
+
 static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* positions,
                                  const KVView& kvv, int splits, cudaStream_t s) {
   const nc_config& c = m->cfg;
@@ -382,12 +394,24 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
   const int H = c.hidden, D = c.head_dim, F = c.ffn, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   const int nqkv = (Hq + 2 * Hkv) * D;
   const bool i8 = c.wtype == NC_INT8;
+  // the W8A8 diagnostic's slots of this layer (null when it is off)
+  int8_t* dq[4] = {nullptr, nullptr, nullptr, nullptr};
+  float* ds[4] = {nullptr, nullptr, nullptr, nullptr};
+  if (i8 && m->dbg_codes) {
+    const size_t per = (size_t)batch * (2 * (size_t)H + (size_t)Hq * D + F);
+    int8_t* base = m->dbg_codes + (size_t)layer * per;
+    dq[0] = base;
+    dq[1] = dq[0] + (size_t)batch * H;
+    dq[2] = dq[1] + (size_t)batch * Hq * D;
+    dq[3] = dq[2] + (size_t)batch * H;
+    for (int k = 0; k < 4; ++k) ds[k] = m->dbg_scales + ((size_t)layer * 4 + k) * batch;
+  }
   cudaError_t e;
   if (!i8) {
     e = launch_gemv(Epi::Store, {m->x, P.g_attn, c.rms_eps, P.w_qkv, P.b_qkv, batch, H, nqkv, m->qkv}, s);
   } else {
     W8Args a{m->x, P.g_attn, c.rms_eps, P.q_qkv, P.s_qkv, P.b_qkv, batch, H, nqkv, m->qkv,
-             nullptr, nullptr, nullptr};
+             dq[0], ds[0], nullptr};
     e = launch_w8a8(Epi::Store, a, s);
   }
   if (e) return e;
@@ -407,11 +431,11 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
       return e;
     return launch_gemv(Epi::Residual, {m->h, nullptr, 0.f, P.w_d, nullptr, batch, F, H, m->x}, s);
   }
-  W8Args o{m->attn, nullptr, 0.f, P.q_o, P.s_o, nullptr, batch, Hq * D, H, m->x, nullptr, nullptr, nullptr};
+  W8Args o{m->attn, nullptr, 0.f, P.q_o, P.s_o, nullptr, batch, Hq * D, H, m->x, dq[1], ds[1], nullptr};
   if ((e = launch_w8a8(Epi::Residual, o, s))) return e;
-  W8Args gu{m->x, P.g_mlp, c.rms_eps, P.q_gu, P.s_gu, nullptr, batch, H, F, m->h, nullptr, nullptr, nullptr};
+  W8Args gu{m->x, P.g_mlp, c.rms_eps, P.q_gu, P.s_gu, nullptr, batch, H, F, m->h, dq[2], ds[2], nullptr};
   if ((e = launch_w8a8(Epi::SwiGLU, gu, s))) return e;
-  W8Args dn{m->h, nullptr, 0.f, P.q_d, P.s_d, nullptr, batch, F, H, m->x, nullptr, nullptr, nullptr};
+  W8Args dn{m->h, nullptr, 0.f, P.q_d, P.s_d, nullptr, batch, F, H, m->x, dq[3], ds[3], nullptr};
   return launch_w8a8(Epi::Residual, dn, s);
 }
 
@@ -458,6 +482,12 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
   const int splits = attn_splits(batch, m->cfg.n_kv_heads, m->cfg.head_dim, kv->dtype == NC_KV_BF16,
                                  kv_capacity(*kv));
   const StepIO io{tokens, positions, logits, next, (flags & NC_STEP_ADVANCE) != 0};
+  if (m->dbg_codes) {
+    NC_CHECK(dbg_codes_per_step(m, batch) <= m->dbg_codes_cap &&
+                 dbg_scales_per_step(m, batch) <= m->dbg_scales_cap,
+             NC_ERR_CAPACITY, "the W8A8 diagnostic buffers are too small for batch %d", batch);
+    flags &= ~NC_STEP_GRAPH;  // the diagnostic runs the kernels directly
+  }
   cudaError_t e;
   if (use_persistent(m, batch, *kv, flags)) {
     e = enqueue_persistent(m, batch, tokens, positions, logits, next, io.advance, kvv, s);
@@ -535,6 +565,9 @@ nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t*
            "positions must be 4-byte aligned");
   nc_status st = validate_kv(m, batch, positions_host, kv);
   if (st) return st;
+  NC_CHECK(!m->dbg_codes || (dbg_codes_per_step(m, batch) <= m->dbg_codes_cap &&
+                             dbg_scales_per_step(m, batch) <= m->dbg_scales_cap),
+           NC_ERR_CAPACITY, "the W8A8 diagnostic buffers are too small for batch %d", batch);
   const KVView kvv = kv_view(m, *kv);
   const int splits = attn_splits(batch, m->cfg.n_kv_heads, m->cfg.head_dim, kv->dtype == NC_KV_BF16,
                                  kv_capacity(*kv));

@@ -51,6 +51,11 @@ struct Model {
   unsigned int *pticket = nullptr, *seq = nullptr;
   PLayer* players = nullptr;
   unsigned long long* prof = nullptr;  // phase profile [2 * (5L + 1) + 2]
+  // W8A8 diagnostic (nc_debug_w8a8_codes): caller-owned device buffers that
+  // receive every step's activation codes and scales, or null
+  int8_t* dbg_codes = nullptr;
+  float* dbg_scales = nullptr;
+  size_t dbg_codes_cap = 0, dbg_scales_cap = 0;
   bool prof_on = false;
   bool unhealthy = false;
   cudaStream_t cap_stream = nullptr;  // private stream used only for graph capture
@@ -81,5 +86,8 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
 bool use_persistent(const Model* m, int batch, const nc_kv_cache& kv, int flags);
 nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t* positions,
                         const int32_t* positions_host, const nc_kv_cache* kv, cudaStream_t s);
+// Codes and scales the W8A8 diagnostic holds for one step at this batch.
+size_t dbg_codes_per_step(const Model* m, int batch);
+size_t dbg_scales_per_step(const Model* m, int batch);
 
 }  // namespace nc

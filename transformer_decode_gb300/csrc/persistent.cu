@@ -33,6 +33,7 @@
 // The launch is cooperative: all CTAs must be resident together.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include "kernels.h"
 #include "persistent.h"
@@ -940,20 +941,18 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     consumer_sync();  // the scratch is reused by the next item
     return;
   }
-  // split partials [G][D + 2] = (m, l, o[D]) per head of this (b, g, split)
-  constexpr int DP = D + 2;
+  // split partials [G][DP] per head of this (b, g, split): o[D], then m, l
+  // (rows padded to a 16-byte multiple, so the merge can stage them with
+  // 16-byte asynchronous copies)
+  constexpr int DP = D + 4;
   float* const parts = a.apart + ((size_t)b * kPMaxSplits * Hq + (size_t)g * G) * DP;
   const size_t sstride = (size_t)Hq * DP;  // from one split's partials to the next
   float* const mine = parts + split * sstride;
   if (ct < npair) {
     const float inv = lrun[my_h] > 0.f ? 1.f / lrun[my_h] : 0.f;
-    mine[my_h * DP + 2 + 2 * my_d2] = acc0 * inv;
-    mine[my_h * DP + 3 + 2 * my_d2] = acc1 * inv;
+    *reinterpret_cast<float2*>(mine + my_h * DP + 2 * my_d2) = make_float2(acc0 * inv, acc1 * inv);
   }
-  if (ct < G) {
-    mine[ct * DP] = mrun[ct];
-    mine[ct * DP + 1] = lrun[ct];
-  }
+  if (ct < G) *reinterpret_cast<float2*>(mine + ct * DP + D) = make_float2(mrun[ct], lrun[ct]);
   __threadfence();  // each writer's partials are visible GPU-wide before the ticket
   consumer_sync();
   unsigned int* const tick = a.atick + ((size_t)layer * kPMaxBatch + b) * Hkv + g;
@@ -961,14 +960,22 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   consumer_sync();
   if (!S.merge) return;  // uniform: read after the barrier
   __threadfence();       // the other splits' partials, published before their tickets
-  float* coef = sc;      // [G][ns] merge weights (the score buffers are free now)
+  // (m, l) of every (split, head), one load each, all in flight together
+  float* ml = sc;                          // [ns][G][2]
+  float* coef = sc + 2 * kPMaxSplits * GM;  // [G][kPMaxSplits] merge weights
+  if (ct < ns * G) {
+    const int t = ct / G, h = ct % G;
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(parts + t * sstride + h * DP + D));
+    ml[2 * ct] = v.x;
+    ml[2 * ct + 1] = v.y;
+  }
+  consumer_sync();
   if (ct < G) {
     float M = -INFINITY;
-    for (int t = 0; t < ns; ++t) M = fmaxf(M, __ldcg(parts + t * sstride + ct * DP));
+    for (int t = 0; t < ns; ++t) M = fmaxf(M, ml[2 * (t * G + ct)]);
     float L = 0.f;
     for (int t = 0; t < ns; ++t) {
-      const float m = __ldcg(parts + t * sstride + ct * DP);
-      const float l = __ldcg(parts + t * sstride + ct * DP + 1);
+      const float m = ml[2 * (t * G + ct)], l = ml[2 * (t * G + ct) + 1];
       const float w = m == -INFINITY ? 0.f : expf(m - M) * l;
       coef[ct * kPMaxSplits + t] = w;
       L += w;
@@ -977,15 +984,42 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     for (int t = 0; t < ns; ++t)
       coef[ct * kPMaxSplits + t] = L > 0.f ? coef[ct * kPMaxSplits + t] / L : 0.f;
   }
-  consumer_sync();
-  for (int i = ct; i < G * D; i += kPConsumerThreads) {
-    const int h = i / D, d = i % D;
-    const float* src = parts + h * DP + 2 + d;
-    float o = 0.f;
-    for (int t = 0; t < ns; ++t) o = fmaf(coef[h * kPMaxSplits + t], __ldcg(src + t * sstride), o);
-    st_word(aout + i, o, ep_out);
+  // the splits' outputs, staged into the (idle) input-vector region in rounds
+  // of as many splits as it holds; every thread accumulates its elements
+  // over the splits in index order
+  float* stage = reinterpret_cast<float*>(smem + a.xs_offset);
+  const int per_split = G * DP;  // floats of one split's block
+  const int span = (a.attn_offset - a.xs_offset) / (per_split * 4);
+  constexpr int EPT = (8 * 128 + kPConsumerThreads - 1) / kPConsumerThreads;  // outputs a thread owns
+  float o[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) o[e] = 0.f;
+  for (int t0 = 0; t0 < ns; t0 += span) {
+    const int nt = min(span, ns - t0);
+    const int chunks = nt * (per_split / 4);
+    for (int c = ct; c < chunks; c += kPConsumerThreads) {
+      const int t = c / (per_split / 4), r = c % (per_split / 4);
+      cp_async16(stage + t * per_split + 4 * r, parts + (t0 + t) * sstride + 4 * r);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    consumer_sync();  // staged (and, in the first round, coef written)
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int i = ct + e * kPConsumerThreads;
+      if (i < G * D) {
+        const int h = i / D, d = i % D;
+        for (int t = 0; t < nt; ++t)
+          o[e] = fmaf(coef[h * kPMaxSplits + t0 + t], stage[t * per_split + h * DP + d], o[e]);
+      }
+    }
+    consumer_sync();  // the staging area is rewritten by the next round
   }
-  consumer_sync();  // coef and the scratch are reused by the next item
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int i = ct + e * kPConsumerThreads;
+    if (i < G * D) st_word(aout + i, o[e], ep_out);
+  }
 }
 
 // The tiles of one projection phase (see gemv_phase). MODE 0: batch 1, rows of
@@ -1421,9 +1455,36 @@ static size_t round128(size_t x) { return (x + 127) / 128 * 128; }
 static size_t attn_scratch_bytes(int D) {
   return sizeof(float) * (8 * D + 2 * D + 2 * 8 * kAttnMaxChunk + 3 * 8);
 }
-static size_t persistent_fixed_smem(int H, int qd, int F, int D, int BT) {
+// The longest row a ring slot must hold: a gate|up pair (2 rows of H), a
+// down row (F), an o-proj row (Hq D) or a QKV / LM-head row (H), bf16.
+static size_t max_row_bytes(int H, int qd, int F) {
+  size_t m = (size_t)4 * H;
+  if ((size_t)2 * F > m) m = (size_t)2 * F;
+  if ((size_t)2 * qd > m) m = (size_t)2 * qd;
+  return m;
+}
+
+// Ring slots (NC_PERSIST_SLOTS in the environment, read once; kPSlots by
+// default): the same shared memory cut into more, smaller tiles.
+static int persist_slots() {
+  static const int n = [] {
+    const char* e = getenv("NC_PERSIST_SLOTS");
+    int v = e ? atoi(e) : kPSlots;
+    return v < kPSlots ? kPSlots : (v > kMaxSlots ? kMaxSlots : v);
+  }();
+  return n;
+}
+
+// The input-vector region: BT rows of the longest input, and at least one
+// split's partial block (G heads of D + 4 floats), which the attention merge
+// stages there.
+static size_t xs_bytes(int H, int qd, int F, int D, int G, int BT) {
+  const size_t v = (size_t)BT * kmax_of(H, qd, F) * 4, p = (size_t)G * (D + 4) * 4;
+  return v > p ? v : p;
+}
+static size_t persistent_fixed_smem(int H, int qd, int F, int D, int G, int BT) {
   size_t off = round128(sizeof(PShared));
-  off = round128(off + (size_t)BT * kmax_of(H, qd, F) * 4);
+  off = round128(off + xs_bytes(H, qd, F, D, G, BT));
   off += attn_scratch_bytes(D);
   return round128(off);
 }
@@ -1454,18 +1515,26 @@ static cudaError_t launch_b(const PersistArgs& a, size_t smem, cudaStream_t s) {
 }
 
 cudaError_t launch_persistent(PersistArgs a, cudaStream_t s) {
-  const int qd = a.Hq * a.D, BT = bt_of(a.B);
-  const size_t fixed = persistent_fixed_smem(a.H, qd, a.F, a.D, BT);
+  const int qd = a.Hq * a.D, BT = bt_of(a.B), G = a.Hq / a.Hkv;
+  const size_t fixed = persistent_fixed_smem(a.H, qd, a.F, a.D, G, BT);
   const size_t pshared = round128(sizeof(PShared));
   a.xs_offset = (int)pshared;
-  a.attn_offset = (int)round128(pshared + (size_t)BT * kmax_of(a.H, qd, a.F) * 4);
+  a.attn_offset = (int)round128(pshared + xs_bytes(a.H, qd, a.F, a.D, G, BT));
   a.ring_offset = (int)fixed;
   a.attn_bytes = (int)attn_scratch_bytes(a.D);
   const size_t avail = (size_t)max_smem_optin();
   if (fixed + (size_t)kPMinSlotBytes * kPSlots > avail) return cudaErrorInvalidConfiguration;
-  // the rest of shared memory as kPSlots equal slots (multiples of 128 bytes)
-  a.nslots = kPSlots;
-  a.slot_bytes = (int)(((avail - fixed) / kPSlots) / 128 * 128);
+  // the rest of shared memory as equal slots (multiples of 128 bytes), each
+  // holding at least one row of every matrix: NC_PERSIST_SLOTS slots
+  // (default kPSlots), fewer when a row would not fit
+  const size_t row_max = max_row_bytes(a.H, qd, a.F);
+  int ns = persist_slots();
+  while (ns > kPSlots && ((avail - fixed) / ns / 128 * 128 < row_max ||
+                          (avail - fixed) / ns < (size_t)kPMinSlotBytes))
+    --ns;
+  a.nslots = ns;
+  a.slot_bytes = (int)(((avail - fixed) / ns) / 128 * 128);
+  if ((size_t)a.slot_bytes < row_max) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + (size_t)a.nslots * a.slot_bytes;
   if (BT == 1) return launch_b<1>(a, smem, s);
   if (BT == 2) return launch_b<2>(a, smem, s);
@@ -1483,8 +1552,10 @@ bool persistent_supported(int L, int H, int qd, int F, int D, int G, int B) {
   const int grid = num_sms(), half = grid - grid / 2;
   const long long nqkv = (long long)qd + 2LL * (qd / G);
   if ((H + half - 1) / half > kPMaxRows || (nqkv + grid - 1) / grid > kPMaxRows) return false;
-  const size_t fixed = persistent_fixed_smem(H, qd, F, D, bt_of(B));
-  return fixed + (size_t)kPMinSlotBytes * kPSlots <= (size_t)max_smem_optin();
+  const size_t fixed = persistent_fixed_smem(H, qd, F, D, G, bt_of(B));
+  if (fixed + (size_t)kPMinSlotBytes * kPSlots > (size_t)max_smem_optin()) return false;
+  // every row of every matrix fits one slot
+  return ((size_t)max_smem_optin() - fixed) / kPSlots / 128 * 128 >= max_row_bytes(H, qd, F);
 }
 
 }  // namespace nc

@@ -41,7 +41,7 @@ struct PersistArgs {
   uint64_t* xw;    // [kPMaxBatch][H] residual stream
   uint64_t* qkvw;  // [kPMaxBatch][nqkv]
   uint64_t* aw;    // [kPMaxBatch][Hq D] attention output (merged over the position splits)
-  float* apart;    // [kPMaxBatch][kPMaxSplits][Hq][D + 2] split partials (m, l, o = acc / l)
+  float* apart;    // [kPMaxBatch][kPMaxSplits][Hq][D + 4] split partials (o = acc / l, m, l)
   unsigned int* atick;  // [L][kPMaxBatch][Hkv] split arrivals, zeroed by the step's last CTA
   uint64_t* hw;    // [kPMaxBatch][F] SiLU(gate) * up
   unsigned long long* am_part;  // [B][grid] arg-max partial keys

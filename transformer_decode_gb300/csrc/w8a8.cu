@@ -169,13 +169,15 @@ __global__ void __launch_bounds__(kW8Threads) k_w8a8(W8Args a) {
         if constexpr (R == 2) a.acc_out[(size_t)lane * R * a.N + a.N + n] = v[1];
       }
       float* yp = a.y + (size_t)lane * a.N + n;
-      const float y0 = (float)v[0] * (a.w_scale[n] * s);
+      // each product and the bias add rounded on its own (no contraction), so
+      // the dequantised value is the IEEE result of float(acc) * (s_w * s_x) + b
+      const float y0 = __fmul_rn(__int2float_rn(v[0]), __fmul_rn(a.w_scale[n], s));
       if constexpr (EPI == Epi::Store) {
-        *yp = a.bias ? y0 + bf16_to_f32(a.bias[n]) : y0;
+        *yp = a.bias ? __fadd_rn(y0, bf16_to_f32(a.bias[n])) : y0;
       } else if constexpr (EPI == Epi::Residual) {
-        *yp = *yp + y0;
+        *yp = __fadd_rn(*yp, y0);
       } else {
-        const float y1 = (float)v[R - 1] * (a.w_scale[a.N + n] * s);
+        const float y1 = __fmul_rn(__int2float_rn(v[R - 1]), __fmul_rn(a.w_scale[a.N + n], s));
         *yp = silu_mul8(y0, y1);
       }
     }

@@ -33,6 +33,7 @@ EXPORTS = [
     "nc_rope_qkv", "nc_attn_decode", "nc_lm_head_argmax", "nc_quantize_weight", "nc_w8a8_gemv",
     "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile", "nc_decode_path",
     "nc_sample", "nc_sample_scratch_bytes", "nc_attn_decode_static_status",
+    "nc_debug_w8a8_codes",
 ]
 
 
@@ -106,9 +107,9 @@ def _declare(L):
     L.nc_decode_step.argtypes = [vp, i, vp, vp, vp, C.POINTER(KVStruct), vp, vp, i, vp]
     L.nc_block_forward.argtypes = [vp, i, i, vp, vp, vp, C.POINTER(KVStruct), vp]
     L.nc_get_device_status.argtypes = [vp, vp, C.POINTER(C.c_int)]
-    L.nc_rmsnorm_gemv.argtypes = [vp, vp, f, vp, vp, i, i, i, vp, vp]
-    L.nc_gemv_residual.argtypes = [vp, vp, i, i, i, vp, vp]
-    L.nc_swiglu_gemv.argtypes = [vp, vp, f, vp, i, i, i, vp, vp]
+    L.nc_rmsnorm_gemv.argtypes = [vp, vp, f, vp, i, vp, vp, i, i, i, vp, vp, vp]
+    L.nc_gemv_residual.argtypes = [vp, vp, i, vp, i, i, i, vp, vp]
+    L.nc_swiglu_gemv.argtypes = [vp, vp, f, vp, i, vp, i, i, i, vp, vp]
     L.nc_rope_qkv.argtypes = [vp, i, i, vp, vp, vp, vp, C.POINTER(KVStruct), vp]
     L.nc_attn_decode.argtypes = [vp, i, i, vp, vp, vp, C.POINTER(KVStruct), vp, vp]
     L.nc_lm_head_argmax.argtypes = [vp, vp, vp, f, vp, i, i, i, vp, vp, vp]
@@ -116,6 +117,7 @@ def _declare(L):
     L.nc_w8a8_gemv.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
     L.nc_attn_decode_static.argtypes = [i, i, i, i, i, i, vp, vp, vp, C.POINTER(KVStruct), vp, vp]
     L.nc_attn_decode_static_status.argtypes = [vp, C.POINTER(i)]
+    L.nc_debug_w8a8_codes.argtypes = [vp, vp, C.c_size_t, vp, C.c_size_t]
     L.nc_profile_phases.argtypes = [vp, i]
     L.nc_decode_path.argtypes = [vp, i, vp, i, C.POINTER(i)]
     L.nc_read_phase_profile.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), i, C.POINTER(i)]
@@ -160,27 +162,45 @@ def _host_i32(a):
 
 
 # ------------------------------------------------------------------ stage entry points
-def rmsnorm_gemv(x, gamma, eps, W, bias, y, stream=None):
+def _weights(W, w_scale, rows, K, name):
+    """(pointer, weight type, scale pointer) of a stage GEMV's weights: bf16
+    rows, or int8 rows with their fp32 per-row scales."""
+    if W.dtype == torch.int8:
+        if w_scale is None:
+            raise TypeError(f"int8 {name} needs its per-row scales")
+        return (_ptr(W, torch.int8, name, rows * K), NC_INT8,
+                _ptr(w_scale, torch.float32, "w_scale", rows))
+    if w_scale is not None:
+        raise TypeError(f"scales apply to int8 {name} only")
+    return _ptr(W, torch.bfloat16, name, rows * K), NC_BF16, None
+
+
+def rmsnorm_gemv(x, gamma, eps, W, bias, y, w_scale=None, acc=None, stream=None):
+    """nc_rmsnorm_gemv. W bf16, or int8 with w_scale (W8A8); acc [B, N] int32
+    (int8 only) receives the accumulators."""
     B, K = x.shape
     N = W.shape[0]
+    wp, wt, sp = _weights(W, w_scale, N, K, "W")
     _check(load().nc_rmsnorm_gemv(_ptr(x, torch.float32, "x"), _ptr(gamma, torch.bfloat16, "gamma"),
-                                  float(eps), _ptr(W, torch.bfloat16, "W", N * K),
-                                  _ptr(bias, torch.bfloat16, "bias"), B, K, N,
-                                  _ptr(y, torch.float32, "y", B * N), _stream(stream)))
+                                  float(eps), wp, wt, sp, _ptr(bias, torch.bfloat16, "bias"), B, K,
+                                  N, _ptr(y, torch.float32, "y", B * N),
+                                  _ptr(acc, torch.int32, "acc", B * N), _stream(stream)))
 
 
-def gemv_residual(a, W, x, stream=None):
+def gemv_residual(a, W, x, w_scale=None, stream=None):
     B, K = a.shape
     N = W.shape[0]
-    _check(load().nc_gemv_residual(_ptr(a, torch.float32, "a"), _ptr(W, torch.bfloat16, "W", N * K),
-                                   B, K, N, _ptr(x, torch.float32, "x", B * N), _stream(stream)))
+    wp, wt, sp = _weights(W, w_scale, N, K, "W")
+    _check(load().nc_gemv_residual(_ptr(a, torch.float32, "a"), wp, wt, sp, B, K, N,
+                                   _ptr(x, torch.float32, "x", B * N), _stream(stream)))
 
 
-def swiglu_gemv(x, gamma, eps, W_gu, h, stream=None):
+def swiglu_gemv(x, gamma, eps, W_gu, h, s_gu=None, stream=None):
     B, K = x.shape
     F = W_gu.shape[0] // 2
+    wp, wt, sp = _weights(W_gu, s_gu, 2 * F, K, "W_gu")
     _check(load().nc_swiglu_gemv(_ptr(x, torch.float32, "x"), _ptr(gamma, torch.bfloat16, "gamma"),
-                                 float(eps), _ptr(W_gu, torch.bfloat16, "W_gu", 2 * F * K), B, K, F,
+                                 float(eps), wp, wt, sp, B, K, F,
                                  _ptr(h, torch.float32, "h", B * F), _stream(stream)))
 
 
@@ -458,6 +478,15 @@ class Model:
                                         _ptr(logits, torch.float32, "logits", B * V),
                                         _ptr(next_tokens, torch.int32, "next_tokens"),
                                         _stream(stream)))
+
+    def debug_w8a8_codes(self, codes=None, scales=None):
+        """nc_debug_w8a8_codes: while set, every step writes its W8A8
+        activation codes (int8) and scales (fp32) to these device tensors
+        (layout in include/nc.h); None, None turns it off."""
+        self._dbg = (codes, scales)  # keep them alive while set
+        _check(load().nc_debug_w8a8_codes(
+            self.handle, _ptr(codes, torch.int8, "codes"), 0 if codes is None else codes.numel(),
+            _ptr(scales, torch.float32, "scales"), 0 if scales is None else scales.numel()))
 
     def profile_phases(self, enable=True):
         _check(load().nc_profile_phases(self.handle, int(enable)))
