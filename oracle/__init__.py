@@ -454,11 +454,18 @@ class OracleModel:
             raise ValueError("oracle decode step rejected its input (position or NaN)")
         return (logits, nxt, hid) if hidden else (logits, nxt)
 
-    def block_decode(self, layer, kv, b, pos, x, prec="f32"):
+    def block_decode(self, layer, kv, b, pos, x, prec="f32", trace=None):
+        """One block for sequence b at position pos (x updated and returned);
+        trace as in decode_step (the block's q, k, v, o, gate, up, down
+        products and its K/V stores)."""
         dt, ct = _real(prec)
         x = _np(x, dt).copy()
-        getattr(lib(), f"orc_block_decode_{prec}")(C.byref(self.struct), layer,
-                                                  C.byref(kv.struct), b, pos, _p(x, ct))
+        self.struct.trace = None if trace is None else C.addressof(trace.struct)
+        try:
+            getattr(lib(), f"orc_block_decode_{prec}")(C.byref(self.struct), layer,
+                                                      C.byref(kv.struct), b, pos, _p(x, ct))
+        finally:
+            self.struct.trace = None
         return x
 
     def forward_chunk(self, kv, b, tokens, start_pos, prec="f32"):

@@ -134,6 +134,74 @@ def test_w8a8_gemv_bit_exact_accumulators(B, K, N):
         assert rel_l2(f32(y[r]), ref) < 1e-6
 
 
+@pytest.mark.parametrize("B,K,N", [(1, 896, 1152), (4, 896, 77), (16, 4864, 33)])
+def test_typed_stage_gemvs_w8a8_bit_exact(B, K, N):
+    """The boundary's stage GEMVs with NC_INT8 weights (nc_rmsnorm_gemv with
+    bias and int32 accumulators, nc_gemv_residual, nc_swiglu_gemv), on
+    identical fp32 input (no norm): the accumulators equal the oracle's int64
+    products of its own codes, and the bias and residual epilogues, each IEEE
+    operation rounded on its own, equal the oracle's outputs bit for bit. The
+    SwiGLU epilogue applies exp, whose last bit the device's and the host's
+    libraries may round apart: within 4 ulp of the oracle's composition."""
+    x = _x(B, K, 60 + N)
+    W = synth.normal_bf16(0, 560 + N, (N, K), 0.02)
+    qo, so = oracle.quantize_weight(W)
+    bias = synth.normal_bf16(0, 561, (N,), 0.02)
+    Wq, sw = torch.from_numpy(qo).cuda(), torch.from_numpy(so).cuda()
+    y = torch.empty(B, N, device="cuda")
+    acc = torch.empty(B, N, dtype=torch.int32, device="cuda")
+    nc.rmsnorm_gemv(x.cuda(), None, 0.0, Wq, bias.cuda(), y, w_scale=sw, acc=acc)
+    r0 = _x(B, N, 70 + N)
+    res = r0.cuda()
+    nc.gemv_residual(x.cuda(), Wq, res, w_scale=sw)
+    Wg = synth.normal_bf16(0, 562 + N, (2 * N, K), 0.02)
+    qg, sg = oracle.quantize_weight(Wg)
+    h = torch.empty(B, N, device="cuda")
+    nc.swiglu_gemv(x.cuda(), None, 0.0, torch.from_numpy(qg).cuda(), h,
+                   s_gu=torch.from_numpy(sg).cuda())
+    torch.cuda.synchronize()
+    for r in range(B):
+        xq_o, _ = oracle.quantize_row(x[r].numpy())
+        assert np.array_equal(acc[r].cpu().numpy(), oracle.matvec_i8(qo, xq_o))
+        ref = oracle.linear_w8a8(qo, so, bias, x[r].numpy())
+        assert np.array_equal(f32(y[r]).view(np.uint32), ref.view(np.uint32))
+        lin = oracle.linear_w8a8(qo, so, None, x[r].numpy())
+        want = (r0[r].numpy() + lin).astype(np.float32)
+        assert np.array_equal(f32(res[r]).view(np.uint32), want.view(np.uint32))
+        gu = oracle.linear_w8a8(qg, sg, None, x[r].numpy())
+        hs = np.array([np.float32(oracle.silu(float(g))) * u for g, u in zip(gu[:N], gu[N:])],
+                      np.float32)
+        got = f32(h[r])
+        assert np.all(np.abs(got - hs) <= 4 * np.spacing(np.abs(hs).astype(np.float32))), \
+            np.abs(got - hs).max()
+
+
+def test_typed_stage_gemv_int8_codes_near_boundary_only():
+    """With the RMSNorm in the prologue the normed input is formed on each
+    side by its own fp32 sums; the activation codes then equal the oracle's
+    except where the oracle's quotient lies within CODE_BOUNDARY_TOL of a .5
+    boundary, where neighbouring codes are both correct."""
+    B, K, N = 4, 896, 64
+    x = _x(B, K, 75)
+    gamma = synth.normal_bf16(0, 571, (K,), 0.02, 1.0)
+    W = synth.normal_bf16(0, 572, (N, K), 0.02)
+    qo, so = oracle.quantize_weight(W)
+    y = torch.empty(B, N, device="cuda")
+    xq = torch.empty(B, K, dtype=torch.int8, device="cuda")
+    nc.w8a8_gemv(x.cuda(), gamma.cuda(), 1e-6, torch.from_numpy(qo).cuda(),
+                 torch.from_numpy(so).cuda(), None, y, xq)
+    torch.cuda.synchronize()
+    for r in range(B):
+        xn = oracle.rmsnorm(x[r].numpy(), gamma, 1e-6)
+        own, s = oracle.quantize_row(xn)
+        got = xq[r].cpu().numpy()
+        d = np.nonzero(own != got)[0]
+        if d.size:
+            assert np.all(np.abs(own[d].astype(int) - got[d].astype(int)) == 1)
+            q = np.abs(xn[d].astype(np.float64) / float(s))
+            assert np.all(np.abs(q - np.floor(q) - 0.5) <= 2.0 ** -10)
+
+
 def test_w8a8_gemv_normed_and_zero_input():
     B, K, N = 2, 896, 200
     x = _x(B, K, 55)

@@ -735,7 +735,8 @@ __device__ __forceinline__ float2 kv_smem2(const char* base, int idx) {
 template <int D, bool KV16>
 __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int split, int ns,
                                             int p0, int p1, int layer, uint32_t ep_qkv,
-                                            uint32_t ep_out, int nslots, RingPos& rp, Spin& sp) {
+                                            uint32_t ep_out, int nslots, RingPos& rp, Spin& sp,
+                                            unsigned long long* prof_in) {
   // shared-memory pointers are derived from the dynamic shared array here, so
   // the compiler addresses them as shared, not generic
   extern __shared__ __align__(128) char smem[];
@@ -821,6 +822,7 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     }
   }
   consumer_sync();
+  if (prof_in) *prof_in = global_timer();  // the phase input (q, k, v) is in
   // the new position opens the running state: m = its score, l = 1, acc = v
   const float scale = 1.f / sqrtf((float)D);
   for (int h = warp; h < G; h += kPConsumerWarps) {
@@ -1024,7 +1026,7 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
 
 // The tiles of one projection phase (see gemv_phase). MODE 0: batch 1, rows of
 // at most 1024 (input in registers); 1: batch 1, longer rows (k segments
-// across warps); 2: batch > 1. Inlined: a call here would save and restore
+// across warps); 3: batch 1, longer rows, whole rows per warp; 2: batch > 1. Inlined: a call here would save and restore
 // the live registers of all 352 consumer threads through local memory, which
 // with ~28 KB of L1 next to the ring spills to L2 and costs a round trip.
 template <int BT, int MODE>
@@ -1081,7 +1083,43 @@ __device__ __forceinline__ void gemv_tiles(const PersistArgs& a, const Rows& rin
     //    all of them) and the partials are summed across warps;
     //  batch > 1: units are cut into KS segments as needed, the input is
     //    read from shared memory.
-    if constexpr (BT == 1) {
+    if constexpr (BT == 1 && MODE == 3) {
+      // unit u of the phase (a row, or a gate|up pair) belongs to warp u % W:
+      // the warp reduces its units of this tile over the whole k range
+      // against the input in shared memory, one lane per 16-byte chunk, with
+      // no barrier and no cross-warp sum; units of later tiles keep the other
+      // warps busy meanwhile
+      const int first = (cw - (row - r.r0) % kPConsumerWarps + kPConsumerWarps) % kPConsumerWarps;
+      for (int i = first; i < n; i += kPConsumerWarps) {
+        const uint16_t* w0 = tile + (size_t)i * K;
+        // four chunks per lane in flight, each with its own partial sums
+        float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+        const auto chunk = [&](int cc, float& gs, float& us) {
+          float xb[8];
+          const float4 p0 = *reinterpret_cast<const float4*>(xs + cc * 4);
+          const float4 p1 = *reinterpret_cast<const float4*>(xs + K / 2 + cc * 4);
+          xb[0] = p0.x; xb[1] = p0.y; xb[2] = p0.z; xb[3] = p0.w;
+          xb[4] = p1.x; xb[5] = p1.y; xb[6] = p1.z; xb[7] = p1.w;
+          gs += dot8r(*reinterpret_cast<const uint4*>(w0 + cc * 8), xb);
+          if (two == 2) us += dot8r(*reinterpret_cast<const uint4*>(w0 + ms + cc * 8), xb);
+        };
+        int c = lane;
+        for (; c + 3 * kWarp < C; c += 4 * kWarp) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) chunk(c + q * kWarp, g[q], u[q]);
+          compiler_fence();
+        }
+        for (; c < C; c += kWarp) chunk(c, g[0], u[0]);
+        float v[2] = {(g[0] + g[1]) + (g[2] + g[3]), (u[0] + u[1]) + (u[2] + u[3])};
+        warp_sum_many<2>(v);  // value i in lane 16 i
+        const float vup = __shfl_sync(0xFFFFFFFFu, v[0], 16);
+        if (lane == 0 && nb > 0)
+          tile_epilogue<BT>(S, kind, po, r.r0, row + i, 0, v[0], vup, ep, best, sp);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[rp.s]);  // this warp is done with the slot
+      rp.next(nslots);
+    } else if constexpr (BT == 1) {
       if (xreg) {
         const int U = cw < n ? (n - cw + kPConsumerWarps - 1) / kPConsumerWarps : 0;
         float v[2 * kUnitsPerWarp];
@@ -1280,7 +1318,12 @@ __device__ __forceinline__ void gemv_phase(const PersistArgs& a, int ph, uint32_
   po.logits = a.logits;
   po.stride = kind == kQKV ? a.nqkv : (kind == kGU ? a.F : (kind == kHEAD ? a.V : a.H));
   if constexpr (BT == 1) {
+    // rows of at most 1024: input in registers; longer rows: whole rows per
+    // warp when the phase gives every warp at least two units, else the k
+    // range split over the warps (a few long rows on the latency chain)
     if (K / 8 <= kXReg * kWarp) gemv_tiles<1, 0>(a, r, po, kind, ep, rp_io, kb_io, best_io, sp);
+    else if (r.r1 - r.r0 >= 2 * kPConsumerWarps)
+      gemv_tiles<1, 3>(a, r, po, kind, ep, rp_io, kb_io, best_io, sp);
     else gemv_tiles<1, 1>(a, r, po, kind, ep, rp_io, kb_io, best_io, sp);
   } else {
     gemv_tiles<BT, 2>(a, r, po, kind, ep, rp_io, kb_io, best_io, sp);
@@ -1361,15 +1404,17 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       const int kind = ph == kPhasesPerLayer * L ? kHEAD : ph % kPhasesPerLayer;
       const uint32_t ep = epoch_of(seq, ph);
       if (kind == kATTN) {
+        bool first = true;
         for (int it = blockIdx.x; it < S.item0[kPMaxBatch]; it += gridDim.x) {
           const AttnItem t = attn_item_of(S, a.Hkv, it);
           const int np = cached_positions(a, t.b, S.pos[t.b]);
           const int p0 = (int)(((long long)t.sp * np) / t.ns);
           const int p1 = (int)(((long long)(t.sp + 1) * np) / t.ns);
           attention_item<D, KV16>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, epoch_of(seq, ph - 1),
-                                  ep, nslots, rp, sp);
+                                  ep, nslots, rp, sp, first && prof ? prof + 2 * ph + 1 : nullptr);
+          first = false;
         }
-        if (prof) prof[2 * ph + 1] = global_timer();
+        if (prof && first) prof[2 * ph + 1] = global_timer();  // a CTA with no item
         continue;
       }
       gemv_phase<BT>(a, ph, seq, rp, kb, best, prof, sp);
