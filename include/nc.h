@@ -320,6 +320,19 @@ nc_status nc_w8a8_gemv(const float* x, const void* gamma, float eps, const int8_
                        const float* w_scale, const void* bias, int B, int K, int N, float* y,
                        int8_t* xq_out, float* sx_out, int32_t* acc_out, void* stream);
 
+/* The same product with activations quantised per block of 32 consecutive
+ * values instead of per token (nanoinfer, INT8 activation section: "one per
+ * 32", so an outlier widens only its own block): sx[b, j] = amax of block j
+ * of xn[b] / 127, xq = clamp(round_half_away(xn / sx), -127, 127);
+ * acc[b, n, j] = sum over block j of Wq[n, k] * xq[b, k] in int32;
+ * y[b, n] = sum_j float(acc[b, n, j]) * (w_scale[n] * sx[b, j]) (+ bias[n]).
+ * B in [1, 8], K a multiple of 32. The optional outputs expose xq [B, K] int8,
+ * sx [B, K / 32] fp32 and acc [B, N, K / 32] int32 for bit-exact checks.
+ * Errors as for nc_w8a8_gemv. */
+nc_status nc_w8a8_gemv_b32(const float* x, const void* gamma, float eps, const int8_t* Wq,
+                           const float* w_scale, const void* bias, int B, int K, int N, float* y,
+                           int8_t* xq_out, float* sx_out, int32_t* acc_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

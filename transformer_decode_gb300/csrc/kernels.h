@@ -124,6 +124,23 @@ cudaError_t launch_w8a8(Epi epi, const W8Args& a, cudaStream_t s);
 cudaError_t launch_quantize_weight(const uint16_t* W, int N, int K, int8_t* q, float* scale,
                                    cudaStream_t s);
 
+// W8A8 with activations quantised in blocks of 32 (w8a8_blocks.cu)
+struct W8BArgs {
+  const float* x;
+  const uint16_t* gamma;
+  float eps;
+  const int8_t* Wq;       // [N, K]
+  const float* w_scale;   // [N]
+  const uint16_t* bias;   // [N] or null
+  int B, K, N;
+  float* y;               // [B, N]
+  int8_t* xq_out;         // [B, K] or null
+  float* sx_out;          // [B, K / 32] or null
+  int32_t* acc_out;       // [B, N, K / 32] or null
+};
+size_t w8a8_b32_smem_bytes(int B, int K);
+cudaError_t launch_w8a8_b32(const W8BArgs& a, cudaStream_t s);
+
 // ------------------------------------------------------------ sampling
 // Scratch of nc_sample: per row five arrays of V rounded up to 64 words.
 size_t sample_scratch_bytes(int B, int V);

@@ -32,7 +32,7 @@ EXPORTS = [
     "nc_get_device_status", "nc_rmsnorm_gemv", "nc_gemv_residual", "nc_swiglu_gemv",
     "nc_rope_qkv", "nc_attn_decode", "nc_lm_head_argmax", "nc_quantize_weight", "nc_w8a8_gemv",
     "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile", "nc_decode_path",
-    "nc_sample", "nc_sample_scratch_bytes",
+    "nc_sample", "nc_sample_scratch_bytes", "nc_w8a8_gemv_b32",
 ]
 
 
@@ -120,6 +120,7 @@ def _declare(L):
     L.nc_read_phase_profile.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), i, C.POINTER(i)]
     L.nc_sample.argtypes = [vp, i, i, f, i, f, vp, vp, vp, vp, C.c_size_t, vp]
     L.nc_sample_scratch_bytes.argtypes = [i, i]
+    L.nc_w8a8_gemv_b32.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
     for n in EXPORTS:
         if n not in ("nc_status_string", "nc_last_error_message", "nc_sample_scratch_bytes"):
             getattr(L, n).restype = C.c_int
@@ -201,6 +202,19 @@ def w8a8_gemv(x, gamma, eps, Wq, w_scale, bias, y, xq_out=None, sx_out=None, acc
                                _ptr(y, torch.float32, "y", B * N),
                                _ptr(xq_out, torch.int8, "xq_out"), _ptr(sx_out, torch.float32, "sx_out"),
                                _ptr(acc_out, torch.int32, "acc_out"), _stream(stream)))
+
+
+def w8a8_gemv_b32(x, gamma, eps, Wq, w_scale, bias, y, xq_out=None, sx_out=None, acc_out=None,
+                  stream=None):
+    """nc_w8a8_gemv_b32: the W8A8 product with activations in blocks of 32."""
+    B, K = x.shape
+    N = Wq.shape[0]
+    _check(load().nc_w8a8_gemv_b32(
+        _ptr(x, torch.float32, "x"), _ptr(gamma, torch.bfloat16, "gamma"), float(eps),
+        _ptr(Wq, torch.int8, "Wq", N * K), _ptr(w_scale, torch.float32, "w_scale", N),
+        _ptr(bias, torch.bfloat16, "bias"), B, K, N, _ptr(y, torch.float32, "y", B * N),
+        _ptr(xq_out, torch.int8, "xq_out"), _ptr(sx_out, torch.float32, "sx_out"),
+        _ptr(acc_out, torch.int32, "acc_out"), _stream(stream)))
 
 
 def attn_decode_static(shape, layer, q, positions, positions_host, kv, out, stream=None):
