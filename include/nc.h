@@ -50,7 +50,13 @@ typedef enum {
   NC_ERR_UNSUPPORTED = 9
 } nc_status;
 
-typedef enum { NC_BF16 = 0, NC_INT8 = 1 } nc_wtype;
+/* Weight storage. NC_INT8: the seven projections int8 per output row,
+ * activations quantised per token (nanoinfer "Quantization"). NC_INT8_B32:
+ * the same projections with activations quantised per block of 32 values,
+ * and the embedding stored int8 per row too, which is also the tied head
+ * (nanoinfer, INT8 activation section and its "INT8 + embeddings" level);
+ * needs tie_embeddings and hidden, ffn, n_q_heads * head_dim multiples of 32. */
+typedef enum { NC_BF16 = 0, NC_INT8 = 1, NC_INT8_B32 = 2 } nc_wtype;
 
 /* Hyperparameters. head_dim must be 64 or 128; n_q_heads a multiple of
  * n_kv_heads with group <= 8; hidden, ffn, n_q_heads*head_dim multiples of 8. */

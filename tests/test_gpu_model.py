@@ -98,7 +98,8 @@ def _greedy_compare(shape, wd, wc, prompt, steps, batch=1, past=None, paged=Fals
     that sits within that distance of a rounding boundary flips in the twins
     as it may on the GPU, and with random-init weights one such flip moves
     the logits by about 1e-2 (rel-L2)."""
-    om = oracle.OracleModel(shape, wc, w8a8=w8a8)
+    om = oracle.OracleModel(shape, wc, w8a8=bool(w8a8), act_block=32 if w8a8 == "b32" else 0,
+                            int8_embed=w8a8 == "b32")
     past = past or [0] * batch
     n_total = len(prompt[0]) + steps if prompt is not None else steps
     max_ctx = max(past) + n_total + 1
@@ -231,6 +232,18 @@ def test_decode_0p5b_w8a8_past512():
     worst = _greedy_compare(shape, wd, wc, None, steps=8, past=[512], w8a8=True,
                             derived_gate=True, noise_twins=2)
     print(f"0.5B W8A8: worst logit rel-L2 {worst:.3e}")
+
+
+@pytest.mark.parametrize("shape,past,steps", [(synth.TINY, 0, 12),
+                                               (synth.QWEN2_0P5B, 512, 8)])
+def test_decode_w8a8_b32(shape, past, steps):
+    """W8A8 with activations in blocks of 32 and the int8 embedding as the
+    tied head (NC_INT8_B32) against the oracle's same mode, under the derived
+    gate of the per-token W8A8 test."""
+    wd, wc = weights_both(shape)
+    worst = _greedy_compare(shape, wd, wc, None, steps=steps, past=[past], w8a8="b32",
+                            derived_gate=True, noise_twins=2)
+    print(f"W8A8 blocks of 32 ({shape.hidden}): worst logit rel-L2 {worst:.3e}")
 
 
 @pytest.mark.parametrize("kv_bf16", [False, True])

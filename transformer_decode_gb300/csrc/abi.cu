@@ -287,7 +287,7 @@ nc_status nc_w8a8_gemv_b32(const float* x, const void* gamma, float eps, const i
            "K = %d is too long to keep the batch's codes in shared memory", K);
   W8BArgs a{x, static_cast<const uint16_t*>(gamma), eps, Wq, w_scale,
             static_cast<const uint16_t*>(bias), B, K, N, y, xq_out, sx_out, acc_out};
-  return launch_result(launch_w8a8_b32(a, S(stream)), "nc_w8a8_gemv_b32");
+  return launch_result(launch_w8a8_b32(Epi::Store, a, S(stream)), "nc_w8a8_gemv_b32");
 }
 
 size_t nc_sample_scratch_bytes(int B, int V) {

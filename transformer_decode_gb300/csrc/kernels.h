@@ -136,10 +136,20 @@ struct W8BArgs {
   float* y;               // [B, N]
   int8_t* xq_out;         // [B, K] or null
   float* sx_out;          // [B, K / 32] or null
-  int32_t* acc_out;       // [B, N, K / 32] or null
+  int32_t* acc_out;       // [B, R N, K / 32] or null (R = 2 for SwiGLU)
+  // non-null part: the LM head -- y are the logits, and the arg-max of each
+  // sequence goes to next (and, when non-null, the greedy feedback)
+  unsigned long long* part = nullptr;  // [B, lm_head_grid()] (workspace)
+  unsigned int* ticket = nullptr;      // zero on entry; the last CTA resets it
+  int32_t* next = nullptr;
+  int* status = nullptr;
+  int32_t* advance_tokens = nullptr;
+  int32_t* advance_positions = nullptr;
 };
 size_t w8a8_b32_smem_bytes(int B, int K);
-cudaError_t launch_w8a8_b32(const W8BArgs& a, cudaStream_t s);
+cudaError_t launch_w8a8_b32(Epi epi, const W8BArgs& a, cudaStream_t s);
+cudaError_t launch_embed_i8(const int8_t* q, const float* sc, const int32_t* tokens, int B, int H,
+                            int V, float* x, int* status, cudaStream_t s);
 
 // ------------------------------------------------------------ sampling
 // Scratch of nc_sample: per row five arrays of V rounded up to 64 words.
