@@ -81,3 +81,15 @@ def test_reference_arm_under_torchrun_prints_one_line(tmp_path):
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_step_bytes_int8_head():
+    """With the tied head int8 (one fp32 scale a row), the head and the
+    gathered row cost one byte a weight plus the scales instead of two."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from transformer_decode_gb300 import synth
+    s = synth.QWEN2_0P5B
+    a = bench.step_bytes(s, 1, [95], w8a8=True)
+    b = bench.step_bytes(s, 1, [95], w8a8=True, int8_head=True)
+    assert a - b == (s.vocab * s.hidden - 4 * s.vocab) + (s.hidden - 4)
