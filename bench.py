@@ -66,12 +66,14 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def step_bytes(shape, batch, positions, kv_elem=4, w8a8=False):
+def step_bytes(shape, batch, positions, kv_elem=4, w8a8=False, int8_head=False):
     """Algorithmic HBM bytes of one decode step: every weight byte once, the
     embedding rows, K/V of slots 0..p read once per layer and kv head, the new
     K/V written, the logits written and tokens/positions read. kv_elem is the
     cache element size (4: fp32 cache, 2: bf16); w8a8: the seven projections
-    are int8 with one fp32 scale per output row (the LM head stays bf16)."""
+    are int8 with one fp32 scale per output row (the LM head stays bf16);
+    int8_head: the tied embedding / head rows are int8 with one fp32 scale
+    each too."""
     H, D, F, L, V = shape.hidden, shape.head_dim, shape.ffn, shape.n_layers, shape.vocab
     nqkv = shape.q_dim + 2 * shape.kv_dim
     if w8a8:
@@ -83,8 +85,8 @@ def step_bytes(shape, batch, positions, kv_elem=4, w8a8=False):
         per_layer += 2 * nqkv
     if shape.qk_norm:
         per_layer += 2 * 2 * D
-    head = 2 * V * H + 2 * H
-    emb = 2 * H * batch
+    head = (V * H + 4 * V if int8_head else 2 * V * H) + 2 * H
+    emb = (H + 4 if int8_head else 2 * H) * batch
     kv_row = 2 * shape.kv_dim * kv_elem  # K and V of one position, one layer
     kv_read = sum((p + 1) for p in positions) * L * kv_row
     kv_write = batch * L * kv_row
@@ -638,6 +640,8 @@ WORKLOADS = {
                                               past="uniform 256..4096", gen=32, w8a8=False),
     "qwen2_0p5b_w8a8_b1_past512": dict(shape="QWEN2_0P5B", batch=1, paged=False, past=512,
                                        gen=64, w8a8=True),
+    "qwen2_0p5b_w8a8_b32_b1_past512": dict(shape="QWEN2_0P5B", batch=1, paged=False, past=512,
+                                           gen=64, w8a8="b32"),
 }
 ROUNDS = 5  # the timed region is reported as this many equal rounds as well
 
@@ -696,7 +700,9 @@ def oracle_for(cfg, max_ctx):
     if cfg.get("layers"):
         shape = shape.with_layers(cfg["layers"])
     past = workload_past(cfg)
-    om = oracle.OracleModel(shape, cpu_weights(shape), w8a8=cfg["w8a8"])
+    om = oracle.OracleModel(shape, cpu_weights(shape), w8a8=bool(cfg["w8a8"]),
+                            act_block=32 if cfg["w8a8"] == "b32" else 0,
+                            int8_embed=cfg["w8a8"] == "b32")
     okv = om.new_kv(cfg["batch"], max_ctx)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     for l in range(shape.n_layers):
@@ -865,7 +871,8 @@ def run_workload(args, ws, rank, local, name):
         sampler.stop()
     value, el = replica_rate(ws, B, args.steps, total_s)
     dur = el / args.steps
-    bytes_avg = sum(step_bytes(shape, B, u.tolist(), w8a8=cfg["w8a8"]) for u in used) / len(used)
+    bytes_avg = sum(step_bytes(shape, B, u.tolist(), w8a8=bool(cfg["w8a8"]),
+                               int8_head=cfg["w8a8"] == "b32") for u in used) / len(used)
     peak, peak_kind = peaks()
 
     # e2e: tokens and positions from pinned host memory, next tokens read back
@@ -922,7 +929,9 @@ def run_workload(args, ws, rank, local, name):
             "config": {"workload": name + (f" (first {args.layers} layers only)"
                                            if args.layers else ""),
                        "batch": B, "past": cfg["past"], "greedy_steps": gen,
-                       "weights": ("int8 per-row scales (W8A8)" if cfg["w8a8"] else "bf16") +
+                       "weights": ("int8 per-row scales, activations per 32, int8 tied head"
+                                   if cfg["w8a8"] == "b32" else
+                                   "int8 per-row scales (W8A8)" if cfg["w8a8"] else "bf16") +
                                   " from seeded N(0,0.02), fp32 accumulate",
                        "kv": ("paged (block 16, shuffled tables)" if cfg["paged"] else "contiguous")
                              + " fp32",

@@ -50,7 +50,13 @@ typedef enum {
   NC_ERR_UNSUPPORTED = 9
 } nc_status;
 
-typedef enum { NC_BF16 = 0, NC_INT8 = 1 } nc_wtype;
+/* Weight storage. NC_INT8: the seven projections int8 per output row,
+ * activations quantised per token (nanoinfer "Quantization"). NC_INT8_B32:
+ * the same projections with activations quantised per block of 32 values,
+ * and the embedding stored int8 per row too, which is also the tied head
+ * (nanoinfer, INT8 activation section and its "INT8 + embeddings" level);
+ * needs tie_embeddings and hidden, ffn, n_q_heads * head_dim multiples of 32. */
+typedef enum { NC_BF16 = 0, NC_INT8 = 1, NC_INT8_B32 = 2 } nc_wtype;
 
 /* Hyperparameters. head_dim must be 64 or 128; n_q_heads a multiple of
  * n_kv_heads with group <= 8; hidden, ffn, n_q_heads*head_dim multiples of 8. */
@@ -183,16 +189,20 @@ nc_status nc_decode_path(nc_model* m, int batch, const nc_kv_cache* kv, int flag
 
 /* W8A8 diagnostic (nanoinfer "Quantization": the per-token activation codes;
  * for checking every code a whole-model W8A8 step used against the oracle's).
- * While set, every nc_decode_step and nc_block_forward of this NC_INT8 model
- * writes the activation codes and scales of its W8A8 products to the
- * caller's device buffers, and a decode step runs its kernels directly (no
- * graph). Layout for a step at batch B, per layer l of L:
+ * While set, every nc_decode_step and nc_block_forward of this W8A8 model
+ * (NC_INT8 or NC_INT8_B32) writes the activation codes of its W8A8 products
+ * (and, NC_INT8 only, their per-token scales) to the caller's device
+ * buffers, and a decode step runs its kernels directly (no graph). Layout
+ * for a step at batch B, per layer l of L:
  *   codes_dev + l * B * (2 H + Hq D + F): the codes [B][H] of the QKV
  *     product, then [B][Hq D] of the o-proj, [B][H] of gate|up, [B][F] of
  *     the down product (nc_block_forward writes layer `layer`'s slot);
- *   scales_dev + (l * 4 + p) * B: the B scales of product p in that order.
+ *     NC_INT8_B32 then the int8 head's codes [B][H] after the L layers;
+ *   scales_dev (nullable; NC_INT8) + (l * 4 + p) * B: the B scales of
+ *     product p in that order.
  * Capacities are in elements; a step that needs more returns
- * NC_ERR_CAPACITY. NULL, NULL turns it off. NC_ERR_DTYPE for a bf16 model. */
+ * NC_ERR_CAPACITY. A NULL codes_dev turns it off. NC_ERR_DTYPE for a bf16
+ * model. */
 nc_status nc_debug_w8a8_codes(nc_model* m, int8_t* codes_dev, size_t codes_capacity,
                               float* scales_dev, size_t scales_capacity);
 
@@ -367,6 +377,19 @@ nc_status nc_quantize_weight(const void* W, int N, int K, int8_t* q, float* scal
 nc_status nc_w8a8_gemv(const float* x, const void* gamma, float eps, const int8_t* Wq,
                        const float* w_scale, const void* bias, int B, int K, int N, float* y,
                        int8_t* xq_out, float* sx_out, int32_t* acc_out, void* stream);
+
+/* The same product with activations quantised per block of 32 consecutive
+ * values instead of per token (nanoinfer, INT8 activation section: "one per
+ * 32", so an outlier widens only its own block): sx[b, j] = amax of block j
+ * of xn[b] / 127, xq = clamp(round_half_away(xn / sx), -127, 127);
+ * acc[b, n, j] = sum over block j of Wq[n, k] * xq[b, k] in int32;
+ * y[b, n] = sum_j float(acc[b, n, j]) * (w_scale[n] * sx[b, j]) (+ bias[n]).
+ * B in [1, 8], K a multiple of 32. The optional outputs expose xq [B, K] int8,
+ * sx [B, K / 32] fp32 and acc [B, N, K / 32] int32 for bit-exact checks.
+ * Errors as for nc_w8a8_gemv. */
+nc_status nc_w8a8_gemv_b32(const float* x, const void* gamma, float eps, const int8_t* Wq,
+                           const float* w_scale, const void* bias, int B, int K, int N, float* y,
+                           int8_t* xq_out, float* sx_out, int32_t* acc_out, void* stream);
 
 #ifdef __cplusplus
 }

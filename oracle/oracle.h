@@ -97,11 +97,12 @@ typedef struct {
 /* Trace of the rounding steps inside a decode step (NULL in orc_model: off,
  * and nothing below happens). Two kinds of entries, each appended in call
  * order (per sequence, per layer):
- *   - every per-token W8A8 activation quantisation (the q, k, v, o, gate, up
- *     and down products, in that order): its own codes [K] and the fp32
- *     quotients v / s it rounded [K]; with force_codes set, the product then
- *     uses force_codes (same offsets) in place of its own codes (its own
- *     scale is kept);
+ *   - every W8A8 activation quantisation (the q, k, v, o, gate, up and down
+ *     products, in that order, and with the int8 head its product last): its
+ *     own codes [K] and the fp32 quotients v / s it rounded [K] (s the
+ *     token's scale, or the block's with act_block); with force_codes set,
+ *     the product then uses force_codes (same offsets) in place of its own
+ *     codes (its own scales are kept);
  *   - every bf16 store of the new position's K/V (per kv head: D values of K,
  *     then D of V): its own bits and the fp32 value it rounded; with force_kv
  *     set, force_kv's bits are stored instead.

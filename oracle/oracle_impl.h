@@ -160,17 +160,12 @@ void F(orc_linear_w8a8)(const int8_t* w, const float* sw, const uint16_t* bias, 
  * block): each block is quantised as a row is, acc[j, b] is the int32 sum of
  * block b (int64, checked), and y[j] = sum_b float(acc[j, b]) * (sw[j] * sx[b])
  * in block order, then + bias. A ragged last block is shorter. */
-void F(orc_linear_w8a8_blocked)(const int8_t* w, const float* sw, const uint16_t* bias, int n,
-                                int k, int block, const REAL* x, REAL* y) {
+/* The integer products and the dequantisation of the blocked form, given the
+ * codes xq [k] and the block scales sx [nb]. */
+static void F(w8a8_blocked_product)(const int8_t* w, const float* sw, const uint16_t* bias, int n,
+                                    int k, int block, const int8_t* xq, const float* sx,
+                                    REAL* y) {
   const int nb = (k + block - 1) / block;
-  float* xf = (float*)malloc(sizeof(float) * (size_t)k);
-  int8_t* xq = (int8_t*)malloc((size_t)k);
-  float* sx = (float*)malloc(sizeof(float) * (size_t)nb);
-  for (int i = 0; i < k; ++i) xf[i] = (float)x[i];
-  for (int b = 0; b < nb; ++b) {
-    const int len = k - b * block < block ? k - b * block : block;
-    sx[b] = orc_quantize_row_f32(xf + (long)b * block, len, xq + (long)b * block);
-  }
   int bad = 0;
 #pragma omp parallel for schedule(static) reduction(| : bad)
   for (int j = 0; j < n; ++j) {
@@ -186,6 +181,20 @@ void F(orc_linear_w8a8_blocked)(const int8_t* w, const float* sw, const uint16_t
     y[j] = t;
   }
   if (bad) abort();
+}
+
+void F(orc_linear_w8a8_blocked)(const int8_t* w, const float* sw, const uint16_t* bias, int n,
+                                int k, int block, const REAL* x, REAL* y) {
+  const int nb = (k + block - 1) / block;
+  float* xf = (float*)malloc(sizeof(float) * (size_t)k);
+  int8_t* xq = (int8_t*)malloc((size_t)k);
+  float* sx = (float*)malloc(sizeof(float) * (size_t)nb);
+  for (int i = 0; i < k; ++i) xf[i] = (float)x[i];
+  for (int b = 0; b < nb; ++b) {
+    const int len = k - b * block < block ? k - b * block : block;
+    sx[b] = orc_quantize_row_f32(xf + (long)b * block, len, xq + (long)b * block);
+  }
+  F(w8a8_blocked_product)(w, sw, bias, n, k, block, xq, sx, y);
   free(xf);
   free(xq);
   free(sx);
@@ -220,12 +229,38 @@ void F(orc_linear_int4)(const uint8_t* w4, const float* s4, int group, const uin
 static void F(linear_i8)(const orc_model* m, const int8_t* w8, const float* sw,
                          const uint16_t* bias, int n, int k, const REAL* x, REAL* y) {
   orc_trace* tr = m->trace;
-  if (m->act_block > 0) {
-    F(orc_linear_w8a8_blocked)(w8, sw, bias, n, k, m->act_block, x, y);
+  if (!tr) {
+    if (m->act_block > 0)
+      F(orc_linear_w8a8_blocked)(w8, sw, bias, n, k, m->act_block, x, y);
+    else
+      F(orc_linear_w8a8)(w8, sw, bias, n, k, x, y);
     return;
   }
-  if (!tr) {
-    F(orc_linear_w8a8)(w8, sw, bias, n, k, x, y);
+  if (m->act_block > 0) {  /* traced, blocked: each block's quotients use its scale */
+    const int blk = m->act_block, nb = (k + blk - 1) / blk;
+    float* xf = (float*)malloc(sizeof(float) * (size_t)k);
+    int8_t* xq = (int8_t*)malloc((size_t)k);
+    float* sxb = (float*)malloc(sizeof(float) * (size_t)nb);
+    for (int i = 0; i < k; ++i) xf[i] = (float)x[i];
+    for (int b = 0; b < nb; ++b) {
+      const int len = k - b * blk < blk ? k - b * blk : blk;
+      sxb[b] = orc_quantize_row_f32(xf + (long)b * blk, len, xq + (long)b * blk);
+    }
+    if (tr->n_codes + k <= tr->cap_codes) {
+      for (int i = 0; i < k; ++i) {
+        const float sb = sxb[i / blk];
+        tr->codes[tr->n_codes + i] = xq[i];
+        tr->quot[tr->n_codes + i] = sb == 0.0f ? 0.0f : xf[i] / sb;
+      }
+      if (tr->force_codes) memcpy(xq, tr->force_codes + tr->n_codes, (size_t)k);
+      tr->n_codes += k;
+    } else {
+      tr->overflow = 1;
+    }
+    F(w8a8_blocked_product)(w8, sw, bias, n, k, blk, xq, sxb, y);
+    free(xf);
+    free(xq);
+    free(sxb);
     return;
   }
   float* xf = (float*)malloc(sizeof(float) * (size_t)k);

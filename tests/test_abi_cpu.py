@@ -222,3 +222,16 @@ def test_entry_points_reject_misaligned_pointers(lib):
     assert lib.nc_sample(P, 1, 1000, 0.7, 20, 0.8, P4, P, None, P, n, None) == E
     assert lib.nc_sample(P, 1, 1000, 0.7, 20, 0.8, P, P2, None, P, n, None) == E
     assert lib.nc_sample(P, 1, 1000, 0.7, 20, 0.8, P, P, P2, P, n, None) == E
+
+
+def test_w8a8_b32_rejects_bad_arguments(lib):
+    E = {n: nc.STATUS.index(n) for n in nc.STATUS}
+    P = C.c_void_p(4096)
+    call = lambda x=P, W=P, B=1, K=896, N=8, y=P, sx=None: lib.nc_w8a8_gemv_b32(
+        x, None, 1e-6, W, P, None, B, K, N, y, None, sx, None, None)
+    assert call(x=None) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(W=C.c_void_p(4104)) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(sx=C.c_void_p(4098)) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(B=0) == E["NC_ERR_SHAPE"] and call(B=9) == E["NC_ERR_SHAPE"]
+    assert call(K=880) == E["NC_ERR_SHAPE"] and call(K=16) == E["NC_ERR_SHAPE"]
+    assert call(N=0) == E["NC_ERR_SHAPE"]

@@ -96,8 +96,7 @@ def test_block_forward_w8a8_codes_on_identical_input():
     H, qd, F = shape.hidden, shape.q_dim, shape.ffn
     per_layer = 2 * H + qd + F
     codes = torch.empty(shape.n_layers * per_layer, dtype=torch.int8, device="cuda")
-    scales = torch.empty(shape.n_layers * 4, dtype=torch.float32, device="cuda")
-    model.debug_w8a8_codes(codes, scales)
+    model.debug_w8a8_codes(codes)
     x = synth.normal_bf16(0, 9999, (shape.hidden,), 1.0).float().numpy()
     p = torch.tensor([pos], dtype=torch.int32)
     worst, nd = 0.0, 0
@@ -116,7 +115,7 @@ def test_block_forward_w8a8_codes_on_identical_input():
         worst = max(worst, e)
         assert e < REL_L2_GATE, (l, e)
         x = ref  # the next block starts from the oracle's output on both sides
-    model.debug_w8a8_codes(None, None)
+    model.debug_w8a8_codes(None)
     model.close()
     print(f"W8A8 blocks: worst rel-L2 {worst:.3e}, boundary codes forced {nd}")
 
@@ -223,7 +222,9 @@ def _traced_compare(shape, wd, wc, steps, batch=1, past=None, paged=False, w8a8=
     above), so both sides compute on identical codes and cache bits: then
     every step's logits meet the plain 5e-4 gate and the tokens agree.
     Returns (worst logit rel-L2, differing codes, differing K/V values)."""
-    om = oracle.OracleModel(shape, wc, w8a8=w8a8)
+    b32 = w8a8 == "b32"
+    om = oracle.OracleModel(shape, wc, w8a8=bool(w8a8), act_block=32 if b32 else 0,
+                            int8_embed=b32)
     past = past or [0] * batch
     n_total = (len(prompt[0]) if prompt is not None else 0) + steps
     max_ctx = max(past) + n_total + 1
@@ -241,10 +242,12 @@ def _traced_compare(shape, wd, wc, steps, batch=1, past=None, paged=False, w8a8=
     per_layer = batch * (2 * H + qd + F)
     codes = scales = None
     if w8a8:
-        codes = torch.empty(L * per_layer, dtype=torch.int8, device="cuda")
-        scales = torch.empty(L * 4 * batch, dtype=torch.float32, device="cuda")
-        model.debug_w8a8_codes(codes, scales)
-    n_codes = batch * L * (5 * H + qd + F) if w8a8 else 0  # q, k, v, o, gate, up, down
+        codes = torch.empty(L * per_layer + (batch * H if b32 else 0), dtype=torch.int8,
+                            device="cuda")
+        model.debug_w8a8_codes(codes)
+    # per sequence and layer q, k, v, o, gate, up, down; the blocked mode's
+    # int8 head after the layers
+    n_codes = batch * (L * (5 * H + qd + F) + (H if b32 else 0)) if w8a8 else 0
     n_kv = batch * L * Hkv * 2 * D if kv_bf16 else 0
     logits = torch.empty(batch, shape.vocab, device="cuda")
     nxt = torch.empty(batch, dtype=torch.int32, device="cuda")
@@ -262,7 +265,8 @@ def _traced_compare(shape, wd, wc, steps, batch=1, past=None, paged=False, w8a8=
         torch.cuda.synchronize()
         force_codes = force_kv = None
         if w8a8:
-            c = codes.cpu().numpy().reshape(L, per_layer)
+            call = codes.cpu().numpy()
+            c = call[:L * per_layer].reshape(L, per_layer)
             parts = []
             for b in range(batch):
                 for l in range(L):
@@ -274,6 +278,8 @@ def _traced_compare(shape, wd, wc, steps, batch=1, past=None, paged=False, w8a8=
                     d0 = g0 + batch * H
                     d_b = c[l, d0 + b * F:d0 + (b + 1) * F]
                     parts += [qkv_b, qkv_b, qkv_b, o_b, gu_b, gu_b, d_b]
+                if b32:
+                    parts.append(call[L * per_layer + b * H:L * per_layer + (b + 1) * H])
             force_codes = np.concatenate(parts)
         if kv_bf16:
             rows = []
@@ -303,7 +309,7 @@ def _traced_compare(shape, wd, wc, steps, batch=1, past=None, paged=False, w8a8=
         else:
             tok = on.astype(np.int32)
     if w8a8:
-        model.debug_w8a8_codes(None, None)
+        model.debug_w8a8_codes(None)
     assert model.device_status() == 0
     model.close()
     return worst, n_code_diff, n_kv_diff
@@ -383,6 +389,19 @@ def test_decode_0p5b_w8a8_past512():
     wd, wc = weights_both(shape)
     worst, nd, _ = _traced_compare(shape, wd, wc, steps=64, past=[512], w8a8=True)
     print(f"0.5B W8A8: worst logit rel-L2 {worst:.3e}, boundary codes forced {nd}")
+
+
+@pytest.mark.parametrize("shape,past,steps", [(synth.TINY, 0, 12),
+                                               (synth.QWEN2_0P5B, 512, 64)])
+def test_decode_w8a8_b32(shape, past, steps):
+    """W8A8 with activations in blocks of 32 and the int8 embedding as the
+    tied head (NC_INT8_B32) against the oracle's same mode: every activation
+    code, the head's included, equals the oracle's except boundary cases
+    (checked and forced), and the logits meet the plain 5e-4 gate."""
+    wd, wc = weights_both(shape)
+    worst, nd, _ = _traced_compare(shape, wd, wc, steps=steps, past=[past], w8a8="b32")
+    print(f"W8A8 blocks of 32 ({shape.hidden}): worst logit rel-L2 {worst:.3e}, "
+          f"boundary codes forced {nd}")
 
 
 def test_decode_0p5b_batch16_paged():

@@ -114,3 +114,15 @@ def test_step_bytes_against_the_page_counts():
     rows = s.n_layers * ((s.q_dim + 2 * s.kv_dim) + H + 2 * s.ffn + H)
     assert bench.step_bytes(s, 1, [95], w8a8=True) == \
         bench.step_bytes(s, 1, [95]) - 2 * proj + proj + 4 * rows
+
+
+def test_step_bytes_int8_head():
+    """With the tied head int8 (one fp32 scale a row), the head and the
+    gathered row cost one byte a weight plus the scales instead of two."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from transformer_decode_gb300 import synth
+    s = synth.QWEN2_0P5B
+    a = bench.step_bytes(s, 1, [95], w8a8=True)
+    b = bench.step_bytes(s, 1, [95], w8a8=True, int8_head=True)
+    assert a - b == (s.vocab * s.hidden - 4 * s.vocab) + (s.hidden - 4)

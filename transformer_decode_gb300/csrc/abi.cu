@@ -137,9 +137,8 @@ nc_status nc_debug_w8a8_codes(nc_model* m, int8_t* codes_dev, size_t codes_capac
                               float* scales_dev, size_t scales_capacity) {
   NC_CHECK(m, NC_ERR_INVALID_ARGUMENT, "model is NULL");
   Model* mm = M(m);
-  NC_CHECK(mm->cfg.wtype == NC_INT8, NC_ERR_DTYPE, "the model's projections are not W8A8");
-  NC_CHECK((codes_dev == nullptr) == (scales_dev == nullptr), NC_ERR_INVALID_ARGUMENT,
-           "give both buffers, or neither");
+  NC_CHECK(mm->cfg.wtype != NC_BF16, NC_ERR_DTYPE, "the model's projections are not W8A8");
+  NC_CHECK(codes_dev || !scales_dev, NC_ERR_INVALID_ARGUMENT, "scales need the codes buffer");
   NC_CHECK(aligned(scales_dev, 4), NC_ERR_INVALID_ARGUMENT, "scales must be 4-byte aligned");
   mm->dbg_codes = codes_dev;
   mm->dbg_scales = scales_dev;
@@ -328,6 +327,24 @@ nc_status nc_w8a8_gemv(const float* x, const void* gamma, float eps, const int8_
   W8Args a{x, static_cast<const uint16_t*>(gamma), eps, Wq, w_scale,
            static_cast<const uint16_t*>(bias), B, K, N, y, xq_out, sx_out, acc_out};
   return launch_result(launch_w8a8(Epi::Store, a, S(stream)), "nc_w8a8_gemv");
+}
+
+nc_status nc_w8a8_gemv_b32(const float* x, const void* gamma, float eps, const int8_t* Wq,
+                           const float* w_scale, const void* bias, int B, int K, int N, float* y,
+                           int8_t* xq_out, float* sx_out, int32_t* acc_out, void* stream) {
+  NC_CHECK(x && Wq && w_scale && y, NC_ERR_INVALID_ARGUMENT, "null pointer");
+  NC_CHECK(aligned16(Wq) && aligned(x, 4) && aligned(gamma, 2) && aligned(w_scale, 4) &&
+               aligned(bias, 2) && aligned(y, 4) && aligned(sx_out, 4) && aligned(acc_out, 4),
+           NC_ERR_INVALID_ARGUMENT,
+           "Wq must be 16-byte aligned, fp32 and int32 pointers 4-byte, bf16 2-byte");
+  NC_CHECK(B >= 1 && B <= 8, NC_ERR_SHAPE, "batch %d outside [1, 8]", B);
+  NC_CHECK(K >= 32 && K % 32 == 0, NC_ERR_SHAPE, "K = %d must be a positive multiple of 32", K);
+  NC_CHECK(N >= 1, NC_ERR_SHAPE, "N must be positive");
+  NC_CHECK(w8a8_b32_smem_bytes(B, K) + 4096 <= (size_t)max_smem_optin(), NC_ERR_SHAPE,
+           "K = %d is too long to keep the batch's codes in shared memory", K);
+  W8BArgs a{x, static_cast<const uint16_t*>(gamma), eps, Wq, w_scale,
+            static_cast<const uint16_t*>(bias), B, K, N, y, xq_out, sx_out, acc_out};
+  return launch_result(launch_w8a8_b32(Epi::Store, a, S(stream)), "nc_w8a8_gemv_b32");
 }
 
 size_t nc_sample_scratch_bytes(int B, int V) {

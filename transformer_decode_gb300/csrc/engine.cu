@@ -71,7 +71,11 @@ bool valid_config(const nc_config& c, std::string* why) {
   if (c.hidden % 16 || c.ffn % 16) return bad("hidden and ffn must be multiples of 16");
   if (c.hidden > 16384 || c.ffn > 65536) return bad("hidden or ffn too large");
   if (!(c.rms_eps > 0) || !(c.rope_theta > 1)) return bad("rms_eps must be > 0 and rope_theta > 1");
-  if (c.wtype != NC_BF16 && c.wtype != NC_INT8) return bad("unknown weight type");
+  if (c.wtype != NC_BF16 && c.wtype != NC_INT8 && c.wtype != NC_INT8_B32)
+    return bad("unknown weight type");
+  if (c.wtype == NC_INT8_B32 &&
+      (!c.tie_embeddings || c.hidden % 32 || c.ffn % 32 || (c.n_q_heads * c.head_dim) % 32))
+    return bad("NC_INT8_B32 needs a tied head and hidden, ffn, n_q_heads * head_dim multiples of 32");
   return true;
 }
 
@@ -88,6 +92,8 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
   std::string why;
   NC_CHECK(valid_config(*cfg, &why), NC_ERR_SHAPE, "invalid config: %s", why.c_str());
   NC_CHECK(max_batch >= 1 && max_batch <= 16, NC_ERR_CAPACITY, "max_batch must be in [1, 16]");
+  NC_CHECK(cfg->wtype != NC_INT8_B32 || max_batch <= 8, NC_ERR_CAPACITY,
+           "NC_INT8_B32 models take at most 8 sequences");
   NC_CHECK(max_ctx >= 1 && max_ctx <= (1 << 20), NC_ERR_CAPACITY, "max_ctx out of range");
   const nc_config& c = *cfg;
   const int bt = max_batch <= 1 ? 1 : max_batch <= 2 ? 2 : max_batch <= 4 ? 4 : max_batch <= 8 ? 8 : 16;
@@ -115,7 +121,8 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
   m->max_ctx = max_ctx;
   const int H = c.hidden, D = c.head_dim, F = c.ffn, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   const size_t qd = (size_t)Hq * D, kd = (size_t)Hkv * D, nqkv = qd + 2 * kd;
-  const bool i8 = c.wtype == NC_INT8;
+  const bool i8 = c.wtype != NC_BF16;
+  const bool b32 = c.wtype == NC_INT8_B32;
 
   // Two passes over one layout function: first with null bases to size the
   // arenas, then with the real allocations to assign every pointer.
@@ -150,8 +157,13 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
       P.g_q = c.qk_norm ? A.take<uint16_t>(D) : nullptr;
       P.g_k = c.qk_norm ? A.take<uint16_t>(D) : nullptr;
     }
-    m->embed = A.take<uint16_t>((size_t)c.vocab * H);
-    m->head = c.tie_embeddings ? m->embed : A.take<uint16_t>((size_t)c.vocab * H);
+    if (b32) {  // the int8 rows replace the bf16 table (and serve as the head)
+      m->q_embed = A.take<int8_t>((size_t)c.vocab * H);
+      m->s_embed = A.take<float>(c.vocab);
+    } else {
+      m->embed = A.take<uint16_t>((size_t)c.vocab * H);
+      m->head = c.tie_embeddings ? m->embed : A.take<uint16_t>((size_t)c.vocab * H);
+    }
     m->g_final = A.take<uint16_t>(H);
     m->inv_freq = A.take<float>(D / 2);
 
@@ -237,7 +249,13 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
       if (!e) e = copy(P.g_k, L.g_k, (size_t)D * 2);
     }
   }
-  if (!e) e = copy(m->embed, w->embed, (size_t)c.vocab * H * 2);
+  if (b32) {
+    if (!e)
+      e = launch_quantize_weight(static_cast<const uint16_t*>(w->embed), c.vocab, H, m->q_embed,
+                                 m->s_embed, s);
+  } else if (!e) {
+    e = copy(m->embed, w->embed, (size_t)c.vocab * H * 2);
+  }
   if (!c.tie_embeddings && !e) e = copy(m->head, w->lm_head, (size_t)c.vocab * H * 2);
   if (!e) e = copy(m->g_final, w->g_final, (size_t)H * 2);
   // RoPE frequencies: float(1 / theta^(2i/D)), evaluated in double on the host.
@@ -380,11 +398,14 @@ nc_status validate_kv(const Model* m, int batch, const int32_t* positions_host,
 // and their scales [4][B].
 size_t dbg_codes_per_step(const Model* m, int batch) {
   const nc_config& c = m->cfg;
+  // the blocked mode's int8 head quantises the final norm too: [B][H] last
   return (size_t)c.n_layers * batch *
-         (2 * (size_t)c.hidden + (size_t)c.n_q_heads * c.head_dim + c.ffn);
+             (2 * (size_t)c.hidden + (size_t)c.n_q_heads * c.head_dim + c.ffn) +
+         (c.wtype == NC_INT8_B32 ? (size_t)batch * c.hidden : 0);
 }
 size_t dbg_scales_per_step(const Model* m, int batch) {
-  return (size_t)m->cfg.n_layers * 4 * batch;
+  // per-token scales (the blocked mode's per-block scales are not captured)
+  return m->cfg.wtype == NC_INT8 ? (size_t)m->cfg.n_layers * 4 * batch : 0;
 }
 
 static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* positions,
@@ -393,7 +414,8 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
   const LayerPacked& P = m->layers[layer];
   const int H = c.hidden, D = c.head_dim, F = c.ffn, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   const int nqkv = (Hq + 2 * Hkv) * D;
-  const bool i8 = c.wtype == NC_INT8;
+  const bool i8 = c.wtype != NC_BF16;
+  const bool b32 = c.wtype == NC_INT8_B32;
   // the W8A8 diagnostic's slots of this layer (null when it is off)
   int8_t* dq[4] = {nullptr, nullptr, nullptr, nullptr};
   float* ds[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -404,11 +426,16 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
     dq[1] = dq[0] + (size_t)batch * H;
     dq[2] = dq[1] + (size_t)batch * Hq * D;
     dq[3] = dq[2] + (size_t)batch * H;
-    for (int k = 0; k < 4; ++k) ds[k] = m->dbg_scales + ((size_t)layer * 4 + k) * batch;
+    if (!b32 && m->dbg_scales)
+      for (int k = 0; k < 4; ++k) ds[k] = m->dbg_scales + ((size_t)layer * 4 + k) * batch;
   }
   cudaError_t e;
   if (!i8) {
     e = launch_gemv(Epi::Store, {m->x, P.g_attn, c.rms_eps, P.w_qkv, P.b_qkv, batch, H, nqkv, m->qkv}, s);
+  } else if (b32) {
+    W8BArgs a{m->x, P.g_attn, c.rms_eps, P.q_qkv, P.s_qkv, P.b_qkv, batch, H, nqkv, m->qkv,
+              dq[0], nullptr, nullptr};
+    e = launch_w8a8_b32(Epi::Store, a, s);
   } else {
     W8Args a{m->x, P.g_attn, c.rms_eps, P.q_qkv, P.s_qkv, P.b_qkv, batch, H, nqkv, m->qkv,
              dq[0], ds[0], nullptr};
@@ -431,6 +458,17 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
       return e;
     return launch_gemv(Epi::Residual, {m->h, nullptr, 0.f, P.w_d, nullptr, batch, F, H, m->x}, s);
   }
+  if (b32) {
+    W8BArgs o{m->attn, nullptr, 0.f, P.q_o, P.s_o, nullptr, batch, Hq * D, H, m->x,
+              dq[1], nullptr, nullptr};
+    if ((e = launch_w8a8_b32(Epi::Residual, o, s))) return e;
+    W8BArgs gu{m->x, P.g_mlp, c.rms_eps, P.q_gu, P.s_gu, nullptr, batch, H, F, m->h,
+               dq[2], nullptr, nullptr};
+    if ((e = launch_w8a8_b32(Epi::SwiGLU, gu, s))) return e;
+    W8BArgs dn{m->h, nullptr, 0.f, P.q_d, P.s_d, nullptr, batch, F, H, m->x,
+               dq[3], nullptr, nullptr};
+    return launch_w8a8_b32(Epi::Residual, dn, s);
+  }
   W8Args o{m->attn, nullptr, 0.f, P.q_o, P.s_o, nullptr, batch, Hq * D, H, m->x, dq[1], ds[1], nullptr};
   if ((e = launch_w8a8(Epi::Residual, o, s))) return e;
   W8Args gu{m->x, P.g_mlp, c.rms_eps, P.q_gu, P.s_gu, nullptr, batch, H, F, m->h, dq[2], ds[2], nullptr};
@@ -450,10 +488,29 @@ struct StepIO {
 static cudaError_t enqueue_step(Model* m, int batch, const StepIO& io, const KVView& kvv,
                                 int splits, cudaStream_t s) {
   const nc_config& c = m->cfg;
-  cudaError_t e = launch_embed(m->embed, io.tokens, batch, c.hidden, c.vocab, m->x, m->status, s);
+  const bool b32 = c.wtype == NC_INT8_B32;
+  cudaError_t e = b32 ? launch_embed_i8(m->q_embed, m->s_embed, io.tokens, batch, c.hidden,
+                                        c.vocab, m->x, m->status, s)
+                      : launch_embed(m->embed, io.tokens, batch, c.hidden, c.vocab, m->x,
+                                     m->status, s);
   if (e) return e;
   for (int l = 0; l < c.n_layers; ++l)
     if ((e = enqueue_block(m, l, batch, io.positions, kvv, splits, s))) return e;
+  if (b32) {  // the int8 head: the blocked W8A8 product of the final norm, with the arg-max
+    int8_t* hq = m->dbg_codes
+                     ? m->dbg_codes + (size_t)c.n_layers * batch *
+                                          (2 * (size_t)c.hidden + (size_t)c.n_q_heads * c.head_dim + c.ffn)
+                     : nullptr;  // the W8A8 diagnostic's head slot
+    W8BArgs h{m->x, m->g_final, c.rms_eps, m->q_embed, m->s_embed, nullptr, batch, c.hidden,
+              c.vocab, io.logits, hq, nullptr, nullptr};
+    h.part = m->am_part;
+    h.ticket = m->ticket;
+    h.next = io.next;
+    h.status = m->status;
+    h.advance_tokens = io.advance ? io.tokens : nullptr;
+    h.advance_positions = io.advance ? io.positions : nullptr;
+    return launch_w8a8_b32(Epi::Store, h, s);
+  }
   LmHeadArgs a{m->x, m->g_final, c.rms_eps, m->head, batch, c.hidden, c.vocab, io.logits, io.next,
                m->am_part, m->ticket, m->status, io.advance ? io.tokens : nullptr,
                io.advance ? io.positions : nullptr};
@@ -484,7 +541,7 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
   const StepIO io{tokens, positions, logits, next, (flags & NC_STEP_ADVANCE) != 0};
   if (m->dbg_codes) {
     NC_CHECK(dbg_codes_per_step(m, batch) <= m->dbg_codes_cap &&
-                 dbg_scales_per_step(m, batch) <= m->dbg_scales_cap,
+                 (!m->dbg_scales || dbg_scales_per_step(m, batch) <= m->dbg_scales_cap),
              NC_ERR_CAPACITY, "the W8A8 diagnostic buffers are too small for batch %d", batch);
     flags &= ~NC_STEP_GRAPH;  // the diagnostic runs the kernels directly
   }
@@ -566,7 +623,8 @@ nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t*
   nc_status st = validate_kv(m, batch, positions_host, kv);
   if (st) return st;
   NC_CHECK(!m->dbg_codes || (dbg_codes_per_step(m, batch) <= m->dbg_codes_cap &&
-                             dbg_scales_per_step(m, batch) <= m->dbg_scales_cap),
+                             (!m->dbg_scales ||
+                              dbg_scales_per_step(m, batch) <= m->dbg_scales_cap)),
            NC_ERR_CAPACITY, "the W8A8 diagnostic buffers are too small for batch %d", batch);
   const KVView kvv = kv_view(m, *kv);
   const int splits = attn_splits(batch, m->cfg.n_kv_heads, m->cfg.head_dim, kv->dtype == NC_KV_BF16,

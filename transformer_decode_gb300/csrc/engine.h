@@ -36,6 +36,8 @@ struct Model {
   size_t weight_bytes = 0, workspace_bytes = 0;
   std::vector<LayerPacked> layers;
   uint16_t *embed = nullptr, *head = nullptr, *g_final = nullptr;
+  int8_t* q_embed = nullptr;  // NC_INT8_B32: int8 embedding rows (also the tied head)
+  float* s_embed = nullptr;   // [V] their scales
   float* inv_freq = nullptr;
   // workspace
   float *x = nullptr, *qkv = nullptr, *q = nullptr, *attn = nullptr, *part = nullptr, *h = nullptr;

@@ -124,6 +124,33 @@ cudaError_t launch_w8a8(Epi epi, const W8Args& a, cudaStream_t s);
 cudaError_t launch_quantize_weight(const uint16_t* W, int N, int K, int8_t* q, float* scale,
                                    cudaStream_t s);
 
+// W8A8 with activations quantised in blocks of 32 (w8a8_blocks.cu)
+struct W8BArgs {
+  const float* x;
+  const uint16_t* gamma;
+  float eps;
+  const int8_t* Wq;       // [N, K]
+  const float* w_scale;   // [N]
+  const uint16_t* bias;   // [N] or null
+  int B, K, N;
+  float* y;               // [B, N]
+  int8_t* xq_out;         // [B, K] or null
+  float* sx_out;          // [B, K / 32] or null
+  int32_t* acc_out;       // [B, R N, K / 32] or null (R = 2 for SwiGLU)
+  // non-null part: the LM head -- y are the logits, and the arg-max of each
+  // sequence goes to next (and, when non-null, the greedy feedback)
+  unsigned long long* part = nullptr;  // [B, lm_head_grid()] (workspace)
+  unsigned int* ticket = nullptr;      // zero on entry; the last CTA resets it
+  int32_t* next = nullptr;
+  int* status = nullptr;
+  int32_t* advance_tokens = nullptr;
+  int32_t* advance_positions = nullptr;
+};
+size_t w8a8_b32_smem_bytes(int B, int K);
+cudaError_t launch_w8a8_b32(Epi epi, const W8BArgs& a, cudaStream_t s);
+cudaError_t launch_embed_i8(const int8_t* q, const float* sc, const int32_t* tokens, int B, int H,
+                            int V, float* x, int* status, cudaStream_t s);
+
 // ------------------------------------------------------------ sampling
 // Scratch of nc_sample: per row five arrays of V rounded up to 64 words.
 size_t sample_scratch_bytes(int B, int V);

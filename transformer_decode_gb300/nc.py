@@ -22,7 +22,7 @@ NC_OK = 0
 STATUS = ["NC_OK", "NC_ERR_INVALID_ARGUMENT", "NC_ERR_SHAPE", "NC_ERR_DTYPE", "NC_ERR_CAPACITY",
           "NC_ERR_POSITION", "NC_ERR_CUDA", "NC_ERR_TIMEOUT", "NC_ERR_UNHEALTHY",
           "NC_ERR_UNSUPPORTED"]
-NC_BF16, NC_INT8 = 0, 1
+NC_BF16, NC_INT8, NC_INT8_B32 = 0, 1, 2
 NC_STEP_GRAPH, NC_STEP_ADVANCE, NC_STEP_STAGED = 1, 2, 4
 NC_KV_F32, NC_KV_BF16 = 0, 1
 
@@ -33,7 +33,7 @@ EXPORTS = [
     "nc_rope_qkv", "nc_attn_decode", "nc_lm_head_argmax", "nc_quantize_weight", "nc_w8a8_gemv",
     "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile", "nc_decode_path",
     "nc_sample", "nc_sample_scratch_bytes", "nc_attn_decode_static_status",
-    "nc_debug_w8a8_codes",
+    "nc_debug_w8a8_codes", "nc_w8a8_gemv_b32",
 ]
 
 
@@ -123,6 +123,7 @@ def _declare(L):
     L.nc_read_phase_profile.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), i, C.POINTER(i)]
     L.nc_sample.argtypes = [vp, i, i, f, i, f, vp, vp, vp, vp, C.c_size_t, vp]
     L.nc_sample_scratch_bytes.argtypes = [i, i]
+    L.nc_w8a8_gemv_b32.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
     for n in EXPORTS:
         if n not in ("nc_status_string", "nc_last_error_message", "nc_sample_scratch_bytes"):
             getattr(L, n).restype = C.c_int
@@ -222,6 +223,19 @@ def w8a8_gemv(x, gamma, eps, Wq, w_scale, bias, y, xq_out=None, sx_out=None, acc
                                _ptr(y, torch.float32, "y", B * N),
                                _ptr(xq_out, torch.int8, "xq_out"), _ptr(sx_out, torch.float32, "sx_out"),
                                _ptr(acc_out, torch.int32, "acc_out"), _stream(stream)))
+
+
+def w8a8_gemv_b32(x, gamma, eps, Wq, w_scale, bias, y, xq_out=None, sx_out=None, acc_out=None,
+                  stream=None):
+    """nc_w8a8_gemv_b32: the W8A8 product with activations in blocks of 32."""
+    B, K = x.shape
+    N = Wq.shape[0]
+    _check(load().nc_w8a8_gemv_b32(
+        _ptr(x, torch.float32, "x"), _ptr(gamma, torch.bfloat16, "gamma"), float(eps),
+        _ptr(Wq, torch.int8, "Wq", N * K), _ptr(w_scale, torch.float32, "w_scale", N),
+        _ptr(bias, torch.bfloat16, "bias"), B, K, N, _ptr(y, torch.float32, "y", B * N),
+        _ptr(xq_out, torch.int8, "xq_out"), _ptr(sx_out, torch.float32, "sx_out"),
+        _ptr(acc_out, torch.int32, "acc_out"), _stream(stream)))
 
 
 def attn_decode_static(shape, layer, q, positions, positions_host, kv, out, stream=None):
@@ -379,7 +393,7 @@ class Model:
         cfg = Config(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
                      shape.n_layers, shape.vocab, shape.rms_eps, shape.rope_theta,
                      int(shape.qkv_bias), int(shape.qk_norm), int(shape.tie_embeddings),
-                     NC_INT8 if w8a8 else NC_BF16)
+                     {False: NC_BF16, True: NC_INT8, "b32": NC_INT8_B32}[w8a8])
         layers = (LayerWeights * shape.n_layers)()
         for l, lw in enumerate(weights["layers"]):
             for n in _LW:
