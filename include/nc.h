@@ -270,6 +270,22 @@ nc_status nc_lm_head_argmax(nc_model* m, const float* x, const void* gamma, floa
                             const void* W, int B, int K, int V, float* logits, int32_t* next,
                             void* stream);
 
+/* ---------------- INT4 weights (nanoinfer "Quantization": group-wise INT4) --- */
+
+/* y[b, n] = sum_k (q[n, k] * scales[n, k / group]) * xn[b, k], each
+ * dequantised weight rounded to fp32, with xn = rmsnorm(x[b]) * gamma when
+ * gamma != NULL, else xn = x (nanoinfer, "Quantization": INT4 codes in
+ * [-7, 7], one fp32 scale per group of `group` consecutive weights of a row).
+ * Wq [N, K / 2] bytes: two codes a byte, the even index in the low nibble,
+ * two's-complement nibbles; scales [N, K / group] fp32; x [B, K] fp32,
+ * gamma [K] bf16 or NULL, y [B, N] fp32. B in [1, 8], group 32, 64 or 128,
+ * K a multiple of group, the batch's activations within shared memory
+ * (8 rows of K up to ~5,500). Errors (before anything is enqueued): NULL or
+ * misaligned pointers -> NC_ERR_INVALID_ARGUMENT, other sizes -> NC_ERR_SHAPE. */
+nc_status nc_int4_gemv(const float* x, const void* gamma, float eps, const uint8_t* Wq,
+                       const float* scales, int group, int B, int K, int N, float* y,
+                       void* stream);
+
 /* ---------------- sampling (nanoinfer, sampling section) -------------------- */
 
 /* Bytes of device scratch nc_sample needs for B rows of V logits at

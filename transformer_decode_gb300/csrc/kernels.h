@@ -124,6 +124,19 @@ cudaError_t launch_w8a8(Epi epi, const W8Args& a, cudaStream_t s);
 cudaError_t launch_quantize_weight(const uint16_t* W, int N, int K, int8_t* q, float* scale,
                                    cudaStream_t s);
 
+// ------------------------------------------------------------ INT4 weights
+struct Int4Args {
+  const float* x;         // [B, K]
+  const uint16_t* gamma;  // [K] RMSNorm gain, or null (no norm)
+  float eps;
+  const uint8_t* Wq;      // [N, K / 2]: two codes a byte, the even index in the low nibble
+  const float* scales;    // [N, K / group]
+  int group, B, K, N;
+  float* y;               // [B, N]
+};
+size_t int4_smem_bytes(int B, int K);  // the activations kept in shared memory
+cudaError_t launch_int4_gemv(const Int4Args& a, cudaStream_t s);
+
 // ------------------------------------------------------------ sampling
 // Scratch of nc_sample: per row five arrays of V rounded up to 64 words.
 size_t sample_scratch_bytes(int B, int V);

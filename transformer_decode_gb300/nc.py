@@ -32,7 +32,7 @@ EXPORTS = [
     "nc_get_device_status", "nc_rmsnorm_gemv", "nc_gemv_residual", "nc_swiglu_gemv",
     "nc_rope_qkv", "nc_attn_decode", "nc_lm_head_argmax", "nc_quantize_weight", "nc_w8a8_gemv",
     "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile", "nc_decode_path",
-    "nc_sample", "nc_sample_scratch_bytes",
+    "nc_sample", "nc_sample_scratch_bytes", "nc_int4_gemv",
 ]
 
 
@@ -120,6 +120,7 @@ def _declare(L):
     L.nc_read_phase_profile.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), i, C.POINTER(i)]
     L.nc_sample.argtypes = [vp, i, i, f, i, f, vp, vp, vp, vp, C.c_size_t, vp]
     L.nc_sample_scratch_bytes.argtypes = [i, i]
+    L.nc_int4_gemv.argtypes = [vp, vp, f, vp, vp, i, i, i, i, vp, vp]
     for n in EXPORTS:
         if n not in ("nc_status_string", "nc_last_error_message", "nc_sample_scratch_bytes"):
             getattr(L, n).restype = C.c_int
@@ -215,6 +216,18 @@ def attn_decode_static(shape, layer, q, positions, positions_host, kv, out, stre
         _ptr(q, torch.float32, "q", B * shape.q_dim), _ptr(positions, torch.int32, "positions", B),
         ph.ctypes.data_as(C.c_void_p), C.byref(s),
         _ptr(out, torch.float32, "out", B * shape.q_dim), _stream(stream)))
+
+
+def int4_gemv(x, gamma, eps, Wq, scales, group, y, stream=None):
+    """nc_int4_gemv: y = dequantised INT4 weights (packed [N, K/2] uint8, fp32
+    scales [N, K/group]) times the (normed) activations x [B, K]."""
+    B, K = x.shape
+    N = Wq.shape[0]
+    _check(load().nc_int4_gemv(_ptr(x, torch.float32, "x"), _ptr(gamma, torch.bfloat16, "gamma"),
+                               float(eps), _ptr(Wq, torch.uint8, "Wq", N * K // 2),
+                               _ptr(scales, torch.float32, "scales", N * (K // group)),
+                               int(group), B, K, N, _ptr(y, torch.float32, "y", B * N),
+                               _stream(stream)))
 
 
 # ------------------------------------------------------------------ sampling
