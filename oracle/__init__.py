@@ -58,7 +58,8 @@ class Layer(C.Structure):
 class Model(C.Structure):
     _fields_ = [("cfg", Config), ("embed", C.POINTER(C.c_uint16)),
                 ("lm_head", C.POINTER(C.c_uint16)), ("g_final", C.POINTER(C.c_uint16)),
-                ("layers", C.POINTER(Layer)), ("w8a8", C.c_int)]
+                ("layers", C.POINTER(Layer)), ("w8a8", C.c_int), ("act_block", C.c_int),
+                ("q8_embed", C.POINTER(C.c_int8)), ("s_embed", C.POINTER(C.c_float))]
 
 
 class KV(C.Structure):
@@ -105,6 +106,7 @@ def _declare(L):
         g("softmax").argtypes = [rp, C.c_int, rp]
         g("attention_head").argtypes = [rp, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, rp]
         g("linear_w8a8").argtypes = [i8p, f32p, u16p, C.c_int, C.c_int, rp, rp]
+        g("linear_w8a8_blocked").argtypes = [i8p, f32p, u16p, C.c_int, C.c_int, C.c_int, rp, rp]
         g("block_decode").argtypes = [C.POINTER(Model), C.c_int, C.POINTER(KV), C.c_int,
                                       C.c_int, rp]
         g("decode_step").argtypes = [C.POINTER(Model), C.POINTER(KV), C.c_int, i32p, i32p,
@@ -265,6 +267,21 @@ def linear_w8a8(w8, sw, bias, x, prec="f32"):
     return y
 
 
+def linear_w8a8_blocked(w8, sw, bias, x, block=32, prec="f32"):
+    """W8A8 with activations quantised per block of `block` values."""
+    dt, ct = _real(prec)
+    w8 = _np(w8, np.int8)
+    sw = _np(sw, np.float32)
+    bias = _np(bias, np.uint16)
+    x = _np(x, dt)
+    n, k = w8.shape
+    y = np.empty(n, dt)
+    getattr(lib(), f"orc_linear_w8a8_blocked_{prec}")(_p(w8, C.c_int8), _p(sw, C.c_float),
+                                                     _p(bias, C.c_uint16), n, k, int(block),
+                                                     _p(x, ct), _p(y, ct))
+    return y
+
+
 def argmax(v):
     v = np.ascontiguousarray(v)
     if v.dtype == np.float64:
@@ -296,9 +313,12 @@ class OracleModel:
     weights: the dict produced by the seeded generator (torch or numpy, bf16).
     w8a8: if True, each layer's seven projections are quantised per output
     row by the oracle's own weight quantiser and the int8 path is used.
+    act_block: with w8a8, 0 quantises each token's activations with one
+    scale; 32 uses one scale per block of 32 values.
+    int8_embed: the embedding (and the tied head) is stored int8 per row too.
     """
 
-    def __init__(self, shape, weights, w8a8=False):
+    def __init__(self, shape, weights, w8a8=False, act_block=0, int8_embed=False):
         self.shape = shape
         self._keep = []
         cfg = Config(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
@@ -325,8 +345,14 @@ class OracleModel:
         gf = _np(weights["g_final"], np.uint16)
         self._keep += [emb, head, gf, layers]
         self.layers = layers
+        q8e = se = None
+        if int8_embed:
+            q8e, se = quantize_weight(emb)
+            self._keep += [q8e, se]
+        self.q8_embed = (q8e, se)
         self.struct = Model(cfg, _p(emb, C.c_uint16), _p(head, C.c_uint16),
-                            _p(gf, C.c_uint16), layers, int(w8a8))
+                            _p(gf, C.c_uint16), layers, int(w8a8), int(act_block),
+                            _p(q8e, C.c_int8), _p(se, C.c_float))
 
     def new_kv(self, batch, max_ctx, bf16=False):
         return OracleKV(self.shape, batch, max_ctx, bf16)

@@ -78,6 +78,12 @@ typedef struct {
   const uint16_t *g_final;  /* [H] */
   const orc_layer *layers;  /* [L] */
   int w8a8;                 /* projections use the int8 fields */
+  int act_block;            /* w8a8: 0 = one activation scale per token; n > 0 = one per
+                               block of n values (nanoinfer, INT8 activation section:
+                               "one per 32") */
+  const int8_t* q8_embed;   /* [V, H] int8 rows with one fp32 scale each (s_embed), or
+                               NULL: the embedding, and the tied head, stored int8 */
+  const float* s_embed;     /* [V] */
 } orc_model;
 
 /* Logical KV cache: k, v are [L][B][Hkv][max_ctx][D] of fp32 (bf16 = 0, the
@@ -125,6 +131,9 @@ void orc_rope_inv_freq(double theta, int d, float* inv_freq);
                                 int n_pos, int d, REAL* out);                            \
   void orc_linear_w8a8_##SFX(const int8_t* w, const float* sw, const uint16_t* bias,     \
                              int n, int k, const REAL* x, REAL* y);                       \
+  void orc_linear_w8a8_blocked_##SFX(const int8_t* w, const float* sw,                   \
+                                     const uint16_t* bias, int n, int k, int block,       \
+                                     const REAL* x, REAL* y);                             \
   void orc_block_decode_##SFX(const orc_model* m, int layer, orc_kv* kv, int b, int pos,  \
                               REAL* x);                                                  \
   int orc_decode_step_##SFX(const orc_model* m, orc_kv* kv, int batch,                   \

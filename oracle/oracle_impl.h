@@ -155,12 +155,69 @@ void F(orc_linear_w8a8)(const int8_t* w, const float* sw, const uint16_t* bias, 
   free(acc);
 }
 
+/* W8A8 with activations in blocks of `block` values (nanoinfer, INT8
+ * activation section: one scale per 32, so an outlier widens only its own
+ * block): each block is quantised as a row is, acc[j, b] is the int32 sum of
+ * block b (int64, checked), and y[j] = sum_b float(acc[j, b]) * (sw[j] * sx[b])
+ * in block order, then + bias. A ragged last block is shorter. */
+void F(orc_linear_w8a8_blocked)(const int8_t* w, const float* sw, const uint16_t* bias, int n,
+                                int k, int block, const REAL* x, REAL* y) {
+  const int nb = (k + block - 1) / block;
+  float* xf = (float*)malloc(sizeof(float) * (size_t)k);
+  int8_t* xq = (int8_t*)malloc((size_t)k);
+  float* sx = (float*)malloc(sizeof(float) * (size_t)nb);
+  for (int i = 0; i < k; ++i) xf[i] = (float)x[i];
+  for (int b = 0; b < nb; ++b) {
+    const int len = k - b * block < block ? k - b * block : block;
+    sx[b] = orc_quantize_row_f32(xf + (long)b * block, len, xq + (long)b * block);
+  }
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+  for (int j = 0; j < n; ++j) {
+    REAL t = 0;
+    for (int b = 0; b < nb; ++b) {
+      const int i1 = (b + 1) * block < k ? (b + 1) * block : k;
+      int64_t acc = 0;
+      for (int i = b * block; i < i1; ++i) acc += (int64_t)w[(long)j * k + i] * (int64_t)xq[i];
+      if (acc > INT32_MAX || acc < INT32_MIN) bad = 1;
+      t += (REAL)(int32_t)acc * ((REAL)sw[j] * (REAL)sx[b]);
+    }
+    if (bias) t += F(widen)(bias[j]);
+    y[j] = t;
+  }
+  if (bad) abort();
+  free(xf);
+  free(xq);
+  free(sx);
+}
+
+/* The W8A8 product in the model's activation mode. */
+static void F(linear_i8)(const orc_model* m, const int8_t* w8, const float* sw,
+                         const uint16_t* bias, int n, int k, const REAL* x, REAL* y) {
+  if (m->act_block > 0)
+    F(orc_linear_w8a8_blocked)(w8, sw, bias, n, k, m->act_block, x, y);
+  else
+    F(orc_linear_w8a8)(w8, sw, bias, n, k, x, y);
+}
+
+/* The residual row of a token: the bf16 embedding widened, or an int8 row
+ * times its scale (the product rounded to fp32). */
+static void F(embed_row)(const orc_model* m, int tok, REAL* x) {
+  const int H = m->cfg.hidden;
+  if (m->q8_embed) {
+    for (int i = 0; i < H; ++i)
+      x[i] = (REAL)((float)m->q8_embed[(long)tok * H + i] * m->s_embed[tok]);
+    return;
+  }
+  for (int i = 0; i < H; ++i) x[i] = F(widen)(m->embed[(long)tok * H + i]);
+}
+
 /* y = W x + b for one of a layer's projections, bf16 or W8A8. */
 static void F(project)(const orc_model* m, const uint16_t* w, const int8_t* w8,
                        const float* sw, const uint16_t* bias, int n, int k, const REAL* x,
                        REAL* y) {
   if (m->w8a8) {
-    F(orc_linear_w8a8)(w8, sw, bias, n, k, x, y);
+    F(linear_i8)(m, w8, sw, bias, n, k, x, y);
     return;
   }
   F(orc_matvec_bf16)(w, n, k, x, y);
@@ -258,7 +315,11 @@ static void F(head)(const orc_model* m, const REAL* x, REAL* logits) {
   const orc_config* c = &m->cfg;
   REAL* n = (REAL*)malloc(sizeof(REAL) * (size_t)c->hidden);
   F(orc_rmsnorm)(x, c->hidden, m->g_final, c->rms_eps, n);
-  F(orc_matvec_bf16)(c->tie_embeddings ? m->embed : m->lm_head, c->vocab, c->hidden, n, logits);
+  if (m->q8_embed && c->tie_embeddings)  /* the int8 embedding is the head */
+    F(linear_i8)(m, m->q8_embed, m->s_embed, NULL, c->vocab, c->hidden, n, logits);
+  else
+    F(orc_matvec_bf16)(c->tie_embeddings ? m->embed : m->lm_head, c->vocab, c->hidden, n,
+                       logits);
   free(n);
 }
 
@@ -278,8 +339,7 @@ int F(orc_decode_step)(const orc_model* m, orc_kv* kv, int batch, const int32_t*
       rc = -1;
       break;
     }
-    const uint16_t* row = m->embed + (long)tokens[b] * H;
-    for (int i = 0; i < H; ++i) x[i] = F(widen)(row[i]);
+    F(embed_row)(m, tokens[b], x);
     if (hidden) memcpy(hidden + ((long)b * (L + 1)) * H, x, sizeof(REAL) * (size_t)H);
     for (int l = 0; l < L; ++l) {
       F(orc_block_decode)(m, l, kv, b, positions[b], x);
@@ -313,7 +373,7 @@ int F(orc_forward_chunk)(const orc_model* m, orc_kv* kv, int b, int n, const int
   REAL* v = (REAL*)malloc(sizeof(REAL) * (size_t)kd);
   REAL* a = (REAL*)malloc(sizeof(REAL) * (size_t)qd);
   for (int i = 0; i < n; ++i)
-    for (int j = 0; j < H; ++j) x[(long)i * H + j] = F(widen)(m->embed[(long)tokens[i] * H + j]);
+    F(embed_row)(m, tokens[i], x + (long)i * H);
   for (int l = 0; l < c->n_layers; ++l) {
     for (int i = 0; i < n; ++i) {
       F(qkv_token)(m, l, x + (long)i * H, start_pos + i, q + (long)i * qd, k, v);
@@ -363,7 +423,7 @@ int F(orc_forward_full)(const orc_model* m, int t, const int32_t* tokens, int kv
   REAL* p = (REAL*)malloc(sizeof(REAL) * (size_t)t);
   REAL scale = (REAL)1 / F(sqrtr)((REAL)D);
   for (int i = 0; i < t; ++i)
-    for (int j = 0; j < H; ++j) x[(long)i * H + j] = F(widen)(m->embed[(long)tokens[i] * H + j]);
+    F(embed_row)(m, tokens[i], x + (long)i * H);
   for (int l = 0; l < c->n_layers; ++l) {
     for (int i = 0; i < t; ++i) {
       F(qkv_token)(m, l, x + (long)i * H, i, q + (long)i * qd, k + (long)i * kd, v + (long)i * kd);

@@ -3,8 +3,9 @@ activations in blocks of 32, int8 embedding / LM-head rows, INT4 group-wise
 weights and their packing, and the byte footprint of each level.
 
 TEST INFRASTRUCTURE: only the tests, the smoke check and the benchmark's CPU
-baseline use this module. Plain numpy; every rounding that decides an integer
-is written out element by element in the precision stated.
+baseline use this module. Plain numpy: every step is an elementwise IEEE
+operation in the precision stated, and sums run in the order the definition
+gives (across rows at once, never reassociated).
 
 Definitions (nanoinfer, "Quantization" and the INT8 activation section):
 
@@ -55,11 +56,9 @@ def quantize_group(v: np.ndarray, levels: int):
     if amax == 0:
         return np.zeros(v.size, np.int8), F32(0)
     s = F32(amax / F32(levels))
-    q = np.empty(v.size, np.int8)
-    for i in range(v.size):
-        r = round_half_away(np.float32(v[i] / s))
-        q[i] = int(min(max(r, -levels), levels))
-    return q, s
+    # elementwise: each quotient an IEEE fp32 division, then the rounding rule
+    r = round_half_away((v / s).astype(np.float32))
+    return np.clip(r, -levels, levels).astype(np.int8), s
 
 
 # ------------------------------------------------------------------ int8
@@ -103,13 +102,13 @@ def linear_w8a8_blocked(wq, sw, bias, x, block: int = ACT_BLOCK):
     in blocks; bias (fp32 or None) added last. Returns (y, xq, sx, acc)."""
     xq, sx = quantize_blocks_i8(x, block)
     acc = matvec_i8_blocked(wq, xq, block)
-    n = acc.shape[0]
-    y = np.empty(n, np.float32)
-    for j in range(n):
-        t = F32(0)
-        for b in range(acc.shape[1]):
-            t = F32(t + F32(F32(acc[j, b]) * F32(sw[j] * sx[b])))
-        y[j] = t if bias is None else F32(t + F32(bias[j]))
+    sw = np.asarray(sw, np.float32)
+    # every row at once, the blocks in order: each step an fp32 product and an fp32 sum
+    t = np.zeros(acc.shape[0], np.float32)
+    for b in range(acc.shape[1]):
+        t = (t + (acc[:, b].astype(np.float32) * (sw * sx[b]).astype(np.float32))
+             .astype(np.float32)).astype(np.float32)
+    y = t if bias is None else (t + np.asarray(bias, np.float32)).astype(np.float32)
     return y, xq, sx, acc
 
 
@@ -169,13 +168,11 @@ def linear_int4(packed: np.ndarray, s: np.ndarray, group: int, x: np.ndarray, pr
     x = np.asarray(x, np.float32)
     if prec == "f64":
         return wd.astype(np.float64) @ x.astype(np.float64)
-    y = np.empty(wd.shape[0], np.float32)
-    for j in range(wd.shape[0]):
-        t = F32(0)
-        for kk in range(wd.shape[1]):
-            t = F32(t + F32(wd[j, kk] * x[kk]))
-        y[j] = t
-    return y
+    # every row at once, k in index order: each step an fp32 product and an fp32 sum
+    t = np.zeros(wd.shape[0], np.float32)
+    for kk in range(wd.shape[1]):
+        t = (t + (wd[:, kk] * x[kk]).astype(np.float32)).astype(np.float32)
+    return t
 
 
 # ------------------------------------------------------------------ footprints

@@ -245,60 +245,74 @@ def test_whole_model_matches_torch_library_composition(which, request):
     assert _rel_l2(got, _torch_forward(m.shape, w2, toks.tolist())) > 1e-4
 
 
-def test_w8a8_model_matches_composition_with_the_numpy_quantiser(orc):
-    """The C oracle's W8A8 model against the architecture composed from torch
-    routines with every projection replaced by the numpy quantiser's W8A8
-    product (oracle/quant.py, written separately: per-row int8 weights,
-    per-token int8 activations, int32 sums, float(acc) * (s_w * s_x) + bias).
-    The two reach the quantised activations by different summation orders,
-    so a code can flip at a rounding boundary: the gate is 1e-2, while a
-    wiring mistake (a scale of the wrong row, the bias before the scale)
-    moves the logits by far more."""
+def _w8a8_composition(s, w, toks, block=None, int8_embed=False, wrong_row=False):
+    """The architecture from torch routines in fp64 with every projection (and,
+    with int8_embed, the embedding and the tied head) replaced by the numpy
+    quantiser's W8A8 product: per-row int8 weights, activations per token
+    (block None) or per block, int32 sums, float(acc) * (s_w * s_x) + bias."""
     from oracle import quant
     F = torch.nn.functional
-    s = synth.TINY
-    w = synth.model_weights(s, seed=0)
-    m8 = orc.OracleModel(s, w, w8a8=True)
-    toks = synth.token_ids(6, s.vocab, stream=12)
-    got = m8.forward_full(toks, "f32")
 
-    def lin8(W, b, X, wrong_row=False):
-        wq, sw = quant.quantize_rows_i8(W.float().numpy())
-        if wrong_row:
+    def lin8(Wf, b, X, bad=False):
+        wq, sw = quant.quantize_rows_i8(Wf)
+        if bad:
             sw = sw[::-1].copy()  # row j dequantised with row N-1-j's scale
         bias = None if b is None else b.float().numpy()
-        out = [quant.linear_w8a8_blocked(wq, sw, bias, x, block=x.size)[0]
+        out = [quant.linear_w8a8_blocked(wq, sw, bias, x, block=block or x.size)[0]
                for x in X.numpy().astype(np.float32)]
         return torch.tensor(np.stack(out), dtype=torch.float64)
 
-    def forward(wrong_row=False):
-        H, D, G, T = s.hidden, s.head_dim, s.group, len(toks)
-        x = w["embed"].double()[torch.as_tensor(toks.tolist(), dtype=torch.long)]
-        half = D // 2
-        inv = torch.tensor([1.0 / s.rope_theta ** (2 * i / D) for i in range(half)],
-                           dtype=torch.float64)
-        rot = torch.polar(torch.ones(T, half, dtype=torch.float64),
-                          torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :])
-        rope = lambda t: torch.cat([(z := torch.complex(t[..., :half], t[..., half:]) * rot).real,
-                                    z.imag], -1)
-        for lw in w["layers"]:
-            n = F.rms_norm(x, (H,), lw["g_attn"].double(), s.rms_eps)
-            q = lin8(lw["wq"], lw["bq"], n, wrong_row).view(T, -1, D).transpose(0, 1)
-            k = lin8(lw["wk"], lw["bk"], n, wrong_row).view(T, -1, D).transpose(0, 1)
-            v = lin8(lw["wv"], lw["bv"], n, wrong_row).view(T, -1, D).transpose(0, 1)
-            q, k = rope(q), rope(k)
-            a = F.scaled_dot_product_attention(q[None], k.repeat_interleave(G, 0)[None],
-                                               v.repeat_interleave(G, 0)[None], is_causal=True)[0]
-            x = x + lin8(lw["wo"], None, a.transpose(0, 1).reshape(T, -1), wrong_row)
-            n2 = F.rms_norm(x, (H,), lw["g_mlp"].double(), s.rms_eps)
-            x = x + lin8(lw["wd"], None, F.silu(lin8(lw["wg"], None, n2, wrong_row))
-                         * lin8(lw["wu"], None, n2, wrong_row), wrong_row)
-        e = w["embed"].double()
-        return F.linear(F.rms_norm(x, (H,), w["g_final"].double(), s.rms_eps), e).numpy()
+    f = lambda t: t.float().numpy()
+    H, D, G, T = s.hidden, s.head_dim, s.group, len(toks)
+    idx = torch.as_tensor(toks.tolist(), dtype=torch.long)
+    if int8_embed:
+        eq, es = quant.quantize_rows_i8(f(w["embed"]))
+        x = torch.tensor(np.stack([quant.embed_i8(eq, es, int(t)) for t in toks]),
+                         dtype=torch.float64)
+    else:
+        x = w["embed"].double()[idx]
+    half = D // 2
+    inv = torch.tensor([1.0 / s.rope_theta ** (2 * i / D) for i in range(half)],
+                       dtype=torch.float64)
+    rot = torch.polar(torch.ones(T, half, dtype=torch.float64),
+                      torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :])
+    rope = lambda t: torch.cat([(z := torch.complex(t[..., :half], t[..., half:]) * rot).real,
+                                z.imag], -1)
+    bad = wrong_row
+    for lw in w["layers"]:
+        n = F.rms_norm(x, (H,), lw["g_attn"].double(), s.rms_eps)
+        q = lin8(f(lw["wq"]), lw["bq"], n, bad).view(T, -1, D).transpose(0, 1)
+        k = lin8(f(lw["wk"]), lw["bk"], n, bad).view(T, -1, D).transpose(0, 1)
+        v = lin8(f(lw["wv"]), lw["bv"], n, bad).view(T, -1, D).transpose(0, 1)
+        q, k = rope(q), rope(k)
+        a = F.scaled_dot_product_attention(q[None], k.repeat_interleave(G, 0)[None],
+                                           v.repeat_interleave(G, 0)[None], is_causal=True)[0]
+        x = x + lin8(f(lw["wo"]), None, a.transpose(0, 1).reshape(T, -1), bad)
+        n2 = F.rms_norm(x, (H,), lw["g_mlp"].double(), s.rms_eps)
+        x = x + lin8(f(lw["wd"]), None, F.silu(lin8(f(lw["wg"]), None, n2, bad))
+                     * lin8(f(lw["wu"]), None, n2, bad), bad)
+    nf = F.rms_norm(x, (H,), w["g_final"].double(), s.rms_eps)
+    if int8_embed:
+        return lin8(f(w["embed"]), None, nf).numpy()
+    return F.linear(nf, w["embed"].double()).numpy()
 
-    err = _rel_l2(got, forward())
+
+@pytest.mark.parametrize("block,int8_embed", [(None, False), (32, True)])
+def test_w8a8_model_matches_composition_with_the_numpy_quantiser(orc, block, int8_embed):
+    """The C oracle's W8A8 models (activations per token; per 32 with the
+    embedding and tied head int8 too) against the composition above. The two
+    reach the quantised activations by different summation orders, so a code
+    can flip at a rounding boundary: the gate is 1e-2, while a wiring mistake
+    (a scale of the wrong row) moves the logits by far more."""
+    s = synth.TINY
+    w = synth.model_weights(s, seed=0)
+    m8 = orc.OracleModel(s, w, w8a8=True, act_block=block or 0, int8_embed=int8_embed)
+    toks = synth.token_ids(6, s.vocab, stream=12)
+    got = m8.forward_full(toks, "f32")
+    err = _rel_l2(got, _w8a8_composition(s, w, toks, block, int8_embed))
     assert err < 1e-2, err
-    assert _rel_l2(got, forward(wrong_row=True)) > 10 * max(err, 1e-3)
+    bad = _rel_l2(got, _w8a8_composition(s, w, toks, block, int8_embed, wrong_row=True))
+    assert bad > 10 * max(err, 1e-3)
 
 
 def test_oracle_bits_do_not_depend_on_the_thread_count(orc, tiny, tiny_qk):
@@ -317,3 +331,31 @@ def test_oracle_bits_do_not_depend_on_the_thread_count(orc, tiny, tiny_qk):
                 assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
     finally:
         orc.set_threads(before)
+
+
+def test_blocked_w8a8_int8_embedding_model(orc):
+    """The oracle's int8 embedding / head with activations in blocks of 32:
+    the residual row is q * s exactly, the cached decode equals the uncached
+    forward, the head is the blocked W8A8 product of the final norm, and the
+    model stays near the bf16 one."""
+    from oracle import quant
+    s = synth.TINY
+    w = synth.model_weights(s, seed=0)
+    m = orc.OracleModel(s, w, w8a8=True, act_block=32, int8_embed=True)
+    eq, es = m.q8_embed
+    toks = synth.token_ids(6, s.vocab, stream=14)
+    kv = m.new_kv(1, 8)
+    for i in range(6):
+        lg, _, hid = m.decode_step(kv, toks[i:i + 1], np.array([i], np.int32), "f64",
+                                   hidden=True)
+    assert np.array_equal(hid[0, 0], quant.embed_i8(eq, es, int(toks[5])).astype(np.float64))
+    full = m.forward_full(toks, "f64")
+    assert _rel_l2(lg[0], full[-1]) < 1e-14
+    n = orc.rmsnorm(hid[0, -1], w["g_final"], s.rms_eps, "f64")
+    assert np.allclose(orc.linear_w8a8_blocked(eq, es, None, n, 32, "f64"), lg[0], rtol=1e-14,
+                       atol=1e-14)
+    bf = orc.OracleModel(s, w).forward_full(toks, "f64")
+    assert 0 < _rel_l2(full, bf) < 0.1
+    # per-32 blocks sit closer to the bf16 model than one scale per token
+    per_tok = orc.OracleModel(s, w, w8a8=True, int8_embed=True).forward_full(toks, "f64")
+    assert _rel_l2(full, bf) < _rel_l2(per_tok, bf)

@@ -178,3 +178,24 @@ def test_int8_embedding_rows():
         row = quant.embed_i8(eq, es, t)
         assert np.array_equal(row, eq[t].astype(np.float32) * es[t])
         assert np.abs(row - e[t]).max() <= es[t] * (0.5 + 1e-6)
+
+
+@pytest.mark.parametrize("K", [96, 100, 896, 4864])
+def test_c_blocked_linear_equals_the_numpy_quantiser(orc, K):
+    """The C oracle's blocked W8A8 product and oracle/quant.py, written
+    separately, agree bit for bit in fp32 (same quantiser, same block-order
+    epilogue), including a ragged last block (K = 100)."""
+    rng = np.random.default_rng(K)
+    N = 40
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    wq, sw = quant.quantize_rows_i8(w)
+    x = rng.standard_normal(K).astype(np.float32)
+    x[3] *= 68.0
+    bias16 = orc.f32_to_bf16((rng.standard_normal(N) * 0.02).astype(np.float32))
+    y_c = orc.linear_w8a8_blocked(wq, sw, bias16, x, 32)
+    y_n, _, _, _ = quant.linear_w8a8_blocked(wq, sw, orc.bf16_to_f32(bias16), x, 32)
+    assert np.array_equal(np.asarray(y_c, np.float32).view(np.uint32), y_n.view(np.uint32))
+    # one block as wide as the row is the per-token path
+    y_row = orc.linear_w8a8(wq, sw, bias16, x)
+    y_one = orc.linear_w8a8_blocked(wq, sw, bias16, x, K)
+    assert np.array_equal(np.asarray(y_row, np.float32), np.asarray(y_one, np.float32))
