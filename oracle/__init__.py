@@ -46,20 +46,25 @@ _LAYER_U16 = ["wq", "wk", "wv", "bq", "bk", "bv", "wo", "wg", "wu", "wd",
               "g_attn", "g_mlp", "g_q", "g_k"]
 _LAYER_I8 = ["q8_wq", "q8_wk", "q8_wv", "q8_wo", "q8_wg", "q8_wu", "q8_wd"]
 _LAYER_F32 = ["s_wq", "s_wk", "s_wv", "s_wo", "s_wg", "s_wu", "s_wd"]
+_LAYER_U8_4 = ["q4_wq", "q4_wk", "q4_wv", "q4_wo", "q4_wg", "q4_wu", "q4_wd"]
+_LAYER_F32_4 = ["s4_wq", "s4_wk", "s4_wv", "s4_wo", "s4_wg", "s4_wu", "s4_wd"]
 PROJ = ["wq", "wk", "wv", "wo", "wg", "wu", "wd"]
 
 
 class Layer(C.Structure):
     _fields_ = ([(n, C.POINTER(C.c_uint16)) for n in _LAYER_U16]
                 + [(n, C.POINTER(C.c_int8)) for n in _LAYER_I8]
-                + [(n, C.POINTER(C.c_float)) for n in _LAYER_F32])
+                + [(n, C.POINTER(C.c_float)) for n in _LAYER_F32]
+                + [(n, C.POINTER(C.c_uint8)) for n in _LAYER_U8_4]
+                + [(n, C.POINTER(C.c_float)) for n in _LAYER_F32_4])
 
 
 class Model(C.Structure):
     _fields_ = [("cfg", Config), ("embed", C.POINTER(C.c_uint16)),
                 ("lm_head", C.POINTER(C.c_uint16)), ("g_final", C.POINTER(C.c_uint16)),
                 ("layers", C.POINTER(Layer)), ("w8a8", C.c_int), ("act_block", C.c_int),
-                ("q8_embed", C.POINTER(C.c_int8)), ("s_embed", C.POINTER(C.c_float))]
+                ("q8_embed", C.POINTER(C.c_int8)), ("s_embed", C.POINTER(C.c_float)),
+                ("int4_group", C.c_int)]
 
 
 class KV(C.Structure):
@@ -107,6 +112,8 @@ def _declare(L):
         g("attention_head").argtypes = [rp, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, rp]
         g("linear_w8a8").argtypes = [i8p, f32p, u16p, C.c_int, C.c_int, rp, rp]
         g("linear_w8a8_blocked").argtypes = [i8p, f32p, u16p, C.c_int, C.c_int, C.c_int, rp, rp]
+        g("linear_int4").argtypes = [C.POINTER(C.c_uint8), f32p, C.c_int, u16p, C.c_int,
+                                     C.c_int, rp, rp]
         g("block_decode").argtypes = [C.POINTER(Model), C.c_int, C.POINTER(KV), C.c_int,
                                       C.c_int, rp]
         g("decode_step").argtypes = [C.POINTER(Model), C.POINTER(KV), C.c_int, i32p, i32p,
@@ -282,6 +289,23 @@ def linear_w8a8_blocked(w8, sw, bias, x, block=32, prec="f32"):
     return y
 
 
+def linear_int4(packed, s4, group, bias, x, prec="f32"):
+    """y = the INT4 group-wise rows (packed [N, K/2] uint8, scales [N, K/group])
+    times x, + bias."""
+    dt, ct = _real(prec)
+    packed = _np(packed, np.uint8)
+    s4 = _np(s4, np.float32)
+    bias = _np(bias, np.uint16)
+    x = _np(x, dt)
+    n = packed.shape[0]
+    k = 2 * packed.shape[1]
+    y = np.empty(n, dt)
+    getattr(lib(), f"orc_linear_int4_{prec}")(_p(packed, C.c_uint8), _p(s4, C.c_float),
+                                             int(group), _p(bias, C.c_uint16), n, k,
+                                             _p(x, ct), _p(y, ct))
+    return y
+
+
 def argmax(v):
     v = np.ascontiguousarray(v)
     if v.dtype == np.float64:
@@ -316,9 +340,12 @@ class OracleModel:
     act_block: with w8a8, 0 quantises each token's activations with one
     scale; 32 uses one scale per block of 32 values.
     int8_embed: the embedding (and the tied head) is stored int8 per row too.
+    int4_group: > 0 stores the seven projections as INT4 with one scale per
+    group of that many weights (quantised by oracle/quant.py), fp32 activations.
     """
 
-    def __init__(self, shape, weights, w8a8=False, act_block=0, int8_embed=False):
+    def __init__(self, shape, weights, w8a8=False, act_block=0, int8_embed=False,
+                 int4_group=0):
         self.shape = shape
         self._keep = []
         cfg = Config(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
@@ -332,6 +359,16 @@ class OracleModel:
                 a = _np(lw.get(n), np.uint16)
                 self._keep.append(a)
                 setattr(layers[l], n, _p(a, C.c_uint16))
+            if int4_group:
+                from . import quant
+                for n in PROJ:
+                    wf = bf16_to_f32(_np(lw[n], np.uint16))
+                    q4, s4 = quant.quantize_int4(wf, int4_group)
+                    p4 = quant.pack_int4(q4)
+                    q8l["int4_" + n] = (p4, s4)
+                    self._keep += [p4, s4]
+                    setattr(layers[l], "q4_" + n, _p(p4, C.c_uint8))
+                    setattr(layers[l], "s4_" + n, _p(s4, C.c_float))
             if w8a8:
                 for n in PROJ:
                     q, s = quantize_weight(lw[n])
@@ -352,7 +389,7 @@ class OracleModel:
         self.q8_embed = (q8e, se)
         self.struct = Model(cfg, _p(emb, C.c_uint16), _p(head, C.c_uint16),
                             _p(gf, C.c_uint16), layers, int(w8a8), int(act_block),
-                            _p(q8e, C.c_int8), _p(se, C.c_float))
+                            _p(q8e, C.c_int8), _p(se, C.c_float), int(int4_group))
 
     def new_kv(self, batch, max_ctx, bf16=False):
         return OracleKV(self.shape, batch, max_ctx, bf16)

@@ -69,6 +69,11 @@ typedef struct {
   const uint16_t *g_attn, *g_mlp, *g_q, *g_k;
   const int8_t *q8_wq, *q8_wk, *q8_wv, *q8_wo, *q8_wg, *q8_wu, *q8_wd;
   const float *s_wq, *s_wk, *s_wv, *s_wo, *s_wg, *s_wu, *s_wd;
+  /* INT4 form (orc_model.int4_group > 0): packed codes [out, in / 2], two a
+   * byte with the even index in the low nibble, and fp32 scales
+   * [out, in / group] */
+  const uint8_t *q4_wq, *q4_wk, *q4_wv, *q4_wo, *q4_wg, *q4_wu, *q4_wd;
+  const float *s4_wq, *s4_wk, *s4_wv, *s4_wo, *s4_wg, *s4_wu, *s4_wd;
 } orc_layer;
 
 typedef struct {
@@ -84,6 +89,8 @@ typedef struct {
   const int8_t* q8_embed;   /* [V, H] int8 rows with one fp32 scale each (s_embed), or
                                NULL: the embedding, and the tied head, stored int8 */
   const float* s_embed;     /* [V] */
+  int int4_group;           /* > 0: the projections use the INT4 fields, one scale per
+                               group of this many weights (nanoinfer "Quantization") */
 } orc_model;
 
 /* Logical KV cache: k, v are [L][B][Hkv][max_ctx][D] of fp32 (bf16 = 0, the
@@ -134,6 +141,8 @@ void orc_rope_inv_freq(double theta, int d, float* inv_freq);
   void orc_linear_w8a8_blocked_##SFX(const int8_t* w, const float* sw,                   \
                                      const uint16_t* bias, int n, int k, int block,       \
                                      const REAL* x, REAL* y);                             \
+  void orc_linear_int4_##SFX(const uint8_t* w4, const float* s4, int group,              \
+                             const uint16_t* bias, int n, int k, const REAL* x, REAL* y); \
   void orc_block_decode_##SFX(const orc_model* m, int layer, orc_kv* kv, int b, int pos,  \
                               REAL* x);                                                  \
   int orc_decode_step_##SFX(const orc_model* m, orc_kv* kv, int batch,                   \

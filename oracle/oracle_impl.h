@@ -191,6 +191,29 @@ void F(orc_linear_w8a8_blocked)(const int8_t* w, const float* sw, const uint16_t
   free(sx);
 }
 
+/* INT4 group-wise weights (nanoinfer "Quantization": fifteen symmetric levels,
+ * one fp32 scale per group of `group` weights of a row; two codes a byte, the
+ * even index in the low nibble): y[j] = sum_i float(q[j, i] * s[j, i / group])
+ * * x[i] in index order (the dequantised weight rounded to fp32, as in the
+ * page's quantise-dequantise evaluation), then + bias. */
+void F(orc_linear_int4)(const uint8_t* w4, const float* s4, int group, const uint16_t* bias,
+                        int n, int k, const REAL* x, REAL* y) {
+  const int ng = (k + group - 1) / group;
+#pragma omp parallel for schedule(static)
+  for (int j = 0; j < n; ++j) {
+    REAL t = 0;
+    for (int i = 0; i < k; ++i) {
+      const uint8_t byte = w4[(long)j * (k / 2) + i / 2];
+      int q = (i & 1) ? (byte >> 4) : (byte & 0xF);
+      if (q >= 8) q -= 16;
+      const float wd = (float)q * s4[(long)j * ng + i / group];
+      t += (REAL)wd * x[i];
+    }
+    if (bias) t += F(widen)(bias[j]);
+    y[j] = t;
+  }
+}
+
 /* The W8A8 product in the model's activation mode. */
 static void F(linear_i8)(const orc_model* m, const int8_t* w8, const float* sw,
                          const uint16_t* bias, int n, int k, const REAL* x, REAL* y) {
@@ -214,10 +237,14 @@ static void F(embed_row)(const orc_model* m, int tok, REAL* x) {
 
 /* y = W x + b for one of a layer's projections, bf16 or W8A8. */
 static void F(project)(const orc_model* m, const uint16_t* w, const int8_t* w8,
-                       const float* sw, const uint16_t* bias, int n, int k, const REAL* x,
-                       REAL* y) {
+                       const float* sw, const uint8_t* w4, const float* s4,
+                       const uint16_t* bias, int n, int k, const REAL* x, REAL* y) {
   if (m->w8a8) {
     F(linear_i8)(m, w8, sw, bias, n, k, x, y);
+    return;
+  }
+  if (m->int4_group > 0) {
+    F(orc_linear_int4)(w4, s4, m->int4_group, bias, n, k, x, y);
     return;
   }
   F(orc_matvec_bf16)(w, n, k, x, y);
@@ -238,9 +265,9 @@ static void F(qkv_token)(const orc_model* m, int layer, const REAL* x, int pos, 
   int H = c->hidden, D = c->head_dim, qd = c->n_q_heads * D, kd = c->n_kv_heads * D;
   REAL* n = (REAL*)malloc(sizeof(REAL) * (size_t)H);
   F(orc_rmsnorm)(x, H, w->g_attn, c->rms_eps, n);
-  F(project)(m, w->wq, w->q8_wq, w->s_wq, c->qkv_bias ? w->bq : NULL, qd, H, n, q);
-  F(project)(m, w->wk, w->q8_wk, w->s_wk, c->qkv_bias ? w->bk : NULL, kd, H, n, k);
-  F(project)(m, w->wv, w->q8_wv, w->s_wv, c->qkv_bias ? w->bv : NULL, kd, H, n, v);
+  F(project)(m, w->wq, w->q8_wq, w->s_wq, w->q4_wq, w->s4_wq, c->qkv_bias ? w->bq : NULL, qd, H, n, q);
+  F(project)(m, w->wk, w->q8_wk, w->s_wk, w->q4_wk, w->s4_wk, c->qkv_bias ? w->bk : NULL, kd, H, n, k);
+  F(project)(m, w->wv, w->q8_wv, w->s_wv, w->q4_wv, w->s4_wv, c->qkv_bias ? w->bv : NULL, kd, H, n, v);
   if (c->qk_norm) {
     for (int h = 0; h < c->n_q_heads; ++h) F(orc_rmsnorm)(q + h * D, D, w->g_q, c->rms_eps, q + h * D);
     for (int h = 0; h < c->n_kv_heads; ++h) F(orc_rmsnorm)(k + h * D, D, w->g_k, c->rms_eps, k + h * D);
@@ -259,13 +286,13 @@ static void F(post_attention)(const orc_model* m, int layer, const REAL* a, REAL
   REAL* n2 = (REAL*)malloc(sizeof(REAL) * (size_t)H);
   REAL* gate = (REAL*)malloc(sizeof(REAL) * (size_t)Fd);
   REAL* up = (REAL*)malloc(sizeof(REAL) * (size_t)Fd);
-  F(project)(m, w->wo, w->q8_wo, w->s_wo, NULL, H, qd, a, o);
+  F(project)(m, w->wo, w->q8_wo, w->s_wo, w->q4_wo, w->s4_wo, NULL, H, qd, a, o);
   for (int i = 0; i < H; ++i) x[i] = x[i] + o[i];
   F(orc_rmsnorm)(x, H, w->g_mlp, c->rms_eps, n2);
-  F(project)(m, w->wg, w->q8_wg, w->s_wg, NULL, Fd, H, n2, gate);
-  F(project)(m, w->wu, w->q8_wu, w->s_wu, NULL, Fd, H, n2, up);
+  F(project)(m, w->wg, w->q8_wg, w->s_wg, w->q4_wg, w->s4_wg, NULL, Fd, H, n2, gate);
+  F(project)(m, w->wu, w->q8_wu, w->s_wu, w->q4_wu, w->s4_wu, NULL, Fd, H, n2, up);
   for (int j = 0; j < Fd; ++j) gate[j] = F(orc_silu)(gate[j]) * up[j];
-  F(project)(m, w->wd, w->q8_wd, w->s_wd, NULL, H, Fd, gate, o);
+  F(project)(m, w->wd, w->q8_wd, w->s_wd, w->q4_wd, w->s4_wd, NULL, H, Fd, gate, o);
   for (int i = 0; i < H; ++i) x[i] = x[i] + o[i];
   free(o);
   free(n2);

@@ -81,3 +81,29 @@ def test_reference_arm_under_torchrun_prints_one_line(tmp_path):
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_step_bytes_against_the_page_counts():
+    """The roofline's algorithmic bytes: every parameter read once per step
+    (the tied embedding as the head) is 2 bytes x the nanoinfer page's
+    494,032,768 parameters; the embedding row, the K/V of the cached
+    positions (24 KiB per token in fp32 across the 24 layers, the page's
+    figure), the new K/V, the logits and token/position words come on top."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from transformer_decode_gb300 import synth
+    s = synth.QWEN2_0P5B
+    total_params = 494032768
+    H, V = s.hidden, s.vocab
+    for p in (0, 31, 95):
+        want = (2 * total_params + 2 * H          # weights once, plus the gathered row
+                + (p + 1) * 24576 + 24576          # K/V read for slots 0..p, and written
+                + 4 * V + 8)                       # logits out, token and position in
+        assert bench.step_bytes(s, 1, [p]) == want
+    # the bf16 cache halves only the K/V terms
+    assert bench.step_bytes(s, 1, [95], kv_elem=2) == bench.step_bytes(s, 1, [95]) - 97 * 12288
+    # W8A8: the seven projections at one byte per weight plus one fp32 scale per row
+    proj = s.n_layers * ((s.q_dim + 2 * s.kv_dim) * H + s.q_dim * H + 3 * s.ffn * H)
+    rows = s.n_layers * ((s.q_dim + 2 * s.kv_dim) + H + 2 * s.ffn + H)
+    assert bench.step_bytes(s, 1, [95], w8a8=True) == \
+        bench.step_bytes(s, 1, [95]) - 2 * proj + proj + 4 * rows

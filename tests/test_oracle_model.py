@@ -359,3 +359,75 @@ def test_blocked_w8a8_int8_embedding_model(orc):
     # per-32 blocks sit closer to the bf16 model than one scale per token
     per_tok = orc.OracleModel(s, w, w8a8=True, int8_embed=True).forward_full(toks, "f64")
     assert _rel_l2(full, bf) < _rel_l2(per_tok, bf)
+
+
+def _int4_composition(s, w, toks, group, shift_scales=False):
+    """The architecture from torch routines in fp64 with every projection
+    replaced by the numpy INT4 product of the same weights (oracle/quant.py,
+    its fp64 form): W_deq x with W_deq = q * s rounded to fp32."""
+    from oracle import quant
+    F = torch.nn.functional
+    f = lambda t: t.float().numpy()
+
+    def lin4(Wt, b, X):
+        q, sc = quant.quantize_int4(f(Wt), group)
+        if shift_scales:
+            sc = np.roll(sc, 1, axis=1)  # each group dequantised with its neighbour's scale
+        wd = torch.tensor(quant.dequant_int4(q, sc, group), dtype=torch.float64)
+        return F.linear(X, wd, None if b is None else b.double())
+
+    H, D, G, T = s.hidden, s.head_dim, s.group, len(toks)
+    x = w["embed"].double()[torch.as_tensor(toks.tolist(), dtype=torch.long)]
+    half = D // 2
+    inv = torch.tensor([1.0 / s.rope_theta ** (2 * i / D) for i in range(half)],
+                       dtype=torch.float64)
+    rot = torch.polar(torch.ones(T, half, dtype=torch.float64),
+                      torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :])
+    rope = lambda t: torch.cat([(z := torch.complex(t[..., :half], t[..., half:]) * rot).real,
+                                z.imag], -1)
+    for lw in w["layers"]:
+        n = F.rms_norm(x, (H,), lw["g_attn"].double(), s.rms_eps)
+        q = lin4(lw["wq"], lw["bq"], n).view(T, -1, D).transpose(0, 1)
+        k = lin4(lw["wk"], lw["bk"], n).view(T, -1, D).transpose(0, 1)
+        v = lin4(lw["wv"], lw["bv"], n).view(T, -1, D).transpose(0, 1)
+        q, k = rope(q), rope(k)
+        a = F.scaled_dot_product_attention(q[None], k.repeat_interleave(G, 0)[None],
+                                           v.repeat_interleave(G, 0)[None], is_causal=True)[0]
+        x = x + lin4(lw["wo"], None, a.transpose(0, 1).reshape(T, -1))
+        n2 = F.rms_norm(x, (H,), lw["g_mlp"].double(), s.rms_eps)
+        x = x + lin4(lw["wd"], None, F.silu(lin4(lw["wg"], None, n2)) * lin4(lw["wu"], None, n2))
+    return F.linear(F.rms_norm(x, (H,), w["g_final"].double(), s.rms_eps),
+                    w["embed"].double()).numpy()
+
+
+@pytest.mark.parametrize("group", [32, 128])
+def test_int4_model(orc, group):
+    """The oracle's INT4 model mode: no activation is quantised, so it meets
+    the torch composition with the numpy product at fp64 rounding (a shifted
+    group scale is caught), the cached decode equals the uncached forward,
+    and it stays near the bf16 model."""
+    s = synth.TINY
+    w = synth.model_weights(s, seed=0)
+    m = orc.OracleModel(s, w, int4_group=group)
+    toks = synth.token_ids(6, s.vocab, stream=15)
+    full = m.forward_full(toks, "f64")
+    ref = _int4_composition(s, w, toks, group)
+    assert _rel_l2(full, ref) < 1e-6
+    assert _rel_l2(full, _int4_composition(s, w, toks, group, shift_scales=True)) > 1e-3
+    kv = m.new_kv(1, 8)
+    for i in range(6):
+        lg, _ = m.decode_step(kv, toks[i:i + 1], np.array([i], np.int32), "f64")
+    assert _rel_l2(lg[0], full[-1]) < 1e-14
+    assert 0 < _rel_l2(full, orc.OracleModel(s, w).forward_full(toks, "f64")) < 0.5
+
+
+def test_int4_group_32_is_closer_to_bf16_than_128(orc):
+    """Smaller groups confine each large weight to fewer neighbours (the page:
+    group 32 cuts weight error from 12.3% to 9.9%)."""
+    s = synth.TINY
+    w = synth.model_weights(s, seed=0)
+    toks = synth.token_ids(6, s.vocab, stream=16)
+    bf = orc.OracleModel(s, w).forward_full(toks, "f64")
+    e32 = _rel_l2(orc.OracleModel(s, w, int4_group=32).forward_full(toks, "f64"), bf)
+    e128 = _rel_l2(orc.OracleModel(s, w, int4_group=128).forward_full(toks, "f64"), bf)
+    assert e32 < e128

@@ -199,3 +199,21 @@ def test_c_blocked_linear_equals_the_numpy_quantiser(orc, K):
     y_row = orc.linear_w8a8(wq, sw, bias16, x)
     y_one = orc.linear_w8a8_blocked(wq, sw, bias16, x, K)
     assert np.array_equal(np.asarray(y_row, np.float32), np.asarray(y_one, np.float32))
+
+
+@pytest.mark.parametrize("N,K,group", [(40, 64, 32), (17, 896, 128), (9, 4864, 32), (5, 192, 64)])
+def test_c_int4_linear_equals_the_numpy_product(orc, N, K, group):
+    """The C oracle's INT4 product and oracle/quant.py, written separately,
+    agree bit for bit in fp32: the same fp32 dequantised weights, the same
+    index-order sum."""
+    rng = np.random.default_rng(N + K)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w[:, 3] = 0.4
+    q, s = quant.quantize_int4(w, group)
+    p = quant.pack_int4(q)
+    x = rng.standard_normal(K).astype(np.float32)
+    y_c = np.asarray(orc.linear_int4(p, s, group, None, x), np.float32)
+    y_n = quant.linear_int4(p, s, group, x)
+    assert np.array_equal(y_c.view(np.uint32), y_n.view(np.uint32))
+    y64 = orc.linear_int4(p, s, group, None, x.astype(np.float64), "f64")
+    assert np.allclose(y64, quant.linear_int4(p, s, group, x, "f64"), rtol=1e-12, atol=1e-15)
