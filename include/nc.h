@@ -50,7 +50,13 @@ typedef enum {
   NC_ERR_UNSUPPORTED = 9
 } nc_status;
 
-typedef enum { NC_BF16 = 0, NC_INT8 = 1 } nc_wtype;
+/* Weight storage of the seven projections. NC_INT8: int8 per output row,
+ * activations quantised per token (W8A8). NC_INT4_G32 / NC_INT4_G128: INT4
+ * codes in [-7, 7] with one fp32 scale per group of 32 / 128 weights of a
+ * row, fp32 activations (nanoinfer "Quantization"); hidden, ffn and
+ * n_q_heads * head_dim must be multiples of the group. The embedding and
+ * the head stay bf16 in every type. */
+typedef enum { NC_BF16 = 0, NC_INT8 = 1, NC_INT4_G32 = 3, NC_INT4_G128 = 4 } nc_wtype;
 
 /* Hyperparameters. head_dim must be 64 or 128; n_q_heads a multiple of
  * n_kv_heads with group <= 8; hidden, ffn, n_q_heads*head_dim multiples of 8. */

@@ -81,7 +81,7 @@ def test_block_forward_0p5b_past16(paged, kv_bf16):
 # ------------------------------------------------------------------ greedy decode
 def _greedy_compare(shape, wd, wc, prompt, steps, batch=1, past=None, paged=False, w8a8=False,
                     use_graph=True, gate=REL_L2_GATE, kv_bf16=False, derived_gate=False,
-                    staged=False, noise_twins=0):
+                    staged=False, noise_twins=0, int4_group=0):
     """Teacher-forced greedy decode: both sides consume the oracle's token.
     Returns the worst logit rel-L2 seen.
 
@@ -98,11 +98,12 @@ def _greedy_compare(shape, wd, wc, prompt, steps, batch=1, past=None, paged=Fals
     that sits within that distance of a rounding boundary flips in the twins
     as it may on the GPU, and with random-init weights one such flip moves
     the logits by about 1e-2 (rel-L2)."""
-    om = oracle.OracleModel(shape, wc, w8a8=w8a8)
+    om = oracle.OracleModel(shape, wc, w8a8=w8a8, int4_group=int4_group)
     past = past or [0] * batch
     n_total = len(prompt[0]) + steps if prompt is not None else steps
     max_ctx = max(past) + n_total + 1
-    model = nc.Model(shape, wd, max_batch=batch, max_ctx=max_ctx + 16, w8a8=w8a8)
+    model = nc.Model(shape, wd, max_batch=batch, max_ctx=max_ctx + 16, w8a8=w8a8,
+                     int4_group=int4_group)
     kdt = torch.bfloat16 if kv_bf16 else torch.float32
     if paged:
         table, nblk = synth.block_tables(past, n_total, 16)
@@ -231,6 +232,18 @@ def test_decode_0p5b_w8a8_past512():
     worst = _greedy_compare(shape, wd, wc, None, steps=8, past=[512], w8a8=True,
                             derived_gate=True, noise_twins=2)
     print(f"0.5B W8A8: worst logit rel-L2 {worst:.3e}")
+
+
+@pytest.mark.parametrize("shape,group,past,steps", [(synth.TINY, 32, 0, 12),
+                                                     (synth.TINY, 128, 5, 12),
+                                                     (synth.QWEN2_0P5B, 128, 512, 8)])
+def test_decode_int4(shape, group, past, steps):
+    """INT4 group-wise projections (NC_INT4_G32 / NC_INT4_G128) against the
+    oracle's INT4 mode. Only weights are quantised (on the device, by the
+    same operations as the oracle's quantiser), so the plain 5e-4 gate holds."""
+    wd, wc = weights_both(shape)
+    worst = _greedy_compare(shape, wd, wc, None, steps=steps, past=[past], int4_group=group)
+    print(f"INT4 group {group} ({shape.hidden}): worst logit rel-L2 {worst:.3e}")
 
 
 @pytest.mark.parametrize("kv_bf16", [False, True])

@@ -289,7 +289,7 @@ nc_status nc_int4_gemv(const float* x, const void* gamma, float eps, const uint8
   NC_CHECK(int4_smem_bytes(B, K) + 4096 <= (size_t)max_smem_optin(), NC_ERR_SHAPE,
            "K = %d is too long to keep the batch's activations in shared memory", K);
   Int4Args a{x, static_cast<const uint16_t*>(gamma), eps, Wq, scales, group, B, K, N, y};
-  return launch_result(launch_int4_gemv(a, S(stream)), "nc_int4_gemv");
+  return launch_result(launch_int4_gemv(Epi::Store, a, S(stream)), "nc_int4_gemv");
 }
 
 size_t nc_sample_scratch_bytes(int B, int V) {

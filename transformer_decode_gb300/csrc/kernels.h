@@ -132,10 +132,13 @@ struct Int4Args {
   const uint8_t* Wq;      // [N, K / 2]: two codes a byte, the even index in the low nibble
   const float* scales;    // [N, K / group]
   int group, B, K, N;
-  float* y;               // [B, N]
+  float* y;               // [B, N] (Residual: in place); SwiGLU: Wq and scales hold 2N rows
+  const uint16_t* bias = nullptr;  // [N] bf16 or null (Store only)
 };
 size_t int4_smem_bytes(int B, int K);  // the activations kept in shared memory
-cudaError_t launch_int4_gemv(const Int4Args& a, cudaStream_t s);
+cudaError_t launch_int4_gemv(Epi epi, const Int4Args& a, cudaStream_t s);
+cudaError_t launch_quantize_int4(const uint16_t* W, int N, int K, int group, uint8_t* q,
+                                 float* sc, cudaStream_t s);
 
 // ------------------------------------------------------------ sampling
 // Scratch of nc_sample: per row five arrays of V rounded up to 64 words.

@@ -22,7 +22,7 @@ NC_OK = 0
 STATUS = ["NC_OK", "NC_ERR_INVALID_ARGUMENT", "NC_ERR_SHAPE", "NC_ERR_DTYPE", "NC_ERR_CAPACITY",
           "NC_ERR_POSITION", "NC_ERR_CUDA", "NC_ERR_TIMEOUT", "NC_ERR_UNHEALTHY",
           "NC_ERR_UNSUPPORTED"]
-NC_BF16, NC_INT8 = 0, 1
+NC_BF16, NC_INT8, NC_INT4_G32, NC_INT4_G128 = 0, 1, 3, 4
 NC_STEP_GRAPH, NC_STEP_ADVANCE, NC_STEP_STAGED = 1, 2, 4
 NC_KV_F32, NC_KV_BF16 = 0, 1
 
@@ -355,7 +355,8 @@ class Model:
     The model keeps its own packed copy; the caller may free the originals.
     """
 
-    def __init__(self, shape, weights, max_batch=1, max_ctx=4096, w8a8=False, stream=None):
+    def __init__(self, shape, weights, max_batch=1, max_ctx=4096, w8a8=False, int4_group=0,
+                 stream=None):
         L = load()
         self.shape = shape
         self.max_batch = max_batch
@@ -363,7 +364,8 @@ class Model:
         cfg = Config(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
                      shape.n_layers, shape.vocab, shape.rms_eps, shape.rope_theta,
                      int(shape.qkv_bias), int(shape.qk_norm), int(shape.tie_embeddings),
-                     NC_INT8 if w8a8 else NC_BF16)
+                     NC_INT8 if w8a8 else {0: NC_BF16, 32: NC_INT4_G32,
+                                           128: NC_INT4_G128}[int4_group])
         layers = (LayerWeights * shape.n_layers)()
         for l, lw in enumerate(weights["layers"]):
             for n in _LW:
