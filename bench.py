@@ -66,17 +66,23 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def step_bytes(shape, batch, positions, kv_elem=4, w8a8=False, int8_head=False):
+def step_bytes(shape, batch, positions, kv_elem=4, w8a8=False, int8_head=False,
+               int4_group=0):
     """Algorithmic HBM bytes of one decode step: every weight byte once, the
     embedding rows, K/V of slots 0..p read once per layer and kv head, the new
     K/V written, the logits written and tokens/positions read. kv_elem is the
     cache element size (4: fp32 cache, 2: bf16); w8a8: the seven projections
     are int8 with one fp32 scale per output row (the LM head stays bf16);
     int8_head: the tied embedding / head rows are int8 with one fp32 scale
-    each too."""
+    each too. int4_group: the projections are INT4, half a byte a weight and
+    one fp32 scale per group of that many weights."""
     H, D, F, L, V = shape.hidden, shape.head_dim, shape.ffn, shape.n_layers, shape.vocab
     nqkv = shape.q_dim + 2 * shape.kv_dim
-    if w8a8:
+    if int4_group:
+        g = int4_group
+        per_layer = (nqkv * H + shape.q_dim * H + 2 * F * H + H * F) // 2 + 4 * (
+            nqkv * (H // g) + H * (shape.q_dim // g) + 2 * F * (H // g) + H * (F // g))
+    elif w8a8:
         per_layer = (nqkv * H + shape.q_dim * H + 2 * F * H + H * F) + 4 * (nqkv + H + 2 * F + H)
     else:
         per_layer = 2 * (nqkv * H + shape.q_dim * H + 2 * F * H + H * F)
@@ -642,6 +648,8 @@ WORKLOADS = {
                                        gen=64, w8a8=True),
     "qwen2_0p5b_w8a8_b32_b1_past512": dict(shape="QWEN2_0P5B", batch=1, paged=False, past=512,
                                            gen=64, w8a8="b32"),
+    "qwen2_0p5b_int4_g128_b1_past512": dict(shape="QWEN2_0P5B", batch=1, paged=False,
+                                            past=512, gen=64, w8a8=False, int4=128),
 }
 ROUNDS = 5  # the timed region is reported as this many equal rounds as well
 
@@ -702,7 +710,7 @@ def oracle_for(cfg, max_ctx):
     past = workload_past(cfg)
     om = oracle.OracleModel(shape, cpu_weights(shape), w8a8=bool(cfg["w8a8"]),
                             act_block=32 if cfg["w8a8"] == "b32" else 0,
-                            int8_embed=cfg["w8a8"] == "b32")
+                            int8_embed=cfg["w8a8"] == "b32", int4_group=cfg.get("int4", 0))
     okv = om.new_kv(cfg["batch"], max_ctx)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     for l in range(shape.n_layers):
@@ -823,7 +831,8 @@ def run_workload(args, ws, rank, local, name):
     past = workload_past(cfg)
     wd = synth.model_weights(shape, device="cuda")
     max_ctx = max(past) + gen + 16
-    model = nc.Model(shape, wd, max_batch=B, max_ctx=max_ctx, w8a8=cfg["w8a8"])
+    model = nc.Model(shape, wd, max_batch=B, max_ctx=max_ctx, w8a8=cfg["w8a8"],
+                     int4_group=cfg.get("int4", 0))
     del wd
     torch.cuda.empty_cache()
     if cfg["paged"]:
@@ -872,7 +881,8 @@ def run_workload(args, ws, rank, local, name):
     value, el = replica_rate(ws, B, args.steps, total_s)
     dur = el / args.steps
     bytes_avg = sum(step_bytes(shape, B, u.tolist(), w8a8=bool(cfg["w8a8"]),
-                               int8_head=cfg["w8a8"] == "b32") for u in used) / len(used)
+                               int8_head=cfg["w8a8"] == "b32", int4_group=cfg.get("int4", 0))
+                    for u in used) / len(used)
     peak, peak_kind = peaks()
 
     # e2e: tokens and positions from pinned host memory, next tokens read back
@@ -925,13 +935,16 @@ def run_workload(args, ws, rank, local, name):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dur * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "i8/i32" if cfg["w8a8"] else "f32", "data": "synthetic",
+            "dtype": ("i8/i32" if cfg["w8a8"] else "i4/f32" if cfg.get("int4") else "f32"),
+            "data": "synthetic",
             "config": {"workload": name + (f" (first {args.layers} layers only)"
                                            if args.layers else ""),
                        "batch": B, "past": cfg["past"], "greedy_steps": gen,
                        "weights": ("int8 per-row scales, activations per 32, int8 tied head"
                                    if cfg["w8a8"] == "b32" else
-                                   "int8 per-row scales (W8A8)" if cfg["w8a8"] else "bf16") +
+                                   "int8 per-row scales (W8A8)" if cfg["w8a8"] else
+                                   f"INT4, fp32 scale per {cfg['int4']} weights" if cfg.get("int4")
+                                   else "bf16") +
                                   " from seeded N(0,0.02), fp32 accumulate",
                        "kv": ("paged (block 16, shuffled tables)" if cfg["paged"] else "contiguous")
                              + " fp32",

@@ -50,13 +50,23 @@ typedef enum {
   NC_ERR_UNSUPPORTED = 9
 } nc_status;
 
-/* Weight storage. NC_INT8: the seven projections int8 per output row,
- * activations quantised per token (nanoinfer "Quantization"). NC_INT8_B32:
- * the same projections with activations quantised per block of 32 values,
- * and the embedding stored int8 per row too, which is also the tied head
- * (nanoinfer, INT8 activation section and its "INT8 + embeddings" level);
- * needs tie_embeddings and hidden, ffn, n_q_heads * head_dim multiples of 32. */
-typedef enum { NC_BF16 = 0, NC_INT8 = 1, NC_INT8_B32 = 2 } nc_wtype;
+/* Weight storage of the seven projections (nanoinfer "Quantization").
+ * NC_INT8: int8 per output row, activations quantised per token (W8A8).
+ * NC_INT8_B32: the same projections with activations quantised per block of
+ * 32 values, and the embedding stored int8 per row too, which is also the
+ * tied head (nanoinfer, INT8 activation section and its "INT8 + embeddings"
+ * level); needs tie_embeddings and hidden, ffn, n_q_heads * head_dim
+ * multiples of 32. NC_INT4_G32 / NC_INT4_G128: INT4 codes in [-7, 7] with
+ * one fp32 scale per group of 32 / 128 weights of a row, fp32 activations;
+ * hidden, ffn and n_q_heads * head_dim must be multiples of the group. In
+ * the other types the embedding and the head stay bf16. */
+typedef enum {
+  NC_BF16 = 0,
+  NC_INT8 = 1,
+  NC_INT8_B32 = 2,
+  NC_INT4_G32 = 3,
+  NC_INT4_G128 = 4
+} nc_wtype;
 
 /* Hyperparameters. head_dim must be 64 or 128; n_q_heads a multiple of
  * n_kv_heads with group <= 8; hidden, ffn, n_q_heads*head_dim multiples of 8. */
@@ -327,6 +337,22 @@ nc_status nc_attn_decode_static_status(void* stream, int* code);
 nc_status nc_lm_head_argmax(nc_model* m, const float* x, const void* gamma, float eps,
                             const void* W, int B, int K, int V, float* logits, int32_t* next,
                             void* stream);
+
+/* ---------------- INT4 weights (nanoinfer "Quantization": group-wise INT4) --- */
+
+/* y[b, n] = sum_k (q[n, k] * scales[n, k / group]) * xn[b, k], each
+ * dequantised weight rounded to fp32, with xn = rmsnorm(x[b]) * gamma when
+ * gamma != NULL, else xn = x (nanoinfer, "Quantization": INT4 codes in
+ * [-7, 7], one fp32 scale per group of `group` consecutive weights of a row).
+ * Wq [N, K / 2] bytes: two codes a byte, the even index in the low nibble,
+ * two's-complement nibbles; scales [N, K / group] fp32; x [B, K] fp32,
+ * gamma [K] bf16 or NULL, y [B, N] fp32. B in [1, 8], group 32, 64 or 128,
+ * K a multiple of group, the batch's activations within shared memory
+ * (8 rows of K up to ~5,500). Errors (before anything is enqueued): NULL or
+ * misaligned pointers -> NC_ERR_INVALID_ARGUMENT, other sizes -> NC_ERR_SHAPE. */
+nc_status nc_int4_gemv(const float* x, const void* gamma, float eps, const uint8_t* Wq,
+                       const float* scales, int group, int B, int K, int N, float* y,
+                       void* stream);
 
 /* ---------------- sampling (nanoinfer, sampling section) -------------------- */
 

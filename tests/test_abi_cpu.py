@@ -234,4 +234,18 @@ def test_w8a8_b32_rejects_bad_arguments(lib):
     assert call(sx=C.c_void_p(4098)) == E["NC_ERR_INVALID_ARGUMENT"]
     assert call(B=0) == E["NC_ERR_SHAPE"] and call(B=9) == E["NC_ERR_SHAPE"]
     assert call(K=880) == E["NC_ERR_SHAPE"] and call(K=16) == E["NC_ERR_SHAPE"]
+
+
+def test_int4_gemv_rejects_bad_arguments(lib):
+    E = {n: nc.STATUS.index(n) for n in nc.STATUS}
+    P = C.c_void_p(4096)
+    call = lambda x=P, W=P, sc=P, group=32, B=1, K=896, N=8, y=P, g=None: lib.nc_int4_gemv(
+        x, g, 1e-6, W, sc, group, B, K, N, y, None)
+    assert call(x=None) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(W=C.c_void_p(4104)) == E["NC_ERR_INVALID_ARGUMENT"]  # packed rows need 16 bytes
+    assert call(g=C.c_void_p(4097)) == E["NC_ERR_INVALID_ARGUMENT"]
+    assert call(B=0) == E["NC_ERR_SHAPE"] and call(B=9) == E["NC_ERR_SHAPE"]
+    assert call(group=48) == E["NC_ERR_SHAPE"]
+    assert call(K=880, group=32) == E["NC_ERR_SHAPE"]             # not a multiple of the group
+    assert call(K=960, group=128) == E["NC_ERR_SHAPE"]            # 960 is not a multiple of 128
     assert call(N=0) == E["NC_ERR_SHAPE"]

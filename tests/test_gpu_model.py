@@ -122,17 +122,17 @@ def test_block_forward_w8a8_codes_on_identical_input():
 
 # ------------------------------------------------------------------ greedy decode
 def _greedy_compare(shape, wd, wc, prompt, steps, batch=1, past=None, paged=False,
-                    use_graph=True, gate=REL_L2_GATE, staged=False):
+                    use_graph=True, gate=REL_L2_GATE, staged=False, int4_group=0):
     """Teacher-forced greedy decode: both sides consume the oracle's token.
     Every step's logits within `gate` (rel-L2) and the greedy tokens equal
     under the near-tie rule. Returns the worst logit rel-L2 seen. (Paths with
     a rounding step inside the model, W8A8 codes or bf16 K/V, use
     _traced_compare.)"""
-    om = oracle.OracleModel(shape, wc)
+    om = oracle.OracleModel(shape, wc, int4_group=int4_group)
     past = past or [0] * batch
     n_total = len(prompt[0]) + steps if prompt is not None else steps
     max_ctx = max(past) + n_total + 1
-    model = nc.Model(shape, wd, max_batch=batch, max_ctx=max_ctx + 16)
+    model = nc.Model(shape, wd, max_batch=batch, max_ctx=max_ctx + 16, int4_group=int4_group)
     if paged:
         table, nblk = synth.block_tables(past, n_total, 16)
         kv = nc.KVCache(shape, batch, paged=True, block_table=table, num_blocks=nblk)
@@ -402,6 +402,18 @@ def test_decode_w8a8_b32(shape, past, steps):
     worst, nd, _ = _traced_compare(shape, wd, wc, steps=steps, past=[past], w8a8="b32")
     print(f"W8A8 blocks of 32 ({shape.hidden}): worst logit rel-L2 {worst:.3e}, "
           f"boundary codes forced {nd}")
+
+
+@pytest.mark.parametrize("shape,group,past,steps", [(synth.TINY, 32, 0, 12),
+                                                     (synth.TINY, 128, 5, 12),
+                                                     (synth.QWEN2_0P5B, 128, 512, 64)])
+def test_decode_int4(shape, group, past, steps):
+    """INT4 group-wise projections (NC_INT4_G32 / NC_INT4_G128) against the
+    oracle's INT4 mode. Only weights are quantised (on the device, by the
+    same operations as the oracle's quantiser), so the plain 5e-4 gate holds."""
+    wd, wc = weights_both(shape)
+    worst = _greedy_compare(shape, wd, wc, None, steps=steps, past=[past], int4_group=group)
+    print(f"INT4 group {group} ({shape.hidden}): worst logit rel-L2 {worst:.3e}")
 
 
 def test_decode_0p5b_batch16_paged():

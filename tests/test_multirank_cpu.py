@@ -126,3 +126,21 @@ def test_step_bytes_int8_head():
     a = bench.step_bytes(s, 1, [95], w8a8=True)
     b = bench.step_bytes(s, 1, [95], w8a8=True, int8_head=True)
     assert a - b == (s.vocab * s.hidden - 4 * s.vocab) + (s.hidden - 4)
+
+
+def test_step_bytes_int4_matches_the_footprint_formula():
+    """INT4 bytes per step: the projections' share equals the one the
+    quantisation oracle's footprint (pinned to the page's table) implies:
+    footprint(int4-gG) - footprint(fp32) + 4 x projection weights."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from oracle import quant
+    from transformer_decode_gb300 import synth
+    s = synth.QWEN2_0P5B
+    proj = s.n_layers * ((s.q_dim + 2 * s.kv_dim) * s.hidden + s.q_dim * s.hidden
+                         + 3 * s.ffn * s.hidden)
+    for g in (32, 128):
+        int4_proj = (quant.footprint_bytes(s, f"int4-g{g}") - quant.footprint_bytes(s, "fp32")
+                     + 4 * proj)
+        assert bench.step_bytes(s, 1, [95], int4_group=g) == \
+            bench.step_bytes(s, 1, [95]) - 2 * proj + int4_proj

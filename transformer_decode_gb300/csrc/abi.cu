@@ -347,6 +347,26 @@ nc_status nc_w8a8_gemv_b32(const float* x, const void* gamma, float eps, const i
   return launch_result(launch_w8a8_b32(Epi::Store, a, S(stream)), "nc_w8a8_gemv_b32");
 }
 
+nc_status nc_int4_gemv(const float* x, const void* gamma, float eps, const uint8_t* Wq,
+                       const float* scales, int group, int B, int K, int N, float* y,
+                       void* stream) {
+  NC_CHECK(x && Wq && scales && y, NC_ERR_INVALID_ARGUMENT, "null pointer");
+  NC_CHECK(aligned(x, 4) && aligned(gamma, 2) && aligned16(Wq) && aligned(scales, 4) &&
+               aligned(y, 4),
+           NC_ERR_INVALID_ARGUMENT,
+           "Wq must be 16-byte aligned, x, scales and y 4-byte, gamma 2-byte");
+  NC_CHECK(B >= 1 && B <= 8, NC_ERR_SHAPE, "batch %d outside [1, 8]", B);
+  NC_CHECK(group == 32 || group == 64 || group == 128, NC_ERR_SHAPE,
+           "group = %d must be 32, 64 or 128", group);
+  NC_CHECK(K >= group && K % group == 0, NC_ERR_SHAPE, "K = %d must be a positive multiple of group %d",
+           K, group);
+  NC_CHECK(N >= 1, NC_ERR_SHAPE, "N must be positive");
+  NC_CHECK(int4_smem_bytes(B, K) + 4096 <= (size_t)max_smem_optin(), NC_ERR_SHAPE,
+           "K = %d is too long to keep the batch's activations in shared memory", K);
+  Int4Args a{x, static_cast<const uint16_t*>(gamma), eps, Wq, scales, group, B, K, N, y};
+  return launch_result(launch_int4_gemv(Epi::Store, a, S(stream)), "nc_int4_gemv");
+}
+
 size_t nc_sample_scratch_bytes(int B, int V) {
   if (B < 1 || V < 1) return 0;
   return sample_scratch_bytes(B, V);

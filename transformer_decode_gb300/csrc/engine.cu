@@ -71,11 +71,17 @@ bool valid_config(const nc_config& c, std::string* why) {
   if (c.hidden % 16 || c.ffn % 16) return bad("hidden and ffn must be multiples of 16");
   if (c.hidden > 16384 || c.ffn > 65536) return bad("hidden or ffn too large");
   if (!(c.rms_eps > 0) || !(c.rope_theta > 1)) return bad("rms_eps must be > 0 and rope_theta > 1");
-  if (c.wtype != NC_BF16 && c.wtype != NC_INT8 && c.wtype != NC_INT8_B32)
+  if (c.wtype != NC_BF16 && c.wtype != NC_INT8 && c.wtype != NC_INT8_B32 &&
+      c.wtype != NC_INT4_G32 && c.wtype != NC_INT4_G128)
     return bad("unknown weight type");
   if (c.wtype == NC_INT8_B32 &&
       (!c.tie_embeddings || c.hidden % 32 || c.ffn % 32 || (c.n_q_heads * c.head_dim) % 32))
     return bad("NC_INT8_B32 needs a tied head and hidden, ffn, n_q_heads * head_dim multiples of 32");
+  if (c.wtype == NC_INT4_G32 || c.wtype == NC_INT4_G128) {
+    const int g = c.wtype == NC_INT4_G32 ? 32 : 128;
+    if (c.hidden % g || c.ffn % g || (c.n_q_heads * c.head_dim) % g)
+      return bad("INT4 weights need hidden, ffn and n_q_heads * head_dim multiples of the group");
+  }
   return true;
 }
 
@@ -97,6 +103,14 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
   NC_CHECK(max_ctx >= 1 && max_ctx <= (1 << 20), NC_ERR_CAPACITY, "max_ctx out of range");
   const nc_config& c = *cfg;
   const int bt = max_batch <= 1 ? 1 : max_batch <= 2 ? 2 : max_batch <= 4 ? 4 : max_batch <= 8 ? 8 : 16;
+  const int g4 = c.wtype == NC_INT4_G32 ? 32 : c.wtype == NC_INT4_G128 ? 128 : 0;
+  if (g4) {
+    NC_CHECK(max_batch <= 8, NC_ERR_CAPACITY, "INT4 models take at most 8 sequences");
+    const int kmax = std::max(std::max(c.hidden, c.ffn), c.n_q_heads * c.head_dim);
+    NC_CHECK(int4_smem_bytes(max_batch, kmax) + 4096 <= (size_t)max_smem_optin(), NC_ERR_SHAPE,
+             "the INT4 GEMV keeps %d sequences of %d activations in shared memory: too many",
+             max_batch, kmax);
+  }
   NC_CHECK(bt * c.hidden <= 51200, NC_ERR_SHAPE,
            "max_batch (rounded up to a power of 2) * hidden must be <= 51200 for the LM head");
   nc_status st;
@@ -121,7 +135,7 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
   m->max_ctx = max_ctx;
   const int H = c.hidden, D = c.head_dim, F = c.ffn, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   const size_t qd = (size_t)Hq * D, kd = (size_t)Hkv * D, nqkv = qd + 2 * kd;
-  const bool i8 = c.wtype != NC_BF16;
+  const bool i8 = c.wtype == NC_INT8 || c.wtype == NC_INT8_B32;
   const bool b32 = c.wtype == NC_INT8_B32;
 
   // Two passes over one layout function: first with null bases to size the
@@ -136,7 +150,16 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     m->layers.assign(c.n_layers, LayerPacked{});
     for (int l = 0; l < c.n_layers; ++l) {
       LayerPacked& P = m->layers[l];
-      if (!i8) {
+      if (g4) {
+        P.p4_qkv = A.take<uint8_t>(nqkv * H / 2);
+        P.p4_o = A.take<uint8_t>(qd * H / 2);
+        P.p4_gu = A.take<uint8_t>((size_t)F * H);
+        P.p4_d = A.take<uint8_t>((size_t)H * F / 2);
+        P.s4_qkv = A.take<float>(nqkv * (H / g4));
+        P.s4_o = A.take<float>((size_t)H * (qd / g4));
+        P.s4_gu = A.take<float>(2 * (size_t)F * (H / g4));
+        P.s4_d = A.take<float>((size_t)H * (F / g4));
+      } else if (!i8) {
         P.w_qkv = A.take<uint16_t>(nqkv * H);
         P.w_o = A.take<uint16_t>(qd * H);
         P.w_gu = A.take<uint16_t>(2 * (size_t)F * H);
@@ -220,7 +243,18 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     const uint16_t* wg = static_cast<const uint16_t*>(L.wg);
     const uint16_t* wu = static_cast<const uint16_t*>(L.wu);
     const uint16_t* wd = static_cast<const uint16_t*>(L.wd);
-    if (!i8) {
+    if (g4) {
+      auto q4 = [&](const uint16_t* src, int rows, int k, uint8_t* p, float* sc) {
+        if (!e) e = launch_quantize_int4(src, rows, k, g4, p, sc, s);
+      };
+      q4(wq, (int)qd, H, P.p4_qkv, P.s4_qkv);
+      q4(wk, (int)kd, H, P.p4_qkv + qd * H / 2, P.s4_qkv + qd * (H / g4));
+      q4(wv, (int)kd, H, P.p4_qkv + (qd + kd) * H / 2, P.s4_qkv + (qd + kd) * (H / g4));
+      q4(wo, H, (int)qd, P.p4_o, P.s4_o);
+      q4(wg, F, H, P.p4_gu, P.s4_gu);
+      q4(wu, F, H, P.p4_gu + (size_t)F * H / 2, P.s4_gu + (size_t)F * (H / g4));
+      q4(wd, H, F, P.p4_d, P.s4_d);
+    } else if (!i8) {
       if (!e) e = copy(P.w_qkv, wq, qd * H * 2);
       if (!e) e = copy(P.w_qkv + qd * H, wk, kd * H * 2);
       if (!e) e = copy(P.w_qkv + (qd + kd) * H, wv, kd * H * 2);
@@ -414,7 +448,7 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
   const LayerPacked& P = m->layers[layer];
   const int H = c.hidden, D = c.head_dim, F = c.ffn, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   const int nqkv = (Hq + 2 * Hkv) * D;
-  const bool i8 = c.wtype != NC_BF16;
+  const bool i8 = c.wtype == NC_INT8 || c.wtype == NC_INT8_B32;
   const bool b32 = c.wtype == NC_INT8_B32;
   // the W8A8 diagnostic's slots of this layer (null when it is off)
   int8_t* dq[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -429,8 +463,12 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
     if (!b32 && m->dbg_scales)
       for (int k = 0; k < 4; ++k) ds[k] = m->dbg_scales + ((size_t)layer * 4 + k) * batch;
   }
+  const int g4 = c.wtype == NC_INT4_G32 ? 32 : c.wtype == NC_INT4_G128 ? 128 : 0;
   cudaError_t e;
-  if (!i8) {
+  if (g4) {
+    Int4Args a{m->x, P.g_attn, c.rms_eps, P.p4_qkv, P.s4_qkv, g4, batch, H, nqkv, m->qkv, P.b_qkv};
+    e = launch_int4_gemv(Epi::Store, a, s);
+  } else if (!i8) {
     e = launch_gemv(Epi::Store, {m->x, P.g_attn, c.rms_eps, P.w_qkv, P.b_qkv, batch, H, nqkv, m->qkv}, s);
   } else if (b32) {
     W8BArgs a{m->x, P.g_attn, c.rms_eps, P.q_qkv, P.s_qkv, P.b_qkv, batch, H, nqkv, m->qkv,
@@ -451,6 +489,14 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
   at.g_k = P.g_k;
   at.eps = c.rms_eps;
   if ((e = launch_attn(at, s))) return e;
+  if (g4) {
+    Int4Args o{m->attn, nullptr, 0.f, P.p4_o, P.s4_o, g4, batch, Hq * D, H, m->x};
+    if ((e = launch_int4_gemv(Epi::Residual, o, s))) return e;
+    Int4Args gu{m->x, P.g_mlp, c.rms_eps, P.p4_gu, P.s4_gu, g4, batch, H, F, m->h};
+    if ((e = launch_int4_gemv(Epi::SwiGLU, gu, s))) return e;
+    Int4Args dn{m->h, nullptr, 0.f, P.p4_d, P.s4_d, g4, batch, F, H, m->x};
+    return launch_int4_gemv(Epi::Residual, dn, s);
+  }
   if (!i8) {
     if ((e = launch_gemv(Epi::Residual, {m->attn, nullptr, 0.f, P.w_o, nullptr, batch, Hq * D, H, m->x}, s)))
       return e;

@@ -22,6 +22,9 @@ struct LayerPacked {
   uint16_t* w_d = nullptr;    // [H, F]
   int8_t *q_qkv = nullptr, *q_o = nullptr, *q_gu = nullptr, *q_d = nullptr;  // NC_INT8 rows
   float *s_qkv = nullptr, *s_o = nullptr, *s_gu = nullptr, *s_d = nullptr;   // per-row scales
+  // NC_INT4_*: packed codes [rows, in / 2] and per-group scales [rows, in / group]
+  uint8_t *p4_qkv = nullptr, *p4_o = nullptr, *p4_gu = nullptr, *p4_d = nullptr;
+  float *s4_qkv = nullptr, *s4_o = nullptr, *s4_gu = nullptr, *s4_d = nullptr;
   uint16_t *g_attn = nullptr, *g_mlp = nullptr, *g_q = nullptr, *g_k = nullptr;
 };
 

@@ -150,6 +150,21 @@ size_t w8a8_b32_smem_bytes(int B, int K);
 cudaError_t launch_w8a8_b32(Epi epi, const W8BArgs& a, cudaStream_t s);
 cudaError_t launch_embed_i8(const int8_t* q, const float* sc, const int32_t* tokens, int B, int H,
                             int V, float* x, int* status, cudaStream_t s);
+// ------------------------------------------------------------ INT4 weights
+struct Int4Args {
+  const float* x;         // [B, K]
+  const uint16_t* gamma;  // [K] RMSNorm gain, or null (no norm)
+  float eps;
+  const uint8_t* Wq;      // [N, K / 2]: two codes a byte, the even index in the low nibble
+  const float* scales;    // [N, K / group]
+  int group, B, K, N;
+  float* y;               // [B, N] (Residual: in place); SwiGLU: Wq and scales hold 2N rows
+  const uint16_t* bias = nullptr;  // [N] bf16 or null (Store only)
+};
+size_t int4_smem_bytes(int B, int K);  // the activations kept in shared memory
+cudaError_t launch_int4_gemv(Epi epi, const Int4Args& a, cudaStream_t s);
+cudaError_t launch_quantize_int4(const uint16_t* W, int N, int K, int group, uint8_t* q,
+                                 float* sc, cudaStream_t s);
 
 // ------------------------------------------------------------ sampling
 // Scratch of nc_sample: per row five arrays of V rounded up to 64 words.

@@ -22,7 +22,7 @@ NC_OK = 0
 STATUS = ["NC_OK", "NC_ERR_INVALID_ARGUMENT", "NC_ERR_SHAPE", "NC_ERR_DTYPE", "NC_ERR_CAPACITY",
           "NC_ERR_POSITION", "NC_ERR_CUDA", "NC_ERR_TIMEOUT", "NC_ERR_UNHEALTHY",
           "NC_ERR_UNSUPPORTED"]
-NC_BF16, NC_INT8, NC_INT8_B32 = 0, 1, 2
+NC_BF16, NC_INT8, NC_INT8_B32, NC_INT4_G32, NC_INT4_G128 = 0, 1, 2, 3, 4
 NC_STEP_GRAPH, NC_STEP_ADVANCE, NC_STEP_STAGED = 1, 2, 4
 NC_KV_F32, NC_KV_BF16 = 0, 1
 
@@ -34,6 +34,7 @@ EXPORTS = [
     "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile", "nc_decode_path",
     "nc_sample", "nc_sample_scratch_bytes", "nc_attn_decode_static_status",
     "nc_debug_w8a8_codes", "nc_w8a8_gemv_b32",
+    "nc_int4_gemv",
 ]
 
 
@@ -124,6 +125,7 @@ def _declare(L):
     L.nc_sample.argtypes = [vp, i, i, f, i, f, vp, vp, vp, vp, C.c_size_t, vp]
     L.nc_sample_scratch_bytes.argtypes = [i, i]
     L.nc_w8a8_gemv_b32.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
+    L.nc_int4_gemv.argtypes = [vp, vp, f, vp, vp, i, i, i, i, vp, vp]
     for n in EXPORTS:
         if n not in ("nc_status_string", "nc_last_error_message", "nc_sample_scratch_bytes"):
             getattr(L, n).restype = C.c_int
@@ -260,6 +262,18 @@ def attn_decode_static_status(stream=None):
     return code.value
 
 
+def int4_gemv(x, gamma, eps, Wq, scales, group, y, stream=None):
+    """nc_int4_gemv: y = dequantised INT4 weights (packed [N, K/2] uint8, fp32
+    scales [N, K/group]) times the (normed) activations x [B, K]."""
+    B, K = x.shape
+    N = Wq.shape[0]
+    _check(load().nc_int4_gemv(_ptr(x, torch.float32, "x"), _ptr(gamma, torch.bfloat16, "gamma"),
+                               float(eps), _ptr(Wq, torch.uint8, "Wq", N * K // 2),
+                               _ptr(scales, torch.float32, "scales", N * (K // group)),
+                               int(group), B, K, N, _ptr(y, torch.float32, "y", B * N),
+                               _stream(stream)))
+
+
 # ------------------------------------------------------------------ sampling
 def sample_scratch_bytes(B, V):
     return int(load().nc_sample_scratch_bytes(int(B), int(V)))
@@ -385,7 +399,8 @@ class Model:
     The model keeps its own packed copy; the caller may free the originals.
     """
 
-    def __init__(self, shape, weights, max_batch=1, max_ctx=4096, w8a8=False, stream=None):
+    def __init__(self, shape, weights, max_batch=1, max_ctx=4096, w8a8=False, int4_group=0,
+                 stream=None):
         L = load()
         self.shape = shape
         self.max_batch = max_batch
@@ -393,7 +408,8 @@ class Model:
         cfg = Config(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
                      shape.n_layers, shape.vocab, shape.rms_eps, shape.rope_theta,
                      int(shape.qkv_bias), int(shape.qk_norm), int(shape.tie_embeddings),
-                     {False: NC_BF16, True: NC_INT8, "b32": NC_INT8_B32}[w8a8])
+                     {False: NC_BF16, True: NC_INT8, "b32": NC_INT8_B32}[w8a8] if w8a8 else
+                     {0: NC_BF16, 32: NC_INT4_G32, 128: NC_INT4_G128}[int4_group])
         layers = (LayerWeights * shape.n_layers)()
         for l, lw in enumerate(weights["layers"]):
             for n in _LW:
