@@ -147,7 +147,10 @@ int nc_abi_version(void);
 nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, int max_batch, int max_ctx,
                           void* stream, nc_model** out);
 nc_status nc_model_destroy(nc_model* m);
-/* Bytes of packed weights and of workspace held by the model. */
+/* Bytes of packed weights and of workspace held by the model (the static
+ * memory plan of nanocompile's phase 7: everything a step touches is
+ * reserved at creation; the pages give no call of this kind). Either
+ * pointer may be NULL. */
 nc_status nc_model_memory(const nc_model* m, size_t* weight_bytes, size_t* workspace_bytes);
 
 /* Flags of nc_decode_step. */
@@ -183,13 +186,48 @@ nc_status nc_block_forward(nc_model* m, int layer, int batch, float* x_dev,
                            const int32_t* positions_dev, const int32_t* positions_host,
                            const nc_kv_cache* kv, void* stream);
 
+/* ---------------- prefill (a prompt chunk as one forward pass) ------------- */
+
+/* Bytes of caller-owned device scratch nc_prefill needs for a chunk of T
+ * tokens (the chunk's activations and the tensor cores' input planes). 0 for
+ * an invalid model or T. */
+size_t nc_prefill_scratch_bytes(const nc_model* m, int T);
+
+/* The T tokens tokens_dev [T] int32 enter cache sequence `seq` at positions
+ * start_pos .. start_pos + T - 1, as one causal forward pass instead of T
+ * decode steps (the nanoinfer page's batched prefill: each weight row read
+ * once for the whole prompt; Tang section 2.3: attention fused under the
+ * online-softmax monoid). Per layer: the projections of all T tokens as
+ * tensor-core GEMMs (tcgen05, fp32 accumulation, activations as bf16 hi / lo
+ * planes), RoPE and the K/V append of every token, and a flash-style
+ * attention where token i sees slots 0 .. start_pos + i (the cache's earlier
+ * positions and the chunk's tokens up to itself). logits_dev [V] fp32
+ * receives the last token's logits and next_dev [1] int32 (nullable) their
+ * arg-max (lowest index on ties; -1 on NaN). Positions after the chunk are
+ * untouched; a following nc_decode_step continues at start_pos + T.
+ * bf16 models only (NC_ERR_UNSUPPORTED otherwise); hidden, ffn and
+ * n_q_heads * head_dim must be multiples of 64. scratch: device memory of at
+ * least nc_prefill_scratch_bytes(m, T) bytes, 16-byte aligned, owned by the
+ * caller. Validation uses host data: start_pos + T within the cache's
+ * capacity, seq within batch_capacity (contiguous) or every block of the
+ * chunk in the pool (paged), else NC_ERR_POSITION / NC_ERR_CAPACITY before
+ * anything is enqueued. Uses the model's workspace (non-reentrant). */
+nc_status nc_prefill(nc_model* m, int seq, int T, const int32_t* tokens_dev, int start_pos,
+                     const nc_kv_cache* kv, float* logits_dev, int32_t* next_dev, void* scratch,
+                     size_t scratch_bytes, void* stream);
+
 /* Device watchdog word (0 = fine, else an nc_status set by a kernel, e.g. a
  * NaN in the logits or an expired bounded wait). Synchronises `stream`,
- * reads the word and clears it. */
+ * reads the word and clears it. It is how device-side failures reach the
+ * host without a read-back inside a step (nanoserve: host read-backs were
+ * the graph breaks, so the step never reads the device itself; ForgeML
+ * "Leader/worker protocol and failure semantics": after a backend failure
+ * the engine goes unhealthy and fails later calls). */
 nc_status nc_get_device_status(nc_model* m, void* stream, int* code);
 
 /* Which implementation nc_decode_step runs for these arguments (nothing is
- * launched): NC_PATH_PERSISTENT, the whole step as one cooperative
+ * launched; the pages have no counterpart: it reports a dispatch decision of
+ * this library): NC_PATH_PERSISTENT, the whole step as one cooperative
  * persistent kernel (bf16 weights, batch <= 4, shape within its
  * shared-memory plan, NC_STEP_STAGED not set), else
  * NC_PATH_STAGED, the per-stage kernels (2 + 5 per layer launches, in a CUDA

@@ -370,6 +370,18 @@ def test_decode_tiny_persistent_splits(paged):
     _greedy_compare(shape, wd, wc, None, steps=6, batch=4, past=[300, 200, 129, 5], paged=paged)
 
 
+@pytest.mark.parametrize("shape", [synth.TINY, synth.TINY_QKNORM])
+@pytest.mark.parametrize("batch,paged", [(9, False), (16, True)])
+def test_decode_tiny_tensor_cores(shape, batch, paged):
+    """Batch 9..16: the projections and the LM head run on the tensor cores
+    (tcgen05 with the accumulator in tensor memory, activations as bf16
+    hi / lo planes); ragged output rows (TINY_QKNORM's 328-token vocabulary,
+    2.6 tiles of 128) and a batch that fills 9 of the 16 token columns."""
+    wd, wc = weights_both(shape)
+    past = [(7 * b) % 37 for b in range(batch)]
+    _greedy_compare(shape, wd, wc, None, steps=6, batch=batch, past=past, paged=paged)
+
+
 def test_decode_tiny_batch_paged():
     shape = synth.TINY
     wd, wc = weights_both(shape)

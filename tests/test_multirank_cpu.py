@@ -40,7 +40,7 @@ def _rank(rank, ws, port, out):
 
 def test_replica_rate_two_gloo_ranks():
     ws = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank, args=(ws, _free_port(), out), nprocs=ws, join=True)
     for r in range(ws):
         rate, el = out[r]

@@ -367,6 +367,18 @@ nc_status nc_int4_gemv(const float* x, const void* gamma, float eps, const uint8
   return launch_result(launch_int4_gemv(Epi::Store, a, S(stream)), "nc_int4_gemv");
 }
 
+size_t nc_prefill_scratch_bytes(const nc_model* m, int T) {
+  if (!m || T < 1) return 0;
+  return prefill_scratch_bytes(M(m), T);
+}
+
+nc_status nc_prefill(nc_model* m, int seq, int T, const int32_t* tokens_dev, int start_pos,
+                     const nc_kv_cache* kv, float* logits_dev, int32_t* next_dev, void* scratch,
+                     size_t scratch_bytes, void* stream) {
+  return prefill(M(m), seq, T, tokens_dev, start_pos, kv, logits_dev, next_dev, scratch,
+                 scratch_bytes, S(stream));
+}
+
 size_t nc_sample_scratch_bytes(int B, int V) {
   if (B < 1 || V < 1) return 0;
   return sample_scratch_bytes(B, V);

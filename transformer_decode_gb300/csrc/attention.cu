@@ -26,8 +26,9 @@ __global__ void __launch_bounds__(256) k_rope_qkv(RopeArgs a) {
   pdl_wait();
   const int b = blockIdx.x;
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-  const int pos = a.positions[b];
-  if (!a.kv.slot_ok(b, pos)) {
+  const int pos = a.seq >= 0 ? a.pos0 + b : a.positions[b];
+  const int kb = a.seq >= 0 ? a.seq : b;  // the cache sequence of row b
+  if (!a.kv.slot_ok(kb, pos)) {
     if (threadIdx.x == 0 && blockIdx.y == 0 && a.status) atomicCAS(a.status, 0, (int)NC_ERR_POSITION);
     return;
   }
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(256) k_rope_qkv(RopeArgs a) {
       for (int j = 0; j < E; ++j) a.q_out[((size_t)b * a.Hq + hh) * D + lane + 32 * j] = e[j];
     } else {
       const int g = hh - a.Hq;
-      const size_t off = a.kv.offset(a.layer, b, g, pos);
+      const size_t off = a.kv.offset(a.layer, kb, g, pos);
       const float* vv = src + (size_t)(a.Hq + a.Hkv + g) * D;
 #pragma unroll
       for (int j = 0; j < E; ++j) {

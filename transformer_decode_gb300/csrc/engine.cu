@@ -18,6 +18,7 @@
 // graph breaks).
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <map>
@@ -196,7 +197,15 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     m->attn = W.take<float>((size_t)max_batch * qd);
     m->part = W.take<float>(part_max);
     m->h = W.take<float>((size_t)max_batch * F);
-    m->am_part = W.take<unsigned long long>((size_t)max_batch * lm_head_grid());
+    // arg-max partial keys: one per CTA of the LM head (the tensor-core head
+    // at batch 9..16 runs one CTA per 128 vocabulary rows)
+    m->am_part = W.take<unsigned long long>(
+        (size_t)max_batch * std::max(lm_head_grid(), (c.vocab + 127) / 128));
+    // bf16 hi / lo activation planes of the tensor-core projections
+    m->xb = max_batch > 8 && !i8 && !g4
+                ? W.take<uint16_t>(umma_act_bytes(max_batch, std::max(std::max(H, F), (int)qd)) / 2 +
+                                   512)
+                : nullptr;
     m->ticket = W.take<unsigned int>(1);
     m->atickets = W.take<unsigned int>((size_t)max_batch * Hkv);
     m->status = W.take<int>(1);
@@ -442,6 +451,27 @@ size_t dbg_scales_per_step(const Model* m, int batch) {
   return m->cfg.wtype == NC_INT8 ? (size_t)m->cfg.n_layers * 4 * batch : 0;
 }
 
+// Batch 9..16 with bf16 weights runs the projections and the LM head on the
+// tensor cores (tcgen05); NC_UMMA=0 in the environment uses the CUDA-core
+// and mma.sync stage kernels instead (for comparison).
+static bool umma_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("NC_UMMA");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+static bool use_umma(const Model* m, int batch) {
+  const nc_config& c = m->cfg;
+  return umma_enabled() && m->xb && batch > 8 && c.wtype == NC_BF16 && umma_supported(c.hidden) &&
+         umma_supported(c.ffn) && umma_supported(c.n_q_heads * c.head_dim);
+}
+// The tensor-core scratch, aligned for TMA (1024 bytes).
+static uint16_t* xb_aligned(const Model* m) {
+  return reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(m->xb) + 1023) &
+                                     ~uintptr_t(1023));
+}
+
 static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* positions,
                                  const KVView& kvv, int splits, cudaStream_t s) {
   const nc_config& c = m->cfg;
@@ -468,6 +498,10 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
   if (g4) {
     Int4Args a{m->x, P.g_attn, c.rms_eps, P.p4_qkv, P.s4_qkv, g4, batch, H, nqkv, m->qkv, P.b_qkv};
     e = launch_int4_gemv(Epi::Store, a, s);
+  } else if (!i8 && use_umma(m, batch)) {
+    UmmaArgs u{m->x, P.g_attn, c.rms_eps, P.w_qkv, P.b_qkv, batch, H, nqkv, m->qkv, nqkv,
+               xb_aligned(m)};
+    e = launch_umma(Epi::Store, u, s);
   } else if (!i8) {
     e = launch_gemv(Epi::Store, {m->x, P.g_attn, c.rms_eps, P.w_qkv, P.b_qkv, batch, H, nqkv, m->qkv}, s);
   } else if (b32) {
@@ -496,6 +530,15 @@ static cudaError_t enqueue_block(Model* m, int layer, int batch, const int32_t* 
     if ((e = launch_int4_gemv(Epi::SwiGLU, gu, s))) return e;
     Int4Args dn{m->h, nullptr, 0.f, P.p4_d, P.s4_d, g4, batch, F, H, m->x};
     return launch_int4_gemv(Epi::Residual, dn, s);
+  }
+  if (!i8 && use_umma(m, batch)) {
+    uint16_t* xb = xb_aligned(m);
+    UmmaArgs o{m->attn, nullptr, 0.f, P.w_o, nullptr, batch, Hq * D, H, m->x, H, xb};
+    if ((e = launch_umma(Epi::Residual, o, s))) return e;
+    UmmaArgs gu{m->x, P.g_mlp, c.rms_eps, P.w_gu, nullptr, batch, H, F, m->h, F, xb};
+    if ((e = launch_umma(Epi::SwiGLU, gu, s))) return e;
+    UmmaArgs dn{m->h, nullptr, 0.f, P.w_d, nullptr, batch, F, H, m->x, H, xb};
+    return launch_umma(Epi::Residual, dn, s);
   }
   if (!i8) {
     if ((e = launch_gemv(Epi::Residual, {m->attn, nullptr, 0.f, P.w_o, nullptr, batch, Hq * D, H, m->x}, s)))
@@ -556,6 +599,18 @@ static cudaError_t enqueue_step(Model* m, int batch, const StepIO& io, const KVV
     h.advance_tokens = io.advance ? io.tokens : nullptr;
     h.advance_positions = io.advance ? io.positions : nullptr;
     return launch_w8a8_b32(Epi::Store, h, s);
+  }
+  if (use_umma(m, batch)) {  // logits and the arg-max on the tensor cores
+    UmmaArgs u{m->x, m->g_final, c.rms_eps, m->head, nullptr, batch, c.hidden, c.vocab,
+               io.logits, c.vocab, xb_aligned(m)};
+    u.lm = true;
+    u.part = m->am_part;
+    u.ticket = m->ticket;
+    u.next = io.next;
+    u.status = m->status;
+    u.advance_tokens = io.advance ? io.tokens : nullptr;
+    u.advance_positions = io.advance ? io.positions : nullptr;
+    return launch_umma(Epi::Store, u, s);
   }
   LmHeadArgs a{m->x, m->g_final, c.rms_eps, m->head, batch, c.hidden, c.vocab, io.logits, io.next,
                m->am_part, m->ticket, m->status, io.advance ? io.tokens : nullptr,
@@ -683,6 +738,129 @@ nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t*
   if (e) {
     m->unhealthy = true;
     return fail(NC_ERR_CUDA, "block launch failed: %s", cudaGetErrorString(e));
+  }
+  return NC_OK;
+}
+
+}  // namespace nc
+
+// ------------------------------------------------------------------ prefill
+namespace nc {
+
+// Scratch of a prefill chunk of T tokens: residual x [T][H], projections
+// [T][(Hq + 2 Hkv) D], rotated q and attention output [T][Hq D], SiLU * up
+// [T][F], and the tensor-core activation planes; pieces 1024-byte aligned.
+struct PrefillPlan {
+  size_t x, qkv, q, attn, h, xb, total;
+};
+static PrefillPlan prefill_plan(const Model* m, int T) {
+  const nc_config& c = m->cfg;
+  const size_t qd = (size_t)c.n_q_heads * c.head_dim, nqkv = qd + 2 * (size_t)c.n_kv_heads * c.head_dim;
+  const int kmax = std::max(std::max(c.hidden, c.ffn), (int)qd);
+  PrefillPlan p{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 1024);
+    return at;
+  };
+  p.x = take((size_t)T * c.hidden * 4);
+  p.qkv = take((size_t)T * nqkv * 4);
+  p.q = take((size_t)T * qd * 4);
+  p.attn = take((size_t)T * qd * 4);
+  p.h = take((size_t)T * c.ffn * 4);
+  p.xb = take(umma_act_bytes(T, kmax));
+  p.total = off + 1024;  // room to align the caller's base
+  return p;
+}
+
+size_t prefill_scratch_bytes(const Model* m, int T) { return prefill_plan(m, T).total; }
+
+nc_status prefill(Model* m, int seq, int T, const int32_t* tokens, int start,
+                  const nc_kv_cache* kv, float* logits, int32_t* next, void* scratch,
+                  size_t scratch_bytes, cudaStream_t s) {
+  NC_CHECK(m, NC_ERR_INVALID_ARGUMENT, "model is NULL");
+  NC_CHECK(!m->unhealthy, NC_ERR_UNHEALTHY, "model saw an earlier CUDA failure");
+  const nc_config& c = m->cfg;
+  NC_CHECK(c.wtype == NC_BF16, NC_ERR_UNSUPPORTED, "prefill runs bf16 weights only");
+  NC_CHECK(umma_supported(c.hidden) && umma_supported(c.ffn) &&
+               umma_supported(c.n_q_heads * c.head_dim),
+           NC_ERR_SHAPE, "prefill needs hidden, ffn and n_q_heads * head_dim multiples of 64");
+  NC_CHECK(tokens && logits && scratch, NC_ERR_INVALID_ARGUMENT, "null pointer");
+  NC_CHECK(reinterpret_cast<uintptr_t>(tokens) % 4 == 0 && reinterpret_cast<uintptr_t>(logits) % 4 == 0 &&
+               reinterpret_cast<uintptr_t>(next) % 4 == 0 &&
+               reinterpret_cast<uintptr_t>(scratch) % 16 == 0,
+           NC_ERR_INVALID_ARGUMENT,
+           "tokens, logits and next must be 4-byte aligned, scratch 16-byte aligned");
+  NC_CHECK(T >= 1 && T <= 32768, NC_ERR_SHAPE, "T = %d outside [1, 32768]", T);
+  NC_CHECK(start >= 0, NC_ERR_POSITION, "start position %d is negative", start);
+  NC_CHECK(kv && kv->k && kv->v, NC_ERR_INVALID_ARGUMENT, "kv cache pointers are NULL");
+  NC_CHECK(kv->dtype == NC_KV_F32 || kv->dtype == NC_KV_BF16, NC_ERR_DTYPE, "unknown kv dtype");
+  NC_CHECK(reinterpret_cast<uintptr_t>(kv->k) % 16 == 0 && reinterpret_cast<uintptr_t>(kv->v) % 16 == 0,
+           NC_ERR_INVALID_ARGUMENT, "kv cache pointers must be 16-byte aligned");
+  const int cap = kv_capacity(*kv);
+  NC_CHECK(cap >= 1 && cap <= m->max_ctx, NC_ERR_CAPACITY,
+           "kv capacity %d outside [1, %d] reserved at model creation", cap, m->max_ctx);
+  NC_CHECK((long long)start + T <= cap, NC_ERR_POSITION,
+           "positions %d .. %d do not fit the cache's %d slots", start, start + T - 1, cap);
+  NC_CHECK(seq >= 0, NC_ERR_INVALID_ARGUMENT, "sequence %d is negative", seq);
+  if (!kv->paged) {
+    NC_CHECK(seq < kv->batch_capacity, NC_ERR_CAPACITY, "sequence %d beyond batch_capacity %d",
+             seq, kv->batch_capacity);
+  } else {
+    NC_CHECK(kv->block_table && kv->block_table_host && kv->block_size >= 1 &&
+                 kv->num_blocks >= 1 && kv->max_blocks_per_seq >= 1,
+             NC_ERR_INVALID_ARGUMENT, "paged cache needs block tables and positive sizes");
+    for (int i = 0; i <= (start + T - 1) / kv->block_size; ++i) {
+      const int blk = kv->block_table_host[(size_t)seq * kv->max_blocks_per_seq + i];
+      NC_CHECK(blk >= 0 && blk < kv->num_blocks, NC_ERR_POSITION,
+               "block table entry %d of sequence %d is %d (pool has %d blocks)", i, seq, blk,
+               kv->num_blocks);
+    }
+  }
+  const PrefillPlan p = prefill_plan(m, T);
+  NC_CHECK(scratch_bytes >= p.total, NC_ERR_CAPACITY, "scratch holds %zu bytes, %zu needed",
+           scratch_bytes, p.total);
+  char* base = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(scratch) + 1023) &
+                                       ~uintptr_t(1023));
+  float* x = reinterpret_cast<float*>(base + p.x);
+  float* qkv = reinterpret_cast<float*>(base + p.qkv);
+  float* q = reinterpret_cast<float*>(base + p.q);
+  float* attn = reinterpret_cast<float*>(base + p.attn);
+  float* h = reinterpret_cast<float*>(base + p.h);
+  uint16_t* xb = reinterpret_cast<uint16_t*>(base + p.xb);
+  const int H = c.hidden, D = c.head_dim, F = c.ffn, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
+  const int qd = Hq * D, nqkv = (Hq + 2 * Hkv) * D;
+  const KVView kvv = kv_view(m, *kv);
+
+  cudaError_t e = launch_embed(m->embed, tokens, T, H, c.vocab, x, m->status, s);
+  for (int l = 0; l < c.n_layers && !e; ++l) {
+    const LayerPacked& P = m->layers[l];
+    UmmaArgs u{x, P.g_attn, c.rms_eps, P.w_qkv, P.b_qkv, T, H, nqkv, qkv, nqkv, xb};
+    if ((e = launch_umma(Epi::Store, u, s))) break;
+    RopeArgs r{qkv, nullptr, m->inv_freq, P.g_q, P.g_k, c.rms_eps, T, Hq, Hkv, D, l, q, kvv,
+               m->status};
+    r.seq = seq;
+    r.pos0 = start;
+    if ((e = launch_rope_qkv(r, s))) break;
+    PrefillAttnArgs at{q, attn, T, start, seq, l, Hq, Hkv, D, kvv};
+    if ((e = launch_prefill_attn(at, s))) break;
+    UmmaArgs o{attn, nullptr, 0.f, P.w_o, nullptr, T, qd, H, x, H, xb};
+    if ((e = launch_umma(Epi::Residual, o, s))) break;
+    UmmaArgs gu{x, P.g_mlp, c.rms_eps, P.w_gu, nullptr, T, H, F, h, F, xb};
+    if ((e = launch_umma(Epi::SwiGLU, gu, s))) break;
+    UmmaArgs dn{h, nullptr, 0.f, P.w_d, nullptr, T, F, H, x, H, xb};
+    if ((e = launch_umma(Epi::Residual, dn, s))) break;
+  }
+  if (!e) {
+    // logits of the last token only: the next token is all a prompt yields
+    LmHeadArgs a{x + (size_t)(T - 1) * H, m->g_final, c.rms_eps, m->head, 1, H, c.vocab, logits,
+                 next, m->am_part, m->ticket, m->status, nullptr, nullptr};
+    e = launch_lm_head(a, s);
+  }
+  if (e) {
+    m->unhealthy = true;
+    return fail(NC_ERR_CUDA, "prefill launch failed: %s", cudaGetErrorString(e));
   }
   return NC_OK;
 }

@@ -45,6 +45,7 @@ struct Model {
   // workspace
   float *x = nullptr, *qkv = nullptr, *q = nullptr, *attn = nullptr, *part = nullptr, *h = nullptr;
   unsigned long long* am_part = nullptr;
+  uint16_t* xb = nullptr;  // tensor-core activation planes (batch 9..16), or null
   unsigned int* ticket = nullptr;
   unsigned int* atickets = nullptr;  // [max_batch, Hkv] split-attention merge tickets
   int* status = nullptr;
@@ -91,6 +92,13 @@ nc_status decode_step(Model* m, int batch, int32_t* tokens, int32_t* positions,
 bool use_persistent(const Model* m, int batch, const nc_kv_cache& kv, int flags);
 nc_status block_forward(Model* m, int layer, int batch, float* x, const int32_t* positions,
                         const int32_t* positions_host, const nc_kv_cache* kv, cudaStream_t s);
+// A prompt chunk of T tokens of sequence `seq` at positions start .. start +
+// T - 1 as one forward pass (tensor-core projections, flash-style causal
+// attention); logits of the last token. Scratch is caller-owned.
+size_t prefill_scratch_bytes(const Model* m, int T);
+nc_status prefill(Model* m, int seq, int T, const int32_t* tokens, int start,
+                  const nc_kv_cache* kv, float* logits, int32_t* next, void* scratch,
+                  size_t scratch_bytes, cudaStream_t s);
 // Codes and scales the W8A8 diagnostic holds for one step at this batch.
 size_t dbg_codes_per_step(const Model* m, int batch);
 size_t dbg_scales_per_step(const Model* m, int batch);

@@ -50,6 +50,34 @@ cudaError_t launch_gemv(Epi epi, const GemvArgs& a, cudaStream_t s);
 bool gemm16_supported(Epi epi, int B, int K);
 cudaError_t launch_gemm16(Epi epi, const GemvArgs& a, cudaStream_t s);
 
+// Dense tiles on the tensor cores (umma.cu, tcgen05): y[t, n] = W[n, :] .
+// xn[t, :] for T tokens, xn = rmsnorm(x[t]) * gamma when gamma is set. The
+// activations are first written to xb as bf16 hi / lo planes.
+struct UmmaArgs {
+  const float* x;          // [T, K] fp32
+  const uint16_t* gamma;   // [K] or null
+  float eps;
+  const uint16_t* W;       // [N, K] bf16; SwiGLU: [2N, K] (gate rows, then up rows)
+  const uint16_t* bias;    // [N] or null (Store)
+  int T, K, N;
+  float* y;                // [T, ldy]; Residual: updated in place
+  int ldy;
+  uint16_t* xb;            // scratch of umma_act_bytes(T, K) bytes, 1024-byte aligned
+  // LM head (Store with lm): per-CTA arg-max keys [T][ceil(N / 128)], the
+  // ticket, and what the last CTA writes
+  bool lm = false;
+  unsigned long long* part = nullptr;
+  unsigned int* ticket = nullptr;
+  int32_t* next = nullptr;
+  int* status = nullptr;
+  int32_t* advance_tokens = nullptr;
+  int32_t* advance_positions = nullptr;
+};
+bool umma_supported(int K);
+int umma_tokens_per_tile(int T);
+size_t umma_act_bytes(int T, int K);
+cudaError_t launch_umma(Epi epi, const UmmaArgs& a, cudaStream_t s);
+
 // LM head: logits = W rmsnorm(x) and the greedy token per sequence.
 struct LmHeadArgs {
   const float* x;
@@ -82,8 +110,25 @@ struct RopeArgs {
   float* q_out;             // [B, Hq D]
   KVView kv;
   int* status;              // device status word (NC_ERR_POSITION on a bad slot)
+  // Prefill: seq >= 0 makes every row b a token of cache sequence `seq` at
+  // position pos0 + b (positions is then unused).
+  int seq = -1;
+  int pos0 = 0;
 };
 cudaError_t launch_rope_qkv(const RopeArgs& a, cudaStream_t s);
+
+// Causal attention of a prefill chunk (prefill.cu): T tokens of cache
+// sequence `seq` at positions start .. start + T - 1 (their K/V already in the
+// cache), each over slots 0 .. its own position; online softmax over tiles
+// of 64 positions (Tang section 2.2).
+struct PrefillAttnArgs {
+  const float* q;           // [T, Hq D] rotated
+  float* out;               // [T, Hq D]
+  int T, start, seq, layer, Hq, Hkv, D;
+  KVView kv;
+};
+size_t prefill_attn_smem(int D);
+cudaError_t launch_prefill_attn(const PrefillAttnArgs& a, cudaStream_t s);
 
 struct AttnArgs {
   const float* q;           // [B, Hq D] rotated

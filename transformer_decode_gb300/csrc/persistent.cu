@@ -391,9 +391,9 @@ __device__ void producer(const PersistArgs& a, PShared& S, char* ring, int slot_
                          Spin& sp) {
   const int nph = kPhasesPerLayer * a.L + 1;
   RingPos rp;
-  prefetch_phase<KV16>(a, S, 0);
+  if (a.l2_prefetch) prefetch_phase<KV16>(a, S, 0);
   for (int ph = 0; ph < nph; ++ph) {
-    prefetch_phase<KV16>(a, S, ph + 1);
+    if (a.l2_prefetch) prefetch_phase<KV16>(a, S, ph + 1);
     if (ph < kPhasesPerLayer * a.L && ph % kPhasesPerLayer == kATTN) {
       for (int it = blockIdx.x; it < S.item0[kPMaxBatch]; it += gridDim.x) {
         AttnItem t = attn_item_of(S, a.Hkv, it);
@@ -1583,6 +1583,16 @@ static size_t max_row_bytes(int H, int qd, int F) {
   return m;
 }
 
+// L2 prefetch of the next phase by the producer (NC_PERSIST_PREFETCH=1 in
+// the environment, read once; off by default).
+static int persist_prefetch() {
+  static const int on = [] {
+    const char* e = getenv("NC_PERSIST_PREFETCH");
+    return e && e[0] == '1' ? 1 : 0;
+  }();
+  return on;
+}
+
 // Ring slots (NC_PERSIST_SLOTS in the environment, read once; kPSlots by
 // default): the same shared memory cut into more, smaller tiles.
 static int persist_slots() {
@@ -1653,6 +1663,7 @@ cudaError_t launch_persistent(PersistArgs a, cudaStream_t s) {
     --ns;
   a.nslots = ns;
   a.slot_bytes = (int)(((avail - fixed) / ns) / 128 * 128);
+  a.l2_prefetch = persist_prefetch();
   if ((size_t)a.slot_bytes < row_max) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + (size_t)a.nslots * a.slot_bytes;
   if (BT == 1) return launch_b<1>(a, smem, s);

@@ -127,7 +127,10 @@ __global__ void __launch_bounds__(kB32Threads) k_w8a8_b32(const __grid_constant_
       rows[r] = a.Wq + ((size_t)r * a.N + n) * K;
       sw[r] = a.w_scale[(size_t)r * a.N + n];
     }
-    for (int c0 = lane; c0 < nchunk; c0 += U * kWarp) {
+    // the trip count is the same on every lane (the pair shuffle below needs
+    // the whole warp); chunks past the row are predicated off
+    for (int cb = 0; cb < nchunk; cb += U * kWarp) {
+      const int c0 = cb + lane;
       uint4 w[R][U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {

@@ -34,7 +34,7 @@ EXPORTS = [
     "nc_attn_decode_static", "nc_profile_phases", "nc_read_phase_profile", "nc_decode_path",
     "nc_sample", "nc_sample_scratch_bytes", "nc_attn_decode_static_status",
     "nc_debug_w8a8_codes", "nc_w8a8_gemv_b32",
-    "nc_int4_gemv",
+    "nc_int4_gemv", "nc_prefill", "nc_prefill_scratch_bytes",
 ]
 
 
@@ -118,6 +118,8 @@ def _declare(L):
     L.nc_w8a8_gemv.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
     L.nc_attn_decode_static.argtypes = [i, i, i, i, i, i, vp, vp, vp, C.POINTER(KVStruct), vp, vp]
     L.nc_attn_decode_static_status.argtypes = [vp, C.POINTER(i)]
+    L.nc_prefill.argtypes = [vp, i, i, vp, i, C.POINTER(KVStruct), vp, vp, vp, C.c_size_t, vp]
+    L.nc_prefill_scratch_bytes.argtypes = [vp, i]
     L.nc_debug_w8a8_codes.argtypes = [vp, vp, C.c_size_t, vp, C.c_size_t]
     L.nc_profile_phases.argtypes = [vp, i]
     L.nc_decode_path.argtypes = [vp, i, vp, i, C.POINTER(i)]
@@ -127,9 +129,11 @@ def _declare(L):
     L.nc_w8a8_gemv_b32.argtypes = [vp, vp, f, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp]
     L.nc_int4_gemv.argtypes = [vp, vp, f, vp, vp, i, i, i, i, vp, vp]
     for n in EXPORTS:
-        if n not in ("nc_status_string", "nc_last_error_message", "nc_sample_scratch_bytes"):
+        if n not in ("nc_status_string", "nc_last_error_message", "nc_sample_scratch_bytes",
+                     "nc_prefill_scratch_bytes"):
             getattr(L, n).restype = C.c_int
     L.nc_sample_scratch_bytes.restype = C.c_size_t
+    L.nc_prefill_scratch_bytes.restype = C.c_size_t
 
 
 def _check(rc):
@@ -508,6 +512,27 @@ class Model:
                                         _ptr(logits, torch.float32, "logits", B * V),
                                         _ptr(next_tokens, torch.int32, "next_tokens"),
                                         _stream(stream)))
+
+    def prefill_scratch_bytes(self, T):
+        return int(load().nc_prefill_scratch_bytes(self.handle, int(T)))
+
+    def prefill(self, seq, tokens, start, kv, logits, next_tokens=None, scratch=None, stream=None):
+        """nc_prefill: tokens [T] int32 (device) enter sequence seq at positions
+        start .. start + T - 1 in one forward pass; logits [V] receives the last
+        token's logits. scratch: a device buffer of prefill_scratch_bytes(T)
+        bytes (allocated here when None)."""
+        T = tokens.numel()
+        need = self.prefill_scratch_bytes(T)
+        if scratch is None:
+            scratch = torch.empty(need, dtype=torch.uint8, device=tokens.device)
+        s = kv.struct()
+        _check(load().nc_prefill(self.handle, int(seq), T, _ptr(tokens, torch.int32, "tokens", T),
+                                 int(start), C.byref(s),
+                                 _ptr(logits, torch.float32, "logits", self.shape.vocab),
+                                 _ptr(next_tokens, torch.int32, "next_tokens"),
+                                 _ptr(scratch, None, "scratch"),
+                                 scratch.numel() * scratch.element_size(), _stream(stream)))
+        return scratch
 
     def debug_w8a8_codes(self, codes=None, scales=None):
         """nc_debug_w8a8_codes: while set, every step writes its W8A8
