@@ -276,7 +276,20 @@ def run_reference(args, ws, rank):
     name = args.workload
     if name == SAMPLED:
         name = C1
-    if name == C1:
+    if name in PREFILLS:
+        cfg = PREFILLS[name]
+        shape = getattr(synth, cfg["shape"])
+        T = cfg["T"]
+        oracle.build()
+        om = oracle.OracleModel(shape, cpu_weights(shape))
+        okv = om.new_kv(1, T + 1)
+        toks = synth.token_ids(T, shape.vocab).numpy().astype(np.int32)
+
+        def step(i):
+            om.forward_chunk(okv, 0, toks, 0)
+        batch = T
+        config = {"workload": name, "prompt_tokens": T, "start": 0}
+    elif name == C1:
         shape = synth.QWEN2_0P5B
         n_prompt, n_gen = 32, 64
         prompt = synth.token_ids(n_prompt, shape.vocab).tolist()
@@ -971,6 +984,113 @@ def run_workload(args, ws, rank, local, name):
         }), flush=True)
 
 
+# Prefill workloads: a prompt of T tokens from position 0 as one forward pass
+# (nc_prefill), repeated; the line reports prompt tokens per second and the
+# tensor-core throughput of the pass.
+PREFILLS = {
+    "qwen2_0p5b_prefill512": dict(shape="QWEN2_0P5B", T=512),
+    "qwen3_8b_shape_prefill512": dict(shape="QWEN3_8B", T=512),
+}
+
+
+def prefill_flops(shape, T, start=0):
+    """Algorithmic FLOPs of one prefill pass: 2 per weight per token for the
+    projections, 2 D per (query head, visible position) for each of the two
+    attention products, and the last token's LM head."""
+    H, F, L, V = shape.hidden, shape.ffn, shape.n_layers, shape.vocab
+    nqkv = shape.q_dim + 2 * shape.kv_dim
+    proj = L * (nqkv * H + shape.q_dim * H + 2 * F * H + H * F)
+    seen = sum(start + i + 1 for i in range(T))
+    attn = L * shape.n_q_heads * 4 * shape.head_dim * seen
+    return 2 * proj * T + attn + 2 * V * H
+
+
+def run_prefill(args, ws, rank, local, name):
+    cfg = PREFILLS[name]
+    torch.cuda.set_device(local)
+    shape = getattr(synth, cfg["shape"])
+    T = cfg["T"]
+    wd = synth.model_weights(shape, device="cuda")
+    model = nc.Model(shape, wd, max_batch=1, max_ctx=T + 16)
+    del wd
+    torch.cuda.empty_cache()
+    kv = nc.KVCache(shape, 1, max_ctx=T + 16)
+    tokens = synth.token_ids(T, shape.vocab).to(torch.int32).cuda()
+    logits = torch.empty(shape.vocab, device="cuda")
+    nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(model.prefill_scratch_bytes(T), dtype=torch.uint8, device="cuda")
+
+    def run_steps(k, off=0):
+        for _ in range(k):
+            model.prefill(0, tokens, 0, kv, logits, nxt, scratch=scratch)
+        return [None] * k
+
+    run_steps(args.warmup)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    st = torch.cuda.current_stream()
+    barrier(ws)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    total_s, per_round, _ = timed_rounds(st, run_steps, args.steps)
+    w1 = time.time()
+    barrier(ws)
+    if rank == 0:
+        time.sleep(0.2)
+        sampler.stop()
+    value, el = replica_rate(ws, T, args.steps, total_s)
+    dur = el / args.steps
+    flops = prefill_flops(shape, T)
+    peak = 1891.1
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak_kind = "fallback"
+    if os.path.exists(pk):
+        peak, peak_kind = float(json.load(open(pk))["bf16_tflops"]), "measured"
+    # e2e: the prompt from pinned host memory, the next token read back
+    tok_h = tokens.cpu().pin_memory()
+    nxt_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    k_e2e = min(args.steps, 16)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        tokens.copy_(tok_h, non_blocking=True)
+        model.prefill(0, tokens, 0, kv, logits, nxt, scratch=scratch)
+        nxt_h.copy_(nxt, non_blocking=True)
+        st.synchronize()
+    e2e_value, _ = replica_rate(ws, T, k_e2e, time.perf_counter() - t0)
+    # embed; per layer 2 launches per projection (activation planes, GEMM),
+    # RoPE/append and attention; the head
+    launches = 2 + 10 * shape.n_layers
+    model.close()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "prefill tokens/s at 1 GB300 (prompt as one forward pass)",
+            "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dur * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x (bf16 hi + lo) -> f32",
+            "data": "synthetic",
+            "config": {"workload": name, "prompt_tokens": T, "start": 0,
+                       "weights": "bf16 from seeded N(0,0.02)", "kv": "contiguous fp32",
+                       "path": "nc_prefill: tcgen05 projections, flash-style attention",
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "rounds": rounds_summary(per_round),
+            "roofline": {"bound": "tensor", "kernel": "the whole prefill pass",
+                         "achieved": flops / dur / 1e12, "peak": peak, "unit": "TFLOP/s",
+                         "frac": flops / dur / 1e12 / peak, "traffic": None,
+                         "peak_kind": peak_kind, "algorithmic_flops_per_pass": flops,
+                         "note": "the tensor cores run each product twice (bf16 hi and lo "
+                                 "planes of the fp32 activations); achieved counts it once"},
+            "cpu_baseline": None,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": k_e2e,
+                    "h2d_bytes_per_step": 4 * T, "d2h_bytes_per_step": 4},
+            "gpu_launches": args.steps * launches,
+            "clocks": sampler.summary(w0, w1),
+        }), flush=True)
+
+
 def print_phase_profile(model, shape, run_steps, path):
     """Critical-path timeline of the persistent kernel (nc_profile_phases) over
     a few steps, printed to stderr. For phase p: `handover` = the last CTA's
@@ -1026,7 +1146,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[C1, SAMPLED] + list(WORKLOADS))
+                    choices=[C1, SAMPLED] + list(WORKLOADS) + list(PREFILLS))
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload's model (a small "
                          "case for profiler captures; not a metric line)")
@@ -1041,6 +1161,8 @@ def main():
         run_sampled(args, ws, rank, local)
     elif args.workload == C1:
         run_nc(args, ws, rank, local)
+    elif args.workload in PREFILLS:
+        run_prefill(args, ws, rank, local, args.workload)
     else:
         run_workload(args, ws, rank, local, args.workload)
     if ws > 1:

@@ -181,13 +181,15 @@ def _greedy_compare(shape, wd, wc, prompt, steps, batch=1, past=None, paged=Fals
 # the oracle's own: it must be the neighbouring code (or bf16 value), and the
 # oracle's unrounded value must lie within these distances of the boundary
 # between the two. The GPU and oracle inputs of a rounding step agree to fp32
-# drift, relative 4e-6 or better of the vector's scale over a whole model
-# (the measured logit rel-L2); a quotient v / s of at most 127 code units then
-# moves by at most 127 * 2 * 4e-6 = 1e-3 = 2^-10 units, and a K/V value by
-# 4e-6 of its head vector's largest magnitude (the bound below leaves a
-# factor 8).
+# drift: relative 4e-6 or better of the vector's scale over a whole model on
+# the CUDA-core paths (the measured logit rel-L2), and 3e-5 on the tensor-core
+# path of batch 9..16 (its activations enter as bf16 hi / lo planes: 2^-18 of
+# each input element is lost). A quotient v / s of at most 127 code units
+# then moves by at most 127 * 2 * 4e-6 = 1e-3 = 2^-10 units (W8A8 runs on the
+# CUDA cores), and a K/V value by 3e-5 of its head vector's largest
+# magnitude (the bound below leaves a factor 8).
 CODE_BOUNDARY_TOL = 2.0 ** -10   # code units from a .5 boundary
-KV_BOUNDARY_TOL = 2.0 ** -15     # distance from the rounding interval, in units of the
+KV_BOUNDARY_TOL = 2.0 ** -12     # distance from the rounding interval, in units of the
                                  # head vector's largest magnitude
 
 

@@ -159,33 +159,20 @@ __device__ __forceinline__ void ll_settle(const Addr& addr, uint32_t valid, uint
   }
 }
 
-constexpr int kLLBatch = 16;  // word pairs a thread has in flight per round
-
-// Two adjacent words in one 16-byte load (p 16-byte aligned). Each 8-byte
-// element of a vector access is read as one unit, so each word's value and
-// epoch still come from the same store.
-__device__ __forceinline__ void ld_word2(const uint64_t* p, uint64_t& w0, uint64_t& w1) {
-  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];"
-               : "=l"(w0), "=l"(w1)
-               : "l"(p)
-               : "memory");
-}
-
-// Read `count` word pairs p[0..1], p[stride..stride + 1], ... (count <=
-// kLLBatch, p and stride even): all loads in flight at once, then settle the
-// stale words. out[2 u + e] = word e of pair u.
-__device__ __forceinline__ void ll_get_pairs(const uint64_t* p, int stride, int count,
+// Read `count` words p[0], p[stride], ... (count <= kLLBatch): all loads in
+// flight at once, then settle the stale ones.
+constexpr int kLLBatch = 16;
+__device__ __forceinline__ void ll_get_batch(const uint64_t* p, int stride, int count,
                                              uint32_t epoch, float* out, Spin& sp) {
-  uint64_t w[2 * kLLBatch];
-  const auto addr = [p, stride](int u) { return p + (size_t)(u >> 1) * stride + (u & 1); };
+  uint64_t w[kLLBatch];
+  const auto addr = [p, stride](int u) { return p + (size_t)u * stride; };
 #pragma unroll
   for (int u = 0; u < kLLBatch; ++u)
-    if (u < count) ld_word2(p + (size_t)u * stride, w[2 * u], w[2 * u + 1]);
-  const uint32_t valid = 2 * count >= 32 ? ~0u : ((1u << (2 * count)) - 1u);
-  ll_settle<2 * kLLBatch>(addr, valid, epoch, w, sp);
+    if (u < count) w[u] = ld_word(addr(u));
+  ll_settle<kLLBatch>(addr, (1u << count) - 1u, epoch, w, sp);
 #pragma unroll
-  for (int u = 0; u < 2 * kLLBatch; ++u)
-    if (u < 2 * count) out[u] = __uint_as_float(static_cast<uint32_t>(w[u]));
+  for (int u = 0; u < kLLBatch; ++u)
+    if (u < count) out[u] = __uint_as_float(static_cast<uint32_t>(w[u]));
 }
 
 __device__ __forceinline__ uint32_t epoch_of(uint32_t seq, int phase) {
@@ -336,64 +323,12 @@ __device__ bool produce_kv(const PersistArgs& a, PShared& S, char* ring, int slo
                            int nslots, int layer, int b, int g, int p0, int p1, RingPos& rp,
                            Spin& sp);
 
-// Prefetch into L2 the start of phase ph's data for this CTA: up to
-// kPrefetchBytes of its weight rows, or the cached K/V of its attention
-// items. Issued when the producer begins the phase before it, so the ring
-// refills that follow a hand-over read L2 rather than HBM (the ring itself
-// runs only a few tiles ahead of the consumers).
-constexpr uint32_t kPrefetchBytes = 256 * 1024;
-constexpr uint32_t kPrefetchPiece = 64 * 1024;  // bytes per prefetch instruction
-__device__ __forceinline__ void prefetch_range(const void* p, uint64_t bytes) {
-  const char* c = static_cast<const char*>(p);
-  for (uint64_t o = 0; o < bytes; o += kPrefetchPiece) {
-    const uint64_t n = bytes - o < kPrefetchPiece ? bytes - o : kPrefetchPiece;
-    prefetch_l2(c + o, (uint32_t)n);
-  }
-}
-
-template <bool KV16>
-__device__ void prefetch_phase(const PersistArgs& a, PShared& S, int ph) {
-  const int nph = kPhasesPerLayer * a.L + 1;
-  if (ph >= nph) return;
-  if (ph < kPhasesPerLayer * a.L && ph % kPhasesPerLayer == kATTN) {
-    constexpr int ES = KV16 ? 2 : 4;
-    const int layer = ph / kPhasesPerLayer, D = a.D;
-    const int bs = a.kv.paged ? a.kv.block_size : (1 << 30);
-    for (int it = blockIdx.x; it < S.item0[kPMaxBatch]; it += gridDim.x) {
-      AttnItem t = attn_item_of(S, a.Hkv, it);
-      const int np = cached_positions(a, t.b, S.pos[t.b]);
-      const int p0 = (int)(((long long)t.sp * np) / t.ns);
-      const int p1 = (int)(((long long)(t.sp + 1) * np) / t.ns);
-      for (int q = p0; q < p1;) {  // runs of positions contiguous in the cache
-        const int len = min(p1 - q, bs - q % bs);
-        if (a.kv.slot_ok(t.b, q)) {
-          const size_t off = a.kv.offset(layer, t.b, t.g, q) * ES;
-          const uint64_t nb = (uint64_t)len * D * ES;
-          prefetch_range(static_cast<const char*>(a.kv.k) + off, nb);
-          prefetch_range(static_cast<const char*>(a.kv.v) + off, nb);
-        }
-        q += len;
-      }
-    }
-    return;
-  }
-  const Rows r = phase_rows(a, S, ph);
-  if (r.r0 >= r.r1) return;
-  uint64_t bytes = (uint64_t)(r.r1 - r.r0) * r.K * 2;
-  const uint64_t cap = r.m1 ? kPrefetchBytes / 2 : kPrefetchBytes;
-  if (bytes > cap) bytes = cap & ~uint64_t(15);
-  prefetch_range(r.m0 + (size_t)r.r0 * r.K, bytes);
-  if (r.m1) prefetch_range(r.m1 + (size_t)r.r0 * r.K, bytes);
-}
-
 template <bool KV16>
 __device__ void producer(const PersistArgs& a, PShared& S, char* ring, int slot_bytes, int nslots,
                          Spin& sp) {
   const int nph = kPhasesPerLayer * a.L + 1;
   RingPos rp;
-  if (a.l2_prefetch) prefetch_phase<KV16>(a, S, 0);
   for (int ph = 0; ph < nph; ++ph) {
-    if (a.l2_prefetch) prefetch_phase<KV16>(a, S, ph + 1);
     if (ph < kPhasesPerLayer * a.L && ph % kPhasesPerLayer == kATTN) {
       for (int it = blockIdx.x; it < S.item0[kPMaxBatch]; it += gridDim.x) {
         AttnItem t = attn_item_of(S, a.Hkv, it);
@@ -479,34 +414,25 @@ __device__ __noinline__ void gather_input(const PersistArgs& a, const uint64_t* 
 #pragma unroll 1
   for (int b = 0; b < BT; ++b) {
     float ss = 0.f;
-    // thread ct takes the element pairs ct, ct + T, ... (n is a multiple of 8)
-    for (int q0 = ct; 2 * q0 < n; q0 += kLLBatch * kPConsumerThreads) {
-      const int count = min(kLLBatch, (n / 2 - q0 + kPConsumerThreads - 1) / kPConsumerThreads);
-      float v[2 * kLLBatch];
+    for (int i0 = ct; i0 < n; i0 += kLLBatch * kPConsumerThreads) {
+      const int count = min(kLLBatch, (n - i0 + kPConsumerThreads - 1) / kPConsumerThreads);
+      float v[kLLBatch];
       if (b >= nb) {
 #pragma unroll
-        for (int u = 0; u < 2 * kLLBatch; ++u) v[u] = 0.f;
+        for (int u = 0; u < kLLBatch; ++u) v[u] = 0.f;
       } else if (embed_rows) {
 #pragma unroll
         for (int u = 0; u < kLLBatch; ++u)
-          if (u < count) {
-            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(
-                embed_rows + (size_t)S.tok[b] * n + 2 * (q0 + u * kPConsumerThreads));
-            v[2 * u] = bf16_lo(w2);
-            v[2 * u + 1] = bf16_hi(w2);
-          }
+          if (u < count)
+            v[u] = bf16_to_f32(embed_rows[(size_t)S.tok[b] * n + i0 + u * kPConsumerThreads]);
       } else {
-        ll_get_pairs(src + (size_t)b * src_stride + 2 * q0, 2 * kPConsumerThreads, count, epoch,
-                     v, sp);
+        ll_get_batch(src + (size_t)b * src_stride + i0, kPConsumerThreads, count, epoch, v, sp);
       }
 #pragma unroll
       for (int u = 0; u < kLLBatch; ++u) {
         if (u >= count) break;
-        const int i = 2 * (q0 + u * kPConsumerThreads);
-        xs[b * n + xs_at(i, n)] = v[2 * u];
-        xs[b * n + xs_at(i + 1, n)] = v[2 * u + 1];
-        ss = fmaf(v[2 * u], v[2 * u], ss);
-        ss = fmaf(v[2 * u + 1], v[2 * u + 1], ss);
+        xs[b * n + xs_at(i0 + u * kPConsumerThreads, n)] = v[u];
+        ss = fmaf(v[u], v[u], ss);
       }
     }
     if (gamma) {
@@ -1583,16 +1509,6 @@ static size_t max_row_bytes(int H, int qd, int F) {
   return m;
 }
 
-// L2 prefetch of the next phase by the producer (NC_PERSIST_PREFETCH=1 in
-// the environment, read once; off by default).
-static int persist_prefetch() {
-  static const int on = [] {
-    const char* e = getenv("NC_PERSIST_PREFETCH");
-    return e && e[0] == '1' ? 1 : 0;
-  }();
-  return on;
-}
-
 // Ring slots (NC_PERSIST_SLOTS in the environment, read once; kPSlots by
 // default): the same shared memory cut into more, smaller tiles.
 static int persist_slots() {
@@ -1663,7 +1579,6 @@ cudaError_t launch_persistent(PersistArgs a, cudaStream_t s) {
     --ns;
   a.nslots = ns;
   a.slot_bytes = (int)(((avail - fixed) / ns) / 128 * 128);
-  a.l2_prefetch = persist_prefetch();
   if ((size_t)a.slot_bytes < row_max) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + (size_t)a.nslots * a.slot_bytes;
   if (BT == 1) return launch_b<1>(a, smem, s);

@@ -57,7 +57,6 @@ struct PersistArgs {
   unsigned long long* prof;
   // shared-memory plan (filled by launch_persistent)
   int slot_bytes, nslots, ring_offset, xs_offset, attn_offset, attn_bytes;
-  int l2_prefetch;  // the producer prefetches the next phase into L2
 };
 
 // True when the persistent kernel fits this shape (shared memory, batch,
