@@ -722,6 +722,18 @@ __device__ __forceinline__ float2 kv_smem2(const char* base, int idx) {
   }
 }
 
+// Elements idx .. idx + E - 1 (E = 2 or 4, idx a multiple of E) in one load.
+template <bool KV16, int E>
+__device__ __forceinline__ void kv_smemE(const char* base, int idx, float (&o)[E]) {
+  if constexpr (E == 4) {
+    kv_smem4<KV16>(base, idx, o);
+  } else {
+    const float2 v = kv_smem2<KV16>(base, idx);
+    o[0] = v.x;
+    o[1] = v.y;
+  }
+}
+
 // Consumer: one item, i.e. split `split` of the ns splits of (sequence b, kv
 // head g). RoPE (+ q/k norm) of the G query heads and the key; split 0
 // appends K/V at slot pos and opens the online-softmax state with the new
@@ -732,7 +744,7 @@ __device__ __forceinline__ float2 kv_smem2(const char* base, int idx) {
 // of them (Tang section 2.2: per head M = max_s m_s, weights
 // w_s = exp(m_s - M) l_s, out = sum_s (w_s / sum_t w_t) o_s; one split gives
 // weight l / l = 1 and out = o exactly) and writes the output words.
-template <int D, bool KV16>
+template <int D, bool KV16, int GP>
 __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int split, int ns,
                                             int p0, int p1, int layer, uint32_t ep_qkv,
                                             uint32_t ep_out, int nslots, RingPos& rp, Spin& sp,
@@ -759,10 +771,7 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   float* qs = scratch;                        // [GM][D]
   float* kn = qs + GM * D;                    // [D]
   float* vn = kn + D;                         // [D]
-  float* sc = vn + D;                         // [2][GM][kAttnMaxChunk], by chunk parity
-  float* mrun = sc + 2 * GM * kAttnMaxChunk;  // [GM] running max
-  float* lrun = mrun + GM;                    // [GM] running sum
-  float* resc = lrun + GM;                    // [GM] rescale of the chunk
+  float* sc = vn + D;                         // the scan warps' (m, l), then the merge's
   const PLayer& P = S.layers[layer];
 
   // Warp w < G gathers query head w, warp G the key, warp G + 1 the value;
@@ -823,126 +832,127 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   }
   consumer_sync();
   if (prof_in) *prof_in = global_timer();  // the phase input (q, k, v) is in
-  // the new position opens the running state: m = its score, l = 1, acc = v
+  // The scan. Warps 0 .. SW - 1 each keep their own online-softmax state of
+  // every query head over the positions they take, with no block barrier
+  // inside a chunk: lane l holds dims l E .. l E + E - 1 of each head in
+  // registers; a group of PG = 32 / GP positions (GP = G rounded up to a
+  // power of two) gives 32 partial dot products per lane, which one
+  // reduce-scatter turns into lane i's score of (position i / GP, head
+  // i % GP). The warps' states are combined once, after the scan.
+  constexpr int SW = 8;           // scan warps
+  constexpr int PG = kWarp / GP;  // positions per group
   const float scale = 1.f / sqrtf((float)D);
-  for (int h = warp; h < G; h += kPConsumerWarps) {
-    float s = 0.f;
+  float qr[GP][E], acc[GP][E], mh[GP], lh[GP];
 #pragma unroll
-    for (int j = 0; j < E; ++j) s = fmaf(qs[h * D + lane + 32 * j], kn[lane + 32 * j], s);
-    s = warp_sum(s) * scale;
-    if (lane == 0) {
-      mrun[h] = own_new ? s : -INFINITY;
-      lrun[h] = own_new ? 1.f : 0.f;
+  for (int h = 0; h < GP; ++h) {
+    mh[h] = -INFINITY;
+    lh[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      acc[h][e] = 0.f;
+      qr[h][e] = h < G ? qs[h * D + lane * E + e] : 0.f;
     }
   }
-  const int npair = G * (D / 2);
-  const int my_h = ct / (D / 2), my_d2 = ct % (D / 2);
-  float acc0 = 0.f, acc1 = 0.f;
-  if (ct < npair && own_new) {
-    acc0 = vn[2 * my_d2];
-    acc1 = vn[2 * my_d2 + 1];
+  // the new position opens warp 0's state: m = its score, l = 1, acc = v
+  if (warp == 0 && own_new) {
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) d = fmaf(qr[h][e], kn[lane * E + e], d);
+      d = warp_sum(d) * scale;
+      if (h < G) {
+        mh[h] = d;
+        lh[h] = 1.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[h][e] = vn[lane * E + e];
+      }
+    }
   }
-  consumer_sync();
-  int cpar = 0;
-  for (int t0 = p0; t0 < p1; t0 += CP, cpar ^= 1) {
+  const int hl = lane % GP, pl = lane / GP;  // what lane holds after the reduce
+  for (int t0 = p0; t0 < p1; t0 += CP) {
     const int n = min(CP, p1 - t0);
     const int s = rp.s;
     ring_wait(&S.full[s], rp.par, sp);
     const char* Ks = ring + (size_t)s * slot_bytes;
     const char* Vs = Ks + (size_t)CP * D * ES;
-    float* scc = sc + cpar * GM * kAttnMaxChunk;  // the other buffer may still be read
-    // scores: warp -> (head, 32 positions); lane l reads its row from column
-    // (d + l) mod D so the 32 rows of a warp fall in different banks
-    const int blocks = (n + 31) / 32;
-    for (int wb = warp; wb < G * blocks; wb += kPConsumerWarps) {
-      const int h = wb % G, p = (wb / G) * 32 + lane;
-      if (p < n) {
-        float sv = -INFINITY;
-        if (kv.slot_ok(b, t0 + p)) {
-          // 4-element columns, skewed by lane: the 8 lanes of each 16-byte
-          // load phase read 8 different bank groups
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
-          const float* qh = qs + h * D;
+    if (warp < SW) {
+      for (int g0 = warp * PG; g0 < n; g0 += SW * PG) {
+        float part[kWarp];
 #pragma unroll
-          for (int j = 0; j < D / 4; ++j) {
-            const int c = ((j + lane) & (D / 4 - 1)) * 4;
-            const float4 q4 = *reinterpret_cast<const float4*>(qh + c);
-            float k4[4];
-            kv_smem4<KV16>(Ks, p * D + c, k4);
-            s4[0] = fmaf(q4.x, k4[0], s4[0]);
-            s4[1] = fmaf(q4.y, k4[1], s4[1]);
-            s4[2] = fmaf(q4.z, k4[2], s4[2]);
-            s4[3] = fmaf(q4.w, k4[3], s4[3]);
+        for (int p = 0; p < PG; ++p) {
+          float k[E];
+          kv_smemE<KV16, E>(Ks, (g0 + p < n ? g0 + p : 0) * D + lane * E, k);
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) d = fmaf(qr[h][e], k[e], d);
+            part[p * GP + h] = d;
           }
-          sv = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * scale;
         }
-        scc[h * kAttnMaxChunk + p] = sv;
+        warp_sum_many<kWarp>(part);
+        const int pp = g0 + pl;
+        const bool ok = pp < n && hl < G && kv.slot_ok(b, t0 + pp);
+        const float sv = ok ? part[0] * scale : -INFINITY;
+        float mx = sv;  // the group's max of each head, over the lanes holding it
+#pragma unroll
+        for (int o = GP; o < kWarp; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        float corr[GP], mine_m = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+          const float mn = fmaxf(mh[h], __shfl_sync(0xFFFFFFFFu, mx, h));
+          corr[h] = mh[h] == -INFINITY ? 0.f : expf(mh[h] - mn);
+          mh[h] = mn;
+          if (h == hl) mine_m = mn;
+        }
+        const float pr = sv == -INFINITY ? 0.f : expf(sv - mine_m);
+        float sm = pr;
+#pragma unroll
+        for (int o = GP; o < kWarp; o <<= 1) sm += __shfl_xor_sync(0xFFFFFFFFu, sm, o);
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+          lh[h] = lh[h] * corr[h] + __shfl_sync(0xFFFFFFFFu, sm, h);
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[h][e] *= corr[h];
+        }
+#pragma unroll
+        for (int p = 0; p < PG; ++p) {
+          float v[E];
+          kv_smemE<KV16, E>(Vs, (g0 + p < n ? g0 + p : 0) * D + lane * E, v);
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            const float ph = __shfl_sync(0xFFFFFFFFu, pr, p * GP + h);
+            // a masked position (weight 0) may sit over stale shared memory,
+            // so its value is replaced, not multiplied
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[h][e] = fmaf(ph, ph == 0.f ? 0.f : v[e], acc[h][e]);
+          }
+        }
       }
-    }
-    consumer_sync();
-    for (int h = warp; h < G; h += kPConsumerWarps) {
-      float m = -INFINITY;
-      for (int t = lane; t < n; t += kWarp) m = fmaxf(m, scc[h * kAttnMaxChunk + t]);
-      m = warp_max(m);
-      const float m_new = fmaxf(mrun[h], m);
-      float l = 0.f;
-      for (int t = lane; t < n; t += kWarp) {
-        const float x = scc[h * kAttnMaxChunk + t];
-        const float p = x == -INFINITY ? 0.f : expf(x - m_new);
-        scc[h * kAttnMaxChunk + t] = p;
-        l += p;
-      }
-      l = warp_sum(l);
-      if (lane == 0) {
-        const float r = mrun[h] == -INFINITY ? 0.f : expf(mrun[h] - m_new);
-        resc[h] = r;
-        lrun[h] = lrun[h] * r + l;
-        mrun[h] = m_new;
-      }
-    }
-    consumer_sync();
-    if (ct < npair) {
-      const float r = resc[my_h];
-      // two interleaved chains per output; a masked position (p = 0) may sit
-      // over stale shared memory, so its value is replaced, not multiplied
-      float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;
-      const float* ph = scc + my_h * kAttnMaxChunk;
-      int t = 0;
-#pragma unroll 4
-      for (; t + 1 < n; t += 2) {
-        const float pa = ph[t], pb = ph[t + 1];
-        const float2 va = kv_smem2<KV16>(Vs, t * D + 2 * my_d2);
-        const float2 vb = kv_smem2<KV16>(Vs, (t + 1) * D + 2 * my_d2);
-        e0 = fmaf(pa, pa == 0.f ? 0.f : va.x, e0);
-        e1 = fmaf(pa, pa == 0.f ? 0.f : va.y, e1);
-        o0 = fmaf(pb, pb == 0.f ? 0.f : vb.x, o0);
-        o1 = fmaf(pb, pb == 0.f ? 0.f : vb.y, o1);
-      }
-      if (t < n) {
-        const float pa = ph[t];
-        const float2 va = kv_smem2<KV16>(Vs, t * D + 2 * my_d2);
-        e0 = fmaf(pa, pa == 0.f ? 0.f : va.x, e0);
-        e1 = fmaf(pa, pa == 0.f ? 0.f : va.y, e1);
-      }
-      acc0 = fmaf(acc0, r, e0 + o0);
-      acc1 = fmaf(acc1, r, e1 + o1);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[s]);
     rp.next(nslots);
-    // no barrier here: the next chunk writes the other score buffer, and the
-    // one after it is behind that chunk's two barriers
   }
+  // combine the scan warps' states per head: M = max_w m_w, weights
+  // c_w = e^(m_w - M), L = sum_w c_w l_w, O = sum_w c_w acc_w (warps in order)
+  float* cmb = reinterpret_cast<float*>(smem + a.xs_offset);  // [SW][G][D] (idle now)
+  float* mlw = sc;                                            // [SW][GM][2]
+  if (warp < SW) {
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+      if (h < G) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) cmb[(warp * G + h) * D + lane * E + e] = acc[h][e];
+        if (lane == 0) {
+          mlw[(warp * GM + h) * 2] = mh[h];
+          mlw[(warp * GM + h) * 2 + 1] = lh[h];
+        }
+      }
+  }
+  consumer_sync();
   uint64_t* const aout = a.aw + (size_t)b * Hq * D + (size_t)g * G * D;  // [G][D] words
-  if (ns == 1) {
-    if (ct < npair) {
-      const float inv = lrun[my_h] > 0.f ? 1.f / lrun[my_h] : 0.f;
-      st_word(aout + my_h * D + 2 * my_d2, acc0 * inv, ep_out);
-      st_word(aout + my_h * D + 2 * my_d2 + 1, acc1 * inv, ep_out);
-    }
-    consumer_sync();  // the scratch is reused by the next item
-    return;
-  }
   // split partials [G][DP] per head of this (b, g, split): o[D], then m, l
   // (rows padded to a 16-byte multiple, so the merge can stage them with
   // 16-byte asynchronous copies)
@@ -950,11 +960,31 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   float* const parts = a.apart + ((size_t)b * kPMaxSplits * Hq + (size_t)g * G) * DP;
   const size_t sstride = (size_t)Hq * DP;  // from one split's partials to the next
   float* const mine = parts + split * sstride;
-  if (ct < npair) {
-    const float inv = lrun[my_h] > 0.f ? 1.f / lrun[my_h] : 0.f;
-    *reinterpret_cast<float2*>(mine + my_h * DP + 2 * my_d2) = make_float2(acc0 * inv, acc1 * inv);
+  for (int i = ct; i < G * D; i += kPConsumerThreads) {
+    const int h = i / D, d = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < SW; ++w) M = fmaxf(M, mlw[(w * GM + h) * 2]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < SW; ++w) {
+      const float m = mlw[(w * GM + h) * 2];
+      const float c = m == -INFINITY ? 0.f : expf(m - M);
+      L = fmaf(c, mlw[(w * GM + h) * 2 + 1], L);
+      O = fmaf(c, cmb[(w * G + h) * D + d], O);
+    }
+    const float o = L > 0.f ? O / L : 0.f;
+    if (ns == 1) {
+      st_word(aout + i, o, ep_out);
+    } else {
+      mine[h * DP + d] = o;
+      if (d == 0) *reinterpret_cast<float2*>(mine + h * DP + D) = make_float2(M, L);
+    }
   }
-  if (ct < G) *reinterpret_cast<float2*>(mine + ct * DP + D) = make_float2(mrun[ct], lrun[ct]);
+  if (ns == 1) {
+    consumer_sync();  // the scratch is reused by the next item
+    return;
+  }
   __threadfence();  // each writer's partials are visible GPU-wide before the ticket
   consumer_sync();
   unsigned int* const tick = a.atick + ((size_t)layer * kPMaxBatch + b) * Hkv + g;
@@ -1410,8 +1440,18 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
           const int np = cached_positions(a, t.b, S.pos[t.b]);
           const int p0 = (int)(((long long)t.sp * np) / t.ns);
           const int p1 = (int)(((long long)(t.sp + 1) * np) / t.ns);
-          attention_item<D, KV16>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, epoch_of(seq, ph - 1),
-                                  ep, nslots, rp, sp, first && prof ? prof + 2 * ph + 1 : nullptr);
+          unsigned long long* const pin = first && prof ? prof + 2 * ph + 1 : nullptr;
+          const uint32_t eq = epoch_of(seq, ph - 1);
+          const int G = a.Hq / a.Hkv;
+          if (G <= 2)
+            attention_item<D, KV16, 2>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp,
+                                       sp, pin);
+          else if (G <= 4)
+            attention_item<D, KV16, 4>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp,
+                                       sp, pin);
+          else
+            attention_item<D, KV16, 8>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp,
+                                       sp, pin);
           first = false;
         }
         if (prof && first) prof[2 * ph + 1] = global_timer();  // a CTA with no item
@@ -1524,8 +1564,11 @@ static int persist_slots() {
 // split's partial block (G heads of D + 4 floats), which the attention merge
 // stages there.
 static size_t xs_bytes(int H, int qd, int F, int D, int G, int BT) {
-  const size_t v = (size_t)BT * kmax_of(H, qd, F) * 4, p = (size_t)G * (D + 4) * 4;
-  return v > p ? v : p;
+  // also the attention scan's combine buffer [8 warps][G][D]
+  size_t v = (size_t)BT * kmax_of(H, qd, F) * 4;
+  const size_t p = (size_t)G * (D + 4) * 4, c = (size_t)8 * G * D * 4;
+  if (p > v) v = p;
+  return c > v ? c : v;
 }
 static size_t persistent_fixed_smem(int H, int qd, int F, int D, int G, int BT) {
   size_t off = round128(sizeof(PShared));
