@@ -1106,6 +1106,8 @@ def print_phase_profile(model, shape, run_steps, path):
     names = ["qkv", "attention", "o-proj", "gate|up", "down", "lm-head"]
     hand = {n: [] for n in names}
     work = {n: [] for n in names}
+    sub = {k: [] for k in ("scan", "publish", "merge", "to next phase", "scan per CTA (max)",
+                           "first chunk wait (max)", "last chunk wait (max)")}
     totals = []
     model.profile_phases(True)
     for it in range(4):
@@ -1127,6 +1129,21 @@ def print_phase_profile(model, shape, run_steps, path):
             fin = start[:, p + 1].max() if p + 1 < nph else c1.max()
             hand[kind].append((last_in - fin_prev) / 1e3)
             work[kind].append((fin - last_in) / 1e3)
+            if kind == "attention":
+                at = rec["attn"].numpy().astype(np.int64)[:, p // 5]
+                done = ok & (at[:, 0] >= inp[:, p])
+                if done.any():
+                    scan = at[done, 0].max()
+                    pub = at[done, 1].max()
+                    merged = at[done, 2]
+                    mg = merged[merged > 0].max() if (merged > 0).any() else pub
+                    sub["scan"].append((scan - last_in) / 1e3)
+                    sub["publish"].append((pub - scan) / 1e3)
+                    sub["merge"].append((mg - pub) / 1e3)
+                    sub["to next phase"].append((fin - mg) / 1e3)
+                    sub["scan per CTA (max)"].append((at[done, 0] - inp[done, p]).max() / 1e3)
+                    sub["first chunk wait (max)"].append((at[done, 3] - inp[done, p]).max() / 1e3)
+                    sub["last chunk wait (max)"].append((at[done, 4] - inp[done, p]).max() / 1e3)
     model.profile_phases(False)
     print(f"phase profile ({len(totals)} steps, median step {statistics.median(totals):.1f} us):",
           file=sys.stderr)
@@ -1135,6 +1152,10 @@ def print_phase_profile(model, shape, run_steps, path):
         if hand[k]:
             print(f"{k:10s} {statistics.median(hand[k]):12.2f} {statistics.median(work[k]):9.2f}",
                   file=sys.stderr)
+    if sub["scan"]:
+        print("attention work, critical path (last CTA to reach each mark), us: "
+              + ", ".join(f"{k} {statistics.median(v):.2f}" for k, v in sub.items()),
+              file=sys.stderr)
 
 
 def main():

@@ -260,11 +260,16 @@ nc_status nc_debug_w8a8_codes(nc_model* m, int8_t* codes_dev, size_t codes_capac
  * start of each phase and when the phase's input had arrived; phases are, per
  * layer, QKV, attention, o-proj, gate|up, down, then the LM head.
  * nc_read_phase_profile synchronises `stream` and copies the last step's
- * record: for each of the n_sm CTAs (one per SM) 2 * P + 2 values, P =
- * 5 * n_layers + 1: [2p] start of phase p, [2p + 1] its input in, then the
- * CTA's start and end (the CTA that finishes the step: the step's end).
- * *n receives the count n_sm * (2 * P + 2); a smaller capacity returns
- * NC_ERR_CAPACITY. */
+ * record: for each of the n_sm CTAs (one per SM) 2 * P + 2 + 8 * n_layers
+ * values, P = 5 * n_layers + 1: [2p] start of phase p, [2p + 1] its input
+ * in, then the CTA's start and end (the CTA that finishes the step: the
+ * step's end), then per layer l eight values of the CTA's first attention
+ * item: [2P + 2 + 8l] its split's softmax states combined, [+1] its output
+ * (or split partials and ticket) published, [+2] the merge of the splits
+ * done (0 unless this CTA merged), [+3] and [+4] the first and the last K/V
+ * chunk in shared memory (as the first scan warp saw them), [+5] that
+ * warp's scan done, [+6], [+7] unused. *n receives the count; a smaller
+ * capacity returns NC_ERR_CAPACITY. */
 nc_status nc_profile_phases(nc_model* m, int enable);
 nc_status nc_read_phase_profile(nc_model* m, void* stream, unsigned long long* out_host,
                                 int capacity, int* n);

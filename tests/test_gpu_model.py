@@ -353,6 +353,18 @@ def test_decode_path_dispatch():
     model.close()
 
 
+def test_decode_group6_d128_runs_staged():
+    """Six query heads per kv head at D = 128 are beyond the persistent
+    kernel's attention instances (groups of at most 4 at that head size): the
+    step runs on the stage kernels, and its tokens still match the oracle."""
+    shape = dataclasses.replace(synth.TINY_QKNORM, n_q_heads=6, n_kv_heads=1)
+    wd, wc = weights_both(shape)
+    model = nc.Model(shape, wd, max_batch=1, max_ctx=64)
+    assert model.decode_path(1, nc.KVCache(shape, 1, max_ctx=64)) == "staged"
+    model.close()
+    _greedy_compare(shape, wd, wc, None, steps=6, past=[20])
+
+
 @pytest.mark.parametrize("batch", [2, 4])
 def test_decode_tiny_persistent_batch(batch):
     """The persistent kernel at batch 2 and 4, mixed positions."""

@@ -157,7 +157,7 @@ nc_status nc_read_phase_profile(nc_model* m, void* stream, unsigned long long* o
                                 int capacity, int* n) {
   NC_CHECK(m && out_host && n, NC_ERR_INVALID_ARGUMENT, "null argument");
   Model* mm = M(m);
-  const int count = num_sms() * (2 * (5 * mm->cfg.n_layers + 1) + 2);
+  const int count = num_sms() * (int)prof_values(mm->cfg.n_layers);
   NC_CHECK(capacity >= count, NC_ERR_CAPACITY, "the profile holds %d values", count);
   cudaError_t e = cudaStreamSynchronize(S(stream));
   if (!e) e = cudaMemcpy(out_host, mm->prof, sizeof(unsigned long long) * count,

@@ -218,7 +218,7 @@ nc_status model_create(const nc_config* cfg, const nc_weights* w, int max_batch,
     m->hw = W.take<uint64_t>(pb * F);
     m->pticket = W.take<unsigned int>(1);
     m->seq = W.take<unsigned int>(1);
-    m->prof = W.take<unsigned long long>((size_t)num_sms() * (2 * (5 * (size_t)c.n_layers + 1) + 2));
+    m->prof = W.take<unsigned long long>((size_t)num_sms() * prof_values(c.n_layers));
     m->players = A.take<PLayer>(c.n_layers);
   };
   Arena A0, W0;

@@ -748,7 +748,8 @@ template <int D, bool KV16, int GP>
 __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int split, int ns,
                                             int p0, int p1, int layer, uint32_t ep_qkv,
                                             uint32_t ep_out, int nslots, RingPos& rp, Spin& sp,
-                                            unsigned long long* prof_in) {
+                                            unsigned long long* prof_in,
+                                            unsigned long long* prof_sub) {
   // shared-memory pointers are derived from the dynamic shared array here, so
   // the compiler addresses them as shared, not generic
   extern __shared__ __align__(128) char smem[];
@@ -870,10 +871,12 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     }
   }
   const int hl = lane % GP, pl = lane / GP;  // what lane holds after the reduce
+  unsigned long long* const mark = prof_sub && ct == 0 ? prof_sub : nullptr;
   for (int t0 = p0; t0 < p1; t0 += CP) {
     const int n = min(CP, p1 - t0);
     const int s = rp.s;
     ring_wait(&S.full[s], rp.par, sp);
+    if (mark) mark[t0 == p0 ? 3 : 4] = global_timer();
     const char* Ks = ring + (size_t)s * slot_bytes;
     const char* Vs = Ks + (size_t)CP * D * ES;
     if (warp < SW) {
@@ -935,6 +938,12 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     if (lane == 0) mbar_arrive(&S.empty[s]);
     rp.next(nslots);
   }
+  if (mark) {
+    const unsigned long long now = global_timer();
+    if (p1 <= p0) mark[3] = now;           // nothing to scan
+    if (p1 - p0 <= CP) mark[4] = mark[3];  // one chunk: the first is the last
+    mark[5] = now;
+  }
   // combine the scan warps' states per head: M = max_w m_w, weights
   // c_w = e^(m_w - M), L = sum_w c_w l_w, O = sum_w c_w acc_w (warps in order)
   float* cmb = reinterpret_cast<float*>(smem + a.xs_offset);  // [SW][G][D] (idle now)
@@ -952,6 +961,10 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
       }
   }
   consumer_sync();
+  if (prof_sub && ct == 0) {
+    prof_sub[0] = global_timer();
+    prof_sub[2] = 0ull;
+  }
   uint64_t* const aout = a.aw + (size_t)b * Hq * D + (size_t)g * G * D;  // [G][D] words
   // split partials [G][DP] per head of this (b, g, split): o[D], then m, l
   // (rows padded to a 16-byte multiple, so the merge can stage them with
@@ -983,18 +996,45 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   }
   if (ns == 1) {
     consumer_sync();  // the scratch is reused by the next item
+    if (prof_sub && ct == 0) prof_sub[1] = global_timer();
     return;
   }
-  __threadfence();  // each writer's partials are visible GPU-wide before the ticket
+  // The ticket. The barrier orders every thread's partials before thread
+  // 0's fence, which publishes them GPU-wide (cumulatively) before its
+  // arrival; the split that arrives last fences again before the barrier
+  // that lets its threads read the others' partials.
   consumer_sync();
   unsigned int* const tick = a.atick + ((size_t)layer * kPMaxBatch + b) * Hkv + g;
-  if (ct == 0) S.merge = atomicAdd(tick, 1u) == (unsigned)(ns - 1);
+  if (ct == 0) {
+    __threadfence();
+    const bool last = atomicAdd(tick, 1u) == (unsigned)(ns - 1);
+    if (last) __threadfence();
+    S.merge = last;
+  }
   consumer_sync();
+  if (prof_sub && ct == 0) prof_sub[1] = global_timer();
   if (!S.merge) return;  // uniform: read after the barrier
-  __threadfence();       // the other splits' partials, published before their tickets
-  // (m, l) of every (split, head), one load each, all in flight together
+  // The splits' outputs are staged into the (idle) input-vector region in
+  // rounds of as many splits as it holds. The first round's copies are in
+  // flight while the (m, l) of every (split, head) are loaded (one load
+  // each); then warp h forms head h's merge weights, lane t that of split t:
+  // M = max_t m_t, w_t = e^(m_t - M) l_t, coef_t = w_t / sum w (a division,
+  // not a reciprocal, as in the single-split case). Every thread accumulates
+  // its elements over the splits in index order.
   float* ml = sc;                          // [ns][G][2]
   float* coef = sc + 2 * kPMaxSplits * GM;  // [G][kPMaxSplits] merge weights
+  float* stage = reinterpret_cast<float*>(smem + a.xs_offset);
+  const int per_split = G * DP;  // floats of one split's block
+  const int span = (a.attn_offset - a.xs_offset) / (per_split * 4);
+  const auto stage_round = [&](int t0) {
+    const int chunks = min(span, ns - t0) * (per_split / 4);
+    for (int c = ct; c < chunks; c += kPConsumerThreads) {
+      const int t = c / (per_split / 4), r = c % (per_split / 4);
+      cp_async16(stage + t * per_split + 4 * r, parts + (t0 + t) * sstride + 4 * r);
+    }
+    cp_async_commit();
+  };
+  stage_round(0);
   if (ct < ns * G) {
     const int t = ct / G, h = ct % G;
     const float2 v = __ldcg(reinterpret_cast<const float2*>(parts + t * sstride + h * DP + D));
@@ -1002,38 +1042,21 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     ml[2 * ct + 1] = v.y;
   }
   consumer_sync();
-  if (ct < G) {
-    float M = -INFINITY;
-    for (int t = 0; t < ns; ++t) M = fmaxf(M, ml[2 * (t * G + ct)]);
-    float L = 0.f;
-    for (int t = 0; t < ns; ++t) {
-      const float m = ml[2 * (t * G + ct)], l = ml[2 * (t * G + ct) + 1];
-      const float w = m == -INFINITY ? 0.f : expf(m - M) * l;
-      coef[ct * kPMaxSplits + t] = w;
-      L += w;
-    }
-    // a division (not a reciprocal) so that one split gives l / l = 1
-    for (int t = 0; t < ns; ++t)
-      coef[ct * kPMaxSplits + t] = L > 0.f ? coef[ct * kPMaxSplits + t] / L : 0.f;
+  if (warp < G) {
+    const float m = lane < ns ? ml[2 * (lane * G + warp)] : -INFINITY;
+    const float l = lane < ns ? ml[2 * (lane * G + warp) + 1] : 0.f;
+    const float M = warp_max(m);
+    const float w = m == -INFINITY ? 0.f : expf(m - M) * l;
+    const float L = warp_sum(w);
+    if (lane < ns) coef[warp * kPMaxSplits + lane] = L > 0.f ? w / L : 0.f;
   }
-  // the splits' outputs, staged into the (idle) input-vector region in rounds
-  // of as many splits as it holds; every thread accumulates its elements
-  // over the splits in index order
-  float* stage = reinterpret_cast<float*>(smem + a.xs_offset);
-  const int per_split = G * DP;  // floats of one split's block
-  const int span = (a.attn_offset - a.xs_offset) / (per_split * 4);
   constexpr int EPT = (8 * 128 + kPConsumerThreads - 1) / kPConsumerThreads;  // outputs a thread owns
   float o[EPT];
 #pragma unroll
   for (int e = 0; e < EPT; ++e) o[e] = 0.f;
   for (int t0 = 0; t0 < ns; t0 += span) {
     const int nt = min(span, ns - t0);
-    const int chunks = nt * (per_split / 4);
-    for (int c = ct; c < chunks; c += kPConsumerThreads) {
-      const int t = c / (per_split / 4), r = c % (per_split / 4);
-      cp_async16(stage + t * per_split + 4 * r, parts + (t0 + t) * sstride + 4 * r);
-    }
-    cp_async_commit();
+    if (t0 > 0) stage_round(t0);
     cp_async_wait_all();
     consumer_sync();  // staged (and, in the first round, coef written)
 #pragma unroll
@@ -1052,6 +1075,7 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     const int i = ct + e * kPConsumerThreads;
     if (i < G * D) st_word(aout + i, o[e], ep_out);
   }
+  if (prof_sub && ct == 0) prof_sub[2] = global_timer();
 }
 
 // The tiles of one projection phase (see gemv_phase). MODE 0: batch 1, rows of
@@ -1361,6 +1385,43 @@ __device__ __forceinline__ void gemv_phase(const PersistArgs& a, int ph, uint32_
 }
 
 // ------------------------------------------------------------------ the kernel
+// The attention phase of one CTA: its items, each scanned by the instance
+// for the group size rounded up to a power of two (at most 4 heads a group
+// with D = 128, whose 8-head instance's registers would crowd the
+// projection phases' code out of registers; persistent_supported keeps
+// such shapes on the stage path). A function of its own, so that the
+// kernel's loop keeps few values live across the call.
+template <int D, bool KV16>
+__device__ __noinline__ void attention_phase(const PersistArgs& a, int ph, int layer, uint32_t seq,
+                                             uint32_t ep, int nslots, RingPos& rp, Spin& sp,
+                                             unsigned long long* prof) {
+  extern __shared__ __align__(128) char smem[];
+  const PShared& S = *reinterpret_cast<const PShared*>(smem);
+  const uint32_t eq = epoch_of(seq, ph - 1);
+  const int G = a.Hq / a.Hkv;
+  bool first = true;
+  for (int it = blockIdx.x; it < S.item0[kPMaxBatch]; it += gridDim.x) {
+    const AttnItem t = attn_item_of(S, a.Hkv, it);
+    const int np = cached_positions(a, t.b, S.pos[t.b]);
+    const int p0 = (int)(((long long)t.sp * np) / t.ns);
+    const int p1 = (int)(((long long)(t.sp + 1) * np) / t.ns);
+    unsigned long long* const pin = first && prof ? prof + 2 * ph + 1 : nullptr;
+    unsigned long long* const psub =
+        pin ? prof + 2 * (kPhasesPerLayer * a.L + 1) + 2 + kProfAttnMarks * layer : nullptr;
+    if (G <= 2)
+      attention_item<D, KV16, 2>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp, sp, pin,
+                                 psub);
+    else if (G <= 4)
+      attention_item<D, KV16, 4>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp, sp, pin,
+                                 psub);
+    else  // D = 128 never gets here
+      attention_item<D, KV16, D == 128 ? 4 : 8>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep,
+                                                 nslots, rp, sp, pin, psub);
+    first = false;
+  }
+  if (prof && first) prof[2 * ph + 1] = global_timer();  // a CTA with no item
+}
+
 template <int BT, int D, bool KV16>
 __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid_constant__ PersistArgs a) {
   extern __shared__ __align__(128) char smem[];
@@ -1402,7 +1463,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
   Spin sp{global_timer() + a.timeout_ns, &S.abort, a.status};
   const int nph_all = kPhasesPerLayer * a.L + 1;
   unsigned long long* const prof_cta =
-      a.prof ? a.prof + (size_t)blockIdx.x * (2 * nph_all + 2) : nullptr;
+      a.prof ? a.prof + (size_t)blockIdx.x * prof_values(a.L) : nullptr;
   if (prof_cta && threadIdx.x == 0) prof_cta[2 * nph_all] = global_timer();
 
   if (warp == 0) {
@@ -1434,27 +1495,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
       const int kind = ph == kPhasesPerLayer * L ? kHEAD : ph % kPhasesPerLayer;
       const uint32_t ep = epoch_of(seq, ph);
       if (kind == kATTN) {
-        bool first = true;
-        for (int it = blockIdx.x; it < S.item0[kPMaxBatch]; it += gridDim.x) {
-          const AttnItem t = attn_item_of(S, a.Hkv, it);
-          const int np = cached_positions(a, t.b, S.pos[t.b]);
-          const int p0 = (int)(((long long)t.sp * np) / t.ns);
-          const int p1 = (int)(((long long)(t.sp + 1) * np) / t.ns);
-          unsigned long long* const pin = first && prof ? prof + 2 * ph + 1 : nullptr;
-          const uint32_t eq = epoch_of(seq, ph - 1);
-          const int G = a.Hq / a.Hkv;
-          if (G <= 2)
-            attention_item<D, KV16, 2>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp,
-                                       sp, pin);
-          else if (G <= 4)
-            attention_item<D, KV16, 4>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp,
-                                       sp, pin);
-          else
-            attention_item<D, KV16, 8>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp,
-                                       sp, pin);
-          first = false;
-        }
-        if (prof && first) prof[2 * ph + 1] = global_timer();  // a CTA with no item
+        attention_phase<D, KV16>(a, ph, layer, seq, ep, nslots, rp, sp, prof);
         continue;
       }
       gemv_phase<BT>(a, ph, seq, rp, kb, best, prof, sp);
@@ -1633,6 +1674,7 @@ bool persistent_supported(int L, int H, int qd, int F, int D, int G, int B) {
   if (B < 1 || B > kPMaxBatch || (D != 64 && D != 128)) return false;
   if (L < 1 || L > kPMaxLayers) return false;
   if (G < 1 || G > 8 || G * (D / 2) > kPConsumerThreads) return false;
+  if (D == 128 && G > 4) return false;  // the scan instances (attention_phase)
   if (H % 8 || qd % 8 || F % 8) return false;
   if (G + 2 > kPConsumerWarps) return false;  // one gathering warp per q head, k and v
   if (qd / D > kPMaxHeads) return false;

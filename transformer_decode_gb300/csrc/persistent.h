@@ -50,14 +50,25 @@ struct PersistArgs {
   int* status;
   unsigned long long timeout_ns;  // bound of every wait
   int grid;                       // CTAs (one per SM)
-  // Optional phase profile (null: off), [grid][2 * nph + 2]: each CTA records
-  // %globaltimer at the start of every phase (2*ph) and when its input is in
-  // (2*ph + 1); then its own start (2*nph) and end (2*nph + 1; for the CTA
-  // that finishes the step, the end of the step).
+  // Optional phase profile (null: off), [grid][prof_values(L)]: each CTA
+  // records %globaltimer at the start of every phase (2*ph) and when its
+  // input is in (2*ph + 1); then its own start (2*nph) and end (2*nph + 1;
+  // for the CTA that finishes the step, the end of the step); then per layer
+  // kProfAttnMarks marks of its first attention item (2*nph + 2 +
+  // kProfAttnMarks*layer + k): the scan's states combined (k = 0), its
+  // output or partials published (k = 1), the merge done (k = 2; 0 unless
+  // this CTA merged), scan warp 0's first and last K/V chunk in shared
+  // memory (k = 3, 4) and its scan done (k = 5).
   unsigned long long* prof;
   // shared-memory plan (filled by launch_persistent)
   int slot_bytes, nslots, ring_offset, xs_offset, attn_offset, attn_bytes;
 };
+
+// Values per CTA in the phase profile of an L-layer step.
+constexpr int kProfAttnMarks = 8;
+__host__ __device__ inline size_t prof_values(int L) {
+  return 2 * (5 * (size_t)L + 1) + 2 + kProfAttnMarks * (size_t)L;
+}
 
 // True when the persistent kernel fits this shape (shared memory, batch,
 // head_dim, GQA group).

@@ -549,17 +549,22 @@ class Model:
     def read_phase_profile(self, stream=None):
         """Last persistent step's phase timestamps (ns), one row per CTA: a
         dict of int64 tensors 'start' [ncta, 5L+1], 'input' [ncta, 5L+1]
-        (input arrived), 'cta_start' [ncta], 'cta_end' [ncta]."""
+        (input arrived), 'cta_start' [ncta], 'cta_end' [ncta], and
+        'attn' [ncta, L, 8]: per layer, for the CTA's first attention item,
+        the scan combined, the output or partials published, the merge done
+        (0 where the CTA did not merge), scan warp 0's first and last K/V
+        chunk in, its scan done, one unused slot."""
         L = self.shape.n_layers
         nph = 5 * L + 1
+        per = 2 * nph + 2 + 8 * L
         ncta = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-        cap = ncta * (2 * nph + 2)
+        cap = ncta * per
         buf = (C.c_ulonglong * cap)()
         n = C.c_int()
         _check(load().nc_read_phase_profile(self.handle, _stream(stream), buf, cap, C.byref(n)))
-        v = torch.tensor(list(buf)[:n.value], dtype=torch.int64).view(-1, 2 * nph + 2)
+        v = torch.tensor(list(buf)[:n.value], dtype=torch.int64).view(-1, per)
         return {"start": v[:, 0:2 * nph:2], "input": v[:, 1:2 * nph:2], "cta_start": v[:, 2 * nph],
-                "cta_end": v[:, 2 * nph + 1]}
+                "cta_end": v[:, 2 * nph + 1], "attn": v[:, 2 * nph + 2:].reshape(-1, L, 8)}
 
     def device_status(self, stream=None):
         code = C.c_int()
