@@ -409,7 +409,7 @@ def run_nc(args, ws, rank, local):
     run_steps(args.warmup)
     torch.cuda.synchronize()
     if args.phase_profile:
-        print_phase_profile(model, shape, run_steps, model.decode_path(B, kv))
+        print_phase_profile(model, shape, run_steps, model.decode_path(B, kv), args.phase_dump)
 
     sampler = ClockSampler(local)
     if rank == 0:
@@ -876,7 +876,7 @@ def run_workload(args, ws, rank, local, name):
     torch.cuda.synchronize()
     path = model.decode_path(B, kv)
     if args.phase_profile:
-        print_phase_profile(model, shape, run_steps, path)
+        print_phase_profile(model, shape, run_steps, path, args.phase_dump)
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
@@ -1091,7 +1091,7 @@ def run_prefill(args, ws, rank, local, name):
         }), flush=True)
 
 
-def print_phase_profile(model, shape, run_steps, path):
+def print_phase_profile(model, shape, run_steps, path, dump=None):
     """Critical-path timeline of the persistent kernel (nc_profile_phases) over
     a few steps, printed to stderr. For phase p: `handover` = the last CTA's
     input arrival minus the moment the last CTA finished phase p - 1 (the
@@ -1110,9 +1110,11 @@ def print_phase_profile(model, shape, run_steps, path):
                            "first chunk wait (max)", "last chunk wait (max)")}
     totals = []
     model.profile_phases(True)
+    raw = []
     for it in range(4):
         run_steps(1, it)
         rec = model.read_phase_profile()
+        raw.append({k: v.numpy() for k, v in rec.items()})
         start = rec["start"].numpy().astype(np.int64)
         inp = rec["input"].numpy().astype(np.int64)
         c0 = rec["cta_start"].numpy().astype(np.int64)
@@ -1145,6 +1147,8 @@ def print_phase_profile(model, shape, run_steps, path):
                     sub["first chunk wait (max)"].append((at[done, 3] - inp[done, p]).max() / 1e3)
                     sub["last chunk wait (max)"].append((at[done, 4] - inp[done, p]).max() / 1e3)
     model.profile_phases(False)
+    if dump:
+        np.savez_compressed(dump, **{f"{k}_{i}": v for i, r in enumerate(raw) for k, v in r.items()})
     print(f"phase profile ({len(totals)} steps, median step {statistics.median(totals):.1f} us):",
           file=sys.stderr)
     print(f"{'phase':10s} {'handover us':>12s} {'work us':>9s}", file=sys.stderr)
@@ -1171,6 +1175,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload's model (a small "
                          "case for profiler captures; not a metric line)")
+    ap.add_argument("--phase-dump", default=None,
+                    help="with --phase-profile: also save the raw per-CTA records (.npz)")
     ap.add_argument("--phase-profile", action="store_true",
                     help="print the persistent kernel's per-phase critical path (stderr)")
     args = ap.parse_args()

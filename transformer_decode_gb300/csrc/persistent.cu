@@ -734,8 +734,8 @@ __device__ __forceinline__ void kv_smemE(const char* base, int idx, float (&o)[E
   }
 }
 
-// Consumer: one item, i.e. split `split` of the ns splits of (sequence b, kv
-// head g). RoPE (+ q/k norm) of the G query heads and the key; split 0
+// One attention item is split `split` of the ns splits of (sequence b, kv
+// head g): RoPE (+ q/k norm) of the G query heads and the key; split 0
 // appends K/V at slot pos and opens the online-softmax state with the new
 // position; then the scan over the split's cached positions [p0, p1), in
 // chunks from the ring. An unsplit scan writes its output o = acc / l as the
@@ -744,41 +744,38 @@ __device__ __forceinline__ void kv_smemE(const char* base, int idx, float (&o)[E
 // of them (Tang section 2.2: per head M = max_s m_s, weights
 // w_s = exp(m_s - M) l_s, out = sum_s (w_s / sum_t w_t) o_s; one split gives
 // weight l / l = 1 and out = o exactly) and writes the output words.
-template <int D, bool KV16, int GP>
-__device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int split, int ns,
-                                            int p0, int p1, int layer, uint32_t ep_qkv,
-                                            uint32_t ep_out, int nslots, RingPos& rp, Spin& sp,
-                                            unsigned long long* prof_in,
-                                            unsigned long long* prof_sub) {
+//
+// The attention scratch: qs [GM][D] (the query heads; after the scan the
+// normalised outputs), kn [D], vn [D], then sc: the scan's score buffers or
+// per-warp states, the merge's (m, l) and weights, and from sc + kAttnFin the
+// heads' final (m, l).
+constexpr int kAttnFin = 2 * 8 * kAttnMaxChunk;
+
+// The item's inputs: warp w < G gathers query head w, warp G the key, warp
+// G + 1 the value; lane l holds dims l + 32 j, so a RoPE pair (i, i + D/2)
+// sits in one lane: the q/k norm and the rotation run in registers (angles
+// from the per-step table), then K and V go to the cache straight from the
+// owning warps. Returns whether this item owns the new position.
+template <int D, bool KV16>
+__device__ __forceinline__ bool attn_inputs(const PersistArgs& a, int b, int g, int split,
+                                            int layer, uint32_t ep_qkv, Spin& sp) {
   // shared-memory pointers are derived from the dynamic shared array here, so
   // the compiler addresses them as shared, not generic
   extern __shared__ __align__(128) char smem[];
   PShared& S = *reinterpret_cast<PShared*>(smem);
   float* scratch = reinterpret_cast<float*>(smem + a.attn_offset);
-  char* ring = smem + a.ring_offset;
-  const int slot_bytes = a.slot_bytes;
-  constexpr int GM = 8, ES = KV16 ? 2 : 4, E = D / 32;
+  constexpr int GM = 8, E = D / 32;
   const int ct = threadIdx.x - kWarp, warp = ct / kWarp, lane = ct % kWarp;
-  // the arguments this item uses, as locals: `a` sits behind a generic
-  // reference, and every store through the shared-memory pointers below
-  // would otherwise make the compiler read its fields again
   const KVView kv = a.kv;
   const int Hq = a.Hq, Hkv = a.Hkv;
   const float eps = a.eps;
   int* const status = a.status;
   const int G = Hq / Hkv;
-  const int CP = attn_chunk(slot_bytes, D, ES);
   const int pos = S.pos[b];
-  float* qs = scratch;                        // [GM][D]
-  float* kn = qs + GM * D;                    // [D]
-  float* vn = kn + D;                         // [D]
-  float* sc = vn + D;                         // the scan warps' (m, l), then the merge's
+  float* qs = scratch;
+  float* kn = qs + GM * D;
+  float* vn = kn + D;
   const PLayer& P = S.layers[layer];
-
-  // Warp w < G gathers query head w, warp G the key, warp G + 1 the value;
-  // lane l holds dims l + 32 j, so a RoPE pair (i, i + D/2) sits in one lane:
-  // the q/k norm and the rotation run in registers (angles from the per-step
-  // table), then K and V go to the cache straight from the owning warps.
   const bool pos_ok = kv.slot_ok(b, pos);
   const bool own_new = pos_ok && split == 0;  // the new position belongs to split 0
   if (!pos_ok && split == 0 && ct == 0 && status) atomicCAS(status, 0, (int)NC_ERR_POSITION);
@@ -832,14 +829,169 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     }
   }
   consumer_sync();
+  return own_new;
+}
+
+// The item's end: the normalised outputs ofin [G][D] and the heads' (m, l)
+// are in shared memory (behind a barrier). An unsplit item writes the output
+// words; a split publishes its partials, takes the ticket, and the last
+// split merges.
+template <int D>
+__device__ __forceinline__ void attn_finish(const PersistArgs& a, int b, int g, int split, int ns,
+                                            int layer, uint32_t ep_out,
+                                            unsigned long long* prof_sub) {
+  // shared-memory pointers are derived from the dynamic shared array here, so
+  // the compiler addresses them as shared, not generic
+  extern __shared__ __align__(128) char smem[];
+  PShared& S = *reinterpret_cast<PShared*>(smem);
+  float* scratch = reinterpret_cast<float*>(smem + a.attn_offset);
+  constexpr int GM = 8;
+  const int ct = threadIdx.x - kWarp, warp = ct / kWarp, lane = ct % kWarp;
+  const int Hq = a.Hq, Hkv = a.Hkv;
+  const int G = Hq / Hkv;
+  const float* ofin = scratch;      // [G][D]
+  float* sc = scratch + (GM + 2) * D;
+  const float* mfin = sc + kAttnFin;  // [G]
+  const float* lfin = mfin + GM;      // [G]
+  if (prof_sub && ct == 0) {
+    prof_sub[0] = global_timer();
+    prof_sub[2] = 0ull;
+  }
+  uint64_t* const aout = a.aw + (size_t)b * Hq * D + (size_t)g * G * D;  // [G][D] words
+  // split partials [G][DP] per head of this (b, g, split): o[D], then m, l
+  // (rows padded to a 16-byte multiple, so the merge can stage them with
+  // 16-byte asynchronous copies)
+  constexpr int DP = D + 4;
+  float* const parts = a.apart + ((size_t)b * kPMaxSplits * Hq + (size_t)g * G) * DP;
+  const size_t sstride = (size_t)Hq * DP;  // from one split's partials to the next
+  float* const mine = parts + split * sstride;
+  for (int i = ct; i < G * D; i += kPConsumerThreads) {
+    const int h = i / D, d = i % D;
+    if (ns == 1) {
+      st_word(aout + i, ofin[i], ep_out);
+    } else {
+      mine[h * DP + d] = ofin[i];
+      if (d == 0) *reinterpret_cast<float2*>(mine + h * DP + D) = make_float2(mfin[h], lfin[h]);
+    }
+  }
+  if (ns == 1) {
+    consumer_sync();  // the scratch is reused by the next item
+    if (prof_sub && ct == 0) prof_sub[1] = global_timer();
+    return;
+  }
+  // The ticket. The barrier orders every thread's partials before thread
+  // 0's fence, which publishes them GPU-wide (cumulatively) before its
+  // arrival; the split that arrives last fences again before the barrier
+  // that lets its threads read the others' partials.
+  consumer_sync();
+  unsigned int* const tick = a.atick + ((size_t)layer * kPMaxBatch + b) * Hkv + g;
+  if (ct == 0) {
+    __threadfence();
+    const bool last = atomicAdd(tick, 1u) == (unsigned)(ns - 1);
+    if (last) __threadfence();
+    S.merge = last;
+  }
+  consumer_sync();
+  if (prof_sub && ct == 0) prof_sub[1] = global_timer();
+  if (!S.merge) return;  // uniform: read after the barrier
+  // The splits' outputs are staged into the (idle) input-vector region in
+  // rounds of as many splits as it holds. The first round's copies are in
+  // flight while the (m, l) of every (split, head) are loaded (one load
+  // each); then warp h forms head h's merge weights, lane t that of split t:
+  // M = max_t m_t, w_t = e^(m_t - M) l_t, coef_t = w_t / sum w (a division,
+  // not a reciprocal, as in the single-split case). Every thread accumulates
+  // its elements over the splits in index order.
+  float* ml = sc;                          // [ns][G][2]
+  float* coef = sc + 2 * kPMaxSplits * GM;  // [G][kPMaxSplits] merge weights
+  float* stage = reinterpret_cast<float*>(smem + a.xs_offset);
+  const int per_split = G * DP;  // floats of one split's block
+  const int span = (a.attn_offset - a.xs_offset) / (per_split * 4);
+  const auto stage_round = [&](int t0) {
+    const int chunks = min(span, ns - t0) * (per_split / 4);
+    for (int c = ct; c < chunks; c += kPConsumerThreads) {
+      const int t = c / (per_split / 4), r = c % (per_split / 4);
+      cp_async16(stage + t * per_split + 4 * r, parts + (t0 + t) * sstride + 4 * r);
+    }
+    cp_async_commit();
+  };
+  stage_round(0);
+  if (ct < ns * G) {
+    const int t = ct / G, h = ct % G;
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(parts + t * sstride + h * DP + D));
+    ml[2 * ct] = v.x;
+    ml[2 * ct + 1] = v.y;
+  }
+  consumer_sync();
+  if (warp < G) {
+    const float m = lane < ns ? ml[2 * (lane * G + warp)] : -INFINITY;
+    const float l = lane < ns ? ml[2 * (lane * G + warp) + 1] : 0.f;
+    const float M = warp_max(m);
+    const float w = m == -INFINITY ? 0.f : expf(m - M) * l;
+    const float L = warp_sum(w);
+    if (lane < ns) coef[warp * kPMaxSplits + lane] = L > 0.f ? w / L : 0.f;
+  }
+  constexpr int EPT = (8 * 128 + kPConsumerThreads - 1) / kPConsumerThreads;  // outputs a thread owns
+  float o[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) o[e] = 0.f;
+  for (int t0 = 0; t0 < ns; t0 += span) {
+    const int nt = min(span, ns - t0);
+    if (t0 > 0) stage_round(t0);
+    cp_async_wait_all();
+    consumer_sync();  // staged (and, in the first round, coef written)
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int i = ct + e * kPConsumerThreads;
+      if (i < G * D) {
+        const int h = i / D, d = i % D;
+        for (int t = 0; t < nt; ++t)
+          o[e] = fmaf(coef[h * kPMaxSplits + t0 + t], stage[t * per_split + h * DP + d], o[e]);
+      }
+    }
+    consumer_sync();  // the staging area is rewritten by the next round
+  }
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int i = ct + e * kPConsumerThreads;
+    if (i < G * D) st_word(aout + i, o[e], ep_out);
+  }
+  if (prof_sub && ct == 0) prof_sub[2] = global_timer();
+}
+
+
+// Scan with per-warp states (head size 128). Warps 0 .. SW - 1 each keep
+// their own online-softmax state of every query head over the positions
+// they take, with no block barrier inside a chunk: lane l holds dims
+// l E .. l E + E - 1 of each head in registers; a group of PG = 32 / GP
+// positions (GP = G rounded up to a power of two) gives 32 partial dot
+// products per lane, which one reduce-scatter turns into lane i's score of
+// (position i / GP, head i % GP). The warps' states are combined once, after
+// the scan.
+template <int D, bool KV16, int GP>
+__device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, int split, int ns,
+                                            int p0, int p1, int layer, uint32_t ep_qkv,
+                                            uint32_t ep_out, int nslots, RingPos& rp, Spin& sp,
+                                            unsigned long long* prof_in,
+                                            unsigned long long* prof_sub) {
+  const bool own_new = attn_inputs<D, KV16>(a, b, g, split, layer, ep_qkv, sp);
   if (prof_in) *prof_in = global_timer();  // the phase input (q, k, v) is in
-  // The scan. Warps 0 .. SW - 1 each keep their own online-softmax state of
-  // every query head over the positions they take, with no block barrier
-  // inside a chunk: lane l holds dims l E .. l E + E - 1 of each head in
-  // registers; a group of PG = 32 / GP positions (GP = G rounded up to a
-  // power of two) gives 32 partial dot products per lane, which one
-  // reduce-scatter turns into lane i's score of (position i / GP, head
-  // i % GP). The warps' states are combined once, after the scan.
+  // shared-memory pointers are derived from the dynamic shared array here, so
+  // the compiler addresses them as shared, not generic
+  extern __shared__ __align__(128) char smem[];
+  PShared& S = *reinterpret_cast<PShared*>(smem);
+  float* scratch = reinterpret_cast<float*>(smem + a.attn_offset);
+  constexpr int GM = 8, E = D / 32;
+  const int ct = threadIdx.x - kWarp, warp = ct / kWarp, lane = ct % kWarp;
+  char* ring = smem + a.ring_offset;
+  const int slot_bytes = a.slot_bytes;
+  constexpr int ES = KV16 ? 2 : 4;
+  const KVView kv = a.kv;
+  const int G = a.Hq / a.Hkv;
+  const int CP = attn_chunk(slot_bytes, D, ES);
+  float* qs = scratch;
+  float* kn = qs + GM * D;
+  float* vn = kn + D;
+  float* sc = vn + D;
   constexpr int SW = 8;           // scan warps
   constexpr int PG = kWarp / GP;  // positions per group
   const float scale = 1.f / sqrtf((float)D);
@@ -961,18 +1113,10 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
       }
   }
   consumer_sync();
-  if (prof_sub && ct == 0) {
-    prof_sub[0] = global_timer();
-    prof_sub[2] = 0ull;
-  }
-  uint64_t* const aout = a.aw + (size_t)b * Hq * D + (size_t)g * G * D;  // [G][D] words
-  // split partials [G][DP] per head of this (b, g, split): o[D], then m, l
-  // (rows padded to a 16-byte multiple, so the merge can stage them with
-  // 16-byte asynchronous copies)
-  constexpr int DP = D + 4;
-  float* const parts = a.apart + ((size_t)b * kPMaxSplits * Hq + (size_t)g * G) * DP;
-  const size_t sstride = (size_t)Hq * DP;  // from one split's partials to the next
-  float* const mine = parts + split * sstride;
+  // the heads' combined states: normalised outputs to qs (idle after the
+  // scan), (M, L) after the merge's buffers
+  float* mfin = sc + kAttnFin;
+  float* lfin = mfin + GM;
   for (int i = ct; i < G * D; i += kPConsumerThreads) {
     const int h = i / D, d = i % D;
     float M = -INFINITY;
@@ -986,96 +1130,172 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
       L = fmaf(c, mlw[(w * GM + h) * 2 + 1], L);
       O = fmaf(c, cmb[(w * G + h) * D + d], O);
     }
-    const float o = L > 0.f ? O / L : 0.f;
-    if (ns == 1) {
-      st_word(aout + i, o, ep_out);
-    } else {
-      mine[h * DP + d] = o;
-      if (d == 0) *reinterpret_cast<float2*>(mine + h * DP + D) = make_float2(M, L);
+    qs[i] = L > 0.f ? O / L : 0.f;
+    if (d == 0) {
+      mfin[h] = M;
+      lfin[h] = L;
     }
   }
-  if (ns == 1) {
-    consumer_sync();  // the scratch is reused by the next item
-    if (prof_sub && ct == 0) prof_sub[1] = global_timer();
-    return;
-  }
-  // The ticket. The barrier orders every thread's partials before thread
-  // 0's fence, which publishes them GPU-wide (cumulatively) before its
-  // arrival; the split that arrives last fences again before the barrier
-  // that lets its threads read the others' partials.
   consumer_sync();
-  unsigned int* const tick = a.atick + ((size_t)layer * kPMaxBatch + b) * Hkv + g;
-  if (ct == 0) {
-    __threadfence();
-    const bool last = atomicAdd(tick, 1u) == (unsigned)(ns - 1);
-    if (last) __threadfence();
-    S.merge = last;
-  }
-  consumer_sync();
-  if (prof_sub && ct == 0) prof_sub[1] = global_timer();
-  if (!S.merge) return;  // uniform: read after the barrier
-  // The splits' outputs are staged into the (idle) input-vector region in
-  // rounds of as many splits as it holds. The first round's copies are in
-  // flight while the (m, l) of every (split, head) are loaded (one load
-  // each); then warp h forms head h's merge weights, lane t that of split t:
-  // M = max_t m_t, w_t = e^(m_t - M) l_t, coef_t = w_t / sum w (a division,
-  // not a reciprocal, as in the single-split case). Every thread accumulates
-  // its elements over the splits in index order.
-  float* ml = sc;                          // [ns][G][2]
-  float* coef = sc + 2 * kPMaxSplits * GM;  // [G][kPMaxSplits] merge weights
-  float* stage = reinterpret_cast<float*>(smem + a.xs_offset);
-  const int per_split = G * DP;  // floats of one split's block
-  const int span = (a.attn_offset - a.xs_offset) / (per_split * 4);
-  const auto stage_round = [&](int t0) {
-    const int chunks = min(span, ns - t0) * (per_split / 4);
-    for (int c = ct; c < chunks; c += kPConsumerThreads) {
-      const int t = c / (per_split / 4), r = c % (per_split / 4);
-      cp_async16(stage + t * per_split + 4 * r, parts + (t0 + t) * sstride + 4 * r);
+  attn_finish<D>(a, b, g, split, ns, layer, ep_out, prof_sub);
+}
+
+// Scan with block-wide steps (head size 64, short rows and up to 8 heads a
+// group, where every (head, dim pair) has a thread of its own): per chunk the
+// warps compute the scores of (head, 32 positions) blocks, one warp per head
+// updates that head's running (m, l) and turns the scores into weights, and
+// thread (h, d pair) accumulates its two output dims over the chunk.
+template <int D, bool KV16>
+__device__ __noinline__ void attention_item_block(const PersistArgs& a, int b, int g, int split,
+                                                  int ns, int p0, int p1, int layer,
+                                                  uint32_t ep_qkv, uint32_t ep_out, int nslots,
+                                                  RingPos& rp, Spin& sp,
+                                                  unsigned long long* prof_in,
+                                                  unsigned long long* prof_sub) {
+  const bool own_new = attn_inputs<D, KV16>(a, b, g, split, layer, ep_qkv, sp);
+  if (prof_in) *prof_in = global_timer();  // the phase input (q, k, v) is in
+  extern __shared__ __align__(128) char smem[];
+  PShared& S = *reinterpret_cast<PShared*>(smem);
+  float* scratch = reinterpret_cast<float*>(smem + a.attn_offset);
+  constexpr int GM = 8, E = D / 32, ES = KV16 ? 2 : 4;
+  const int ct = threadIdx.x - kWarp, warp = ct / kWarp, lane = ct % kWarp;
+  char* ring = smem + a.ring_offset;
+  const int slot_bytes = a.slot_bytes;
+  const KVView kv = a.kv;
+  const int G = a.Hq / a.Hkv;
+  const int CP = attn_chunk(slot_bytes, D, ES);
+  float* qs = scratch;
+  float* kn = qs + GM * D;
+  float* vn = kn + D;
+  float* sc = vn + D;                 // [2][GM][kAttnMaxChunk] scores, by chunk parity
+  float* mrun = sc + kAttnFin;        // [GM] running max (the final m)
+  float* lrun = mrun + GM;            // [GM] running sum (the final l)
+  float* resc = lrun + GM;            // [GM] rescale of the chunk
+  unsigned long long* const mark = prof_sub && ct == 0 ? prof_sub : nullptr;
+  // the new position opens the running state: m = its score, l = 1, acc = v
+  const float scale = 1.f / sqrtf((float)D);
+  for (int h = warp; h < G; h += kPConsumerWarps) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < E; ++j) s = fmaf(qs[h * D + lane + 32 * j], kn[lane + 32 * j], s);
+    s = warp_sum(s) * scale;
+    if (lane == 0) {
+      mrun[h] = own_new ? s : -INFINITY;
+      lrun[h] = own_new ? 1.f : 0.f;
     }
-    cp_async_commit();
-  };
-  stage_round(0);
-  if (ct < ns * G) {
-    const int t = ct / G, h = ct % G;
-    const float2 v = __ldcg(reinterpret_cast<const float2*>(parts + t * sstride + h * DP + D));
-    ml[2 * ct] = v.x;
-    ml[2 * ct + 1] = v.y;
+  }
+  const int npair = G * (D / 2);
+  const int my_h = ct / (D / 2), my_d2 = ct % (D / 2);
+  float acc0 = 0.f, acc1 = 0.f;
+  if (ct < npair && own_new) {
+    acc0 = vn[2 * my_d2];
+    acc1 = vn[2 * my_d2 + 1];
   }
   consumer_sync();
-  if (warp < G) {
-    const float m = lane < ns ? ml[2 * (lane * G + warp)] : -INFINITY;
-    const float l = lane < ns ? ml[2 * (lane * G + warp) + 1] : 0.f;
-    const float M = warp_max(m);
-    const float w = m == -INFINITY ? 0.f : expf(m - M) * l;
-    const float L = warp_sum(w);
-    if (lane < ns) coef[warp * kPMaxSplits + lane] = L > 0.f ? w / L : 0.f;
-  }
-  constexpr int EPT = (8 * 128 + kPConsumerThreads - 1) / kPConsumerThreads;  // outputs a thread owns
-  float o[EPT];
+  int cpar = 0;
+  for (int t0 = p0; t0 < p1; t0 += CP, cpar ^= 1) {
+    const int n = min(CP, p1 - t0);
+    const int s = rp.s;
+    ring_wait(&S.full[s], rp.par, sp);
+    const char* Ks = ring + (size_t)s * slot_bytes;
+    const char* Vs = Ks + (size_t)CP * D * ES;
+    float* scc = sc + cpar * GM * kAttnMaxChunk;  // the other buffer may still be read
+    // scores: warp -> (head, 32 positions); lane l reads its row from column
+    // (d + l) mod D so the 32 rows of a warp fall in different banks
+    const int blocks = (n + 31) / 32;
+    for (int wb = warp; wb < G * blocks; wb += kPConsumerWarps) {
+      const int h = wb % G, p = (wb / G) * 32 + lane;
+      if (p < n) {
+        float sv = -INFINITY;
+        if (kv.slot_ok(b, t0 + p)) {
+          // 4-element columns, skewed by lane: the 8 lanes of each 16-byte
+          // load phase read 8 different bank groups
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+          const float* qh = qs + h * D;
 #pragma unroll
-  for (int e = 0; e < EPT; ++e) o[e] = 0.f;
-  for (int t0 = 0; t0 < ns; t0 += span) {
-    const int nt = min(span, ns - t0);
-    if (t0 > 0) stage_round(t0);
-    cp_async_wait_all();
-    consumer_sync();  // staged (and, in the first round, coef written)
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      const int i = ct + e * kPConsumerThreads;
-      if (i < G * D) {
-        const int h = i / D, d = i % D;
-        for (int t = 0; t < nt; ++t)
-          o[e] = fmaf(coef[h * kPMaxSplits + t0 + t], stage[t * per_split + h * DP + d], o[e]);
+          for (int j = 0; j < D / 4; ++j) {
+            const int c = ((j + lane) & (D / 4 - 1)) * 4;
+            const float4 q4 = *reinterpret_cast<const float4*>(qh + c);
+            float k4[4];
+            kv_smem4<KV16>(Ks, p * D + c, k4);
+            s4[0] = fmaf(q4.x, k4[0], s4[0]);
+            s4[1] = fmaf(q4.y, k4[1], s4[1]);
+            s4[2] = fmaf(q4.z, k4[2], s4[2]);
+            s4[3] = fmaf(q4.w, k4[3], s4[3]);
+          }
+          sv = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * scale;
+        }
+        scc[h * kAttnMaxChunk + p] = sv;
       }
     }
-    consumer_sync();  // the staging area is rewritten by the next round
+    consumer_sync();
+    for (int h = warp; h < G; h += kPConsumerWarps) {
+      float m = -INFINITY;
+      for (int t = lane; t < n; t += kWarp) m = fmaxf(m, scc[h * kAttnMaxChunk + t]);
+      m = warp_max(m);
+      const float m_new = fmaxf(mrun[h], m);
+      float l = 0.f;
+      for (int t = lane; t < n; t += kWarp) {
+        const float x = scc[h * kAttnMaxChunk + t];
+        const float p = x == -INFINITY ? 0.f : expf(x - m_new);
+        scc[h * kAttnMaxChunk + t] = p;
+        l += p;
+      }
+      l = warp_sum(l);
+      if (lane == 0) {
+        const float r = mrun[h] == -INFINITY ? 0.f : expf(mrun[h] - m_new);
+        resc[h] = r;
+        lrun[h] = lrun[h] * r + l;
+        mrun[h] = m_new;
+      }
+    }
+    consumer_sync();
+    if (ct < npair) {
+      const float r = resc[my_h];
+      // two interleaved chains per output; a masked position (p = 0) may sit
+      // over stale shared memory, so its value is replaced, not multiplied
+      float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;
+      const float* ph = scc + my_h * kAttnMaxChunk;
+      int t = 0;
+#pragma unroll 4
+      for (; t + 1 < n; t += 2) {
+        const float pa = ph[t], pb = ph[t + 1];
+        const float2 va = kv_smem2<KV16>(Vs, t * D + 2 * my_d2);
+        const float2 vb = kv_smem2<KV16>(Vs, (t + 1) * D + 2 * my_d2);
+        e0 = fmaf(pa, pa == 0.f ? 0.f : va.x, e0);
+        e1 = fmaf(pa, pa == 0.f ? 0.f : va.y, e1);
+        o0 = fmaf(pb, pb == 0.f ? 0.f : vb.x, o0);
+        o1 = fmaf(pb, pb == 0.f ? 0.f : vb.y, o1);
+      }
+      if (t < n) {
+        const float pa = ph[t];
+        const float2 va = kv_smem2<KV16>(Vs, t * D + 2 * my_d2);
+        e0 = fmaf(pa, pa == 0.f ? 0.f : va.x, e0);
+        e1 = fmaf(pa, pa == 0.f ? 0.f : va.y, e1);
+      }
+      acc0 = fmaf(acc0, r, e0 + o0);
+      acc1 = fmaf(acc1, r, e1 + o1);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+    rp.next(nslots);
+    // no barrier here: the next chunk writes the other score buffer, and the
+    // one after it is behind that chunk's two barriers
   }
-#pragma unroll
-  for (int e = 0; e < EPT; ++e) {
-    const int i = ct + e * kPConsumerThreads;
-    if (i < G * D) st_word(aout + i, o[e], ep_out);
+  if (mark) {
+    const unsigned long long now = global_timer();
+    mark[3] = mark[4] = now;  // the chunks' arrivals are not marked by this scan
+    mark[5] = now;
   }
-  if (prof_sub && ct == 0) prof_sub[2] = global_timer();
+  // normalised outputs to qs (no score step reads it any more: the last
+  // chunk's scores are behind two barriers)
+  if (ct < npair) {
+    const float inv = lrun[my_h] > 0.f ? 1.f / lrun[my_h] : 0.f;
+    qs[my_h * D + 2 * my_d2] = acc0 * inv;
+    qs[my_h * D + 2 * my_d2 + 1] = acc1 * inv;
+  }
+  consumer_sync();
+  attn_finish<D>(a, b, g, split, ns, layer, ep_out, prof_sub);
 }
 
 // The tiles of one projection phase (see gemv_phase). MODE 0: batch 1, rows of
@@ -1385,12 +1605,12 @@ __device__ __forceinline__ void gemv_phase(const PersistArgs& a, int ph, uint32_
 }
 
 // ------------------------------------------------------------------ the kernel
-// The attention phase of one CTA: its items, each scanned by the instance
-// for the group size rounded up to a power of two (at most 4 heads a group
-// with D = 128, whose 8-head instance's registers would crowd the
-// projection phases' code out of registers; persistent_supported keeps
-// such shapes on the stage path). A function of its own, so that the
-// kernel's loop keeps few values live across the call.
+// The attention phase of one CTA: its items. Head size 64 takes the
+// block-wide scan; head size 128 the per-warp scan, instantiated for the
+// group size rounded up to a power of two, at most 4 (an 8-head instance's
+// registers would crowd the projection phases' code out of registers;
+// persistent_supported keeps such shapes on the stage path). A function of
+// its own, so that the kernel's loop keeps few values live across the call.
 template <int D, bool KV16>
 __device__ __noinline__ void attention_phase(const PersistArgs& a, int ph, int layer, uint32_t seq,
                                              uint32_t ep, int nslots, RingPos& rp, Spin& sp,
@@ -1408,15 +1628,17 @@ __device__ __noinline__ void attention_phase(const PersistArgs& a, int ph, int l
     unsigned long long* const pin = first && prof ? prof + 2 * ph + 1 : nullptr;
     unsigned long long* const psub =
         pin ? prof + 2 * (kPhasesPerLayer * a.L + 1) + 2 + kProfAttnMarks * layer : nullptr;
-    if (G <= 2)
-      attention_item<D, KV16, 2>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp, sp, pin,
-                                 psub);
-    else if (G <= 4)
-      attention_item<D, KV16, 4>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp, sp, pin,
-                                 psub);
-    else  // D = 128 never gets here
-      attention_item<D, KV16, D == 128 ? 4 : 8>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep,
-                                                 nslots, rp, sp, pin, psub);
+    if constexpr (D == 64) {
+      attention_item_block<D, KV16>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp, sp,
+                                    pin, psub);
+    } else {
+      if (G <= 2)
+        attention_item<D, KV16, 2>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp, sp,
+                                   pin, psub);
+      else
+        attention_item<D, KV16, 4>(a, t.b, t.g, t.sp, t.ns, p0, p1, layer, eq, ep, nslots, rp, sp,
+                                   pin, psub);
+    }
     first = false;
   }
   if (prof && first) prof[2 * ph + 1] = global_timer();  // a CTA with no item
