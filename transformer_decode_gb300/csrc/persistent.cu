@@ -992,8 +992,8 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   float* kn = qs + GM * D;
   float* vn = kn + D;
   float* sc = vn + D;
-  constexpr int SW = 8;           // scan warps
-  constexpr int PG = kWarp / GP;  // positions per group
+  constexpr int SW = kPConsumerWarps;  // scan warps: all of them
+  constexpr int PG = kWarp / GP;       // positions per group
   const float scale = 1.f / sqrtf((float)D);
   float qr[GP][E], acc[GP][E], mh[GP], lh[GP];
 #pragma unroll
@@ -1024,6 +1024,10 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
   }
   const int hl = lane % GP, pl = lane / GP;  // what lane holds after the reduce
   unsigned long long* const mark = prof_sub && ct == 0 ? prof_sub : nullptr;
+  // Groups are numbered across the chunks and warp w takes the groups
+  // congruent to w modulo SW, so a chunk of fewer than SW groups leaves the
+  // other warps to the next chunk (the ring holds several) instead of idle.
+  int gbase = 0;  // groups of the earlier chunks
   for (int t0 = p0; t0 < p1; t0 += CP) {
     const int n = min(CP, p1 - t0);
     const int s = rp.s;
@@ -1031,8 +1035,8 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     if (mark) mark[t0 == p0 ? 3 : 4] = global_timer();
     const char* Ks = ring + (size_t)s * slot_bytes;
     const char* Vs = Ks + (size_t)CP * D * ES;
-    if (warp < SW) {
-      for (int g0 = warp * PG; g0 < n; g0 += SW * PG) {
+    {
+      for (int g0 = ((warp - gbase % SW + SW) % SW) * PG; g0 < n; g0 += SW * PG) {
         float part[kWarp];
 #pragma unroll
         for (int p = 0; p < PG; ++p) {
@@ -1089,6 +1093,7 @@ __device__ __noinline__ void attention_item(const PersistArgs& a, int b, int g, 
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[s]);
     rp.next(nslots);
+    gbase += (n + PG - 1) / PG;
   }
   if (mark) {
     const unsigned long long now = global_timer();
@@ -1827,9 +1832,9 @@ static int persist_slots() {
 // split's partial block (G heads of D + 4 floats), which the attention merge
 // stages there.
 static size_t xs_bytes(int H, int qd, int F, int D, int G, int BT) {
-  // also the attention scan's combine buffer [8 warps][G][D]
+  // also the attention scan's combine buffer [consumer warps][G][D]
   size_t v = (size_t)BT * kmax_of(H, qd, F) * 4;
-  const size_t p = (size_t)G * (D + 4) * 4, c = (size_t)8 * G * D * 4;
+  const size_t p = (size_t)G * (D + 4) * 4, c = (size_t)kPConsumerWarps * G * D * 4;
   if (p > v) v = p;
   return c > v ? c : v;
 }
