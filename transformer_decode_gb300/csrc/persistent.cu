@@ -138,6 +138,7 @@ __device__ __forceinline__ float ll_get(const uint64_t* p, uint32_t epoch, Spin&
 // One round costs one memory round trip however many words are stale (a
 // word-by-word re-poll would pay one per word). On expiry the stale words
 // read as 0.
+constexpr unsigned kPollPauseNs = 128;
 template <int N, class Addr>
 __device__ __forceinline__ void ll_settle(const Addr& addr, uint32_t valid, uint32_t epoch,
                                           uint64_t (&w)[N], Spin& sp) {
@@ -153,6 +154,10 @@ __device__ __forceinline__ void ll_settle(const Addr& addr, uint32_t valid, uint
         if (((valid >> u) & 1u) && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = 0;
       return;
     }
+    // a short pause before the next round: every consumer thread of every
+    // CTA polls at once, and back-to-back rounds crowd the L2 the weight
+    // stream goes through
+    __nanosleep(kPollPauseNs);
 #pragma unroll
     for (int u = 0; u < N; ++u)
       if (((valid >> u) & 1u) && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = ld_word(addr(u));
