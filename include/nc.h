@@ -268,7 +268,8 @@ nc_status nc_debug_w8a8_codes(nc_model* m, int8_t* codes_dev, size_t codes_capac
  * (or split partials and ticket) published, [+2] the merge of the splits
  * done (0 unless this CTA merged), [+3] and [+4] the first and the last K/V
  * chunk in shared memory (as the first scan warp saw them), [+5] that
- * warp's scan done, [+6], [+7] unused. *n receives the count; a smaller
+ * warp's scan done, [+6] and [+7] (head size 64, the block-wide scan) the
+ * first chunk's scores and weights done. *n receives the count; a smaller
  * capacity returns NC_ERR_CAPACITY. */
 nc_status nc_profile_phases(nc_model* m, int enable);
 nc_status nc_read_phase_profile(nc_model* m, void* stream, unsigned long long* out_host,

@@ -1207,6 +1207,7 @@ __device__ __noinline__ void attention_item_block(const PersistArgs& a, int b, i
     const int n = min(CP, p1 - t0);
     const int s = rp.s;
     ring_wait(&S.full[s], rp.par, sp);
+    if (mark) mark[t0 == p0 ? 3 : 4] = global_timer();
     const char* Ks = ring + (size_t)s * slot_bytes;
     const char* Vs = Ks + (size_t)CP * D * ES;
     float* scc = sc + cpar * GM * kAttnMaxChunk;  // the other buffer may still be read
@@ -1239,6 +1240,7 @@ __device__ __noinline__ void attention_item_block(const PersistArgs& a, int b, i
       }
     }
     consumer_sync();
+    if (mark && t0 == p0) mark[6] = global_timer();  // the first chunk's scores
     for (int h = warp; h < G; h += kPConsumerWarps) {
       float m = -INFINITY;
       for (int t = lane; t < n; t += kWarp) m = fmaxf(m, scc[h * kAttnMaxChunk + t]);
@@ -1260,6 +1262,7 @@ __device__ __noinline__ void attention_item_block(const PersistArgs& a, int b, i
       }
     }
     consumer_sync();
+    if (mark && t0 == p0) mark[7] = global_timer();  // ... and its weights
     if (ct < npair) {
       const float r = resc[my_h];
       // two interleaved chains per output; a masked position (p = 0) may sit
@@ -1294,7 +1297,8 @@ __device__ __noinline__ void attention_item_block(const PersistArgs& a, int b, i
   }
   if (mark) {
     const unsigned long long now = global_timer();
-    mark[3] = mark[4] = now;  // the chunks' arrivals are not marked by this scan
+    if (p1 <= p0) mark[3] = mark[6] = mark[7] = now;  // nothing to scan
+    if (p1 - p0 <= CP) mark[4] = mark[3];             // one chunk: the first is the last
     mark[5] = now;
   }
   // normalised outputs to qs (no score step reads it any more: the last

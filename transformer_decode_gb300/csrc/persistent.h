@@ -58,7 +58,8 @@ struct PersistArgs {
   // kProfAttnMarks*layer + k): the scan's states combined (k = 0), its
   // output or partials published (k = 1), the merge done (k = 2; 0 unless
   // this CTA merged), scan warp 0's first and last K/V chunk in shared
-  // memory (k = 3, 4) and its scan done (k = 5).
+  // memory (k = 3, 4), its scan done (k = 5), and for the block-wide scan
+  // the first chunk's scores and weights done (k = 6, 7).
   unsigned long long* prof;
   // shared-memory plan (filled by launch_persistent)
   int slot_bytes, nslots, ring_offset, xs_offset, attn_offset, attn_bytes;

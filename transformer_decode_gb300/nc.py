@@ -553,7 +553,8 @@ class Model:
         'attn' [ncta, L, 8]: per layer, for the CTA's first attention item,
         the scan combined, the output or partials published, the merge done
         (0 where the CTA did not merge), scan warp 0's first and last K/V
-        chunk in, its scan done, one unused slot."""
+        chunk in, its scan done, and (head size 64) the first chunk's scores
+        and weights done."""
         L = self.shape.n_layers
         nph = 5 * L + 1
         per = 2 * nph + 2 + 8 * L
