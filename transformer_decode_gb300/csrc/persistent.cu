@@ -154,10 +154,10 @@ __device__ __forceinline__ void ll_settle(const Addr& addr, uint32_t valid, uint
         if (((valid >> u) & 1u) && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = 0;
       return;
     }
-    // a short pause before the next round: every consumer thread of every
-    // CTA polls at once, and back-to-back rounds crowd the L2 the weight
-    // stream goes through
-    __nanosleep(kPollPauseNs);
+    // a short pause before the next round, longer once the wait is long:
+    // every consumer thread of every CTA polls at once, and back-to-back
+    // rounds crowd the L2 the weight stream goes through
+    __nanosleep(round < 8 ? kPollPauseNs : 4 * kPollPauseNs);
 #pragma unroll
     for (int u = 0; u < N; ++u)
       if (((valid >> u) & 1u) && static_cast<uint32_t>(w[u] >> 32) != epoch) w[u] = ld_word(addr(u));
