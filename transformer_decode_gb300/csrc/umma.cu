@@ -287,6 +287,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
           if constexpr (EPI == Epi::Residual) {
             if (gridDim.z > 1) atomicAdd(yp, v[j]);
             else *yp = *yp + v[j];
+          } else if (gridDim.z > 1) {  // k split: y was zeroed; the first slice adds the bias
+            atomicAdd(yp, blockIdx.z == 0 ? v[j] + b : v[j]);
           } else {
             *yp = v[j] + b;
           }
@@ -374,21 +376,38 @@ __global__ void __launch_bounds__(kUThreads, 1)
 // xb [T_tiles][2][NT][K] bf16: per tile of NT tokens the hi plane then the
 // lo plane of the (normed) activations; rows past T are zero. One CTA per
 // token: the RMSNorm factor (when gamma is set) from the row's sum of squares.
+// One pass: every thread loads its 16-byte chunks of the token's row at once
+// (kActChunks per thread covers rows up to 256 * 4 * kActChunks), forms the
+// RMSNorm factor from them, and writes the hi / lo planes from registers.
+// With yz set it also zeroes the product's output rows yz[t][0, yN) (stride
+// yld), which a k-split store then accumulates into.
+constexpr int kActChunks = 12;
+constexpr int kActMaxK = 256 * 4 * kActChunks;
 __global__ void __launch_bounds__(256) k_umma_act(const float* x, const uint16_t* gamma, float eps,
-                                                  int T, int K, int NT, uint16_t* xb) {
+                                                  int T, int K, int NT, uint16_t* xb, float* yz,
+                                                  int yN, int yld) {
   pdl_wait();
   const int t = blockIdx.x;
+  if (yz && t < T)
+    for (int n = threadIdx.x; n < yN; n += 256) yz[(size_t)t * yld + n] = 0.f;
   const int tile = t / NT, tt = t % NT;
   uint16_t* hi = xb + ((size_t)tile * 2 * NT + tt) * K;
   uint16_t* lo = hi + (size_t)NT * K;
   __shared__ float red[8];
+  const int C4 = K / 4;  // 16-byte chunks of the row
+  float4 v[kActChunks];
+#pragma unroll
+  for (int j = 0; j < kActChunks; ++j) {
+    const int c = threadIdx.x + j * 256;
+    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < T && c < C4) v[j] = reinterpret_cast<const float4*>(x + (size_t)t * K)[c];
+  }
   float r = 1.f;
   if (t < T && gamma) {
     float ss = 0.f;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-      const float v = x[(size_t)t * K + k];
-      ss = fmaf(v, v, ss);
-    }
+#pragma unroll
+    for (int j = 0; j < kActChunks; ++j)
+      ss = fmaf(v[j].x, v[j].x, fmaf(v[j].y, v[j].y, fmaf(v[j].z, v[j].z, fmaf(v[j].w, v[j].w, ss))));
     ss = warp_sum(ss);
     if (threadIdx.x % kWarp == 0) red[threadIdx.x / kWarp] = ss;
     __syncthreads();
@@ -396,15 +415,21 @@ __global__ void __launch_bounds__(256) k_umma_act(const float* x, const uint16_t
     for (int w = 0; w < (int)blockDim.x / kWarp; ++w) tot += red[w];
     r = 1.f / sqrtf(tot / (float)K + eps);
   }
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    float v = 0.f;
-    if (t < T) {
-      v = x[(size_t)t * K + k];
-      if (gamma) v = (v * r) * bf16_to_f32(gamma[k]);
+#pragma unroll
+  for (int j = 0; j < kActChunks; ++j) {
+    const int c = threadIdx.x + j * 256;
+    if (c >= C4) break;
+    float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    uint16_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float u = f[e];
+      if (gamma && t < T) u = (u * r) * bf16_to_f32(gamma[4 * c + e]);
+      h[e] = f32_to_bf16(u);
+      l[e] = f32_to_bf16(u - bf16_to_f32(h[e]));
     }
-    const uint16_t h = f32_to_bf16(v);
-    hi[k] = h;
-    lo[k] = f32_to_bf16(v - bf16_to_f32(h));
+    reinterpret_cast<uint2*>(hi)[c] = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+    reinterpret_cast<uint2*>(lo)[c] = make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
   }
 }
 
@@ -495,31 +520,36 @@ static cudaError_t launch_umma_epi(const UmmaArgs& g, const CUtensorMap& tw, con
   }
 }
 
-bool umma_supported(int K) { return K >= kUKBlock && K % kUKBlock == 0 && encode_fn() != nullptr; }
+bool umma_supported(int K) {
+  return K >= kUKBlock && K % kUKBlock == 0 && K <= kActMaxK && encode_fn() != nullptr;
+}
 
 cudaError_t launch_umma(Epi epi, const UmmaArgs& g, cudaStream_t s) {
   const int NT = umma_tokens_per_tile(g.T);
   const int tiles = (g.T + NT - 1) / NT;
   // the activation planes (normed when gamma is set)
-  cudaError_t e = launch_pdl(k_umma_act, dim3(tiles * NT), dim3(256), 0, s, g.x, g.gamma, g.eps,
-                             g.T, g.K, NT, g.xb);
-  if (e != cudaSuccess) return e;
-  CUtensorMap tw, tx;
-  const uint64_t wrows = epi == Epi::SwiGLU ? 2 * (uint64_t)g.N : (uint64_t)g.N;
-  if ((e = make_map(&tw, g.W, g.K, wrows, kURows / 2)) != cudaSuccess) return e;
-  if ((e = make_map(&tx, g.xb, g.K, (uint64_t)tiles * 2 * NT, 2 * NT)) != cudaSuccess) return e;
-  // k split over CTAs only for the residual form (atomic adds), when the
-  // tiles alone leave most SMs idle
+  // k split over CTAs when the tiles alone leave most SMs idle, for the
+  // residual form and the plain store (atomic adds; the store's output is
+  // zeroed by the activation kernel first), not for the LM head (its arg-max
+  // wants finished logits)
   int ks = 1;
-  if (epi == Epi::Residual) {
+  if (epi == Epi::Residual || (epi == Epi::Store && !g.lm)) {
     const int ctas = ((g.N + kURows - 1) / kURows) * tiles;
     const int nkb = g.K / kUKBlock;
     ks = (num_sms() + ctas - 1) / ctas;
     if (ks > nkb / 2) ks = nkb / 2;
     if (ks < 1) ks = 1;
   }
+  const bool zero = epi == Epi::Store && ks > 1;
+  cudaError_t e = launch_pdl(k_umma_act, dim3(tiles * NT), dim3(256), 0, s, g.x, g.gamma, g.eps,
+                             g.T, g.K, NT, g.xb, zero ? g.y : nullptr, g.N, g.ldy);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tw, tx;
+  const uint64_t wrows = epi == Epi::SwiGLU ? 2 * (uint64_t)g.N : (uint64_t)g.N;
+  if ((e = make_map(&tw, g.W, g.K, wrows, kURows / 2)) != cudaSuccess) return e;
+  if ((e = make_map(&tx, g.xb, g.K, (uint64_t)tiles * 2 * NT, 2 * NT)) != cudaSuccess) return e;
   switch (epi) {
-    case Epi::Store: return launch_umma_epi<Epi::Store>(g, tw, tx, NT, 1, s);
+    case Epi::Store: return launch_umma_epi<Epi::Store>(g, tw, tx, NT, ks, s);
     case Epi::Residual: return launch_umma_epi<Epi::Residual>(g, tw, tx, NT, ks, s);
     default: return launch_umma_epi<Epi::SwiGLU>(g, tw, tx, NT, 1, s);
   }
