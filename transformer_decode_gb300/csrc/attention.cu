@@ -182,13 +182,21 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   __shared__ float den_s[GM];
   __shared__ unsigned long long valid_s[kAttnStages];  // positions of each stage that were copied
   __shared__ bool last_s;
+  __shared__ int left_s[kAttnStages];  // warps yet to finish the chunk a stage holds
+  __shared__ int issued_s;             // chunks issued so far
+  __shared__ int abort_s;              // a chunk never landed
   __shared__ float q_s[ROPE ? GM : 1][D], kn_s[ROPE ? D : 1], vn_s[ROPE ? D : 1];
   __shared__ int plan_s[5];  // sequence (-1: idle), split, the sequence's splits, its first, position
   const int g = blockIdx.y, NB = gridDim.x;
   const int G = a.Hq / a.Hkv;
   const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
   if (tid == 0) {
-    for (int s = 0; s < kAttnStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < kAttnStages; ++s) {
+      mbar_init(&full[s], 1);
+      left_s[s] = kAttnWarps;
+    }
+    issued_s = 0;
+    abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   const int cap = a.kv.capacity();
@@ -273,6 +281,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
     const uint32_t vhi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(vmask >> 32));
     if (lane == 0) {
       valid_s[st] = ((unsigned long long)vhi << 32) | vlo;
+      issued_s = ci + 1;
       mbar_expect_tx(&full[st], bytes);
     }
     __syncwarp();
@@ -384,18 +393,22 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
       }
     }
   }
+  // No block barrier between chunks: each warp takes the chunks in order,
+  // and the warp that finishes a stage's chunk last refills the stage with
+  // chunk ci + kAttnStages (a shared-memory count of the warps still at it).
+  // A chunk that never lands ends the scan of the warp that waited for it;
+  // the CTA then keeps no partial.
   const uint64_t deadline = global_timer() + kAttnWaitNs;
-  int done = 0;  // chunks consumed
   for (int ci = 0; ci < nch; ++ci) {
     const int st = ci % kAttnStages;
-    int late = 0;
+    bool late = false;
     while (!mbar_try_wait(&full[st], (uint32_t)(ci / kAttnStages) & 1u))
-      if (global_timer() > deadline) {
-        late = 1;
+      if (global_timer() > deadline || *reinterpret_cast<volatile int*>(&abort_s)) {
+        late = true;
         break;
       }
-    if (__syncthreads_or(late)) {  // a copy that never lands: report it, keep no partial
-      if (tid == 0 && a.status) atomicCAS(a.status, 0, (int)NC_ERR_TIMEOUT);
+    if (late) {
+      if (lane == 0) abort_s = 1;
       break;
     }
     const unsigned char* kc = sm + (size_t)st * Geo::kStage;
@@ -454,16 +467,29 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
         }
       }
     }
-    __syncthreads();  // stage st is free again
-    ++done;
-    if (warp == 0 && ci + kAttnStages < nch) issue(ci + kAttnStages);
+    // this warp is done with the stage; the last one refills it
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();  // this warp's reads of the stage come first
+      last = atomicSub(&left_s[st], 1) == 1;
+      if (last) {
+        left_s[st] = kAttnWarps;
+        __threadfence_block();
+      }
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (last && ci + kAttnStages < nch) issue(ci + kAttnStages);
   }
-  if (done < nch) {
+  __syncthreads();
+  if (abort_s) {
     // abandoned: let the copies already issued land (bounded) before the
     // shared memory is reused or released; this split contributes nothing
     if (tid == 0) {
+      if (a.status) atomicCAS(a.status, 0, (int)NC_ERR_TIMEOUT);
       const uint64_t dl = global_timer() + kAttnWaitNs;
-      for (int ci = done; ci < nch && ci < done + kAttnStages; ++ci)
+      const int is = issued_s;
+      for (int ci = is > kAttnStages ? is - kAttnStages : 0; ci < is; ++ci)
         while (!mbar_try_wait(&full[ci % kAttnStages], (uint32_t)(ci / kAttnStages) & 1u))
           if (global_timer() > dl) break;
     }
