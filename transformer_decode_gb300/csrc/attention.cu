@@ -452,18 +452,37 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[h][e] *= rh;
       }
-      // values: position p's weights come from lanes p GM .. p GM + GM - 1
+      // values: position p's weights come from lanes p GM .. p GM + GM - 1;
+      // a hole (no row copied, weight 0) left its row unwritten, so its
+      // value is replaced, not multiplied: only steps with a hole take that
+      // path (the mask is the chunk's, the test warp-uniform)
+      const unsigned long long stepm = (NP >= 64 ? ~0ull : ((1ull << NP) - 1ull)) << p0;
+      const bool hole = (valid & stepm) != stepm;
+      if (hole) {
 #pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        if (p0 + p >= m) break;  // warp-uniform
-        float vf[E];
-        load_row<E, KV16>(vc + (size_t)(p0 + p) * Geo::kRow + (size_t)lane * E * ES, vf);
+        for (int p = 0; p < NP; ++p) {
+          if (p0 + p >= m) break;  // warp-uniform
+          float vf[E];
+          load_row<E, KV16>(vc + (size_t)(p0 + p) * Geo::kRow + (size_t)lane * E * ES, vf);
 #pragma unroll
-        for (int h = 0; h < GM; ++h) {
-          const float w = __shfl_sync(0xFFFFFFFFu, pr, p * GM + h);
+          for (int h = 0; h < GM; ++h) {
+            const float w = __shfl_sync(0xFFFFFFFFu, pr, p * GM + h);
 #pragma unroll
-          for (int e = 0; e < E; ++e)  // a hole (w = 0) left its row unwritten: not multiplied
-            acc[h][e] = fmaf(w, w == 0.f ? 0.f : vf[e], acc[h][e]);
+            for (int e = 0; e < E; ++e) acc[h][e] = fmaf(w, w == 0.f ? 0.f : vf[e], acc[h][e]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          if (p0 + p >= m) break;  // warp-uniform
+          float vf[E];
+          load_row<E, KV16>(vc + (size_t)(p0 + p) * Geo::kRow + (size_t)lane * E * ES, vf);
+#pragma unroll
+          for (int h = 0; h < GM; ++h) {
+            const float w = __shfl_sync(0xFFFFFFFFu, pr, p * GM + h);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[h][e] = fmaf(w, vf[e], acc[h][e]);
+          }
         }
       }
     }
