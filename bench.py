@@ -467,7 +467,7 @@ def run_nc(args, ws, rank, local):
     # duration is the timed region over the steps (CUDA events on its stream;
     # the region holds only these launches and the 8-byte cycle resets)
     path = model.decode_path(B, kv)
-    launches_per_step = 1 if path == "persistent" else 2 + 5 * shape.n_layers
+    launches_per_step = step_launches(path, shape, B, {"w8a8": False})
     dur = el / args.steps
     achieved = bytes_avg / dur / 1e9
 
@@ -833,6 +833,20 @@ def rounds_summary(per):
             "spread": (max(per) - min(per)) / med if med > 0 else None}
 
 
+def step_launches(path, shape, B, cfg):
+    """Kernel launches of one decode step: the persistent kernel is one; the
+    stage path is the embedding gather, five per layer (QKV, attention with
+    RoPE and the K/V append, o-proj, gate|up, down) and the LM head, and at
+    batch 9..16 with bf16 weights (the tensor cores) each of the five products
+    follows its activation-plane kernel: 3 + 9 L."""
+    if path == "persistent":
+        return 1
+    L = shape.n_layers
+    umma = (B > 8 and not cfg.get("w8a8") and not cfg.get("int4")
+            and os.environ.get("NC_UMMA", "1") != "0")
+    return 3 + 9 * L if umma else 2 + 5 * L
+
+
 def run_workload(args, ws, rank, local, name):
     cfg = dict(WORKLOADS[name])
     torch.cuda.set_device(local)
@@ -927,7 +941,7 @@ def run_workload(args, ws, rank, local, name):
         st.synchronize()
         cur = nxt_h.clone()
     e2e_value, t_e2e = replica_rate(ws, B, k_e2e, time.perf_counter() - t0)
-    launches_per_step = 1 if path == "persistent" else 2 + 5 * shape.n_layers
+    launches_per_step = step_launches(path, shape, B, cfg)
     model.close()
     del kv
     torch.cuda.empty_cache()
