@@ -134,9 +134,15 @@ template <int NT>
 __host__ __device__ constexpr int ustage_bytes() {
   return kUAStage + 2 * NT * kUKBlock * 2;
 }
+// Token tiles of 64 or more (prefill) run two CTAs per SM, so one CTA's
+// epilogue overlaps the other's products: half the shared memory (and at
+// most 256 tensor-memory columns) each. Smaller tiles keep one CTA per SM.
+template <int NT>
+__host__ __device__ constexpr int uctas_per_sm() { return NT >= 64 ? 2 : 1; }
 template <int NT>
 __host__ __device__ constexpr int ustages() {
-  return (200 * 1024) / ustage_bytes<NT>() > 8 ? 8 : (200 * 1024) / ustage_bytes<NT>();
+  constexpr int budget = (uctas_per_sm<NT>() == 2 ? 100 : 200) * 1024;
+  return budget / ustage_bytes<NT>() > 8 ? 8 : budget / ustage_bytes<NT>();
 }
 template <int NT>
 __host__ __device__ constexpr uint32_t utmem_cols() {
@@ -152,7 +158,7 @@ struct UShared {
 };
 
 template <Epi EPI, int NT>
-__global__ void __launch_bounds__(kUThreads, 1)
+__global__ void __launch_bounds__(kUThreads, uctas_per_sm<NT>())
     k_umma(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
            const UArgs a) {
   constexpr int S = ustages<NT>();
