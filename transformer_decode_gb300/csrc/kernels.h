@@ -126,6 +126,7 @@ struct PrefillAttnArgs {
   float* out;               // [T, Hq D]
   int T, start, seq, layer, Hq, Hkv, D;
   KVView kv;
+  int pair = 0;             // set by the launcher: a CTA takes token blocks x and n - 1 - x
 };
 size_t prefill_attn_smem(int D);
 cudaError_t launch_prefill_attn(const PrefillAttnArgs& a, cudaStream_t s);
