@@ -147,6 +147,14 @@ def test_prefill_8b_shape_two_layers():
     print(f"prefill 8B shape (2 layers) T=130: worst rel-L2 {worst:.3e}")
 
 
+def test_prefill_8b_shape_paired_blocks():
+    """330 tokens at the 8B shape: 21 token blocks of 16 x 8 kv heads outnumber
+    the SMs, so each attention CTA takes an early and a late block (the middle
+    one alone, the last one partial)."""
+    worst = _run(synth.QWEN3_8B.with_layers(2), 330, 0, False, decode_steps=2, seq=0)
+    print(f"prefill 8B shape (2 layers) T=330, paired blocks: worst rel-L2 {worst:.3e}")
+
+
 def test_prefill_rejects_bad_arguments():
     shape = synth.TINY
     wd, _ = weights_both(shape)
