@@ -663,6 +663,9 @@ WORKLOADS = {
                                            gen=64, w8a8="b32"),
     "qwen2_0p5b_int4_g128_b1_past512": dict(shape="QWEN2_0P5B", batch=1, paged=False,
                                             past=512, gen=64, w8a8=False, int4=128),
+    # the 8B shape with a bf16 cache (the bytes of the 70%-of-8-TB/s target)
+    "qwen3_8b_shape_b1_past4096_kvbf16": dict(shape="QWEN3_8B", batch=1, paged=False,
+                                              past=4096, gen=64, w8a8=False, kv_bf16=True),
 }
 ROUNDS = 5  # the timed region is reported as this many equal rounds as well
 
@@ -724,7 +727,7 @@ def oracle_for(cfg, max_ctx):
     om = oracle.OracleModel(shape, cpu_weights(shape), w8a8=bool(cfg["w8a8"]),
                             act_block=32 if cfg["w8a8"] == "b32" else 0,
                             int8_embed=cfg["w8a8"] == "b32", int4_group=cfg.get("int4", 0))
-    okv = om.new_kv(cfg["batch"], max_ctx)
+    okv = om.new_kv(cfg["batch"], max_ctx, bf16=bool(cfg.get("kv_bf16")))
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     for l in range(shape.n_layers):
         for b, p in enumerate(past):
@@ -733,9 +736,17 @@ def oracle_for(cfg, max_ctx):
             for g in range(shape.n_kv_heads):
                 kr = synth.synthetic_kv_rows(shape, l, b, g, 0, p, device=dev)
                 vr = synth.synthetic_kv_rows(shape, l, b, g, 1, p, device=dev)
-                okv.k[l, b, g, :p] = kr.float().cpu().numpy().reshape(p, -1)
-                okv.v[l, b, g, :p] = vr.float().cpu().numpy().reshape(p, -1)
+                okv.k[l, b, g, :p] = oracle_rows(kr, okv.bf16, p)
+                okv.v[l, b, g, :p] = oracle_rows(vr, okv.bf16, p)
     return om, okv, past
+
+
+def oracle_rows(t, bf16, p):
+    """Synthetic K/V rows as the oracle cache holds them: fp32 values, or the
+    bf16 bits (uint16) of a bf16 cache."""
+    if bf16:
+        return t.to(torch.bfloat16).contiguous().view(torch.int16).cpu().numpy().view(np.uint16).reshape(p, -1)
+    return t.float().cpu().numpy().reshape(p, -1)
 
 
 def cpu_model_name():
@@ -862,11 +873,12 @@ def run_workload(args, ws, rank, local, name):
                      int4_group=cfg.get("int4", 0))
     del wd
     torch.cuda.empty_cache()
+    kv_dtype = torch.bfloat16 if cfg.get("kv_bf16") else torch.float32
     if cfg["paged"]:
         table, nblk = synth.block_tables(past, gen + 1, 16)
-        kv = nc.KVCache(shape, B, paged=True, block_table=table, num_blocks=nblk)
+        kv = nc.KVCache(shape, B, paged=True, block_table=table, num_blocks=nblk, dtype=kv_dtype)
     else:
-        kv = nc.KVCache(shape, B, max_ctx=max_ctx)
+        kv = nc.KVCache(shape, B, max_ctx=max_ctx, dtype=kv_dtype)
     fill_past(kv, shape, past)
     logits = torch.empty(B, shape.vocab, device="cuda")
     tok = torch.empty(B, dtype=torch.int32, device="cuda")
@@ -907,8 +919,9 @@ def run_workload(args, ws, rank, local, name):
         sampler.stop()
     value, el = replica_rate(ws, B, args.steps, total_s)
     dur = el / args.steps
-    bytes_avg = sum(step_bytes(shape, B, u.tolist(), w8a8=bool(cfg["w8a8"]),
-                               int8_head=cfg["w8a8"] == "b32", int4_group=cfg.get("int4", 0))
+    bytes_avg = sum(step_bytes(shape, B, u.tolist(), kv_elem=2 if cfg.get("kv_bf16") else 4,
+                               w8a8=bool(cfg["w8a8"]), int8_head=cfg["w8a8"] == "b32",
+                               int4_group=cfg.get("int4", 0))
                     for u in used) / len(used)
     peak, peak_kind = peaks()
 
@@ -953,7 +966,7 @@ def run_workload(args, ws, rank, local, name):
     if rank == 0:
         if path == "persistent":
             kernel = f"k_decode_persistent<{1 if B == 1 else (2 if B == 2 else 4)}," \
-                     f"{shape.head_dim},fp32 KV> (the whole step, one launch)"
+                     f"{shape.head_dim},{'bf16' if cfg.get('kv_bf16') else 'fp32'} KV> (the whole step, one launch)"
             traffic = counted_traffic(name)
         else:
             kernel = "stage kernels (whole step, one CUDA graph)"
@@ -974,7 +987,7 @@ def run_workload(args, ws, rank, local, name):
                                    else "bf16") +
                                   " from seeded N(0,0.02), fp32 accumulate",
                        "kv": ("paged (block 16, shuffled tables)" if cfg["paged"] else "contiguous")
-                             + " fp32",
+                             + (" bf16" if cfg.get("kv_bf16") else " fp32"),
                        "positions": f"cycles of {gen} greedy steps from the past length(s)",
                        "path": ("nc_decode_step: one persistent cooperative launch per step"
                                 if path == "persistent" else "nc_decode_step: stage kernels, CUDA graph"),
