@@ -91,7 +91,7 @@ constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / kWarp;
 constexpr int kAttnCh = 64;      // positions per staged chunk
 constexpr int kAttnStages = 3;   // chunks in shared memory: two in flight while one is used
-constexpr int kMaxSplits = 128;  // splits of one (sequence, kv head); the merge keeps one weight each
+constexpr int kMaxSplits = 256;  // splits of one (sequence, kv head); the merge keeps one weight each
 constexpr uint64_t kAttnWaitNs = 1000000000ull;  // bound on any wait for a staged chunk
 constexpr int kAttnMinPer = 32;  // positions per split at least (shorter scans are not split)
 
@@ -103,6 +103,8 @@ struct AttnGeo {
   static constexpr size_t kSmem = kAttnStages * kStage + sizeof(uint64_t) * kAttnStages;
   static_assert(kAttnStages * kStage >= sizeof(float) * (8 * 8 * D + 2 * 8 * 8),
                 "the warps' states are combined in the spent stages");
+  static_assert(kAttnStages * kStage >= sizeof(float) * 8 * kMaxSplits,
+                "the merge's split weights fit in the spent stages");
 };
 
 // CTAs of the split kernel one SM holds (shared memory bound), cached per shape.

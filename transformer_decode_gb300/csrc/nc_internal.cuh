@@ -64,6 +64,14 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 // is a no-op. (Letting the successor launch early, from the top of a kernel,
 // measured slower: its L2 warm-up then runs too far ahead of use.)
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel in the stream launch before this one exits (once every
+// CTA of this grid has called it or exited). A kernel calls it only after its
+// own pdl_wait, so everything before it in the stream is complete when the
+// successor's prologue runs; the successor still waits in pdl_wait for this
+// grid's writes.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 // Fetch [p, p + bytes) into L2 without waiting (p 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");

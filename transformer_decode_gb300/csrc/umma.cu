@@ -191,6 +191,21 @@ __global__ void __launch_bounds__(kUThreads, uctas_per_sm<NT>())
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // No kernel writes the weights: the first stages' weight boxes are issued
+  // before the wait, so their round trip overlaps the activation kernel
+  // (which lets this grid launch once its own wait is over, so every kernel
+  // before it has completed).
+  const int pre = nkb < S ? nkb : S;
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < pre; ++i) {
+      uint8_t* st = usm + (size_t)i * SB;
+      const int kx = (kb0 + i) * kUKBlock;
+      mbar_expect_tx(&U.full[i], (uint32_t)SB);
+      tma_load_2d(st, &tw, kx, n0, &U.full[i]);
+      tma_load_2d(st + kUAStage / 2, &tw,
+                  kx, EPI == Epi::SwiGLU ? a.up_row0 + n0 : n0 + kURows / 2, &U.full[i]);
+    }
+  }
   // the activation planes and (residual form) the output come from earlier
   // kernels: every thread waits for them to be complete and visible
   pdl_wait();
@@ -216,14 +231,16 @@ __global__ void __launch_bounds__(kUThreads, uctas_per_sm<NT>())
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < nkb; ++i) {
       const int s = i % S;
-      if (i >= S && !wait_bar(&U.empty[s], ((i / S) - 1) & 1)) break;
-      if (*reinterpret_cast<volatile int*>(&U.abort)) break;
       uint8_t* st = usm + (size_t)s * SB;
       const int kx = (kb0 + i) * kUKBlock;
-      mbar_expect_tx(&U.full[s], (uint32_t)SB);
-      tma_load_2d(st, &tw, kx, n0, &U.full[s]);
-      tma_load_2d(st + kUAStage / 2, &tw,
-                  kx, EPI == Epi::SwiGLU ? a.up_row0 + n0 : n0 + kURows / 2, &U.full[s]);
+      if (i >= pre) {  // the first stages' weights are in flight already
+        if (i >= S && !wait_bar(&U.empty[s], ((i / S) - 1) & 1)) break;
+        if (*reinterpret_cast<volatile int*>(&U.abort)) break;
+        mbar_expect_tx(&U.full[s], (uint32_t)SB);
+        tma_load_2d(st, &tw, kx, n0, &U.full[s]);
+        tma_load_2d(st + kUAStage / 2, &tw,
+                    kx, EPI == Epi::SwiGLU ? a.up_row0 + n0 : n0 + kURows / 2, &U.full[s]);
+      }
       tma_load_2d(st + kUAStage, &tx, kx, blockIdx.y * 2 * NT, &U.full[s]);
       issued = i + 1;
     }
@@ -249,6 +266,7 @@ __global__ void __launch_bounds__(kUThreads, uctas_per_sm<NT>())
   wait_bar(&U.done, 0);
   tc_fence_after();
   const bool ok = !*reinterpret_cast<volatile int*>(&U.abort) && nkb > 0;
+  pdl_trigger();  // the next kernel's launch overlaps this epilogue
 
   // ---------------------------------------------------------------- epilogue
   // thread (warp w, lane l) owns TMEM lane 32 w + l = weight row r of the tile
@@ -393,6 +411,7 @@ __global__ void __launch_bounds__(256) k_umma_act(const float* x, const uint16_t
                                                   int T, int K, int NT, uint16_t* xb, float* yz,
                                                   int yN, int yld) {
   pdl_wait();
+  pdl_trigger();  // the product kernel may launch and fetch its weights meanwhile
   const int t = blockIdx.x;
   if (yz && t < T)
     for (int n = threadIdx.x; n < yN; n += 256) yz[(size_t)t * yld + n] = 0.f;
