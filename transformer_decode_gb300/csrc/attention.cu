@@ -153,6 +153,45 @@ __device__ __forceinline__ void load_row(const unsigned char* p, float (&f)[E]) 
   }
 }
 
+// Head size 64 with groups of 8 heads: lane (position p = lane / 8, slice
+// s = lane % 8) holds 8 dims of the position's K row and of every query head:
+// fp32 dims 4s..4s+3 and 32+4s..32+4s+3 (two 16-byte loads, the 8 lanes of a
+// load phase on 8 bank groups), bf16 dims 8s..8s+7 (one 16-byte load).
+template <bool KV16>
+__host__ __device__ __forceinline__ int slice_dim(int s, int j) {
+  return KV16 ? 8 * s + j : (j < 4 ? 4 * s + j : 32 + 4 * s + (j - 4));
+}
+template <bool KV16>
+__device__ __forceinline__ void load_slice(const unsigned char* row, int s, float (&f)[8]) {
+  if constexpr (KV16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * s);
+    f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+    f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z); f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(row + 16 * s);
+    const float4 b = *reinterpret_cast<const float4*>(row + 128 + 16 * s);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+}
+// Sum v[i] over the N lanes of each aligned group of N, value i landing in
+// the group's lane i (a reduce-scatter of N - 1 shuffles).
+template <int N>
+__device__ __forceinline__ void group_sum_scatter(float (&v)[N]) {
+  const int lane = threadIdx.x % kWarp;
+  int o = N / 2;
+#pragma unroll
+  for (int half = N / 2; half >= 1; half /= 2, o /= 2) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = upper ? v[k] : v[k + half];
+      const float keep = upper ? v[k + half] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+    }
+  }
+}
+
 // One CTA per (split c, kv head g, sequence b). Thread 0 streams the split's
 // positions through a ring of kAttnStages shared-memory stages with bulk
 // copies (one per run of positions contiguous in the cache: the whole chunk
@@ -353,15 +392,21 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
   }
   __syncthreads();  // the rotated heads in shared memory
 
-  // this lane's dimensions [lane E, lane E + E) of every query head
-  float qr[GM][E];
+  // The scores' layout. Sliced (head size 64, groups of 8): the 8 dims of
+  // slice lane % 8 of every query head; otherwise dims [lane E, lane E + E)
+  // of every query head, the 32 lanes' partial dots summed over the warp.
+  constexpr bool SLICED = D == 64 && GM == 8;
+  constexpr int QE = SLICED ? 8 : E;
+  float qr[GM][QE];
 #pragma unroll
   for (int h = 0; h < GM; ++h)
 #pragma unroll
-    for (int e = 0; e < E; ++e)
+    for (int e = 0; e < QE; ++e) {
+      const int d = SLICED ? slice_dim<KV16>(lane % GM, e) : lane * E + e;
       qr[h][e] = h >= G ? 0.f
-                 : ROPE ? q_s[ROPE ? h : 0][lane * E + e]
-                        : a.q[((size_t)b * a.Hq + g * G + h) * D + lane * E + e];
+                 : ROPE ? q_s[ROPE ? h : 0][d]
+                        : a.q[((size_t)b * a.Hq + g * G + h) * D + d];
+    }
 
 
   // Each warp keeps its own online-softmax state over the positions it
@@ -418,21 +463,37 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_split(AttnArgs a) {
     const int m = min(kAttnCh, len - ci * kAttnCh);
     const unsigned long long valid = valid_s[st];
     for (int p0 = warp * NP; p0 < m; p0 += kAttnWarps * NP) {
-      // scores of NP positions x GM heads
-      float v[GM * NP];
-#pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        float kf[E];
-        load_row<E, KV16>(kc + (size_t)(p0 + p) * Geo::kRow + (size_t)lane * E * ES, kf);
+      // scores of NP positions x GM heads; lane i ends with value i =
+      // (position i / GM, head i % GM)
+      float v[SLICED ? GM : GM * NP];
+      if constexpr (SLICED) {
+        // a row past the chunk's end is stale shared memory inside the
+        // stage; its score is masked below
+        float kf[8];
+        load_slice<KV16>(kc + (size_t)(p0 + lane / GM) * Geo::kRow, lane % GM, kf);
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
           float d = 0.f;
 #pragma unroll
-          for (int e = 0; e < E; ++e) d = fmaf(qr[h][e], kf[e], d);
-          v[p * GM + h] = d;
+          for (int e = 0; e < 8; ++e) d = fmaf(qr[h][e], kf[e], d);
+          v[h] = d;
         }
+        group_sum_scatter<GM>(v);
+      } else {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          float kf[E];
+          load_row<E, KV16>(kc + (size_t)(p0 + p) * Geo::kRow + (size_t)lane * E * ES, kf);
+#pragma unroll
+          for (int h = 0; h < GM; ++h) {
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) d = fmaf(qr[h][e], kf[e], d);
+            v[p * GM + h] = d;
+          }
+        }
+        warp_sum_many<GM * NP>(v);
       }
-      warp_sum_many<GM * NP>(v);  // lane i: value i = (position i / GM, head i % GM)
       const int t = p0 + lane / GM;
       // a block-table hole (no row copied) scores -inf
       const float sc = hl < G && t < m && ((valid >> t) & 1ull) ? v[0] * scale : -INFINITY;
