@@ -56,13 +56,15 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 }
 
 // Programmatic dependent launch. Stage kernels are launched so that the next
-// kernel in the stream may start once every CTA of this one has exited,
-// before the grid's completion is flushed: its prologue does only work that
-// reads no output of an earlier kernel and writes no global memory (warming
-// L2 with its weights), then waits for the earlier kernels to complete and
-// their writes to be visible (pdl_wait). Launched the ordinary way, the wait
-// is a no-op. (Letting the successor launch early, from the top of a kernel,
-// measured slower: its L2 warm-up then runs too far ahead of use.)
+// kernel in the stream may start once every CTA of this one has exited (or
+// called pdl_trigger), before the grid's completion is flushed: its prologue
+// does only work that reads no output of an earlier kernel and writes no
+// global memory (warming L2 with its weights, or loading weight tiles), then
+// waits for the earlier kernels to complete and their writes to be visible
+// (pdl_wait). Launched the ordinary way, the wait is a no-op. Only the
+// tensor-core activation and product kernels trigger early; for the GEMV
+// kernels an early trigger from the top measured slower (the successor's L2
+// warm-up then runs too far ahead of use).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Let the next kernel in the stream launch before this one exits (once every
 // CTA of this grid has called it or exited). A kernel calls it only after its
