@@ -258,6 +258,10 @@ CASES = [
     (dataclasses.replace(synth.TINY_QKNORM, hidden=1024, n_q_heads=8, n_kv_heads=1), [300, 64], True),
     # one query head per kv head
     (dataclasses.replace(synth.TINY, n_kv_heads=4), [130, 2], False),
+    # head size 64, scored in 8-dim slices: a full group of 8 heads, and a group
+    # of 5 (three padding heads)
+    (dataclasses.replace(synth.TINY, hidden=512, n_q_heads=8, n_kv_heads=1), [200, 37], True),
+    (dataclasses.replace(synth.TINY, hidden=640, n_q_heads=10, n_kv_heads=2), [70, 129], False),
 ]
 
 
